@@ -1,0 +1,598 @@
+// Steps a2 (node build), a3 (lattice encoder) and the fusion/head contractions of a4.
+//
+// Sources: LiLiCorr: Lightweight Likelihood Correlation of Parallel Drafts for
+// Speculative Decoding -- Sec. 3.2 (node = embedding + drafter hidden + confidence
+// network + slot/rank encodings; small Transformer over the (B-1) x K lattice; fusion
+// with the target state; out and in heads) and App. A "Architecture" (five confidence
+// scalars, two layers, RMSNorm, SiLU, per-head slot-distance and same-slot biases,
+// concat [h; t; h*t] -> linear -> SiLU).
+//
+// Precision.  Activations enter the tensor cores as a pair of bf16 numbers hi + lo
+// (hi = bf16(v), lo = bf16(v - hi), about 16 significant bits) against exact bf16
+// weights, accumulating in f32: C = A_hi W^T + A_lo W^T.  A split activation matrix is
+// stored [M, 2K] = [A_hi | A_lo], so each contraction is one GEMM over 2K columns whose
+// weight column index wraps (k mod K).  Attention products use three terms
+// (hi*hi + hi*lo + lo*hi).  Everything else (norms, softmax, residual stream) is f32.
+#include <float.h>
+
+#include "kernels.cuh"
+
+namespace lilicorr {
+
+// ------------------------------------------------------------------ PTX helpers
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, bool pred) {
+  const int n = pred ? 16 : 0;
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(smem)),
+               "l"(gmem), "r"(n)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3,
+                                        uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                          uint32_t& r3, uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo_elem, float hi_elem) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo_elem, hi_elem);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// Byte offset of 16-byte chunk `c` of row `r` in a tile whose rows hold CH chunks,
+// XOR-swizzled so that ldmatrix over 8 consecutive rows is bank-conflict free.
+template <int CH>
+__device__ __forceinline__ int swz(int r, int c) {
+  if constexpr (CH >= 8)
+    return r * CH * 16 + ((c ^ (r & 7)) << 4);
+  else
+    return r * CH * 16 + ((c ^ ((r >> 1) & 3)) << 4);
+}
+
+// ------------------------------------------------------------------ a2: confidence MLP
+// U[m, :] = SiLU(Wc1 f(m) + bc1) written split [M, 2H]; f = (lp, p, gap, r, top):
+// lp = l - lse, p = exp(lp), gap = lp - lp of the slot's top candidate, r = k/(K-1),
+// top = [k == 0] (App. A: log-probability and probability under the full vocabulary,
+// the gap to the slot's most likely token, the rank normalised to [0,1], top indicator).
+__global__ void conf_hidden_kernel(const float* __restrict__ cand_logit,
+                                   const float* __restrict__ lse, int64_t M, int K, int H,
+                                   const float* __restrict__ w1, const float* __restrict__ b1,
+                                   __nv_bfloat16* __restrict__ U) {
+  const int64_t m = blockIdx.x;
+  if (m >= M) return;
+  const int64_t row = m / K;  // (block, slot) row of the logit pass
+  const int k = static_cast<int>(m % K);
+  const float l = lse[row];
+  const float lp = cand_logit[m] - l;
+  const float lp_top = cand_logit[row * K] - l;
+  float f[5];
+  f[0] = lp;
+  f[1] = expf(lp);
+  f[2] = lp - lp_top;
+  f[3] = K > 1 ? float(k) / float(K - 1) : 0.f;
+  f[4] = k == 0 ? 1.f : 0.f;
+  for (int h = threadIdx.x; h < H; h += blockDim.x) {
+    float acc = b1[h];
+#pragma unroll
+    for (int j = 0; j < 5; ++j) acc = fmaf(w1[h * 5 + j], f[j], acc);
+    const float u = silu(acc);
+    __nv_bfloat16 hi, lo;
+    split_bf16(u, hi, lo);
+    U[m * 2 * H + h] = hi;
+    U[m * 2 * H + H + h] = lo;
+  }
+}
+
+// ------------------------------------------------------------------ GEMM (mma.sync)
+
+constexpr int GM_BM = 128, GM_BN = 128, GM_BK = 64, GM_STAGES = 3, GM_THREADS = 256;
+constexpr int GM_TILE_BYTES = GM_BM * GM_BK * 2;  // 16 KB (A and W tiles are the same size)
+constexpr int GM_SMEM = GM_STAGES * 2 * GM_TILE_BYTES;
+
+template <int EPI>
+__device__ __forceinline__ void gemm_store2(const GemmArgs& g, int64_t m, int n, float v0,
+                                            float v1) {
+  if (m >= g.M || n >= g.N) return;
+  v0 += g.bias[n];
+  v1 += g.bias[n + 1];
+  if constexpr (EPI == EPI_F32) {
+    *reinterpret_cast<float2*>(g.out + m * g.N + n) = make_float2(v0, v1);
+  } else if constexpr (EPI == EPI_RESID) {
+    float2* p = reinterpret_cast<float2*>(g.out + m * g.N + n);
+    float2 x = *p;
+    x.x += v0;
+    x.y += v1;
+    *p = x;
+  } else if constexpr (EPI == EPI_SPLIT || EPI == EPI_SPLIT_SILU) {
+    if constexpr (EPI == EPI_SPLIT_SILU) {
+      v0 = silu(v0);
+      v1 = silu(v1);
+    }
+    __nv_bfloat16 h0, l0, h1, l1;
+    split_bf16(v0, h0, l0);
+    split_bf16(v1, h1, l1);
+    __nv_bfloat16* o = g.out_split + m * 2 * g.N;
+    *reinterpret_cast<__nv_bfloat162*>(o + n) = __halves2bfloat162(h0, h1);
+    *reinterpret_cast<__nv_bfloat162*>(o + g.N + n) = __halves2bfloat162(l0, l1);
+  } else {  // EPI_NODE
+    const int S = (g.B - 1) * g.K;
+    const int64_t b = m / S;
+    const int t = static_cast<int>(m % S);
+    const int slot = t / g.K + 1, k = t % g.K;
+    // ids come from the logit pass and are < V; the clamp keeps a violated precondition
+    // (e.g. NaN logits) from turning into an out-of-bounds gather.
+    int64_t id = g.cand_id[m];
+    id = id < 0 ? 0 : (id >= g.vocab ? g.vocab - 1 : id);
+    const __nv_bfloat162 e = *reinterpret_cast<const __nv_bfloat162*>(g.embed + id * g.N + n);
+    v0 += __bfloat162float(e.x) + g.slot_table[(slot - 1) * g.N + n] + g.rank_table[k * g.N + n];
+    v1 += __bfloat162float(e.y) + g.slot_table[(slot - 1) * g.N + n + 1] +
+          g.rank_table[k * g.N + n + 1];
+    if (g.slot_hidden) {
+      const __nv_bfloat162 hh = *reinterpret_cast<const __nv_bfloat162*>(
+          g.slot_hidden + (b * g.B + slot) * g.N + n);
+      v0 += __bfloat162float(hh.x);
+      v1 += __bfloat162float(hh.y);
+    }
+    *reinterpret_cast<float2*>(g.out + m * g.N + n) = make_float2(v0, v1);
+    if (g.nodes_tap) *reinterpret_cast<float2*>(g.nodes_tap + m * g.N + n) = make_float2(v0, v1);
+  }
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(GM_THREADS) gemm_kernel(const GemmArgs g) {
+  extern __shared__ __align__(128) uint8_t gm_smem[];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int warp_m = warp >> 2, warp_n = warp & 3;  // 2 x 4 warps, 64 x 32 each
+  const int64_t m0 = int64_t(blockIdx.y) * GM_BM;
+  const int n0 = blockIdx.x * GM_BN;
+  const int KT = g.Ka / GM_BK;
+
+  auto a_tile = [&](int s) { return gm_smem + s * 2 * GM_TILE_BYTES; };
+  auto b_tile = [&](int s) { return gm_smem + s * 2 * GM_TILE_BYTES + GM_TILE_BYTES; };
+
+  auto load = [&](int s, int kt) {
+    const int ka = kt * GM_BK;
+    const int kw = ka % g.Kw;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int c = tid + i * GM_THREADS;  // 0..1023
+      const int r = c >> 3, ch = c & 7;
+      const int64_t m = m0 + r;
+      const bool pa = m < g.M;
+      cp_async16(a_tile(s) + swz<8>(r, ch), g.A + (pa ? m : 0) * g.Ka + ka + ch * 8, pa);
+      const int n = n0 + r;
+      const bool pb = n < g.N;
+      cp_async16(b_tile(s) + swz<8>(r, ch), g.W + int64_t(pb ? n : 0) * g.Kw + kw + ch * 8, pb);
+    }
+  };
+
+  float acc[4][4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) acc[i][j][k] = 0.f;
+
+#pragma unroll
+  for (int s = 0; s < GM_STAGES - 1; ++s) {
+    if (s < KT) load(s, s);
+    cp_async_commit();
+  }
+
+  for (int kt = 0; kt < KT; ++kt) {
+    cp_async_wait<GM_STAGES - 2>();
+    __syncthreads();
+    if (kt + GM_STAGES - 1 < KT) load((kt + GM_STAGES - 1) % GM_STAGES, kt + GM_STAGES - 1);
+    cp_async_commit();
+    const uint32_t sa = smem_addr(a_tile(kt % GM_STAGES));
+    const uint32_t sb = smem_addr(b_tile(kt % GM_STAGES));
+#pragma unroll
+    for (int kk = 0; kk < GM_BK / 16; ++kk) {
+      uint32_t af[4][4];
+#pragma unroll
+      for (int mt = 0; mt < 4; ++mt) {
+        const int r = warp_m * 64 + mt * 16 + (lane & 15);
+        const int ch = kk * 2 + (lane >> 4);
+        ldsm_x4(af[mt][0], af[mt][1], af[mt][2], af[mt][3], sa + swz<8>(r, ch));
+      }
+      uint32_t bf[4][2];
+#pragma unroll
+      for (int np = 0; np < 2; ++np) {
+        const int r = warp_n * 32 + np * 16 + (lane & 7) + ((lane >> 4) << 3);
+        const int ch = kk * 2 + ((lane >> 3) & 1);
+        ldsm_x4(bf[2 * np][0], bf[2 * np][1], bf[2 * np + 1][0], bf[2 * np + 1][1],
+                sb + swz<8>(r, ch));
+      }
+#pragma unroll
+      for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) mma_bf16(acc[mt][nt], af[mt], bf[nt][0], bf[nt][1]);
+    }
+  }
+  cp_async_wait<0>();
+
+#pragma unroll
+  for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+      const int64_t m = m0 + warp_m * 64 + mt * 16 + (lane >> 2);
+      const int n = n0 + warp_n * 32 + nt * 8 + (lane & 3) * 2;
+      gemm_store2<EPI>(g, m, n, acc[mt][nt][0], acc[mt][nt][1]);
+      gemm_store2<EPI>(g, m + 8, n, acc[mt][nt][2], acc[mt][nt][3]);
+    }
+}
+
+cudaError_t launch_gemm(int epi, const GemmArgs& g, cudaStream_t stream) {
+  static bool attr = false;
+  if (!attr) {
+    cudaFuncSetAttribute(gemm_kernel<EPI_F32>, cudaFuncAttributeMaxDynamicSharedMemorySize, GM_SMEM);
+    cudaFuncSetAttribute(gemm_kernel<EPI_RESID>, cudaFuncAttributeMaxDynamicSharedMemorySize, GM_SMEM);
+    cudaFuncSetAttribute(gemm_kernel<EPI_SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize, GM_SMEM);
+    cudaFuncSetAttribute(gemm_kernel<EPI_SPLIT_SILU>, cudaFuncAttributeMaxDynamicSharedMemorySize, GM_SMEM);
+    cudaFuncSetAttribute(gemm_kernel<EPI_NODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, GM_SMEM);
+    attr = true;
+  }
+  const dim3 grid((g.N + GM_BN - 1) / GM_BN, static_cast<unsigned>((g.M + GM_BM - 1) / GM_BM));
+  switch (epi) {
+    case EPI_F32: gemm_kernel<EPI_F32><<<grid, GM_THREADS, GM_SMEM, stream>>>(g); break;
+    case EPI_RESID: gemm_kernel<EPI_RESID><<<grid, GM_THREADS, GM_SMEM, stream>>>(g); break;
+    case EPI_SPLIT: gemm_kernel<EPI_SPLIT><<<grid, GM_THREADS, GM_SMEM, stream>>>(g); break;
+    case EPI_SPLIT_SILU: gemm_kernel<EPI_SPLIT_SILU><<<grid, GM_THREADS, GM_SMEM, stream>>>(g); break;
+    default: gemm_kernel<EPI_NODE><<<grid, GM_THREADS, GM_SMEM, stream>>>(g); break;
+  }
+  note_launch();
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ RMSNorm -> split
+// y = x / sqrt(mean(x^2) + eps) * g, one warp per row.
+__global__ void rmsnorm_split_kernel(const float* __restrict__ X, const float* __restrict__ gain,
+                                     int64_t M, int H, float eps, __nv_bfloat16* __restrict__ out) {
+  const int lane = threadIdx.x & 31;
+  const int64_t m = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (m >= M) return;
+  const float* x = X + m * H;
+  float ss = 0.f;
+  for (int h = lane; h < H; h += 32) ss = fmaf(x[h], x[h], ss);
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) ss += __shfl_xor_sync(FULL_MASK, ss, o);
+  const float inv = 1.0f / sqrtf(ss / float(H) + eps);
+  __nv_bfloat16* o = out + m * 2 * H;
+  for (int h = lane; h < H; h += 32) {
+    __nv_bfloat16 hi, lo;
+    split_bf16(x[h] * inv * gain[h], hi, lo);
+    o[h] = hi;
+    o[H + h] = lo;
+  }
+}
+
+// ------------------------------------------------------------------ attention
+// Per (block, head): softmax_j(q_i.k_j / sqrt(dh) + dist[slot_j - slot_i + B_max - 2]
+// + [slot_i == slot_j] * same) v_j over all S lattice tokens (bidirectional, no mask).
+// qkv: split [M, 6H] = [q|k|v]_hi | [q|k|v]_lo.  out: split [M, 2H].
+// 4 warps x 16 query rows per CTA; keys streamed in tiles of 64 (cp.async, 2 buffers);
+// online softmax in f32; three-term split products for q.k and p.v.
+constexpr int AT_QROWS = 64, AT_KT = 64, AT_THREADS = 128;
+
+template <int DH>
+__global__ void __launch_bounds__(AT_THREADS) attention_kernel(
+    const __nv_bfloat16* __restrict__ qkv, int S, int K, int H, int B_max,
+    const float* __restrict__ dist_bias, const float* __restrict__ same_bias,
+    __nv_bfloat16* __restrict__ out) {
+  constexpr int CH = DH / 8;                 // 16-byte chunks per row
+  constexpr int TB = AT_KT * DH * 2;         // bytes of one [64 x DH] bf16 tile
+  extern __shared__ __align__(128) uint8_t at_smem[];
+  uint8_t* sq_hi = at_smem;
+  uint8_t* sq_lo = at_smem + TB;
+  uint8_t* skv = at_smem + 2 * TB;           // [2 buffers][k_hi, k_lo, v_hi, v_lo]
+  __shared__ float s_dist[128];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int q0 = blockIdx.x * AT_QROWS, h = blockIdx.y;
+  const int64_t b = blockIdx.z;
+  const int64_t tok0 = b * S;
+  const int ld = 6 * H;
+  const int nd = 2 * B_max - 3;
+  for (int i = tid; i < nd; i += AT_THREADS) s_dist[i] = dist_bias[h * nd + i];
+  const float same = same_bias[h];
+  const float scale = 1.0f / sqrtf(float(DH));
+
+  // Q tile
+  for (int c = tid; c < AT_QROWS * CH; c += AT_THREADS) {
+    const int r = c / CH, ch = c % CH;
+    const bool pr = q0 + r < S;
+    const __nv_bfloat16* src = qkv + (tok0 + (pr ? q0 + r : 0)) * ld + h * DH + ch * 8;
+    cp_async16(sq_hi + swz<CH>(r, ch), src, pr);
+    cp_async16(sq_lo + swz<CH>(r, ch), src + 3 * H, pr);
+  }
+  auto load_kv = [&](int buf, int j0) {
+    uint8_t* base = skv + buf * 4 * TB;
+    for (int c = tid; c < AT_KT * CH; c += AT_THREADS) {
+      const int r = c / CH, ch = c % CH;
+      const bool pr = j0 + r < S;
+      const __nv_bfloat16* src = qkv + (tok0 + (pr ? j0 + r : 0)) * ld + h * DH + ch * 8;
+      cp_async16(base + swz<CH>(r, ch), src + H, pr);                 // k hi
+      cp_async16(base + TB + swz<CH>(r, ch), src + H + 3 * H, pr);    // k lo
+      cp_async16(base + 2 * TB + swz<CH>(r, ch), src + 2 * H, pr);    // v hi
+      cp_async16(base + 3 * TB + swz<CH>(r, ch), src + 2 * H + 3 * H, pr);  // v lo
+    }
+  };
+  load_kv(0, 0);
+  cp_async_commit();
+
+  const int nkt = (S + AT_KT - 1) / AT_KT;
+  float o[DH / 8][4];
+#pragma unroll
+  for (int i = 0; i < DH / 8; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) o[i][j] = 0.f;
+  float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
+  uint32_t qh[DH / 16][4], ql[DH / 16][4];
+
+  const int i_row0 = q0 + warp * 16 + (lane >> 2);  // this thread's rows: i_row0, i_row0 + 8
+  // padded query rows (i >= S) borrow the last token's slot; their output is dropped
+  const int slot_i0 = min(i_row0, S - 1) / K, slot_i1 = min(i_row0 + 8, S - 1) / K;
+
+  for (int kt = 0; kt < nkt; ++kt) {
+    if (kt + 1 < nkt) load_kv((kt + 1) & 1, (kt + 1) * AT_KT);
+    cp_async_commit();
+    cp_async_wait<1>();
+    __syncthreads();
+    if (kt == 0) {
+#pragma unroll
+      for (int kk = 0; kk < DH / 16; ++kk) {
+        const int r = warp * 16 + (lane & 15), ch = kk * 2 + (lane >> 4);
+        ldsm_x4(qh[kk][0], qh[kk][1], qh[kk][2], qh[kk][3], smem_addr(sq_hi) + swz<CH>(r, ch));
+        ldsm_x4(ql[kk][0], ql[kk][1], ql[kk][2], ql[kk][3], smem_addr(sq_lo) + swz<CH>(r, ch));
+      }
+    }
+    const uint8_t* base = skv + (kt & 1) * 4 * TB;
+    const uint32_t skh = smem_addr(base), skl = smem_addr(base + TB);
+    const uint32_t svh = smem_addr(base + 2 * TB), svl = smem_addr(base + 3 * TB);
+
+    float sc[AT_KT / 8][4];
+#pragma unroll
+    for (int i = 0; i < AT_KT / 8; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) sc[i][j] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < DH / 16; ++kk) {
+#pragma unroll
+      for (int np = 0; np < AT_KT / 16; ++np) {
+        const int r = np * 16 + (lane & 7) + ((lane >> 4) << 3);
+        const int ch = kk * 2 + ((lane >> 3) & 1);
+        uint32_t h0, h1, h2, h3, l0, l1, l2, l3;
+        ldsm_x4(h0, h1, h2, h3, skh + swz<CH>(r, ch));
+        ldsm_x4(l0, l1, l2, l3, skl + swz<CH>(r, ch));
+        mma_bf16(sc[2 * np], qh[kk], h0, h1);
+        mma_bf16(sc[2 * np], qh[kk], l0, l1);
+        mma_bf16(sc[2 * np], ql[kk], h0, h1);
+        mma_bf16(sc[2 * np + 1], qh[kk], h2, h3);
+        mma_bf16(sc[2 * np + 1], qh[kk], l2, l3);
+        mma_bf16(sc[2 * np + 1], ql[kk], h2, h3);
+      }
+    }
+    // scale, biases, mask; running max
+    float tmax[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int nt = 0; nt < AT_KT / 8; ++nt) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int j = kt * AT_KT + nt * 8 + (lane & 3) * 2 + (e & 1);
+        const int si = (e < 2) ? slot_i0 : slot_i1;
+        float v;
+        if (j < S) {
+          const int sj = j / K;
+          v = sc[nt][e] * scale + s_dist[sj - si + B_max - 2] + (sj == si ? same : 0.f);
+        } else {
+          v = -INFINITY;
+        }
+        sc[nt][e] = v;
+        tmax[e >> 1] = fmaxf(tmax[e >> 1], v);
+      }
+    }
+    float corr[2];
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+      tmax[rr] = fmaxf(tmax[rr], __shfl_xor_sync(FULL_MASK, tmax[rr], 1));
+      tmax[rr] = fmaxf(tmax[rr], __shfl_xor_sync(FULL_MASK, tmax[rr], 2));
+      const float mnew = fmaxf(mrow[rr], tmax[rr]);
+      corr[rr] = expf(mrow[rr] - mnew);
+      mrow[rr] = mnew;
+      lrow[rr] *= corr[rr];
+    }
+#pragma unroll
+    for (int dt = 0; dt < DH / 8; ++dt) {
+      o[dt][0] *= corr[0];
+      o[dt][1] *= corr[0];
+      o[dt][2] *= corr[1];
+      o[dt][3] *= corr[1];
+    }
+    // P = exp(s - m) in f32, split into hi/lo A fragments
+#pragma unroll
+    for (int kk = 0; kk < AT_KT / 16; ++kk) {
+      float pv[8];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        pv[e] = expf(sc[2 * kk][e] - mrow[e >> 1]);
+        pv[4 + e] = expf(sc[2 * kk + 1][e] - mrow[e >> 1]);
+      }
+      lrow[0] += pv[0] + pv[1] + pv[4] + pv[5];
+      lrow[1] += pv[2] + pv[3] + pv[6] + pv[7];
+      float ph[8], pl[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        ph[e] = __bfloat162float(__float2bfloat16_rn(pv[e]));
+        pl[e] = pv[e] - ph[e];
+      }
+      const uint32_t ah[4] = {pack_bf16(ph[0], ph[1]), pack_bf16(ph[2], ph[3]),
+                              pack_bf16(ph[4], ph[5]), pack_bf16(ph[6], ph[7])};
+      const uint32_t al[4] = {pack_bf16(pl[0], pl[1]), pack_bf16(pl[2], pl[3]),
+                              pack_bf16(pl[4], pl[5]), pack_bf16(pl[6], pl[7])};
+#pragma unroll
+      for (int dp = 0; dp < DH / 16; ++dp) {
+        const int r = kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+        const int ch = dp * 2 + (lane >> 4);
+        uint32_t h0, h1, h2, h3, l0, l1, l2, l3;
+        ldsm_x4_t(h0, h1, h2, h3, svh + swz<CH>(r, ch));
+        ldsm_x4_t(l0, l1, l2, l3, svl + swz<CH>(r, ch));
+        mma_bf16(o[2 * dp], ah, h0, h1);
+        mma_bf16(o[2 * dp], ah, l0, l1);
+        mma_bf16(o[2 * dp], al, h0, h1);
+        mma_bf16(o[2 * dp + 1], ah, h2, h3);
+        mma_bf16(o[2 * dp + 1], ah, l2, l3);
+        mma_bf16(o[2 * dp + 1], al, h2, h3);
+      }
+    }
+    __syncthreads();
+  }
+  cp_async_wait<0>();
+
+  // normalise and store split
+#pragma unroll
+  for (int rr = 0; rr < 2; ++rr) {
+    lrow[rr] += __shfl_xor_sync(FULL_MASK, lrow[rr], 1);
+    lrow[rr] += __shfl_xor_sync(FULL_MASK, lrow[rr], 2);
+  }
+#pragma unroll
+  for (int rr = 0; rr < 2; ++rr) {
+    const int i = i_row0 + rr * 8;
+    if (i >= S) continue;
+    const float inv = 1.0f / lrow[rr];
+    __nv_bfloat16* dst = out + (tok0 + i) * 2 * H + h * DH;
+#pragma unroll
+    for (int dt = 0; dt < DH / 8; ++dt) {
+      const int d = dt * 8 + (lane & 3) * 2;
+      __nv_bfloat16 h0, l0, h1, l1;
+      split_bf16(o[dt][rr * 2] * inv, h0, l0);
+      split_bf16(o[dt][rr * 2 + 1] * inv, h1, l1);
+      *reinterpret_cast<__nv_bfloat162*>(dst + d) = __halves2bfloat162(h0, h1);
+      *reinterpret_cast<__nv_bfloat162*>(dst + H + d) = __halves2bfloat162(l0, l1);
+    }
+  }
+}
+
+cudaError_t launch_attention(const __nv_bfloat16* qkv, int64_t batch, int S, int K, int H,
+                             int heads, int B_max, const float* dist_bias,
+                             const float* same_bias, __nv_bfloat16* out, cudaStream_t stream) {
+  const int dh = H / heads;
+  const dim3 grid((S + AT_QROWS - 1) / AT_QROWS, heads, static_cast<unsigned>(batch));
+  const int smem = (2 + 8) * AT_KT * dh * 2;
+  static bool attr = false;
+  if (!attr) {
+    cudaFuncSetAttribute(attention_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, 10 * 64 * 32 * 2);
+    cudaFuncSetAttribute(attention_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, 10 * 64 * 64 * 2);
+    cudaFuncSetAttribute(attention_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, 10 * 64 * 128 * 2);
+    attr = true;
+  }
+  switch (dh) {
+    case 32: attention_kernel<32><<<grid, AT_THREADS, smem, stream>>>(qkv, S, K, H, B_max, dist_bias, same_bias, out); break;
+    case 64: attention_kernel<64><<<grid, AT_THREADS, smem, stream>>>(qkv, S, K, H, B_max, dist_bias, same_bias, out); break;
+    case 128: attention_kernel<128><<<grid, AT_THREADS, smem, stream>>>(qkv, S, K, H, B_max, dist_bias, same_bias, out); break;
+    default: return cudaErrorInvalidValue;
+  }
+  note_launch();
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ fusion input
+// out split [M, 6H] = [h, t, h*t]_hi | [h, t, h*t]_lo (App. A: "concatenating the
+// candidate state, the target state, and their elementwise product").
+__global__ void fuse_concat_kernel(const float* __restrict__ X,
+                                   const __nv_bfloat16* __restrict__ target, int S, int64_t M,
+                                   int H, __nv_bfloat16* __restrict__ out) {
+  const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= M * H) return;
+  const int64_t m = idx / H;
+  const int h = static_cast<int>(idx % H);
+  const float x = X[idx];
+  const float t = target ? __bfloat162float(target[(m / S) * H + h]) : 0.f;
+  __nv_bfloat16* o = out + m * 6 * H;
+  __nv_bfloat16 hi, lo;
+  split_bf16(x, hi, lo);
+  o[h] = hi;
+  o[3 * H + h] = lo;
+  split_bf16(t, hi, lo);
+  o[H + h] = hi;
+  o[4 * H + h] = lo;
+  split_bf16(x * t, hi, lo);
+  o[2 * H + h] = hi;
+  o[5 * H + h] = lo;
+}
+
+// ------------------------------------------------------------------ anchor head (raw)
+// anchor_raw[b, e] = Wa[e, :] . t_b + ba[e]; t is exact bf16, accumulated in f32.
+__global__ void anchor_kernel(const __nv_bfloat16* __restrict__ target,
+                              const __nv_bfloat16* __restrict__ Wa, const float* __restrict__ ba,
+                              int H, int E, float* __restrict__ anchor_raw) {
+  const int64_t b = blockIdx.x;
+  const int lane = threadIdx.x & 31;
+  for (int e = threadIdx.x >> 5; e < E; e += blockDim.x >> 5) {
+    float acc = 0.f;
+    if (target)
+      for (int h = lane; h < H; h += 32)
+        acc = fmaf(__bfloat162float(Wa[int64_t(e) * H + h]), __bfloat162float(target[b * H + h]), acc);
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) acc += __shfl_xor_sync(FULL_MASK, acc, o);
+    if (lane == 0) anchor_raw[b * E + e] = acc + ba[e];
+  }
+}
+
+// ------------------------------------------------------------------ launchers
+
+cudaError_t launch_conf_hidden(const float* cand_logit, const float* lse, int64_t M, int K, int H,
+                               const float* w1, const float* b1, __nv_bfloat16* U,
+                               cudaStream_t stream) {
+  conf_hidden_kernel<<<static_cast<unsigned>(M), 128, 0, stream>>>(cand_logit, lse, M, K, H, w1, b1, U);
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rmsnorm_split(const float* X, const float* gain, int64_t M, int H, float eps,
+                                 __nv_bfloat16* out, cudaStream_t stream) {
+  const int wpb = 8;
+  rmsnorm_split_kernel<<<static_cast<unsigned>((M + wpb - 1) / wpb), wpb * 32, 0, stream>>>(
+      X, gain, M, H, eps, out);
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fuse_concat(const float* X, const __nv_bfloat16* target, int S, int64_t M,
+                               int H, __nv_bfloat16* out, cudaStream_t stream) {
+  const int64_t n = M * H;
+  fuse_concat_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, stream>>>(X, target, S, M, H, out);
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_anchor(const __nv_bfloat16* target, const __nv_bfloat16* Wa, const float* ba,
+                          int64_t batch, int H, int E, float* anchor_raw, cudaStream_t stream) {
+  anchor_kernel<<<static_cast<unsigned>(batch), 256, 0, stream>>>(target, Wa, ba, H, E, anchor_raw);
+  note_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace lilicorr

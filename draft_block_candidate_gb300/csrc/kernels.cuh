@@ -1,0 +1,60 @@
+// Host-side launchers of the rerank kernels (one declaration shared by all units).
+#pragma once
+
+#include "common.cuh"
+
+namespace lilicorr {
+
+// a1 logit pass (logit_pass.cu)
+size_t k1_workspace_bytes(int64_t batch, int B, int64_t V, int esize);
+cudaError_t k1_launch(const void* logits, int esize, int64_t batch, int B, int64_t V, int K,
+                      int32_t* cand_id, float* cand_logit, float* lse, void* ws,
+                      cudaStream_t stream);
+cudaError_t k1_read_device_error(uint32_t* code);
+
+// a4 scores + a5 walk (walk.cu)
+cudaError_t launch_pair_scores(const float* heads, const float* anchor_raw, int64_t batch, int B,
+                               int K, int E, float sigma, float* scores, float* out_tap,
+                               float* in_tap, float* anchor_tap, cudaStream_t stream);
+cudaError_t launch_greedy_walk(const float* scores, const int32_t* cand_id,
+                               const int32_t* anchor_ids, int64_t batch, int B, int K,
+                               int32_t* tokens, int32_t* choice, float* path,
+                               cudaStream_t stream);
+
+// a2/a3/a4 contractions (encoder.cu)
+enum Epi : int { EPI_F32 = 0, EPI_RESID = 1, EPI_SPLIT = 2, EPI_SPLIT_SILU = 3, EPI_NODE = 4 };
+
+struct GemmArgs {
+  const __nv_bfloat16* A;  // [M, Ka] (Ka = Kw, or 2*Kw for a split operand [A_hi | A_lo])
+  const __nv_bfloat16* W;  // [N, Kw]
+  int64_t M;
+  int N, Kw, Ka;
+  const float* bias;       // [N]
+  float* out;              // EPI_F32 / EPI_RESID / EPI_NODE: [M, N] f32
+  __nv_bfloat16* out_split;  // EPI_SPLIT*: [M, 2N]
+  // EPI_NODE extras: X = acc + bias + E[cand] + slot_table[s-1] + rank_table[k] + hidden
+  const __nv_bfloat16* embed;       // [V, N]
+  const int32_t* cand_id;           // [M]
+  const float* slot_table;          // [B_max-1, N]
+  const float* rank_table;          // [K_max, N]
+  const __nv_bfloat16* slot_hidden; // [batch, B, N] or null
+  int K, B;
+  int64_t vocab;                    // rows of embed (gather index is clamped to it)
+  float* nodes_tap;                 // [M, N] or null
+};
+
+cudaError_t launch_gemm(int epi, const GemmArgs& g, cudaStream_t stream);
+cudaError_t launch_conf_hidden(const float* cand_logit, const float* lse, int64_t M, int K, int H,
+                               const float* w1, const float* b1, __nv_bfloat16* U,
+                               cudaStream_t stream);
+cudaError_t launch_rmsnorm_split(const float* X, const float* gain, int64_t M, int H, float eps,
+                                 __nv_bfloat16* out, cudaStream_t stream);
+cudaError_t launch_attention(const __nv_bfloat16* qkv, int64_t batch, int S, int K, int H,
+                             int heads, int B_max, const float* dist_bias,
+                             const float* same_bias, __nv_bfloat16* out, cudaStream_t stream);
+cudaError_t launch_fuse_concat(const float* X, const __nv_bfloat16* target, int S, int64_t M,
+                               int H, __nv_bfloat16* out, cudaStream_t stream);
+cudaError_t launch_anchor(const __nv_bfloat16* target, const __nv_bfloat16* Wa, const float* ba,
+                          int64_t batch, int H, int E, float* anchor_raw, cudaStream_t stream);
+
+}  // namespace lilicorr

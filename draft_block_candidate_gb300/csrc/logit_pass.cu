@@ -1,0 +1,498 @@
+// Step a1: fused full-vocabulary log-partition + exact top-K, one read per logit row.
+//
+// What it computes (LiLiCorr: Lightweight Likelihood Correlation of Parallel Drafts for
+// Speculative Decoding, Sec. 3.2 "retains the drafter's top-K candidate tokens" and
+// App. A "log-probability ... under the full vocabulary"; serving PR "[Spec] Add
+// LiLiCorr", section "Why the custom kernels": exact top-k plus the log-partition from a
+// single pass over [n, V]):
+//   for each block b and drafted slot s = 1..B-1 (row 0, the anchor, is never read)
+//     lse[b,s-1]        = log sum_v exp(l[b,s,v])
+//     cand_*[b,s-1,0:K] = the K largest logits ordered by (value desc, token id asc)
+//
+// GB300 design.  The pass is HBM-bound (one streaming read of batch*(B-1)*V elements), so
+// each CTA streams a contiguous segment of one row through shared memory with 1-D bulk
+// copies (cp.async.bulk, 16 KB stages, 3 in flight, L2 evict-first) and every thread
+// consumes 16-byte chunks:
+//   * online log-sum-exp in base 2: per chunk one max, one FFMA + ex2 per element;
+//   * top-K: each warp keeps a sorted queue of 32 (value, id) pairs, one per lane; a
+//     chunk is only inspected when its maximum reaches the warp's K-th value (or a
+//     CTA-wide lower bound shared through shared memory), so after warm-up almost all
+//     chunks cost one compare; queues are merged with a 32-wide bitonic network.
+// Rows are split into P segments when there are too few rows to fill 152 SMs; the last
+// CTA of a row (atomic counter, no waiting) merges the P partial results.
+#include <float.h>
+#include <limits.h>
+
+#include <algorithm>
+#include <cmath>
+
+#include "kernels.cuh"
+
+namespace lilicorr {
+
+static __device__ uint32_t g_err_k1;
+
+constexpr int K1_THREADS = 512;
+constexpr int K1_WARPS = K1_THREADS / 32;
+constexpr int K1_STAGE_BYTES = 16384;
+constexpr int K1_NSTAGES = 4;
+constexpr int K1_CPT = K1_STAGE_BYTES / 16 / K1_THREADS;  // 16-byte chunks per thread per stage
+constexpr int KQ = 32;                                      // queue slots per warp
+constexpr float LOG2E = 1.4426950408889634f;
+constexpr float M2_INIT = -1e30f;                           // "no element yet", finite
+
+struct K1Partial {
+  float m2, s;
+  float v[KQ];
+  int id[KQ];
+};
+
+struct K1Params {
+  const char* logits;
+  int64_t batch;
+  int B;
+  int64_t V;
+  int K;
+  int P;
+  int64_t seg_bytes;
+  int32_t* cand_id;
+  float* cand_logit;
+  float* lse;
+  K1Partial* partials;
+  unsigned* counters;
+};
+
+__device__ __forceinline__ int64_t i64min(int64_t a, int64_t b) { return a < b ? a : b; }
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// (va, ia) ranks before (vb, ib): larger value, then smaller id.
+__device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
+  return va > vb || (va == vb && ia < ib);
+}
+
+struct WarpQueue {
+  float qv;   // this lane's entry (lane = position in the sorted queue)
+  int qid;
+  float tv;   // the K-th entry, warp-uniform
+  int tid;
+
+  __device__ void init() {
+    qv = -INFINITY;
+    qid = INT_MAX;
+    tv = -INFINITY;
+    tid = INT_MAX;
+  }
+  // Warp-uniform call: insert (v, id), known to rank before the K-th entry.
+  __device__ void insert(float v, int id, int lane, int K) {
+    const unsigned bm = __ballot_sync(FULL_MASK, better(qv, qid, v, id));
+    const int pos = __popc(bm);
+    const float uv = __shfl_up_sync(FULL_MASK, qv, 1);
+    const int uid = __shfl_up_sync(FULL_MASK, qid, 1);
+    if (lane > pos) {
+      qv = uv;
+      qid = uid;
+    } else if (lane == pos) {
+      qv = v;
+      qid = id;
+    }
+    tv = __shfl_sync(FULL_MASK, qv, K - 1);
+    tid = __shfl_sync(FULL_MASK, qid, K - 1);
+  }
+};
+
+// Merge sorted list (bv, bi) (one entry per lane, descending) into (v, id): afterwards
+// (v, id) holds the best 32 of the union, sorted.
+__device__ __forceinline__ void bitonic_merge(float& v, int& id, float bv, int bi, int lane) {
+  const float rv = __shfl_sync(FULL_MASK, bv, 31 - lane);
+  const int ri = __shfl_sync(FULL_MASK, bi, 31 - lane);
+  if (better(rv, ri, v, id)) {
+    v = rv;
+    id = ri;
+  }
+#pragma unroll
+  for (int st = 16; st >= 1; st >>= 1) {
+    const float ov = __shfl_xor_sync(FULL_MASK, v, st);
+    const int oi = __shfl_xor_sync(FULL_MASK, id, st);
+    const bool ob = better(ov, oi, v, id);
+    const bool lower = (lane & st) == 0;
+    if (lower ? ob : !ob) {
+      v = ov;
+      id = oi;
+    }
+  }
+}
+
+__device__ __forceinline__ void lse_merge(float& m2, float& s, float om2, float os) {
+  const float M = fmaxf(m2, om2);
+  s = s * ex2(m2 - M) + os * ex2(om2 - M);
+  m2 = M;
+}
+
+// Consume one chunk of n (0..NV) values held by this lane, ids id0..id0+n-1.
+// Warp-uniform call (lanes with n == 0 take part in the ballots).
+template <int NV>
+__device__ __forceinline__ void consume(const float (&x)[NV], int n, int id0, float& m2,
+                                        float& s, WarpQueue& q, float tau, int lane, int K) {
+  float cm = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < NV; ++j)
+    if (j < n) cm = fmaxf(cm, x[j]);
+  if (n > 0) {
+    const float cm2 = cm * LOG2E;
+    if (cm2 > m2) {
+      s *= ex2(m2 - cm2);
+      m2 = cm2;
+    }
+#pragma unroll
+    for (int j = 0; j < NV; ++j)
+      if (j < n) s += ex2(fmaf(x[j], LOG2E, -m2));
+  }
+  const float thr = fmaxf(q.tv, tau);
+  unsigned mask = __ballot_sync(FULL_MASK, n > 0 && cm >= thr);
+  while (mask) {
+    const int src = __ffs(mask) - 1;
+    mask &= mask - 1;
+    const int sid0 = __shfl_sync(FULL_MASK, id0, src);
+    const int sn = __shfl_sync(FULL_MASK, n, src);
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      const float v = __shfl_sync(FULL_MASK, x[j], src);
+      if (j < sn && better(v, sid0 + j, q.tv, q.tid)) q.insert(v, sid0 + j, lane, K);
+    }
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ float load_elem(const char* p);
+template <>
+__device__ __forceinline__ float load_elem<float>(const char* p) {
+  return __ldg(reinterpret_cast<const float*>(p));
+}
+template <>
+__device__ __forceinline__ float load_elem<__nv_bfloat16>(const char* p) {
+  return __bfloat162float(__ldg(reinterpret_cast<const __nv_bfloat16*>(p)));
+}
+
+template <typename T>
+__global__ void __launch_bounds__(K1_THREADS, 2) logit_pass_kernel(const K1Params p) {
+  constexpr int ES = sizeof(T);
+  constexpr int NV = 16 / ES;
+  extern __shared__ __align__(128) uint8_t k1_dyn_smem[];
+  uint8_t(*stage)[K1_STAGE_BYTES] = reinterpret_cast<uint8_t(*)[K1_STAGE_BYTES]>(k1_dyn_smem);
+  __shared__ __align__(8) uint64_t full_bar[K1_NSTAGES];
+  __shared__ float sq_v[K1_WARPS][KQ];
+  __shared__ int sq_i[K1_WARPS][KQ];
+  __shared__ float s_m2[K1_WARPS], s_s[K1_WARPS];
+  __shared__ int s_tau;
+  __shared__ int s_abort;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int K = p.K;
+  const int64_t u = blockIdx.x;
+  const int64_t r = u / p.P;
+  const int seg = static_cast<int>(u % p.P);
+  const int64_t b = r / (p.B - 1);
+  const int64_t s_slot = r % (p.B - 1) + 1;
+
+  // Row geometry in bytes relative to p.logits; body = 16-byte aligned part.
+  const int64_t row_start = (b * p.B + s_slot) * p.V * ES;
+  const int64_t row_end = row_start + p.V * ES;
+  const uintptr_t base = reinterpret_cast<uintptr_t>(p.logits);
+  int64_t body_start = static_cast<int64_t>(((base + row_start + 15) & ~uintptr_t(15)) - base);
+  int64_t body_end = static_cast<int64_t>(((base + row_end) & ~uintptr_t(15)) - base);
+  if (body_start >= body_end) body_start = body_end = row_end;
+  const int64_t seg_lo = i64min(body_end, body_start + seg * p.seg_bytes);
+  const int64_t seg_hi = i64min(body_end, seg_lo + p.seg_bytes);
+  const int nstages = static_cast<int>((seg_hi - seg_lo + K1_STAGE_BYTES - 1) / K1_STAGE_BYTES);
+
+  if (tid == 0) {
+    for (int i = 0; i < K1_NSTAGES; ++i) mbar_init(&full_bar[i], 1);
+    fence_mbar_init();
+    s_tau = float_key(-INFINITY);
+    s_abort = 0;
+  }
+  __syncthreads();
+
+  const uint64_t pol = policy_evict_first();
+  auto issue = [&](int st) {
+    const int64_t off = seg_lo + int64_t(st) * K1_STAGE_BYTES;
+    const uint32_t bytes = static_cast<uint32_t>(i64min(K1_STAGE_BYTES, seg_hi - off));
+    uint64_t* bar = &full_bar[st % K1_NSTAGES];
+    mbar_arrive_expect_tx(bar, bytes);
+    bulk_g2s(stage[st % K1_NSTAGES], p.logits + off, bytes, bar, pol);
+  };
+  if (tid == 0)
+    for (int st = 0; st < min(K1_NSTAGES - 1, nstages); ++st) issue(st);
+
+  float m2 = M2_INIT, ssum = 0.f;
+  WarpQueue q;
+  q.init();
+  float tau = -INFINITY;
+
+  // Unaligned head (segment 0) and tail (last segment) elements: plain loads by warp 0.
+  if (warp == 0) {
+    const int64_t row_elem0 = row_start / ES;
+    if (seg == 0) {
+      const int nh = static_cast<int>((body_start - row_start) / ES);
+      float x[NV];
+      const bool v = lane < nh;
+      x[0] = v ? load_elem<T>(p.logits + row_start + int64_t(lane) * ES) : 0.f;
+#pragma unroll
+      for (int j = 1; j < NV; ++j) x[j] = 0.f;
+      consume<NV>(x, v ? 1 : 0, lane, m2, ssum, q, tau, lane, K);
+    }
+    if (seg == p.P - 1 && body_end < row_end) {
+      const int nt = static_cast<int>((row_end - body_end) / ES);
+      float x[NV];
+      const bool v = lane < nt;
+      x[0] = v ? load_elem<T>(p.logits + body_end + int64_t(lane) * ES) : 0.f;
+#pragma unroll
+      for (int j = 1; j < NV; ++j) x[j] = 0.f;
+      consume<NV>(x, v ? 1 : 0, static_cast<int>((body_end / ES - row_elem0) + lane), m2, ssum,
+                  q, tau, lane, K);
+    }
+  }
+
+  const int seg_elem0 = static_cast<int>((seg_lo - row_start) / ES);  // id of first body elem
+  bool ok = true;
+  for (int st = 0; st < nstages; ++st) {
+    if (tid == 0 && st + K1_NSTAGES - 1 < nstages) issue(st + K1_NSTAGES - 1);
+    if (!mbar_wait_bounded(&full_bar[st % K1_NSTAGES], (st / K1_NSTAGES) & 1, &g_err_k1,
+                           ERR_K1_FULL_WAIT))
+      s_abort = 1;
+    tau = key_float(s_tau);
+    const int64_t off = int64_t(st) * K1_STAGE_BYTES;
+    const int nbytes = static_cast<int>(i64min(K1_STAGE_BYTES, (seg_hi - seg_lo) - off));
+    const uint8_t* sbuf = stage[st % K1_NSTAGES];
+#pragma unroll
+    for (int i = 0; i < K1_CPT; ++i) {
+      const int c = tid + i * K1_THREADS;
+      const bool valid = c * 16 < nbytes;
+      float x[NV];
+      if (valid) {
+        const uint4 w = *reinterpret_cast<const uint4*>(sbuf + c * 16);
+        if constexpr (ES == 2) {
+          const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            x[2 * k] = __uint_as_float(ww[k] << 16);
+            x[2 * k + 1] = __uint_as_float(ww[k] & 0xffff0000u);
+          }
+        } else {
+          x[0] = __uint_as_float(w.x);
+          x[1] = __uint_as_float(w.y);
+          x[2] = __uint_as_float(w.z);
+          x[3] = __uint_as_float(w.w);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < NV; ++j) x[j] = 0.f;
+      }
+      const int id0 = seg_elem0 + static_cast<int>((off + c * 16) / ES);
+      consume<NV>(x, valid ? NV : 0, id0, m2, ssum, q, tau, lane, K);
+    }
+    if (lane == 0 && q.tid != INT_MAX) atomicMax(&s_tau, float_key(q.tv));
+    __syncthreads();
+    if (s_abort) {
+      ok = false;
+      break;
+    }
+  }
+  if (!ok) {
+    // Give copies still in flight a bounded chance to land before the CTA exits.
+    if (tid == 0)
+      for (int st = 0; st < nstages; ++st)
+        if (!mbar_try_wait(&full_bar[st % K1_NSTAGES], (st / K1_NSTAGES) & 1))
+          mbar_wait_bounded(&full_bar[st % K1_NSTAGES], (st / K1_NSTAGES) & 1, &g_err_k1,
+                            ERR_K1_DRAIN);
+    return;
+  }
+
+  // ---- CTA merge: lse over threads, top-K over warps ----
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    const float om = __shfl_xor_sync(FULL_MASK, m2, o);
+    const float os = __shfl_xor_sync(FULL_MASK, ssum, o);
+    lse_merge(m2, ssum, om, os);
+  }
+  sq_v[warp][lane] = q.qv;
+  sq_i[warp][lane] = q.qid;
+  if (lane == 0) {
+    s_m2[warp] = m2;
+    s_s[warp] = ssum;
+  }
+  __syncthreads();
+  for (int half = K1_WARPS / 2; half >= 1; half >>= 1) {
+    if (warp < half) {
+      float v = sq_v[warp][lane];
+      int id = sq_i[warp][lane];
+      bitonic_merge(v, id, sq_v[warp + half][lane], sq_i[warp + half][lane], lane);
+      __syncwarp();
+      sq_v[warp][lane] = v;
+      sq_i[warp][lane] = id;
+    }
+    __syncthreads();
+  }
+  if (warp != 0) return;
+
+  float v = sq_v[0][lane];
+  int id = sq_i[0][lane];
+  float M = lane < K1_WARPS ? s_m2[lane] : M2_INIT;
+  float S = lane < K1_WARPS ? s_s[lane] : 0.f;
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    const float om = __shfl_xor_sync(FULL_MASK, M, o);
+    const float os = __shfl_xor_sync(FULL_MASK, S, o);
+    lse_merge(M, S, om, os);
+  }
+
+  if (p.P > 1) {
+    K1Partial* part = p.partials + u;
+    part->v[lane] = v;
+    part->id[lane] = id;
+    if (lane == 0) {
+      part->m2 = M;
+      part->s = S;
+    }
+    __threadfence();
+    __syncwarp();
+    unsigned prev = 0;
+    if (lane == 0) prev = atomicAdd(&p.counters[r], 1u);
+    prev = __shfl_sync(FULL_MASK, prev, 0);
+    if (prev != static_cast<unsigned>(p.P - 1)) return;
+    __threadfence();
+    const K1Partial* parts = p.partials + r * p.P;
+    v = __ldcg(&parts[0].v[lane]);
+    id = __ldcg(&parts[0].id[lane]);
+    M = __ldcg(&parts[0].m2);
+    S = __ldcg(&parts[0].s);
+    for (int k = 1; k < p.P; ++k) {
+      bitonic_merge(v, id, __ldcg(&parts[k].v[lane]), __ldcg(&parts[k].id[lane]), lane);
+      lse_merge(M, S, __ldcg(&parts[k].m2), __ldcg(&parts[k].s));
+    }
+    if (lane == 0) p.counters[r] = 0u;
+  }
+
+  if (lane < K) {
+    p.cand_id[r * K + lane] = id;
+    p.cand_logit[r * K + lane] = v;
+  }
+  if (lane == 0) {
+    const double l2 = static_cast<double>(M) + log2(static_cast<double>(S));
+    p.lse[r] = static_cast<float>(l2 / static_cast<double>(LOG2E));
+  }
+}
+
+// ------------------------------------------------------------------------------ host
+
+struct K1Plan {
+  int P;
+  int64_t seg_bytes;
+  size_t ws_bytes;
+};
+
+static int g_num_sms = 0;
+
+static int num_sms() {
+  if (g_num_sms == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (g_num_sms <= 0) g_num_sms = 148;
+  }
+  return g_num_sms;
+}
+
+K1Plan k1_plan(int64_t batch, int B, int64_t V, int esize) {
+  K1Plan pl{1, 0, 0};
+  const int64_t rows = batch * (B - 1);
+  const int64_t row_bytes = V * esize;
+  const int64_t stages = (row_bytes + K1_STAGE_BYTES - 1) / K1_STAGE_BYTES;
+  const int64_t conc = int64_t(num_sms()) * 2;  // resident CTAs
+  // Smallest P (1..64, at least one stage per segment) whose work fills whole waves
+  // of resident CTAs to within 5%; otherwise the best-filled P.
+  int bestP = 1;
+  double best_eff = -1.0;
+  const int64_t pmax = std::max<int64_t>(1, std::min<int64_t>(64, stages));
+  for (int P = 1; P <= pmax; ++P) {
+    const double waves = double(rows * P) / double(conc);
+    const double eff = waves / std::ceil(waves);
+    if (eff >= 0.95) {
+      bestP = P;
+      break;
+    }
+    if (eff > best_eff + 1e-9) {
+      best_eff = eff;
+      bestP = P;
+    }
+  }
+  pl.P = bestP;
+  const int64_t seg = (row_bytes + pl.P - 1) / pl.P;
+  pl.seg_bytes = std::max<int64_t>(16, (seg + 15) / 16 * 16);
+  if (pl.P > 1)
+    pl.ws_bytes = size_t(rows * pl.P) * sizeof(K1Partial) + size_t(rows) * sizeof(unsigned) + 256;
+  return pl;
+}
+
+size_t k1_workspace_bytes(int64_t batch, int B, int64_t V, int esize) {
+  return k1_plan(batch, B, V, esize).ws_bytes;
+}
+
+cudaError_t k1_launch(const void* logits, int esize, int64_t batch, int B, int64_t V, int K,
+                      int32_t* cand_id, float* cand_logit, float* lse, void* ws,
+                      cudaStream_t stream) {
+  const K1Plan pl = k1_plan(batch, B, V, esize);
+  K1Params prm;
+  prm.logits = static_cast<const char*>(logits);
+  prm.batch = batch;
+  prm.B = B;
+  prm.V = V;
+  prm.K = K;
+  prm.P = pl.P;
+  prm.seg_bytes = pl.seg_bytes;
+  prm.cand_id = cand_id;
+  prm.cand_logit = cand_logit;
+  prm.lse = lse;
+  prm.partials = nullptr;
+  prm.counters = nullptr;
+  const int64_t rows = batch * (B - 1);
+  if (pl.P > 1) {
+    prm.partials = static_cast<K1Partial*>(ws);
+    prm.counters = reinterpret_cast<unsigned*>(static_cast<char*>(ws) +
+                                               size_t(rows * pl.P) * sizeof(K1Partial));
+    cudaError_t e = cudaMemsetAsync(prm.counters, 0, size_t(rows) * sizeof(unsigned), stream);
+    if (e != cudaSuccess) return e;
+  }
+  const dim3 grid(static_cast<unsigned>(rows * pl.P));
+  constexpr int dyn = K1_NSTAGES * K1_STAGE_BYTES;
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaFuncSetAttribute(logit_pass_kernel<__nv_bfloat16>,
+                         cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
+    cudaFuncSetAttribute(logit_pass_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         dyn);
+    attr_done = true;
+  }
+  if (esize == 2)
+    logit_pass_kernel<__nv_bfloat16><<<grid, K1_THREADS, dyn, stream>>>(prm);
+  else
+    logit_pass_kernel<float><<<grid, K1_THREADS, dyn, stream>>>(prm);
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t k1_read_device_error(uint32_t* code) {
+  uint32_t v = 0, zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_err_k1, sizeof(v));
+  if (e != cudaSuccess) return e;
+  if (v) e = cudaMemcpyToSymbol(g_err_k1, &zero, sizeof(zero));
+  *code |= v;
+  return e;
+}
+
+}  // namespace lilicorr

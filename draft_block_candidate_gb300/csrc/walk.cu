@@ -1,0 +1,164 @@
+// Steps a4 (normalise + matching scores) and a5 (greedy commit).
+//
+// Matching score (LiLiCorr: Lightweight Likelihood Correlation of Parallel Drafts for
+// Speculative Decoding, Sec. 3.2, Eq. 1): phi(s,k,k') = sigma * cos(o_{s,k}, i_{s+1,k'})
+// for s = 0..B-2, with one anchor out vector o_0 (K_0 = 1).  Sec. 3.5: the (B-2)K^2 + K
+// terms are one small product per adjacent slot pair, batched over the block.
+// Greedy commit (Sec. 3.5, Eq. 8): c_s = argmax_k phi(s-1, c_{s-1}, k), ties to the
+// lowest k (serving PR "[Spec] Add LiLiCorr", "Why the custom kernels": the argmax
+// breaks ties toward the lower index).
+#include <float.h>
+#include <limits.h>
+
+#include "kernels.cuh"
+
+namespace lilicorr {
+
+// One CTA per (block b, pair p).  heads [batch*S, 2E] holds the raw out | in head
+// outputs; anchor_raw [batch, E] the raw anchor head output.  Vectors are normalised
+// here (nrm(v) = v / max(||v||, 1e-12)) and dotted in f32.
+__global__ void __launch_bounds__(256) pair_scores_kernel(
+    const float* __restrict__ heads, const float* __restrict__ anchor_raw, int B, int K, int E,
+    float sigma, float* __restrict__ scores, float* __restrict__ out_tap,
+    float* __restrict__ in_tap, float* __restrict__ anchor_tap) {
+  extern __shared__ float ps_smem[];
+  const int E1 = E + 1;
+  float* so = ps_smem;            // [K][E1] out vectors of slot p (or o_0 in row 0)
+  float* si = ps_smem + K * E1;   // [K][E1] in vectors of slot p+1
+  const int p = blockIdx.x, b = blockIdx.y;
+  const int S = (B - 1) * K;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
+  const int64_t blk_row0 = int64_t(b) * S;
+
+  // rows to normalise: out rows of slot p (p >= 1) or the anchor (p == 0); in rows of
+  // slot p+1; the p == 0 CTA also normalises slot B-1's out rows for the tap.
+  const int n_out = (p == 0) ? 1 : K;
+  for (int r = warp; r < n_out + K; r += nw) {
+    const float* src;
+    float* dst;
+    float* tap = nullptr;
+    if (r < n_out) {
+      if (p == 0) {
+        src = anchor_raw + int64_t(b) * E;
+        tap = anchor_tap ? anchor_tap + int64_t(b) * E : nullptr;
+      } else {
+        const int64_t row = blk_row0 + int64_t(p - 1) * K + r;
+        src = heads + row * (2 * E);
+        tap = out_tap ? out_tap + row * E : nullptr;
+      }
+      dst = so + r * E1;
+    } else {
+      const int k = r - n_out;
+      const int64_t row = blk_row0 + int64_t(p) * K + k;
+      src = heads + row * (2 * E) + E;
+      tap = in_tap ? in_tap + row * E : nullptr;
+      dst = si + k * E1;
+    }
+    float ss = 0.f;
+    for (int e = lane; e < E; e += 32) {
+      const float v = src[e];
+      ss = fmaf(v, v, ss);
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) ss += __shfl_xor_sync(FULL_MASK, ss, o);
+    const float inv = 1.0f / fmaxf(sqrtf(ss), 1e-12f);
+    for (int e = lane; e < E; e += 32) {
+      const float v = src[e] * inv;
+      dst[e] = v;
+      if (tap) tap[e] = v;
+    }
+  }
+  if (p == 0 && out_tap) {
+    for (int k = warp; k < K; k += nw) {
+      const int64_t row = blk_row0 + int64_t(B - 2) * K + k;
+      const float* src = heads + row * (2 * E);
+      float ss = 0.f;
+      for (int e = lane; e < E; e += 32) ss = fmaf(src[e], src[e], ss);
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) ss += __shfl_xor_sync(FULL_MASK, ss, o);
+      const float inv = 1.0f / fmaxf(sqrtf(ss), 1e-12f);
+      for (int e = lane; e < E; e += 32) out_tap[row * E + e] = src[e] * inv;
+    }
+  }
+  __syncthreads();
+
+  float* dst = scores + (int64_t(b) * (B - 1) + p) * K * K;
+  for (int t = tid; t < K * K; t += blockDim.x) {
+    const int k = t / K, kk = t % K;
+    float v;
+    if (p == 0 && k > 0) {
+      v = -INFINITY;
+    } else {
+      const float* a = so + k * E1;
+      const float* c = si + kk * E1;
+      float acc = 0.f;
+      for (int e = 0; e < E; ++e) acc = fmaf(a[e], c[e], acc);
+      v = sigma * acc;
+    }
+    dst[t] = v;
+  }
+}
+
+// One warp per block: B-1 dependent argmaxes over K <= 32 candidates.
+__global__ void __launch_bounds__(128) greedy_walk_kernel(
+    const float* __restrict__ scores, const int32_t* __restrict__ cand_id,
+    const int32_t* __restrict__ anchor_ids, int64_t batch, int B, int K,
+    int32_t* __restrict__ tokens, int32_t* __restrict__ choice, float* __restrict__ path) {
+  const int lane = threadIdx.x & 31;
+  const int64_t b = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (b >= batch) return;
+  if (lane == 0) tokens[b * B] = anchor_ids ? anchor_ids[b] : -1;
+  int prev = 0;
+  for (int p = 0; p < B - 1; ++p) {
+    const int64_t pr = b * (B - 1) + p;
+    const float* row = scores + (pr * K + prev) * K;
+    float v = lane < K ? row[lane] : -INFINITY;
+    int idx = lane < K ? lane : INT_MAX;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+      const float ov = __shfl_xor_sync(FULL_MASK, v, o);
+      const int oi = __shfl_xor_sync(FULL_MASK, idx, o);
+      if (ov > v || (ov == v && oi < idx)) {
+        v = ov;
+        idx = oi;
+      }
+    }
+    if (lane == 0) {
+      if (choice) choice[pr] = idx;
+      if (path) path[pr] = v;
+      tokens[b * B + p + 1] = cand_id[pr * K + idx];
+    }
+    prev = idx;
+  }
+}
+
+cudaError_t launch_pair_scores(const float* heads, const float* anchor_raw, int64_t batch, int B,
+                               int K, int E, float sigma, float* scores, float* out_tap,
+                               float* in_tap, float* anchor_tap, cudaStream_t stream) {
+  const size_t smem = size_t(2) * K * (E + 1) * sizeof(float);
+  static bool attr = false;
+  if (!attr) {
+    cudaFuncSetAttribute(pair_scores_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         2 * 32 * 257 * 4);
+    attr = true;
+  }
+  const dim3 grid(B - 1, static_cast<unsigned>(batch));
+  pair_scores_kernel<<<grid, 256, smem, stream>>>(heads, anchor_raw, B, K, E, sigma, scores,
+                                                  out_tap, in_tap, anchor_tap);
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_greedy_walk(const float* scores, const int32_t* cand_id,
+                               const int32_t* anchor_ids, int64_t batch, int B, int K,
+                               int32_t* tokens, int32_t* choice, float* path,
+                               cudaStream_t stream) {
+  const int wpb = 4;
+  const unsigned grid = static_cast<unsigned>((batch + wpb - 1) / wpb);
+  greedy_walk_kernel<<<grid, 32 * wpb, 0, stream>>>(scores, cand_id, anchor_ids, batch, B, K,
+                                                     tokens, choice, path);
+  note_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace lilicorr

@@ -1,0 +1,194 @@
+/*
+ * lilicorr.h -- C ABI of the GB300 (sm_103a) LiLiCorr draft-time rerank path.
+ *
+ * The path (LiLiCorr: Lightweight Likelihood Correlation of Parallel Drafts for
+ * Speculative Decoding, Sec. 3.2, Sec. 3.5 and App. A):
+ *   a1  per drafted slot, one read of the vocabulary logits gives the full-vocabulary
+ *       log-partition and the top-K candidates            (App. A "Serving"; serving PR
+ *       "[Spec] Add LiLiCorr ...", section "Why the custom kernels")
+ *   a2  each candidate becomes a node: embedding + drafter hidden + confidence MLP over
+ *       five scalars + slot and rank tables                (Sec. 3.2; App. A "Architecture")
+ *   a3  a two-layer bidirectional transformer over the (B-1) x K lattice (App. A)
+ *   a4  target fusion, out/in/anchor heads, unit norm, matching scores
+ *       phi(s,k,k') = sigma * cos(o_{s,k}, i_{s+1,k'})     (Sec. 3.2, Eq. 1)
+ *   a5  greedy commit c_s = argmax_k phi(s-1, c_{s-1}, k)  (Sec. 3.5, Eq. 8)
+ *
+ * Conventions for every entry point:
+ *   - Device pointers are caller-owned CUDA device memory, contiguous, row-major.
+ *   - `stream` is a cudaStream_t passed as void*; NULL means the legacy default stream.
+ *     Device entry points only enqueue work on `stream`: they never allocate and never
+ *     synchronise, so a call can be captured in a CUDA graph.
+ *   - All arguments are checked on the host before any launch; a violation returns an
+ *     error status and launches nothing.  A failed launch returns LILICORR_ERR_CUDA
+ *     (lilicorr_last_error() has the CUDA message).  No device-side trap is used.
+ *   - Logits are finite or -inf (no NaN, no +inf); each row holds a finite value.
+ *   - Index arguments use 0-based slots for arrays; drafted slot s (1..B-1) is stored
+ *     at index s-1 of [.., B-1, ..] arrays.
+ */
+#ifndef LILICORR_H_
+#define LILICORR_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  LILICORR_OK = 0,
+  LILICORR_ERR_INVALID_ARG = 1,     /* a size, pointer or alignment is out of contract   */
+  LILICORR_ERR_UNSUPPORTED = 2,     /* legal but not built (e.g. K > 32, f32 weights)     */
+  LILICORR_ERR_WEIGHTS_MISSING = 3, /* a required head tensor is absent                   */
+  LILICORR_ERR_WEIGHTS_SURPLUS = 4, /* an unknown head tensor was given                   */
+  LILICORR_ERR_WEIGHTS_SHAPE = 5,   /* a head tensor's shape or dtype disagrees with dims */
+  LILICORR_ERR_CUDA = 6,            /* a CUDA call failed                                 */
+  LILICORR_ERR_WORKSPACE = 7,       /* workspace missing, too small or misaligned         */
+  LILICORR_ERR_DEVICE = 8           /* a kernel reported a device-side error (timeout)    */
+} lilicorr_status;
+
+typedef enum { LILICORR_F32 = 0, LILICORR_BF16 = 1 } lilicorr_dtype;
+
+/* Head geometry (LiLiCorr App. A, Table 4).  Constraints checked at weight creation:
+ * hidden % 64 == 0; heads divides hidden with hidden/heads in {32, 64, 128};
+ * ffn % 64 == 0; d_e % 32 == 0 and d_e <= 256; 2 <= B_max <= 64; 1 <= K_max <= 32;
+ * V >= 1.  sigma is the cosine scale (8.0 in Table 4), rms_eps the RMSNorm epsilon. */
+typedef struct {
+  int32_t layers, hidden, heads, ffn, d_e, B_max, K_max;
+  int64_t V;
+  float sigma;
+  float rms_eps;
+} lilicorr_dims;
+
+/* One named head tensor in host memory.  Weights are bf16 bit patterns (dtype must be
+ * LILICORR_BF16), row-major, shapes as listed in DESIGN notes and checked exactly:
+ *   embed [V,H]  slot_table [B_max-1,H]  rank_table [K_max,H]
+ *   conf.w1 [H,5] conf.b1 [H] conf.w2 [H,H] conf.b2 [H]
+ *   layers.{l}.norm1 [H] .in_proj_w [3H,H] .in_proj_b [3H] .out_proj_w [H,H]
+ *     .out_proj_b [H] .dist_bias [heads,2*B_max-3] .same_bias [heads] .norm2 [H]
+ *     .ffn.w1 [F,H] .ffn.b1 [F] .ffn.w2 [H,F] .ffn.b2 [H]
+ *   fuse.w [H,3H] fuse.b [H]  head_out.w [E,H] head_out.b [E]
+ *   head_in.w [E,H] head_in.b [E]  head_anchor.w [E,H] head_anchor.b [E]
+ * The in_proj layout is nn.MultiheadAttention's packed [q; k; v] (serving PR, design
+ * note 3).  The host data is copied; the caller may free it after the call returns. */
+typedef struct {
+  const char* name;
+  const void* host_data;
+  lilicorr_dtype dtype;
+  int32_t ndim;
+  int64_t shape[4];
+} lilicorr_tensor;
+
+typedef struct lilicorr_weights lilicorr_weights; /* opaque, library-owned device arena */
+
+/* Validate the tensor set against dims and copy it into a device arena on `device`.
+ * Missing names -> WEIGHTS_MISSING, unknown names -> WEIGHTS_SURPLUS (both directions
+ * are refused, as the serving PR's loader does, design note 4), wrong shape or dtype ->
+ * WEIGHTS_SHAPE.  Synchronous; allocates device memory (the only call that does). */
+lilicorr_status lilicorr_weights_create(const lilicorr_dims* dims,
+                                        const lilicorr_tensor* tensors, int32_t n,
+                                        int device, lilicorr_weights** out);
+void lilicorr_weights_destroy(lilicorr_weights* w);
+/* Copy of the dims the weights were created with. */
+lilicorr_status lilicorr_weights_dims(const lilicorr_weights* w, lilicorr_dims* out);
+
+/* Bytes of device workspace lilicorr_rerank needs for this call shape (0 on bad args). */
+size_t lilicorr_workspace_bytes(const lilicorr_weights* w, int64_t batch, int32_t B,
+                                int32_t K);
+
+/* Optional extra outputs of lilicorr_rerank (any member may be NULL; the struct
+ * pointer itself may be NULL).  S = (B-1)*K lattice nodes per block, slot-major. */
+typedef struct {
+  int32_t* choice;      /* [batch,B-1]      committed candidate index per slot          */
+  int32_t* cand_id;     /* [batch,B-1,K]    top-K token ids, (logit desc, id asc)        */
+  float* cand_logit;    /* [batch,B-1,K]    their logits, exactly widened to f32         */
+  float* lse;           /* [batch,B-1]      natural-log full-vocabulary log-partition    */
+  float* pair_scores;   /* [batch,B-1,K,K]  [p,k,k'] = phi(p,k,k'); pair 0 row>0 = -inf */
+  float* nodes;         /* [batch,S,H]      node vectors (encoder input)                 */
+  float* hidden;        /* [batch,S,H]      encoder output                               */
+  float* out_vec;       /* [batch,S,d_e]    unit out vectors                             */
+  float* in_vec;        /* [batch,S,d_e]    unit in vectors                              */
+  float* anchor_vec;    /* [batch,d_e]      unit anchor out vector o_0                   */
+} lilicorr_taps;
+
+/* The whole rerank on `stream`.
+ *   logits       [batch,B,V] of ldtype (F32 or BF16); row 0 of each block (the anchor
+ *                position) is not read.  Rows need only element alignment.
+ *   B            2 <= B <= dims.B_max;  V == dims.V;  1 <= K <= min(dims.K_max, V)
+ *   slot_hidden  nullable [batch,B,H] bf16: drafter hidden per slot (row 0 unused)
+ *   target_state nullable [batch,H] bf16: projected target state t
+ *   anchor_ids   nullable [batch] int32: written to tokens[:,0] (else -1)
+ *   tokens       [batch,B] int32 out;  path_score [batch,B-1] f32 out:
+ *                path_score[b,s-1] = phi(s-1, c_{s-1}, c_s)
+ *   workspace    device memory of >= lilicorr_workspace_bytes(...) bytes, 256-B aligned;
+ *                its contents need no initialisation and are clobbered.
+ * Concurrent calls must not share a workspace. */
+lilicorr_status lilicorr_rerank(const lilicorr_weights* w, const void* logits,
+                                lilicorr_dtype ldtype, int64_t batch, int32_t B, int64_t V,
+                                int32_t K, const void* slot_hidden, const void* target_state,
+                                const int32_t* anchor_ids, int32_t* tokens, float* path_score,
+                                const lilicorr_taps* taps, void* workspace,
+                                size_t workspace_bytes, void* stream);
+
+/* Host-memory form of lilicorr_rerank: logits, slot_hidden, target_state and anchor_ids
+ * are host pointers (pinned memory makes the copies asynchronous), tokens and
+ * path_score are host outputs.  The inputs are copied to device staging inside
+ * `workspace` (size from lilicorr_workspace_bytes_host), the rerank runs on `stream`,
+ * the outputs are copied back, and the call returns after synchronising `stream`. */
+size_t lilicorr_workspace_bytes_host(const lilicorr_weights* w, int64_t batch, int32_t B,
+                                     int32_t K, lilicorr_dtype ldtype);
+lilicorr_status lilicorr_rerank_host(const lilicorr_weights* w, const void* logits_host,
+                                     lilicorr_dtype ldtype, int64_t batch, int32_t B,
+                                     int64_t V, int32_t K, const void* slot_hidden_host,
+                                     const void* target_state_host,
+                                     const int32_t* anchor_ids_host, int32_t* tokens_host,
+                                     float* path_score_host, void* workspace,
+                                     size_t workspace_bytes, void* stream);
+
+/* Step a1 alone (serving PR, "Why the custom kernels": exact per-row top-k plus the
+ * full-vocabulary log-partition from one pass over the logits).  For every block b and
+ * drafted slot s = 1..B-1 it reads row logits[b,s,:] once and writes
+ *   cand_id[b,s-1,:K] int32, cand_logit[b,s-1,:K] f32 (logit desc, token id asc) and
+ *   lse[b,s-1] = log sum_v exp(logits[b,s,v]) (f32, natural log).
+ * 1 <= K <= min(32, V).  Workspace: lilicorr_topk_lse_workspace_bytes (may be 0). */
+size_t lilicorr_topk_lse_workspace_bytes(int64_t batch, int32_t B, int64_t V, int32_t K,
+                                         lilicorr_dtype ldtype);
+lilicorr_status lilicorr_topk_lse(const void* logits, lilicorr_dtype ldtype, int64_t batch,
+                                  int32_t B, int64_t V, int32_t K, int32_t* cand_id,
+                                  float* cand_logit, float* lse, void* workspace,
+                                  size_t workspace_bytes, void* stream);
+
+/* Step a5 alone (LiLiCorr Sec. 3.5, Eq. 8) on given scores pair_scores [batch,B-1,K,K]
+ * (layout as in lilicorr_taps).  c_1 = argmax_k pair_scores[b,0,0,k]; c_s = argmax_k
+ * pair_scores[b,s-1,c_{s-1},k]; ties go to the lowest k (serving PR: the Triton
+ * argmax breaks ties toward the lower index).  cand_id [batch,B-1,K] maps choices to
+ * tokens.  Outputs: tokens [batch,B] (tokens[:,0] = anchor_ids or -1), choice
+ * [batch,B-1] (nullable), path_score [batch,B-1] (nullable).  1 <= K <= 32. */
+lilicorr_status lilicorr_greedy_walk(const float* pair_scores, const int32_t* cand_id,
+                                     const int32_t* anchor_ids, int64_t batch, int32_t B,
+                                     int32_t K, int32_t* tokens, int32_t* choice,
+                                     float* path_score, void* stream);
+
+/* Human-readable name of a status; never NULL. */
+const char* lilicorr_status_string(lilicorr_status s);
+/* Message of the most recent CUDA failure in this thread ("" if none). */
+const char* lilicorr_last_error(void);
+/* Kernels this library has launched since load (all threads). */
+uint64_t lilicorr_launch_count(void);
+/* Read and clear the device-side error word of the current device (synchronises the
+ * device): 0 = no error; otherwise a bit set per failed wait site. */
+lilicorr_status lilicorr_device_error(uint32_t* code);
+
+/* Per-stage timing.  When enabled, lilicorr_rerank records CUDA events on its stream
+ * around each stage; lilicorr_stage_times() synchronises on them and adds the elapsed
+ * milliseconds per stage into ms[0..n) (stage order: see lilicorr_stage_name), returns
+ * the number of stages, and resets the accumulators. */
+void lilicorr_stage_timing(int enable);
+int32_t lilicorr_stage_times(double* ms, int32_t n, int64_t* calls);
+const char* lilicorr_stage_name(int32_t i);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LILICORR_H_ */

@@ -1,0 +1,154 @@
+"""The whole path on the GPU against the oracle.
+
+Walk (a5) fed the oracle's own scores: choices bit-exact.  End to end: candidate ids
+bit-exact, lse within 1e-5, pair scores within 1e-3, committed tokens bit-exact unless
+the oracle's own top-2 margin at the first differing slot is below twice the measured
+score difference (reported as tie-ambiguous, never silently accepted)."""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import lilicorr_oracle as O
+from synth import make_workload
+from tests.gpu_util import (SCORE_ATOL, check_block, dev_bf16, dev_logits, oracle_block)
+
+pytestmark = pytest.mark.gpu
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+@pytest.fixture(scope="module")
+def lc():
+    import __graft_entry__
+    __graft_entry__.build()
+    import draft_block_candidate_gb300 as m
+    return m
+
+
+# ------------------------------------------------------------------ walk on given scores
+
+def test_walk_golden(lc):
+    gd = json.load(open(os.path.join(GOLDEN, "greedy_vs_exact_path.json")))
+    sc = np.array([[[float(v) for v in r] for r in p] for p in gd["scores"]], np.float32)
+    cid = torch.tensor(gd["cand_id"], dtype=torch.int32).cuda()[None]
+    tok, ch, path = lc.greedy_walk(torch.from_numpy(sc).cuda()[None], cid,
+                                   torch.tensor([gd["anchor_id"]], dtype=torch.int32).cuda())
+    assert ch.cpu().numpy()[0].tolist() == gd["greedy_choice"]
+    assert tok.cpu().numpy()[0].tolist() == gd["greedy_tokens"]
+    assert path.cpu().numpy()[0].tolist() == gd["greedy_path_score"]
+
+
+@pytest.mark.parametrize("K", [1, 2, 3, 8, 16, 31, 32])
+def test_walk_matches_oracle_on_oracle_scores(lc, K):
+    rng = np.random.default_rng(K)
+    batch, B = 37, 16
+    sc = (np.round(rng.standard_normal((batch, B - 1, K, K)) * 3) / 4).astype(np.float32)  # ties
+    sc[:, 0, 1:] = -np.inf
+    cid = rng.integers(0, 151936, size=(batch, B - 1, K)).astype(np.int32)
+    tok, ch, path = lc.greedy_walk(torch.from_numpy(sc).cuda(), torch.from_numpy(cid).cuda())
+    tok, ch, path = tok.cpu().numpy(), ch.cpu().numpy(), path.cpu().numpy()
+    for b in range(batch):
+        rc, rp, _ = O.greedy_walk(sc[b].astype(np.float64))
+        assert ch[b].tolist() == rc.tolist()
+        assert np.array_equal(path[b], rp.astype(np.float32))
+        assert tok[b, 0] == -1 and tok[b, 1:].tolist() == cid[b, np.arange(B - 1), rc].tolist()
+
+
+# ------------------------------------------------------------------ end to end
+
+def _gpu_run(lc, wl, weights=None, taps=True, blocks=None):
+    w = weights or lc.Weights(wl.dims, wl.weights)
+    out = lc.rerank(w, dev_logits(wl), wl.K, slot_hidden=dev_bf16(wl.slot_hidden),
+                    target_state=dev_bf16(wl.target_state),
+                    anchor_ids=None if wl.anchor_ids is None else torch.from_numpy(wl.anchor_ids).cuda(),
+                    taps=taps)
+    torch.cuda.synchronize()
+    res = {k: v.cpu().numpy() for k, v in out.items()}
+    if weights is None:
+        w.close()
+    return res
+
+
+def _compare(lc, wl, blocks=None, report=None):
+    gpu = _gpu_run(lc, wl)
+    report = {} if report is None else report
+    for b in (range(wl.batch) if blocks is None else blocks):
+        ref = oracle_block(wl, b)
+        check_block(gpu, ref, b, report)
+    return gpu, report
+
+
+SMALL = [  # name, overrides
+    ("tiny", {}),
+    ("tiny", dict(batch=3, seed=11)),
+    ("single", dict(V=4096, batch=3)),
+    ("sweep", dict(V=4096, batch=4)),
+    ("highconc", dict(V=4096, batch=2, tier="low")),
+    ("highconc", dict(V=4096, batch=2, tier="high")),
+    ("widepool", dict(V=4096, batch=2)),
+    ("single", dict(V=3001, batch=2, B=9)),          # shorter block than B_max, odd V
+    ("single", dict(V=4096, batch=2, with_slot_hidden=True)),
+    ("single", dict(V=4096, batch=1, with_target=False, with_anchor=False)),
+    ("highconc", dict(V=2048, batch=5, K=1)),
+]
+
+
+@pytest.mark.parametrize("name,kw", SMALL)
+def test_rerank_small(lc, name, kw):
+    wl = make_workload(name, **kw)
+    gpu, rep = _compare(lc, wl)
+    print(name, kw, rep)
+    if kw.get("K") == 1:      # K = 1 reproduces the per-slot argmax block
+        x = wl.logits_f32()
+        for b in range(wl.batch):
+            assert gpu["tokens"][b, 1:].tolist() == [int(np.argmax(x[b, s])) for s in range(1, wl.B)]
+
+
+def test_rerank_taps_match_oracle_intermediates(lc):
+    wl = make_workload("single", V=4096, batch=2, with_slot_hidden=True)
+    gpu = _gpu_run(lc, wl)
+    for b in range(wl.batch):
+        ref = oracle_block(wl, b)
+        for name, atol in (("nodes", 1e-5), ("hidden", 1e-4), ("out_vec", 1e-5), ("in_vec", 1e-5)):
+            g = gpu[name][b].reshape(ref[name].shape)
+            assert np.abs(g - ref[name]).max() <= atol, (name, np.abs(g - ref[name]).max())
+        assert np.abs(gpu["anchor_vec"][b] - ref["anchor_vec"]).max() <= 1e-6
+
+
+def test_rerank_is_deterministic(lc):
+    wl = make_workload("highconc", V=8192, batch=8)
+    a = _gpu_run(lc, wl)
+    b = _gpu_run(lc, wl)
+    for k in a:
+        assert np.array_equal(a[k], b[k], equal_nan=True), k
+
+
+def test_permuted_candidates_commit_same_tokens(lc):
+    """Two workloads whose logits differ only in vocabulary order give the same tokens
+    up to the relabelling (the path sees tokens only through their embeddings)."""
+    wl = make_workload("single", V=4096, batch=2)
+    gpu_a = _gpu_run(lc, wl, taps=False)
+    rng = np.random.default_rng(5)
+    perm = rng.permutation(wl.V)
+    wl2 = make_workload("single", V=4096, batch=2)
+    wl2.logits = wl.logits[:, :, perm]
+    wl2.weights = dict(wl.weights)
+    wl2.weights["embed"] = wl.weights["embed"][perm]
+    gpu_b = _gpu_run(lc, wl2, taps=False)
+    assert np.array_equal(perm[gpu_b["tokens"][:, 1:]], gpu_a["tokens"][:, 1:])
+
+
+@pytest.mark.parametrize("name,kw,nblocks", [
+    ("single", {}, 1),
+    ("highconc", dict(tier="medium"), 3),
+    ("widepool", {}, 3),
+    ("sweep", dict(batch=128), 2),
+])
+def test_rerank_full_size_sampled_blocks(lc, name, kw, nblocks):
+    wl = make_workload(name, **kw)
+    rng = np.random.default_rng(1)
+    blocks = sorted(rng.choice(wl.batch, nblocks, replace=False).tolist())
+    _, rep = _compare(lc, wl, blocks)
+    print(name, rep)
