@@ -1,0 +1,391 @@
+#!/usr/bin/env python
+"""Throughput of the LiLiCorr draft-time rerank on GB300: draft blocks reranked per second.
+
+Default workload: the high-concurrency shape (batch 256 blocks of B = 16 positions,
+V = 151,936, K = 16, bf16 logits, medium-entropy tier, encoder 2 x hidden 256 / 4 heads /
+FFN 1024, d_e 128), synthetic seeded inputs and random-init weights.
+
+One step = one lilicorr_rerank call over the batch (logit pass, node build, encoder,
+fusion/heads/scores, greedy walk) with inputs resident in HBM.  The logits (1,167 MB per
+step) are larger than L2, so no flush is needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+
+Under torchrun every rank runs its own batch (blocks are independent: weak scaling, no
+collective on the data path); rank 0 prints one JSON line.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "draft blocks reranked/sec at 1 GB300; logit-pass HBM GB/s as % of peak"
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return PEAKS_FALLBACK, "fallback"
+
+
+def describe(wl):
+    d = wl.dims
+    return (f"{wl.name}: batch {wl.batch}, B {wl.B}, V {wl.V}, K {wl.K}, {wl.ldtype} logits; "
+            f"encoder {d['layers']} layers, hidden {d['hidden']}, {d['heads']} heads, "
+            f"FFN {d['ffn']}, d_e {d['d_e']}")
+
+
+# ------------------------------------------------------------------ clocks during timing
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.path = tempfile.mktemp(suffix=".csv")
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(gpu_index)],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = [l.strip().split(",") for l in open(self.path) if l.strip()]
+        os.unlink(self.path)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [x.strip() for x in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ CPU oracle timing
+
+def oracle_timing(workload, tier, blocks, steps, warmup, threads=1):
+    env = dict(os.environ)
+    for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[v] = str(threads)
+    cmd = [sys.executable, "-m", "oracle.time_oracle", "--workload", workload,
+           "--blocks", str(blocks), "--steps", str(steps), "--warmup", str(warmup)]
+    if tier:
+        cmd += ["--tier", tier]
+    r = subprocess.run(cmd, cwd=ROOT, env=env, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"oracle timing failed: {r.stderr[-2000:]}")
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+# ------------------------------------------------------------------ ncu traffic record
+
+def recorded_traffic(kernel: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, only if the
+    kernel's source is unchanged since the capture (sha256 recorded beside the figure)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    for line in open(path):
+        f = dict(kv.split("=", 1) for kv in line.split() if "=" in kv)
+        if f.get("kernel") != kernel:
+            continue
+        src = os.path.join(ROOT, "draft_block_candidate_gb300", "csrc", f.get("source", ""))
+        if not os.path.exists(src):
+            return None
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        if sha != f.get("src_sha"):
+            return None
+        return float(f["bytes_per_launch"])
+    return None
+
+
+# ------------------------------------------------------------------ arms
+
+def run_reference(a):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    res = oracle_timing(a.workload, a.tier, a.ref_blocks, a.steps, a.warmup)
+    v = res["blocks_per_s"]
+    wlname = a.workload + (f"/{a.tier}" if a.tier else "")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "blocks/s",
+        "n_gpus": a.gpus, "steps": a.steps, "warmup": a.warmup,
+        "ms_per_step": 1e3 * statistics.mean(res["step_s"]), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wlname, "sample": f"{a.ref_blocks} block(s) per step"},
+        "cpu_baseline": {"value": v, "unit": "blocks/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{a.ref_blocks} block(s) of {wlname} per step, "
+                                   f"{a.steps} steps, 1 thread (BLAS/OpenMP pinned)"},
+        "e2e": {"value": v, "unit": "blocks/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_gb300(a):
+    import numpy as np
+    import torch
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import draft_block_candidate_gb300 as lc
+    from synth import make_workload
+
+    # CPU baseline first (a fresh, thread-pinned process), rank 0 at N = 1 only.
+    cpu = None
+    if rank == 0 and world == 1 and not a.no_cpu_baseline:
+        res = oracle_timing(a.workload, a.tier, a.cpu_blocks, 2, 1)
+        cpu = {"value": res["blocks_per_s"], "unit": "blocks/s", "cores": 1, "kind": "oracle",
+               "sample": f"{a.cpu_blocks} blocks x 2 timed steps of the same workload "
+                         f"(full rows, float64, 1 thread)"}
+
+    wl = make_workload(a.workload, tier=a.tier, batch=a.batch)
+    batch, B, V, K = wl.batch, wl.B, wl.V, wl.K
+    logits_host = torch.from_numpy(wl.logits.view(np.int16)).view(torch.bfloat16)
+    logits = logits_host.to(dev)
+    tgt_host = torch.from_numpy(wl.target_state.view(np.int16)).view(torch.bfloat16)
+    tgt = tgt_host.to(dev)
+    anc_host = torch.from_numpy(wl.anchor_ids)
+    anc = anc_host.to(dev)
+    w = lc.Weights(wl.dims, wl.weights, device=local)
+    ws = w.workspace(batch, B, K)
+    out = {"tokens": torch.empty(batch, B, dtype=torch.int32, device=dev),
+           "path_score": torch.empty(batch, B - 1, dtype=torch.float32, device=dev)}
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        lc.rerank(w, logits, K, target_state=tgt, anchor_ids=anc, workspace=ws, out=out,
+                  stream=stream)
+
+    for _ in range(a.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    clocks = ClockSampler(local)
+    time.sleep(0.3)
+    lc.stage_timing(True)
+    lc.stage_times()  # clear
+    barrier()
+    torch.cuda.synchronize(dev)
+    n0 = lc.launch_count()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(a.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    launches = lc.launch_count() - n0
+    ms = e0.elapsed_time(e1)
+    lc.stage_timing(False)
+    st = lc.stage_times()
+    clk = clocks.stop()
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    value = batch * a.steps * world / (ms / 1e3)
+
+    # e2e through the host-memory entry point: H2D copies in, D2H tokens out, per step.
+    e2e = None
+    if not a.no_e2e:
+        pin_logits = logits_host.pin_memory()
+        pin_tgt = tgt_host.pin_memory()
+        pin_anc = anc_host.pin_memory()
+        tok_h = torch.empty(batch, B, dtype=torch.int32).pin_memory()
+        ps_h = torch.empty(batch, B - 1, dtype=torch.float32).pin_memory()
+        wsh = lc.rerank_host_workspace(w, batch, B, K, lc.BF16)
+        for _ in range(2):
+            lc.rerank_host(w, pin_logits, K, target_state=pin_tgt, anchor_ids=pin_anc,
+                           tokens=tok_h, path_score=ps_h, workspace=wsh, stream=stream)
+        barrier()
+        t0 = time.perf_counter()
+        for _ in range(a.e2e_steps):
+            lc.rerank_host(w, pin_logits, K, target_state=pin_tgt, anchor_ids=pin_anc,
+                           tokens=tok_h, path_score=ps_h, workspace=wsh, stream=stream)
+        el = time.perf_counter() - t0
+        barrier()
+        if world > 1:
+            t = torch.tensor([el], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            el = float(t.item())
+        h2d = (pin_logits.numel() * 2 + pin_tgt.numel() * 2 + pin_anc.numel() * 4)
+        d2h = tok_h.numel() * 4 + ps_h.numel() * 4
+        e2e = {"value": batch * a.e2e_steps * world / el, "unit": "blocks/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": a.e2e_steps,
+               "api": "lilicorr_rerank_host (pinned host buffers)"}
+        del wsh
+
+    if rank != 0:
+        return
+
+    pk, pk_kind = peaks()
+    calls = st.pop("calls")
+    per_kernel = {k: {"ms_per_step": v["ms"] / max(calls, 1),
+                      "avg_launch_us": 1e3 * v["ms"] / max(v["launches"], 1),
+                      "launches_per_step": v["launches"] / max(calls, 1)}
+                  for k, v in st.items() if v["launches"]}
+    step_ms = ms / a.steps
+    dominant = max(per_kernel, key=lambda k: per_kernel[k]["ms_per_step"])
+    H, F, E, S = wl.dims["hidden"], wl.dims["ffn"], wl.dims["d_e"], (B - 1) * K
+    M = batch * S
+    logit_bytes = batch * (B - 1) * V * 2
+    # executed tensor work per launch (split-bf16: the contraction dimension is doubled)
+    gemm_flops = {"qkv_gemm": 2 * M * 3 * H * 2 * H, "out_gemm": 2 * M * H * 2 * H,
+                  "ffn1_gemm": 2 * M * F * 2 * H, "ffn2_gemm": 2 * M * H * 2 * F,
+                  "node_gemm": 2 * M * H * 2 * H, "fuse_gemm": 2 * M * H * 6 * H,
+                  "heads_gemm": 2 * M * 2 * E * 2 * H}
+    k1 = per_kernel["logit_pass"]
+    k1_gbs = logit_bytes / (k1["avg_launch_us"] * 1e-6) / 1e9
+    logit_pass = {"achieved": k1_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                  "frac": k1_gbs / pk["hbm_gbs"], "bytes_per_launch": logit_bytes,
+                  "avg_launch_us": k1["avg_launch_us"], "peak_kind": pk_kind}
+    if dominant == "logit_pass":
+        roof = {"bound": "hbm", "kernel": "logit_pass", "achieved": k1_gbs, "peak": pk["hbm_gbs"],
+                "unit": "GB/s", "frac": k1_gbs / pk["hbm_gbs"],
+                "traffic": recorded_traffic("logit_pass"), "peak_kind": pk_kind}
+    elif dominant in gemm_flops:
+        tf = gemm_flops[dominant] / (per_kernel[dominant]["avg_launch_us"] * 1e-6) / 1e12
+        peak = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
+        roof = {"bound": "tensor", "kernel": dominant, "achieved": tf, "peak": peak,
+                "unit": "TFLOP/s", "frac": tf / peak, "traffic": recorded_traffic(dominant),
+                "peak_kind": pk_kind + " sustained bf16"}
+    else:
+        roof = {"bound": "latency", "kernel": dominant, "achieved": None, "peak": None,
+                "unit": None, "frac": None, "traffic": None}
+    line = {
+        "metric": METRIC, "value": value, "unit": "blocks/s", "n_gpus": world,
+        "steps": a.steps, "warmup": a.warmup, "ms_per_step": step_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": describe(wl), "batch_per_gpu": batch, "B": B, "V": V, "K": K,
+                   "l2": f"inputs larger than L2 ({logit_bytes / 1e6:.0f} MB of logits per step); no flush",
+                   "parallelism": f"dp{world} (independent blocks per rank)"},
+        "roofline": roof,
+        "logit_pass": logit_pass,
+        "e2e_fraction_of_logits_roofline": (logit_bytes / (pk["hbm_gbs"] * 1e9)) / (step_ms / 1e3),
+        "gpu_launches": launches,
+        "kernels": per_kernel,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+    w.close()
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def run_logit_pass_only(a):
+    """lilicorr_topk_lse alone on the workload's logits (a small --batch keeps an ncu
+    capture short); CUDA-event timing on the launching stream."""
+    import numpy as np
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import draft_block_candidate_gb300 as lc
+    from synth import make_workload
+
+    wl = make_workload(a.workload, tier=a.tier, batch=a.batch)
+    x = torch.from_numpy(wl.logits.view(np.int16)).view(torch.bfloat16).cuda()
+    ws = lc.topk_lse_workspace(wl.batch, wl.B, wl.V, wl.K, lc.BF16, x.device)
+    out = lc.topk_lse(x, wl.K, workspace=ws)
+    for _ in range(a.warmup):
+        lc.topk_lse(x, wl.K, workspace=ws, out=out)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(a.steps):
+        lc.topk_lse(x, wl.K, workspace=ws, out=out)
+    e1.record()
+    torch.cuda.synchronize()
+    us = 1e3 * e0.elapsed_time(e1) / a.steps
+    nbytes = wl.batch * (wl.B - 1) * wl.V * 2
+    pk, kind = peaks()
+    print(json.dumps({"kernel": "logit_pass", "workload": describe(wl), "avg_launch_us": us,
+                      "GB/s": nbytes / us / 1e3, "frac_of_peak": nbytes / us / 1e3 / pk["hbm_gbs"],
+                      "peak_kind": kind, "bytes_per_launch": nbytes}), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default="highconc")
+    ap.add_argument("--tier", default="medium")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--cpu-blocks", type=int, default=4)
+    ap.add_argument("--ref-blocks", type=int, default=1)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=None, help="override the workload's batch")
+    ap.add_argument("--only", default=None, choices=["logit_pass"],
+                    help="time one kernel alone (profiling driver); prints its own JSON")
+    a = ap.parse_args()
+    if a.workload != "highconc":
+        a.tier = None
+    if a.warmup < 3:
+        a.warmup = 3
+    if a.impl == "reference":
+        run_reference(a)
+    elif a.only == "logit_pass":
+        run_logit_pass_only(a)
+    else:
+        run_gb300(a)
+
+
+if __name__ == "__main__":
+    main()

@@ -38,8 +38,8 @@ SIGNATURES = {
     "lilicorr_launch_count": (C.c_uint64, []),
     "lilicorr_device_error": (C.c_int, [C.POINTER(C.c_uint32)]),
     "lilicorr_stage_timing": (None, [C.c_int]),
-    "lilicorr_stage_times": (C.c_int32, [C.POINTER(C.c_double), C.c_int32,
-                                         C.POINTER(C.c_int64)]),
+    "lilicorr_stage_times": (C.c_int32, [C.POINTER(C.c_double), C.POINTER(C.c_int64),
+                                         C.c_int32, C.POINTER(C.c_int64)]),
     "lilicorr_stage_name": (C.c_char_p, [C.c_int32]),
 }
 

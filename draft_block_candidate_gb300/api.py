@@ -231,11 +231,15 @@ def stage_timing(enable: bool) -> None:
     L.lib().lilicorr_stage_timing(1 if enable else 0)
 
 
-def stage_times() -> Dict[str, float]:
-    """Accumulated milliseconds per stage since the last read, plus 'calls'."""
-    ms = (C.c_double * 8)()
+def stage_times() -> Dict[str, dict]:
+    """Per-kernel timing accumulated since the last read: {name: {"ms": total ms,
+    "launches": n}} plus "calls"."""
+    n = 32
+    ms = (C.c_double * n)()
+    la = (C.c_int64 * n)()
     calls = C.c_int64(0)
-    n = L.lib().lilicorr_stage_times(ms, 8, C.byref(calls))
-    out = {L.lib().lilicorr_stage_name(i).decode(): ms[i] for i in range(n)}
+    k = L.lib().lilicorr_stage_times(ms, la, n, C.byref(calls))
+    out = {L.lib().lilicorr_stage_name(i).decode(): {"ms": ms[i], "launches": int(la[i])}
+           for i in range(k)}
     out["calls"] = int(calls.value)
     return out

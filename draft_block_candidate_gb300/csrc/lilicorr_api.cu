@@ -26,18 +26,58 @@ static lilicorr_status cuda_fail(cudaError_t e, const char* where) {
     if (e_ != cudaSuccess) return cuda_fail(e_, where); \
   } while (0)
 
-// ---- stage timing
-constexpr int NSTAGE = 5;
-static const char* kStageNames[NSTAGE] = {"logit_pass", "node_build", "encoder", "fuse_heads",
-                                          "scores_walk"};
+// ---- per-kernel timing: events recorded on the caller's stream after each launch
+enum Slot : int {
+  T_LOGIT = 0, T_CONF, T_NODE, T_NORM, T_QKV, T_ATTN, T_OUT, T_FFN1, T_FFN2, T_FUSECAT,
+  T_FUSE, T_HEADS, T_ANCHOR, T_SCORES, T_WALK, NSLOT
+};
+static const char* kSlotNames[NSLOT] = {
+    "logit_pass", "conf_hidden", "node_gemm", "rmsnorm", "qkv_gemm", "attention", "out_gemm",
+    "ffn1_gemm", "ffn2_gemm", "fuse_concat", "fuse_gemm", "heads_gemm", "anchor_head",
+    "pair_scores", "greedy_walk"};
+
+struct CallRecord {
+  cudaEvent_t start;
+  std::vector<std::pair<int, cudaEvent_t>> marks;
+};
 struct StageTimer {
   std::mutex mu;
   bool enabled = false;
-  std::vector<cudaEvent_t> pending;  // groups of NSTAGE + 1 events
-  double ms[NSTAGE] = {0, 0, 0, 0, 0};
+  std::vector<CallRecord> pending;
+  double ms[NSLOT] = {};
+  int64_t launches[NSLOT] = {};
   int64_t calls = 0;
 };
 static StageTimer g_timer;
+
+struct CallTimer {
+  bool on = false;
+  cudaStream_t stream = nullptr;
+  CallRecord rec{};
+  cudaError_t begin(cudaStream_t s) {
+    {
+      std::lock_guard<std::mutex> lk(g_timer.mu);
+      on = g_timer.enabled;
+    }
+    stream = s;
+    if (!on) return cudaSuccess;
+    cudaError_t e = cudaEventCreate(&rec.start);
+    return e == cudaSuccess ? cudaEventRecord(rec.start, s) : e;
+  }
+  cudaError_t mark(int slot) {
+    if (!on) return cudaSuccess;
+    cudaEvent_t e;
+    cudaError_t r = cudaEventCreate(&e);
+    if (r != cudaSuccess) return r;
+    rec.marks.push_back({slot, e});
+    return cudaEventRecord(e, stream);
+  }
+  void finish() {
+    if (!on) return;
+    std::lock_guard<std::mutex> lk(g_timer.mu);
+    g_timer.pending.push_back(rec);
+  }
+};
 
 }  // namespace lilicorr
 
@@ -423,26 +463,17 @@ lilicorr_status lilicorr_rerank(const lilicorr_weights* w, const void* logits,
   float* anchor_raw = reinterpret_cast<float*>(ws + pl.anchor);
   const __nv_bfloat16* target = static_cast<const __nv_bfloat16*>(target_state);
 
-  bool timing;
-  {
-    std::lock_guard<std::mutex> lk(g_timer.mu);
-    timing = g_timer.enabled;
-  }
-  cudaEvent_t ev[NSTAGE + 1];
-  if (timing)
-    for (auto& e : ev) LC_CUDA(cudaEventCreate(&e), "cudaEventCreate");
-  auto mark = [&](int i) -> cudaError_t {
-    return timing ? cudaEventRecord(ev[i], stream) : cudaSuccess;
-  };
-
-  LC_CUDA(mark(0), "event");
+  CallTimer tm;
+  LC_CUDA(tm.begin(stream), "timing event");
+#define MARK(slot) LC_CUDA(tm.mark(slot), "timing event")
   // a1: logit pass
   LC_CUDA(k1_launch(logits, es, batch, B, V, K, cand_id, cand_logit, lse, ws + pl.k1, stream),
           "logit pass");
-  LC_CUDA(mark(1), "event");
+  MARK(T_LOGIT);
   // a2: node build
   LC_CUDA(launch_conf_hidden(cand_logit, lse, M, K, H, w->conf_w1, w->conf_b1, act1, stream),
           "confidence features");
+  MARK(T_CONF);
   {
     GemmArgs g{};
     g.A = act1; g.W = w->conf_w2; g.M = M; g.N = H; g.Kw = H; g.Ka = 2 * H; g.bias = w->conf_b2;
@@ -450,59 +481,67 @@ lilicorr_status lilicorr_rerank(const lilicorr_weights* w, const void* logits,
     g.rank_table = w->rank_table; g.slot_hidden = static_cast<const __nv_bfloat16*>(slot_hidden);
     g.K = K; g.B = B; g.vocab = d.V; g.nodes_tap = tp.nodes;
     LC_CUDA(launch_gemm(EPI_NODE, g, stream), "node gemm");
+    MARK(T_NODE);
   }
-  LC_CUDA(mark(2), "event");
   // a3: encoder
   for (const auto& L : w->layers) {
     LC_CUDA(launch_rmsnorm_split(X, L.norm1, M, H, d.rms_eps, act1, stream), "rmsnorm");
+    MARK(T_NORM);
     GemmArgs g{};
     g.A = act1; g.W = L.in_w; g.M = M; g.N = 3 * H; g.Kw = H; g.Ka = 2 * H; g.bias = L.in_b;
     g.out_split = qkv;
     LC_CUDA(launch_gemm(EPI_SPLIT, g, stream), "qkv gemm");
+    MARK(T_QKV);
     LC_CUDA(launch_attention(qkv, batch, S, K, H, d.heads, d.B_max, L.dist, L.same, act1, stream),
             "attention");
+    MARK(T_ATTN);
     g = GemmArgs{};
     g.A = act1; g.W = L.out_w; g.M = M; g.N = H; g.Kw = H; g.Ka = 2 * H; g.bias = L.out_b; g.out = X;
     LC_CUDA(launch_gemm(EPI_RESID, g, stream), "out-proj gemm");
+    MARK(T_OUT);
     LC_CUDA(launch_rmsnorm_split(X, L.norm2, M, H, d.rms_eps, act1, stream), "rmsnorm");
+    MARK(T_NORM);
     g = GemmArgs{};
     g.A = act1; g.W = L.w1; g.M = M; g.N = F; g.Kw = H; g.Ka = 2 * H; g.bias = L.b1; g.out_split = ffh;
     LC_CUDA(launch_gemm(EPI_SPLIT_SILU, g, stream), "ffn1 gemm");
+    MARK(T_FFN1);
     g = GemmArgs{};
     g.A = ffh; g.W = L.w2; g.M = M; g.N = H; g.Kw = F; g.Ka = 2 * F; g.bias = L.b2; g.out = X;
     LC_CUDA(launch_gemm(EPI_RESID, g, stream), "ffn2 gemm");
+    MARK(T_FFN2);
   }
   if (tp.hidden)
     LC_CUDA(cudaMemcpyAsync(tp.hidden, X, size_t(M) * H * 4, cudaMemcpyDeviceToDevice, stream),
             "hidden tap");
-  LC_CUDA(mark(3), "event");
   // a4: fusion and heads
   LC_CUDA(launch_fuse_concat(X, target, S, M, H, qkv, stream), "fusion input");
+  MARK(T_FUSECAT);
   {
     GemmArgs g{};
     g.A = qkv; g.W = w->fuse_w; g.M = M; g.N = H; g.Kw = 3 * H; g.Ka = 6 * H; g.bias = w->fuse_b;
     g.out_split = act1;
     LC_CUDA(launch_gemm(EPI_SPLIT_SILU, g, stream), "fusion gemm");
+    MARK(T_FUSE);
     g = GemmArgs{};
     g.A = act1; g.W = w->heads_w; g.M = M; g.N = 2 * E; g.Kw = H; g.Ka = 2 * H; g.bias = w->heads_b;
     g.out = heads;
     LC_CUDA(launch_gemm(EPI_F32, g, stream), "heads gemm");
+    MARK(T_HEADS);
   }
   LC_CUDA(launch_anchor(target, w->anchor_w, w->anchor_b, batch, H, E, anchor_raw, stream),
           "anchor head");
-  LC_CUDA(mark(4), "event");
+  MARK(T_ANCHOR);
   // a4 scores + a5 walk
   LC_CUDA(launch_pair_scores(heads, anchor_raw, batch, B, K, E, d.sigma, scores, tp.out_vec,
                              tp.in_vec, tp.anchor_vec, stream),
           "pair scores");
+  MARK(T_SCORES);
   LC_CUDA(launch_greedy_walk(scores, cand_id, anchor_ids, batch, B, K, tokens, tp.choice,
                              path_score, stream),
           "greedy walk");
-  LC_CUDA(mark(5), "event");
-  if (timing) {
-    std::lock_guard<std::mutex> lk(g_timer.mu);
-    for (auto& e : ev) g_timer.pending.push_back(e);
-  }
+  MARK(T_WALK);
+#undef MARK
+  tm.finish();
   return LILICORR_OK;
 }
 
@@ -575,29 +614,36 @@ void lilicorr_stage_timing(int enable) {
   g_timer.enabled = enable != 0;
 }
 
-int32_t lilicorr_stage_times(double* ms, int32_t n, int64_t* calls) {
+int32_t lilicorr_stage_times(double* ms, int64_t* launches, int32_t n, int64_t* calls) {
   std::lock_guard<std::mutex> lk(g_timer.mu);
-  for (size_t i = 0; i + NSTAGE + 1 <= g_timer.pending.size(); i += NSTAGE + 1) {
-    cudaEvent_t* e = &g_timer.pending[i];
-    cudaEventSynchronize(e[NSTAGE]);
-    for (int s = 0; s < NSTAGE; ++s) {
+  for (auto& rec : g_timer.pending) {
+    if (!rec.marks.empty()) cudaEventSynchronize(rec.marks.back().second);
+    cudaEvent_t prev = rec.start;
+    for (auto& m : rec.marks) {
       float t = 0.f;
-      cudaEventElapsedTime(&t, e[s], e[s + 1]);
-      g_timer.ms[s] += t;
+      cudaEventElapsedTime(&t, prev, m.second);
+      g_timer.ms[m.first] += t;
+      g_timer.launches[m.first] += 1;
+      prev = m.second;
     }
-    for (int s = 0; s <= NSTAGE; ++s) cudaEventDestroy(e[s]);
+    cudaEventDestroy(rec.start);
+    for (auto& m : rec.marks) cudaEventDestroy(m.second);
     g_timer.calls += 1;
   }
   g_timer.pending.clear();
-  for (int s = 0; s < n && s < NSTAGE; ++s) ms[s] = g_timer.ms[s];
+  for (int s = 0; s < n && s < NSLOT; ++s) {
+    if (ms) ms[s] = g_timer.ms[s];
+    if (launches) launches[s] = g_timer.launches[s];
+  }
   if (calls) *calls = g_timer.calls;
-  for (int s = 0; s < NSTAGE; ++s) g_timer.ms[s] = 0;
+  for (int s = 0; s < NSLOT; ++s) {
+    g_timer.ms[s] = 0;
+    g_timer.launches[s] = 0;
+  }
   g_timer.calls = 0;
-  return NSTAGE;
+  return NSLOT;
 }
 
-const char* lilicorr_stage_name(int32_t i) {
-  return (i >= 0 && i < NSTAGE) ? kStageNames[i] : "";
-}
+const char* lilicorr_stage_name(int32_t i) { return (i >= 0 && i < NSLOT) ? kSlotNames[i] : ""; }
 
 }  // extern "C"

@@ -178,6 +178,22 @@ __device__ __forceinline__ float load_elem<__nv_bfloat16>(const char* p) {
   return __bfloat162float(__ldg(reinterpret_cast<const __nv_bfloat16*>(p)));
 }
 
+// Descending bitonic sort of one value per lane across the warp.
+__device__ __forceinline__ float warp_sort_desc(float v, int lane) {
+#pragma unroll
+  for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      const float o = __shfl_xor_sync(FULL_MASK, v, j);
+      const bool keep_max = ((lane & j) == 0) == ((lane & k) == 0);
+      v = keep_max ? fmaxf(v, o) : fminf(v, o);
+    }
+  }
+  return v;
+}
+
+constexpr int K1_CAP = 1024;  // candidate buffer entries per CTA
+
 template <typename T>
 __global__ void __launch_bounds__(K1_THREADS, 2) logit_pass_kernel(const K1Params p) {
   constexpr int ES = sizeof(T);
@@ -187,9 +203,11 @@ __global__ void __launch_bounds__(K1_THREADS, 2) logit_pass_kernel(const K1Param
   __shared__ __align__(8) uint64_t full_bar[K1_NSTAGES];
   __shared__ float sq_v[K1_WARPS][KQ];
   __shared__ int sq_i[K1_WARPS][KQ];
+  __shared__ float s_buf_v[K1_CAP];
+  __shared__ int s_buf_i[K1_CAP];
   __shared__ float s_m2[K1_WARPS], s_s[K1_WARPS];
-  __shared__ int s_tau;
-  __shared__ int s_abort;
+  __shared__ float s_tau_v, s_L0;
+  __shared__ int s_tau_i, s_cnt, s_abort;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int K = p.K;
@@ -213,7 +231,7 @@ __global__ void __launch_bounds__(K1_THREADS, 2) logit_pass_kernel(const K1Param
   if (tid == 0) {
     for (int i = 0; i < K1_NSTAGES; ++i) mbar_init(&full_bar[i], 1);
     fence_mbar_init();
-    s_tau = float_key(-INFINITY);
+    s_cnt = 0;
     s_abort = 0;
   }
   __syncthreads();
@@ -230,31 +248,34 @@ __global__ void __launch_bounds__(K1_THREADS, 2) logit_pass_kernel(const K1Param
     for (int st = 0; st < min(K1_NSTAGES - 1, nstages); ++st) issue(st);
 
   float m2 = M2_INIT, ssum = 0.f;
-  WarpQueue q;
-  q.init();
-  float tau = -INFINITY;
+  // Warp 0 owns the running top-K of everything consumed so far (one entry per lane,
+  // sorted); the other warps see its K-th entry through s_tau_v / s_tau_i.
+  WarpQueue run;
+  run.init();
 
-  // Unaligned head (segment 0) and tail (last segment) elements: plain loads by warp 0.
+  // Unaligned head (segment 0) and tail (last segment) elements: plain loads by warp 0,
+  // straight into the running queue.
   if (warp == 0) {
     const int64_t row_elem0 = row_start / ES;
+    float x[NV];
+#pragma unroll
+    for (int j = 1; j < NV; ++j) x[j] = 0.f;
     if (seg == 0) {
       const int nh = static_cast<int>((body_start - row_start) / ES);
-      float x[NV];
       const bool v = lane < nh;
       x[0] = v ? load_elem<T>(p.logits + row_start + int64_t(lane) * ES) : 0.f;
-#pragma unroll
-      for (int j = 1; j < NV; ++j) x[j] = 0.f;
-      consume<NV>(x, v ? 1 : 0, lane, m2, ssum, q, tau, lane, K);
+      consume<NV>(x, v ? 1 : 0, lane, m2, ssum, run, -INFINITY, lane, K);
     }
     if (seg == p.P - 1 && body_end < row_end) {
       const int nt = static_cast<int>((row_end - body_end) / ES);
-      float x[NV];
       const bool v = lane < nt;
       x[0] = v ? load_elem<T>(p.logits + body_end + int64_t(lane) * ES) : 0.f;
-#pragma unroll
-      for (int j = 1; j < NV; ++j) x[j] = 0.f;
       consume<NV>(x, v ? 1 : 0, static_cast<int>((body_end / ES - row_elem0) + lane), m2, ssum,
-                  q, tau, lane, K);
+                  run, -INFINITY, lane, K);
+    }
+    if (lane == 0) {
+      s_tau_v = run.tv;
+      s_tau_i = run.tid;
     }
   }
 
@@ -265,38 +286,150 @@ __global__ void __launch_bounds__(K1_THREADS, 2) logit_pass_kernel(const K1Param
     if (!mbar_wait_bounded(&full_bar[st % K1_NSTAGES], (st / K1_NSTAGES) & 1, &g_err_k1,
                            ERR_K1_FULL_WAIT))
       s_abort = 1;
-    tau = key_float(s_tau);
     const int64_t off = int64_t(st) * K1_STAGE_BYTES;
     const int nbytes = static_cast<int>(i64min(K1_STAGE_BYTES, (seg_hi - seg_lo) - off));
     const uint8_t* sbuf = stage[st % K1_NSTAGES];
+
+    // ---- load this thread's chunks and fold them into the log-sum-exp
+    float x[K1_CPT][NV];
+    int n[K1_CPT], id0[K1_CPT];
+    float tmax = -INFINITY;
 #pragma unroll
     for (int i = 0; i < K1_CPT; ++i) {
       const int c = tid + i * K1_THREADS;
-      const bool valid = c * 16 < nbytes;
-      float x[NV];
-      if (valid) {
+      n[i] = c * 16 < nbytes ? NV : 0;
+      id0[i] = seg_elem0 + static_cast<int>((off + c * 16) / ES);
+      if (n[i]) {
         const uint4 w = *reinterpret_cast<const uint4*>(sbuf + c * 16);
         if constexpr (ES == 2) {
           const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            x[2 * k] = __uint_as_float(ww[k] << 16);
-            x[2 * k + 1] = __uint_as_float(ww[k] & 0xffff0000u);
+            x[i][2 * k] = __uint_as_float(ww[k] << 16);
+            x[i][2 * k + 1] = __uint_as_float(ww[k] & 0xffff0000u);
           }
         } else {
-          x[0] = __uint_as_float(w.x);
-          x[1] = __uint_as_float(w.y);
-          x[2] = __uint_as_float(w.z);
-          x[3] = __uint_as_float(w.w);
+          x[i][0] = __uint_as_float(w.x);
+          x[i][1] = __uint_as_float(w.y);
+          x[i][2] = __uint_as_float(w.z);
+          x[i][3] = __uint_as_float(w.w);
         }
+        float cm = x[i][0];
+#pragma unroll
+        for (int j = 1; j < NV; ++j) cm = fmaxf(cm, x[i][j]);
+        tmax = fmaxf(tmax, cm);
+        const float cm2 = cm * LOG2E;
+        if (cm2 > m2) {
+          ssum *= ex2(m2 - cm2);
+          m2 = cm2;
+        }
+#pragma unroll
+        for (int j = 0; j < NV; ++j) ssum += ex2(fmaf(x[i][j], LOG2E, -m2));
       } else {
 #pragma unroll
-        for (int j = 0; j < NV; ++j) x[j] = 0.f;
+        for (int j = 0; j < NV; ++j) x[i][j] = -INFINITY;
       }
-      const int id0 = seg_elem0 + static_cast<int>((off + c * 16) / ES);
-      consume<NV>(x, valid ? NV : 0, id0, m2, ssum, q, tau, lane, K);
     }
-    if (lane == 0 && q.tid != INT_MAX) atomicMax(&s_tau, float_key(q.tv));
+
+    // ---- value threshold: the running K-th entry; in the first stage also the K-th
+    // largest per-thread maximum (K distinct threads hold an element at least that large,
+    // so the row's K-th largest value is not below it).
+    float L0 = -INFINITY;
+    if (st == 0) {
+      float v = warp_sort_desc(tmax, lane);
+      sq_v[warp][lane] = v;
+      __syncthreads();
+      for (int half = K1_WARPS / 2; half >= 1; half >>= 1) {
+        if (warp < half) {
+          float a = sq_v[warp][lane];
+          int ai = 0;
+          bitonic_merge(a, ai, sq_v[warp + half][lane], 0, lane);
+          __syncwarp();
+          sq_v[warp][lane] = a;
+        }
+        __syncthreads();
+      }
+      if (tid == 0) s_L0 = sq_v[0][K - 1];
+      __syncthreads();
+      L0 = s_L0;
+    }
+    // written by warp 0 before the previous barrier (head/tail, or the last stage)
+    const float tv = s_tau_v;
+    const int ti = s_tau_i;
+    const float thr = fmaxf(tv, L0);
+
+    // ---- append the rare elements that can still enter the top-K
+    if (tmax >= thr) {
+#pragma unroll
+      for (int i = 0; i < K1_CPT; ++i)
+#pragma unroll
+        for (int j = 0; j < NV; ++j)
+          if (j < n[i] && x[i][j] >= thr && better(x[i][j], id0[i] + j, tv, ti)) {
+            const int idx = atomicAdd(&s_cnt, 1);
+            if (idx < K1_CAP) {
+              s_buf_v[idx] = x[i][j];
+              s_buf_i[idx] = id0[i] + j;
+            }
+          }
+    }
+    __syncthreads();
+    const int cnt = s_cnt;
+    if (cnt > K1_CAP) {
+      // Too many ties for the buffer: exact per-warp queues over this stage's elements
+      // (still in registers), merged into the running queue.
+      WarpQueue q;
+      q.init();
+#pragma unroll
+      for (int i = 0; i < K1_CPT; ++i) {
+        float mm = M2_INIT, sd = 0.f;  // lse already accounted; scratch accumulators
+        consume<NV>(x[i], n[i], id0[i], mm, sd, q, -INFINITY, lane, K);
+      }
+      sq_v[warp][lane] = q.qv;
+      sq_i[warp][lane] = q.qid;
+      __syncthreads();
+      for (int half = K1_WARPS / 2; half >= 1; half >>= 1) {
+        if (warp < half) {
+          float a = sq_v[warp][lane];
+          int ai = sq_i[warp][lane];
+          bitonic_merge(a, ai, sq_v[warp + half][lane], sq_i[warp + half][lane], lane);
+          __syncwarp();
+          sq_v[warp][lane] = a;
+          sq_i[warp][lane] = ai;
+        }
+        __syncthreads();
+      }
+      if (warp == 0) {
+        float a = run.qv;
+        int ai = run.qid;
+        bitonic_merge(a, ai, sq_v[0][lane], sq_i[0][lane], lane);
+        run.qv = a;
+        run.qid = ai;
+        run.tv = __shfl_sync(FULL_MASK, a, K - 1);
+        run.tid = __shfl_sync(FULL_MASK, ai, K - 1);
+      }
+    } else if (cnt > 0 && warp == 0) {
+      for (int c0 = 0; c0 < cnt; c0 += 32) {
+        float v = -INFINITY;
+        int vi = INT_MAX;
+        if (c0 + lane < cnt) {
+          v = s_buf_v[c0 + lane];
+          vi = s_buf_i[c0 + lane];
+        }
+        unsigned m = __ballot_sync(FULL_MASK, better(v, vi, run.tv, run.tid));
+        while (m) {
+          const int src = __ffs(m) - 1;
+          m &= m - 1;
+          const float ev = __shfl_sync(FULL_MASK, v, src);
+          const int ei = __shfl_sync(FULL_MASK, vi, src);
+          if (better(ev, ei, run.tv, run.tid)) run.insert(ev, ei, lane, K);
+        }
+      }
+    }
+    if (tid == 0) {
+      s_tau_v = run.tv;
+      s_tau_i = run.tid;
+      s_cnt = 0;
+    }
     __syncthreads();
     if (s_abort) {
       ok = false;
@@ -313,35 +446,22 @@ __global__ void __launch_bounds__(K1_THREADS, 2) logit_pass_kernel(const K1Param
     return;
   }
 
-  // ---- CTA merge: lse over threads, top-K over warps ----
+  // ---- CTA log-sum-exp reduction; the running queue is the CTA's top-K
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) {
     const float om = __shfl_xor_sync(FULL_MASK, m2, o);
     const float os = __shfl_xor_sync(FULL_MASK, ssum, o);
     lse_merge(m2, ssum, om, os);
   }
-  sq_v[warp][lane] = q.qv;
-  sq_i[warp][lane] = q.qid;
   if (lane == 0) {
     s_m2[warp] = m2;
     s_s[warp] = ssum;
   }
   __syncthreads();
-  for (int half = K1_WARPS / 2; half >= 1; half >>= 1) {
-    if (warp < half) {
-      float v = sq_v[warp][lane];
-      int id = sq_i[warp][lane];
-      bitonic_merge(v, id, sq_v[warp + half][lane], sq_i[warp + half][lane], lane);
-      __syncwarp();
-      sq_v[warp][lane] = v;
-      sq_i[warp][lane] = id;
-    }
-    __syncthreads();
-  }
   if (warp != 0) return;
 
-  float v = sq_v[0][lane];
-  int id = sq_i[0][lane];
+  float v = run.qv;
+  int id = run.qid;
   float M = lane < K1_WARPS ? s_m2[lane] : M2_INIT;
   float S = lane < K1_WARPS ? s_s[lane] : 0.f;
 #pragma unroll

@@ -61,7 +61,7 @@ typedef struct {
 } lilicorr_dims;
 
 /* One named head tensor in host memory.  Weights are bf16 bit patterns (dtype must be
- * LILICORR_BF16), row-major, shapes as listed in DESIGN notes and checked exactly:
+ * LILICORR_BF16), row-major, with exactly these shapes (H hidden, F ffn, E d_e):
  *   embed [V,H]  slot_table [B_max-1,H]  rank_table [K_max,H]
  *   conf.w1 [H,5] conf.b1 [H] conf.w2 [H,H] conf.b2 [H]
  *   layers.{l}.norm1 [H] .in_proj_w [3H,H] .in_proj_b [3H] .out_proj_w [H,H]
@@ -179,12 +179,14 @@ uint64_t lilicorr_launch_count(void);
  * device): 0 = no error; otherwise a bit set per failed wait site. */
 lilicorr_status lilicorr_device_error(uint32_t* code);
 
-/* Per-stage timing.  When enabled, lilicorr_rerank records CUDA events on its stream
- * around each stage; lilicorr_stage_times() synchronises on them and adds the elapsed
- * milliseconds per stage into ms[0..n) (stage order: see lilicorr_stage_name), returns
- * the number of stages, and resets the accumulators. */
+/* Per-kernel timing.  When enabled, lilicorr_rerank records a CUDA event on its stream
+ * after each of its launches.  lilicorr_stage_times() synchronises on the recorded
+ * events and, for every timing slot i < n (names: lilicorr_stage_name(i)), writes the
+ * elapsed milliseconds summed over all calls since the last read into ms[i] and the
+ * number of launches into launches[i] (either array may be NULL); *calls gets the
+ * number of calls.  It returns the number of slots and resets the accumulators. */
 void lilicorr_stage_timing(int enable);
-int32_t lilicorr_stage_times(double* ms, int32_t n, int64_t* calls);
+int32_t lilicorr_stage_times(double* ms, int64_t* launches, int32_t n, int64_t* calls);
 const char* lilicorr_stage_name(int32_t i);
 
 #ifdef __cplusplus
