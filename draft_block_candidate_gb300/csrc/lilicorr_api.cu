@@ -203,6 +203,7 @@ lilicorr_status check_call(const lilicorr_weights* w, lilicorr_dtype ldtype, int
   if (batch < 1 || B < 2 || B > w->d.B_max || V != w->d.V) return LILICORR_ERR_INVALID_ARG;
   if (K < 1 || K > w->d.K_max || K > V) return LILICORR_ERR_INVALID_ARG;
   if (batch * (B - 1) * int64_t(K) > (int64_t(1) << 31) - 1) return LILICORR_ERR_INVALID_ARG;
+  if (V * (ldtype == LILICORR_BF16 ? 2 : 4) > (int64_t(1) << 31) - 64) return LILICORR_ERR_INVALID_ARG;
   return LILICORR_OK;
 }
 
@@ -406,6 +407,7 @@ lilicorr_status lilicorr_topk_lse(const void* logits, lilicorr_dtype ldtype, int
   if (ldtype != LILICORR_F32 && ldtype != LILICORR_BF16) return LILICORR_ERR_INVALID_ARG;
   const int es = ldtype == LILICORR_BF16 ? 2 : 4;
   if (reinterpret_cast<uintptr_t>(logits) % es) return LILICORR_ERR_INVALID_ARG;
+  if (V * es > (int64_t(1) << 31) - 64) return LILICORR_ERR_INVALID_ARG;  // row < 2 GiB
   const size_t need = k1_workspace_bytes(batch, B, V, es);
   if (need && (!workspace || workspace_bytes < need ||
                reinterpret_cast<uintptr_t>(workspace) % 256))

@@ -11,13 +11,15 @@
 //
 // GB300 design.  The pass is HBM-bound (one streaming read of batch*(B-1)*V elements), so
 // each CTA streams a contiguous segment of one row through shared memory with 1-D bulk
-// copies (cp.async.bulk, 16 KB stages, 3 in flight, L2 evict-first) and every thread
+// copies (cp.async.bulk, 16 KB stages, 3 in flight, 3 CTAs per SM) and every thread
 // consumes 16-byte chunks:
 //   * online log-sum-exp in base 2: per chunk one max, one FFMA + ex2 per element;
-//   * top-K: each warp keeps a sorted queue of 32 (value, id) pairs, one per lane; a
-//     chunk is only inspected when its maximum reaches the warp's K-th value (or a
-//     CTA-wide lower bound shared through shared memory), so after warm-up almost all
-//     chunks cost one compare; queues are merged with a 32-wide bitonic network.
+//   * top-K: warp 0 keeps the running top-32 (value, id) pairs sorted across its lanes.
+//     Every thread compares its elements with the running K-th entry (floored in the
+//     first stage by the K-th largest per-thread maximum, a valid lower bound), so after
+//     warm-up almost every element costs one compare; the rare survivors go to a shared
+//     buffer that warp 0 folds in 32 at a time (warp bitonic sort + bitonic merge)
+//     during the next stage.
 // Rows are split into P segments when there are too few rows to fill 152 SMs; the last
 // CTA of a row (atomic counter, no waiting) merges the P partial results.
 #include <float.h>
@@ -87,22 +89,6 @@ struct WarpQueue {
     tv = -INFINITY;
     tid = INT_MAX;
   }
-  // Warp-uniform call: insert (v, id), known to rank before the K-th entry.
-  __device__ void insert(float v, int id, int lane, int K) {
-    const unsigned bm = __ballot_sync(FULL_MASK, better(qv, qid, v, id));
-    const int pos = __popc(bm);
-    const float uv = __shfl_up_sync(FULL_MASK, qv, 1);
-    const int uid = __shfl_up_sync(FULL_MASK, qid, 1);
-    if (lane > pos) {
-      qv = uv;
-      qid = uid;
-    } else if (lane == pos) {
-      qv = v;
-      qid = id;
-    }
-    tv = __shfl_sync(FULL_MASK, qv, K - 1);
-    tid = __shfl_sync(FULL_MASK, qid, K - 1);
-  }
 };
 
 // Merge sorted list (bv, bi) (one entry per lane, descending) into (v, id): afterwards
@@ -133,40 +119,6 @@ __device__ __forceinline__ void lse_merge(float& m2, float& s, float om2, float 
   m2 = M;
 }
 
-// Consume one chunk of n (0..NV) values held by this lane, ids id0..id0+n-1.
-// Warp-uniform call (lanes with n == 0 take part in the ballots).
-template <int NV>
-__device__ __forceinline__ void consume(const float (&x)[NV], int n, int id0, float& m2,
-                                        float& s, WarpQueue& q, float tau, int lane, int K) {
-  float cm = -INFINITY;
-#pragma unroll
-  for (int j = 0; j < NV; ++j)
-    if (j < n) cm = fmaxf(cm, x[j]);
-  if (n > 0) {
-    const float cm2 = cm * LOG2E;
-    if (cm2 > m2) {
-      s *= ex2(m2 - cm2);
-      m2 = cm2;
-    }
-#pragma unroll
-    for (int j = 0; j < NV; ++j)
-      if (j < n) s += ex2(fmaf(x[j], LOG2E, -m2));
-  }
-  const float thr = fmaxf(q.tv, tau);
-  unsigned mask = __ballot_sync(FULL_MASK, n > 0 && cm >= thr);
-  while (mask) {
-    const int src = __ffs(mask) - 1;
-    mask &= mask - 1;
-    const int sid0 = __shfl_sync(FULL_MASK, id0, src);
-    const int sn = __shfl_sync(FULL_MASK, n, src);
-#pragma unroll
-    for (int j = 0; j < NV; ++j) {
-      const float v = __shfl_sync(FULL_MASK, x[j], src);
-      if (j < sn && better(v, sid0 + j, q.tv, q.tid)) q.insert(v, sid0 + j, lane, K);
-    }
-  }
-}
-
 template <typename T>
 __device__ __forceinline__ float load_elem(const char* p);
 template <>
@@ -192,10 +144,105 @@ __device__ __forceinline__ float warp_sort_desc(float v, int lane) {
   return v;
 }
 
-constexpr int K1_CAP = 1024;  // candidate buffer entries per CTA
+constexpr int K1_CAP = 256;  // candidate buffer entries per CTA and stage parity
+
+// The running K-th entry (value, id) shared as one 64-bit word, so a reader never sees
+// the value of one update with the id of another.
+__device__ __forceinline__ unsigned long long pack_tau(float v, int id) {
+  return (static_cast<unsigned long long>(__float_as_uint(v)) << 32) | static_cast<uint32_t>(id);
+}
+__device__ __forceinline__ void unpack_tau(unsigned long long w, float& v, int& id) {
+  v = __uint_as_float(static_cast<uint32_t>(w >> 32));
+  id = static_cast<int>(static_cast<uint32_t>(w));
+}
+
+// Sort one (value, id) pair per lane across the warp into (value desc, id asc) order
+// (bitonic network, 15 compare-exchange steps).
+__device__ __forceinline__ void warp_sort_pairs(float& v, int& id, int lane) {
+#pragma unroll
+  for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      const float ov = __shfl_xor_sync(FULL_MASK, v, j);
+      const int oi = __shfl_xor_sync(FULL_MASK, id, j);
+      const bool ob = better(ov, oi, v, id);
+      const bool keep_better = ((lane & j) == 0) == ((lane & k) == 0);
+      if (keep_better ? ob : !ob) {
+        v = ov;
+        id = oi;
+      }
+    }
+  }
+}
+
+// Warp-uniform: fold one candidate per lane (sentinel -inf / INT_MAX for none) into the
+// sorted 32-entry queue q, 32 candidates at a time: sort them, bitonic-merge, keep the
+// best 32.  Skipped when no lane beats the queue's K-th entry.
+__device__ __forceinline__ void queue_absorb(WarpQueue& q, float v, int id, int lane, int K) {
+  if (!__any_sync(FULL_MASK, better(v, id, q.tv, q.tid))) return;
+  warp_sort_pairs(v, id, lane);
+  bitonic_merge(q.qv, q.qid, v, id, lane);
+  q.tv = __shfl_sync(FULL_MASK, q.qv, K - 1);
+  q.tid = __shfl_sync(FULL_MASK, q.qid, K - 1);
+}
+
+// Warp-uniform: fold the buffered candidates into the running queue, publish its K-th
+// entry, empty the buffer.
+__device__ __forceinline__ void merge_buffer(WarpQueue& run, const float* bv, const int* bi,
+                                             int* cnt_p, volatile unsigned long long* tau,
+                                             int lane, int K) {
+  const int cnt = min(*cnt_p, K1_CAP);
+  for (int c0 = 0; c0 < cnt; c0 += 32) {
+    float v = -INFINITY;
+    int vi = INT_MAX;
+    if (c0 + lane < cnt) {
+      v = bv[c0 + lane];
+      vi = bi[c0 + lane];
+    }
+    queue_absorb(run, v, vi, lane, K);
+  }
+  __syncwarp();
+  if (lane == 0) {
+    *tau = pack_tau(run.tv, run.tid);
+    *cnt_p = 0;
+  }
+}
+
+// Unpack one 16-byte chunk (8 bf16 or 4 f32) into floats.
+template <int NV>
+__device__ __forceinline__ void unpack16(const uint4 w, float (&x)[NV]) {
+  if constexpr (NV == 8) {
+    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      x[2 * k] = __uint_as_float(ww[k] << 16);
+      x[2 * k + 1] = __uint_as_float(ww[k] & 0xffff0000u);
+    }
+  } else {
+    x[0] = __uint_as_float(w.x);
+    x[1] = __uint_as_float(w.y);
+    x[2] = __uint_as_float(w.z);
+    x[3] = __uint_as_float(w.w);
+  }
+}
+
+// Append this chunk's elements that can still enter the top-K to the stage buffer.
+template <int NV>
+__device__ __forceinline__ void append_chunk(const float (&x)[NV], int id0, float thr, float tv,
+                                             int ti, float* bv, int* bi, int* cnt) {
+#pragma unroll
+  for (int j = 0; j < NV; ++j)
+    if (x[j] >= thr && better(x[j], id0 + j, tv, ti)) {
+      const int idx = atomicAdd(cnt, 1);
+      if (idx < K1_CAP) {
+        bv[idx] = x[j];
+        bi[idx] = id0 + j;
+      }
+    }
+}
 
 template <typename T>
-__global__ void __launch_bounds__(K1_THREADS, 2) logit_pass_kernel(const K1Params p) {
+__global__ void __launch_bounds__(K1_THREADS, 3) logit_pass_kernel(const K1Params p) {
   constexpr int ES = sizeof(T);
   constexpr int NV = 16 / ES;
   extern __shared__ __align__(128) uint8_t k1_dyn_smem[];
@@ -203,11 +250,13 @@ __global__ void __launch_bounds__(K1_THREADS, 2) logit_pass_kernel(const K1Param
   __shared__ __align__(8) uint64_t full_bar[K1_NSTAGES];
   __shared__ float sq_v[K1_WARPS][KQ];
   __shared__ int sq_i[K1_WARPS][KQ];
-  __shared__ float s_buf_v[K1_CAP];
-  __shared__ int s_buf_i[K1_CAP];
+  __shared__ float s_buf_v[2][K1_CAP];
+  __shared__ int s_buf_i[2][K1_CAP];
   __shared__ float s_m2[K1_WARPS], s_s[K1_WARPS];
-  __shared__ float s_tau_v, s_L0;
-  __shared__ int s_tau_i, s_cnt, s_abort;
+  __shared__ float s_L0;
+  __shared__ int s_abort;
+  __shared__ int s_cnt[2];
+  __shared__ volatile unsigned long long s_tau;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int K = p.K;
@@ -227,117 +276,117 @@ __global__ void __launch_bounds__(K1_THREADS, 2) logit_pass_kernel(const K1Param
   const int64_t seg_lo = i64min(body_end, body_start + seg * p.seg_bytes);
   const int64_t seg_hi = i64min(body_end, seg_lo + p.seg_bytes);
   const int nstages = static_cast<int>((seg_hi - seg_lo + K1_STAGE_BYTES - 1) / K1_STAGE_BYTES);
+  const int seg_bytes = static_cast<int>(seg_hi - seg_lo);
+  const int seg_elem0 = static_cast<int>((seg_lo - row_start) / ES);  // id of first body elem
 
   if (tid == 0) {
     for (int i = 0; i < K1_NSTAGES; ++i) mbar_init(&full_bar[i], 1);
     fence_mbar_init();
-    s_cnt = 0;
+    s_cnt[0] = s_cnt[1] = 0;
     s_abort = 0;
+    s_tau = pack_tau(-INFINITY, INT_MAX);
   }
   __syncthreads();
 
-  const uint64_t pol = policy_evict_first();
-  auto issue = [&](int st) {
-    const int64_t off = seg_lo + int64_t(st) * K1_STAGE_BYTES;
-    const uint32_t bytes = static_cast<uint32_t>(i64min(K1_STAGE_BYTES, seg_hi - off));
-    uint64_t* bar = &full_bar[st % K1_NSTAGES];
-    mbar_arrive_expect_tx(bar, bytes);
-    bulk_g2s(stage[st % K1_NSTAGES], p.logits + off, bytes, bar, pol);
-  };
   if (tid == 0)
-    for (int st = 0; st < min(K1_NSTAGES - 1, nstages); ++st) issue(st);
+    for (int st = 0; st < min(K1_NSTAGES - 1, nstages); ++st) {
+      const int off = st * K1_STAGE_BYTES;
+      const uint32_t bytes = static_cast<uint32_t>(min(K1_STAGE_BYTES, seg_bytes - off));
+      mbar_arrive_expect_tx(&full_bar[st], bytes);
+      bulk_g2s(stage[st], p.logits + seg_lo + off, bytes, &full_bar[st]);
+    }
 
   float m2 = M2_INIT, ssum = 0.f;
-  // Warp 0 owns the running top-K of everything consumed so far (one entry per lane,
-  // sorted); the other warps see its K-th entry through s_tau_v / s_tau_i.
+  // Warp 0 owns the running top-32 of everything consumed so far (one entry per lane,
+  // sorted); the other warps see its K-th entry through s_tau.
   WarpQueue run;
   run.init();
 
   // Unaligned head (segment 0) and tail (last segment) elements: plain loads by warp 0,
-  // straight into the running queue.
+  // one element per lane, straight into the running queue.
   if (warp == 0) {
     const int64_t row_elem0 = row_start / ES;
-    float x[NV];
-#pragma unroll
-    for (int j = 1; j < NV; ++j) x[j] = 0.f;
-    if (seg == 0) {
-      const int nh = static_cast<int>((body_start - row_start) / ES);
-      const bool v = lane < nh;
-      x[0] = v ? load_elem<T>(p.logits + row_start + int64_t(lane) * ES) : 0.f;
-      consume<NV>(x, v ? 1 : 0, lane, m2, ssum, run, -INFINITY, lane, K);
+    for (int part = 0; part < 2; ++part) {
+      int64_t first = 0;
+      int cnt = 0;
+      if (part == 0 && seg == 0) {
+        first = row_start;
+        cnt = static_cast<int>((body_start - row_start) / ES);
+      } else if (part == 1 && seg == p.P - 1 && body_end < row_end) {
+        first = body_end;
+        cnt = static_cast<int>((row_end - body_end) / ES);
+      }
+      if (cnt == 0) continue;  // warp-uniform
+      const bool has = lane < cnt;
+      const float xv = has ? load_elem<T>(p.logits + first + int64_t(lane) * ES) : -INFINITY;
+      if (has) {
+        const float c2 = xv * LOG2E;
+        if (c2 > m2) {
+          ssum *= ex2(m2 - c2);
+          m2 = c2;
+        }
+        ssum += ex2(fmaf(xv, LOG2E, -m2));
+      }
+      queue_absorb(run, xv, has ? static_cast<int>(first / ES - row_elem0) + lane : INT_MAX, lane,
+                   K);
     }
-    if (seg == p.P - 1 && body_end < row_end) {
-      const int nt = static_cast<int>((row_end - body_end) / ES);
-      const bool v = lane < nt;
-      x[0] = v ? load_elem<T>(p.logits + body_end + int64_t(lane) * ES) : 0.f;
-      consume<NV>(x, v ? 1 : 0, static_cast<int>((body_end / ES - row_elem0) + lane), m2, ssum,
-                  run, -INFINITY, lane, K);
-    }
-    if (lane == 0) {
-      s_tau_v = run.tv;
-      s_tau_i = run.tid;
-    }
+    if (lane == 0) s_tau = pack_tau(run.tv, run.tid);
   }
 
-  const int seg_elem0 = static_cast<int>((seg_lo - row_start) / ES);  // id of first body elem
+  float L0 = -INFINITY;  // lower bound of the segment's K-th largest value (from stage 0)
   bool ok = true;
   for (int st = 0; st < nstages; ++st) {
-    if (tid == 0 && st + K1_NSTAGES - 1 < nstages) issue(st + K1_NSTAGES - 1);
-    if (!mbar_wait_bounded(&full_bar[st % K1_NSTAGES], (st / K1_NSTAGES) & 1, &g_err_k1,
-                           ERR_K1_FULL_WAIT))
+    const int slot = st % K1_NSTAGES;
+    if (tid == 0 && st + K1_NSTAGES - 1 < nstages) {
+      const int nx = st + K1_NSTAGES - 1, ns = nx % K1_NSTAGES;
+      const int off = nx * K1_STAGE_BYTES;
+      const uint32_t bytes = static_cast<uint32_t>(min(K1_STAGE_BYTES, seg_bytes - off));
+      mbar_arrive_expect_tx(&full_bar[ns], bytes);
+      bulk_g2s(stage[ns], p.logits + seg_lo + off, bytes, &full_bar[ns]);
+    }
+    if (!mbar_wait_bounded(&full_bar[slot], (st / K1_NSTAGES) & 1, &g_err_k1, ERR_K1_FULL_WAIT))
       s_abort = 1;
-    const int64_t off = int64_t(st) * K1_STAGE_BYTES;
-    const int nbytes = static_cast<int>(i64min(K1_STAGE_BYTES, (seg_hi - seg_lo) - off));
-    const uint8_t* sbuf = stage[st % K1_NSTAGES];
+    const int soff = st * K1_STAGE_BYTES;
+    const int nbytes = min(K1_STAGE_BYTES, seg_bytes - soff);
+    const uint8_t* sbuf = stage[slot];
+    const int bsel = st & 1;
+    float* bv = s_buf_v[bsel];
+    int* bi = s_buf_i[bsel];
+    // the running K-th entry; warp 0 may raise it concurrently, either value is valid
+    // (stage 0 re-reads it below, after barriers that order warp 0's head/tail update)
+    float tv;
+    int ti;
+    unpack_tau(s_tau, tv, ti);
+    const float thr = fmaxf(tv, L0);
 
-    // ---- load this thread's chunks and fold them into the log-sum-exp
-    float x[K1_CPT][NV];
-    int n[K1_CPT], id0[K1_CPT];
+    // ---- one 16-byte chunk at a time: log-sum-exp, then the (rare) candidate check
     float tmax = -INFINITY;
 #pragma unroll
     for (int i = 0; i < K1_CPT; ++i) {
       const int c = tid + i * K1_THREADS;
-      n[i] = c * 16 < nbytes ? NV : 0;
-      id0[i] = seg_elem0 + static_cast<int>((off + c * 16) / ES);
-      if (n[i]) {
-        const uint4 w = *reinterpret_cast<const uint4*>(sbuf + c * 16);
-        if constexpr (ES == 2) {
-          const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+      if (c * 16 < nbytes) {
+        float x[NV];
+        unpack16<NV>(*reinterpret_cast<const uint4*>(sbuf + c * 16), x);
+        float cm = x[0];
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            x[i][2 * k] = __uint_as_float(ww[k] << 16);
-            x[i][2 * k + 1] = __uint_as_float(ww[k] & 0xffff0000u);
-          }
-        } else {
-          x[i][0] = __uint_as_float(w.x);
-          x[i][1] = __uint_as_float(w.y);
-          x[i][2] = __uint_as_float(w.z);
-          x[i][3] = __uint_as_float(w.w);
-        }
-        float cm = x[i][0];
-#pragma unroll
-        for (int j = 1; j < NV; ++j) cm = fmaxf(cm, x[i][j]);
-        tmax = fmaxf(tmax, cm);
+        for (int j = 1; j < NV; ++j) cm = fmaxf(cm, x[j]);
         const float cm2 = cm * LOG2E;
         if (cm2 > m2) {
           ssum *= ex2(m2 - cm2);
           m2 = cm2;
         }
 #pragma unroll
-        for (int j = 0; j < NV; ++j) ssum += ex2(fmaf(x[i][j], LOG2E, -m2));
-      } else {
-#pragma unroll
-        for (int j = 0; j < NV; ++j) x[i][j] = -INFINITY;
+        for (int j = 0; j < NV; ++j) ssum += ex2(fmaf(x[j], LOG2E, -m2));
+        tmax = fmaxf(tmax, cm);
+        if (st > 0 && cm >= thr)
+          append_chunk<NV>(x, seg_elem0 + (soff + c * 16) / ES, thr, tv, ti, bv, bi, &s_cnt[bsel]);
       }
     }
 
-    // ---- value threshold: the running K-th entry; in the first stage also the K-th
-    // largest per-thread maximum (K distinct threads hold an element at least that large,
-    // so the row's K-th largest value is not below it).
-    float L0 = -INFINITY;
+    // ---- stage 0: floor L0 = the K-th largest per-thread maximum (K distinct threads
+    // hold an element at least that large), then this stage's candidates.
     if (st == 0) {
-      float v = warp_sort_desc(tmax, lane);
-      sq_v[warp][lane] = v;
+      sq_v[warp][lane] = warp_sort_desc(tmax, lane);
       __syncthreads();
       for (int half = K1_WARPS / 2; half >= 1; half >>= 1) {
         if (warp < half) {
@@ -352,37 +401,43 @@ __global__ void __launch_bounds__(K1_THREADS, 2) logit_pass_kernel(const K1Param
       if (tid == 0) s_L0 = sq_v[0][K - 1];
       __syncthreads();
       L0 = s_L0;
-    }
-    // written by warp 0 before the previous barrier (head/tail, or the last stage)
-    const float tv = s_tau_v;
-    const int ti = s_tau_i;
-    const float thr = fmaxf(tv, L0);
-
-    // ---- append the rare elements that can still enter the top-K
-    if (tmax >= thr) {
+      unpack_tau(s_tau, tv, ti);
+      const float thr0 = fmaxf(tv, L0);
+      if (tmax >= thr0) {
 #pragma unroll
-      for (int i = 0; i < K1_CPT; ++i)
-#pragma unroll
-        for (int j = 0; j < NV; ++j)
-          if (j < n[i] && x[i][j] >= thr && better(x[i][j], id0[i] + j, tv, ti)) {
-            const int idx = atomicAdd(&s_cnt, 1);
-            if (idx < K1_CAP) {
-              s_buf_v[idx] = x[i][j];
-              s_buf_i[idx] = id0[i] + j;
-            }
+        for (int i = 0; i < K1_CPT; ++i) {
+          const int c = tid + i * K1_THREADS;
+          if (c * 16 < nbytes) {
+            float x[NV];
+            unpack16<NV>(*reinterpret_cast<const uint4*>(sbuf + c * 16), x);
+            append_chunk<NV>(x, seg_elem0 + (soff + c * 16) / ES, thr0, tv, ti, bv, bi,
+                             &s_cnt[bsel]);
           }
+        }
+      }
     }
+
+    // ---- warp 0 folds the previous stage's buffer into the running queue while the
+    // other warps go on (a stale threshold is still a valid lower bound)
+    if (warp == 0 && st > 0)
+      merge_buffer(run, s_buf_v[bsel ^ 1], s_buf_i[bsel ^ 1], &s_cnt[bsel ^ 1], &s_tau, lane, K);
     __syncthreads();
-    const int cnt = s_cnt;
-    if (cnt > K1_CAP) {
-      // Too many ties for the buffer: exact per-warp queues over this stage's elements
-      // (still in registers), merged into the running queue.
+    if (s_cnt[bsel] > K1_CAP) {
+      // Too many ties for the buffer: exact per-warp queues over this stage's elements,
+      // re-read from shared memory (the slot is not refilled before the next iteration),
+      // merged into the running queue; the buffer is dropped.
       WarpQueue q;
       q.init();
 #pragma unroll
       for (int i = 0; i < K1_CPT; ++i) {
-        float mm = M2_INIT, sd = 0.f;  // lse already accounted; scratch accumulators
-        consume<NV>(x[i], n[i], id0[i], mm, sd, q, -INFINITY, lane, K);
+        const int c = tid + i * K1_THREADS;
+        const bool has = c * 16 < nbytes;
+        float x[NV];
+        if (has) unpack16<NV>(*reinterpret_cast<const uint4*>(sbuf + c * 16), x);
+        const int id0 = seg_elem0 + (soff + c * 16) / ES;
+#pragma unroll
+        for (int j = 0; j < NV; ++j)
+          queue_absorb(q, has ? x[j] : -INFINITY, has ? id0 + j : INT_MAX, lane, K);
       }
       sq_v[warp][lane] = q.qv;
       sq_i[warp][lane] = q.qid;
@@ -399,43 +454,24 @@ __global__ void __launch_bounds__(K1_THREADS, 2) logit_pass_kernel(const K1Param
         __syncthreads();
       }
       if (warp == 0) {
-        float a = run.qv;
-        int ai = run.qid;
-        bitonic_merge(a, ai, sq_v[0][lane], sq_i[0][lane], lane);
-        run.qv = a;
-        run.qid = ai;
-        run.tv = __shfl_sync(FULL_MASK, a, K - 1);
-        run.tid = __shfl_sync(FULL_MASK, ai, K - 1);
-      }
-    } else if (cnt > 0 && warp == 0) {
-      for (int c0 = 0; c0 < cnt; c0 += 32) {
-        float v = -INFINITY;
-        int vi = INT_MAX;
-        if (c0 + lane < cnt) {
-          v = s_buf_v[c0 + lane];
-          vi = s_buf_i[c0 + lane];
-        }
-        unsigned m = __ballot_sync(FULL_MASK, better(v, vi, run.tv, run.tid));
-        while (m) {
-          const int src = __ffs(m) - 1;
-          m &= m - 1;
-          const float ev = __shfl_sync(FULL_MASK, v, src);
-          const int ei = __shfl_sync(FULL_MASK, vi, src);
-          if (better(ev, ei, run.tv, run.tid)) run.insert(ev, ei, lane, K);
+        bitonic_merge(run.qv, run.qid, sq_v[0][lane], sq_i[0][lane], lane);
+        run.tv = __shfl_sync(FULL_MASK, run.qv, K - 1);
+        run.tid = __shfl_sync(FULL_MASK, run.qid, K - 1);
+        if (lane == 0) {
+          s_tau = pack_tau(run.tv, run.tid);
+          s_cnt[bsel] = 0;
         }
       }
+      __syncthreads();
     }
-    if (tid == 0) {
-      s_tau_v = run.tv;
-      s_tau_i = run.tid;
-      s_cnt = 0;
-    }
-    __syncthreads();
     if (s_abort) {
       ok = false;
       break;
     }
   }
+  if (ok && warp == 0 && nstages > 0)
+    merge_buffer(run, s_buf_v[(nstages - 1) & 1], s_buf_i[(nstages - 1) & 1],
+                 &s_cnt[(nstages - 1) & 1], &s_tau, lane, K);
   if (!ok) {
     // Give copies still in flight a bounded chance to land before the CTA exits.
     if (tid == 0)

@@ -150,7 +150,8 @@ lilicorr_status lilicorr_rerank_host(const lilicorr_weights* w, const void* logi
  * drafted slot s = 1..B-1 it reads row logits[b,s,:] once and writes
  *   cand_id[b,s-1,:K] int32, cand_logit[b,s-1,:K] f32 (logit desc, token id asc) and
  *   lse[b,s-1] = log sum_v exp(logits[b,s,v]) (f32, natural log).
- * 1 <= K <= min(32, V).  Workspace: lilicorr_topk_lse_workspace_bytes (may be 0). */
+ * 1 <= K <= min(32, V); one row is under 2 GiB.  Workspace: lilicorr_topk_lse_workspace_bytes
+ * (may be 0). */
 size_t lilicorr_topk_lse_workspace_bytes(int64_t batch, int32_t B, int64_t V, int32_t K,
                                          lilicorr_dtype ldtype);
 lilicorr_status lilicorr_topk_lse(const void* logits, lilicorr_dtype ldtype, int64_t batch,

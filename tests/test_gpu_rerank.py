@@ -139,7 +139,8 @@ def test_permuted_vocabulary_commits_same_tokens(lc):
     wl2.weights["embed"] = np.ascontiguousarray(wl.weights["embed"][perm])
     gpu_b = _gpu_run(lc, wl2, taps=False)
     assert np.array_equal(perm[gpu_b["tokens"][:, 1:]], gpu_a["tokens"][:, 1:])
-    assert np.array_equal(gpu_b["path_score"], gpu_a["path_score"])
+    # the log-partition sums the row in a different order: scores agree to rounding
+    assert np.abs(gpu_b["path_score"] - gpu_a["path_score"]).max() <= SCORE_ATOL
 
 
 @pytest.mark.parametrize("name,kw,nblocks", [
