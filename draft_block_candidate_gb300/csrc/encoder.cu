@@ -106,168 +106,6 @@ __global__ void conf_hidden_kernel(const float* __restrict__ cand_logit,
   }
 }
 
-// ------------------------------------------------------------------ GEMM (mma.sync)
-
-constexpr int GM_BM = 128, GM_BN = 128, GM_BK = 64, GM_STAGES = 3, GM_THREADS = 256;
-constexpr int GM_TILE_BYTES = GM_BM * GM_BK * 2;  // 16 KB (A and W tiles are the same size)
-constexpr int GM_SMEM = GM_STAGES * 2 * GM_TILE_BYTES;
-
-template <int EPI>
-__device__ __forceinline__ void gemm_store2(const GemmArgs& g, int64_t m, int n, float v0,
-                                            float v1) {
-  if (m >= g.M || n >= g.N) return;
-  v0 += g.bias[n];
-  v1 += g.bias[n + 1];
-  if constexpr (EPI == EPI_F32) {
-    *reinterpret_cast<float2*>(g.out + m * g.N + n) = make_float2(v0, v1);
-  } else if constexpr (EPI == EPI_RESID) {
-    float2* p = reinterpret_cast<float2*>(g.out + m * g.N + n);
-    float2 x = *p;
-    x.x += v0;
-    x.y += v1;
-    *p = x;
-  } else if constexpr (EPI == EPI_SPLIT || EPI == EPI_SPLIT_SILU) {
-    if constexpr (EPI == EPI_SPLIT_SILU) {
-      v0 = silu(v0);
-      v1 = silu(v1);
-    }
-    __nv_bfloat16 h0, l0, h1, l1;
-    split_bf16(v0, h0, l0);
-    split_bf16(v1, h1, l1);
-    __nv_bfloat16* o = g.out_split + m * 2 * g.N;
-    *reinterpret_cast<__nv_bfloat162*>(o + n) = __halves2bfloat162(h0, h1);
-    *reinterpret_cast<__nv_bfloat162*>(o + g.N + n) = __halves2bfloat162(l0, l1);
-  } else {  // EPI_NODE
-    const int S = (g.B - 1) * g.K;
-    const int64_t b = m / S;
-    const int t = static_cast<int>(m % S);
-    const int slot = t / g.K + 1, k = t % g.K;
-    // ids come from the logit pass and are < V; the clamp keeps a violated precondition
-    // (e.g. NaN logits) from turning into an out-of-bounds gather.
-    int64_t id = g.cand_id[m];
-    id = id < 0 ? 0 : (id >= g.vocab ? g.vocab - 1 : id);
-    const __nv_bfloat162 e = *reinterpret_cast<const __nv_bfloat162*>(g.embed + id * g.N + n);
-    v0 += __bfloat162float(e.x) + g.slot_table[(slot - 1) * g.N + n] + g.rank_table[k * g.N + n];
-    v1 += __bfloat162float(e.y) + g.slot_table[(slot - 1) * g.N + n + 1] +
-          g.rank_table[k * g.N + n + 1];
-    if (g.slot_hidden) {
-      const __nv_bfloat162 hh = *reinterpret_cast<const __nv_bfloat162*>(
-          g.slot_hidden + (b * g.B + slot) * g.N + n);
-      v0 += __bfloat162float(hh.x);
-      v1 += __bfloat162float(hh.y);
-    }
-    *reinterpret_cast<float2*>(g.out + m * g.N + n) = make_float2(v0, v1);
-    if (g.nodes_tap) *reinterpret_cast<float2*>(g.nodes_tap + m * g.N + n) = make_float2(v0, v1);
-  }
-}
-
-template <int EPI>
-__global__ void __launch_bounds__(GM_THREADS) gemm_kernel(const GemmArgs g) {
-  extern __shared__ __align__(128) uint8_t gm_smem[];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int warp_m = warp >> 2, warp_n = warp & 3;  // 2 x 4 warps, 64 x 32 each
-  const int64_t m0 = int64_t(blockIdx.y) * GM_BM;
-  const int n0 = blockIdx.x * GM_BN;
-  const int KT = g.Ka / GM_BK;
-
-  auto a_tile = [&](int s) { return gm_smem + s * 2 * GM_TILE_BYTES; };
-  auto b_tile = [&](int s) { return gm_smem + s * 2 * GM_TILE_BYTES + GM_TILE_BYTES; };
-
-  auto load = [&](int s, int kt) {
-    const int ka = kt * GM_BK;
-    const int kw = ka % g.Kw;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int c = tid + i * GM_THREADS;  // 0..1023
-      const int r = c >> 3, ch = c & 7;
-      const int64_t m = m0 + r;
-      const bool pa = m < g.M;
-      cp_async16(a_tile(s) + swz<8>(r, ch), g.A + (pa ? m : 0) * g.Ka + ka + ch * 8, pa);
-      const int n = n0 + r;
-      const bool pb = n < g.N;
-      cp_async16(b_tile(s) + swz<8>(r, ch), g.W + int64_t(pb ? n : 0) * g.Kw + kw + ch * 8, pb);
-    }
-  };
-
-  float acc[4][4][4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-#pragma unroll
-      for (int k = 0; k < 4; ++k) acc[i][j][k] = 0.f;
-
-#pragma unroll
-  for (int s = 0; s < GM_STAGES - 1; ++s) {
-    if (s < KT) load(s, s);
-    cp_async_commit();
-  }
-
-  for (int kt = 0; kt < KT; ++kt) {
-    cp_async_wait<GM_STAGES - 2>();
-    __syncthreads();
-    if (kt + GM_STAGES - 1 < KT) load((kt + GM_STAGES - 1) % GM_STAGES, kt + GM_STAGES - 1);
-    cp_async_commit();
-    const uint32_t sa = smem_addr(a_tile(kt % GM_STAGES));
-    const uint32_t sb = smem_addr(b_tile(kt % GM_STAGES));
-#pragma unroll
-    for (int kk = 0; kk < GM_BK / 16; ++kk) {
-      uint32_t af[4][4];
-#pragma unroll
-      for (int mt = 0; mt < 4; ++mt) {
-        const int r = warp_m * 64 + mt * 16 + (lane & 15);
-        const int ch = kk * 2 + (lane >> 4);
-        ldsm_x4(af[mt][0], af[mt][1], af[mt][2], af[mt][3], sa + swz<8>(r, ch));
-      }
-      uint32_t bf[4][2];
-#pragma unroll
-      for (int np = 0; np < 2; ++np) {
-        const int r = warp_n * 32 + np * 16 + (lane & 7) + ((lane >> 4) << 3);
-        const int ch = kk * 2 + ((lane >> 3) & 1);
-        ldsm_x4(bf[2 * np][0], bf[2 * np][1], bf[2 * np + 1][0], bf[2 * np + 1][1],
-                sb + swz<8>(r, ch));
-      }
-#pragma unroll
-      for (int mt = 0; mt < 4; ++mt)
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt) mma_bf16(acc[mt][nt], af[mt], bf[nt][0], bf[nt][1]);
-    }
-  }
-  cp_async_wait<0>();
-
-#pragma unroll
-  for (int mt = 0; mt < 4; ++mt)
-#pragma unroll
-    for (int nt = 0; nt < 4; ++nt) {
-      const int64_t m = m0 + warp_m * 64 + mt * 16 + (lane >> 2);
-      const int n = n0 + warp_n * 32 + nt * 8 + (lane & 3) * 2;
-      gemm_store2<EPI>(g, m, n, acc[mt][nt][0], acc[mt][nt][1]);
-      gemm_store2<EPI>(g, m + 8, n, acc[mt][nt][2], acc[mt][nt][3]);
-    }
-}
-
-cudaError_t launch_gemm(int epi, const GemmArgs& g, cudaStream_t stream) {
-  static bool attr = false;
-  if (!attr) {
-    cudaFuncSetAttribute(gemm_kernel<EPI_F32>, cudaFuncAttributeMaxDynamicSharedMemorySize, GM_SMEM);
-    cudaFuncSetAttribute(gemm_kernel<EPI_RESID>, cudaFuncAttributeMaxDynamicSharedMemorySize, GM_SMEM);
-    cudaFuncSetAttribute(gemm_kernel<EPI_SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize, GM_SMEM);
-    cudaFuncSetAttribute(gemm_kernel<EPI_SPLIT_SILU>, cudaFuncAttributeMaxDynamicSharedMemorySize, GM_SMEM);
-    cudaFuncSetAttribute(gemm_kernel<EPI_NODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, GM_SMEM);
-    attr = true;
-  }
-  const dim3 grid((g.N + GM_BN - 1) / GM_BN, static_cast<unsigned>((g.M + GM_BM - 1) / GM_BM));
-  switch (epi) {
-    case EPI_F32: gemm_kernel<EPI_F32><<<grid, GM_THREADS, GM_SMEM, stream>>>(g); break;
-    case EPI_RESID: gemm_kernel<EPI_RESID><<<grid, GM_THREADS, GM_SMEM, stream>>>(g); break;
-    case EPI_SPLIT: gemm_kernel<EPI_SPLIT><<<grid, GM_THREADS, GM_SMEM, stream>>>(g); break;
-    case EPI_SPLIT_SILU: gemm_kernel<EPI_SPLIT_SILU><<<grid, GM_THREADS, GM_SMEM, stream>>>(g); break;
-    default: gemm_kernel<EPI_NODE><<<grid, GM_THREADS, GM_SMEM, stream>>>(g); break;
-  }
-  note_launch();
-  return cudaGetLastError();
-}
-
 // ------------------------------------------------------------------ RMSNorm -> split
 // y = x / sqrt(mean(x^2) + eps) * g, one warp per row.
 __global__ void rmsnorm_split_kernel(const float* __restrict__ X, const float* __restrict__ gain,

@@ -1,0 +1,376 @@
+// Dense contractions of steps a2-a4 on the 5th-generation tensor cores.
+//
+//   C[M, N] = A[M, Ka] . W[N, Kw]^T (+ fused epilogue),   Ka = Kw or 2 Kw
+//
+// A is an activation stored [A_hi | A_lo] (two bf16 halves whose sum carries ~16
+// significant bits) when Ka = 2 Kw; W is an exact bf16 weight whose column index wraps
+// (k mod Kw), so one accumulation gives A_hi W^T + A_lo W^T.
+//
+// One CTA per 128 x 128 output tile, 6 warps:
+//   warp 0      TMA producer (2-D tiled loads, 128-byte swizzle, 3-stage mbarrier ring)
+//               and TMEM owner (allocates / frees the 128-column f32 accumulator)
+//   warp 1      MMA issuer: one elected thread issues tcgen05.mma (kind::f16, bf16 in,
+//               f32 accumulate in TMEM), 4 per 64-wide K block, and tcgen05.commit
+//   warps 2-5   epilogue: tcgen05.ld of its 32 TMEM lanes (= 32 output rows), then the
+//               fused bias / SiLU / residual / hi-lo split / node-sum, stored to global
+// Every mbarrier wait is bounded; a timeout sets a bit in this unit's error word and the
+// CTA still frees its TMEM before exiting.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "kernels.cuh"
+
+namespace lilicorr {
+
+static __device__ uint32_t g_err_tc;
+
+constexpr int TC_BM = 128, TC_BN = 128, TC_BK = 64, TC_STAGES = 3, TC_THREADS = 192;
+constexpr int TC_A_BYTES = TC_BM * TC_BK * 2;
+constexpr int TC_B_BYTES = TC_BN * TC_BK * 2;
+constexpr int TC_SMEM = TC_STAGES * (TC_A_BYTES + TC_B_BYTES) + 1024;
+constexpr uint32_t TC_TMEM_COLS = 128;
+
+enum TcErr : uint32_t { ERR_TC_EMPTY = 1u << 0, ERR_TC_FULL = 1u << 1, ERR_TC_ACCUM = 1u << 2 };
+
+// ------------------------------------------------------------------ PTX wrappers
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* tm, int c0, int c1,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_addr(dst_smem)),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand tile written by TMA with the 128-byte
+// swizzle (rows of 64 bf16 = 128 bytes, 8-row / 1024-byte swizzle atoms).
+//   bits  0-13 start address >> 4     bits 16-29 leading byte offset >> 4 (unused: 1)
+//   bits 32-45 stride byte offset >> 4 (1024 B between 8-row groups)
+//   bits 46-47 version (1)            bits 61-63 layout (2 = 128-byte swizzle)
+__device__ __forceinline__ uint64_t sw128_desc(const void* smem_tile) {
+  const uint64_t addr = smem_addr(smem_tile);
+  return ((addr >> 4) & 0x3FFFull) | (1ull << 16) | ((1024ull >> 4) << 32) | (1ull << 46) |
+         (2ull << 61);
+}
+
+// Instruction descriptor, kind::f16: f32 accumulator, bf16 A and B, both K-major.
+//   bits 4-5 D format (1 = f32)  bits 7-9 A format (1 = bf16)  bits 10-12 B format (1 = bf16)
+//   bit 15/16 A/B major (0 = K)  bits 17-22 N >> 3             bits 24-28 M >> 4
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_addr(bar))
+      : "memory");
+}
+
+// 32 consecutive f32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// ------------------------------------------------------------------ epilogue
+
+__device__ __forceinline__ uint32_t pack2(__nv_bfloat16 a, __nv_bfloat16 b) {
+  return uint32_t(__bfloat16_as_ushort(a)) | (uint32_t(__bfloat16_as_ushort(b)) << 16);
+}
+
+// v[0..31] = accumulator columns n..n+31 of row m (bias not yet added).
+template <int EPI>
+__device__ __forceinline__ void tc_epilogue32(const GemmArgs& g, int64_t m, int n, float (&v)[32]) {
+#pragma unroll
+  for (int j = 0; j < 32; j += 4) {
+    const float4 b4 = __ldg(reinterpret_cast<const float4*>(g.bias + n + j));
+    v[j] += b4.x;
+    v[j + 1] += b4.y;
+    v[j + 2] += b4.z;
+    v[j + 3] += b4.w;
+  }
+  if constexpr (EPI == EPI_F32) {
+    float4* o = reinterpret_cast<float4*>(g.out + m * g.N + n);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) o[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+  } else if constexpr (EPI == EPI_RESID) {
+    float4* o = reinterpret_cast<float4*>(g.out + m * g.N + n);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      float4 x = o[j];
+      x.x += v[4 * j];
+      x.y += v[4 * j + 1];
+      x.z += v[4 * j + 2];
+      x.w += v[4 * j + 3];
+      o[j] = x;
+    }
+  } else if constexpr (EPI == EPI_SPLIT || EPI == EPI_SPLIT_SILU) {
+    uint32_t hi[16], lo[16];
+#pragma unroll
+    for (int j = 0; j < 32; j += 2) {
+      float a = v[j], b = v[j + 1];
+      if constexpr (EPI == EPI_SPLIT_SILU) {
+        a = silu(a);
+        b = silu(b);
+      }
+      __nv_bfloat16 ha, la, hb, lb;
+      split_bf16(a, ha, la);
+      split_bf16(b, hb, lb);
+      hi[j / 2] = pack2(ha, hb);
+      lo[j / 2] = pack2(la, lb);
+    }
+    uint4* oh = reinterpret_cast<uint4*>(g.out_split + m * 2 * g.N + n);
+    uint4* ol = reinterpret_cast<uint4*>(g.out_split + m * 2 * g.N + g.N + n);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      oh[j] = make_uint4(hi[4 * j], hi[4 * j + 1], hi[4 * j + 2], hi[4 * j + 3]);
+      ol[j] = make_uint4(lo[4 * j], lo[4 * j + 1], lo[4 * j + 2], lo[4 * j + 3]);
+    }
+  } else {  // EPI_NODE: + E[cand] + slot_table[s-1] + rank_table[k] (+ drafter hidden)
+    const int S = (g.B - 1) * g.K;
+    const int64_t b = m / S;
+    const int t = static_cast<int>(m % S);
+    const int slot = t / g.K + 1, k = t % g.K;
+    int64_t id = g.cand_id[m];
+    id = id < 0 ? 0 : (id >= g.vocab ? g.vocab - 1 : id);
+    const uint4* e4 = reinterpret_cast<const uint4*>(g.embed + id * g.N + n);
+    const float4* st4 = reinterpret_cast<const float4*>(g.slot_table + int64_t(slot - 1) * g.N + n);
+    const float4* rk4 = reinterpret_cast<const float4*>(g.rank_table + int64_t(k) * g.N + n);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint4 e = __ldg(e4 + j);
+      const uint32_t ew[4] = {e.x, e.y, e.z, e.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        v[8 * j + 2 * q] += __uint_as_float(ew[q] << 16);
+        v[8 * j + 2 * q + 1] += __uint_as_float(ew[q] & 0xffff0000u);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float4 a = __ldg(st4 + j), c = __ldg(rk4 + j);
+      v[4 * j] += a.x + c.x;
+      v[4 * j + 1] += a.y + c.y;
+      v[4 * j + 2] += a.z + c.z;
+      v[4 * j + 3] += a.w + c.w;
+    }
+    if (g.slot_hidden) {
+      const uint4* h4 = reinterpret_cast<const uint4*>(g.slot_hidden + (b * g.B + slot) * g.N + n);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint4 e = __ldg(h4 + j);
+        const uint32_t ew[4] = {e.x, e.y, e.z, e.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          v[8 * j + 2 * q] += __uint_as_float(ew[q] << 16);
+          v[8 * j + 2 * q + 1] += __uint_as_float(ew[q] & 0xffff0000u);
+        }
+      }
+    }
+    float4* o = reinterpret_cast<float4*>(g.out + m * g.N + n);
+    float4* tp = g.nodes_tap ? reinterpret_cast<float4*>(g.nodes_tap + m * g.N + n) : nullptr;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float4 x = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+      o[j] = x;
+      if (tp) tp[j] = x;
+    }
+  }
+}
+
+// ------------------------------------------------------------------ kernel
+
+template <int EPI>
+__global__ void __launch_bounds__(TC_THREADS, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const GemmArgs g) {
+  extern __shared__ uint8_t tc_smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + TC_STAGES * TC_A_BYTES;
+  __shared__ __align__(8) uint64_t full_bar[TC_STAGES], empty_bar[TC_STAGES], accum_bar;
+  __shared__ uint32_t s_tmem;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t m0 = int64_t(blockIdx.y) * TC_BM;
+  const int n0 = blockIdx.x * TC_BN;
+  const int KB = g.Ka / TC_BK;
+
+  if (tid == 0) {
+    for (int s = 0; s < TC_STAGES; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    mbar_init(&accum_bar, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) tmem_alloc(&s_tmem, TC_TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+
+  if (warp == 0 && lane == 0) {
+    // ---- producer
+    for (int kb = 0; kb < KB; ++kb) {
+      const int s = kb % TC_STAGES, use = kb / TC_STAGES;
+      if (use > 0 && !mbar_wait_bounded(&empty_bar[s], (use - 1) & 1, &g_err_tc, ERR_TC_EMPTY))
+        break;
+      mbar_arrive_expect_tx(&full_bar[s], TC_A_BYTES + TC_B_BYTES);
+      tma_load_2d(sA + s * TC_A_BYTES, &tmA, kb * TC_BK, static_cast<int>(m0), &full_bar[s]);
+      tma_load_2d(sB + s * TC_B_BYTES, &tmB, (kb * TC_BK) % g.Kw, n0, &full_bar[s]);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---- MMA issuer
+    constexpr uint32_t idesc = idesc_bf16(TC_BM, TC_BN);
+    bool ok = true;
+    for (int kb = 0; kb < KB && ok; ++kb) {
+      const int s = kb % TC_STAGES, use = kb / TC_STAGES;
+      if (!mbar_wait_bounded(&full_bar[s], use & 1, &g_err_tc, ERR_TC_FULL)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < TC_BK / 16; ++kk)
+        umma_bf16(tmem, sw128_desc(sA + s * TC_A_BYTES + kk * 32),
+                  sw128_desc(sB + s * TC_B_BYTES + kk * 32), idesc, (kb | kk) != 0);
+      umma_commit(&empty_bar[s]);
+    }
+    umma_commit(&accum_bar);
+  } else if (warp >= 2) {
+    // ---- epilogue: warp w reads TMEM lanes 32*(w%4) .. +31
+    const int lg = warp & 3;
+    if (mbar_wait_bounded(&accum_bar, 0, &g_err_tc, ERR_TC_ACCUM)) {
+      tc_fence_after();
+      const int64_t m = m0 + 32 * lg + lane;
+#pragma unroll 1
+      for (int cc = 0; cc < TC_BN / 32; ++cc) {
+        float v[32];
+        tmem_ld32(tmem + (uint32_t(32 * lg) << 16) + uint32_t(cc * 32), v);
+        const int n = n0 + cc * 32;
+        if (m < g.M && n < g.N) tc_epilogue32<EPI>(g, m, n, v);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TC_TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------ host
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// Row-major bf16 matrix [rows, cols] read in boxes of box_rows x 64 columns.
+static bool make_tmap(CUtensorMap* tm, const void* ptr, uint64_t rows, uint64_t cols,
+                      uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {TC_BK, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool gemm_tc_supported(const GemmArgs& g) {
+  return g.Kw % TC_BK == 0 && g.Ka % TC_BK == 0 && (g.Ka == g.Kw || g.Ka == 2 * g.Kw) &&
+         g.N % 32 == 0 && g.M > 0 &&
+         (reinterpret_cast<uintptr_t>(g.A) % 16) == 0 && (reinterpret_cast<uintptr_t>(g.W) % 16) == 0;
+}
+
+cudaError_t launch_gemm(int epi, const GemmArgs& g, cudaStream_t stream) {
+  if (!gemm_tc_supported(g)) return cudaErrorInvalidValue;
+  CUtensorMap ta, tb;
+  if (!make_tmap(&ta, g.A, uint64_t(g.M), uint64_t(g.Ka), TC_BM) ||
+      !make_tmap(&tb, g.W, uint64_t(g.N), uint64_t(g.Kw), TC_BN))
+    return cudaErrorInvalidValue;
+  static bool attr = false;
+  if (!attr) {
+    cudaFuncSetAttribute(gemm_tc_kernel<EPI_F32>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
+    cudaFuncSetAttribute(gemm_tc_kernel<EPI_RESID>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
+    cudaFuncSetAttribute(gemm_tc_kernel<EPI_SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
+    cudaFuncSetAttribute(gemm_tc_kernel<EPI_SPLIT_SILU>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
+    cudaFuncSetAttribute(gemm_tc_kernel<EPI_NODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
+    attr = true;
+  }
+  const dim3 grid((g.N + TC_BN - 1) / TC_BN, static_cast<unsigned>((g.M + TC_BM - 1) / TC_BM));
+  switch (epi) {
+    case EPI_F32: gemm_tc_kernel<EPI_F32><<<grid, TC_THREADS, TC_SMEM, stream>>>(ta, tb, g); break;
+    case EPI_RESID: gemm_tc_kernel<EPI_RESID><<<grid, TC_THREADS, TC_SMEM, stream>>>(ta, tb, g); break;
+    case EPI_SPLIT: gemm_tc_kernel<EPI_SPLIT><<<grid, TC_THREADS, TC_SMEM, stream>>>(ta, tb, g); break;
+    case EPI_SPLIT_SILU: gemm_tc_kernel<EPI_SPLIT_SILU><<<grid, TC_THREADS, TC_SMEM, stream>>>(ta, tb, g); break;
+    default: gemm_tc_kernel<EPI_NODE><<<grid, TC_THREADS, TC_SMEM, stream>>>(ta, tb, g); break;
+  }
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t tc_read_device_error(uint32_t* code) {
+  uint32_t v = 0, zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_err_tc, sizeof(v));
+  if (e != cudaSuccess) return e;
+  if (v) e = cudaMemcpyToSymbol(g_err_tc, &zero, sizeof(zero));
+  *code |= v << 8;
+  return e;
+}
+
+}  // namespace lilicorr

@@ -43,7 +43,9 @@ struct GemmArgs {
   float* nodes_tap;                 // [M, N] or null
 };
 
+// tcgen05 tensor-core GEMM (gemm_tc.cu)
 cudaError_t launch_gemm(int epi, const GemmArgs& g, cudaStream_t stream);
+cudaError_t tc_read_device_error(uint32_t* code);
 cudaError_t launch_conf_hidden(const float* cand_logit, const float* lse, int64_t M, int K, int H,
                                const float* w1, const float* b1, __nv_bfloat16* U,
                                cudaStream_t stream);

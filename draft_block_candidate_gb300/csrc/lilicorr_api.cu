@@ -235,6 +235,7 @@ lilicorr_status lilicorr_device_error(uint32_t* code) {
   *code = 0;
   LC_CUDA(cudaDeviceSynchronize(), "cudaDeviceSynchronize");
   LC_CUDA(k1_read_device_error(code), "read device error");
+  LC_CUDA(tc_read_device_error(code), "read device error");
   return *code ? LILICORR_ERR_DEVICE : LILICORR_OK;
 }
 

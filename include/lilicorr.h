@@ -176,8 +176,9 @@ const char* lilicorr_status_string(lilicorr_status s);
 const char* lilicorr_last_error(void);
 /* Kernels this library has launched since load (all threads). */
 uint64_t lilicorr_launch_count(void);
-/* Read and clear the device-side error word of the current device (synchronises the
- * device): 0 = no error; otherwise a bit set per failed wait site. */
+/* Read and clear the device-side error words of the current device (synchronises the
+ * device): 0 = no error; otherwise one bit per wait site that gave up (bits 0-7 the logit
+ * pass, bits 8-15 the tensor-core GEMM). */
 lilicorr_status lilicorr_device_error(uint32_t* code);
 
 /* Per-kernel timing.  When enabled, lilicorr_rerank records a CUDA event on its stream
