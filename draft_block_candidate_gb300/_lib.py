@@ -31,6 +31,8 @@ SIGNATURES = {
                                                        C.c_int32, C.c_int]),
     "lilicorr_topk_lse": (C.c_int, [_P, C.c_int, C.c_int64, C.c_int32, C.c_int64, C.c_int32,
                                     _P, _P, _P, _P, C.c_size_t, _P]),
+    "lilicorr_topk_lse_noalloc": (C.c_int, [_P, C.c_int, C.c_int64, C.c_int32, C.c_int64,
+                                            C.c_int32, _P, _P, _P, _P]),
     "lilicorr_greedy_walk": (C.c_int, [_P, _P, _P, C.c_int64, C.c_int32, C.c_int32, _P, _P, _P,
                                        _P]),
     "lilicorr_status_string": (C.c_char_p, [C.c_int]),

@@ -12,6 +12,9 @@ cudaError_t k1_launch(const void* logits, int esize, int64_t batch, int B, int64
                       cudaStream_t stream);
 cudaError_t k1_read_device_error(uint32_t* code);
 
+// message returned by lilicorr_last_error() for this thread (lilicorr_api.cu)
+void set_last_error(const char* msg);
+
 // a4 scores + a5 walk (walk.cu)
 cudaError_t launch_pair_scores(const float* heads, const float* anchor_raw, int64_t batch, int B,
                                int K, int E, float sigma, float* scores, float* out_tap,

@@ -15,6 +15,7 @@ namespace lilicorr {
 static std::atomic<uint64_t> g_launches{0};
 void note_launch(int n) { g_launches.fetch_add(uint64_t(n), std::memory_order_relaxed); }
 static thread_local std::string t_last_error;
+void set_last_error(const char* msg) { t_last_error = msg; }
 
 static lilicorr_status cuda_fail(cudaError_t e, const char* where) {
   t_last_error = std::string(where) + ": " + cudaGetErrorString(e);

@@ -27,6 +27,8 @@
 
 #include <algorithm>
 #include <cmath>
+#include <cstdio>
+#include <mutex>
 
 #include "kernels.cuh"
 
@@ -651,4 +653,72 @@ cudaError_t k1_read_device_error(uint32_t* code) {
   return e;
 }
 
+// ------------------------------------------------------------------ allocation-free form
+// Scratch for lilicorr_topk_lse_noalloc: the split-row partial results and their
+// arrival counters, compiled into the library so that a caller needs no workspace.
+// Every device that loads the library holds these bytes until the process exits.
+constexpr size_t K1_STATIC_SCRATCH_BYTES = size_t(4) << 20;
+static __device__ __align__(256) uint8_t g_k1_static_scratch[K1_STATIC_SCRATCH_BYTES];
+
+static std::mutex g_static_scratch_mu;
+static void* g_static_scratch_dev[128] = {};  // device address of the array, per device
+
+// Device address of the static scratch on the current device.  In host code the
+// array's name is only a host-side stand-in, so the address is looked up once per device
+// (with that device current) and cached.
+static cudaError_t k1_static_scratch(void** ptr) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_static_scratch_mu);
+  if (!g_static_scratch_dev[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_k1_static_scratch);
+    if (e != cudaSuccess) return e;
+    g_static_scratch_dev[dev] = p;
+  }
+  *ptr = g_static_scratch_dev[dev];
+  return cudaSuccess;
+}
+
 }  // namespace lilicorr
+
+extern "C" lilicorr_status lilicorr_topk_lse_noalloc(const void* logits, lilicorr_dtype ldtype,
+                                                     int64_t batch, int32_t B, int64_t V,
+                                                     int32_t K, int32_t* cand_id,
+                                                     float* cand_logit, float* lse,
+                                                     void* stream) {
+  using namespace lilicorr;
+  if (!logits || !cand_id || !cand_logit || !lse) return LILICORR_ERR_INVALID_ARG;
+  if (batch < 1 || B < 2 || V < 1 || V > (int64_t(1) << 31) - 2 || K < 1 || K > 32 || K > V)
+    return LILICORR_ERR_INVALID_ARG;
+  if (ldtype != LILICORR_F32 && ldtype != LILICORR_BF16) return LILICORR_ERR_INVALID_ARG;
+  const int es = ldtype == LILICORR_BF16 ? 2 : 4;
+  if (reinterpret_cast<uintptr_t>(logits) % es) return LILICORR_ERR_INVALID_ARG;
+  if (V * es > (int64_t(1) << 31) - 64) return LILICORR_ERR_INVALID_ARG;
+  const size_t need = k1_workspace_bytes(batch, B, V, es);
+  if (need > K1_STATIC_SCRATCH_BYTES) {
+    char msg[160];
+    snprintf(msg, sizeof(msg),
+             "lilicorr_topk_lse_noalloc: this shape needs %zu bytes of scratch; the static "
+             "scratch holds %zu (use lilicorr_topk_lse with a workspace)",
+             need, K1_STATIC_SCRATCH_BYTES);
+    set_last_error(msg);
+    return LILICORR_ERR_WORKSPACE;
+  }
+  void* scratch = nullptr;
+  cudaError_t e = k1_static_scratch(&scratch);
+  if (e != cudaSuccess) {
+    set_last_error(cudaGetErrorString(e));
+    return LILICORR_ERR_CUDA;
+  }
+  // k1_launch zeroes the arrival counters inside the scratch before the kernel runs.
+  e = k1_launch(logits, es, batch, B, V, K, cand_id, cand_logit, lse, scratch,
+                static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) {
+    set_last_error(cudaGetErrorString(e));
+    return LILICORR_ERR_CUDA;
+  }
+  return LILICORR_OK;
+}

@@ -159,6 +159,27 @@ lilicorr_status lilicorr_topk_lse(const void* logits, lilicorr_dtype ldtype, int
                                   float* cand_logit, float* lse, void* workspace,
                                   size_t workspace_bytes, void* stream);
 
+/* lilicorr_topk_lse without a workspace (the paper has no counterpart: this is a
+ * convenience of this library).  Some callers cannot allocate device memory when they
+ * run the logit pass: a serving loop whose memory is all handed to its own pool and that
+ * forbids further cudaMalloc, code running while a CUDA graph is being captured (where
+ * allocation is not allowed), or a plain C host that has no device allocator at all.
+ * This form computes exactly what lilicorr_topk_lse computes, but keeps the split-row
+ * scratch in a 4 MiB array compiled into the library (every GPU that loads the library
+ * holds it until the process exits); it allocates nothing and frees nothing.
+ *   - A shape that needs more scratch than 4 MiB returns LILICORR_ERR_WORKSPACE with a
+ *     message in lilicorr_last_error(); use lilicorr_topk_lse for it.
+ *   - The first call on each device looks up the scratch's device address (the library
+ *     caches it per device); make that first call before any stream capture.
+ *   - All calls share the one scratch array, which keeps the previous call's contents
+ *     (the parts that must start at zero are cleared by every call).  Calls whose work
+ *     overlaps on the GPU (different streams, or host threads without ordering) race on
+ *     it: serialise them. */
+lilicorr_status lilicorr_topk_lse_noalloc(const void* logits, lilicorr_dtype ldtype,
+                                          int64_t batch, int32_t B, int64_t V, int32_t K,
+                                          int32_t* cand_id, float* cand_logit, float* lse,
+                                          void* stream);
+
 /* Step a5 alone (LiLiCorr Sec. 3.5, Eq. 8) on given scores pair_scores [batch,B-1,K,K]
  * (layout as in lilicorr_taps).  c_1 = argmax_k pair_scores[b,0,0,k]; c_s = argmax_k
  * pair_scores[b,s-1,c_{s-1},k]; ties go to the lowest k (serving PR: the Triton
