@@ -6,15 +6,18 @@
 // significant bits) when Ka = 2 Kw; W is an exact bf16 weight whose column index wraps
 // (k mod Kw), so one accumulation gives A_hi W^T + A_lo W^T.
 //
-// One CTA per 128 x 128 output tile, 6 warps:
-//   warp 0      TMA producer (2-D tiled loads, 128-byte swizzle, 3-stage mbarrier ring)
-//               and TMEM owner (allocates / frees the 128-column f32 accumulator)
+// Persistent: one CTA per SM walks the 128 x 128 output tiles (n fastest, so the CTAs
+// working at the same time share A tiles through L2).  10 warps:
+//   warp 0      TMA producer (2-D tiled loads, 128-byte swizzle, 4-stage mbarrier ring
+//               that runs on across tiles) and TMEM owner (2 x 128 f32 columns)
 //   warp 1      MMA issuer: one elected thread issues tcgen05.mma (kind::f16, bf16 in,
 //               f32 accumulate in TMEM), 4 per 64-wide K block, and tcgen05.commit
-//   warps 2-5   epilogue: tcgen05.ld of its 32 TMEM lanes (= 32 output rows), then the
-//               fused bias / SiLU / residual / hi-lo split / node-sum, stored to global
-// Every mbarrier wait is bounded; a timeout sets a bit in this unit's error word and the
-// CTA still frees its TMEM before exiting.
+//   warps 2-9   epilogue: two warps per 32-lane TMEM quarter (= 32 output rows), each
+//               taking half of the columns; tcgen05.ld, then the fused bias / SiLU /
+//               residual / hi-lo split / node-sum, stored to global
+// The accumulator is double-buffered: the epilogue of tile i overlaps the MMAs of tile
+// i + 1.  Every mbarrier wait is bounded; a timeout sets a bit in this unit's error word
+// and the CTA still frees its TMEM before exiting.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -24,13 +27,19 @@ namespace lilicorr {
 
 static __device__ uint32_t g_err_tc;
 
-constexpr int TC_BM = 128, TC_BN = 128, TC_BK = 64, TC_STAGES = 3, TC_THREADS = 192;
+constexpr int TC_BM = 128, TC_BN = 128, TC_BK = 64, TC_STAGES = 4;
+constexpr int TC_EPI_WARPS = 8, TC_THREADS = 32 * (2 + TC_EPI_WARPS);
 constexpr int TC_A_BYTES = TC_BM * TC_BK * 2;
 constexpr int TC_B_BYTES = TC_BN * TC_BK * 2;
 constexpr int TC_SMEM = TC_STAGES * (TC_A_BYTES + TC_B_BYTES) + 1024;
-constexpr uint32_t TC_TMEM_COLS = 128;
+constexpr uint32_t TC_TMEM_COLS = 2 * TC_BN;  // two accumulator buffers
 
-enum TcErr : uint32_t { ERR_TC_EMPTY = 1u << 0, ERR_TC_FULL = 1u << 1, ERR_TC_ACCUM = 1u << 2 };
+enum TcErr : uint32_t {
+  ERR_TC_EMPTY = 1u << 0,
+  ERR_TC_FULL = 1u << 1,
+  ERR_TC_ACCUM = 1u << 2,
+  ERR_TC_ACC_EMPTY = 1u << 3
+};
 
 // ------------------------------------------------------------------ PTX wrappers
 
@@ -229,20 +238,25 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       (reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + TC_STAGES * TC_A_BYTES;
-  __shared__ __align__(8) uint64_t full_bar[TC_STAGES], empty_bar[TC_STAGES], accum_bar;
+  __shared__ __align__(8) uint64_t full_bar[TC_STAGES], empty_bar[TC_STAGES];
+  __shared__ __align__(8) uint64_t acc_full[2], acc_empty[2];
   __shared__ uint32_t s_tmem;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int64_t m0 = int64_t(blockIdx.y) * TC_BM;
-  const int n0 = blockIdx.x * TC_BN;
   const int KB = g.Ka / TC_BK;
+  const int NT = (g.N + TC_BN - 1) / TC_BN;
+  const int MT = static_cast<int>((g.M + TC_BM - 1) / TC_BM);
+  const int ntiles = NT * MT;
 
   if (tid == 0) {
     for (int s = 0; s < TC_STAGES; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
     }
-    mbar_init(&accum_bar, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], TC_EPI_WARPS);
+    }
     fence_mbar_init();
   }
   if (warp == 0) tmem_alloc(&s_tmem, TC_TMEM_COLS);
@@ -252,46 +266,73 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   const uint32_t tmem = s_tmem;
 
   if (warp == 0 && lane == 0) {
-    // ---- producer
-    for (int kb = 0; kb < KB; ++kb) {
-      const int s = kb % TC_STAGES, use = kb / TC_STAGES;
-      if (use > 0 && !mbar_wait_bounded(&empty_bar[s], (use - 1) & 1, &g_err_tc, ERR_TC_EMPTY))
-        break;
-      mbar_arrive_expect_tx(&full_bar[s], TC_A_BYTES + TC_B_BYTES);
-      tma_load_2d(sA + s * TC_A_BYTES, &tmA, kb * TC_BK, static_cast<int>(m0), &full_bar[s]);
-      tma_load_2d(sB + s * TC_B_BYTES, &tmB, (kb * TC_BK) % g.Kw, n0, &full_bar[s]);
+    // ---- producer: the smem ring runs on across this CTA's tiles
+    int it = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+      const int m0 = (t / NT) * TC_BM, n0 = (t % NT) * TC_BN;
+      for (int kb = 0; kb < KB; ++kb, ++it) {
+        const int s = it % TC_STAGES, use = it / TC_STAGES;
+        if (use > 0 && !mbar_wait_bounded(&empty_bar[s], (use - 1) & 1, &g_err_tc, ERR_TC_EMPTY)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&full_bar[s], TC_A_BYTES + TC_B_BYTES);
+        tma_load_2d(sA + s * TC_A_BYTES, &tmA, kb * TC_BK, m0, &full_bar[s]);
+        tma_load_2d(sB + s * TC_B_BYTES, &tmB, (kb * TC_BK) % g.Kw, n0, &full_bar[s]);
+      }
     }
   } else if (warp == 1 && lane == 0) {
     // ---- MMA issuer
     constexpr uint32_t idesc = idesc_bf16(TC_BM, TC_BN);
+    int it = 0, i = 0;
     bool ok = true;
-    for (int kb = 0; kb < KB && ok; ++kb) {
-      const int s = kb % TC_STAGES, use = kb / TC_STAGES;
-      if (!mbar_wait_bounded(&full_bar[s], use & 1, &g_err_tc, ERR_TC_FULL)) {
+    for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++i) {
+      const int buf = i & 1;
+      const uint32_t acc = tmem + uint32_t(buf * TC_BN);
+      if (i >= 2 && !mbar_wait_bounded(&acc_empty[buf], ((i >> 1) - 1) & 1, &g_err_tc,
+                                        ERR_TC_ACC_EMPTY)) {
         ok = false;
         break;
       }
       tc_fence_after();
+      for (int kb = 0; kb < KB; ++kb, ++it) {
+        const int s = it % TC_STAGES, use = it / TC_STAGES;
+        if (!mbar_wait_bounded(&full_bar[s], use & 1, &g_err_tc, ERR_TC_FULL)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
 #pragma unroll
-      for (int kk = 0; kk < TC_BK / 16; ++kk)
-        umma_bf16(tmem, sw128_desc(sA + s * TC_A_BYTES + kk * 32),
-                  sw128_desc(sB + s * TC_B_BYTES + kk * 32), idesc, (kb | kk) != 0);
-      umma_commit(&empty_bar[s]);
+        for (int kk = 0; kk < TC_BK / 16; ++kk)
+          umma_bf16(acc, sw128_desc(sA + s * TC_A_BYTES + kk * 32),
+                    sw128_desc(sB + s * TC_B_BYTES + kk * 32), idesc, (kb | kk) != 0);
+        umma_commit(&empty_bar[s]);
+      }
+      umma_commit(&acc_full[buf]);
     }
-    umma_commit(&accum_bar);
   } else if (warp >= 2) {
-    // ---- epilogue: warp w reads TMEM lanes 32*(w%4) .. +31
-    const int lg = warp & 3;
-    if (mbar_wait_bounded(&accum_bar, 0, &g_err_tc, ERR_TC_ACCUM)) {
+    // ---- epilogue: quarter q = warp % 4 owns TMEM lanes 32q..32q+31 (output rows);
+    // the two warps of a quarter split the tile's columns in halves
+    const int q = warp & 3, half = (warp - 2) >> 2;
+    int i = 0;
+    for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
+      const int buf = i & 1;
+      const int64_t m0 = int64_t(t / NT) * TC_BM;
+      const int n0 = (t % NT) * TC_BN;
+      if (!mbar_wait_bounded(&acc_full[buf], (i >> 1) & 1, &g_err_tc, ERR_TC_ACCUM)) break;
       tc_fence_after();
-      const int64_t m = m0 + 32 * lg + lane;
+      const int64_t m = m0 + 32 * q + lane;
 #pragma unroll 1
-      for (int cc = 0; cc < TC_BN / 32; ++cc) {
+      for (int cc = half * (TC_BN / 64); cc < (half + 1) * (TC_BN / 64); ++cc) {
         float v[32];
-        tmem_ld32(tmem + (uint32_t(32 * lg) << 16) + uint32_t(cc * 32), v);
+        tmem_ld32(tmem + (uint32_t(32 * q) << 16) + uint32_t(buf * TC_BN + cc * 32), v);
         const int n = n0 + cc * 32;
         if (m < g.M && n < g.N) tc_epilogue32<EPI>(g, m, n, v);
       }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[buf]);
     }
   }
   tc_fence_before();
@@ -352,7 +393,15 @@ cudaError_t launch_gemm(int epi, const GemmArgs& g, cudaStream_t stream) {
     cudaFuncSetAttribute(gemm_tc_kernel<EPI_NODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
     attr = true;
   }
-  const dim3 grid((g.N + TC_BN - 1) / TC_BN, static_cast<unsigned>((g.M + TC_BM - 1) / TC_BM));
+  static int sms = 0;
+  if (!sms) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (sms <= 0) sms = 148;
+  }
+  const int64_t ntiles = int64_t((g.N + TC_BN - 1) / TC_BN) * ((g.M + TC_BM - 1) / TC_BM);
+  const dim3 grid(static_cast<unsigned>(ntiles < sms ? ntiles : sms));
   switch (epi) {
     case EPI_F32: gemm_tc_kernel<EPI_F32><<<grid, TC_THREADS, TC_SMEM, stream>>>(ta, tb, g); break;
     case EPI_RESID: gemm_tc_kernel<EPI_RESID><<<grid, TC_THREADS, TC_SMEM, stream>>>(ta, tb, g); break;
