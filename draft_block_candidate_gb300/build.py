@@ -10,7 +10,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "liblilicorr.so")
-SOURCES = ["logit_pass.cu", "walk.cu", "encoder.cu", "gemm_tc.cu", "lilicorr_api.cu"]
+SOURCES = ["logit_pass.cu", "walk.cu", "encoder.cu", "gemm_tc.cu", "attn_tc.cu", "lilicorr_api.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
               "--expt-relaxed-constexpr"]

@@ -1,0 +1,381 @@
+// Lattice self-attention of step a3 on the 5th-generation tensor cores (head dim 64,
+// up to 256 lattice tokens per block).
+//
+// Per head: softmax_j(q_i . k_j / sqrt(dh) + dist[slot_j - slot_i + B_max - 2]
+//                     + [slot_i == slot_j] * same) v_j          (LiLiCorr App. A)
+// over all tokens of the block (bidirectional, no mask).
+//
+// One CTA per (block, head, 128-query tile), 10 warps:
+//   warp 0     TMA: Q (128 x 64), K and V (256 x 64), each as bf16 hi and lo, 128-byte
+//              swizzle; owns the TMEM allocation (S: 256 f32 columns, O: 64 columns)
+//   warp 1     MMA: S = Qh Kh^T + Qh Kl^T + Ql Kh^T (M 128, N 256, K 64), then
+//              O = Ph Vh + Ph Vl + Pl Vh over all 256 keys (V read as an MN-major operand)
+//   warps 2-9  two warps per query row quarter, each taking half of the keys: pass 1
+//              scales, adds the slot bias (one table lookup), masks keys beyond the
+//              block, takes the row max (halves combined through shared memory) and
+//              writes the logits back to TMEM; pass 2 forms p = exp(s - max) and its sum
+//              and writes p as bf16 hi/lo into swizzled shared memory (over the finished
+//              Q and K tiles); the epilogue divides O by the sum and stores it split.
+// Every mbarrier wait is bounded; on a timeout the CTA records it and still frees TMEM.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "kernels.cuh"
+
+namespace lilicorr {
+
+static __device__ uint32_t g_err_at;
+
+constexpr int AT_DH = 64, AT_QT = 128, AT_KMAX = 256, AT_SOFT_WARPS = 8;
+constexpr int AT_THREADS = 32 * (2 + AT_SOFT_WARPS);
+constexpr int AT_TILE = 128 * 64 * 2;  // one [128 x 64] bf16 swizzled tile
+constexpr int AT_SMEM = 12 * AT_TILE + 1024;
+constexpr uint32_t AT_TMEM_COLS = 512, AT_O_COL = 256;
+constexpr float AT_LOG2E = 1.4426950408889634f;
+
+enum AtErr : uint32_t {
+  ERR_AT_QK = 1u << 0,
+  ERR_AT_S = 1u << 1,
+  ERR_AT_V = 1u << 2,
+  ERR_AT_P = 1u << 3,
+  ERR_AT_O = 1u << 4
+};
+
+__device__ __forceinline__ void at_tma(void* dst, const CUtensorMap* tm, int c0, int c1,
+                                       uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(smem_addr(bar))
+      : "memory");
+}
+__device__ __forceinline__ void at_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void at_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// 128-byte-swizzle descriptor (K-major tiles of 64-element rows, or MN-major tiles whose
+// rows are the K index); 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t at_desc(const void* p) {
+  const uint64_t a = smem_addr(p);
+  return ((a >> 4) & 0x3FFFull) | (1ull << 16) | ((1024ull >> 4) << 32) | (1ull << 46) |
+         (2ull << 61);
+}
+__device__ __forceinline__ void at_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                       uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void at_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_addr(bar))
+      : "memory");
+}
+__device__ __forceinline__ void at_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void at_st32(uint32_t taddr, const float (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+      "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+      "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+      "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+      "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+      "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ float at_ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ uint32_t at_pack(__nv_bfloat16 a, __nv_bfloat16 b) {
+  return uint32_t(__bfloat16_as_ushort(a)) | (uint32_t(__bfloat16_as_ushort(b)) << 16);
+}
+
+// idesc kind::f16, f32 D, bf16 A/B; b_mn selects an MN-major B operand.
+__host__ __device__ constexpr uint32_t at_idesc(int M, int N, bool b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (b_mn ? (1u << 16) : 0u) |
+         (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void soft_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(32 * AT_SOFT_WARPS) : "memory");
+}
+
+__global__ void __launch_bounds__(AT_THREADS, 1)
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tm, int S, int Kc, int H, int B_max,
+                   const float* __restrict__ dist_bias, const float* __restrict__ same_bias,
+                   int64_t M, __nv_bfloat16* __restrict__ out) {
+  extern __shared__ uint8_t at_smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(at_smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQh = sm;                 // Q hi / lo: 1 tile each
+  uint8_t* sQl = sm + AT_TILE;
+  uint8_t* sKh = sm + 2 * AT_TILE;   // K hi / lo: 2 tiles each (256 keys)
+  uint8_t* sKl = sm + 4 * AT_TILE;
+  uint8_t* sVh = sm + 8 * AT_TILE;   // V hi / lo: 2 tiles each
+  uint8_t* sVl = sm + 10 * AT_TILE;
+  uint8_t* sPh = sm;                 // after S: P hi = 4 tiles of 64 keys, P lo = 4 tiles
+  uint8_t* sPl = sm + 4 * AT_TILE;
+  __shared__ __align__(8) uint64_t bar_qk, bar_v, bar_s, bar_p, bar_o;
+  __shared__ uint32_t s_tmem;
+  __shared__ float s_bias[128];      // dist + same-slot bias by slot distance
+  __shared__ int s_kslot[AT_KMAX];
+  __shared__ float s_pmax[2][128], s_psum[2][128];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int q0 = blockIdx.x * AT_QT, h = blockIdx.y;
+  const int64_t blk = blockIdx.z;
+  const int tok0 = static_cast<int>(blk * S);
+  const int nd = 2 * B_max - 3;
+
+  if (tid == 0) {
+    mbar_init(&bar_qk, 1);
+    mbar_init(&bar_v, 1);
+    mbar_init(&bar_s, 1);
+    mbar_init(&bar_p, 32 * AT_SOFT_WARPS);
+    mbar_init(&bar_o, 1);
+    fence_mbar_init();
+  }
+  for (int i = tid; i < nd; i += AT_THREADS)
+    s_bias[i] = dist_bias[h * nd + i] + (i == B_max - 2 ? same_bias[h] : 0.f);
+  for (int j = tid; j < AT_KMAX; j += AT_THREADS) s_kslot[j] = j < S ? j / Kc : 0;
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr(&s_tmem)),
+                 "r"(AT_TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  at_fence_before();
+  __syncthreads();
+  at_fence_after();
+  const uint32_t tmem = s_tmem;
+  const uint32_t tS = tmem, tO = tmem + AT_O_COL;
+
+  if (warp == 0 && lane == 0) {
+    const int cq = h * AT_DH, ck = H + h * AT_DH, cv = 2 * H + h * AT_DH, lo = 3 * H;
+    mbar_arrive_expect_tx(&bar_qk, 6 * AT_TILE);
+    at_tma(sQh, &tm, cq, tok0 + q0, &bar_qk);
+    at_tma(sQl, &tm, lo + cq, tok0 + q0, &bar_qk);
+    at_tma(sKh, &tm, ck, tok0, &bar_qk);
+    at_tma(sKh + AT_TILE, &tm, ck, tok0 + 128, &bar_qk);
+    at_tma(sKl, &tm, lo + ck, tok0, &bar_qk);
+    at_tma(sKl + AT_TILE, &tm, lo + ck, tok0 + 128, &bar_qk);
+    mbar_arrive_expect_tx(&bar_v, 4 * AT_TILE);
+    at_tma(sVh, &tm, cv, tok0, &bar_v);
+    at_tma(sVh + AT_TILE, &tm, cv, tok0 + 128, &bar_v);
+    at_tma(sVl, &tm, lo + cv, tok0, &bar_v);
+    at_tma(sVl + AT_TILE, &tm, lo + cv, tok0 + 128, &bar_v);
+  } else if (warp == 1 && lane == 0) {
+    constexpr uint32_t id_s = at_idesc(128, 256, false);
+    constexpr uint32_t id_o = at_idesc(128, 64, true);
+    bool ok = mbar_wait_bounded(&bar_qk, 0, &g_err_at, ERR_AT_QK);
+    if (ok) {
+      at_fence_after();
+#pragma unroll
+      for (int ks = 0; ks < AT_DH / 16; ++ks) {
+        at_mma(tS, at_desc(sQh + ks * 32), at_desc(sKh + ks * 32), id_s, ks > 0);
+        at_mma(tS, at_desc(sQh + ks * 32), at_desc(sKl + ks * 32), id_s, 1);
+        at_mma(tS, at_desc(sQl + ks * 32), at_desc(sKh + ks * 32), id_s, 1);
+      }
+    }
+    at_commit(&bar_s);
+    ok = ok && mbar_wait_bounded(&bar_v, 0, &g_err_at, ERR_AT_V) &&
+         mbar_wait_bounded(&bar_p, 0, &g_err_at, ERR_AT_P);
+    if (ok) {
+      at_fence_after();
+#pragma unroll 4
+      for (int j = 0; j < AT_KMAX / 16; ++j) {
+        const int kt = j >> 2, off = (j & 3) * 32;
+        const uint8_t* ph = sPh + kt * AT_TILE + off;
+        const uint8_t* pl = sPl + kt * AT_TILE + off;
+        at_mma(tO, at_desc(ph), at_desc(sVh + 16 * j * 128), id_o, j > 0);
+        at_mma(tO, at_desc(ph), at_desc(sVl + 16 * j * 128), id_o, 1);
+        at_mma(tO, at_desc(pl), at_desc(sVh + 16 * j * 128), id_o, 1);
+      }
+    }
+    at_commit(&bar_o);
+  } else if (warp >= 2) {
+    const int qq = warp & 3, hf = (warp - 2) >> 2;
+    const int r = 32 * qq + lane;  // TMEM lane = query row of the tile
+    const int i = q0 + r;
+    const int boff = B_max - 2 - min(i, S - 1) / Kc;  // bias index = slot_j + boff
+    const uint32_t lane_off = uint32_t(32 * qq) << 16;
+    const int j0 = 128 * hf;         // this warp's keys j0 .. j0 + 127
+    float mx = -INFINITY;
+    bool ok = mbar_wait_bounded(&bar_s, 0, &g_err_at, ERR_AT_S);
+    at_fence_after();
+    // pass 1: logits with bias and mask, partial row max, written back
+#pragma unroll 1
+    for (int cc = 0; cc < 4; ++cc) {
+      const int jb = j0 + 32 * cc;
+      float v[32];
+      at_ld32(tS + lane_off + jb, v);
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const float x = jb + e < S ? fmaf(v[e], 0.125f, s_bias[s_kslot[jb + e] + boff]) : -INFINITY;
+        v[e] = x;
+        mx = fmaxf(mx, x);
+      }
+      at_st32(tS + lane_off + jb, v);
+    }
+    s_pmax[hf][r] = mx;
+    soft_sync();
+    mx = fmaxf(s_pmax[0][r], s_pmax[1][r]);
+    // pass 2: p = exp(s - max), partial sum, p as bf16 hi/lo into the P tiles
+    const float m2 = mx * AT_LOG2E;
+    float l = 0.f;
+#pragma unroll 1
+    for (int cc = 0; cc < 4; ++cc) {
+      const int jb = j0 + 32 * cc;
+      float v[32];
+      at_ld32(tS + lane_off + jb, v);
+      uint32_t ph[16], pl[16];
+#pragma unroll
+      for (int e = 0; e < 32; e += 2) {
+        const float pa = at_ex2(fmaf(v[e], AT_LOG2E, -m2));
+        const float pb = at_ex2(fmaf(v[e + 1], AT_LOG2E, -m2));
+        l += pa + pb;
+        __nv_bfloat16 ha, la, hb, lb;
+        split_bf16(pa, ha, la);
+        split_bf16(pb, hb, lb);
+        ph[e / 2] = at_pack(ha, hb);
+        pl[e / 2] = at_pack(la, lb);
+      }
+      // keys jb..jb+31: tile kt = jb / 64, 16-byte chunks 4 * ((jb / 32) & 1) + u
+      const int kt = jb >> 6;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int ch = 4 * ((jb >> 5) & 1) + u;
+        const int off = kt * AT_TILE + r * 128 + ((ch ^ (r & 7)) << 4);
+        *reinterpret_cast<uint4*>(sPh + off) =
+            make_uint4(ph[4 * u], ph[4 * u + 1], ph[4 * u + 2], ph[4 * u + 3]);
+        *reinterpret_cast<uint4*>(sPl + off) =
+            make_uint4(pl[4 * u], pl[4 * u + 1], pl[4 * u + 2], pl[4 * u + 3]);
+      }
+    }
+    s_psum[hf][r] = l;
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    at_fence_before();
+    mbar_arrive(&bar_p);
+    soft_sync();
+    const float inv = 1.0f / (s_psum[0][r] + s_psum[1][r]);
+    // epilogue: O / l for this warp's 32 of the 64 output columns, split, stored
+    ok = mbar_wait_bounded(&bar_o, 0, &g_err_at, ERR_AT_O) && ok;
+    at_fence_after();
+    float v[32];
+    at_ld32(tO + lane_off + 32 * hf, v);
+    if (i < S && ok) {
+      __nv_bfloat16* dst = out + (int64_t(tok0) + i) * 2 * H + h * AT_DH + 32 * hf;
+      uint32_t hi[16], lo[16];
+#pragma unroll
+      for (int e = 0; e < 32; e += 2) {
+        __nv_bfloat16 ha, la, hb, lb;
+        split_bf16(v[e] * inv, ha, la);
+        split_bf16(v[e + 1] * inv, hb, lb);
+        hi[e / 2] = at_pack(ha, hb);
+        lo[e / 2] = at_pack(la, lb);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        *reinterpret_cast<uint4*>(dst + 8 * u) = make_uint4(hi[4 * u], hi[4 * u + 1], hi[4 * u + 2], hi[4 * u + 3]);
+        *reinterpret_cast<uint4*>(dst + H + 8 * u) = make_uint4(lo[4 * u], lo[4 * u + 1], lo[4 * u + 2], lo[4 * u + 3]);
+      }
+    }
+  }
+  at_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    at_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(AT_TMEM_COLS)
+                 : "memory");
+  }
+}
+
+// ------------------------------------------------------------------ host
+
+static PFN_cuTensorMapEncodeTiled_v12000 at_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+bool attention_tc_supported(int S, int H, int heads) {
+  return H / heads == AT_DH && S >= 1 && S <= AT_KMAX && H % 64 == 0;
+}
+
+cudaError_t launch_attention_tc(const __nv_bfloat16* qkv, int64_t batch, int S, int K, int H,
+                                int heads, int B_max, const float* dist_bias,
+                                const float* same_bias, __nv_bfloat16* out,
+                                cudaStream_t stream) {
+  auto fn = at_encode_fn();
+  if (!fn || !attention_tc_supported(S, H, heads)) return cudaErrorInvalidValue;
+  const int64_t M = batch * S;
+  CUtensorMap tm;
+  const cuuint64_t dims[2] = {cuuint64_t(6 * H), cuuint64_t(M)};
+  const cuuint64_t strides[1] = {cuuint64_t(6 * H) * 2};
+  const cuuint32_t box[2] = {64, 128};
+  const cuuint32_t estr[2] = {1, 1};
+  if (fn(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<__nv_bfloat16*>(qkv), dims, strides,
+         box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  static bool attr = false;
+  if (!attr) {
+    cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, AT_SMEM);
+    attr = true;
+  }
+  const dim3 grid((S + AT_QT - 1) / AT_QT, heads, static_cast<unsigned>(batch));
+  attn_tc_kernel<<<grid, AT_THREADS, AT_SMEM, stream>>>(tm, S, K, H, B_max, dist_bias,
+                                                        same_bias, M, out);
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t at_read_device_error(uint32_t* code) {
+  uint32_t v = 0, zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_err_at, sizeof(v));
+  if (e != cudaSuccess) return e;
+  if (v) e = cudaMemcpyToSymbol(g_err_at, &zero, sizeof(zero));
+  *code |= v << 16;
+  return e;
+}
+
+}  // namespace lilicorr

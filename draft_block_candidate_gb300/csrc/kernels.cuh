@@ -57,6 +57,12 @@ cudaError_t launch_rmsnorm_split(const float* X, const float* gain, int64_t M, i
 cudaError_t launch_attention(const __nv_bfloat16* qkv, int64_t batch, int S, int K, int H,
                              int heads, int B_max, const float* dist_bias,
                              const float* same_bias, __nv_bfloat16* out, cudaStream_t stream);
+// tcgen05 attention for head dim 64 and up to 256 tokens (attn_tc.cu)
+bool attention_tc_supported(int S, int H, int heads);
+cudaError_t launch_attention_tc(const __nv_bfloat16* qkv, int64_t batch, int S, int K, int H,
+                                int heads, int B_max, const float* dist_bias,
+                                const float* same_bias, __nv_bfloat16* out, cudaStream_t stream);
+cudaError_t at_read_device_error(uint32_t* code);
 cudaError_t launch_fuse_concat(const float* X, const __nv_bfloat16* target, int S, int64_t M,
                                int H, __nv_bfloat16* out, cudaStream_t stream);
 cudaError_t launch_anchor(const __nv_bfloat16* target, const __nv_bfloat16* Wa, const float* ba,

@@ -237,6 +237,7 @@ lilicorr_status lilicorr_device_error(uint32_t* code) {
   LC_CUDA(cudaDeviceSynchronize(), "cudaDeviceSynchronize");
   LC_CUDA(k1_read_device_error(code), "read device error");
   LC_CUDA(tc_read_device_error(code), "read device error");
+  LC_CUDA(at_read_device_error(code), "read device error");
   return *code ? LILICORR_ERR_DEVICE : LILICORR_OK;
 }
 
@@ -496,8 +497,13 @@ lilicorr_status lilicorr_rerank(const lilicorr_weights* w, const void* logits,
     g.out_split = qkv;
     LC_CUDA(launch_gemm(EPI_SPLIT, g, stream), "qkv gemm");
     MARK(T_QKV);
-    LC_CUDA(launch_attention(qkv, batch, S, K, H, d.heads, d.B_max, L.dist, L.same, act1, stream),
-            "attention");
+    if (attention_tc_supported(S, H, d.heads))
+      LC_CUDA(launch_attention_tc(qkv, batch, S, K, H, d.heads, d.B_max, L.dist, L.same, act1,
+                                  stream),
+              "attention");
+    else
+      LC_CUDA(launch_attention(qkv, batch, S, K, H, d.heads, d.B_max, L.dist, L.same, act1, stream),
+              "attention");
     MARK(T_ATTN);
     g = GemmArgs{};
     g.A = act1; g.W = L.out_w; g.M = M; g.N = H; g.Kw = H; g.Ka = 2 * H; g.bias = L.out_b; g.out = X;

@@ -199,7 +199,7 @@ const char* lilicorr_last_error(void);
 uint64_t lilicorr_launch_count(void);
 /* Read and clear the device-side error words of the current device (synchronises the
  * device): 0 = no error; otherwise one bit per wait site that gave up (bits 0-7 the logit
- * pass, bits 8-15 the tensor-core GEMM). */
+ * pass, bits 8-15 the tensor-core GEMM, bits 16-23 the tensor-core attention). */
 lilicorr_status lilicorr_device_error(uint32_t* code);
 
 /* Per-kernel timing.  When enabled, lilicorr_rerank records a CUDA event on its stream
