@@ -5,17 +5,20 @@
 //                     + [slot_i == slot_j] * same) v_j          (LiLiCorr App. A)
 // over all tokens of the block (bidirectional, no mask).
 //
-// One CTA per (block, head, 128-query tile), 10 warps:
+// Persistent: one CTA per SM walks the (block, head, 128-query tile) items, 10 warps:
 //   warp 0     TMA: Q (128 x 64), K and V (256 x 64), each as bf16 hi and lo, 128-byte
-//              swizzle; owns the TMEM allocation (S: 256 f32 columns, O: 64 columns)
+//              swizzle; the next item's Q and K load as soon as this item's S is formed,
+//              its V as soon as this item's second product is done; owns the TMEM
+//              allocation (S / P: 256 columns, O: 64 columns)
 //   warp 1     MMA: S = Qh Kh^T + Qh Kl^T + Ql Kh^T (M 128, N 256, K 64), then
-//              O = Ph Vh + Ph Vl + Pl Vh over all 256 keys (V read as an MN-major operand)
-//   warps 2-9  two warps per query row quarter, each taking half of the keys: pass 1
+//              O = Ph Vh + Ph Vl + Pl Vh with P read from TMEM and V as an MN-major
+//              shared-memory operand
+//   warps 2-9  two warps per query-row quarter, each taking half of the keys: pass 1
 //              scales, adds the slot bias (one table lookup), masks keys beyond the
 //              block, takes the row max (halves combined through shared memory) and
 //              writes the logits back to TMEM; pass 2 forms p = exp(s - max) and its sum
-//              and writes p as bf16 hi/lo into swizzled shared memory (over the finished
-//              Q and K tiles); the epilogue divides O by the sum and stores it split.
+//              and writes p as packed bf16 hi / lo over the logits it came from; the
+//              epilogue divides O by the sum and stores it split (hi | lo).
 // Every mbarrier wait is bounded; on a timeout the CTA records it and still frees TMEM.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -29,7 +32,7 @@ static __device__ uint32_t g_err_at;
 constexpr int AT_DH = 64, AT_QT = 128, AT_KMAX = 256, AT_SOFT_WARPS = 8;
 constexpr int AT_THREADS = 32 * (2 + AT_SOFT_WARPS);
 constexpr int AT_TILE = 128 * 64 * 2;  // one [128 x 64] bf16 swizzled tile
-constexpr int AT_SMEM = 12 * AT_TILE + 1024;
+constexpr int AT_SMEM = 10 * AT_TILE + 1024;
 constexpr uint32_t AT_TMEM_COLS = 512, AT_O_COL = 256;
 constexpr float AT_LOG2E = 1.4426950408889634f;
 
@@ -38,7 +41,10 @@ enum AtErr : uint32_t {
   ERR_AT_S = 1u << 1,
   ERR_AT_V = 1u << 2,
   ERR_AT_P = 1u << 3,
-  ERR_AT_O = 1u << 4
+  ERR_AT_O = 1u << 4,
+  ERR_AT_QKFREE = 1u << 5,
+  ERR_AT_VFREE = 1u << 6,
+  ERR_AT_OFREE = 1u << 7
 };
 
 __device__ __forceinline__ void at_tma(void* dst, const CUtensorMap* tm, int c0, int c1,
@@ -68,6 +74,15 @@ __device__ __forceinline__ void at_mma(uint32_t d, uint64_t a, uint64_t b, uint3
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
       "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+// A operand from TMEM (packed bf16 pairs, one row per lane), B from shared memory.
+__device__ __forceinline__ void at_mma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                          uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
       : "memory");
 }
 __device__ __forceinline__ void at_commit(uint64_t* bar) {
@@ -111,6 +126,15 @@ __device__ __forceinline__ void at_st32(uint32_t taddr, const float (&v)[32]) {
       : "memory");
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
+__device__ __forceinline__ void at_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+      "r"(v[15])
+      : "memory");
+}
 __device__ __forceinline__ float at_ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -132,8 +156,8 @@ __device__ __forceinline__ void soft_sync() {
 
 __global__ void __launch_bounds__(AT_THREADS, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm, int S, int Kc, int H, int B_max,
-                   const float* __restrict__ dist_bias, const float* __restrict__ same_bias,
-                   int64_t M, __nv_bfloat16* __restrict__ out) {
+                   int heads, int64_t batch, const float* __restrict__ dist_bias,
+                   const float* __restrict__ same_bias, __nv_bfloat16* __restrict__ out) {
   extern __shared__ uint8_t at_smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(at_smem_raw) + 1023) & ~uintptr_t(1023));
@@ -141,33 +165,32 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   uint8_t* sQl = sm + AT_TILE;
   uint8_t* sKh = sm + 2 * AT_TILE;   // K hi / lo: 2 tiles each (256 keys)
   uint8_t* sKl = sm + 4 * AT_TILE;
-  uint8_t* sVh = sm + 8 * AT_TILE;   // V hi / lo: 2 tiles each
-  uint8_t* sVl = sm + 10 * AT_TILE;
-  uint8_t* sPh = sm;                 // after S: P hi = 4 tiles of 64 keys, P lo = 4 tiles
-  uint8_t* sPl = sm + 4 * AT_TILE;
-  __shared__ __align__(8) uint64_t bar_qk, bar_v, bar_s, bar_p, bar_o;
+  uint8_t* sVh = sm + 6 * AT_TILE;   // V hi / lo: 2 tiles each
+  uint8_t* sVl = sm + 8 * AT_TILE;
+  __shared__ __align__(8) uint64_t bar_qk, bar_qkfree, bar_v, bar_vfree, bar_s, bar_p, bar_o,
+      bar_ofree;
   __shared__ uint32_t s_tmem;
-  __shared__ float s_bias[128];      // dist + same-slot bias by slot distance
-  __shared__ int s_kslot[AT_KMAX];
+  __shared__ float s_bias[128];      // dist + same-slot bias by slot distance, current head
+  __shared__ uint8_t s_kslot[AT_KMAX];
   __shared__ float s_pmax[2][128], s_psum[2][128];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int q0 = blockIdx.x * AT_QT, h = blockIdx.y;
-  const int64_t blk = blockIdx.z;
-  const int tok0 = static_cast<int>(blk * S);
+  const int QT = (S + AT_QT - 1) / AT_QT;
+  const int64_t nitems = batch * heads * QT;
   const int nd = 2 * B_max - 3;
 
   if (tid == 0) {
     mbar_init(&bar_qk, 1);
+    mbar_init(&bar_qkfree, 1);
     mbar_init(&bar_v, 1);
+    mbar_init(&bar_vfree, 1);
     mbar_init(&bar_s, 1);
     mbar_init(&bar_p, 32 * AT_SOFT_WARPS);
     mbar_init(&bar_o, 1);
+    mbar_init(&bar_ofree, 32 * AT_SOFT_WARPS);
     fence_mbar_init();
   }
-  for (int i = tid; i < nd; i += AT_THREADS)
-    s_bias[i] = dist_bias[h * nd + i] + (i == B_max - 2 ? same_bias[h] : 0.f);
-  for (int j = tid; j < AT_KMAX; j += AT_THREADS) s_kslot[j] = j < S ? j / Kc : 0;
+  for (int j = tid; j < AT_KMAX; j += AT_THREADS) s_kslot[j] = j < S ? uint8_t(j / Kc) : 0;
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_addr(&s_tmem)),
@@ -182,133 +205,165 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   const uint32_t tS = tmem, tO = tmem + AT_O_COL;
 
   if (warp == 0 && lane == 0) {
-    const int cq = h * AT_DH, ck = H + h * AT_DH, cv = 2 * H + h * AT_DH, lo = 3 * H;
-    mbar_arrive_expect_tx(&bar_qk, 6 * AT_TILE);
-    at_tma(sQh, &tm, cq, tok0 + q0, &bar_qk);
-    at_tma(sQl, &tm, lo + cq, tok0 + q0, &bar_qk);
-    at_tma(sKh, &tm, ck, tok0, &bar_qk);
-    at_tma(sKh + AT_TILE, &tm, ck, tok0 + 128, &bar_qk);
-    at_tma(sKl, &tm, lo + ck, tok0, &bar_qk);
-    at_tma(sKl + AT_TILE, &tm, lo + ck, tok0 + 128, &bar_qk);
-    mbar_arrive_expect_tx(&bar_v, 4 * AT_TILE);
-    at_tma(sVh, &tm, cv, tok0, &bar_v);
-    at_tma(sVh + AT_TILE, &tm, cv, tok0 + 128, &bar_v);
-    at_tma(sVl, &tm, lo + cv, tok0, &bar_v);
-    at_tma(sVl + AT_TILE, &tm, lo + cv, tok0 + 128, &bar_v);
+    // ---- producer
+    int i = 0;
+    for (int64_t t = blockIdx.x; t < nitems; t += gridDim.x, ++i) {
+      const int qt = static_cast<int>(t % QT);
+      const int h = static_cast<int>((t / QT) % heads);
+      const int tok0 = static_cast<int>((t / QT / heads) * S);
+      const int cq = h * AT_DH, ck = H + h * AT_DH, cv = 2 * H + h * AT_DH, lo = 3 * H;
+      if (i > 0 && !mbar_wait_bounded(&bar_qkfree, (i - 1) & 1, &g_err_at, ERR_AT_QKFREE)) break;
+      mbar_arrive_expect_tx(&bar_qk, 6 * AT_TILE);
+      at_tma(sQh, &tm, cq, tok0 + qt * AT_QT, &bar_qk);
+      at_tma(sQl, &tm, lo + cq, tok0 + qt * AT_QT, &bar_qk);
+      at_tma(sKh, &tm, ck, tok0, &bar_qk);
+      at_tma(sKh + AT_TILE, &tm, ck, tok0 + 128, &bar_qk);
+      at_tma(sKl, &tm, lo + ck, tok0, &bar_qk);
+      at_tma(sKl + AT_TILE, &tm, lo + ck, tok0 + 128, &bar_qk);
+      if (i > 0 && !mbar_wait_bounded(&bar_vfree, (i - 1) & 1, &g_err_at, ERR_AT_VFREE)) break;
+      mbar_arrive_expect_tx(&bar_v, 4 * AT_TILE);
+      at_tma(sVh, &tm, cv, tok0, &bar_v);
+      at_tma(sVh + AT_TILE, &tm, cv, tok0 + 128, &bar_v);
+      at_tma(sVl, &tm, lo + cv, tok0, &bar_v);
+      at_tma(sVl + AT_TILE, &tm, lo + cv, tok0 + 128, &bar_v);
+    }
   } else if (warp == 1 && lane == 0) {
+    // ---- MMA issuer
     constexpr uint32_t id_s = at_idesc(128, 256, false);
     constexpr uint32_t id_o = at_idesc(128, 64, true);
-    bool ok = mbar_wait_bounded(&bar_qk, 0, &g_err_at, ERR_AT_QK);
-    if (ok) {
-      at_fence_after();
+    int i = 0;
+    bool ok = true;
+    for (int64_t t = blockIdx.x; t < nitems && ok; t += gridDim.x, ++i) {
+      // S of this item overwrites the TMEM columns the previous item's second product
+      // read P from: start only once that product has completed.
+      ok = (i == 0 || mbar_wait_bounded(&bar_o, (i - 1) & 1, &g_err_at, ERR_AT_O)) &&
+           mbar_wait_bounded(&bar_qk, i & 1, &g_err_at, ERR_AT_QK);
+      if (ok) {
+        at_fence_after();
 #pragma unroll
-      for (int ks = 0; ks < AT_DH / 16; ++ks) {
-        at_mma(tS, at_desc(sQh + ks * 32), at_desc(sKh + ks * 32), id_s, ks > 0);
-        at_mma(tS, at_desc(sQh + ks * 32), at_desc(sKl + ks * 32), id_s, 1);
-        at_mma(tS, at_desc(sQl + ks * 32), at_desc(sKh + ks * 32), id_s, 1);
+        for (int ks = 0; ks < AT_DH / 16; ++ks) {
+          at_mma(tS, at_desc(sQh + ks * 32), at_desc(sKh + ks * 32), id_s, ks > 0);
+          at_mma(tS, at_desc(sQh + ks * 32), at_desc(sKl + ks * 32), id_s, 1);
+          at_mma(tS, at_desc(sQl + ks * 32), at_desc(sKh + ks * 32), id_s, 1);
+        }
       }
-    }
-    at_commit(&bar_s);
-    ok = ok && mbar_wait_bounded(&bar_v, 0, &g_err_at, ERR_AT_V) &&
-         mbar_wait_bounded(&bar_p, 0, &g_err_at, ERR_AT_P);
-    if (ok) {
-      at_fence_after();
+      at_commit(&bar_s);
+      at_commit(&bar_qkfree);
+      ok = ok && mbar_wait_bounded(&bar_p, i & 1, &g_err_at, ERR_AT_P) &&
+           mbar_wait_bounded(&bar_v, i & 1, &g_err_at, ERR_AT_V) &&
+           (i == 0 || mbar_wait_bounded(&bar_ofree, (i - 1) & 1, &g_err_at, ERR_AT_OFREE));
+      if (ok) {
+        at_fence_after();
+        // P for keys 32c..32c+31 sits in TMEM columns 32c (hi, 16 packed columns) and
+        // 32c + 16 (lo); a 16-key step j uses 8 of them.
 #pragma unroll 4
-      for (int j = 0; j < AT_KMAX / 16; ++j) {
-        const int kt = j >> 2, off = (j & 3) * 32;
-        const uint8_t* ph = sPh + kt * AT_TILE + off;
-        const uint8_t* pl = sPl + kt * AT_TILE + off;
-        at_mma(tO, at_desc(ph), at_desc(sVh + 16 * j * 128), id_o, j > 0);
-        at_mma(tO, at_desc(ph), at_desc(sVl + 16 * j * 128), id_o, 1);
-        at_mma(tO, at_desc(pl), at_desc(sVh + 16 * j * 128), id_o, 1);
+        for (int j = 0; j < AT_KMAX / 16; ++j) {
+          const uint32_t pc = uint32_t(32 * (j >> 1) + 8 * (j & 1));
+          const uint64_t vh = at_desc(sVh + 16 * j * 128), vl = at_desc(sVl + 16 * j * 128);
+          at_mma_ts(tO, tS + pc, vh, id_o, j > 0);
+          at_mma_ts(tO, tS + pc, vl, id_o, 1);
+          at_mma_ts(tO, tS + pc + 16, vh, id_o, 1);
+        }
       }
+      at_commit(&bar_o);
+      at_commit(&bar_vfree);
     }
-    at_commit(&bar_o);
   } else if (warp >= 2) {
+    // ---- softmax and epilogue
     const int qq = warp & 3, hf = (warp - 2) >> 2;
     const int r = 32 * qq + lane;  // TMEM lane = query row of the tile
-    const int i = q0 + r;
-    const int boff = B_max - 2 - min(i, S - 1) / Kc;  // bias index = slot_j + boff
     const uint32_t lane_off = uint32_t(32 * qq) << 16;
-    const int j0 = 128 * hf;         // this warp's keys j0 .. j0 + 127
-    float mx = -INFINITY;
-    bool ok = mbar_wait_bounded(&bar_s, 0, &g_err_at, ERR_AT_S);
-    at_fence_after();
-    // pass 1: logits with bias and mask, partial row max, written back
+    const int j0 = 128 * hf;       // this warp's keys j0 .. j0 + 127
+    int i = 0;
+    int cur_h = -1;
+    for (int64_t t = blockIdx.x; t < nitems; t += gridDim.x, ++i) {
+      const int qt = static_cast<int>(t % QT);
+      const int h = static_cast<int>((t / QT) % heads);
+      const int64_t tok0 = (t / QT / heads) * S;
+      const int q = qt * AT_QT + r;
+      const int boff = B_max - 2 - min(q, S - 1) / Kc;  // bias index = slot_j + boff
+      if (h != cur_h) {  // bias table of this head (all softmax warps take the same items)
+        soft_sync();
+        for (int k = tid - 64; k < nd; k += 32 * AT_SOFT_WARPS)
+          s_bias[k] = dist_bias[h * nd + k] + (k == B_max - 2 ? same_bias[h] : 0.f);
+        soft_sync();
+        cur_h = h;
+      }
+      bool ok = mbar_wait_bounded(&bar_s, i & 1, &g_err_at, ERR_AT_S);
+      at_fence_after();
+      // pass 1: logits with bias and mask, partial row max, written back
+      float mx = -INFINITY;
 #pragma unroll 1
-    for (int cc = 0; cc < 4; ++cc) {
-      const int jb = j0 + 32 * cc;
-      float v[32];
-      at_ld32(tS + lane_off + jb, v);
+      for (int cc = 0; cc < 4; ++cc) {
+        const int jb = j0 + 32 * cc;
+        float v[32];
+        at_ld32(tS + lane_off + jb, v);
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const float x = jb + e < S ? fmaf(v[e], 0.125f, s_bias[s_kslot[jb + e] + boff]) : -INFINITY;
-        v[e] = x;
-        mx = fmaxf(mx, x);
+        for (int e = 0; e < 32; ++e) {
+          const float x =
+              jb + e < S ? fmaf(v[e], 0.125f, s_bias[s_kslot[jb + e] + boff]) : -INFINITY;
+          v[e] = x;
+          mx = fmaxf(mx, x);
+        }
+        at_st32(tS + lane_off + jb, v);
       }
-      at_st32(tS + lane_off + jb, v);
-    }
-    s_pmax[hf][r] = mx;
-    soft_sync();
-    mx = fmaxf(s_pmax[0][r], s_pmax[1][r]);
-    // pass 2: p = exp(s - max), partial sum, p as bf16 hi/lo into the P tiles
-    const float m2 = mx * AT_LOG2E;
-    float l = 0.f;
+      s_pmax[hf][r] = mx;
+      soft_sync();
+      mx = fmaxf(s_pmax[0][r], s_pmax[1][r]);
+      // pass 2: p = exp(s - max) and its sum; p as packed bf16 hi / lo over its logits
+      const float m2 = mx * AT_LOG2E;
+      float l = 0.f;
 #pragma unroll 1
-    for (int cc = 0; cc < 4; ++cc) {
-      const int jb = j0 + 32 * cc;
+      for (int cc = 0; cc < 4; ++cc) {
+        const int jb = j0 + 32 * cc;
+        float v[32];
+        at_ld32(tS + lane_off + jb, v);
+        uint32_t ph[16], pl[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const float pa = at_ex2(fmaf(v[e], AT_LOG2E, -m2));
+          const float pb = at_ex2(fmaf(v[e + 1], AT_LOG2E, -m2));
+          l += pa + pb;
+          __nv_bfloat16 ha, la, hb, lb;
+          split_bf16(pa, ha, la);
+          split_bf16(pb, hb, lb);
+          ph[e / 2] = at_pack(ha, hb);
+          pl[e / 2] = at_pack(la, lb);
+        }
+        at_st16(tS + lane_off + jb, ph);
+        at_st16(tS + lane_off + jb + 16, pl);
+      }
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+      s_psum[hf][r] = l;
+      at_fence_before();
+      mbar_arrive(&bar_p);
+      soft_sync();
+      const float inv = 1.0f / (s_psum[0][r] + s_psum[1][r]);
+      // epilogue: O / l for this warp's 32 of the 64 output columns, split, stored
+      ok = mbar_wait_bounded(&bar_o, i & 1, &g_err_at, ERR_AT_O) && ok;
+      at_fence_after();
       float v[32];
-      at_ld32(tS + lane_off + jb, v);
-      uint32_t ph[16], pl[16];
+      at_ld32(tO + lane_off + 32 * hf, v);
+      at_fence_before();
+      mbar_arrive(&bar_ofree);
+      if (q < S && ok) {
+        __nv_bfloat16* dst = out + (tok0 + q) * 2 * H + h * AT_DH + 32 * hf;
+        uint32_t hi[16], lo[16];
 #pragma unroll
-      for (int e = 0; e < 32; e += 2) {
-        const float pa = at_ex2(fmaf(v[e], AT_LOG2E, -m2));
-        const float pb = at_ex2(fmaf(v[e + 1], AT_LOG2E, -m2));
-        l += pa + pb;
-        __nv_bfloat16 ha, la, hb, lb;
-        split_bf16(pa, ha, la);
-        split_bf16(pb, hb, lb);
-        ph[e / 2] = at_pack(ha, hb);
-        pl[e / 2] = at_pack(la, lb);
-      }
-      // keys jb..jb+31: tile kt = jb / 64, 16-byte chunks 4 * ((jb / 32) & 1) + u
-      const int kt = jb >> 6;
+        for (int e = 0; e < 32; e += 2) {
+          __nv_bfloat16 ha, la, hb, lb;
+          split_bf16(v[e] * inv, ha, la);
+          split_bf16(v[e + 1] * inv, hb, lb);
+          hi[e / 2] = at_pack(ha, hb);
+          lo[e / 2] = at_pack(la, lb);
+        }
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int ch = 4 * ((jb >> 5) & 1) + u;
-        const int off = kt * AT_TILE + r * 128 + ((ch ^ (r & 7)) << 4);
-        *reinterpret_cast<uint4*>(sPh + off) =
-            make_uint4(ph[4 * u], ph[4 * u + 1], ph[4 * u + 2], ph[4 * u + 3]);
-        *reinterpret_cast<uint4*>(sPl + off) =
-            make_uint4(pl[4 * u], pl[4 * u + 1], pl[4 * u + 2], pl[4 * u + 3]);
-      }
-    }
-    s_psum[hf][r] = l;
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    at_fence_before();
-    mbar_arrive(&bar_p);
-    soft_sync();
-    const float inv = 1.0f / (s_psum[0][r] + s_psum[1][r]);
-    // epilogue: O / l for this warp's 32 of the 64 output columns, split, stored
-    ok = mbar_wait_bounded(&bar_o, 0, &g_err_at, ERR_AT_O) && ok;
-    at_fence_after();
-    float v[32];
-    at_ld32(tO + lane_off + 32 * hf, v);
-    if (i < S && ok) {
-      __nv_bfloat16* dst = out + (int64_t(tok0) + i) * 2 * H + h * AT_DH + 32 * hf;
-      uint32_t hi[16], lo[16];
-#pragma unroll
-      for (int e = 0; e < 32; e += 2) {
-        __nv_bfloat16 ha, la, hb, lb;
-        split_bf16(v[e] * inv, ha, la);
-        split_bf16(v[e + 1] * inv, hb, lb);
-        hi[e / 2] = at_pack(ha, hb);
-        lo[e / 2] = at_pack(la, lb);
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        *reinterpret_cast<uint4*>(dst + 8 * u) = make_uint4(hi[4 * u], hi[4 * u + 1], hi[4 * u + 2], hi[4 * u + 3]);
-        *reinterpret_cast<uint4*>(dst + H + 8 * u) = make_uint4(lo[4 * u], lo[4 * u + 1], lo[4 * u + 2], lo[4 * u + 3]);
+        for (int u = 0; u < 4; ++u) {
+          *reinterpret_cast<uint4*>(dst + 8 * u) =
+              make_uint4(hi[4 * u], hi[4 * u + 1], hi[4 * u + 2], hi[4 * u + 3]);
+          *reinterpret_cast<uint4*>(dst + H + 8 * u) =
+              make_uint4(lo[4 * u], lo[4 * u + 1], lo[4 * u + 2], lo[4 * u + 3]);
+        }
       }
     }
   }
@@ -337,8 +392,8 @@ static PFN_cuTensorMapEncodeTiled_v12000 at_encode_fn() {
   return fn;
 }
 
-bool attention_tc_supported(int S, int H, int heads) {
-  return H / heads == AT_DH && S >= 1 && S <= AT_KMAX && H % 64 == 0;
+bool attention_tc_supported(int S, int H, int heads, int B_max) {
+  return H / heads == AT_DH && S >= 1 && S <= AT_KMAX && H % 64 == 0 && B_max <= 64;
 }
 
 cudaError_t launch_attention_tc(const __nv_bfloat16* qkv, int64_t batch, int S, int K, int H,
@@ -346,7 +401,7 @@ cudaError_t launch_attention_tc(const __nv_bfloat16* qkv, int64_t batch, int S, 
                                 const float* same_bias, __nv_bfloat16* out,
                                 cudaStream_t stream) {
   auto fn = at_encode_fn();
-  if (!fn || !attention_tc_supported(S, H, heads)) return cudaErrorInvalidValue;
+  if (!fn || !attention_tc_supported(S, H, heads, B_max)) return cudaErrorInvalidValue;
   const int64_t M = batch * S;
   CUtensorMap tm;
   const cuuint64_t dims[2] = {cuuint64_t(6 * H), cuuint64_t(M)};
@@ -362,9 +417,17 @@ cudaError_t launch_attention_tc(const __nv_bfloat16* qkv, int64_t batch, int S, 
     cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, AT_SMEM);
     attr = true;
   }
-  const dim3 grid((S + AT_QT - 1) / AT_QT, heads, static_cast<unsigned>(batch));
-  attn_tc_kernel<<<grid, AT_THREADS, AT_SMEM, stream>>>(tm, S, K, H, B_max, dist_bias,
-                                                        same_bias, M, out);
+  static int sms = 0;
+  if (!sms) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (sms <= 0) sms = 148;
+  }
+  const int64_t nitems = batch * heads * ((S + AT_QT - 1) / AT_QT);
+  const dim3 grid(static_cast<unsigned>(nitems < sms ? nitems : sms));
+  attn_tc_kernel<<<grid, AT_THREADS, AT_SMEM, stream>>>(tm, S, K, H, B_max, heads, batch,
+                                                        dist_bias, same_bias, out);
   note_launch();
   return cudaGetLastError();
 }
