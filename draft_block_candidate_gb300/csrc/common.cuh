@@ -17,6 +17,7 @@ constexpr unsigned FULL_MASK = 0xffffffffu;
 enum ErrSite : uint32_t {
   ERR_K1_FULL_WAIT = 1u << 0,
   ERR_K1_DRAIN = 1u << 1,
+  ERR_K1_EMPTY_WAIT = 1u << 2,
 };
 
 // About one second at GB300 clocks: any wait longer than this is treated as a failure.
@@ -49,6 +50,19 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
       : "memory");
 }
 
+// Non-blocking probe: has the phase with this parity completed?
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -67,13 +81,13 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
                                                   uint32_t* err_word, uint32_t site) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
-  while (!mbar_try_wait(bar, parity)) {
-    if (clock64() - t0 > WAIT_LIMIT_CYCLES) {
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((n & 63) == 0 && clock64() - t0 > WAIT_LIMIT_CYCLES) {
       atomicOr(err_word, site);
       return false;
     }
   }
-  return true;
 }
 
 // L2 policy for data read exactly once.

@@ -11,15 +11,24 @@
 //
 // GB300 design.  The pass is HBM-bound (one streaming read of batch*(B-1)*V elements), so
 // each CTA streams a contiguous segment of one row through shared memory with 1-D bulk
-// copies (cp.async.bulk, 16 KB stages, 3 in flight, 3 CTAs per SM) and every thread
-// consumes 16-byte chunks:
-//   * online log-sum-exp in base 2: per chunk one max, one FFMA + ex2 per element;
-//   * top-K: warp 0 keeps the running top-32 (value, id) pairs sorted across its lanes.
-//     Every thread compares its elements with the running K-th entry (floored in the
-//     first stage by the K-th largest per-thread maximum, a valid lower bound), so after
-//     warm-up almost every element costs one compare; the rare survivors go to a shared
-//     buffer that warp 0 folds in 32 at a time (warp bitonic sort + bitonic merge)
-//     during the next stage.
+// copies (cp.async.bulk, 32 KB stages, 3 in flight, 2 CTAs per SM).  A producer warp
+// refills a ring slot as soon as the 16 consumer warps have each released it (an
+// mbarrier per slot; no CTA-wide barrier while streaming).  Every consumer thread takes
+// four 16-byte chunks per stage:
+//   * online log-sum-exp in base 2: per chunk one 3-input max tree, then packed f32x2
+//     FFMA / FADD around one ex2 per element (two partial sums per thread);
+//   * top-K: each consumer warp keeps its own running top-32 (value, id) pairs, sorted
+//     across its lanes.  After a stage, each thread compares its chunk maxima with the
+//     warp's threshold, the better of its own K-th entry and a CTA-wide floor; one vote
+//     skips the rest in the common case.  Only a hit re-reads its chunk from shared
+//     memory and appends the elements that can still enter to the warp's buffer, which
+//     is folded in 32 at a time (warp bitonic sort + bitonic merge).
+//   * the CTA floor is the K-th largest of 32 thread-group running maxima (K distinct
+//     elements are at least that large), kept fresh by the producer warp while it waits
+//     and raised by every warp's own K-th entry.  Stage 0 is checked one stage late, when
+//     the group maxima already cover it.
+// At the end the 17 warp queues (the producer's holds the unaligned head and tail) are
+// merged in a tree.
 // Rows are split into P segments when there are too few rows to fill 152 SMs; the last
 // CTA of a row (atomic counter, no waiting) merges the P partial results.
 #include <float.h>
@@ -36,11 +45,24 @@ namespace lilicorr {
 
 static __device__ uint32_t g_err_k1;
 
-constexpr int K1_THREADS = 512;
-constexpr int K1_WARPS = K1_THREADS / 32;
-constexpr int K1_STAGE_BYTES = 16384;
-constexpr int K1_NSTAGES = 4;
-constexpr int K1_CPT = K1_STAGE_BYTES / 16 / K1_THREADS;  // 16-byte chunks per thread per stage
+constexpr int K1_CWARPS = 16;                      // consumer warps
+constexpr int K1_CTHREADS = 32 * K1_CWARPS;
+constexpr int K1_THREADS = K1_CTHREADS + 32;       // + one producer warp
+#ifndef K1_MIN_BLOCKS
+#define K1_MIN_BLOCKS 2
+#endif
+#ifndef K1_STAGE_KB
+#define K1_STAGE_KB 32
+#endif
+#ifndef K1_POLL_NS
+#define K1_POLL_NS 64
+#endif
+constexpr int K1_STAGE_BYTES = K1_STAGE_KB * 1024;
+#ifndef K1_NST
+#define K1_NST 3
+#endif
+constexpr int K1_NSTAGES = K1_NST;
+constexpr int K1_CPT = K1_STAGE_BYTES / 16 / K1_CTHREADS;  // 16-byte chunks per consumer per stage
 constexpr int KQ = 32;                                      // queue slots per warp
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float M2_INIT = -1e30f;                           // "no element yet", finite
@@ -146,18 +168,6 @@ __device__ __forceinline__ float warp_sort_desc(float v, int lane) {
   return v;
 }
 
-constexpr int K1_CAP = 256;  // candidate buffer entries per CTA and stage parity
-
-// The running K-th entry (value, id) shared as one 64-bit word, so a reader never sees
-// the value of one update with the id of another.
-__device__ __forceinline__ unsigned long long pack_tau(float v, int id) {
-  return (static_cast<unsigned long long>(__float_as_uint(v)) << 32) | static_cast<uint32_t>(id);
-}
-__device__ __forceinline__ void unpack_tau(unsigned long long w, float& v, int& id) {
-  v = __uint_as_float(static_cast<uint32_t>(w >> 32));
-  id = static_cast<int>(static_cast<uint32_t>(w));
-}
-
 // Sort one (value, id) pair per lane across the warp into (value desc, id asc) order
 // (bitonic network, 15 compare-exchange steps).
 __device__ __forceinline__ void warp_sort_pairs(float& v, int& id, int lane) {
@@ -178,36 +188,14 @@ __device__ __forceinline__ void warp_sort_pairs(float& v, int& id, int lane) {
 }
 
 // Warp-uniform: fold one candidate per lane (sentinel -inf / INT_MAX for none) into the
-// sorted 32-entry queue q, 32 candidates at a time: sort them, bitonic-merge, keep the
-// best 32.  Skipped when no lane beats the queue's K-th entry.
+// sorted 32-entry queue q: sort the 32 candidates, bitonic-merge, keep the best 32.
+// Skipped when no lane beats the queue's K-th entry.
 __device__ __forceinline__ void queue_absorb(WarpQueue& q, float v, int id, int lane, int K) {
   if (!__any_sync(FULL_MASK, better(v, id, q.tv, q.tid))) return;
   warp_sort_pairs(v, id, lane);
   bitonic_merge(q.qv, q.qid, v, id, lane);
   q.tv = __shfl_sync(FULL_MASK, q.qv, K - 1);
   q.tid = __shfl_sync(FULL_MASK, q.qid, K - 1);
-}
-
-// Warp-uniform: fold the buffered candidates into the running queue, publish its K-th
-// entry, empty the buffer.
-__device__ __forceinline__ void merge_buffer(WarpQueue& run, const float* bv, const int* bi,
-                                             int* cnt_p, volatile unsigned long long* tau,
-                                             int lane, int K) {
-  const int cnt = min(*cnt_p, K1_CAP);
-  for (int c0 = 0; c0 < cnt; c0 += 32) {
-    float v = -INFINITY;
-    int vi = INT_MAX;
-    if (c0 + lane < cnt) {
-      v = bv[c0 + lane];
-      vi = bi[c0 + lane];
-    }
-    queue_absorb(run, v, vi, lane, K);
-  }
-  __syncwarp();
-  if (lane == 0) {
-    *tau = pack_tau(run.tv, run.tid);
-    *cnt_p = 0;
-  }
 }
 
 // Unpack one 16-byte chunk (8 bf16 or 4 f32) into floats.
@@ -228,37 +216,67 @@ __device__ __forceinline__ void unpack16(const uint4 w, float (&x)[NV]) {
   }
 }
 
-// Append this chunk's elements that can still enter the top-K to the stage buffer.
+constexpr int K1_WCAP = 64;    // per-warp candidate buffer entries
+constexpr int K1_GROUPS = 32;  // thread groups whose running maxima give the CTA floor
+constexpr int K1_GSIZE = K1_CTHREADS / K1_GROUPS;
+
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// Consumer-side log-sum-exp of one 16-byte chunk; returns the chunk maximum.  The sum is
+// kept as two partial sums (even / odd elements) updated with packed f32x2 arithmetic.
+// When the thread's running maximum rises (the rescale branch), it is offered to its
+// group's maximum in shared memory.
 template <int NV>
-__device__ __forceinline__ void append_chunk(const float (&x)[NV], int id0, float thr, float tv,
-                                             int ti, float* bv, int* bi, int* cnt) {
+__device__ __forceinline__ float lse_chunk_g(const float (&x)[NV], float& m2, float2& s2,
+                                             int* gmax) {
+  float cm;
+  if constexpr (NV == 8)
+    cm = fmaxf(max3f(x[0], x[1], x[2]), max3f(x[3], x[4], max3f(x[5], x[6], x[7])));
+  else
+    cm = fmaxf(max3f(x[0], x[1], x[2]), x[3]);
+  const float cm2 = cm * LOG2E;
+  if (cm2 > m2) {
+    const float sc = ex2(m2 - cm2);
+    s2 = __fmul2_rn(s2, make_float2(sc, sc));
+    m2 = cm2;
+    atomicMax(gmax, float_key(cm));
+  }
+  const float2 l2 = make_float2(LOG2E, LOG2E);
+  const float2 nm = make_float2(-m2, -m2);
 #pragma unroll
-  for (int j = 0; j < NV; ++j)
-    if (x[j] >= thr && better(x[j], id0 + j, tv, ti)) {
-      const int idx = atomicAdd(cnt, 1);
-      if (idx < K1_CAP) {
-        bv[idx] = x[j];
-        bi[idx] = id0 + j;
-      }
-    }
+  for (int j = 0; j < NV; j += 2) {
+    const float2 y = __ffma2_rn(make_float2(x[j], x[j + 1]), l2, nm);
+    s2 = __fadd2_rn(s2, make_float2(ex2(y.x), ex2(y.y)));
+  }
+  return cm;
+}
+
+// Warp-uniform: the K-th largest of the 32 group maxima.  Each group's maximum is an
+// element of a distinct set of threads, so K elements of the segment are at least this
+// large: a valid inclusive floor for the K-th largest value.
+__device__ __forceinline__ float group_floor(const int* gmax, int lane, int K) {
+  const float g = key_float(*reinterpret_cast<const volatile int*>(&gmax[lane]));
+  return __shfl_sync(FULL_MASK, warp_sort_desc(g, lane), K - 1);
 }
 
 template <typename T>
-__global__ void __launch_bounds__(K1_THREADS, 3) logit_pass_kernel(const K1Params p) {
+__global__ void __launch_bounds__(K1_THREADS, K1_MIN_BLOCKS) logit_pass_kernel(const K1Params p) {
   constexpr int ES = sizeof(T);
   constexpr int NV = 16 / ES;
   extern __shared__ __align__(128) uint8_t k1_dyn_smem[];
   uint8_t(*stage)[K1_STAGE_BYTES] = reinterpret_cast<uint8_t(*)[K1_STAGE_BYTES]>(k1_dyn_smem);
-  __shared__ __align__(8) uint64_t full_bar[K1_NSTAGES];
-  __shared__ float sq_v[K1_WARPS][KQ];
-  __shared__ int sq_i[K1_WARPS][KQ];
-  __shared__ float s_buf_v[2][K1_CAP];
-  __shared__ int s_buf_i[2][K1_CAP];
-  __shared__ float s_m2[K1_WARPS], s_s[K1_WARPS];
-  __shared__ float s_L0;
+  __shared__ __align__(8) uint64_t full_bar[K1_NSTAGES], empty_bar[K1_NSTAGES];
+  __shared__ float s_bv[K1_CWARPS + 1][K1_WCAP];  // per-warp candidates, then the queues
+  __shared__ int s_bi[K1_CWARPS + 1][K1_WCAP];
+  __shared__ int s_wcnt[K1_CWARPS];
+  __shared__ int s_gmax[K1_GROUPS];  // float_key of each thread group's running maximum
+  __shared__ int s_floor;            // float_key of the CTA floor (atomic max)
+  __shared__ float s_m2[K1_CWARPS + 1], s_s[K1_CWARPS + 1];
   __shared__ int s_abort;
-  __shared__ int s_cnt[2];
-  __shared__ volatile unsigned long long s_tau;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int K = p.K;
@@ -282,31 +300,36 @@ __global__ void __launch_bounds__(K1_THREADS, 3) logit_pass_kernel(const K1Param
   const int seg_elem0 = static_cast<int>((seg_lo - row_start) / ES);  // id of first body elem
 
   if (tid == 0) {
-    for (int i = 0; i < K1_NSTAGES; ++i) mbar_init(&full_bar[i], 1);
+    for (int i = 0; i < K1_NSTAGES; ++i) {
+      mbar_init(&full_bar[i], 1);
+      mbar_init(&empty_bar[i], K1_CWARPS);
+    }
     fence_mbar_init();
-    s_cnt[0] = s_cnt[1] = 0;
     s_abort = 0;
-    s_tau = pack_tau(-INFINITY, INT_MAX);
+    s_floor = float_key(-INFINITY);
   }
+  if (tid < K1_GROUPS) s_gmax[tid] = float_key(-INFINITY);
+  if (tid < K1_CWARPS) s_wcnt[tid] = 0;
   __syncthreads();
 
-  if (tid == 0)
-    for (int st = 0; st < min(K1_NSTAGES - 1, nstages); ++st) {
-      const int off = st * K1_STAGE_BYTES;
-      const uint32_t bytes = static_cast<uint32_t>(min(K1_STAGE_BYTES, seg_bytes - off));
-      mbar_arrive_expect_tx(&full_bar[st], bytes);
-      bulk_g2s(stage[st], p.logits + seg_lo + off, bytes, &full_bar[st]);
-    }
-
   float m2 = M2_INIT, ssum = 0.f;
-  // Warp 0 owns the running top-32 of everything consumed so far (one entry per lane,
-  // sorted); the other warps see its K-th entry through s_tau.
-  WarpQueue run;
-  run.init();
+  WarpQueue q;  // this warp's running top-32 (one entry per lane, sorted)
+  q.init();
+  int issued = 0;  // copies issued (producer warp, lane 0)
 
-  // Unaligned head (segment 0) and tail (last segment) elements: plain loads by warp 0,
-  // one element per lane, straight into the running queue.
-  if (warp == 0) {
+  if (warp == K1_CWARPS) {
+    // ================= producer warp =================
+    auto issue = [&](int st) {
+      const int off = st * K1_STAGE_BYTES;
+      const int sl = st % K1_NSTAGES;
+      const uint32_t bytes = static_cast<uint32_t>(min(K1_STAGE_BYTES, seg_bytes - off));
+      mbar_arrive_expect_tx(&full_bar[sl], bytes);
+      bulk_g2s(stage[sl], p.logits + seg_lo + off, bytes, &full_bar[sl]);
+      issued = st + 1;
+    };
+    if (lane == 0)
+      for (int st = 0; st < min(K1_NSTAGES, nstages); ++st) issue(st);
+    // Unaligned head (segment 0) and tail (last segment): one element per lane.
     const int64_t row_elem0 = row_start / ES;
     for (int part = 0; part < 2; ++part) {
       int64_t first = 0;
@@ -321,187 +344,222 @@ __global__ void __launch_bounds__(K1_THREADS, 3) logit_pass_kernel(const K1Param
       if (cnt == 0) continue;  // warp-uniform
       const bool has = lane < cnt;
       const float xv = has ? load_elem<T>(p.logits + first + int64_t(lane) * ES) : -INFINITY;
-      if (has) {
-        const float c2 = xv * LOG2E;
-        if (c2 > m2) {
-          ssum *= ex2(m2 - c2);
-          m2 = c2;
-        }
-        ssum += ex2(fmaf(xv, LOG2E, -m2));
-      }
-      queue_absorb(run, xv, has ? static_cast<int>(first / ES - row_elem0) + lane : INT_MAX, lane,
+      if (has) lse_merge(m2, ssum, xv * LOG2E, 1.0f);
+      queue_absorb(q, xv, has ? static_cast<int>(first / ES - row_elem0) + lane : INT_MAX, lane,
                    K);
     }
-    if (lane == 0) s_tau = pack_tau(run.tv, run.tid);
-  }
-
-  float L0 = -INFINITY;  // lower bound of the segment's K-th largest value (from stage 0)
-  bool ok = true;
-  for (int st = 0; st < nstages; ++st) {
-    const int slot = st % K1_NSTAGES;
-    if (tid == 0 && st + K1_NSTAGES - 1 < nstages) {
-      const int nx = st + K1_NSTAGES - 1, ns = nx % K1_NSTAGES;
-      const int off = nx * K1_STAGE_BYTES;
-      const uint32_t bytes = static_cast<uint32_t>(min(K1_STAGE_BYTES, seg_bytes - off));
-      mbar_arrive_expect_tx(&full_bar[ns], bytes);
-      bulk_g2s(stage[ns], p.logits + seg_lo + off, bytes, &full_bar[ns]);
-    }
-    if (!mbar_wait_bounded(&full_bar[slot], (st / K1_NSTAGES) & 1, &g_err_k1, ERR_K1_FULL_WAIT))
-      s_abort = 1;
-    const int soff = st * K1_STAGE_BYTES;
-    const int nbytes = min(K1_STAGE_BYTES, seg_bytes - soff);
-    const uint8_t* sbuf = stage[slot];
-    const int bsel = st & 1;
-    float* bv = s_buf_v[bsel];
-    int* bi = s_buf_i[bsel];
-    // the running K-th entry; warp 0 may raise it concurrently, either value is valid
-    // (stage 0 re-reads it below, after barriers that order warp 0's head/tail update)
-    float tv;
-    int ti;
-    unpack_tau(s_tau, tv, ti);
-    const float thr = fmaxf(tv, L0);
-
-    // ---- one 16-byte chunk at a time: log-sum-exp, then the (rare) candidate check
-    float tmax = -INFINITY;
-#pragma unroll
-    for (int i = 0; i < K1_CPT; ++i) {
-      const int c = tid + i * K1_THREADS;
-      if (c * 16 < nbytes) {
-        float x[NV];
-        unpack16<NV>(*reinterpret_cast<const uint4*>(sbuf + c * 16), x);
-        float cm = x[0];
-#pragma unroll
-        for (int j = 1; j < NV; ++j) cm = fmaxf(cm, x[j]);
-        const float cm2 = cm * LOG2E;
-        if (cm2 > m2) {
-          ssum *= ex2(m2 - cm2);
-          m2 = cm2;
+    // Refill each slot as soon as every consumer warp has released it; while waiting,
+    // keep the CTA floor fresh from the group maxima.
+    for (int st = K1_NSTAGES; st < nstages; ++st) {
+      const int sl = st % K1_NSTAGES;
+      const uint32_t par = ((st / K1_NSTAGES) - 1) & 1;
+      const long long t0 = clock64();
+      int ready = 0;
+      for (;;) {
+        if (lane == 0) {
+          if (mbar_test_wait(&empty_bar[sl], par)) {
+            ready = 1;
+          } else if (s_abort) {
+            ready = 2;
+          } else if (clock64() - t0 > WAIT_LIMIT_CYCLES) {
+            atomicOr(&g_err_k1, ERR_K1_EMPTY_WAIT);
+            s_abort = 1;
+            ready = 2;
+          }
         }
-#pragma unroll
-        for (int j = 0; j < NV; ++j) ssum += ex2(fmaf(x[j], LOG2E, -m2));
-        tmax = fmaxf(tmax, cm);
-        if (st > 0 && cm >= thr)
-          append_chunk<NV>(x, seg_elem0 + (soff + c * 16) / ES, thr, tv, ti, bv, bi, &s_cnt[bsel]);
+        ready = __shfl_sync(FULL_MASK, ready, 0);
+        if (ready != 0) break;
+        const float f = group_floor(s_gmax, lane, K);
+        if (lane == 0) atomicMax(&s_floor, float_key(f));
+        __nanosleep(K1_POLL_NS);
       }
+      if (ready == 2) break;
+      if (lane == 0) issue(st);
     }
+  } else {
+    // ================= consumer warps =================
+    float* bv = s_bv[warp];
+    int* bi = s_bi[warp];
+    int* gmax = &s_gmax[tid / K1_GSIZE];
+    int* wcnt = &s_wcnt[warp];
+    float2 s2 = make_float2(0.f, 0.f);  // partial sums of this thread's exponentials
+    float cm0[K1_CPT];  // stage 0, checked one stage late against a CTA floor
+    unsigned valid0 = 0;
 
-    // ---- stage 0: floor L0 = the K-th largest per-thread maximum (K distinct threads
-    // hold an element at least that large), then this stage's candidates.
-    if (st == 0) {
-      sq_v[warp][lane] = warp_sort_desc(tmax, lane);
-      __syncthreads();
-      for (int half = K1_WARPS / 2; half >= 1; half >>= 1) {
-        if (warp < half) {
-          float a = sq_v[warp][lane];
-          int ai = 0;
-          bitonic_merge(a, ai, sq_v[warp + half][lane], 0, lane);
-          __syncwarp();
-          sq_v[warp][lane] = a;
-        }
-        __syncthreads();
+    // Candidates of stage st (chunk maxima cmx, validity bits vmask): compare with the
+    // threshold, re-read hit chunks from the slot, append to the warp buffer, fold.
+    auto check_stage = [&](int st, const float (&cmx)[K1_CPT], unsigned vmask) {
+      const int sl = st % K1_NSTAGES;
+      const int soff = st * K1_STAGE_BYTES;
+      const uint8_t* sbuf = stage[sl];
+      const float fl = key_float(*reinterpret_cast<volatile int*>(&s_floor));
+      float tv = q.tv;
+      int ti = q.tid;
+      if (fl > tv) {
+        tv = fl;
+        ti = INT_MAX;
       }
-      if (tid == 0) s_L0 = sq_v[0][K - 1];
-      __syncthreads();
-      L0 = s_L0;
-      unpack_tau(s_tau, tv, ti);
-      const float thr0 = fmaxf(tv, L0);
-      if (tmax >= thr0) {
+      bool hit = false;
+#pragma unroll
+      for (int i = 0; i < K1_CPT; ++i) hit |= ((vmask >> i) & 1u) && cmx[i] >= tv;
+      if (__any_sync(FULL_MASK, hit)) {
+        const int prev = *reinterpret_cast<volatile int*>(wcnt);
+        __syncwarp();
 #pragma unroll
         for (int i = 0; i < K1_CPT; ++i) {
-          const int c = tid + i * K1_THREADS;
-          if (c * 16 < nbytes) {
+          if (((vmask >> i) & 1u) && cmx[i] >= tv) {
+            const int c = tid + i * K1_CTHREADS;
             float x[NV];
             unpack16<NV>(*reinterpret_cast<const uint4*>(sbuf + c * 16), x);
-            append_chunk<NV>(x, seg_elem0 + (soff + c * 16) / ES, thr0, tv, ti, bv, bi,
-                             &s_cnt[bsel]);
+            const int id0 = seg_elem0 + (soff + c * 16) / ES;
+#pragma unroll
+            for (int j = 0; j < NV; ++j)
+              if (better(x[j], id0 + j, tv, ti)) {
+                const int idx = atomicAdd(wcnt, 1);
+                if (idx < K1_WCAP) {
+                  bv[idx] = x[j];
+                  bi[idx] = id0 + j;
+                }
+              }
+          }
+        }
+        __syncwarp();
+        int cnt = *reinterpret_cast<volatile int*>(wcnt);
+        if (cnt >= 32) {
+          if (cnt > K1_WCAP) {
+            // Too many ties for the buffer: fold the earlier stages' entries, then this
+            // stage's chunks element by element from the slot; the buffer is dropped.
+            const bool has = lane < prev;
+            queue_absorb(q, has ? bv[lane] : -INFINITY, has ? bi[lane] : INT_MAX, lane, K);
+#pragma unroll
+            for (int i = 0; i < K1_CPT; ++i) {
+              const int c = tid + i * K1_CTHREADS;
+              const bool hv = (vmask >> i) & 1u;
+              float x[NV];
+              if (hv) unpack16<NV>(*reinterpret_cast<const uint4*>(sbuf + c * 16), x);
+              const int id0 = seg_elem0 + (soff + c * 16) / ES;
+#pragma unroll
+              for (int j = 0; j < NV; ++j)
+                queue_absorb(q, hv ? x[j] : -INFINITY, hv ? id0 + j : INT_MAX, lane, K);
+            }
+            cnt = 0;
+          } else {
+            while (cnt >= 32) {
+              const float v = bv[lane];
+              const int id = bi[lane];
+              const bool more = lane + 32 < cnt;
+              const float v2 = more ? bv[lane + 32] : 0.f;
+              const int i2 = more ? bi[lane + 32] : 0;
+              __syncwarp();
+              if (more) {
+                bv[lane] = v2;
+                bi[lane] = i2;
+              }
+              cnt -= 32;
+              queue_absorb(q, v, id, lane, K);
+              __syncwarp();
+            }
+          }
+          __syncwarp();
+          if (lane == 0) {
+            *wcnt = cnt;
+            if (q.tv != -INFINITY) atomicMax(&s_floor, float_key(q.tv));
           }
         }
       }
-    }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty_bar[sl]);
+    };
 
-    // ---- warp 0 folds the previous stage's buffer into the running queue while the
-    // other warps go on (a stale threshold is still a valid lower bound)
-    if (warp == 0 && st > 0)
-      merge_buffer(run, s_buf_v[bsel ^ 1], s_buf_i[bsel ^ 1], &s_cnt[bsel ^ 1], &s_tau, lane, K);
-    __syncthreads();
-    if (s_cnt[bsel] > K1_CAP) {
-      // Too many ties for the buffer: exact per-warp queues over this stage's elements,
-      // re-read from shared memory (the slot is not refilled before the next iteration),
-      // merged into the running queue; the buffer is dropped.
-      WarpQueue q;
-      q.init();
+    for (int st = 0; st < nstages; ++st) {
+      const int sl = st % K1_NSTAGES;
+      if (!mbar_wait_bounded(&full_bar[sl], (st / K1_NSTAGES) & 1, &g_err_k1, ERR_K1_FULL_WAIT))
+        s_abort = 1;
+      if (s_abort) break;
+      const int soff = st * K1_STAGE_BYTES;
+      const int nbytes = min(K1_STAGE_BYTES, seg_bytes - soff);
+      const uint8_t* sbuf = stage[sl];
+      float cm[K1_CPT];
+      unsigned valid = 0;  // bit i: this thread has chunk i of the stage
 #pragma unroll
       for (int i = 0; i < K1_CPT; ++i) {
-        const int c = tid + i * K1_THREADS;
-        const bool has = c * 16 < nbytes;
-        float x[NV];
-        if (has) unpack16<NV>(*reinterpret_cast<const uint4*>(sbuf + c * 16), x);
-        const int id0 = seg_elem0 + (soff + c * 16) / ES;
+        const int c = tid + i * K1_CTHREADS;
+        cm[i] = -INFINITY;
+        if (c * 16 < nbytes) {
+          valid |= 1u << i;
+          float x[NV];
+          unpack16<NV>(*reinterpret_cast<const uint4*>(sbuf + c * 16), x);
+          cm[i] = lse_chunk_g<NV>(x, m2, s2, gmax);
+        }
+      }
+      if (st == 0) {
 #pragma unroll
-        for (int j = 0; j < NV; ++j)
-          queue_absorb(q, has ? x[j] : -INFINITY, has ? id0 + j : INT_MAX, lane, K);
+        for (int i = 0; i < K1_CPT; ++i) cm0[i] = cm[i];
+        valid0 = valid;
       }
-      sq_v[warp][lane] = q.qv;
-      sq_i[warp][lane] = q.qid;
-      __syncthreads();
-      for (int half = K1_WARPS / 2; half >= 1; half >>= 1) {
-        if (warp < half) {
-          float a = sq_v[warp][lane];
-          int ai = sq_i[warp][lane];
-          bitonic_merge(a, ai, sq_v[warp + half][lane], sq_i[warp + half][lane], lane);
-          __syncwarp();
-          sq_v[warp][lane] = a;
-          sq_i[warp][lane] = ai;
-        }
-        __syncthreads();
+      if (st == 1 || (st == 0 && nstages == 1)) {
+        // the group maxima now cover (most of) stage 0: the first CTA floor
+        const float f = group_floor(s_gmax, lane, K);
+        if (lane == 0) atomicMax(&s_floor, float_key(f));
+        __syncwarp();
+        check_stage(0, cm0, valid0);
       }
-      if (warp == 0) {
-        bitonic_merge(run.qv, run.qid, sq_v[0][lane], sq_i[0][lane], lane);
-        run.tv = __shfl_sync(FULL_MASK, run.qv, K - 1);
-        run.tid = __shfl_sync(FULL_MASK, run.qid, K - 1);
-        if (lane == 0) {
-          s_tau = pack_tau(run.tv, run.tid);
-          s_cnt[bsel] = 0;
-        }
-      }
-      __syncthreads();
+      if (st >= 1) check_stage(st, cm, valid);
     }
-    if (s_abort) {
-      ok = false;
-      break;
+    ssum = s2.x + s2.y;
+    // flush the warp buffer into the queue
+    __syncwarp();
+    const int cnt = *reinterpret_cast<volatile int*>(wcnt);
+    if (cnt > 0 && !s_abort) {
+      const bool has = lane < cnt;
+      queue_absorb(q, has ? bv[lane] : -INFINITY, has ? bi[lane] : INT_MAX, lane, K);
     }
-  }
-  if (ok && warp == 0 && nstages > 0)
-    merge_buffer(run, s_buf_v[(nstages - 1) & 1], s_buf_i[(nstages - 1) & 1],
-                 &s_cnt[(nstages - 1) & 1], &s_tau, lane, K);
-  if (!ok) {
-    // Give copies still in flight a bounded chance to land before the CTA exits.
-    if (tid == 0)
-      for (int st = 0; st < nstages; ++st)
-        if (!mbar_try_wait(&full_bar[st % K1_NSTAGES], (st / K1_NSTAGES) & 1))
-          mbar_wait_bounded(&full_bar[st % K1_NSTAGES], (st / K1_NSTAGES) & 1, &g_err_k1,
-                            ERR_K1_DRAIN);
-    return;
   }
 
-  // ---- CTA log-sum-exp reduction; the running queue is the CTA's top-K
+  // ---- CTA reduction: log-sum-exp partials and the 17 warp queues
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) {
     const float om = __shfl_xor_sync(FULL_MASK, m2, o);
     const float os = __shfl_xor_sync(FULL_MASK, ssum, o);
     lse_merge(m2, ssum, om, os);
   }
+  __syncwarp();
+  s_bv[warp][lane] = q.qv;
+  s_bi[warp][lane] = q.qid;
   if (lane == 0) {
     s_m2[warp] = m2;
     s_s[warp] = ssum;
   }
   __syncthreads();
+  if (s_abort) {
+    // let every copy still in flight land before the CTA exits
+    if (warp == K1_CWARPS && lane == 0)
+      for (int st = max(0, issued - K1_NSTAGES); st < issued; ++st)
+        mbar_wait_bounded(&full_bar[st % K1_NSTAGES], (st / K1_NSTAGES) & 1, &g_err_k1,
+                          ERR_K1_DRAIN);
+    return;
+  }
+  // tree merge of the queues: 17 -> 16 -> 8 -> 4 -> 2 -> 1
+  auto merge_into = [&](int dst, int src) {
+    float v = s_bv[dst][lane];
+    int id = s_bi[dst][lane];
+    bitonic_merge(v, id, s_bv[src][lane], s_bi[src][lane], lane);
+    __syncwarp();
+    s_bv[dst][lane] = v;
+    s_bi[dst][lane] = id;
+  };
+  if (warp == 0) merge_into(0, K1_CWARPS);
+  __syncthreads();
+  for (int half = K1_CWARPS / 2; half >= 1; half >>= 1) {
+    if (warp < half) merge_into(warp, warp + half);
+    __syncthreads();
+  }
   if (warp != 0) return;
 
-  float v = run.qv;
-  int id = run.qid;
-  float M = lane < K1_WARPS ? s_m2[lane] : M2_INIT;
-  float S = lane < K1_WARPS ? s_s[lane] : 0.f;
+  float v = s_bv[0][lane];
+  int id = s_bi[0][lane];
+  float M = lane <= K1_CWARPS ? s_m2[lane] : M2_INIT;
+  float S = lane <= K1_CWARPS ? s_s[lane] : 0.f;
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) {
     const float om = __shfl_xor_sync(FULL_MASK, M, o);
@@ -571,7 +629,7 @@ K1Plan k1_plan(int64_t batch, int B, int64_t V, int esize) {
   const int64_t rows = batch * (B - 1);
   const int64_t row_bytes = V * esize;
   const int64_t stages = (row_bytes + K1_STAGE_BYTES - 1) / K1_STAGE_BYTES;
-  const int64_t conc = int64_t(num_sms()) * 2;  // resident CTAs
+  const int64_t conc = int64_t(num_sms()) * K1_MIN_BLOCKS;  // resident CTAs
   // Smallest P (1..64, at least one stage per segment) whose work fills whole waves
   // of resident CTAs to within 5%; otherwise the best-filled P.
   int bestP = 1;
