@@ -6,15 +6,21 @@
 // significant bits) when Ka = 2 Kw; W is an exact bf16 weight whose column index wraps
 // (k mod Kw), so one accumulation gives A_hi W^T + A_lo W^T.
 //
-// Persistent: one CTA per SM walks the 128 x 128 output tiles (n fastest, so the CTAs
-// working at the same time share A tiles through L2).  10 warps:
-//   warp 0      TMA producer (2-D tiled loads, 128-byte swizzle, 4-stage mbarrier ring
-//               that runs on across tiles) and TMEM owner (2 x 128 f32 columns)
+// Persistent: one CTA per SM walks the 128 x 256 output tiles (n fastest, so the CTAs
+// working at the same time share A tiles through L2; 256 columns per tile halve the
+// A re-reads of 128-wide tiles, which left these small-K contractions short of L2
+// bandwidth).  10 warps:
+//   warp 0      TMA producer (2-D tiled loads, 128-byte swizzle, 3-stage mbarrier ring
+//               that runs on across tiles) and TMEM owner (2 x 256 f32 columns)
 //   warp 1      MMA issuer: one elected thread issues tcgen05.mma (kind::f16, bf16 in,
-//               f32 accumulate in TMEM), 4 per 64-wide K block, and tcgen05.commit
+//               f32 accumulate in TMEM, M 128 x N 256), 4 per 64-wide K block, and
+//               tcgen05.commit
 //   warps 2-9   epilogue: two warps per 32-lane TMEM quarter (= 32 output rows), each
 //               taking half of the columns; tcgen05.ld, then the fused bias / SiLU /
-//               residual / hi-lo split / node-sum, stored to global
+//               hi-lo split in registers, 32 x 32 chunks staged through swizzled shared
+//               memory and written by bulk tensor stores (the residual add is a bulk
+//               tensor reduce-add into the f32 stream); the node epilogue's gathers and
+//               sums store directly
 // The accumulator is double-buffered: the epilogue of tile i overlaps the MMAs of tile
 // i + 1.  Every mbarrier wait is bounded; a timeout sets a bit in this unit's error word
 // and the CTA still frees its TMEM before exiting.
@@ -27,11 +33,13 @@ namespace lilicorr {
 
 static __device__ uint32_t g_err_tc;
 
-constexpr int TC_BM = 128, TC_BN = 128, TC_BK = 64, TC_STAGES = 4;
+constexpr int TC_BM = 128, TC_BN = 256, TC_BK = 64, TC_STAGES = 3;
 constexpr int TC_EPI_WARPS = 8, TC_THREADS = 32 * (2 + TC_EPI_WARPS);
 constexpr int TC_A_BYTES = TC_BM * TC_BK * 2;
 constexpr int TC_B_BYTES = TC_BN * TC_BK * 2;
-constexpr int TC_SMEM = TC_STAGES * (TC_A_BYTES + TC_B_BYTES) + 1024;
+constexpr int TC_STG_BYTES = 4096;  // one 32 x 32 output chunk (f32, or bf16 hi + lo)
+constexpr int TC_SMEM =
+    TC_STAGES * (TC_A_BYTES + TC_B_BYTES) + TC_EPI_WARPS * 2 * TC_STG_BYTES + 1024;
 constexpr uint32_t TC_TMEM_COLS = 2 * TC_BN;  // two accumulator buffers
 
 enum TcErr : uint32_t {
@@ -50,6 +58,36 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* tm, in
       "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(dst)),
       "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(smem_addr(bar))
       : "memory");
+}
+
+// Bulk tensor store / reduce-add of a shared-memory box to global memory.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* tm, const void* src, int c0,
+                                             int c1) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(tm)),
+               "r"(smem_addr(src)), "r"(c0), "r"(c1)
+               : "memory");
+}
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* tm, const void* src, int c0,
+                                                  int c1) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(tm)),
+      "r"(smem_addr(src)), "r"(c0), "r"(c1)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Wait until at most one committed bulk group still reads shared memory.
+__device__ __forceinline__ void bulk_wait_read1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+__device__ __forceinline__ void fence_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
@@ -227,17 +265,84 @@ __device__ __forceinline__ void tc_epilogue32(const GemmArgs& g, int64_t m, int 
   }
 }
 
+// Staged form of the bias / SiLU / split / residual epilogues: v[0..31] = accumulator
+// columns n..n+31 of this lane's row; the warp's 32 x 32 chunk goes to shared memory in
+// the layout of the output tensor map's swizzle (16-byte unit u of row r at u ^ f(r)),
+// then one lane stores it (or adds it into the residual) with a bulk tensor copy.
+template <int EPI>
+__device__ __forceinline__ void tc_epilogue_staged(const GemmArgs& g, const CUtensorMap* tmC,
+                                                   uint8_t* stg, int lane, int64_t row0, int n,
+                                                   float (&v)[32]) {
+#pragma unroll
+  for (int j = 0; j < 32; j += 4) {
+    const float4 b4 = __ldg(reinterpret_cast<const float4*>(g.bias + n + j));
+    v[j] += b4.x;
+    v[j + 1] += b4.y;
+    v[j + 2] += b4.z;
+    v[j + 3] += b4.w;
+  }
+  if constexpr (EPI == EPI_SPLIT || EPI == EPI_SPLIT_SILU) {
+    uint32_t hi[16], lo[16];
+#pragma unroll
+    for (int j = 0; j < 32; j += 2) {
+      float a = v[j], b = v[j + 1];
+      if constexpr (EPI == EPI_SPLIT_SILU) {
+        a = silu(a);
+        b = silu(b);
+      }
+      __nv_bfloat16 ha, la, hb, lb;
+      split_bf16(a, ha, la);
+      split_bf16(b, hb, lb);
+      hi[j / 2] = pack2(ha, hb);
+      lo[j / 2] = pack2(la, lb);
+    }
+    // 64-byte rows, 64-byte swizzle: unit u of row r lands at u ^ ((r >> 1) & 3)
+    const int sw = (lane >> 1) & 3;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int off = lane * 64 + ((u ^ sw) << 4);
+      *reinterpret_cast<uint4*>(stg + off) = make_uint4(hi[4 * u], hi[4 * u + 1], hi[4 * u + 2], hi[4 * u + 3]);
+      *reinterpret_cast<uint4*>(stg + 2048 + off) =
+          make_uint4(lo[4 * u], lo[4 * u + 1], lo[4 * u + 2], lo[4 * u + 3]);
+    }
+    fence_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(tmC, stg, n, static_cast<int>(row0));
+      tma_store_2d(tmC, stg + 2048, g.N + n, static_cast<int>(row0));
+      bulk_commit();
+    }
+  } else {
+    // 128-byte rows, 128-byte swizzle: unit u of row r lands at u ^ (r & 7)
+    const int sw = lane & 7;
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      *reinterpret_cast<float4*>(stg + lane * 128 + ((u ^ sw) << 4)) =
+          make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+    fence_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      if constexpr (EPI == EPI_RESID)
+        tma_reduce_add_2d(tmC, stg, n, static_cast<int>(row0));
+      else
+        tma_store_2d(tmC, stg, n, static_cast<int>(row0));
+      bulk_commit();
+    }
+  }
+}
+
 // ------------------------------------------------------------------ kernel
 
 template <int EPI>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const GemmArgs g) {
+                   const __grid_constant__ CUtensorMap tmC, const GemmArgs g) {
   extern __shared__ uint8_t tc_smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + TC_STAGES * TC_A_BYTES;
+  uint8_t* sStage = smem + TC_STAGES * (TC_A_BYTES + TC_B_BYTES);  // epilogue staging
   __shared__ __align__(8) uint64_t full_bar[TC_STAGES], empty_bar[TC_STAGES];
   __shared__ __align__(8) uint64_t acc_full[2], acc_empty[2];
   __shared__ uint32_t s_tmem;
@@ -315,6 +420,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     // ---- epilogue: quarter q = warp % 4 owns TMEM lanes 32q..32q+31 (output rows);
     // the two warps of a quarter split the tile's columns in halves
     const int q = warp & 3, half = (warp - 2) >> 2;
+    uint8_t* stg = sStage + (warp - 2) * 2 * TC_STG_BYTES;
+    int sb = 0;  // staging buffer of the next chunk
     int i = 0;
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
       const int buf = i & 1;
@@ -328,12 +435,22 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         float v[32];
         tmem_ld32(tmem + (uint32_t(32 * q) << 16) + uint32_t(buf * TC_BN + cc * 32), v);
         const int n = n0 + cc * 32;
-        if (m < g.M && n < g.N) tc_epilogue32<EPI>(g, m, n, v);
+        if constexpr (EPI == EPI_NODE) {
+          if (m < g.M && n < g.N) tc_epilogue32<EPI>(g, m, n, v);
+        } else if (n < g.N) {
+          // the buffer written two chunks ago must have been read by its bulk copy
+          if (lane == 0) bulk_wait_read1();
+          __syncwarp();
+          tc_epilogue_staged<EPI>(g, &tmC, stg + sb * TC_STG_BYTES, lane, m0 + 32 * q, n, v);
+          sb ^= 1;
+        }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[buf]);
     }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
   }
   tc_fence_before();
   __syncthreads();
@@ -372,6 +489,22 @@ static bool make_tmap(CUtensorMap* tm, const void* ptr, uint64_t rows, uint64_t 
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Output matrix [rows, cols] (bf16 or f32) written in 32 x 32 boxes whose 64- or
+// 128-byte rows use the matching swizzle.
+static bool make_tmap_out(CUtensorMap* tm, void* ptr, uint64_t rows, uint64_t cols, bool f32) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const uint64_t es = f32 ? 4 : 2;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * es};
+  const cuuint32_t box[2] = {32, 32};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(tm, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr,
+            dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool gemm_tc_supported(const GemmArgs& g) {
   return g.Kw % TC_BK == 0 && g.Ka % TC_BK == 0 && (g.Ka == g.Kw || g.Ka == 2 * g.Kw) &&
          g.N % 32 == 0 && g.M > 0 &&
@@ -380,10 +513,21 @@ bool gemm_tc_supported(const GemmArgs& g) {
 
 cudaError_t launch_gemm(int epi, const GemmArgs& g, cudaStream_t stream) {
   if (!gemm_tc_supported(g)) return cudaErrorInvalidValue;
-  CUtensorMap ta, tb;
+  CUtensorMap ta, tb, tc;
   if (!make_tmap(&ta, g.A, uint64_t(g.M), uint64_t(g.Ka), TC_BM) ||
       !make_tmap(&tb, g.W, uint64_t(g.N), uint64_t(g.Kw), TC_BN))
     return cudaErrorInvalidValue;
+  if (epi == EPI_SPLIT || epi == EPI_SPLIT_SILU) {
+    if (!g.out_split || reinterpret_cast<uintptr_t>(g.out_split) % 16 ||
+        !make_tmap_out(&tc, g.out_split, uint64_t(g.M), uint64_t(2 * g.N), false))
+      return cudaErrorInvalidValue;
+  } else if (epi != EPI_NODE) {
+    if (!g.out || reinterpret_cast<uintptr_t>(g.out) % 16 ||
+        !make_tmap_out(&tc, g.out, uint64_t(g.M), uint64_t(g.N), true))
+      return cudaErrorInvalidValue;
+  } else {
+    tc = ta;  // unused by the node epilogue
+  }
   static bool attr = false;
   if (!attr) {
     cudaFuncSetAttribute(gemm_tc_kernel<EPI_F32>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
@@ -403,11 +547,11 @@ cudaError_t launch_gemm(int epi, const GemmArgs& g, cudaStream_t stream) {
   const int64_t ntiles = int64_t((g.N + TC_BN - 1) / TC_BN) * ((g.M + TC_BM - 1) / TC_BM);
   const dim3 grid(static_cast<unsigned>(ntiles < sms ? ntiles : sms));
   switch (epi) {
-    case EPI_F32: gemm_tc_kernel<EPI_F32><<<grid, TC_THREADS, TC_SMEM, stream>>>(ta, tb, g); break;
-    case EPI_RESID: gemm_tc_kernel<EPI_RESID><<<grid, TC_THREADS, TC_SMEM, stream>>>(ta, tb, g); break;
-    case EPI_SPLIT: gemm_tc_kernel<EPI_SPLIT><<<grid, TC_THREADS, TC_SMEM, stream>>>(ta, tb, g); break;
-    case EPI_SPLIT_SILU: gemm_tc_kernel<EPI_SPLIT_SILU><<<grid, TC_THREADS, TC_SMEM, stream>>>(ta, tb, g); break;
-    default: gemm_tc_kernel<EPI_NODE><<<grid, TC_THREADS, TC_SMEM, stream>>>(ta, tb, g); break;
+    case EPI_F32: gemm_tc_kernel<EPI_F32><<<grid, TC_THREADS, TC_SMEM, stream>>>(ta, tb, tc, g); break;
+    case EPI_RESID: gemm_tc_kernel<EPI_RESID><<<grid, TC_THREADS, TC_SMEM, stream>>>(ta, tb, tc, g); break;
+    case EPI_SPLIT: gemm_tc_kernel<EPI_SPLIT><<<grid, TC_THREADS, TC_SMEM, stream>>>(ta, tb, tc, g); break;
+    case EPI_SPLIT_SILU: gemm_tc_kernel<EPI_SPLIT_SILU><<<grid, TC_THREADS, TC_SMEM, stream>>>(ta, tb, tc, g); break;
+    default: gemm_tc_kernel<EPI_NODE><<<grid, TC_THREADS, TC_SMEM, stream>>>(ta, tb, tc, g); break;
   }
   note_launch();
   return cudaGetLastError();
