@@ -32,7 +32,8 @@ static __device__ uint32_t g_err_at;
 constexpr int AT_DH = 64, AT_QT = 128, AT_KMAX = 256, AT_SOFT_WARPS = 8;
 constexpr int AT_THREADS = 32 * (2 + AT_SOFT_WARPS);
 constexpr int AT_TILE = 128 * 64 * 2;  // one [128 x 64] bf16 swizzled tile
-constexpr int AT_SMEM = 10 * AT_TILE + 1024;
+constexpr int AT_SMEM = 10 * AT_TILE + 1024;  // + the bias table, sized per launch
+constexpr int AT_BSTRIDE = AT_KMAX + 4;        // floats per bias-table row (bank offset)
 constexpr uint32_t AT_TMEM_COLS = 512, AT_O_COL = 256;
 constexpr float AT_LOG2E = 1.4426950408889634f;
 
@@ -150,6 +151,16 @@ __host__ __device__ constexpr uint32_t at_idesc(int M, int N, bool b_mn) {
          (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
 }
 
+// (a, b) -> packed bf16 hi words and lo words: hi = bf16(x), lo = bf16(x - hi).
+__device__ __forceinline__ void at_split2(float a, float b, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  const uint32_t hw = *reinterpret_cast<const uint32_t*>(&h);
+  const __nv_bfloat162 l2 = __floats2bfloat162_rn(a - __uint_as_float(hw << 16),
+                                                  b - __uint_as_float(hw & 0xffff0000u));
+  hi = hw;
+  lo = *reinterpret_cast<const uint32_t*>(&l2);
+}
+
 __device__ __forceinline__ void soft_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(32 * AT_SOFT_WARPS) : "memory");
 }
@@ -167,11 +178,12 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   uint8_t* sKl = sm + 4 * AT_TILE;
   uint8_t* sVh = sm + 6 * AT_TILE;   // V hi / lo: 2 tiles each
   uint8_t* sVl = sm + 8 * AT_TILE;
+  // [query slot][key]: (dist + same-slot bias) * log2(e) of the current head, -inf for
+  // keys beyond the block
+  float* s_btab = reinterpret_cast<float*>(sm + 10 * AT_TILE);
   __shared__ __align__(8) uint64_t bar_qk, bar_qkfree, bar_v, bar_vfree, bar_s, bar_p, bar_o,
       bar_ofree;
   __shared__ uint32_t s_tmem;
-  __shared__ float s_bias[128];      // dist + same-slot bias by slot distance, current head
-  __shared__ uint8_t s_kslot[AT_KMAX];
   __shared__ float s_pmax[2][128], s_psum[2][128];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -190,7 +202,6 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     mbar_init(&bar_ofree, 32 * AT_SOFT_WARPS);
     fence_mbar_init();
   }
-  for (int j = tid; j < AT_KMAX; j += AT_THREADS) s_kslot[j] = j < S ? uint8_t(j / Kc) : 0;
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_addr(&s_tmem)),
@@ -274,6 +285,8 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     const int r = 32 * qq + lane;  // TMEM lane = query row of the tile
     const uint32_t lane_off = uint32_t(32 * qq) << 16;
     const int j0 = 128 * hf;       // this warp's keys j0 .. j0 + 127
+    const int nq = S / Kc;         // query slots
+    constexpr float C = 0.125f * AT_LOG2E;  // 1 / sqrt(64), in log2 units
     int i = 0;
     int cur_h = -1;
     for (int64_t t = blockIdx.x; t < nitems; t += gridDim.x, ++i) {
@@ -281,17 +294,25 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       const int h = static_cast<int>((t / QT) % heads);
       const int64_t tok0 = (t / QT / heads) * S;
       const int q = qt * AT_QT + r;
-      const int boff = B_max - 2 - min(q, S - 1) / Kc;  // bias index = slot_j + boff
       if (h != cur_h) {  // bias table of this head (all softmax warps take the same items)
         soft_sync();
-        for (int k = tid - 64; k < nd; k += 32 * AT_SOFT_WARPS)
-          s_bias[k] = dist_bias[h * nd + k] + (k == B_max - 2 ? same_bias[h] : 0.f);
+        for (int idx = tid - 64; idx < nq * AT_KMAX; idx += 32 * AT_SOFT_WARPS) {
+          const int qs = idx / AT_KMAX, j = idx % AT_KMAX;
+          float b = -INFINITY;
+          if (j < S) {
+            const int sj = j / Kc;
+            b = (dist_bias[h * nd + sj - qs + B_max - 2] + (sj == qs ? same_bias[h] : 0.f)) *
+                AT_LOG2E;
+          }
+          s_btab[qs * AT_BSTRIDE + j] = b;
+        }
         soft_sync();
         cur_h = h;
       }
+      const float* brow = s_btab + (min(q, S - 1) / Kc) * AT_BSTRIDE;
       bool ok = mbar_wait_bounded(&bar_s, i & 1, &g_err_at, ERR_AT_S);
       at_fence_after();
-      // pass 1: logits with bias and mask, partial row max, written back
+      // pass 1: row max of the biased, masked logits (log2 units)
       float mx = -INFINITY;
 #pragma unroll 1
       for (int cc = 0; cc < 4; ++cc) {
@@ -299,19 +320,16 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         float v[32];
         at_ld32(tS + lane_off + jb, v);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const float x =
-              jb + e < S ? fmaf(v[e], 0.125f, s_bias[s_kslot[jb + e] + boff]) : -INFINITY;
-          v[e] = x;
-          mx = fmaxf(mx, x);
+        for (int u = 0; u < 8; ++u) {
+          const float4 b4 = *reinterpret_cast<const float4*>(brow + jb + 4 * u);
+          mx = fmaxf(mx, fmaxf(fmaxf(fmaf(v[4 * u], C, b4.x), fmaf(v[4 * u + 1], C, b4.y)),
+                               fmaxf(fmaf(v[4 * u + 2], C, b4.z), fmaf(v[4 * u + 3], C, b4.w))));
         }
-        at_st32(tS + lane_off + jb, v);
       }
       s_pmax[hf][r] = mx;
       soft_sync();
-      mx = fmaxf(s_pmax[0][r], s_pmax[1][r]);
-      // pass 2: p = exp(s - max) and its sum; p as packed bf16 hi / lo over its logits
-      const float m2 = mx * AT_LOG2E;
+      const float m2 = fmaxf(s_pmax[0][r], s_pmax[1][r]);
+      // pass 2: p = 2^(x - max) and its sum; p as packed bf16 hi / lo over its logits
       float l = 0.f;
 #pragma unroll 1
       for (int cc = 0; cc < 4; ++cc) {
@@ -320,15 +338,15 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         at_ld32(tS + lane_off + jb, v);
         uint32_t ph[16], pl[16];
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const float pa = at_ex2(fmaf(v[e], AT_LOG2E, -m2));
-          const float pb = at_ex2(fmaf(v[e + 1], AT_LOG2E, -m2));
-          l += pa + pb;
-          __nv_bfloat16 ha, la, hb, lb;
-          split_bf16(pa, ha, la);
-          split_bf16(pb, hb, lb);
-          ph[e / 2] = at_pack(ha, hb);
-          pl[e / 2] = at_pack(la, lb);
+        for (int u = 0; u < 8; ++u) {
+          const float4 b4 = *reinterpret_cast<const float4*>(brow + jb + 4 * u);
+          const float p0 = at_ex2(fmaf(v[4 * u], C, b4.x) - m2);
+          const float p1 = at_ex2(fmaf(v[4 * u + 1], C, b4.y) - m2);
+          const float p2 = at_ex2(fmaf(v[4 * u + 2], C, b4.z) - m2);
+          const float p3 = at_ex2(fmaf(v[4 * u + 3], C, b4.w) - m2);
+          l += (p0 + p1) + (p2 + p3);
+          at_split2(p0, p1, ph[2 * u], pl[2 * u]);
+          at_split2(p2, p3, ph[2 * u + 1], pl[2 * u + 1]);
         }
         at_st16(tS + lane_off + jb, ph);
         at_st16(tS + lane_off + jb + 16, pl);
@@ -412,10 +430,11 @@ cudaError_t launch_attention_tc(const __nv_bfloat16* qkv, int64_t batch, int S, 
          box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
-  static bool attr = false;
-  if (!attr) {
-    cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, AT_SMEM);
-    attr = true;
+  const int smem = AT_SMEM + (S / K) * AT_BSTRIDE * 4;
+  static int attr = 0;
+  if (attr < smem) {
+    cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    attr = smem;
   }
   static int sms = 0;
   if (!sms) {
@@ -426,7 +445,7 @@ cudaError_t launch_attention_tc(const __nv_bfloat16* qkv, int64_t batch, int S, 
   }
   const int64_t nitems = batch * heads * ((S + AT_QT - 1) / AT_QT);
   const dim3 grid(static_cast<unsigned>(nitems < sms ? nitems : sms));
-  attn_tc_kernel<<<grid, AT_THREADS, AT_SMEM, stream>>>(tm, S, K, H, B_max, heads, batch,
+  attn_tc_kernel<<<grid, AT_THREADS, smem, stream>>>(tm, S, K, H, B_max, heads, batch,
                                                         dist_bias, same_bias, out);
   note_launch();
   return cudaGetLastError();

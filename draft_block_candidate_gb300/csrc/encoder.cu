@@ -15,6 +15,8 @@
 // (hi*hi + hi*lo + lo*hi).  Everything else (norms, softmax, residual stream) is f32.
 #include <float.h>
 
+#include <algorithm>
+
 #include "kernels.cuh"
 
 namespace lilicorr {
@@ -72,42 +74,78 @@ __device__ __forceinline__ int swz(int r, int c) {
     return r * CH * 16 + ((c ^ ((r >> 1) & 3)) << 4);
 }
 
+// Split 8 floats into packed bf16 hi / lo words and store them 16 bytes at a time.
+__device__ __forceinline__ void store_split8(const float (&v)[8], __nv_bfloat16* hi_dst,
+                                             __nv_bfloat16* lo_dst) {
+  uint32_t hi[4], lo[4];
+#pragma unroll
+  for (int j = 0; j < 8; j += 2) {
+    __nv_bfloat16 ha, la, hb, lb;
+    split_bf16(v[j], ha, la);
+    split_bf16(v[j + 1], hb, lb);
+    hi[j / 2] = uint32_t(__bfloat16_as_ushort(ha)) | (uint32_t(__bfloat16_as_ushort(hb)) << 16);
+    lo[j / 2] = uint32_t(__bfloat16_as_ushort(la)) | (uint32_t(__bfloat16_as_ushort(lb)) << 16);
+  }
+  *reinterpret_cast<uint4*>(hi_dst) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+  *reinterpret_cast<uint4*>(lo_dst) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+}
+
+__device__ __forceinline__ void load8(const float* p, float (&v)[8]) {
+  const float4 a = *reinterpret_cast<const float4*>(p);
+  const float4 b = *reinterpret_cast<const float4*>(p + 4);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+
 // ------------------------------------------------------------------ a2: confidence MLP
 // U[m, :] = SiLU(Wc1 f(m) + bc1) written split [M, 2H]; f = (lp, p, gap, r, top):
 // lp = l - lse, p = exp(lp), gap = lp - lp of the slot's top candidate, r = k/(K-1),
 // top = [k == 0] (App. A: log-probability and probability under the full vocabulary,
 // the gap to the slot's most likely token, the rank normalised to [0,1], top indicator).
+// Eight rows per CTA (one per warp), each lane 8 consecutive hidden units per pass:
+// 16-byte hi and lo stores; W1 and b1 staged in shared memory once per CTA.
 __global__ void conf_hidden_kernel(const float* __restrict__ cand_logit,
                                    const float* __restrict__ lse, int64_t M, int K, int H,
                                    const float* __restrict__ w1, const float* __restrict__ b1,
                                    __nv_bfloat16* __restrict__ U) {
-  const int64_t m = blockIdx.x;
-  if (m >= M) return;
-  const int64_t row = m / K;  // (block, slot) row of the logit pass
-  const int k = static_cast<int>(m % K);
-  const float l = lse[row];
-  const float lp = cand_logit[m] - l;
-  const float lp_top = cand_logit[row * K] - l;
-  float f[5];
-  f[0] = lp;
-  f[1] = expf(lp);
-  f[2] = lp - lp_top;
-  f[3] = K > 1 ? float(k) / float(K - 1) : 0.f;
-  f[4] = k == 0 ? 1.f : 0.f;
-  for (int h = threadIdx.x; h < H; h += blockDim.x) {
-    float acc = b1[h];
+  extern __shared__ float ch_smem[];  // [H][6]: w1 row (5) + bias
+  for (int i = threadIdx.x; i < H; i += blockDim.x) {
 #pragma unroll
-    for (int j = 0; j < 5; ++j) acc = fmaf(w1[h * 5 + j], f[j], acc);
-    const float u = silu(acc);
-    __nv_bfloat16 hi, lo;
-    split_bf16(u, hi, lo);
-    U[m * 2 * H + h] = hi;
-    U[m * 2 * H + H + h] = lo;
+    for (int j = 0; j < 5; ++j) ch_smem[i * 6 + j] = w1[i * 5 + j];
+    ch_smem[i * 6 + 5] = b1[i];
+  }
+  __syncthreads();
+  const int lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  for (int64_t m = int64_t(blockIdx.x) * nw + (threadIdx.x >> 5); m < M;
+       m += int64_t(gridDim.x) * nw) {
+    const int64_t row = m / K;  // (block, slot) row of the logit pass
+    const int k = static_cast<int>(m % K);
+    const float l = __ldg(lse + row);
+    const float lp = __ldg(cand_logit + m) - l;
+    const float lp_top = __ldg(cand_logit + row * K) - l;
+    float f[5];
+    f[0] = lp;
+    f[1] = expf(lp);
+    f[2] = lp - lp_top;
+    f[3] = K > 1 ? float(k) / float(K - 1) : 0.f;
+    f[4] = k == 0 ? 1.f : 0.f;
+    for (int h0 = lane * 8; h0 < H; h0 += 256) {
+      float u[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float* wr = ch_smem + (h0 + j) * 6;
+        float acc = wr[5];
+#pragma unroll
+        for (int i = 0; i < 5; ++i) acc = fmaf(wr[i], f[i], acc);
+        u[j] = silu(acc);
+      }
+      store_split8(u, U + m * 2 * H + h0, U + m * 2 * H + H + h0);
+    }
   }
 }
 
 // ------------------------------------------------------------------ RMSNorm -> split
-// y = x / sqrt(mean(x^2) + eps) * g, one warp per row.
+// y = x / sqrt(mean(x^2) + eps) * g, one warp per row, 8 columns per lane per pass.
 __global__ void rmsnorm_split_kernel(const float* __restrict__ X, const float* __restrict__ gain,
                                      int64_t M, int H, float eps, __nv_bfloat16* __restrict__ out) {
   const int lane = threadIdx.x & 31;
@@ -115,16 +153,23 @@ __global__ void rmsnorm_split_kernel(const float* __restrict__ X, const float* _
   if (m >= M) return;
   const float* x = X + m * H;
   float ss = 0.f;
-  for (int h = lane; h < H; h += 32) ss = fmaf(x[h], x[h], ss);
+  for (int c = lane * 8; c < H; c += 256) {
+    float v[8];
+    load8(x + c, v);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) ss = fmaf(v[j], v[j], ss);
+  }
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) ss += __shfl_xor_sync(FULL_MASK, ss, o);
   const float inv = 1.0f / sqrtf(ss / float(H) + eps);
   __nv_bfloat16* o = out + m * 2 * H;
-  for (int h = lane; h < H; h += 32) {
-    __nv_bfloat16 hi, lo;
-    split_bf16(x[h] * inv * gain[h], hi, lo);
-    o[h] = hi;
-    o[H + h] = lo;
+  for (int c = lane * 8; c < H; c += 256) {
+    float v[8], g[8];
+    load8(x + c, v);
+    load8(gain + c, g);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = v[j] * inv * g[j];
+    store_split8(v, o + c, o + H + c);
   }
 }
 
@@ -359,44 +404,35 @@ cudaError_t launch_attention(const __nv_bfloat16* qkv, int64_t batch, int S, int
 // ------------------------------------------------------------------ fusion input
 // out split [M, 6H] = [h, t, h*t]_hi | [h, t, h*t]_lo (App. A: "concatenating the
 // candidate state, the target state, and their elementwise product").
+// One thread per (row m, 8 consecutive columns): 16-byte stores of all six parts.
 __global__ void fuse_concat_kernel(const float* __restrict__ X,
                                    const __nv_bfloat16* __restrict__ target, int S, int64_t M,
                                    int H, __nv_bfloat16* __restrict__ out) {
+  const int hv = H / 8;
   const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (idx >= M * H) return;
-  const int64_t m = idx / H;
-  const int h = static_cast<int>(idx % H);
-  const float x = X[idx];
-  const float t = target ? __bfloat162float(target[(m / S) * H + h]) : 0.f;
-  __nv_bfloat16* o = out + m * 6 * H;
-  __nv_bfloat16 hi, lo;
-  split_bf16(x, hi, lo);
-  o[h] = hi;
-  o[3 * H + h] = lo;
-  split_bf16(t, hi, lo);
-  o[H + h] = hi;
-  o[4 * H + h] = lo;
-  split_bf16(x * t, hi, lo);
-  o[2 * H + h] = hi;
-  o[5 * H + h] = lo;
-}
-
-// ------------------------------------------------------------------ anchor head (raw)
-// anchor_raw[b, e] = Wa[e, :] . t_b + ba[e]; t is exact bf16, accumulated in f32.
-__global__ void anchor_kernel(const __nv_bfloat16* __restrict__ target,
-                              const __nv_bfloat16* __restrict__ Wa, const float* __restrict__ ba,
-                              int H, int E, float* __restrict__ anchor_raw) {
-  const int64_t b = blockIdx.x;
-  const int lane = threadIdx.x & 31;
-  for (int e = threadIdx.x >> 5; e < E; e += blockDim.x >> 5) {
-    float acc = 0.f;
-    if (target)
-      for (int h = lane; h < H; h += 32)
-        acc = fmaf(__bfloat162float(Wa[int64_t(e) * H + h]), __bfloat162float(target[b * H + h]), acc);
+  if (idx >= M * hv) return;
+  const int64_t m = idx / hv;
+  const int h0 = static_cast<int>(idx % hv) * 8;
+  float x[8], t[8], xt[8];
+  load8(X + m * H + h0, x);
+  if (target) {
+    const uint4 w = __ldg(reinterpret_cast<const uint4*>(target + (m / S) * H + h0));
+    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) acc += __shfl_xor_sync(FULL_MASK, acc, o);
-    if (lane == 0) anchor_raw[b * E + e] = acc + ba[e];
+    for (int j = 0; j < 4; ++j) {
+      t[2 * j] = __uint_as_float(ww[j] << 16);
+      t[2 * j + 1] = __uint_as_float(ww[j] & 0xffff0000u);
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) t[j] = 0.f;
   }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) xt[j] = x[j] * t[j];
+  __nv_bfloat16* o = out + m * 6 * H;
+  store_split8(x, o + h0, o + 3 * H + h0);
+  store_split8(t, o + H + h0, o + 4 * H + h0);
+  store_split8(xt, o + 2 * H + h0, o + 5 * H + h0);
 }
 
 // ------------------------------------------------------------------ launchers
@@ -404,13 +440,19 @@ __global__ void anchor_kernel(const __nv_bfloat16* __restrict__ target,
 cudaError_t launch_conf_hidden(const float* cand_logit, const float* lse, int64_t M, int K, int H,
                                const float* w1, const float* b1, __nv_bfloat16* U,
                                cudaStream_t stream) {
-  conf_hidden_kernel<<<static_cast<unsigned>(M), 128, 0, stream>>>(cand_logit, lse, M, K, H, w1, b1, U);
+  if (H % 8 || H > 2048) return cudaErrorInvalidValue;
+  const int64_t rows_per_cta = 8;
+  const unsigned grid =
+      static_cast<unsigned>(std::min<int64_t>((M + rows_per_cta - 1) / rows_per_cta, 152 * 32));
+  conf_hidden_kernel<<<grid, 256, size_t(H) * 6 * sizeof(float), stream>>>(cand_logit, lse, M, K,
+                                                                            H, w1, b1, U);
   note_launch();
   return cudaGetLastError();
 }
 
 cudaError_t launch_rmsnorm_split(const float* X, const float* gain, int64_t M, int H, float eps,
                                  __nv_bfloat16* out, cudaStream_t stream) {
+  if (H % 8) return cudaErrorInvalidValue;
   const int wpb = 8;
   rmsnorm_split_kernel<<<static_cast<unsigned>((M + wpb - 1) / wpb), wpb * 32, 0, stream>>>(
       X, gain, M, H, eps, out);
@@ -420,17 +462,12 @@ cudaError_t launch_rmsnorm_split(const float* X, const float* gain, int64_t M, i
 
 cudaError_t launch_fuse_concat(const float* X, const __nv_bfloat16* target, int S, int64_t M,
                                int H, __nv_bfloat16* out, cudaStream_t stream) {
-  const int64_t n = M * H;
+  if (H % 8) return cudaErrorInvalidValue;
+  const int64_t n = M * (H / 8);
   fuse_concat_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, stream>>>(X, target, S, M, H, out);
   note_launch();
   return cudaGetLastError();
 }
 
-cudaError_t launch_anchor(const __nv_bfloat16* target, const __nv_bfloat16* Wa, const float* ba,
-                          int64_t batch, int H, int E, float* anchor_raw, cudaStream_t stream) {
-  anchor_kernel<<<static_cast<unsigned>(batch), 256, 0, stream>>>(target, Wa, ba, H, E, anchor_raw);
-  note_launch();
-  return cudaGetLastError();
-}
 
 }  // namespace lilicorr

@@ -16,8 +16,9 @@ cudaError_t k1_read_device_error(uint32_t* code);
 void set_last_error(const char* msg);
 
 // a4 scores + a5 walk (walk.cu)
-cudaError_t launch_pair_scores(const float* heads, const float* anchor_raw, int64_t batch, int B,
-                               int K, int E, float sigma, float* scores, float* out_tap,
+cudaError_t launch_pair_scores(const float* heads, const __nv_bfloat16* target,
+                               const __nv_bfloat16* Wa, const float* ba, int64_t batch, int B,
+                               int K, int E, int H, float sigma, float* scores, float* out_tap,
                                float* in_tap, float* anchor_tap, cudaStream_t stream);
 cudaError_t launch_greedy_walk(const float* scores, const int32_t* cand_id,
                                const int32_t* anchor_ids, int64_t batch, int B, int K,
@@ -65,7 +66,4 @@ cudaError_t launch_attention_tc(const __nv_bfloat16* qkv, int64_t batch, int S, 
 cudaError_t at_read_device_error(uint32_t* code);
 cudaError_t launch_fuse_concat(const float* X, const __nv_bfloat16* target, int S, int64_t M,
                                int H, __nv_bfloat16* out, cudaStream_t stream);
-cudaError_t launch_anchor(const __nv_bfloat16* target, const __nv_bfloat16* Wa, const float* ba,
-                          int64_t batch, int H, int E, float* anchor_raw, cudaStream_t stream);
-
 }  // namespace lilicorr

@@ -30,12 +30,12 @@ static lilicorr_status cuda_fail(cudaError_t e, const char* where) {
 // ---- per-kernel timing: events recorded on the caller's stream after each launch
 enum Slot : int {
   T_LOGIT = 0, T_CONF, T_NODE, T_NORM, T_QKV, T_ATTN, T_OUT, T_FFN1, T_FFN2, T_FUSECAT,
-  T_FUSE, T_HEADS, T_ANCHOR, T_SCORES, T_WALK, NSLOT
+  T_FUSE, T_HEADS, T_SCORES, T_WALK, NSLOT
 };
 static const char* kSlotNames[NSLOT] = {
     "logit_pass", "conf_hidden", "node_gemm", "rmsnorm", "qkv_gemm", "attention", "out_gemm",
-    "ffn1_gemm", "ffn2_gemm", "fuse_concat", "fuse_gemm", "heads_gemm", "anchor_head",
-    "pair_scores", "greedy_walk"};
+    "ffn1_gemm", "ffn2_gemm", "fuse_concat", "fuse_gemm", "heads_gemm", "pair_scores",
+    "greedy_walk"};
 
 struct CallRecord {
   cudaEvent_t start;
@@ -168,7 +168,7 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // Workspace layout of one rerank call.
 struct WsPlan {
-  size_t k1, cand_id, cand_logit, lse, act1, X, qkv, ffh, heads, anchor, scores, total;
+  size_t k1, cand_id, cand_logit, lse, act1, X, qkv, ffh, heads, scores, total;
 };
 
 WsPlan ws_plan(const lilicorr_dims& d, int64_t batch, int B, int K, int esize) {
@@ -191,7 +191,6 @@ WsPlan ws_plan(const lilicorr_dims& d, int64_t batch, int B, int K, int esize) {
   p.qkv = take(size_t(M) * 6 * H * 2);
   p.ffh = take(size_t(M) * 2 * F * 2);
   p.heads = take(size_t(M) * 2 * E * 4);
-  p.anchor = take(size_t(batch) * E * 4);
   p.scores = take(size_t(rows) * K * K * 4);
   p.total = off;
   return p;
@@ -444,6 +443,11 @@ lilicorr_status lilicorr_rerank(const lilicorr_weights* w, const void* logits,
   if (!logits || !tokens || !path_score) return LILICORR_ERR_INVALID_ARG;
   const int es = ldtype == LILICORR_BF16 ? 2 : 4;
   if (reinterpret_cast<uintptr_t>(logits) % es) return LILICORR_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(slot_hidden) % 16 || reinterpret_cast<uintptr_t>(target_state) % 16)
+  {
+    lilicorr::set_last_error("slot_hidden / target_state must be 16-byte aligned");
+    return LILICORR_ERR_INVALID_ARG;
+  }
   const WsPlan pl = ws_plan(w->d, batch, B, K, es);
   if (!workspace || workspace_bytes < pl.total || reinterpret_cast<uintptr_t>(workspace) % 256)
     return LILICORR_ERR_WORKSPACE;
@@ -465,7 +469,6 @@ lilicorr_status lilicorr_rerank(const lilicorr_weights* w, const void* logits,
   __nv_bfloat16* qkv = reinterpret_cast<__nv_bfloat16*>(ws + pl.qkv);
   __nv_bfloat16* ffh = reinterpret_cast<__nv_bfloat16*>(ws + pl.ffh);
   float* heads = reinterpret_cast<float*>(ws + pl.heads);
-  float* anchor_raw = reinterpret_cast<float*>(ws + pl.anchor);
   const __nv_bfloat16* target = static_cast<const __nv_bfloat16*>(target_state);
 
   CallTimer tm;
@@ -538,12 +541,9 @@ lilicorr_status lilicorr_rerank(const lilicorr_weights* w, const void* logits,
     LC_CUDA(launch_gemm(EPI_F32, g, stream), "heads gemm");
     MARK(T_HEADS);
   }
-  LC_CUDA(launch_anchor(target, w->anchor_w, w->anchor_b, batch, H, E, anchor_raw, stream),
-          "anchor head");
-  MARK(T_ANCHOR);
-  // a4 scores + a5 walk
-  LC_CUDA(launch_pair_scores(heads, anchor_raw, batch, B, K, E, d.sigma, scores, tp.out_vec,
-                             tp.in_vec, tp.anchor_vec, stream),
+  // a4 scores (with the anchor head) + a5 walk
+  LC_CUDA(launch_pair_scores(heads, target, w->anchor_w, w->anchor_b, batch, B, K, E, H, d.sigma,
+                             scores, tp.out_vec, tp.in_vec, tp.anchor_vec, stream),
           "pair scores");
   MARK(T_SCORES);
   LC_CUDA(launch_greedy_walk(scores, cand_id, anchor_ids, batch, B, K, tokens, tp.choice,

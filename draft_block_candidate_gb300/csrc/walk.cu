@@ -15,10 +15,12 @@
 namespace lilicorr {
 
 // One CTA per (block b, pair p).  heads [batch*S, 2E] holds the raw out | in head
-// outputs; anchor_raw [batch, E] the raw anchor head output.  Vectors are normalised
-// here (nrm(v) = v / max(||v||, 1e-12)) and dotted in f32.
+// outputs.  The p == 0 CTA of a block also evaluates the anchor head on the block's
+// target state (anchor_raw = Wa t + ba, f32 accumulation of exact bf16 products).
+// Vectors are normalised here (nrm(v) = v / max(||v||, 1e-12)) and dotted in f32.
 __global__ void __launch_bounds__(256) pair_scores_kernel(
-    const float* __restrict__ heads, const float* __restrict__ anchor_raw, int B, int K, int E,
+    const float* __restrict__ heads, const __nv_bfloat16* __restrict__ target,
+    const __nv_bfloat16* __restrict__ Wa, const float* __restrict__ ba, int B, int K, int E, int H,
     float sigma, float* __restrict__ scores, float* __restrict__ out_tap,
     float* __restrict__ in_tap, float* __restrict__ anchor_tap) {
   extern __shared__ float ps_smem[];
@@ -30,6 +32,30 @@ __global__ void __launch_bounds__(256) pair_scores_kernel(
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
   const int64_t blk_row0 = int64_t(b) * S;
 
+  if (p == 0) {
+    // raw anchor head output for this block, into row 0 of so
+    const __nv_bfloat16* t = target ? target + int64_t(b) * H : nullptr;
+    for (int e = warp; e < E; e += nw) {
+      float acc = 0.f;
+      if (t)
+        for (int h = lane * 8; h < H; h += 256) {
+          const uint4 wa = __ldg(reinterpret_cast<const uint4*>(Wa + int64_t(e) * H + h));
+          const uint4 tv = __ldg(reinterpret_cast<const uint4*>(t + h));
+          const uint32_t aw[4] = {wa.x, wa.y, wa.z, wa.w}, tw[4] = {tv.x, tv.y, tv.z, tv.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            acc = fmaf(__uint_as_float(aw[j] << 16), __uint_as_float(tw[j] << 16), acc);
+            acc = fmaf(__uint_as_float(aw[j] & 0xffff0000u), __uint_as_float(tw[j] & 0xffff0000u),
+                       acc);
+          }
+        }
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) acc += __shfl_xor_sync(FULL_MASK, acc, o);
+      if (lane == 0) so[e] = acc + ba[e];
+    }
+    __syncthreads();
+  }
+
   // rows to normalise: out rows of slot p (p >= 1) or the anchor (p == 0); in rows of
   // slot p+1; the p == 0 CTA also normalises slot B-1's out rows for the tap.
   const int n_out = (p == 0) ? 1 : K;
@@ -39,7 +65,7 @@ __global__ void __launch_bounds__(256) pair_scores_kernel(
     float* tap = nullptr;
     if (r < n_out) {
       if (p == 0) {
-        src = anchor_raw + int64_t(b) * E;
+        src = so;  // normalised in place
         tap = anchor_tap ? anchor_tap + int64_t(b) * E : nullptr;
       } else {
         const int64_t row = blk_row0 + int64_t(p - 1) * K + r;
@@ -99,19 +125,30 @@ __global__ void __launch_bounds__(256) pair_scores_kernel(
   }
 }
 
-// One warp per block: B-1 dependent argmaxes over K <= 32 candidates.
-__global__ void __launch_bounds__(128) greedy_walk_kernel(
+// One warp per block: the block's (B-1) K x K scores are staged in shared memory with
+// independent coalesced loads, then the B-1 dependent argmaxes over K <= 32 candidates
+// run from there.
+__global__ void __launch_bounds__(32) greedy_walk_kernel(
     const float* __restrict__ scores, const int32_t* __restrict__ cand_id,
     const int32_t* __restrict__ anchor_ids, int64_t batch, int B, int K,
-    int32_t* __restrict__ tokens, int32_t* __restrict__ choice, float* __restrict__ path) {
+    int32_t* __restrict__ tokens, int32_t* __restrict__ choice, float* __restrict__ path,
+    bool staged) {
+  extern __shared__ float gw_smem[];
   const int lane = threadIdx.x & 31;
-  const int64_t b = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int64_t b = blockIdx.x;
   if (b >= batch) return;
+  const int n = (B - 1) * K * K;
+  const float* src = scores + b * n;
+  if (staged) {
+    for (int i = lane; i < n; i += 32) gw_smem[i] = __ldg(src + i);
+    __syncwarp();
+  }
+  const float* sc = staged ? gw_smem : src;
   if (lane == 0) tokens[b * B] = anchor_ids ? anchor_ids[b] : -1;
   int prev = 0;
   for (int p = 0; p < B - 1; ++p) {
     const int64_t pr = b * (B - 1) + p;
-    const float* row = scores + (pr * K + prev) * K;
+    const float* row = sc + (p * K + prev) * K;
     float v = lane < K ? row[lane] : -INFINITY;
     int idx = lane < K ? lane : INT_MAX;
 #pragma unroll
@@ -126,15 +163,18 @@ __global__ void __launch_bounds__(128) greedy_walk_kernel(
     if (lane == 0) {
       if (choice) choice[pr] = idx;
       if (path) path[pr] = v;
-      tokens[b * B + p + 1] = cand_id[pr * K + idx];
+      tokens[b * B + p + 1] = __ldg(cand_id + pr * K + idx);
     }
     prev = idx;
   }
 }
 
-cudaError_t launch_pair_scores(const float* heads, const float* anchor_raw, int64_t batch, int B,
-                               int K, int E, float sigma, float* scores, float* out_tap,
+cudaError_t launch_pair_scores(const float* heads, const __nv_bfloat16* target,
+                               const __nv_bfloat16* Wa, const float* ba, int64_t batch, int B,
+                               int K, int E, int H, float sigma, float* scores, float* out_tap,
                                float* in_tap, float* anchor_tap, cudaStream_t stream) {
+  if (H % 8 || (reinterpret_cast<uintptr_t>(Wa) % 16) || (reinterpret_cast<uintptr_t>(target) % 16))
+    return cudaErrorInvalidValue;
   const size_t smem = size_t(2) * K * (E + 1) * sizeof(float);
   static bool attr = false;
   if (!attr) {
@@ -143,7 +183,7 @@ cudaError_t launch_pair_scores(const float* heads, const float* anchor_raw, int6
     attr = true;
   }
   const dim3 grid(B - 1, static_cast<unsigned>(batch));
-  pair_scores_kernel<<<grid, 256, smem, stream>>>(heads, anchor_raw, B, K, E, sigma, scores,
+  pair_scores_kernel<<<grid, 256, smem, stream>>>(heads, target, Wa, ba, B, K, E, H, sigma, scores,
                                                   out_tap, in_tap, anchor_tap);
   note_launch();
   return cudaGetLastError();
@@ -153,10 +193,17 @@ cudaError_t launch_greedy_walk(const float* scores, const int32_t* cand_id,
                                const int32_t* anchor_ids, int64_t batch, int B, int K,
                                int32_t* tokens, int32_t* choice, float* path,
                                cudaStream_t stream) {
-  const int wpb = 4;
-  const unsigned grid = static_cast<unsigned>((batch + wpb - 1) / wpb);
-  greedy_walk_kernel<<<grid, 32 * wpb, 0, stream>>>(scores, cand_id, anchor_ids, batch, B, K,
-                                                     tokens, choice, path);
+  constexpr size_t kMaxStage = 96 * 1024;
+  const size_t need = size_t(B - 1) * K * K * sizeof(float);
+  const bool staged = need <= kMaxStage;  // otherwise the walk reads the scores in place
+  static bool attr = false;
+  if (!attr) {
+    cudaFuncSetAttribute(greedy_walk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         static_cast<int>(kMaxStage));
+    attr = true;
+  }
+  greedy_walk_kernel<<<static_cast<unsigned>(batch), 32, staged ? need : 0, stream>>>(
+      scores, cand_id, anchor_ids, batch, B, K, tokens, choice, path, staged);
   note_launch();
   return cudaGetLastError();
 }

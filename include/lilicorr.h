@@ -117,6 +117,7 @@ typedef struct {
  *   B            2 <= B <= dims.B_max;  V == dims.V;  1 <= K <= min(dims.K_max, V)
  *   slot_hidden  nullable [batch,B,H] bf16: drafter hidden per slot (row 0 unused)
  *   target_state nullable [batch,H] bf16: projected target state t
+ *                (both 16-byte aligned, else LILICORR_ERR_INVALID_ARG)
  *   anchor_ids   nullable [batch] int32: written to tokens[:,0] (else -1)
  *   tokens       [batch,B] int32 out;  path_score [batch,B-1] f32 out:
  *                path_score[b,s-1] = phi(s-1, c_{s-1}, c_s)
