@@ -13,12 +13,13 @@
 //   warp 1     MMA: S = Qh Kh^T + Qh Kl^T + Ql Kh^T (M 128, N 256, K 64), then
 //              O = Ph Vh + Ph Vl + Pl Vh with P read from TMEM and V as an MN-major
 //              shared-memory operand
-//   warps 2-9  two warps per query-row quarter, each taking half of the keys: pass 1
-//              scales, adds the slot bias (one table lookup), masks keys beyond the
-//              block, takes the row max (halves combined through shared memory) and
-//              writes the logits back to TMEM; pass 2 forms p = exp(s - max) and its sum
-//              and writes p as packed bf16 hi / lo over the logits it came from; the
-//              epilogue divides O by the sum and stores it split (hi | lo).
+//   warps 2-17 four warps per query-row quarter, each taking a quarter of the keys:
+//              pass 1 scales, adds the slot bias (a per-query-slot row of the head's
+//              bias table, -inf beyond the block; one 16-byte load per four keys) and
+//              takes the row max (the four parts combined through shared memory); pass 2
+//              recomputes the biased logit, forms p = 2^(x - max) and its sum and writes
+//              p as packed bf16 hi / lo over the logits it came from; the epilogue
+//              divides this warp's 16 columns of O by the sum and stores them split.
 // Every mbarrier wait is bounded; on a timeout the CTA records it and still frees TMEM.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -29,7 +30,10 @@ namespace lilicorr {
 
 static __device__ uint32_t g_err_at;
 
-constexpr int AT_DH = 64, AT_QT = 128, AT_KMAX = 256, AT_SOFT_WARPS = 8;
+constexpr int AT_DH = 64, AT_QT = 128, AT_KMAX = 256, AT_SOFT_WARPS = 16;
+constexpr int AT_NSPLIT = AT_SOFT_WARPS / 4;      // softmax warps per 32-row quarter
+constexpr int AT_KW = AT_KMAX / AT_NSPLIT;        // keys per softmax warp
+constexpr int AT_OW = AT_DH / AT_NSPLIT;          // output columns per softmax warp
 constexpr int AT_THREADS = 32 * (2 + AT_SOFT_WARPS);
 constexpr int AT_TILE = 128 * 64 * 2;  // one [128 x 64] bf16 swizzled tile
 constexpr int AT_SMEM = 10 * AT_TILE + 1024;  // + the bias table, sized per launch
@@ -108,24 +112,18 @@ __device__ __forceinline__ void at_ld32(uint32_t taddr, float (&v)[32]) {
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
-__device__ __forceinline__ void at_st32(uint32_t taddr, const float (&v)[32]) {
+__device__ __forceinline__ void at_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
   asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
-      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
-      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
-      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
-      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
-      "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
-      "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
-      "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
-      "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
-      "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
-      "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
-      : "memory");
-  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 __device__ __forceinline__ void at_st16(uint32_t taddr, const uint32_t (&v)[16]) {
   asm volatile(
@@ -184,7 +182,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   __shared__ __align__(8) uint64_t bar_qk, bar_qkfree, bar_v, bar_vfree, bar_s, bar_p, bar_o,
       bar_ofree;
   __shared__ uint32_t s_tmem;
-  __shared__ float s_pmax[2][128], s_psum[2][128];
+  __shared__ float s_pmax[AT_NSPLIT][128], s_psum[AT_NSPLIT][128];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int QT = (S + AT_QT - 1) / AT_QT;
@@ -284,7 +282,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     const int qq = warp & 3, hf = (warp - 2) >> 2;
     const int r = 32 * qq + lane;  // TMEM lane = query row of the tile
     const uint32_t lane_off = uint32_t(32 * qq) << 16;
-    const int j0 = 128 * hf;       // this warp's keys j0 .. j0 + 127
+    const int j0 = AT_KW * hf;     // this warp's keys j0 .. j0 + AT_KW - 1
     const int nq = S / Kc;         // query slots
     constexpr float C = 0.125f * AT_LOG2E;  // 1 / sqrt(64), in log2 units
     int i = 0;
@@ -315,7 +313,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       // pass 1: row max of the biased, masked logits (log2 units)
       float mx = -INFINITY;
 #pragma unroll 1
-      for (int cc = 0; cc < 4; ++cc) {
+      for (int cc = 0; cc < AT_KW / 32; ++cc) {
         const int jb = j0 + 32 * cc;
         float v[32];
         at_ld32(tS + lane_off + jb, v);
@@ -328,11 +326,13 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       }
       s_pmax[hf][r] = mx;
       soft_sync();
-      const float m2 = fmaxf(s_pmax[0][r], s_pmax[1][r]);
+      float m2 = s_pmax[0][r];
+#pragma unroll
+      for (int k = 1; k < AT_NSPLIT; ++k) m2 = fmaxf(m2, s_pmax[k][r]);
       // pass 2: p = 2^(x - max) and its sum; p as packed bf16 hi / lo over its logits
       float l = 0.f;
 #pragma unroll 1
-      for (int cc = 0; cc < 4; ++cc) {
+      for (int cc = 0; cc < AT_KW / 32; ++cc) {
         const int jb = j0 + 32 * cc;
         float v[32];
         at_ld32(tS + lane_off + jb, v);
@@ -356,27 +356,24 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       at_fence_before();
       mbar_arrive(&bar_p);
       soft_sync();
-      const float inv = 1.0f / (s_psum[0][r] + s_psum[1][r]);
+      float lsum = 0.f;
+#pragma unroll
+      for (int k = 0; k < AT_NSPLIT; ++k) lsum += s_psum[k][r];
+      const float inv = 1.0f / lsum;
       // epilogue: O / l for this warp's 32 of the 64 output columns, split, stored
       ok = mbar_wait_bounded(&bar_o, i & 1, &g_err_at, ERR_AT_O) && ok;
       at_fence_after();
-      float v[32];
-      at_ld32(tO + lane_off + 32 * hf, v);
+      float v[AT_OW];
+      at_ld16(tO + lane_off + AT_OW * hf, v);
       at_fence_before();
       mbar_arrive(&bar_ofree);
       if (q < S && ok) {
-        __nv_bfloat16* dst = out + (tok0 + q) * 2 * H + h * AT_DH + 32 * hf;
-        uint32_t hi[16], lo[16];
+        __nv_bfloat16* dst = out + (tok0 + q) * 2 * H + h * AT_DH + AT_OW * hf;
+        uint32_t hi[AT_OW / 2], lo[AT_OW / 2];
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          __nv_bfloat16 ha, la, hb, lb;
-          split_bf16(v[e] * inv, ha, la);
-          split_bf16(v[e + 1] * inv, hb, lb);
-          hi[e / 2] = at_pack(ha, hb);
-          lo[e / 2] = at_pack(la, lb);
-        }
+        for (int e = 0; e < AT_OW; e += 2) at_split2(v[e] * inv, v[e + 1] * inv, hi[e / 2], lo[e / 2]);
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < AT_OW / 8; ++u) {
           *reinterpret_cast<uint4*>(dst + 8 * u) =
               make_uint4(hi[4 * u], hi[4 * u + 1], hi[4 * u + 2], hi[4 * u + 3]);
           *reinterpret_cast<uint4*>(dst + H + 8 * u) =

@@ -102,20 +102,40 @@ __device__ __forceinline__ void load8(const float* p, float (&v)[8]) {
 // lp = l - lse, p = exp(lp), gap = lp - lp of the slot's top candidate, r = k/(K-1),
 // top = [k == 0] (App. A: log-probability and probability under the full vocabulary,
 // the gap to the slot's most likely token, the rank normalised to [0,1], top indicator).
-// Eight rows per CTA (one per warp), each lane 8 consecutive hidden units per pass:
-// 16-byte hi and lo stores; W1 and b1 staged in shared memory once per CTA.
+// One warp per row at a time, each lane 8 consecutive hidden units per chunk: 16-byte hi
+// and lo stores.  A lane's first chunk of W1 / b1 stays in registers for all its rows.
+__device__ __forceinline__ void conf_chunk(const float (&f)[5], const float (&w)[8][6],
+                                           __nv_bfloat16* hi, __nv_bfloat16* lo) {
+  float u[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    float acc = w[j][5];
+#pragma unroll
+    for (int i = 0; i < 5; ++i) acc = fmaf(w[j][i], f[i], acc);
+    u[j] = silu(acc);
+  }
+  store_split8(u, hi, lo);
+}
+
+__device__ __forceinline__ void conf_load_w(const float* __restrict__ w1,
+                                            const float* __restrict__ b1, int h0,
+                                            float (&w)[8][6]) {
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+#pragma unroll
+    for (int i = 0; i < 5; ++i) w[j][i] = __ldg(w1 + (h0 + j) * 5 + i);
+    w[j][5] = __ldg(b1 + h0 + j);
+  }
+}
+
 __global__ void conf_hidden_kernel(const float* __restrict__ cand_logit,
                                    const float* __restrict__ lse, int64_t M, int K, int H,
                                    const float* __restrict__ w1, const float* __restrict__ b1,
                                    __nv_bfloat16* __restrict__ U) {
-  extern __shared__ float ch_smem[];  // [H][6]: w1 row (5) + bias
-  for (int i = threadIdx.x; i < H; i += blockDim.x) {
-#pragma unroll
-    for (int j = 0; j < 5; ++j) ch_smem[i * 6 + j] = w1[i * 5 + j];
-    ch_smem[i * 6 + 5] = b1[i];
-  }
-  __syncthreads();
   const int lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  const int nch = H / 8;
+  float w[8][6];
+  if (lane < nch) conf_load_w(w1, b1, lane * 8, w);
   for (int64_t m = int64_t(blockIdx.x) * nw + (threadIdx.x >> 5); m < M;
        m += int64_t(gridDim.x) * nw) {
     const int64_t row = m / K;  // (block, slot) row of the logit pass
@@ -129,17 +149,12 @@ __global__ void conf_hidden_kernel(const float* __restrict__ cand_logit,
     f[2] = lp - lp_top;
     f[3] = K > 1 ? float(k) / float(K - 1) : 0.f;
     f[4] = k == 0 ? 1.f : 0.f;
-    for (int h0 = lane * 8; h0 < H; h0 += 256) {
-      float u[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float* wr = ch_smem + (h0 + j) * 6;
-        float acc = wr[5];
-#pragma unroll
-        for (int i = 0; i < 5; ++i) acc = fmaf(wr[i], f[i], acc);
-        u[j] = silu(acc);
-      }
-      store_split8(u, U + m * 2 * H + h0, U + m * 2 * H + H + h0);
+    __nv_bfloat16* u = U + m * 2 * H;
+    if (lane < nch) conf_chunk(f, w, u + lane * 8, u + H + lane * 8);
+    for (int c = lane + 32; c < nch; c += 32) {  // hidden sizes above 256
+      float w2[8][6];
+      conf_load_w(w1, b1, c * 8, w2);
+      conf_chunk(f, w2, u + c * 8, u + H + c * 8);
     }
   }
 }
@@ -440,12 +455,11 @@ __global__ void fuse_concat_kernel(const float* __restrict__ X,
 cudaError_t launch_conf_hidden(const float* cand_logit, const float* lse, int64_t M, int K, int H,
                                const float* w1, const float* b1, __nv_bfloat16* U,
                                cudaStream_t stream) {
-  if (H % 8 || H > 2048) return cudaErrorInvalidValue;
+  if (H % 8) return cudaErrorInvalidValue;
   const int64_t rows_per_cta = 8;
   const unsigned grid =
-      static_cast<unsigned>(std::min<int64_t>((M + rows_per_cta - 1) / rows_per_cta, 152 * 32));
-  conf_hidden_kernel<<<grid, 256, size_t(H) * 6 * sizeof(float), stream>>>(cand_logit, lse, M, K,
-                                                                            H, w1, b1, U);
+      static_cast<unsigned>(std::min<int64_t>((M + rows_per_cta - 1) / rows_per_cta, 152 * 8));
+  conf_hidden_kernel<<<grid, 256, 0, stream>>>(cand_logit, lse, M, K, H, w1, b1, U);
   note_launch();
   return cudaGetLastError();
 }

@@ -23,8 +23,8 @@ __global__ void __launch_bounds__(256) pair_scores_kernel(
     const __nv_bfloat16* __restrict__ Wa, const float* __restrict__ ba, int B, int K, int E, int H,
     float sigma, float* __restrict__ scores, float* __restrict__ out_tap,
     float* __restrict__ in_tap, float* __restrict__ anchor_tap) {
-  extern __shared__ float ps_smem[];
-  const int E1 = E + 1;
+  extern __shared__ __align__(16) float ps_smem[];
+  const int E1 = E + 4;  // row pitch: 16-byte rows, rows of a warp on distinct banks
   float* so = ps_smem;            // [K][E1] out vectors of slot p (or o_0 in row 0)
   float* si = ps_smem + K * E1;   // [K][E1] in vectors of slot p+1
   const int p = blockIdx.x, b = blockIdx.y;
@@ -118,7 +118,14 @@ __global__ void __launch_bounds__(256) pair_scores_kernel(
       const float* a = so + k * E1;
       const float* c = si + kk * E1;
       float acc = 0.f;
-      for (int e = 0; e < E; ++e) acc = fmaf(a[e], c[e], acc);
+      for (int e = 0; e < E; e += 4) {  // E % 4 == 0
+        const float4 a4 = *reinterpret_cast<const float4*>(a + e);
+        const float4 c4 = *reinterpret_cast<const float4*>(c + e);
+        acc = fmaf(a4.x, c4.x, acc);
+        acc = fmaf(a4.y, c4.y, acc);
+        acc = fmaf(a4.z, c4.z, acc);
+        acc = fmaf(a4.w, c4.w, acc);
+      }
       v = sigma * acc;
     }
     dst[t] = v;
@@ -175,11 +182,12 @@ cudaError_t launch_pair_scores(const float* heads, const __nv_bfloat16* target,
                                float* in_tap, float* anchor_tap, cudaStream_t stream) {
   if (H % 8 || (reinterpret_cast<uintptr_t>(Wa) % 16) || (reinterpret_cast<uintptr_t>(target) % 16))
     return cudaErrorInvalidValue;
-  const size_t smem = size_t(2) * K * (E + 1) * sizeof(float);
+  if (E % 4) return cudaErrorInvalidValue;
+  const size_t smem = size_t(2) * K * (E + 4) * sizeof(float);
   static bool attr = false;
   if (!attr) {
     cudaFuncSetAttribute(pair_scores_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         2 * 32 * 257 * 4);
+                         2 * 32 * 260 * 4);
     attr = true;
   }
   const dim3 grid(B - 1, static_cast<unsigned>(batch));
