@@ -419,7 +419,8 @@ cudaError_t launch_attention(const __nv_bfloat16* qkv, int64_t batch, int S, int
 // ------------------------------------------------------------------ fusion input
 // out split [M, 6H] = [h, t, h*t]_hi | [h, t, h*t]_lo (App. A: "concatenating the
 // candidate state, the target state, and their elementwise product").
-// One thread per (row m, 8 consecutive columns): 16-byte stores of all six parts.
+// Fusion input without the target-state block: out split [M, 4H] = [h, h*t]_hi |
+// [h, h*t]_lo.  One thread per (row m, 8 consecutive columns), 16-byte stores.
 __global__ void fuse_concat_kernel(const float* __restrict__ X,
                                    const __nv_bfloat16* __restrict__ target, int S, int64_t M,
                                    int H, __nv_bfloat16* __restrict__ out) {
@@ -428,26 +429,65 @@ __global__ void fuse_concat_kernel(const float* __restrict__ X,
   if (idx >= M * hv) return;
   const int64_t m = idx / hv;
   const int h0 = static_cast<int>(idx % hv) * 8;
-  float x[8], t[8], xt[8];
+  float x[8], xt[8];
   load8(X + m * H + h0, x);
   if (target) {
     const uint4 w = __ldg(reinterpret_cast<const uint4*>(target + (m / S) * H + h0));
     const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      t[2 * j] = __uint_as_float(ww[j] << 16);
-      t[2 * j + 1] = __uint_as_float(ww[j] & 0xffff0000u);
+      xt[2 * j] = x[2 * j] * __uint_as_float(ww[j] << 16);
+      xt[2 * j + 1] = x[2 * j + 1] * __uint_as_float(ww[j] & 0xffff0000u);
     }
   } else {
 #pragma unroll
-    for (int j = 0; j < 8; ++j) t[j] = 0.f;
+    for (int j = 0; j < 8; ++j) xt[j] = 0.f;
   }
+  __nv_bfloat16* o = out + m * 4 * H;
+  store_split8(x, o + h0, o + 2 * H + h0);
+  store_split8(xt, o + H + h0, o + 3 * H + h0);
+}
+
+// Target-state term of the fusion layer, one per block: c[b, n] = Wt[n, :] . t_b + bf[n]
+// with Wt the middle H columns of fuse_w [H, 3H]; exact bf16 products summed in f32.
+__global__ void fuse_tbias_kernel(const __nv_bfloat16* __restrict__ target,
+                                  const __nv_bfloat16* __restrict__ fuse_w,
+                                  const float* __restrict__ fuse_b, int H, float* __restrict__ c) {
+  constexpr int R = 8;  // rows per warp pass, loads in flight together
+  const int64_t b = blockIdx.x;
+  const int lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  const __nv_bfloat16* t = target ? target + b * H : nullptr;
+  for (int n0 = (threadIdx.x >> 5) * R; n0 < H; n0 += nw * R) {
+    float acc[R];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) xt[j] = x[j] * t[j];
-  __nv_bfloat16* o = out + m * 6 * H;
-  store_split8(x, o + h0, o + 3 * H + h0);
-  store_split8(t, o + H + h0, o + 4 * H + h0);
-  store_split8(xt, o + 2 * H + h0, o + 5 * H + h0);
+    for (int r = 0; r < R; ++r) acc[r] = 0.f;
+    if (t)
+      for (int h = lane * 8; h < H; h += 256) {
+        const uint4 tv = __ldg(reinterpret_cast<const uint4*>(t + h));
+        const uint32_t tw[4] = {tv.x, tv.y, tv.z, tv.w};
+        uint4 wv[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+          wv[r] = n0 + r < H ? __ldg(reinterpret_cast<const uint4*>(fuse_w + int64_t(n0 + r) * 3 * H + H + h))
+                             : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          const uint32_t aw[4] = {wv[r].x, wv[r].y, wv[r].z, wv[r].w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            acc[r] = fmaf(__uint_as_float(aw[j] << 16), __uint_as_float(tw[j] << 16), acc[r]);
+            acc[r] = fmaf(__uint_as_float(aw[j] & 0xffff0000u), __uint_as_float(tw[j] & 0xffff0000u),
+                          acc[r]);
+          }
+        }
+      }
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) acc[r] += __shfl_xor_sync(FULL_MASK, acc[r], o);
+      if (lane == 0 && n0 + r < H) c[b * H + n0 + r] = acc[r] + fuse_b[n0 + r];
+    }
+  }
 }
 
 // ------------------------------------------------------------------ launchers
@@ -470,6 +510,15 @@ cudaError_t launch_rmsnorm_split(const float* X, const float* gain, int64_t M, i
   const int wpb = 8;
   rmsnorm_split_kernel<<<static_cast<unsigned>((M + wpb - 1) / wpb), wpb * 32, 0, stream>>>(
       X, gain, M, H, eps, out);
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fuse_tbias(const __nv_bfloat16* target, const __nv_bfloat16* fuse_w,
+                              const float* fuse_b, int64_t batch, int H, float* c,
+                              cudaStream_t stream) {
+  if (H % 8 || reinterpret_cast<uintptr_t>(target) % 16) return cudaErrorInvalidValue;
+  fuse_tbias_kernel<<<static_cast<unsigned>(batch), 256, 0, stream>>>(target, fuse_w, fuse_b, H, c);
   note_launch();
   return cudaGetLastError();
 }

@@ -27,19 +27,26 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
+
 #include "kernels.cuh"
 
 namespace lilicorr {
 
 static __device__ uint32_t g_err_tc;
 
-constexpr int TC_BM = 128, TC_BN = 256, TC_BK = 64, TC_STAGES = 3;
+constexpr int TC_BM = 128, TC_BN = 256, TC_BK = 64;
 constexpr int TC_EPI_WARPS = 8, TC_THREADS = 32 * (2 + TC_EPI_WARPS);
 constexpr int TC_A_BYTES = TC_BM * TC_BK * 2;
 constexpr int TC_B_BYTES = TC_BN * TC_BK * 2;
 constexpr int TC_STG_BYTES = 4096;  // one 32 x 32 output chunk (f32, or bf16 hi + lo)
-constexpr int TC_SMEM =
-    TC_STAGES * (TC_A_BYTES + TC_B_BYTES) + TC_EPI_WARPS * 2 * TC_STG_BYTES + 1024;
+// Shared memory of a configuration: operand ring of ST stages + NB epilogue staging
+// buffers per warp.  Two fit in 227 KB: 4 stages with 1 buffer (the default: more bytes
+// in flight for the operand stream) or 3 stages with 2 (for SiLU epilogues of short K,
+// where the epilogue, not the operand stream, sets the pace).
+__host__ __device__ constexpr int tc_smem(int st, int nb) {
+  return st * (TC_A_BYTES + TC_B_BYTES) + TC_EPI_WARPS * nb * TC_STG_BYTES + 1024;
+}
 constexpr uint32_t TC_TMEM_COLS = 2 * TC_BN;  // two accumulator buffers
 
 enum TcErr : uint32_t {
@@ -82,6 +89,9 @@ __device__ __forceinline__ void bulk_commit() {
 // Wait until at most one committed bulk group still reads shared memory.
 __device__ __forceinline__ void bulk_wait_read1() {
   asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read0() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 __device__ __forceinline__ void bulk_wait_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
@@ -273,9 +283,12 @@ template <int EPI>
 __device__ __forceinline__ void tc_epilogue_staged(const GemmArgs& g, const CUtensorMap* tmC,
                                                    uint8_t* stg, int lane, int64_t row0, int n,
                                                    float (&v)[32]) {
+  const float* bias = g.bias + n;
+  if (g.bias_group > 0)  // per-block bias row (rows past M reuse the last one)
+    bias += (std::min<int64_t>(row0 + lane, g.M - 1) / g.bias_group) * g.N;
 #pragma unroll
   for (int j = 0; j < 32; j += 4) {
-    const float4 b4 = __ldg(reinterpret_cast<const float4*>(g.bias + n + j));
+    const float4 b4 = __ldg(reinterpret_cast<const float4*>(bias + j));
     v[j] += b4.x;
     v[j + 1] += b4.y;
     v[j + 2] += b4.z;
@@ -333,7 +346,7 @@ __device__ __forceinline__ void tc_epilogue_staged(const GemmArgs& g, const CUte
 
 // ------------------------------------------------------------------ kernel
 
-template <int EPI>
+template <int EPI, int TC_STAGES, int TC_STG_BUFS>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const GemmArgs g) {
@@ -420,7 +433,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     // ---- epilogue: quarter q = warp % 4 owns TMEM lanes 32q..32q+31 (output rows);
     // the two warps of a quarter split the tile's columns in halves
     const int q = warp & 3, half = (warp - 2) >> 2;
-    uint8_t* stg = sStage + (warp - 2) * 2 * TC_STG_BYTES;
+    uint8_t* stg = sStage + (warp - 2) * TC_STG_BUFS * TC_STG_BYTES;
     int sb = 0;  // staging buffer of the next chunk
     int i = 0;
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
@@ -438,11 +451,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         if constexpr (EPI == EPI_NODE) {
           if (m < g.M && n < g.N) tc_epilogue32<EPI>(g, m, n, v);
         } else if (n < g.N) {
-          // the buffer written two chunks ago must have been read by its bulk copy
-          if (lane == 0) bulk_wait_read1();
+          // the buffer's previous bulk copy must have finished reading it
+          if (lane == 0) {
+            if constexpr (TC_STG_BUFS == 2)
+              bulk_wait_read1();
+            else
+              bulk_wait_read0();
+          }
           __syncwarp();
           tc_epilogue_staged<EPI>(g, &tmC, stg + sb * TC_STG_BYTES, lane, m0 + 32 * q, n, v);
-          sb ^= 1;
+          sb = (sb + 1) % TC_STG_BUFS;
         }
       }
       tc_fence_before();
@@ -530,11 +548,12 @@ cudaError_t launch_gemm(int epi, const GemmArgs& g, cudaStream_t stream) {
   }
   static bool attr = false;
   if (!attr) {
-    cudaFuncSetAttribute(gemm_tc_kernel<EPI_F32>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
-    cudaFuncSetAttribute(gemm_tc_kernel<EPI_RESID>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
-    cudaFuncSetAttribute(gemm_tc_kernel<EPI_SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
-    cudaFuncSetAttribute(gemm_tc_kernel<EPI_SPLIT_SILU>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
-    cudaFuncSetAttribute(gemm_tc_kernel<EPI_NODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
+    cudaFuncSetAttribute(gemm_tc_kernel<EPI_F32, 4, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, tc_smem(4, 1));
+    cudaFuncSetAttribute(gemm_tc_kernel<EPI_RESID, 4, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, tc_smem(4, 1));
+    cudaFuncSetAttribute(gemm_tc_kernel<EPI_SPLIT, 4, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, tc_smem(4, 1));
+    cudaFuncSetAttribute(gemm_tc_kernel<EPI_SPLIT_SILU, 4, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, tc_smem(4, 1));
+    cudaFuncSetAttribute(gemm_tc_kernel<EPI_SPLIT_SILU, 3, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, tc_smem(3, 2));
+    cudaFuncSetAttribute(gemm_tc_kernel<EPI_NODE, 4, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, tc_smem(4, 1));
     attr = true;
   }
   static int sms = 0;
@@ -546,12 +565,18 @@ cudaError_t launch_gemm(int epi, const GemmArgs& g, cudaStream_t stream) {
   }
   const int64_t ntiles = int64_t((g.N + TC_BN - 1) / TC_BN) * ((g.M + TC_BM - 1) / TC_BM);
   const dim3 grid(static_cast<unsigned>(ntiles < sms ? ntiles : sms));
+  constexpr int s41 = tc_smem(4, 1), s32 = tc_smem(3, 2);
   switch (epi) {
-    case EPI_F32: gemm_tc_kernel<EPI_F32><<<grid, TC_THREADS, TC_SMEM, stream>>>(ta, tb, tc, g); break;
-    case EPI_RESID: gemm_tc_kernel<EPI_RESID><<<grid, TC_THREADS, TC_SMEM, stream>>>(ta, tb, tc, g); break;
-    case EPI_SPLIT: gemm_tc_kernel<EPI_SPLIT><<<grid, TC_THREADS, TC_SMEM, stream>>>(ta, tb, tc, g); break;
-    case EPI_SPLIT_SILU: gemm_tc_kernel<EPI_SPLIT_SILU><<<grid, TC_THREADS, TC_SMEM, stream>>>(ta, tb, tc, g); break;
-    default: gemm_tc_kernel<EPI_NODE><<<grid, TC_THREADS, TC_SMEM, stream>>>(ta, tb, tc, g); break;
+    case EPI_F32: gemm_tc_kernel<EPI_F32, 4, 1><<<grid, TC_THREADS, s41, stream>>>(ta, tb, tc, g); break;
+    case EPI_RESID: gemm_tc_kernel<EPI_RESID, 4, 1><<<grid, TC_THREADS, s41, stream>>>(ta, tb, tc, g); break;
+    case EPI_SPLIT: gemm_tc_kernel<EPI_SPLIT, 4, 1><<<grid, TC_THREADS, s41, stream>>>(ta, tb, tc, g); break;
+    case EPI_SPLIT_SILU:
+      if (g.Ka <= 512)
+        gemm_tc_kernel<EPI_SPLIT_SILU, 3, 2><<<grid, TC_THREADS, s32, stream>>>(ta, tb, tc, g);
+      else
+        gemm_tc_kernel<EPI_SPLIT_SILU, 4, 1><<<grid, TC_THREADS, s41, stream>>>(ta, tb, tc, g);
+      break;
+    default: gemm_tc_kernel<EPI_NODE, 4, 1><<<grid, TC_THREADS, s41, stream>>>(ta, tb, tc, g); break;
   }
   note_launch();
   return cudaGetLastError();

@@ -33,7 +33,8 @@ struct GemmArgs {
   const __nv_bfloat16* W;  // [N, Kw]
   int64_t M;
   int N, Kw, Ka;
-  const float* bias;       // [N]
+  const float* bias;       // [N], or [M / bias_group, N] when bias_group > 0
+  int64_t bias_group;      // rows sharing one bias row (0: one bias for all rows)
   float* out;              // EPI_F32 / EPI_RESID / EPI_NODE: [M, N] f32
   __nv_bfloat16* out_split;  // EPI_SPLIT*: [M, 2N]
   // EPI_NODE extras: X = acc + bias + E[cand] + slot_table[s-1] + rank_table[k] + hidden
@@ -64,6 +65,9 @@ cudaError_t launch_attention_tc(const __nv_bfloat16* qkv, int64_t batch, int S, 
                                 int heads, int B_max, const float* dist_bias,
                                 const float* same_bias, __nv_bfloat16* out, cudaStream_t stream);
 cudaError_t at_read_device_error(uint32_t* code);
+cudaError_t launch_fuse_tbias(const __nv_bfloat16* target, const __nv_bfloat16* fuse_w,
+                              const float* fuse_b, int64_t batch, int H, float* c,
+                              cudaStream_t stream);
 cudaError_t launch_fuse_concat(const float* X, const __nv_bfloat16* target, int S, int64_t M,
                                int H, __nv_bfloat16* out, cudaStream_t stream);
 }  // namespace lilicorr

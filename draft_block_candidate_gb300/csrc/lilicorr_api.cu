@@ -89,7 +89,9 @@ struct lilicorr_weights {
   int device;
   void* arena;
   // bf16 (tensor-core operands and the gathered embedding)
-  const __nv_bfloat16 *embed, *conf_w2, *fuse_w, *heads_w, *anchor_w;
+  // fuse_w is [Wh | Wt | Wht] ([H, 3H]); fuse_w2 = [Wh | Wht] ([H, 2H]) for the
+  // contraction over [h, h*t]; the Wt t term is a per-block bias
+  const __nv_bfloat16 *embed, *conf_w2, *fuse_w, *fuse_w2, *heads_w, *anchor_w;
   // f32 (exact widening of the bf16 inputs)
   const float *slot_table, *rank_table, *conf_w1, *conf_b1, *conf_b2, *fuse_b, *heads_b, *anchor_b;
   struct Layer {
@@ -168,7 +170,7 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // Workspace layout of one rerank call.
 struct WsPlan {
-  size_t k1, cand_id, cand_logit, lse, act1, X, qkv, ffh, heads, scores, total;
+  size_t k1, cand_id, cand_logit, lse, act1, X, qkv, ffh, heads, scores, fuse_c, total;
 };
 
 WsPlan ws_plan(const lilicorr_dims& d, int64_t batch, int B, int K, int esize) {
@@ -192,6 +194,7 @@ WsPlan ws_plan(const lilicorr_dims& d, int64_t batch, int B, int K, int esize) {
   p.ffh = take(size_t(M) * 2 * F * 2);
   p.heads = take(size_t(M) * 2 * E * 4);
   p.scores = take(size_t(rows) * K * K * 4);
+  p.fuse_c = take(size_t(batch) * H * 4);
   p.total = off;
   return p;
 }
@@ -297,6 +300,19 @@ lilicorr_status lilicorr_weights_create(const lilicorr_dims* dims, const lilicor
     else
       put_bf16(kv.first, given[kv.first]->host_data, cnt);
   }
+  // fusion weight without its target-state block: [Wh | Wht] [H, 2H]
+  {
+    const int64_t H = dims->hidden;
+    const size_t o = align256(img.size());
+    img.resize(o + size_t(2 * H * H) * 2);
+    const uint8_t* src = static_cast<const uint8_t*>(given["fuse.w"]->host_data);
+    for (int64_t n = 0; n < H; ++n) {
+      std::memcpy(img.data() + o + size_t(n * 2 * H) * 2, src + size_t(n * 3 * H) * 2, size_t(H) * 2);
+      std::memcpy(img.data() + o + size_t(n * 2 * H + H) * 2, src + size_t(n * 3 * H + 2 * H) * 2,
+                  size_t(H) * 2);
+    }
+    off["fuse.w2"] = o;
+  }
   // out and in heads are one contraction: W = [Wout; Win] [2E, H], b = [bout; bin].
   {
     const int64_t EH = int64_t(dims->d_e) * dims->hidden;
@@ -342,6 +358,7 @@ lilicorr_status lilicorr_weights_create(const lilicorr_dims* dims, const lilicor
   w->embed = bf("embed");
   w->conf_w2 = bf("conf.w2");
   w->fuse_w = bf("fuse.w");
+  w->fuse_w2 = bf("fuse.w2");
   w->heads_w = bf("heads.w");
   w->anchor_w = bf("head_anchor.w");
   w->slot_table = f32("slot_table");
@@ -527,12 +544,16 @@ lilicorr_status lilicorr_rerank(const lilicorr_weights* w, const void* logits,
     LC_CUDA(cudaMemcpyAsync(tp.hidden, X, size_t(M) * H * 4, cudaMemcpyDeviceToDevice, stream),
             "hidden tap");
   // a4: fusion and heads
+  float* fuse_c = reinterpret_cast<float*>(ws + pl.fuse_c);
+  LC_CUDA(launch_fuse_tbias(target, w->fuse_w, w->fuse_b, batch, H, fuse_c, stream),
+          "fusion target term");
   LC_CUDA(launch_fuse_concat(X, target, S, M, H, qkv, stream), "fusion input");
   MARK(T_FUSECAT);
   {
+    // SiLU(Wh h + Wht (h*t) + [Wt t + bf]_block): A = [h, h*t] split, bias per block
     GemmArgs g{};
-    g.A = qkv; g.W = w->fuse_w; g.M = M; g.N = H; g.Kw = 3 * H; g.Ka = 6 * H; g.bias = w->fuse_b;
-    g.out_split = act1;
+    g.A = qkv; g.W = w->fuse_w2; g.M = M; g.N = H; g.Kw = 2 * H; g.Ka = 4 * H; g.bias = fuse_c;
+    g.bias_group = S; g.out_split = act1;
     LC_CUDA(launch_gemm(EPI_SPLIT_SILU, g, stream), "fusion gemm");
     MARK(T_FUSE);
     g = GemmArgs{};
