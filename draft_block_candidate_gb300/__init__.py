@@ -8,6 +8,7 @@ from .api import (  # noqa: F401
     Weights,
     device_error,
     greedy_walk,
+    viterbi,
     launch_count,
     rerank,
     rerank_host,

@@ -215,6 +215,24 @@ def greedy_walk(pair_scores: torch.Tensor, cand_id: torch.Tensor,
     return tokens, choice, path
 
 
+def viterbi(pair_scores: torch.Tensor, cand_id: torch.Tensor,
+            anchor_ids: Optional[torch.Tensor] = None, stream=None):
+    """lilicorr_viterbi on given scores [batch,B-1,K,K]: the exact best path,
+    (tokens, choice, path_score, total)."""
+    batch, Bm1, K, _ = pair_scores.shape
+    B = Bm1 + 1
+    dev = pair_scores.device
+    tokens = torch.empty(batch, B, dtype=torch.int32, device=dev)
+    choice = torch.empty(batch, Bm1, dtype=torch.int32, device=dev)
+    path = torch.empty(batch, Bm1, dtype=torch.float32, device=dev)
+    total = torch.empty(batch, dtype=torch.float64, device=dev)
+    st = L.lib().lilicorr_viterbi(_ptr(pair_scores), _ptr(cand_id), _ptr(anchor_ids), batch, B, K,
+                                  _ptr(tokens), _ptr(choice), _ptr(path), _ptr(total),
+                                  _stream(stream))
+    _check(st, "lilicorr_viterbi")
+    return tokens, choice, path, total
+
+
 def launch_count() -> int:
     return int(L.lib().lilicorr_launch_count())
 

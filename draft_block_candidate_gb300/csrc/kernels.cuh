@@ -20,6 +20,10 @@ cudaError_t launch_pair_scores(const float* heads, const __nv_bfloat16* target,
                                const __nv_bfloat16* Wa, const float* ba, int64_t batch, int B,
                                int K, int E, int H, float sigma, float* scores, float* out_tap,
                                float* in_tap, float* anchor_tap, cudaStream_t stream);
+cudaError_t launch_viterbi(const float* scores, const int32_t* cand_id,
+                           const int32_t* anchor_ids, int64_t batch, int B, int K,
+                           int32_t* tokens, int32_t* choice, float* path, double* total,
+                           cudaStream_t stream);
 cudaError_t launch_greedy_walk(const float* scores, const int32_t* cand_id,
                                const int32_t* anchor_ids, int64_t batch, int B, int K,
                                int32_t* tokens, int32_t* choice, float* path,

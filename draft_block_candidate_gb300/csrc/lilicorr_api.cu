@@ -449,6 +449,18 @@ lilicorr_status lilicorr_greedy_walk(const float* pair_scores, const int32_t* ca
   return LILICORR_OK;
 }
 
+lilicorr_status lilicorr_viterbi(const float* pair_scores, const int32_t* cand_id,
+                                 const int32_t* anchor_ids, int64_t batch, int32_t B, int32_t K,
+                                 int32_t* tokens, int32_t* choice, float* path_score,
+                                 double* total, void* stream) {
+  if (!pair_scores || !cand_id || !tokens) return LILICORR_ERR_INVALID_ARG;
+  if (batch < 1 || B < 2 || B > 64 || K < 1 || K > 32) return LILICORR_ERR_INVALID_ARG;
+  LC_CUDA(launch_viterbi(pair_scores, cand_id, anchor_ids, batch, B, K, tokens, choice,
+                         path_score, total, static_cast<cudaStream_t>(stream)),
+          "viterbi");
+  return LILICORR_OK;
+}
+
 lilicorr_status lilicorr_rerank(const lilicorr_weights* w, const void* logits,
                                 lilicorr_dtype ldtype, int64_t batch, int32_t B, int64_t V,
                                 int32_t K, const void* slot_hidden, const void* target_state,

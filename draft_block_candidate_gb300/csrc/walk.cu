@@ -176,6 +176,82 @@ __global__ void __launch_bounds__(32) greedy_walk_kernel(
   }
 }
 
+// Exact best path (LiLiCorr App. E, Eq. 12): maximise g(c) = sum_s phi(s-1, c_{s-1}, c_s)
+// by max-plus dynamic programming over the same scores, one warp per block, lane k' =
+// candidate k' of the current slot.  Path sums are accumulated in double from the f32
+// scores (each step is one addition per (k, k'), so the sums are those of the plain
+// definition); ties go to the lowest k, both for the back pointers and for the final
+// candidate.  Back pointers live in shared memory; lane 0 traces the path back.
+__global__ void __launch_bounds__(32) viterbi_kernel(
+    const float* __restrict__ scores, const int32_t* __restrict__ cand_id,
+    const int32_t* __restrict__ anchor_ids, int64_t batch, int B, int K,
+    int32_t* __restrict__ tokens, int32_t* __restrict__ choice, float* __restrict__ path,
+    double* __restrict__ total, bool staged) {
+  extern __shared__ __align__(16) float vt_smem[];
+  const int lane = threadIdx.x & 31;
+  const int64_t b = blockIdx.x;
+  if (b >= batch) return;
+  const int Bm1 = B - 1, KK = K * K;
+  const int n = Bm1 * KK;
+  const float* src = scores + b * n;
+  if (staged)
+    for (int i = lane; i < n; i += 32) vt_smem[i] = __ldg(src + i);
+  uint8_t* back = reinterpret_cast<uint8_t*>(vt_smem + (staged ? n : 0));  // [B-1][K]
+  int* chosen = reinterpret_cast<int*>(back + ((Bm1 * K + 15) & ~15));     // [B-1]
+  __syncwarp();
+  const float* sc = staged ? vt_smem : src;
+  double best = lane < K ? double(sc[lane]) : -INFINITY;  // pair 0 uses row 0 only
+  for (int s = 1; s < Bm1; ++s) {
+    const float* zs = sc + s * KK;
+    double nb = -INFINITY;
+    int arg = 0;
+    for (int k = 0; k < K; ++k) {
+      const double bk = __shfl_sync(FULL_MASK, best, k);
+      if (lane < K) {
+        const double c = bk + double(zs[k * K + lane]);
+        if (c > nb) {
+          nb = c;
+          arg = k;
+        }
+      }
+    }
+    if (lane < K) back[s * K + lane] = static_cast<uint8_t>(arg);
+    best = lane < K ? nb : -INFINITY;
+  }
+  // final candidate: the best total, lowest k on ties
+  double v = best;
+  int idx = lane < K ? lane : INT_MAX;
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    const double ov = __shfl_xor_sync(FULL_MASK, v, o);
+    const int oi = __shfl_xor_sync(FULL_MASK, idx, o);
+    if (ov > v || (ov == v && oi < idx)) {
+      v = ov;
+      idx = oi;
+    }
+  }
+  __syncwarp();
+  if (lane == 0) {
+    int c = idx;
+    chosen[Bm1 - 1] = c;
+    for (int s = Bm1 - 1; s >= 1; --s) {
+      c = back[s * K + c];
+      chosen[s - 1] = c;
+    }
+    if (total) total[b] = v;
+    tokens[b * B] = anchor_ids ? anchor_ids[b] : -1;
+  }
+  __syncwarp();
+  for (int s = lane; s < Bm1; s += 32) {
+    const int c = chosen[s];
+    const int prev = s == 0 ? 0 : chosen[s - 1];
+    const int64_t pr = b * Bm1 + s;
+    if (choice) choice[pr] = c;
+    if (path) path[pr] = sc[s * KK + prev * K + c];
+    tokens[b * B + s + 1] = __ldg(cand_id + pr * K + c);
+  }
+}
+
 cudaError_t launch_pair_scores(const float* heads, const __nv_bfloat16* target,
                                const __nv_bfloat16* Wa, const float* ba, int64_t batch, int B,
                                int K, int E, int H, float sigma, float* scores, float* out_tap,
@@ -212,6 +288,26 @@ cudaError_t launch_greedy_walk(const float* scores, const int32_t* cand_id,
   }
   greedy_walk_kernel<<<static_cast<unsigned>(batch), 32, staged ? need : 0, stream>>>(
       scores, cand_id, anchor_ids, batch, B, K, tokens, choice, path, staged);
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_viterbi(const float* scores, const int32_t* cand_id,
+                           const int32_t* anchor_ids, int64_t batch, int B, int K,
+                           int32_t* tokens, int32_t* choice, float* path, double* total,
+                           cudaStream_t stream) {
+  constexpr size_t kMaxStage = 96 * 1024;
+  const size_t need = size_t(B - 1) * K * K * sizeof(float);
+  const bool staged = need <= kMaxStage;  // otherwise the scores are read in place
+  const size_t aux = ((size_t(B - 1) * K + 15) & ~size_t(15)) + size_t(B - 1) * sizeof(int);
+  static bool attr = false;
+  if (!attr) {
+    cudaFuncSetAttribute(viterbi_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         static_cast<int>(kMaxStage + 4096));
+    attr = true;
+  }
+  viterbi_kernel<<<static_cast<unsigned>(batch), 32, (staged ? need : 0) + aux, stream>>>(
+      scores, cand_id, anchor_ids, batch, B, K, tokens, choice, path, total, staged);
   note_launch();
   return cudaGetLastError();
 }

@@ -192,6 +192,19 @@ lilicorr_status lilicorr_greedy_walk(const float* pair_scores, const int32_t* ca
                                      int32_t K, int32_t* tokens, int32_t* choice,
                                      float* path_score, void* stream);
 
+/* Exact best path on given scores (LiLiCorr App. E, Eq. 12; the follow-on the serving
+ * write-up ranks first): the path c maximising g(c) = sum_s pair_scores[b,s-1,c_{s-1},c_s]
+ * (c_0 = 0, so pair 0 uses its row 0), by max-plus dynamic programming with traceback.
+ * Path sums are formed in double from the f32 scores; ties go to the lowest k, for every
+ * back pointer and for the final candidate.  Same layouts as lilicorr_greedy_walk;
+ * total [batch] (nullable, f64) receives g of the chosen path.  1 <= K <= 32,
+ * 2 <= B <= 64.  Errors: LILICORR_ERR_INVALID_ARG for null required pointers or sizes
+ * out of range, LILICORR_ERR_CUDA for a failed launch. */
+lilicorr_status lilicorr_viterbi(const float* pair_scores, const int32_t* cand_id,
+                                 const int32_t* anchor_ids, int64_t batch, int32_t B,
+                                 int32_t K, int32_t* tokens, int32_t* choice,
+                                 float* path_score, double* total, void* stream);
+
 /* Human-readable name of a status; never NULL. */
 const char* lilicorr_status_string(lilicorr_status s);
 /* Message of the most recent CUDA failure in this thread ("" if none). */

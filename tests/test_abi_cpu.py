@@ -142,3 +142,11 @@ def test_binding_refuses_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(_lib, "_lib", None)
     with pytest.raises(RuntimeError, match="no non-CUDA path"):
         _lib.lib()
+
+
+def test_viterbi_argument_checks(lib):
+    p = C.c_void_p(16)
+    assert lib.lilicorr_viterbi(p, p, None, 1, 16, 33, p, None, None, None, None) == 1
+    assert lib.lilicorr_viterbi(p, p, None, 1, 65, 4, p, None, None, None, None) == 1
+    assert lib.lilicorr_viterbi(None, p, None, 1, 16, 4, p, None, None, None, None) == 1
+    assert lib.lilicorr_viterbi(p, p, None, 0, 16, 4, p, None, None, None, None) == 1
