@@ -120,6 +120,8 @@ def recorded_traffic(kernel: str):
     if not os.path.exists(path):
         return None
     for line in open(path):
+        if line.lstrip().startswith("#"):
+            continue
         f = dict(kv.split("=", 1) for kv in line.split() if "=" in kv)
         if f.get("kernel") != kernel:
             continue
@@ -283,7 +285,7 @@ def run_gb300(a):
     # executed tensor work per launch (split-bf16: the contraction dimension is doubled)
     gemm_flops = {"qkv_gemm": 2 * M * 3 * H * 2 * H, "out_gemm": 2 * M * H * 2 * H,
                   "ffn1_gemm": 2 * M * F * 2 * H, "ffn2_gemm": 2 * M * H * 2 * F,
-                  "node_gemm": 2 * M * H * 2 * H, "fuse_gemm": 2 * M * H * 6 * H,
+                  "node_gemm": 2 * M * H * 2 * H, "fuse_gemm": 2 * M * H * 4 * H,
                   "heads_gemm": 2 * M * 2 * E * 2 * H}
     # attention: executed tensor work per launch (three-term split products, 128-query
     # tiles, 256 key columns): S = Q K^T and O = P V
