@@ -13,6 +13,7 @@ from .api import (  # noqa: F401
     rerank,
     rerank_host,
     rerank_host_workspace,
+    sample_walk,
     stage_timing,
     stage_times,
     topk_lse,

@@ -233,6 +233,27 @@ def viterbi(pair_scores: torch.Tensor, cand_id: torch.Tensor,
     return tokens, choice, path, total
 
 
+def sample_walk(pair_scores: torch.Tensor, cand_id: torch.Tensor,
+                temperature: Optional[torch.Tensor] = None,
+                uniforms: Optional[torch.Tensor] = None,
+                anchor_ids: Optional[torch.Tensor] = None, stream=None):
+    """lilicorr_sample_walk on given scores [batch,B-1,K,K] with per-row temperature
+    [batch] and uniforms [batch,B-1]: (tokens, choice, path_score, proposal)."""
+    batch, Bm1, K, _ = pair_scores.shape
+    B = Bm1 + 1
+    dev = pair_scores.device
+    tokens = torch.empty(batch, B, dtype=torch.int32, device=dev)
+    choice = torch.empty(batch, Bm1, dtype=torch.int32, device=dev)
+    path = torch.empty(batch, Bm1, dtype=torch.float32, device=dev)
+    prop = torch.empty(batch, Bm1, K, dtype=torch.float32, device=dev)
+    st = L.lib().lilicorr_sample_walk(_ptr(pair_scores), _ptr(cand_id), _ptr(anchor_ids),
+                                      _ptr(temperature), _ptr(uniforms), batch, B, K,
+                                      _ptr(tokens), _ptr(choice), _ptr(path), _ptr(prop),
+                                      _stream(stream))
+    _check(st, "lilicorr_sample_walk")
+    return tokens, choice, path, prop
+
+
 def launch_count() -> int:
     return int(L.lib().lilicorr_launch_count())
 

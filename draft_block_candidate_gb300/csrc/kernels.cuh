@@ -24,6 +24,11 @@ cudaError_t launch_viterbi(const float* scores, const int32_t* cand_id,
                            const int32_t* anchor_ids, int64_t batch, int B, int K,
                            int32_t* tokens, int32_t* choice, float* path, double* total,
                            cudaStream_t stream);
+cudaError_t launch_sample_walk(const float* scores, const int32_t* cand_id,
+                               const int32_t* anchor_ids, const float* temperature,
+                               const float* uniforms, int64_t batch, int B, int K,
+                               int32_t* tokens, int32_t* choice, float* path, float* proposal,
+                               cudaStream_t stream);
 cudaError_t launch_greedy_walk(const float* scores, const int32_t* cand_id,
                                const int32_t* anchor_ids, int64_t batch, int B, int K,
                                int32_t* tokens, int32_t* choice, float* path,

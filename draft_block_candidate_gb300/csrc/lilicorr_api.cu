@@ -461,6 +461,21 @@ lilicorr_status lilicorr_viterbi(const float* pair_scores, const int32_t* cand_i
   return LILICORR_OK;
 }
 
+lilicorr_status lilicorr_sample_walk(const float* pair_scores, const int32_t* cand_id,
+                                     const int32_t* anchor_ids, const float* temperature,
+                                     const float* uniforms, int64_t batch, int32_t B,
+                                     int32_t K, int32_t* tokens, int32_t* choice,
+                                     float* path_score, float* proposal, void* stream) {
+  if (!pair_scores || !cand_id || !tokens) return LILICORR_ERR_INVALID_ARG;
+  if (temperature && !uniforms) return LILICORR_ERR_INVALID_ARG;
+  if (batch < 1 || B < 2 || K < 1 || K > 32) return LILICORR_ERR_INVALID_ARG;
+  LC_CUDA(launch_sample_walk(pair_scores, cand_id, anchor_ids, temperature, uniforms, batch, B,
+                             K, tokens, choice, path_score, proposal,
+                             static_cast<cudaStream_t>(stream)),
+          "sample walk");
+  return LILICORR_OK;
+}
+
 lilicorr_status lilicorr_rerank(const lilicorr_weights* w, const void* logits,
                                 lilicorr_dtype ldtype, int64_t batch, int32_t B, int64_t V,
                                 int32_t K, const void* slot_hidden, const void* target_state,

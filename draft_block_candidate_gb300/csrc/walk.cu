@@ -252,6 +252,79 @@ __global__ void __launch_bounds__(32) viterbi_kernel(
   }
 }
 
+// Sampled commit (serving PR, "Sampling the committed path"; LiLiCorr Eq. 2): each
+// slot draws c_s from softmax_k(z_s[k] / T_b) given the previous draw, by inverse CDF
+// with the caller's uniform u[b, s]: w_k = exp((z_k - max z) / T) in double, W = their
+// sum in k order, c_s = the first k whose running sum exceeds u * W (the last k with
+// w > 0 if rounding leaves none).  Rows with T_b <= 0 (or no temperature array) take the
+// same f32 argmax, lowest k on ties, as the greedy walk and publish a one-hot proposal.
+// One warp per block; lane k holds candidate k; lane 0 forms the running sums in order.
+__global__ void __launch_bounds__(32) sample_walk_kernel(
+    const float* __restrict__ scores, const int32_t* __restrict__ cand_id,
+    const int32_t* __restrict__ anchor_ids, const float* __restrict__ temperature,
+    const float* __restrict__ uniforms, int64_t batch, int B, int K,
+    int32_t* __restrict__ tokens, int32_t* __restrict__ choice, float* __restrict__ path,
+    float* __restrict__ proposal) {
+  __shared__ double s_w[32];
+  const int lane = threadIdx.x & 31;
+  const int64_t b = blockIdx.x;
+  if (b >= batch) return;
+  const int Bm1 = B - 1;
+  const float T = temperature ? temperature[b] : 0.f;
+  const float* src = scores + b * int64_t(Bm1) * K * K;
+  if (lane == 0) tokens[b * B] = anchor_ids ? anchor_ids[b] : -1;
+  int prev = 0;
+  for (int s = 0; s < Bm1; ++s) {
+    const int64_t pr = b * Bm1 + s;
+    const float z = lane < K ? __ldg(src + (int64_t(s) * K + prev) * K + lane) : -INFINITY;
+    // f32 argmax, lowest k on ties (the greedy decision)
+    float v = z;
+    int idx = lane < K ? lane : INT_MAX;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+      const float ov = __shfl_xor_sync(FULL_MASK, v, o);
+      const int oi = __shfl_xor_sync(FULL_MASK, idx, o);
+      if (ov > v || (ov == v && oi < idx)) {
+        v = ov;
+        idx = oi;
+      }
+    }
+    int c = idx;
+    float q = lane == idx ? 1.f : 0.f;
+    if (T > 0.f && v != -INFINITY) {
+      const double w = lane < K ? exp((double(z) - double(v)) / double(T)) : 0.0;
+      s_w[lane] = w;
+      __syncwarp();
+      int pick = 0;
+      double W = 0.0;
+      if (lane == 0) {
+        for (int k = 0; k < K; ++k) W += s_w[k];
+        const double thr = double(uniforms[pr]) * W;
+        double cum = 0.0;
+        int last = 0;
+        pick = -1;
+        for (int k = 0; k < K; ++k) {
+          cum += s_w[k];
+          if (s_w[k] > 0.0) last = k;
+          if (pick < 0 && cum > thr) pick = k;
+        }
+        if (pick < 0) pick = last;
+      }
+      c = __shfl_sync(FULL_MASK, pick, 0);
+      W = __shfl_sync(FULL_MASK, W, 0);
+      q = static_cast<float>(w / W);
+      __syncwarp();
+    }
+    if (proposal && lane < K) proposal[pr * K + lane] = q;
+    if (lane == 0) {
+      if (choice) choice[pr] = c;
+      if (path) path[pr] = __ldg(src + (int64_t(s) * K + prev) * K + c);
+      tokens[b * B + s + 1] = __ldg(cand_id + pr * K + c);
+    }
+    prev = c;
+  }
+}
+
 cudaError_t launch_pair_scores(const float* heads, const __nv_bfloat16* target,
                                const __nv_bfloat16* Wa, const float* ba, int64_t batch, int B,
                                int K, int E, int H, float sigma, float* scores, float* out_tap,
@@ -308,6 +381,18 @@ cudaError_t launch_viterbi(const float* scores, const int32_t* cand_id,
   }
   viterbi_kernel<<<static_cast<unsigned>(batch), 32, (staged ? need : 0) + aux, stream>>>(
       scores, cand_id, anchor_ids, batch, B, K, tokens, choice, path, total, staged);
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_sample_walk(const float* scores, const int32_t* cand_id,
+                               const int32_t* anchor_ids, const float* temperature,
+                               const float* uniforms, int64_t batch, int B, int K,
+                               int32_t* tokens, int32_t* choice, float* path, float* proposal,
+                               cudaStream_t stream) {
+  sample_walk_kernel<<<static_cast<unsigned>(batch), 32, 0, stream>>>(
+      scores, cand_id, anchor_ids, temperature, uniforms, batch, B, K, tokens, choice, path,
+      proposal);
   note_launch();
   return cudaGetLastError();
 }

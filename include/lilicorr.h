@@ -205,6 +205,28 @@ lilicorr_status lilicorr_viterbi(const float* pair_scores, const int32_t* cand_i
                                  int32_t K, int32_t* tokens, int32_t* choice,
                                  float* path_score, double* total, void* stream);
 
+/* Sampled commit on given scores (serving PR, "Sampling the committed path"; LiLiCorr
+ * Sec. 3.3, Eq. 2): slot s draws c_s from softmax_k(pair_scores[b,s-1,c_{s-1},k] / T_b)
+ * given the previous draw (c_0 = 0), and publishes the distribution it drew from so a
+ * verifier can accept by rejection sampling.
+ *   temperature [batch] f32, nullable (null: every row greedy).  Rows with T_b <= 0 take
+ *               the greedy argmax (f32, lowest k on ties), bit-identical to
+ *               lilicorr_greedy_walk, with a one-hot proposal.
+ *   uniforms    [batch,B-1] f32 in [0,1), the caller's random numbers (one per slot,
+ *               e.g. from its own Philox stream); required when temperature is given.
+ *               The draw is by inverse CDF: weights exp((z - max z)/T) and their running
+ *               sums in double, in k order; c_s = the first k whose running sum exceeds
+ *               u * (total).
+ *   proposal    [batch,B-1,K] f32, nullable: the drawn-from distribution per slot.
+ * Other layouts as lilicorr_greedy_walk.  1 <= K <= 32.  Errors: LILICORR_ERR_INVALID_ARG
+ * for null required pointers, temperature without uniforms or sizes out of range;
+ * LILICORR_ERR_CUDA for a failed launch. */
+lilicorr_status lilicorr_sample_walk(const float* pair_scores, const int32_t* cand_id,
+                                     const int32_t* anchor_ids, const float* temperature,
+                                     const float* uniforms, int64_t batch, int32_t B,
+                                     int32_t K, int32_t* tokens, int32_t* choice,
+                                     float* path_score, float* proposal, void* stream);
+
 /* Human-readable name of a status; never NULL. */
 const char* lilicorr_status_string(lilicorr_status s);
 /* Message of the most recent CUDA failure in this thread ("" if none). */

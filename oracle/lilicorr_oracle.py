@@ -14,6 +14,8 @@ reranker for DFlash drafts", cited as the serving PR):
   * sigma = 8.0, B = 16, two layers ............................ LiLiCorr App. A, Table 4
   * greedy commit c_s = argmax_k phi(s-1, c_{s-1}, k) .......... LiLiCorr Sec. 3.5, Eq. 8
   * path score g(c) and its exact maximiser (Viterbi) ......... LiLiCorr App. E, Eq. 12
+  * sampled commit from softmax(z_s / T), proposal published .. serving PR, "Sampling the
+                                                                 committed path"; LiLiCorr Eq. 2
   * exact top-k + full-vocabulary log-partition, argmax ties
     to the lower index ........................................ serving PR, "Why the custom kernels"
   * attention parameter layout of nn.MultiheadAttention ........ serving PR, "Design notes" 3
@@ -38,6 +40,9 @@ pages leave a step open (each listed in the design notes of the repository):
   R-score    z_s[k] = phi(s-1, c_{s-1}, k); the draft log-prob is not added to z.
   R-argmax   the argmax over scores is taken on scores rounded to float32 (the
              precision the kernels decide in); ties go to the lowest rank.
+  R-sample   the sampled commit draws by inverse CDF from caller-supplied uniforms, with
+             weights and their running sums in float64 over the float32 scores, in rank
+             order (see sample_walk).
 
 Precision: the default (mirror=False) is plain float64 math at every step, the
 definition the CUDA path is held to.  mirror=True (or a set of point names) rounds to
@@ -295,6 +300,59 @@ def greedy_walk(scores: np.ndarray, rank: Optional[np.ndarray] = None):
             margin[s] = z[c] - np.max(np.delete(z, c))
         prev = c
     return choice, path, margin
+
+
+def sample_walk(scores: np.ndarray, temperature: float, u: np.ndarray,
+                rank: Optional[np.ndarray] = None):
+    """Sampled commit (serving PR, "Sampling the committed path"; LiLiCorr Sec. 3.3,
+    Eq. 2): each slot draws c_s from softmax_k(z_s[k] / T) with z_s[k] = phi(s-1,
+    c_{s-1}, k), given the previous draw.  T <= 0 is the greedy commit (same decisions as
+    greedy_walk) with a one-hot proposal.
+
+    Reading R-sample: the draw is by inverse CDF with one uniform u_s in [0, 1) per slot
+    supplied by the caller: weights w_k = exp((z_k - max z) / T) in float64 from the
+    float32-rounded scores, W = their sum taken in rank order, and c_s = the first
+    candidate in rank order whose running sum exceeds u_s * W (the last candidate with
+    w > 0 if rounding leaves none).  A slot whose scores are all -inf takes rank 0.
+    Returns (choice [B-1], path_score [B-1], proposal [B-1, K]) with proposal[s] = w / W
+    in candidate order."""
+    z32 = scores.astype(np.float32).astype(np.float64)
+    Bm1, K, _ = z32.shape
+    rank = np.tile(np.arange(K), (Bm1, 1)) if rank is None else rank
+    if temperature <= 0:
+        choice, path, _ = greedy_walk(scores, rank)
+        prop = np.zeros((Bm1, K))
+        prop[np.arange(Bm1), choice] = 1.0
+        return choice, path, prop
+    choice = np.zeros(Bm1, dtype=np.int64)
+    path = np.zeros(Bm1)
+    prop = np.zeros((Bm1, K))
+    prev = 0
+    for s in range(Bm1):
+        z = z32[s, prev]
+        order = np.argsort(rank[s], kind="stable")
+        m = z.max()
+        if m == -np.inf:
+            c = int(order[0])
+            prop[s, c] = 1.0
+        else:
+            w = np.exp((z - m) / float(temperature))
+            W = 0.0
+            for k in order:
+                W += w[k]
+            thr = float(np.float32(u[s])) * W
+            cum, c = 0.0, -1
+            for k in order:
+                cum += w[k]
+                if cum > thr:
+                    c = int(k)
+                    break
+            if c < 0:
+                c = int([k for k in order if w[k] > 0][-1])
+            prop[s] = w / W
+        choice[s], path[s] = c, z[c]
+        prev = c
+    return choice, path, prop
 
 
 def viterbi(scores: np.ndarray, rank: Optional[np.ndarray] = None):

@@ -150,3 +150,12 @@ def test_viterbi_argument_checks(lib):
     assert lib.lilicorr_viterbi(p, p, None, 1, 65, 4, p, None, None, None, None) == 1
     assert lib.lilicorr_viterbi(None, p, None, 1, 16, 4, p, None, None, None, None) == 1
     assert lib.lilicorr_viterbi(p, p, None, 0, 16, 4, p, None, None, None, None) == 1
+
+
+def test_sample_walk_argument_checks(lib):
+    p = C.c_void_p(16)
+    f = lib.lilicorr_sample_walk
+    assert f(p, p, None, p, None, 1, 16, 4, p, None, None, None, None) == 1  # T without u
+    assert f(p, p, None, None, None, 1, 16, 33, p, None, None, None, None) == 1
+    assert f(None, p, None, None, None, 1, 16, 4, p, None, None, None, None) == 1
+    assert f(p, p, None, None, None, 0, 16, 4, p, None, None, None, None) == 1

@@ -427,3 +427,68 @@ def test_mirror_changes_little(rng):
     fin = np.isfinite(a["pair_scores"])
     d = np.abs(a["pair_scores"][fin] - b["pair_scores"][fin]).max()
     assert 0 < d < 0.1
+
+
+# ----------------------------------------------------------------------------- sampled commit
+
+def test_sample_walk_zero_temperature_is_greedy(rng):
+    sc = np.round(rng.standard_normal((7, 5, 5)) * 4) / 4
+    sc[0, 1:] = -np.inf
+    g_choice, g_path, _ = O.greedy_walk(sc)
+    choice, path, prop = O.sample_walk(sc, 0.0, np.full(7, 0.5))
+    assert choice.tolist() == g_choice.tolist() and np.array_equal(path, g_path)
+    assert np.array_equal(prop, np.eye(5)[g_choice])
+
+
+def test_sample_walk_proposal_is_softmax(rng):
+    import scipy.special
+    sc = rng.standard_normal((6, 8, 8)) * 3
+    sc[0, 1:] = -np.inf
+    T = 0.7
+    u = rng.random(6)
+    choice, path, prop = O.sample_walk(sc, T, u)
+    z = sc.astype(np.float32).astype(np.float64)
+    prev = np.concatenate([[0], choice[:-1]])
+    for s in range(6):
+        ref = scipy.special.softmax(z[s, prev[s]] / T)
+        assert np.allclose(prop[s], ref, rtol=1e-12, atol=1e-15)
+        assert path[s] == z[s, prev[s], choice[s]]
+
+
+def test_sample_walk_draw_frequencies_match_softmax(rng):
+    """Many independent first-slot draws: the histogram follows softmax(z / T) within
+    five binomial standard deviations (a reversed CDF, a missing 1/T or an off-by-one
+    in the inverse CDF all fail)."""
+    import scipy.special
+    K, T, N = 6, 1.3, 40000
+    sc = np.full((1, K, K), -np.inf)
+    sc[0, 0] = np.array([1.0, -0.5, 2.0, 0.25, 2.0, -3.0])
+    counts = np.zeros(K)
+    for u in rng.random(N):
+        c, _, _ = O.sample_walk(sc, T, np.array([u]))
+        counts[c[0]] += 1
+    p = scipy.special.softmax(sc[0, 0] / T)
+    sd = np.sqrt(N * p * (1 - p))
+    assert np.all(np.abs(counts - N * p) <= 5 * sd + 1)
+
+
+def test_sample_walk_inverse_cdf_edges(rng):
+    sc = np.full((1, 5, 5), -np.inf)
+    sc[0, 0] = np.array([-np.inf, 0.3, -0.2, 0.1, -np.inf])
+    assert O.sample_walk(sc, 1.0, np.array([0.0]))[0][0] == 1
+    assert O.sample_walk(sc, 1.0, np.array([np.nextafter(np.float32(1), np.float32(0))]))[0][0] == 3
+    picks = [O.sample_walk(sc, 1.0, np.array([u]))[0][0] for u in np.linspace(0, 0.999, 200)]
+    assert picks == sorted(picks)  # an inverse CDF is monotone in u
+    allinf = np.full((1, 3, 3), -np.inf)
+    c, _, prop = O.sample_walk(allinf, 1.0, np.array([0.4]))
+    assert c[0] == 0 and prop[0].tolist() == [1.0, 0.0, 0.0]
+
+
+def test_sample_walk_conditions_on_the_previous_draw():
+    # slot 1 draws candidate 1 (certain); slot 2 must then use row 1 of pair 1
+    sc = np.full((2, 3, 3), -np.inf)
+    sc[0, 0] = [-np.inf, 0.0, -np.inf]
+    sc[1, 0] = [0.0, -np.inf, -np.inf]
+    sc[1, 1] = [-np.inf, -np.inf, 0.0]
+    c, _, _ = O.sample_walk(sc, 1.0, np.array([0.5, 0.5]))
+    assert c.tolist() == [1, 2]
