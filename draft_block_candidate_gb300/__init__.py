@@ -17,6 +17,8 @@ from .api import (  # noqa: F401
     stage_timing,
     stage_times,
     topk_lse,
+    topk_lse_merge,
+    topk_lse_shard,
     topk_lse_workspace,
 )
 from ._lib import BF16, F32, LIB_PATH  # noqa: F401

@@ -199,6 +199,43 @@ def topk_lse(logits: torch.Tensor, K: int, workspace: Optional[torch.Tensor] = N
     return out
 
 
+def topk_lse_shard(logits_slice: torch.Tensor, id_offset: int, K: int,
+                   records: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """lilicorr_topk_lse_shard on one vocabulary slice [batch,B,V_shard] (last dimension
+    contiguous, rows may be strided, e.g. a column slice of the whole logits): returns
+    the packed row records as a uint8 tensor [batch*(B-1), record_bytes]."""
+    batch, B, Vs = logits_slice.shape
+    if logits_slice.stride(2) != 1 or logits_slice.stride(0) != B * logits_slice.stride(1):
+        raise ValueError("slice rows must have a uniform stride and contiguous columns")
+    ld = _ldtype(logits_slice)
+    rb = int(L.lib().lilicorr_topk_lse_shard_record_bytes(K))
+    rows = batch * (B - 1)
+    if records is None:
+        records = torch.empty(rows, rb, dtype=torch.uint8, device=logits_slice.device)
+    ws = topk_lse_workspace(batch, B, Vs, min(K, Vs), ld, logits_slice.device)
+    # a strided view by design (rows row_stride apart): its pointer is passed as it is
+    st = L.lib().lilicorr_topk_lse_shard(logits_slice.data_ptr(), ld, batch, B, Vs,
+                                         logits_slice.stride(1), id_offset, K, _ptr(records),
+                                         _ptr(ws), 0 if ws is None else ws.numel(),
+                                         _stream(stream))
+    _check(st, "lilicorr_topk_lse_shard")
+    return records
+
+
+def topk_lse_merge(records: torch.Tensor, K: int, stream=None):
+    """lilicorr_topk_lse_merge of records [n_shards, rows, record_bytes] (uint8):
+    (cand_id [rows,K] int32, cand_logit [rows,K] f32, lse [rows] f32)."""
+    n, rows, _ = records.shape
+    dev = records.device
+    cid = torch.empty(rows, K, dtype=torch.int32, device=dev)
+    cv = torch.empty(rows, K, dtype=torch.float32, device=dev)
+    lse = torch.empty(rows, dtype=torch.float32, device=dev)
+    st = L.lib().lilicorr_topk_lse_merge(_ptr(records.contiguous()), n, rows, K, _ptr(cid),
+                                         _ptr(cv), _ptr(lse), _stream(stream))
+    _check(st, "lilicorr_topk_lse_merge")
+    return cid, cv, lse
+
+
 def greedy_walk(pair_scores: torch.Tensor, cand_id: torch.Tensor,
                 anchor_ids: Optional[torch.Tensor] = None, stream=None):
     """lilicorr_greedy_walk on given scores [batch,B-1,K,K]: (tokens, choice, path_score)."""

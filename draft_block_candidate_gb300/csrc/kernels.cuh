@@ -9,7 +9,11 @@ namespace lilicorr {
 size_t k1_workspace_bytes(int64_t batch, int B, int64_t V, int esize);
 cudaError_t k1_launch(const void* logits, int esize, int64_t batch, int B, int64_t V, int K,
                       int32_t* cand_id, float* cand_logit, float* lse, void* ws,
-                      cudaStream_t stream);
+                      cudaStream_t stream, int64_t row_stride = 0, int id_offset = 0,
+                      void* records = nullptr);
+size_t k1_shard_record_bytes(int K);
+cudaError_t k1_merge_launch(const void* records, int n, int64_t rows, int K, int32_t* cand_id,
+                            float* cand_logit, float* lse, cudaStream_t stream);
 cudaError_t k1_read_device_error(uint32_t* code);
 
 // message returned by lilicorr_last_error() for this thread (lilicorr_api.cu)

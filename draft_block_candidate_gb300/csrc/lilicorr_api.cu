@@ -437,6 +437,47 @@ lilicorr_status lilicorr_topk_lse(const void* logits, lilicorr_dtype ldtype, int
   return LILICORR_OK;
 }
 
+size_t lilicorr_topk_lse_shard_record_bytes(int32_t K) {
+  return (K < 1 || K > 32) ? 0 : k1_shard_record_bytes(K);
+}
+
+lilicorr_status lilicorr_topk_lse_shard(const void* logits, lilicorr_dtype ldtype,
+                                        int64_t batch, int32_t B, int64_t V_shard,
+                                        int64_t row_stride, int64_t id_offset, int32_t K,
+                                        void* records, void* workspace, size_t workspace_bytes,
+                                        void* stream) {
+  if (!logits || !records) return LILICORR_ERR_INVALID_ARG;
+  if (batch < 1 || B < 2 || V_shard < 1 || K < 1 || K > 32) return LILICORR_ERR_INVALID_ARG;
+  if (row_stride < V_shard || id_offset < 0 || id_offset + V_shard > (int64_t(1) << 31) - 2)
+    return LILICORR_ERR_INVALID_ARG;
+  if (ldtype != LILICORR_F32 && ldtype != LILICORR_BF16) return LILICORR_ERR_INVALID_ARG;
+  const int es = ldtype == LILICORR_BF16 ? 2 : 4;
+  if (reinterpret_cast<uintptr_t>(logits) % es || reinterpret_cast<uintptr_t>(records) % 4)
+    return LILICORR_ERR_INVALID_ARG;
+  if (V_shard * es > (int64_t(1) << 31) - 64) return LILICORR_ERR_INVALID_ARG;
+  const size_t need = k1_workspace_bytes(batch, B, V_shard, es);
+  if (need && (!workspace || workspace_bytes < need ||
+               reinterpret_cast<uintptr_t>(workspace) % 256))
+    return LILICORR_ERR_WORKSPACE;
+  LC_CUDA(k1_launch(logits, es, batch, B, V_shard, K, nullptr, nullptr, nullptr, workspace,
+                    static_cast<cudaStream_t>(stream), row_stride, static_cast<int>(id_offset),
+                    records),
+          "logit pass (vocabulary shard)");
+  return LILICORR_OK;
+}
+
+lilicorr_status lilicorr_topk_lse_merge(const void* records, int32_t n_shards, int64_t rows,
+                                        int32_t K, int32_t* cand_id, float* cand_logit,
+                                        float* lse, void* stream) {
+  if (!records || !cand_id || !cand_logit || !lse) return LILICORR_ERR_INVALID_ARG;
+  if (n_shards < 1 || rows < 1 || K < 1 || K > 32 || reinterpret_cast<uintptr_t>(records) % 4)
+    return LILICORR_ERR_INVALID_ARG;
+  LC_CUDA(k1_merge_launch(records, n_shards, rows, K, cand_id, cand_logit, lse,
+                          static_cast<cudaStream_t>(stream)),
+          "shard merge");
+  return LILICORR_OK;
+}
+
 lilicorr_status lilicorr_greedy_walk(const float* pair_scores, const int32_t* cand_id,
                                      const int32_t* anchor_ids, int64_t batch, int32_t B,
                                      int32_t K, int32_t* tokens, int32_t* choice,

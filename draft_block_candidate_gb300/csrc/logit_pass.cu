@@ -86,7 +86,15 @@ struct K1Params {
   float* lse;
   K1Partial* partials;
   unsigned* counters;
+  int64_t row_stride;  // elements between consecutive rows (V for a whole-vocabulary pass)
+  int id_offset;       // added to every candidate id (a vocabulary shard's first id)
+  char* records;       // vocabulary-shard mode: packed per-row records instead of outputs
 };
+
+// Packed per-row record of a vocabulary shard: {m2, s, v[K], id[K]}, K * 8 + 8 bytes.
+// m2 = max * log2(e) of the shard's logits, s = sum 2^(x log2(e) - m2); v / id its top-K
+// (value desc, global id asc).
+__host__ __device__ constexpr size_t k1_record_bytes(int K) { return 8 + size_t(K) * 8; }
 
 __device__ __forceinline__ int64_t i64min(int64_t a, int64_t b) { return a < b ? a : b; }
 
@@ -287,7 +295,7 @@ __global__ void __launch_bounds__(K1_THREADS, K1_MIN_BLOCKS) logit_pass_kernel(c
   const int64_t s_slot = r % (p.B - 1) + 1;
 
   // Row geometry in bytes relative to p.logits; body = 16-byte aligned part.
-  const int64_t row_start = (b * p.B + s_slot) * p.V * ES;
+  const int64_t row_start = (b * p.B + s_slot) * p.row_stride * ES;
   const int64_t row_end = row_start + p.V * ES;
   const uintptr_t base = reinterpret_cast<uintptr_t>(p.logits);
   int64_t body_start = static_cast<int64_t>(((base + row_start + 15) & ~uintptr_t(15)) - base);
@@ -594,13 +602,57 @@ __global__ void __launch_bounds__(K1_THREADS, K1_MIN_BLOCKS) logit_pass_kernel(c
     if (lane == 0) p.counters[r] = 0u;
   }
 
+  if (p.records) {
+    char* rec = p.records + r * k1_record_bytes(K);
+    if (lane == 0) {
+      reinterpret_cast<float*>(rec)[0] = M;
+      reinterpret_cast<float*>(rec)[1] = S;
+    }
+    if (lane < K) {
+      reinterpret_cast<float*>(rec + 8)[lane] = v;
+      reinterpret_cast<int32_t*>(rec + 8 + 4 * K)[lane] = id == INT_MAX ? INT_MAX : id + p.id_offset;
+    }
+    return;
+  }
   if (lane < K) {
-    p.cand_id[r * K + lane] = id;
+    p.cand_id[r * K + lane] = id + p.id_offset;
     p.cand_logit[r * K + lane] = v;
   }
   if (lane == 0) {
     const double l2 = static_cast<double>(M) + log2(static_cast<double>(S));
     p.lse[r] = static_cast<float>(l2 / static_cast<double>(LOG2E));
+  }
+}
+
+// Merge of n vocabulary-shard records per row (one warp per row): the shards' sorted
+// top-K lists by bitonic merge under the same (value desc, id asc) order, and their
+// (m2, s) pairs by the online log-sum-exp rule.  Shards hold disjoint ids, so the result
+// is the top-K of the whole row.
+__global__ void __launch_bounds__(128) k1_merge_kernel(const char* __restrict__ records,
+                                                       int n, int64_t rows, int K,
+                                                       int32_t* __restrict__ cand_id,
+                                                       float* __restrict__ cand_logit,
+                                                       float* __restrict__ lse) {
+  const int lane = threadIdx.x & 31;
+  const int64_t r = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (r >= rows) return;
+  const size_t rb = k1_record_bytes(K);
+  float v = -INFINITY, M = M2_INIT, S = 0.f;
+  int id = INT_MAX;
+  for (int j = 0; j < n; ++j) {
+    const char* rec = records + (int64_t(j) * rows + r) * rb;
+    const float bv = lane < K ? __ldg(reinterpret_cast<const float*>(rec + 8) + lane) : -INFINITY;
+    const int bi = lane < K ? __ldg(reinterpret_cast<const int32_t*>(rec + 8 + 4 * K) + lane) : INT_MAX;
+    bitonic_merge(v, id, bv, bi, lane);
+    lse_merge(M, S, __ldg(reinterpret_cast<const float*>(rec)), __ldg(reinterpret_cast<const float*>(rec) + 1));
+  }
+  if (lane < K) {
+    cand_id[r * K + lane] = id;
+    cand_logit[r * K + lane] = v;
+  }
+  if (lane == 0) {
+    const double l2 = static_cast<double>(M) + log2(static_cast<double>(S));
+    lse[r] = static_cast<float>(l2 / static_cast<double>(LOG2E));
   }
 }
 
@@ -661,7 +713,7 @@ size_t k1_workspace_bytes(int64_t batch, int B, int64_t V, int esize) {
 
 cudaError_t k1_launch(const void* logits, int esize, int64_t batch, int B, int64_t V, int K,
                       int32_t* cand_id, float* cand_logit, float* lse, void* ws,
-                      cudaStream_t stream) {
+                      cudaStream_t stream, int64_t row_stride, int id_offset, void* records) {
   const K1Plan pl = k1_plan(batch, B, V, esize);
   K1Params prm;
   prm.logits = static_cast<const char*>(logits);
@@ -676,6 +728,9 @@ cudaError_t k1_launch(const void* logits, int esize, int64_t batch, int B, int64
   prm.lse = lse;
   prm.partials = nullptr;
   prm.counters = nullptr;
+  prm.row_stride = row_stride > 0 ? row_stride : V;
+  prm.id_offset = id_offset;
+  prm.records = static_cast<char*>(records);
   const int64_t rows = batch * (B - 1);
   if (pl.P > 1) {
     prm.partials = static_cast<K1Partial*>(ws);
@@ -698,6 +753,17 @@ cudaError_t k1_launch(const void* logits, int esize, int64_t batch, int B, int64
     logit_pass_kernel<__nv_bfloat16><<<grid, K1_THREADS, dyn, stream>>>(prm);
   else
     logit_pass_kernel<float><<<grid, K1_THREADS, dyn, stream>>>(prm);
+  note_launch();
+  return cudaGetLastError();
+}
+
+size_t k1_shard_record_bytes(int K) { return k1_record_bytes(K); }
+
+cudaError_t k1_merge_launch(const void* records, int n, int64_t rows, int K, int32_t* cand_id,
+                            float* cand_logit, float* lse, cudaStream_t stream) {
+  const int wpb = 4;
+  k1_merge_kernel<<<static_cast<unsigned>((rows + wpb - 1) / wpb), 32 * wpb, 0, stream>>>(
+      static_cast<const char*>(records), n, rows, K, cand_id, cand_logit, lse);
   note_launch();
   return cudaGetLastError();
 }

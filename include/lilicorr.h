@@ -181,6 +181,35 @@ lilicorr_status lilicorr_topk_lse_noalloc(const void* logits, lilicorr_dtype ldt
                                           int32_t* cand_id, float* cand_logit, float* lse,
                                           void* stream);
 
+/* Vocabulary-sharded form of step a1 (serving PR, "Why the custom kernels" and its
+ * tensor-parallel notes: with the LM head sharded over the vocabulary, each rank reduces
+ * its slice to a per-row top-K and a partial log-partition, one packed all-gather moves
+ * K*(4+4) + 8 bytes per row, and a merge finishes the row).  On one GPU the ranks are
+ * emulated by slices of one logits tensor.
+ *   lilicorr_topk_lse_shard_record_bytes(K): bytes of one row record,
+ *     {f32 m2, f32 s, f32 v[K], int32 id[K]} = K*8 + 8 (m2 = max * log2(e) of the
+ *     slice, s = sum 2^(x*log2(e) - m2); v / id the slice's top-K by (value desc, id asc),
+ *     ids global; a slice with fewer than K values pads with (-inf, INT32_MAX)).
+ *   lilicorr_topk_lse_shard: logits points at element [0,0,0] of this shard's slice;
+ *     rows are row_stride >= V_shard elements apart (V_total for a slice of a whole
+ *     tensor); candidate ids are id_offset + column.  Writes records[batch*(B-1)] for the
+ *     drafted rows 1..B-1 (row 0 is not read).  Workspace as lilicorr_topk_lse at V_shard.
+ *   lilicorr_topk_lse_merge: records [n_shards][rows] -> cand_id, cand_logit [rows,K] and
+ *     lse [rows] exactly as lilicorr_topk_lse on the unsharded rows (ids and logits
+ *     identical; lse to f32 rounding).
+ * Errors: LILICORR_ERR_INVALID_ARG for null pointers, sizes out of range (1 <= K <= 32,
+ * id_offset + V_shard < 2^31 - 1), misaligned logits or records; LILICORR_ERR_WORKSPACE;
+ * LILICORR_ERR_CUDA. */
+size_t lilicorr_topk_lse_shard_record_bytes(int32_t K);
+lilicorr_status lilicorr_topk_lse_shard(const void* logits, lilicorr_dtype ldtype,
+                                        int64_t batch, int32_t B, int64_t V_shard,
+                                        int64_t row_stride, int64_t id_offset, int32_t K,
+                                        void* records, void* workspace, size_t workspace_bytes,
+                                        void* stream);
+lilicorr_status lilicorr_topk_lse_merge(const void* records, int32_t n_shards, int64_t rows,
+                                        int32_t K, int32_t* cand_id, float* cand_logit,
+                                        float* lse, void* stream);
+
 /* Step a5 alone (LiLiCorr Sec. 3.5, Eq. 8) on given scores pair_scores [batch,B-1,K,K]
  * (layout as in lilicorr_taps).  c_1 = argmax_k pair_scores[b,0,0,k]; c_s = argmax_k
  * pair_scores[b,s-1,c_{s-1},k]; ties go to the lowest k (serving PR: the Triton

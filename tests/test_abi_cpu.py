@@ -159,3 +159,18 @@ def test_sample_walk_argument_checks(lib):
     assert f(p, p, None, None, None, 1, 16, 33, p, None, None, None, None) == 1
     assert f(None, p, None, None, None, 1, 16, 4, p, None, None, None, None) == 1
     assert f(p, p, None, None, None, 0, 16, 4, p, None, None, None, None) == 1
+
+
+def test_shard_entry_points_check_arguments(lib):
+    p = C.c_void_p(256)
+    assert lib.lilicorr_topk_lse_shard_record_bytes(16) == 16 * 8 + 8
+    assert lib.lilicorr_topk_lse_shard_record_bytes(33) == 0
+    f = lib.lilicorr_topk_lse_shard
+    assert f(p, 1, 1, 16, 100, 99, 0, 8, p, None, 0, None) == 1     # stride < V_shard
+    assert f(p, 1, 1, 16, 100, 100, -1, 8, p, None, 0, None) == 1   # negative offset
+    assert f(p, 1, 1, 16, 100, 100, 0, 33, p, None, 0, None) == 1
+    assert f(None, 1, 1, 16, 100, 100, 0, 8, p, None, 0, None) == 1
+    m = lib.lilicorr_topk_lse_merge
+    assert m(p, 0, 10, 8, p, p, p, None) == 1
+    assert m(p, 2, 10, 33, p, p, p, None) == 1
+    assert m(None, 2, 10, 8, p, p, p, None) == 1
