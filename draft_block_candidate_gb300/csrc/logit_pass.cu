@@ -25,8 +25,9 @@
 //     is folded in 32 at a time (warp bitonic sort + bitonic merge).
 //   * the CTA floor is the K-th largest of 32 thread-group running maxima (K distinct
 //     elements are at least that large), kept fresh by the producer warp while it waits
-//     and raised by every warp's own K-th entry.  Stage 0 is checked one stage late, when
-//     the group maxima already cover it.
+//     and raised by every warp's own K-th entry.  Stage 0 is checked either one stage
+//     late, when the group maxima already cover it, or at once against the warp's own
+//     K-th largest thread maximum (K <= 16 on long segments).
 // At the end the 17 warp queues (the producer's holds the unaligned head and tail) are
 // merged in a tree.
 // Rows are split into P segments when there are too few rows to fill 152 SMs; the last
@@ -271,7 +272,7 @@ __device__ __forceinline__ float group_floor(const int* gmax, int lane, int K) {
   return __shfl_sync(FULL_MASK, warp_sort_desc(g, lane), K - 1);
 }
 
-template <typename T>
+template <typename T, bool DEFER0>
 __global__ void __launch_bounds__(K1_THREADS, K1_MIN_BLOCKS) logit_pass_kernel(const K1Params p) {
   constexpr int ES = sizeof(T);
   constexpr int NV = 16 / ES;
@@ -505,14 +506,27 @@ __global__ void __launch_bounds__(K1_THREADS, K1_MIN_BLOCKS) logit_pass_kernel(c
         for (int i = 0; i < K1_CPT; ++i) cm0[i] = cm[i];
         valid0 = valid;
       }
-      if (st == 1 || (st == 0 && nstages == 1)) {
-        // the group maxima now cover (most of) stage 0: the first CTA floor
-        const float f = group_floor(s_gmax, lane, K);
-        if (lane == 0) atomicMax(&s_floor, float_key(f));
-        __syncwarp();
-        check_stage(0, cm0, valid0);
+      if constexpr (!DEFER0) {
+        if (st == 0) {
+          // immediate first floor: this warp's K-th largest thread maximum of stage 0
+          float tmax = cm[0];
+#pragma unroll
+          for (int i = 1; i < K1_CPT; ++i) tmax = fmaxf(tmax, cm[i]);
+          const float wf = __shfl_sync(FULL_MASK, warp_sort_desc(tmax, lane), K - 1);
+          if (lane == 0 && wf != -INFINITY) atomicMax(&s_floor, float_key(wf));
+          __syncwarp();
+        }
+        check_stage(st, cm, valid);
+      } else {
+        if (st == 1 || (st == 0 && nstages == 1)) {
+          // the group maxima now cover (most of) stage 0: the first CTA floor
+          const float f = group_floor(s_gmax, lane, K);
+          if (lane == 0) atomicMax(&s_floor, float_key(f));
+          __syncwarp();
+          check_stage(0, cm0, valid0);
+        }
+        if (st >= 1) check_stage(st, cm, valid);
       }
-      if (st >= 1) check_stage(st, cm, valid);
     }
     ssum = s2.x + s2.y;
     // flush the warp buffer into the queue
@@ -729,6 +743,11 @@ cudaError_t k1_launch(const void* logits, int esize, int64_t batch, int B, int64
   prm.partials = nullptr;
   prm.counters = nullptr;
   prm.row_stride = row_stride > 0 ? row_stride : V;
+  // First floor.  Deferred: stage 0 is checked one stage late against the K-th largest
+  // of the 32 group maxima, which by then cover it (strong, but holds a ring slot for a
+  // stage).  Immediate: checked at once against the warp's own K-th largest thread
+  // maximum (weaker; better for K <= 16 on long segments, where the slot matters more).
+  const bool defer0 = K > 16 || pl.seg_bytes < 6 * K1_STAGE_BYTES;
   prm.id_offset = id_offset;
   prm.records = static_cast<char*>(records);
   const int64_t rows = batch * (B - 1);
@@ -743,16 +762,27 @@ cudaError_t k1_launch(const void* logits, int esize, int64_t batch, int B, int64
   constexpr int dyn = K1_NSTAGES * K1_STAGE_BYTES;
   static bool attr_done = false;
   if (!attr_done) {
-    cudaFuncSetAttribute(logit_pass_kernel<__nv_bfloat16>,
+    cudaFuncSetAttribute(logit_pass_kernel<__nv_bfloat16, true>,
                          cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
-    cudaFuncSetAttribute(logit_pass_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         dyn);
+    cudaFuncSetAttribute(logit_pass_kernel<__nv_bfloat16, false>,
+                         cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
+    cudaFuncSetAttribute(logit_pass_kernel<float, true>,
+                         cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
+    cudaFuncSetAttribute(logit_pass_kernel<float, false>,
+                         cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
     attr_done = true;
   }
-  if (esize == 2)
-    logit_pass_kernel<__nv_bfloat16><<<grid, K1_THREADS, dyn, stream>>>(prm);
-  else
-    logit_pass_kernel<float><<<grid, K1_THREADS, dyn, stream>>>(prm);
+  if (esize == 2) {
+    if (defer0)
+      logit_pass_kernel<__nv_bfloat16, true><<<grid, K1_THREADS, dyn, stream>>>(prm);
+    else
+      logit_pass_kernel<__nv_bfloat16, false><<<grid, K1_THREADS, dyn, stream>>>(prm);
+  } else {
+    if (defer0)
+      logit_pass_kernel<float, true><<<grid, K1_THREADS, dyn, stream>>>(prm);
+    else
+      logit_pass_kernel<float, false><<<grid, K1_THREADS, dyn, stream>>>(prm);
+  }
   note_launch();
   return cudaGetLastError();
 }
