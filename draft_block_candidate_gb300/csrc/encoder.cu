@@ -136,13 +136,24 @@ __global__ void conf_hidden_kernel(const float* __restrict__ cand_logit,
   const int nch = H / 8;
   float w[8][6];
   if (lane < nch) conf_load_w(w1, b1, lane * 8, w);
-  for (int64_t m = int64_t(blockIdx.x) * nw + (threadIdx.x >> 5); m < M;
-       m += int64_t(gridDim.x) * nw) {
-    const int64_t row = m / K;  // (block, slot) row of the logit pass
+  const int64_t step = int64_t(gridDim.x) * nw;
+  int64_t m = int64_t(blockIdx.x) * nw + (threadIdx.x >> 5);
+  // the three scalars of a row are loaded one row ahead
+  float nl = 0.f, nc = 0.f, nt = 0.f;
+  if (m < M) {
+    nl = __ldg(lse + m / K);
+    nc = __ldg(cand_logit + m);
+    nt = __ldg(cand_logit + (m / K) * K);
+  }
+  for (; m < M; m += step) {
     const int k = static_cast<int>(m % K);
-    const float l = __ldg(lse + row);
-    const float lp = __ldg(cand_logit + m) - l;
-    const float lp_top = __ldg(cand_logit + row * K) - l;
+    const float lp = nc - nl, lp_top = nt - nl;
+    const int64_t mn = m + step;
+    if (mn < M) {
+      nl = __ldg(lse + mn / K);
+      nc = __ldg(cand_logit + mn);
+      nt = __ldg(cand_logit + (mn / K) * K);
+    }
     float f[5];
     f[0] = lp;
     f[1] = expf(lp);

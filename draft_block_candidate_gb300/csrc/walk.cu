@@ -140,14 +140,35 @@ __global__ void __launch_bounds__(32) greedy_walk_kernel(
     const int32_t* __restrict__ anchor_ids, int64_t batch, int B, int K,
     int32_t* __restrict__ tokens, int32_t* __restrict__ choice, float* __restrict__ path,
     bool staged) {
-  extern __shared__ float gw_smem[];
+  extern __shared__ __align__(16) float gw_smem[];
   const int lane = threadIdx.x & 31;
   const int64_t b = blockIdx.x;
   if (b >= batch) return;
   const int n = (B - 1) * K * K;
   const float* src = scores + b * n;
   if (staged) {
-    for (int i = lane; i < n; i += 32) gw_smem[i] = __ldg(src + i);
+    // independent 16-byte loads, eight in flight per lane (n = (B-1) K^2 is a multiple of
+    // 4 when K is even; an odd K takes the scalar loop)
+    if ((K & 1) == 0) {
+      const float4* s4 = reinterpret_cast<const float4*>(src);
+      float4* d4 = reinterpret_cast<float4*>(gw_smem);
+      const int n4 = n >> 2;
+      for (int i0 = 0; i0 < n4; i0 += 256) {
+        float4 t[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int i = i0 + j * 32 + lane;
+          t[j] = i < n4 ? __ldg(s4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int i = i0 + j * 32 + lane;
+          if (i < n4) d4[i] = t[j];
+        }
+      }
+    } else {
+      for (int i = lane; i < n; i += 32) gw_smem[i] = __ldg(src + i);
+    }
     __syncwarp();
   }
   const float* sc = staged ? gw_smem : src;
