@@ -7,7 +7,11 @@ FFN 1024, d_e 128), synthetic seeded inputs and random-init weights.
 
 One step = one lilicorr_rerank call over the batch (logit pass, node build, encoder,
 fusion/heads/scores, greedy walk) with inputs resident in HBM.  The logits (1,167 MB per
-step) are larger than L2, so no flush is needed between steps.
+step) are larger than L2, so no flush is needed between steps.  The headline times the
+step as a CUDA graph (the entry point allocates nothing and never synchronises, so one
+call captures whole) replayed once per step; a separate eager pass with per-kernel
+events gives the breakdown (`kernels`) and the launch count (`--no-graph` times the
+eager pass instead).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
 
@@ -214,6 +218,7 @@ def run_gb300(a):
 
     clocks = ClockSampler(local)
     time.sleep(0.3)
+    # (1) eager steps with per-kernel events: the breakdown and the launch count
     lc.stage_timing(True)
     lc.stage_times()  # clear
     barrier()
@@ -227,10 +232,36 @@ def run_gb300(a):
     e1.record(stream)
     torch.cuda.synchronize(dev)
     barrier()
-    launches = lc.launch_count() - n0
-    ms = e0.elapsed_time(e1)
+    launches_per_step = (lc.launch_count() - n0) / a.steps
+    ms_eager = e0.elapsed_time(e1)
     lc.stage_timing(False)
     st = lc.stage_times()
+    ms = ms_eager
+    launch_mode = "eager (one lilicorr_rerank per step)"
+    # (2) the headline: the same step captured once as a CUDA graph (the entry point
+    # allocates nothing and never synchronises) and replayed W + K times
+    if not a.no_graph:
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=cap):
+            lc.rerank(w, logits, K, target_state=tgt, anchor_ids=anc, workspace=ws, out=out,
+                      stream=cap)
+        torch.cuda.synchronize(dev)
+        for _ in range(a.warmup):
+            graph.replay()
+        torch.cuda.synchronize(dev)
+        barrier()
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for _ in range(a.steps):
+            graph.replay()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+        ms = e0.elapsed_time(e1)
+        launch_mode = "CUDA graph of one lilicorr_rerank, replayed per step"
+    launches = int(round(launches_per_step * a.steps))
     clk = clocks.stop()
     if world > 1:
         t = torch.tensor([ms], device=dev)
@@ -318,11 +349,13 @@ def run_gb300(a):
         "data": "synthetic",
         "config": {"workload": describe(wl), "batch_per_gpu": batch, "B": B, "V": V, "K": K,
                    "l2": f"inputs larger than L2 ({logit_bytes / 1e6:.0f} MB of logits per step); no flush",
-                   "parallelism": f"dp{world} (independent blocks per rank)"},
+                   "parallelism": f"dp{world} (independent blocks per rank)",
+                   "launch": launch_mode},
         "roofline": roof,
         "logit_pass": logit_pass,
         "e2e_fraction_of_logits_roofline": (logit_bytes / (pk["hbm_gbs"] * 1e9)) / (step_ms / 1e3),
         "gpu_launches": launches,
+        "eager_ms_per_step": ms_eager / a.steps,
         "kernels": per_kernel,
         "e2e": e2e,
         "cpu_baseline": cpu,
@@ -379,6 +412,8 @@ def main():
     ap.add_argument("--ref-blocks", type=int, default=1)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="time eager launches instead of a replayed CUDA graph")
     ap.add_argument("--batch", type=int, default=None, help="override the workload's batch")
     ap.add_argument("--only", default=None, choices=["logit_pass"],
                     help="time one kernel alone (profiling driver); prints its own JSON")

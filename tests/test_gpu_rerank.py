@@ -155,3 +155,31 @@ def test_rerank_full_size_sampled_blocks(lc, name, kw, nblocks):
     blocks = sorted(rng.choice(wl.batch, nblocks, replace=False).tolist())
     _, rep = _compare(lc, wl, blocks)
     print(name, rep)
+
+
+def test_rerank_captures_in_a_cuda_graph(lc):
+    """The entry point allocates nothing and never synchronises: one call captures into a
+    CUDA graph whose replays reproduce the eager outputs bit for bit."""
+    wl = make_workload("highconc", batch=8, tier="medium")
+    w = lc.Weights(wl.dims, wl.weights)
+    logits = dev_logits(wl)
+    tgt = dev_bf16(wl.target_state)
+    anc = torch.from_numpy(wl.anchor_ids).cuda()
+    B, K = logits.shape[1], wl.K
+    ws = w.workspace(logits.shape[0], B, K)
+    eager = lc.rerank(w, logits, K, target_state=tgt, anchor_ids=anc, workspace=ws)
+    torch.cuda.synchronize()
+    out = {"tokens": torch.zeros_like(eager["tokens"]),
+           "path_score": torch.zeros_like(eager["path_score"])}
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=cap):
+        lc.rerank(w, logits, K, target_state=tgt, anchor_ids=anc, workspace=ws, out=out,
+                  stream=cap)
+    for _ in range(2):
+        out["tokens"].zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out["tokens"], eager["tokens"])
+        assert torch.equal(out["path_score"], eager["path_score"])
