@@ -175,9 +175,10 @@ __device__ __forceinline__ uint32_t pack2(__nv_bfloat16 a, __nv_bfloat16 b) {
   return uint32_t(__bfloat16_as_ushort(a)) | (uint32_t(__bfloat16_as_ushort(b)) << 16);
 }
 
-// v[0..31] = accumulator columns n..n+31 of row m (bias not yet added).
-template <int EPI>
-__device__ __forceinline__ void tc_epilogue32(const GemmArgs& g, int64_t m, int n, float (&v)[32]) {
+// Node epilogue terms of row m, columns n..n+31: v (the accumulator) += bias + E[cand]
+// + slot_table[s-1] + rank_table[k] (+ drafter hidden); the optional tap is written here,
+// X by the staged f32 store.
+__device__ __forceinline__ void tc_node_terms(const GemmArgs& g, int64_t m, int n, float (&v)[32]) {
 #pragma unroll
   for (int j = 0; j < 32; j += 4) {
     const float4 b4 = __ldg(reinterpret_cast<const float4*>(g.bias + n + j));
@@ -186,44 +187,7 @@ __device__ __forceinline__ void tc_epilogue32(const GemmArgs& g, int64_t m, int 
     v[j + 2] += b4.z;
     v[j + 3] += b4.w;
   }
-  if constexpr (EPI == EPI_F32) {
-    float4* o = reinterpret_cast<float4*>(g.out + m * g.N + n);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) o[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-  } else if constexpr (EPI == EPI_RESID) {
-    float4* o = reinterpret_cast<float4*>(g.out + m * g.N + n);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      float4 x = o[j];
-      x.x += v[4 * j];
-      x.y += v[4 * j + 1];
-      x.z += v[4 * j + 2];
-      x.w += v[4 * j + 3];
-      o[j] = x;
-    }
-  } else if constexpr (EPI == EPI_SPLIT || EPI == EPI_SPLIT_SILU) {
-    uint32_t hi[16], lo[16];
-#pragma unroll
-    for (int j = 0; j < 32; j += 2) {
-      float a = v[j], b = v[j + 1];
-      if constexpr (EPI == EPI_SPLIT_SILU) {
-        a = silu(a);
-        b = silu(b);
-      }
-      __nv_bfloat16 ha, la, hb, lb;
-      split_bf16(a, ha, la);
-      split_bf16(b, hb, lb);
-      hi[j / 2] = pack2(ha, hb);
-      lo[j / 2] = pack2(la, lb);
-    }
-    uint4* oh = reinterpret_cast<uint4*>(g.out_split + m * 2 * g.N + n);
-    uint4* ol = reinterpret_cast<uint4*>(g.out_split + m * 2 * g.N + g.N + n);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      oh[j] = make_uint4(hi[4 * j], hi[4 * j + 1], hi[4 * j + 2], hi[4 * j + 3]);
-      ol[j] = make_uint4(lo[4 * j], lo[4 * j + 1], lo[4 * j + 2], lo[4 * j + 3]);
-    }
-  } else {  // EPI_NODE: + E[cand] + slot_table[s-1] + rank_table[k] (+ drafter hidden)
+  {
     const int S = (g.B - 1) * g.K;
     const int64_t b = m / S;
     const int t = static_cast<int>(m % S);
@@ -264,13 +228,11 @@ __device__ __forceinline__ void tc_epilogue32(const GemmArgs& g, int64_t m, int 
         }
       }
     }
-    float4* o = reinterpret_cast<float4*>(g.out + m * g.N + n);
-    float4* tp = g.nodes_tap ? reinterpret_cast<float4*>(g.nodes_tap + m * g.N + n) : nullptr;
+    // X itself leaves through the staged f32 store; only the optional tap is written here
+    if (g.nodes_tap) {
+      float4* tp = reinterpret_cast<float4*>(g.nodes_tap + m * g.N + n);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const float4 x = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-      o[j] = x;
-      if (tp) tp[j] = x;
+      for (int j = 0; j < 8; ++j) tp[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
     }
   }
 }
@@ -279,7 +241,7 @@ __device__ __forceinline__ void tc_epilogue32(const GemmArgs& g, int64_t m, int 
 // columns n..n+31 of this lane's row; the warp's 32 x 32 chunk goes to shared memory in
 // the layout of the output tensor map's swizzle (16-byte unit u of row r at u ^ f(r)),
 // then one lane stores it (or adds it into the residual) with a bulk tensor copy.
-template <int EPI>
+template <int EPI, bool BIAS = true>
 __device__ __forceinline__ void tc_epilogue_staged(const GemmArgs& g, const CUtensorMap* tmC,
                                                    uint8_t* stg, int lane, int64_t row0, int n,
                                                    float (&v)[32]) {
@@ -287,7 +249,7 @@ __device__ __forceinline__ void tc_epilogue_staged(const GemmArgs& g, const CUte
   if (g.bias_group > 0)  // per-block bias row (rows past M reuse the last one)
     bias += (std::min<int64_t>(row0 + lane, g.M - 1) / g.bias_group) * g.N;
 #pragma unroll
-  for (int j = 0; j < 32; j += 4) {
+  for (int j = 0; j < 32 && BIAS; j += 4) {
     const float4 b4 = __ldg(reinterpret_cast<const float4*>(bias + j));
     v[j] += b4.x;
     v[j + 1] += b4.y;
@@ -449,7 +411,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         tmem_ld32(tmem + (uint32_t(32 * q) << 16) + uint32_t(buf * TC_BN + cc * 32), v);
         const int n = n0 + cc * 32;
         if constexpr (EPI == EPI_NODE) {
-          if (m < g.M && n < g.N) tc_epilogue32<EPI>(g, m, n, v);
+          // gathers and sums per row (bias included), then the staged f32 store of X
+          if (m < g.M && n < g.N) tc_node_terms(g, m, n, v);
+          if (n < g.N) {
+            if (lane == 0) bulk_wait_read0();
+            __syncwarp();
+            tc_epilogue_staged<EPI_F32, false>(g, &tmC, stg + sb * TC_STG_BYTES, lane,
+                                               m0 + 32 * q, n, v);
+            sb = (sb + 1) % TC_STG_BUFS;
+          }
         } else if (n < g.N) {
           // the buffer's previous bulk copy must have finished reading it
           if (lane == 0) {
@@ -539,12 +509,10 @@ cudaError_t launch_gemm(int epi, const GemmArgs& g, cudaStream_t stream) {
     if (!g.out_split || reinterpret_cast<uintptr_t>(g.out_split) % 16 ||
         !make_tmap_out(&tc, g.out_split, uint64_t(g.M), uint64_t(2 * g.N), false))
       return cudaErrorInvalidValue;
-  } else if (epi != EPI_NODE) {
+  } else {
     if (!g.out || reinterpret_cast<uintptr_t>(g.out) % 16 ||
         !make_tmap_out(&tc, g.out, uint64_t(g.M), uint64_t(g.N), true))
       return cudaErrorInvalidValue;
-  } else {
-    tc = ta;  // unused by the node epilogue
   }
   static bool attr = false;
   if (!attr) {
