@@ -5,12 +5,14 @@
 //                     + [slot_i == slot_j] * same) v_j          (LiLiCorr App. A)
 // over all tokens of the block (bidirectional, no mask).
 //
-// Persistent: one CTA per SM walks the (block, head, 128-query tile) items, 10 warps:
+// Persistent: one CTA per SM walks the (128-query tile, head, block) items (the heads of
+// a block run on neighbouring CTAs at the same time, so its Q / K / V rows are read from
+// DRAM together), 18 warps:
 //   warp 0     TMA: Q (128 x 64), K and V (256 x 64), each as bf16 hi and lo, 128-byte
 //              swizzle; the next item's Q and K load as soon as this item's S is formed,
 //              its V as soon as this item's second product is done; owns the TMEM
 //              allocation (S / P: 256 columns, O: 64 columns)
-//   warp 1     MMA: S = Qh Kh^T + Qh Kl^T + Ql Kh^T (M 128, N 256, K 64), then
+//   warp 1     MMA, per item: S0 / S1 = Q K^T over key halves 0-127 / 128-255
 //              O = Ph Vh + Ph Vl + Pl Vh with P read from TMEM and V as an MN-major
 //              shared-memory operand
 //   warps 2-17 four warps per query-row quarter, each taking a quarter of the keys:
@@ -32,7 +34,6 @@ static __device__ uint32_t g_err_at;
 
 constexpr int AT_DH = 64, AT_QT = 128, AT_KMAX = 256, AT_SOFT_WARPS = 16;
 constexpr int AT_NSPLIT = AT_SOFT_WARPS / 4;      // softmax warps per 32-row quarter
-constexpr int AT_KW = AT_KMAX / AT_NSPLIT;        // keys per softmax warp
 constexpr int AT_OW = AT_DH / AT_NSPLIT;          // output columns per softmax warp
 constexpr int AT_THREADS = 32 * (2 + AT_SOFT_WARPS);
 constexpr int AT_TILE = 128 * 64 * 2;  // one [128 x 64] bf16 swizzled tile
@@ -159,6 +160,18 @@ __device__ __forceinline__ void at_split2(float a, float b, uint32_t& hi, uint32
   lo = *reinterpret_cast<const uint32_t*>(&l2);
 }
 
+// The four softmax warps of one 32-row quarter (named barriers 2-5).
+__device__ __forceinline__ void quarter_sync(int q) {
+  asm volatile("bar.sync %0, 128;" ::"r"(2 + q) : "memory");
+}
+__device__ __forceinline__ void at_st16f(uint32_t taddr, const float (&v)[16]) {
+  uint32_t u[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) u[i] = __float_as_uint(v[i]);
+  at_st16(taddr, u);
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ void soft_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(32 * AT_SOFT_WARPS) : "memory");
 }
@@ -179,10 +192,11 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   // [query slot][key]: (dist + same-slot bias) * log2(e) of the current head, -inf for
   // keys beyond the block
   float* s_btab = reinterpret_cast<float*>(sm + 10 * AT_TILE);
-  __shared__ __align__(8) uint64_t bar_qk, bar_qkfree, bar_v, bar_vfree, bar_s, bar_p, bar_o,
-      bar_ofree;
+  __shared__ __align__(8) uint64_t bar_qk, bar_qkfree, bar_v, bar_vfree, bar_s0, bar_s1,
+      bar_p0, bar_p1, bar_pv0, bar_o, bar_ofree[2];
   __shared__ uint32_t s_tmem;
-  __shared__ float s_pmax[AT_NSPLIT][128], s_psum[AT_NSPLIT][128];
+  __shared__ float s_pmax[2][AT_NSPLIT][128], s_psum[AT_NSPLIT][128];
+  __shared__ float s_dist[128];  // dist + same-slot bias of the current head
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int QT = (S + AT_QT - 1) / AT_QT;
@@ -194,10 +208,14 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     mbar_init(&bar_qkfree, 1);
     mbar_init(&bar_v, 1);
     mbar_init(&bar_vfree, 1);
-    mbar_init(&bar_s, 1);
-    mbar_init(&bar_p, 32 * AT_SOFT_WARPS);
+    mbar_init(&bar_s0, 1);
+    mbar_init(&bar_s1, 1);
+    mbar_init(&bar_p0, 32 * AT_SOFT_WARPS);
+    mbar_init(&bar_p1, 32 * AT_SOFT_WARPS);
+    mbar_init(&bar_pv0, 1);
     mbar_init(&bar_o, 1);
-    mbar_init(&bar_ofree, 32 * AT_SOFT_WARPS);
+    mbar_init(&bar_ofree[0], 32 * AT_SOFT_WARPS);
+    mbar_init(&bar_ofree[1], 32 * AT_SOFT_WARPS);
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -211,7 +229,9 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   __syncthreads();
   at_fence_after();
   const uint32_t tmem = s_tmem;
-  const uint32_t tS = tmem, tO = tmem + AT_O_COL;
+  // S / P of key half 0 in columns 0-127, of half 1 in 128-255; O of even / odd items in
+  // 256-319 / 320-383
+  const uint32_t tS = tmem, tO0 = tmem + AT_O_COL;
 
   if (warp == 0 && lane == 0) {
     // ---- producer
@@ -237,54 +257,89 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       at_tma(sVl + AT_TILE, &tm, lo + cv, tok0 + 128, &bar_v);
     }
   } else if (warp == 1 && lane == 0) {
-    // ---- MMA issuer
-    constexpr uint32_t id_s = at_idesc(128, 256, false);
+    // ---- MMA issuer.  Per item i: S0 = Q K[0:128]^T, S1 = Q K[128:256]^T (three-term
+    // products, N 128), PV0 into O[i&1] once P0 is ready, PV1 once P1 is ready.  The next
+    // item's S0 is issued as soon as PV0 has completed and its S1 as soon as PV1 has, so
+    // both overlap this item's softmax.
+    constexpr uint32_t id_s = at_idesc(128, 128, false);
     constexpr uint32_t id_o = at_idesc(128, 64, true);
-    int i = 0;
-    bool ok = true;
-    for (int64_t t = blockIdx.x; t < nitems && ok; t += gridDim.x, ++i) {
-      // S of this item overwrites the TMEM columns the previous item's second product
-      // read P from: start only once that product has completed.
-      ok = (i == 0 || mbar_wait_bounded(&bar_o, (i - 1) & 1, &g_err_at, ERR_AT_O)) &&
-           mbar_wait_bounded(&bar_qk, i & 1, &g_err_at, ERR_AT_QK);
-      if (ok) {
-        at_fence_after();
+    auto qk_half = [&](int half) {
+      const uint32_t d = tS + uint32_t(128 * half);
+      uint8_t* kh = sKh + half * AT_TILE;
+      uint8_t* kl = sKl + half * AT_TILE;
 #pragma unroll
-        for (int ks = 0; ks < AT_DH / 16; ++ks) {
-          at_mma(tS, at_desc(sQh + ks * 32), at_desc(sKh + ks * 32), id_s, ks > 0);
-          at_mma(tS, at_desc(sQh + ks * 32), at_desc(sKl + ks * 32), id_s, 1);
-          at_mma(tS, at_desc(sQl + ks * 32), at_desc(sKh + ks * 32), id_s, 1);
-        }
+      for (int ks = 0; ks < AT_DH / 16; ++ks) {
+        at_mma(d, at_desc(sQh + ks * 32), at_desc(kh + ks * 32), id_s, ks > 0);
+        at_mma(d, at_desc(sQh + ks * 32), at_desc(kl + ks * 32), id_s, 1);
+        at_mma(d, at_desc(sQl + ks * 32), at_desc(kh + ks * 32), id_s, 1);
       }
-      at_commit(&bar_s);
-      at_commit(&bar_qkfree);
-      ok = ok && mbar_wait_bounded(&bar_p, i & 1, &g_err_at, ERR_AT_P) &&
-           mbar_wait_bounded(&bar_v, i & 1, &g_err_at, ERR_AT_V) &&
-           (i == 0 || mbar_wait_bounded(&bar_ofree, (i - 1) & 1, &g_err_at, ERR_AT_OFREE));
-      if (ok) {
-        at_fence_after();
-        // P for keys 32c..32c+31 sits in TMEM columns 32c (hi, 16 packed columns) and
-        // 32c + 16 (lo); a 16-key step j uses 8 of them.
+    };
+    auto pv_half = [&](int half, uint32_t tO) {
+      // P for keys 32c..32c+31 sits in TMEM columns 32c (hi, 16 packed columns) and
+      // 32c + 16 (lo); a 16-key step j uses 8 of them
 #pragma unroll 4
-        for (int j = 0; j < AT_KMAX / 16; ++j) {
-          const uint32_t pc = uint32_t(32 * (j >> 1) + 8 * (j & 1));
-          const uint64_t vh = at_desc(sVh + 16 * j * 128), vl = at_desc(sVl + 16 * j * 128);
-          at_mma_ts(tO, tS + pc, vh, id_o, j > 0);
-          at_mma_ts(tO, tS + pc, vl, id_o, 1);
-          at_mma_ts(tO, tS + pc + 16, vh, id_o, 1);
-        }
+      for (int jj = 0; jj < 8; ++jj) {
+        const int j = 8 * half + jj;
+        const uint32_t pc = uint32_t(32 * (j >> 1) + 8 * (j & 1));
+        const uint64_t vh = at_desc(sVh + 16 * j * 128), vl = at_desc(sVl + 16 * j * 128);
+        at_mma_ts(tO, tS + pc, vh, id_o, (half > 0 || jj > 0));
+        at_mma_ts(tO, tS + pc, vl, id_o, 1);
+        at_mma_ts(tO, tS + pc + 16, vh, id_o, 1);
       }
+    };
+    bool ok = mbar_wait_bounded(&bar_qk, 0, &g_err_at, ERR_AT_QK);
+    if (ok && blockIdx.x < nitems) {
+      at_fence_after();
+      qk_half(0);
+      at_commit(&bar_s0);
+      qk_half(1);
+      at_commit(&bar_s1);
+      at_commit(&bar_qkfree);
+    }
+    int i = 0;
+    for (int64_t t = blockIdx.x; t < nitems && ok; t += gridDim.x, ++i) {
+      const bool more = t + gridDim.x < nitems;
+      const uint32_t tO = tO0 + uint32_t(64 * (i & 1));
+      ok = mbar_wait_bounded(&bar_p0, i & 1, &g_err_at, ERR_AT_P) &&
+           mbar_wait_bounded(&bar_v, i & 1, &g_err_at, ERR_AT_V) &&
+           (i < 2 || mbar_wait_bounded(&bar_ofree[i & 1], ((i >> 1) - 1) & 1, &g_err_at,
+                                       ERR_AT_OFREE));
+      if (!ok) break;
+      at_fence_after();
+      pv_half(0, tO);
+      at_commit(&bar_pv0);
+      if (more) {
+        // S0 of the next item overwrites P0: after PV0 has completed
+        ok = mbar_wait_bounded(&bar_pv0, i & 1, &g_err_at, ERR_AT_O) &&
+             mbar_wait_bounded(&bar_qk, (i + 1) & 1, &g_err_at, ERR_AT_QK);
+        if (!ok) break;
+        at_fence_after();
+        qk_half(0);
+        at_commit(&bar_s0);
+      }
+      ok = mbar_wait_bounded(&bar_p1, i & 1, &g_err_at, ERR_AT_P);
+      if (!ok) break;
+      at_fence_after();
+      pv_half(1, tO);
       at_commit(&bar_o);
       at_commit(&bar_vfree);
+      if (more) {
+        ok = mbar_wait_bounded(&bar_o, i & 1, &g_err_at, ERR_AT_O);
+        if (!ok) break;
+        at_fence_after();
+        qk_half(1);
+        at_commit(&bar_s1);
+        at_commit(&bar_qkfree);
+      }
     }
   } else if (warp >= 2) {
     // ---- softmax and epilogue
     const int qq = warp & 3, hf = (warp - 2) >> 2;
     const int r = 32 * qq + lane;  // TMEM lane = query row of the tile
     const uint32_t lane_off = uint32_t(32 * qq) << 16;
-    const int j0 = AT_KW * hf;     // this warp's keys j0 .. j0 + AT_KW - 1
     const int nq = S / Kc;         // query slots
     constexpr float C = 0.125f * AT_LOG2E;  // 1 / sqrt(64), in log2 units
+    constexpr float RESCALE_AT = 16.f;      // log2 headroom before half 1 re-bases
     int i = 0;
     int cur_h = -1;
     for (int64_t t = blockIdx.x; t < nitems; t += gridDim.x, ++i) {
@@ -292,81 +347,102 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       const int h = static_cast<int>((t / QT) % heads);
       const int64_t tok0 = (t / QT / heads) * S;
       const int q = qt * AT_QT + r;
+      const uint32_t tO = tO0 + uint32_t(64 * (i & 1));
       if (h != cur_h) {  // bias table of this head (all softmax warps take the same items)
+        soft_sync();
+        // the head's distance row and same-slot bias, one global load per thread, then
+        // the [query slot][key] table from shared memory
+        for (int k = tid - 64; k < nd; k += 32 * AT_SOFT_WARPS)
+          s_dist[k] = dist_bias[h * nd + k] + (k == B_max - 2 ? same_bias[h] : 0.f);
         soft_sync();
         for (int idx = tid - 64; idx < nq * AT_KMAX; idx += 32 * AT_SOFT_WARPS) {
           const int qs = idx / AT_KMAX, j = idx % AT_KMAX;
-          float b = -INFINITY;
-          if (j < S) {
-            const int sj = j / Kc;
-            b = (dist_bias[h * nd + sj - qs + B_max - 2] + (sj == qs ? same_bias[h] : 0.f)) *
-                AT_LOG2E;
-          }
-          s_btab[qs * AT_BSTRIDE + j] = b;
+          s_btab[qs * AT_BSTRIDE + j] =
+              j < S ? s_dist[j / Kc - qs + B_max - 2] * AT_LOG2E : -INFINITY;
         }
         soft_sync();
         cur_h = h;
       }
       const float* brow = s_btab + (min(q, S - 1) / Kc) * AT_BSTRIDE;
-      bool ok = mbar_wait_bounded(&bar_s, i & 1, &g_err_at, ERR_AT_S);
-      at_fence_after();
-      // pass 1: row max of the biased, masked logits (log2 units)
-      float mx = -INFINITY;
-#pragma unroll 1
-      for (int cc = 0; cc < AT_KW / 32; ++cc) {
-        const int jb = j0 + 32 * cc;
+      bool ok = true;
+      float m0 = 0.f, l0 = 0.f, l1 = 0.f;
+      for (int half = 0; half < 2; ++half) {
+        ok = mbar_wait_bounded(half ? &bar_s1 : &bar_s0, i & 1, &g_err_at, ERR_AT_S) && ok;
+        at_fence_after();
+        const int jb = 128 * half + 32 * hf;  // this warp's 32 keys of the half
         float v[32];
         at_ld32(tS + lane_off + jb, v);
+        // x = v / 8 * log2(e) + bias (log2 units), two at a time; kept for pass 2
+        float mx = -INFINITY;
+        const float2 c2 = make_float2(C, C);
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
           const float4 b4 = *reinterpret_cast<const float4*>(brow + jb + 4 * u);
-          mx = fmaxf(mx, fmaxf(fmaxf(fmaf(v[4 * u], C, b4.x), fmaf(v[4 * u + 1], C, b4.y)),
-                               fmaxf(fmaf(v[4 * u + 2], C, b4.z), fmaf(v[4 * u + 3], C, b4.w))));
+          const float2 xa = __ffma2_rn(make_float2(v[4 * u], v[4 * u + 1]), c2, make_float2(b4.x, b4.y));
+          const float2 xb = __ffma2_rn(make_float2(v[4 * u + 2], v[4 * u + 3]), c2, make_float2(b4.z, b4.w));
+          v[4 * u] = xa.x;
+          v[4 * u + 1] = xa.y;
+          v[4 * u + 2] = xb.x;
+          v[4 * u + 3] = xb.y;
+          mx = fmaxf(mx, fmaxf(fmaxf(xa.x, xa.y), fmaxf(xb.x, xb.y)));
         }
-      }
-      s_pmax[hf][r] = mx;
-      soft_sync();
-      float m2 = s_pmax[0][r];
+        s_pmax[half][hf][r] = mx;
+        quarter_sync(qq);
+        float mh = s_pmax[half][0][r];
 #pragma unroll
-      for (int k = 1; k < AT_NSPLIT; ++k) m2 = fmaxf(m2, s_pmax[k][r]);
-      // pass 2: p = 2^(x - max) and its sum; p as packed bf16 hi / lo over its logits
-      float l = 0.f;
-#pragma unroll 1
-      for (int cc = 0; cc < AT_KW / 32; ++cc) {
-        const int jb = j0 + 32 * cc;
-        float v[32];
-        at_ld32(tS + lane_off + jb, v);
+        for (int k = 1; k < AT_NSPLIT; ++k) mh = fmaxf(mh, s_pmax[half][k][r]);
+        float mref = mh;
+        if (half == 0) {
+          m0 = mh;
+        } else {
+          // Rows whose half 1 holds a much larger logit re-base on it: O[i] holds half 0's
+          // products (wait for them), scaled down with l0; other rows keep half 0's base
+          // (terms up to 2^RESCALE_AT).  The TMEM access is warp-wide.
+          const bool rebase = mh > m0 + RESCALE_AT;
+          if (!rebase) mref = m0;
+          if (__any_sync(FULL_MASK, rebase)) {
+            const float sc = rebase ? at_ex2(m0 - mh) : 1.f;
+            l0 *= sc;
+            mbar_wait_bounded(&bar_pv0, i & 1, &g_err_at, ERR_AT_O);
+            at_fence_after();
+            float o[AT_OW];
+            at_ld16(tO + lane_off + AT_OW * hf, o);
+#pragma unroll
+            for (int e = 0; e < AT_OW; ++e) o[e] *= sc;
+            at_st16f(tO + lane_off + AT_OW * hf, o);
+          }
+        }
+        float2 l2 = make_float2(0.f, 0.f);
         uint32_t ph[16], pl[16];
+        const float2 nm = make_float2(-mref, -mref);
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const float4 b4 = *reinterpret_cast<const float4*>(brow + jb + 4 * u);
-          const float p0 = at_ex2(fmaf(v[4 * u], C, b4.x) - m2);
-          const float p1 = at_ex2(fmaf(v[4 * u + 1], C, b4.y) - m2);
-          const float p2 = at_ex2(fmaf(v[4 * u + 2], C, b4.z) - m2);
-          const float p3 = at_ex2(fmaf(v[4 * u + 3], C, b4.w) - m2);
-          l += (p0 + p1) + (p2 + p3);
-          at_split2(p0, p1, ph[2 * u], pl[2 * u]);
-          at_split2(p2, p3, ph[2 * u + 1], pl[2 * u + 1]);
+        for (int u = 0; u < 16; ++u) {
+          const float2 y = __fadd2_rn(make_float2(v[2 * u], v[2 * u + 1]), nm);
+          const float p0 = at_ex2(y.x), p1 = at_ex2(y.y);
+          l2 = __fadd2_rn(l2, make_float2(p0, p1));
+          at_split2(p0, p1, ph[u], pl[u]);
         }
+        const float l = l2.x + l2.y;
         at_st16(tS + lane_off + jb, ph);
         at_st16(tS + lane_off + jb + 16, pl);
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        if (half == 0) l0 = l; else l1 = l;
+        at_fence_before();
+        mbar_arrive(half ? &bar_p1 : &bar_p0);
       }
-      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-      s_psum[hf][r] = l;
-      at_fence_before();
-      mbar_arrive(&bar_p);
-      soft_sync();
+      s_psum[hf][r] = l0 + l1;
+      quarter_sync(qq);
       float lsum = 0.f;
 #pragma unroll
       for (int k = 0; k < AT_NSPLIT; ++k) lsum += s_psum[k][r];
       const float inv = 1.0f / lsum;
-      // epilogue: O / l for this warp's 32 of the 64 output columns, split, stored
+      // epilogue: O / l for this warp's 16 of the 64 output columns, split, stored
       ok = mbar_wait_bounded(&bar_o, i & 1, &g_err_at, ERR_AT_O) && ok;
       at_fence_after();
       float v[AT_OW];
       at_ld16(tO + lane_off + AT_OW * hf, v);
       at_fence_before();
-      mbar_arrive(&bar_ofree);
+      mbar_arrive(&bar_ofree[i & 1]);
       if (q < S && ok) {
         __nv_bfloat16* dst = out + (tok0 + q) * 2 * H + h * AT_DH + AT_OW * hf;
         uint32_t hi[AT_OW / 2], lo[AT_OW / 2];

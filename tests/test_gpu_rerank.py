@@ -183,3 +183,23 @@ def test_rerank_captures_in_a_cuda_graph(lc):
         torch.cuda.synchronize()
         assert torch.equal(out["tokens"], eager["tokens"])
         assert torch.equal(out["path_score"], eager["path_score"])
+
+
+def test_attention_rebase_when_far_keys_dominate(lc):
+    """Slot-distance biases of +14 for keys eight or more slots ahead make the second key
+    half (keys 128-239) dominate the first slots' queries by more than 2^16: the
+    tcgen05 attention re-bases those rows on the second half's maximum and rescales the
+    first half's partial output.  Encoder output and tokens still match the oracle."""
+    wl = make_workload("highconc", V=4096, batch=2, tier="medium")
+    Bm = wl.dims["B_max"]
+    from synth.inputs import bf16_bits_to_f32, f32_to_bf16_bits
+    for l in range(wl.dims["layers"]):
+        bits = wl.weights[f"layers.{l}.dist_bias"]
+        f = bf16_bits_to_f32(bits).reshape(bits.shape)
+        f[:, Bm - 2 + 8:] += 14.0
+        wl.weights[f"layers.{l}.dist_bias"] = f32_to_bf16_bits(f).reshape(bits.shape)
+    gpu, rep = _compare(lc, wl)
+    for b in range(wl.batch):
+        ref = oracle_block(wl, b)
+        g = gpu["hidden"][b].reshape(ref["hidden"].shape)
+        assert np.abs(g - ref["hidden"]).max() <= 1e-4
