@@ -683,8 +683,6 @@ lilicorr_status lilicorr_rerank_host(const lilicorr_weights* w, const void* logi
   uint8_t* d_anchor = d_target + align256(size_t(batch) * H * 2);
   uint8_t* d_tokens = d_anchor + align256(size_t(batch) * 4);
   uint8_t* d_path = d_tokens + align256(size_t(batch) * B * 4);
-  LC_CUDA(cudaMemcpyAsync(d_logits, logits_host, size_t(batch) * B * V * es,
-                          cudaMemcpyHostToDevice, stream), "copy logits");
   if (slot_hidden_host)
     LC_CUDA(cudaMemcpyAsync(d_hidden, slot_hidden_host, size_t(batch) * B * H * 2,
                             cudaMemcpyHostToDevice, stream), "copy slot_hidden");
@@ -694,17 +692,71 @@ lilicorr_status lilicorr_rerank_host(const lilicorr_weights* w, const void* logi
   if (anchor_ids_host)
     LC_CUDA(cudaMemcpyAsync(d_anchor, anchor_ids_host, size_t(batch) * 4, cudaMemcpyHostToDevice,
                             stream), "copy anchor ids");
-  st = lilicorr_rerank(w, d_logits, ldtype, batch, B, V, K, slot_hidden_host ? d_hidden : nullptr,
-                       target_state_host ? d_target : nullptr,
-                       anchor_ids_host ? reinterpret_cast<int32_t*>(d_anchor) : nullptr,
-                       reinterpret_cast<int32_t*>(d_tokens), reinterpret_cast<float*>(d_path),
-                       nullptr, p, base, stream_);
-  if (st != LILICORR_OK) return st;
-  LC_CUDA(cudaMemcpyAsync(tokens_host, d_tokens, size_t(batch) * B * 4, cudaMemcpyDeviceToHost,
-                          stream), "copy tokens");
-  LC_CUDA(cudaMemcpyAsync(path_score_host, d_path, size_t(batch) * (B - 1) * 4,
-                          cudaMemcpyDeviceToHost, stream), "copy path score");
-  LC_CUDA(cudaStreamSynchronize(stream), "cudaStreamSynchronize");
+  // The logits arrive in chunks of blocks on a copy stream, rows 1..B-1 only (row 0, the
+  // anchor position, is never read); each chunk's rerank starts on `stream` as soon as
+  // its rows have landed, so the compute of one chunk hides under the copy of the next.
+  const int64_t nchunk = std::min<int64_t>(batch, 8);
+  const int64_t per = (batch + nchunk - 1) / nchunk;
+  cudaStream_t copy = nullptr;
+  std::vector<cudaEvent_t> ev(size_t(nchunk) + 1, nullptr);
+  auto cleanup = [&]() {
+    for (auto& e : ev)
+      if (e) cudaEventDestroy(e);
+    if (copy) cudaStreamDestroy(copy);
+  };
+  cudaError_t ce = cudaStreamCreateWithFlags(&copy, cudaStreamNonBlocking);
+  for (auto& e : ev)
+    if (ce == cudaSuccess) ce = cudaEventCreateWithFlags(&e, cudaEventDisableTiming);
+  if (ce == cudaSuccess) ce = cudaEventRecord(ev[nchunk], stream);  // earlier work first
+  if (ce == cudaSuccess) ce = cudaStreamWaitEvent(copy, ev[nchunk], 0);
+  const size_t row = size_t(V) * es;
+  for (int64_t c = 0; c < nchunk && ce == cudaSuccess; ++c) {
+    const int64_t b0 = c * per, nb = std::min<int64_t>(per, batch - b0);
+    if (nb <= 0) break;
+    const size_t off = (size_t(b0) * B + 1) * row;
+    ce = cudaMemcpy2DAsync(d_logits + off, size_t(B) * row,
+                           static_cast<const uint8_t*>(logits_host) + off, size_t(B) * row,
+                           size_t(B - 1) * row, size_t(nb), cudaMemcpyHostToDevice, copy);
+    if (ce == cudaSuccess) ce = cudaEventRecord(ev[c], copy);
+  }
+  if (ce != cudaSuccess) {
+    cleanup();
+    return cuda_fail(ce, "copy logits");
+  }
+  for (int64_t c = 0; c < nchunk; ++c) {
+    const int64_t b0 = c * per, nb = std::min<int64_t>(per, batch - b0);
+    if (nb <= 0) break;
+    ce = cudaStreamWaitEvent(stream, ev[c], 0);
+    if (ce != cudaSuccess) {
+      cleanup();
+      return cuda_fail(ce, "cudaStreamWaitEvent");
+    }
+    st = lilicorr_rerank(
+        w, d_logits + size_t(b0) * B * row, ldtype, nb, B, V, K,
+        slot_hidden_host ? d_hidden + size_t(b0) * B * H * 2 : nullptr,
+        target_state_host ? d_target + size_t(b0) * H * 2 : nullptr,
+        anchor_ids_host ? reinterpret_cast<int32_t*>(d_anchor) + b0 : nullptr,
+        reinterpret_cast<int32_t*>(d_tokens) + b0 * B, reinterpret_cast<float*>(d_path) + b0 * (B - 1),
+        nullptr, p, base, stream_);
+    if (st != LILICORR_OK) {
+      cudaStreamSynchronize(stream);
+      cleanup();
+      return st;
+    }
+  }
+  ce = cudaMemcpyAsync(tokens_host, d_tokens, size_t(batch) * B * 4, cudaMemcpyDeviceToHost,
+                       stream);
+  if (ce == cudaSuccess)
+    ce = cudaMemcpyAsync(path_score_host, d_path, size_t(batch) * (B - 1) * 4,
+                         cudaMemcpyDeviceToHost, stream);
+  if (ce != cudaSuccess) {
+    cudaStreamSynchronize(stream);
+    cleanup();
+    return cuda_fail(ce, "copy outputs");
+  }
+  ce = cudaStreamSynchronize(stream);
+  cleanup();
+  if (ce != cudaSuccess) return cuda_fail(ce, "cudaStreamSynchronize");
   return LILICORR_OK;
 }
 

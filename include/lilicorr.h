@@ -134,8 +134,11 @@ lilicorr_status lilicorr_rerank(const lilicorr_weights* w, const void* logits,
 /* Host-memory form of lilicorr_rerank: logits, slot_hidden, target_state and anchor_ids
  * are host pointers (pinned memory makes the copies asynchronous), tokens and
  * path_score are host outputs.  The inputs are copied to device staging inside
- * `workspace` (size from lilicorr_workspace_bytes_host), the rerank runs on `stream`,
- * the outputs are copied back, and the call returns after synchronising `stream`. */
+ * `workspace` (size from lilicorr_workspace_bytes_host); the logits travel in up to 8
+ * chunks of blocks on an internal copy stream, rows 1..B-1 only (row 0 is never read),
+ * and each chunk is reranked on `stream` as soon as it has landed, so compute hides
+ * under the copy.  The outputs are copied back and the call returns after synchronising
+ * `stream`.  Results are identical to lilicorr_rerank on the whole batch. */
 size_t lilicorr_workspace_bytes_host(const lilicorr_weights* w, int64_t batch, int32_t B,
                                      int32_t K, lilicorr_dtype ldtype);
 lilicorr_status lilicorr_rerank_host(const lilicorr_weights* w, const void* logits_host,

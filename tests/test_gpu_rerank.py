@@ -203,3 +203,26 @@ def test_attention_rebase_when_far_keys_dominate(lc):
         ref = oracle_block(wl, b)
         g = gpu["hidden"][b].reshape(ref["hidden"].shape)
         assert np.abs(g - ref["hidden"]).max() <= 1e-4
+
+
+@pytest.mark.parametrize("name,kw", [("highconc", dict(V=4096, batch=11)),
+                                     ("single", dict(V=3001, batch=3, B=9, with_slot_hidden=True)),
+                                     ("tiny", dict(batch=1))])
+def test_rerank_host_matches_device_entry(lc, name, kw):
+    """The host-memory entry point (chunked copies of rows 1..B-1 overlapped with the
+    per-chunk reranks) returns exactly what the device entry point returns."""
+    wl = make_workload(name, **kw)
+    w = lc.Weights(wl.dims, wl.weights)
+    dev = _gpu_run(lc, wl, weights=w, taps=False)
+    x = torch.from_numpy(wl.logits.view(np.int16)).view(torch.bfloat16) if wl.ldtype == "bf16" \
+        else torch.from_numpy(wl.logits)
+    pin = lambda t: None if t is None else t.pin_memory()
+    tgt = None if wl.target_state is None else torch.from_numpy(wl.target_state.view(np.int16)).view(torch.bfloat16)
+    sh = None if wl.slot_hidden is None else torch.from_numpy(wl.slot_hidden.view(np.int16)).view(torch.bfloat16)
+    anc = None if wl.anchor_ids is None else torch.from_numpy(wl.anchor_ids)
+    for _ in range(2):  # the second call reuses the staging
+        tok, ps = lc.rerank_host(w, pin(x.contiguous()), wl.K, target_state=pin(tgt),
+                                 slot_hidden=pin(sh), anchor_ids=pin(anc))
+        assert np.array_equal(tok.numpy(), dev["tokens"])
+        assert np.array_equal(ps.numpy(), dev["path_score"])
+    w.close()
