@@ -13,23 +13,24 @@
 // each CTA streams a contiguous segment of one row through shared memory with 1-D bulk
 // copies (cp.async.bulk, 32 KB stages, 3 in flight, 2 CTAs per SM).  A producer warp
 // refills a ring slot as soon as the 16 consumer warps have each released it (an
-// mbarrier per slot; no CTA-wide barrier while streaming).  Every consumer thread takes
-// four 16-byte chunks per stage:
-//   * online log-sum-exp in base 2: per chunk one 3-input max tree, then packed f32x2
-//     FFMA / FADD around one ex2 per element (two partial sums per thread);
+// mbarrier per slot; no CTA-wide barrier while streaming).  Every consumer thread copies
+// its four 16-byte chunks of a stage into registers, takes their maxima and releases the
+// slot at once; the rest of the stage's work runs from registers:
+//   * online log-sum-exp in base 2: the running maximum is raised once per stage, then
+//     packed f32x2 FFMA / FADD around one ex2 per element (two partial sums per thread);
 //   * top-K: each consumer warp keeps its own running top-32 (value, id) pairs, sorted
-//     across its lanes.  After a stage, each thread compares its chunk maxima with the
-//     warp's threshold, the better of its own K-th entry and a CTA-wide floor; one vote
-//     skips the rest in the common case.  Only a hit re-reads its chunk from shared
-//     memory and appends the elements that can still enter to the warp's buffer, which
-//     is folded in 32 at a time (warp bitonic sort + bitonic merge).
+//     across its lanes.  After a stage one vote compares every thread's stage maximum
+//     with the warp's threshold, the better of its own K-th entry and a CTA-wide floor.
+//     Only on a hit are the hit chunks unpacked and the elements that can still enter
+//     appended to the warp's buffer, which is folded in 32 at a time (warp bitonic sort
+//     + bitonic merge).
 //   * the CTA floor is the K-th largest of 32 thread-group running maxima (K distinct
-//     elements are at least that large), kept fresh by the producer warp while it waits
-//     and raised by every warp's own K-th entry.  Stage 0 is checked either one stage
-//     late, when the group maxima already cover it, or at once against the warp's own
-//     K-th largest thread maximum (K <= 16 on long segments).
-// At the end the 17 warp queues (the producer's holds the unaligned head and tail) are
-// merged in a tree.
+//     elements are at least that large).  After stage 0 the consumer warps meet once so
+//     that the first floor covers the whole stage; afterwards the producer warp keeps it
+//     fresh (once per stage and while it waits), and every fold raises it to the warp's
+//     own K-th entry.
+// At the end every warp offers its K-th entry to the floor; only queue and buffer entries
+// at or above the final floor are gathered into one list, which one warp folds.
 // Rows are split into P segments when there are too few rows to fill 152 SMs; the last
 // CTA of a row (atomic counter, no waiting) merges the P partial results.
 #include <float.h>
@@ -228,6 +229,9 @@ __device__ __forceinline__ void unpack16(const uint4 w, float (&x)[NV]) {
 constexpr int K1_WCAP = 64;    // per-warp candidate buffer entries
 constexpr int K1_GROUPS = 32;  // thread groups whose running maxima give the CTA floor
 constexpr int K1_GSIZE = K1_CTHREADS / K1_GROUPS;
+// Final candidate list: at most every queue entry (17 warps) and every buffer entry.
+constexpr int K1_UCAP = (K1_CWARPS + 1) * KQ + K1_CWARPS * K1_WCAP;
+static_assert(K1_UCAP * 8 <= K1_STAGE_BYTES, "final candidate list must fit in one ring slot");
 
 __device__ __forceinline__ float max3f(float a, float b, float c) {
   float r;
@@ -235,52 +239,77 @@ __device__ __forceinline__ float max3f(float a, float b, float c) {
   return r;
 }
 
-// Consumer-side log-sum-exp of one 16-byte chunk; returns the chunk maximum.  The sum is
-// kept as two partial sums (even / odd elements) updated with packed f32x2 arithmetic.
-// When the thread's running maximum rises (the rescale branch), it is offered to its
-// group's maximum in shared memory.
+// Maximum of one 16-byte chunk (8 bf16 compared as packed pairs, or 4 f32).
+template <typename T>
+__device__ __forceinline__ float chunk_max(const uint4 w);
+template <>
+__device__ __forceinline__ float chunk_max<__nv_bfloat16>(const uint4 w) {
+  const __nv_bfloat162 a = __hmax2(*reinterpret_cast<const __nv_bfloat162*>(&w.x),
+                                   *reinterpret_cast<const __nv_bfloat162*>(&w.y));
+  const __nv_bfloat162 b = __hmax2(*reinterpret_cast<const __nv_bfloat162*>(&w.z),
+                                   *reinterpret_cast<const __nv_bfloat162*>(&w.w));
+  const __nv_bfloat162 c = __hmax2(a, b);
+  return fmaxf(__low2float(c), __high2float(c));
+}
+template <>
+__device__ __forceinline__ float chunk_max<float>(const uint4 w) {
+  return fmaxf(max3f(__uint_as_float(w.x), __uint_as_float(w.y), __uint_as_float(w.z)),
+               __uint_as_float(w.w));
+}
+
+// Consumer-side log-sum-exp of one stage held in registers (chunk words w, validity bits,
+// the thread's maximum smax over its chunks).  The running maximum m2 is raised once per stage; when it rises it
+// is offered to the thread group's maximum in shared memory.  The sum is kept as two
+// partial sums (even / odd elements) updated with packed f32x2 arithmetic.
 template <int NV>
-__device__ __forceinline__ float lse_chunk_g(const float (&x)[NV], float& m2, float2& s2,
-                                             int* gmax) {
-  float cm;
-  if constexpr (NV == 8)
-    cm = fmaxf(max3f(x[0], x[1], x[2]), max3f(x[3], x[4], max3f(x[5], x[6], x[7])));
-  else
-    cm = fmaxf(max3f(x[0], x[1], x[2]), x[3]);
-  const float cm2 = cm * LOG2E;
-  if (cm2 > m2) {
-    const float sc = ex2(m2 - cm2);
+__device__ __forceinline__ void lse_stage(const uint4 (&w)[K1_CPT], unsigned valid, float smax,
+                                          float& m2, float2& s2, int* gmax) {
+  const float sm2 = smax * LOG2E;
+  if (sm2 > m2) {
+    const float sc = ex2(m2 - sm2);
     s2 = __fmul2_rn(s2, make_float2(sc, sc));
-    m2 = cm2;
-    atomicMax(gmax, float_key(cm));
+    m2 = sm2;
+    atomicMax(gmax, float_key(smax));
   }
   const float2 l2 = make_float2(LOG2E, LOG2E);
   const float2 nm = make_float2(-m2, -m2);
 #pragma unroll
-  for (int j = 0; j < NV; j += 2) {
-    const float2 y = __ffma2_rn(make_float2(x[j], x[j + 1]), l2, nm);
-    s2 = __fadd2_rn(s2, make_float2(ex2(y.x), ex2(y.y)));
+  for (int i = 0; i < K1_CPT; ++i) {
+    if ((valid >> i) & 1u) {
+      float x[NV];
+      unpack16<NV>(w[i], x);
+#pragma unroll
+      for (int j = 0; j < NV; j += 2) {
+        const float2 y = __ffma2_rn(make_float2(x[j], x[j + 1]), l2, nm);
+        s2 = __fadd2_rn(s2, make_float2(ex2(y.x), ex2(y.y)));
+      }
+    }
   }
-  return cm;
 }
 
 // Warp-uniform: the K-th largest of the 32 group maxima.  Each group's maximum is an
 // element of a distinct set of threads, so K elements of the segment are at least this
 // large: a valid inclusive floor for the K-th largest value.
 __device__ __forceinline__ float group_floor(const int* gmax, int lane, int K) {
-  const float g = key_float(*reinterpret_cast<const volatile int*>(&gmax[lane]));
+  float g = key_float(*reinterpret_cast<const volatile int*>(&gmax[lane]));
+  if (K == 1) {
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) g = fmaxf(g, __shfl_xor_sync(FULL_MASK, g, o));
+    return g;
+  }
   return __shfl_sync(FULL_MASK, warp_sort_desc(g, lane), K - 1);
 }
 
-template <typename T, bool DEFER0>
+template <typename T>
 __global__ void __launch_bounds__(K1_THREADS, K1_MIN_BLOCKS) logit_pass_kernel(const K1Params p) {
   constexpr int ES = sizeof(T);
   constexpr int NV = 16 / ES;
   extern __shared__ __align__(128) uint8_t k1_dyn_smem[];
   uint8_t(*stage)[K1_STAGE_BYTES] = reinterpret_cast<uint8_t(*)[K1_STAGE_BYTES]>(k1_dyn_smem);
   __shared__ __align__(8) uint64_t full_bar[K1_NSTAGES], empty_bar[K1_NSTAGES];
-  __shared__ float s_bv[K1_CWARPS + 1][K1_WCAP];  // per-warp candidates, then the queues
-  __shared__ int s_bi[K1_CWARPS + 1][K1_WCAP];
+  __shared__ float s_bv[K1_CWARPS][K1_WCAP];  // per-warp candidate buffers
+  __shared__ int s_bi[K1_CWARPS][K1_WCAP];
+  __shared__ int s_ucnt;                       // entries of the final candidate list
   __shared__ int s_wcnt[K1_CWARPS];
   __shared__ int s_gmax[K1_GROUPS];  // float_key of each thread group's running maximum
   __shared__ int s_floor;            // float_key of the CTA floor (atomic max)
@@ -315,6 +344,7 @@ __global__ void __launch_bounds__(K1_THREADS, K1_MIN_BLOCKS) logit_pass_kernel(c
     }
     fence_mbar_init();
     s_abort = 0;
+    s_ucnt = 0;
     s_floor = float_key(-INFINITY);
   }
   if (tid < K1_GROUPS) s_gmax[tid] = float_key(-INFINITY);
@@ -362,6 +392,10 @@ __global__ void __launch_bounds__(K1_THREADS, K1_MIN_BLOCKS) logit_pass_kernel(c
     for (int st = K1_NSTAGES; st < nstages; ++st) {
       const int sl = st % K1_NSTAGES;
       const uint32_t par = ((st / K1_NSTAGES) - 1) & 1;
+      {
+        const float f = group_floor(s_gmax, lane, K);
+        if (lane == 0) atomicMax(&s_floor, float_key(f));
+      }
       const long long t0 = clock64();
       int ready = 0;
       for (;;) {
@@ -392,165 +426,148 @@ __global__ void __launch_bounds__(K1_THREADS, K1_MIN_BLOCKS) logit_pass_kernel(c
     int* gmax = &s_gmax[tid / K1_GSIZE];
     int* wcnt = &s_wcnt[warp];
     float2 s2 = make_float2(0.f, 0.f);  // partial sums of this thread's exponentials
-    float cm0[K1_CPT];  // stage 0, checked one stage late against a CTA floor
-    unsigned valid0 = 0;
 
-    // Candidates of stage st (chunk maxima cmx, validity bits vmask): compare with the
-    // threshold, re-read hit chunks from the slot, append to the warp buffer, fold.
-    auto check_stage = [&](int st, const float (&cmx)[K1_CPT], unsigned vmask) {
-      const int sl = st % K1_NSTAGES;
+    // Candidates of stage st (chunk maxima cmx, validity bits vmask, chunk words from
+    // chunk_at(i)): compare with the threshold, the better of the warp's K-th entry and
+    // the CTA floor fl; append the elements of hit chunks that can still enter to the
+    // warp buffer; fold it into the queue 32 entries at a time.
+    auto check_stage = [&](int st, const float (&cmx)[K1_CPT], unsigned vmask, float smax,
+                           float fl, auto&& chunk_at) {
       const int soff = st * K1_STAGE_BYTES;
-      const uint8_t* sbuf = stage[sl];
-      const float fl = key_float(*reinterpret_cast<volatile int*>(&s_floor));
       float tv = q.tv;
       int ti = q.tid;
       if (fl > tv) {
         tv = fl;
         ti = INT_MAX;
       }
-      bool hit = false;
+      if (!__any_sync(FULL_MASK, smax >= tv)) return;
+      const int prev = *reinterpret_cast<volatile int*>(wcnt);
+      __syncwarp();
 #pragma unroll
-      for (int i = 0; i < K1_CPT; ++i) hit |= ((vmask >> i) & 1u) && cmx[i] >= tv;
-      if (__any_sync(FULL_MASK, hit)) {
-        const int prev = *reinterpret_cast<volatile int*>(wcnt);
-        __syncwarp();
+      for (int i = 0; i < K1_CPT; ++i) {
+        if (((vmask >> i) & 1u) && cmx[i] >= tv) {
+          const int c = tid + i * K1_CTHREADS;
+          float x[NV];
+          unpack16<NV>(chunk_at(i), x);
+          const int id0 = seg_elem0 + (soff + c * 16) / ES;
 #pragma unroll
-        for (int i = 0; i < K1_CPT; ++i) {
-          if (((vmask >> i) & 1u) && cmx[i] >= tv) {
-            const int c = tid + i * K1_CTHREADS;
-            float x[NV];
-            unpack16<NV>(*reinterpret_cast<const uint4*>(sbuf + c * 16), x);
-            const int id0 = seg_elem0 + (soff + c * 16) / ES;
-#pragma unroll
-            for (int j = 0; j < NV; ++j)
-              if (better(x[j], id0 + j, tv, ti)) {
-                const int idx = atomicAdd(wcnt, 1);
-                if (idx < K1_WCAP) {
-                  bv[idx] = x[j];
-                  bi[idx] = id0 + j;
-                }
+          for (int j = 0; j < NV; ++j)
+            if (better(x[j], id0 + j, tv, ti)) {
+              const int idx = atomicAdd(wcnt, 1);
+              if (idx < K1_WCAP) {
+                bv[idx] = x[j];
+                bi[idx] = id0 + j;
               }
-          }
-        }
-        __syncwarp();
-        int cnt = *reinterpret_cast<volatile int*>(wcnt);
-        if (cnt >= 32) {
-          if (cnt > K1_WCAP) {
-            // Too many ties for the buffer: fold the earlier stages' entries, then this
-            // stage's chunks element by element from the slot; the buffer is dropped.
-            const bool has = lane < prev;
-            queue_absorb(q, has ? bv[lane] : -INFINITY, has ? bi[lane] : INT_MAX, lane, K);
-#pragma unroll
-            for (int i = 0; i < K1_CPT; ++i) {
-              const int c = tid + i * K1_CTHREADS;
-              const bool hv = (vmask >> i) & 1u;
-              float x[NV];
-              if (hv) unpack16<NV>(*reinterpret_cast<const uint4*>(sbuf + c * 16), x);
-              const int id0 = seg_elem0 + (soff + c * 16) / ES;
-#pragma unroll
-              for (int j = 0; j < NV; ++j)
-                queue_absorb(q, hv ? x[j] : -INFINITY, hv ? id0 + j : INT_MAX, lane, K);
             }
-            cnt = 0;
-          } else {
-            while (cnt >= 32) {
-              const float v = bv[lane];
-              const int id = bi[lane];
-              const bool more = lane + 32 < cnt;
-              const float v2 = more ? bv[lane + 32] : 0.f;
-              const int i2 = more ? bi[lane + 32] : 0;
-              __syncwarp();
-              if (more) {
-                bv[lane] = v2;
-                bi[lane] = i2;
-              }
-              cnt -= 32;
-              queue_absorb(q, v, id, lane, K);
-              __syncwarp();
-            }
-          }
-          __syncwarp();
-          if (lane == 0) {
-            *wcnt = cnt;
-            if (q.tv != -INFINITY) atomicMax(&s_floor, float_key(q.tv));
-          }
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&empty_bar[sl]);
+      int cnt = *reinterpret_cast<volatile int*>(wcnt);
+      if (cnt < 32) return;
+      if (cnt > K1_WCAP) {
+        // Too many ties for the buffer: fold the earlier stages' entries, then this
+        // stage's chunks element by element; the buffer is dropped.
+        const bool has = lane < prev;
+        queue_absorb(q, has ? bv[lane] : -INFINITY, has ? bi[lane] : INT_MAX, lane, K);
+#pragma unroll
+        for (int i = 0; i < K1_CPT; ++i) {
+          const int c = tid + i * K1_CTHREADS;
+          const bool hv = (vmask >> i) & 1u;
+          float x[NV];
+          if (hv) unpack16<NV>(chunk_at(i), x);
+          const int id0 = seg_elem0 + (soff + c * 16) / ES;
+#pragma unroll
+          for (int j = 0; j < NV; ++j)
+            queue_absorb(q, hv ? x[j] : -INFINITY, hv ? id0 + j : INT_MAX, lane, K);
+        }
+        cnt = 0;
+      } else {
+        while (cnt >= 32) {
+          const float v = bv[lane];
+          const int id = bi[lane];
+          const bool more = lane + 32 < cnt;
+          const float v2 = more ? bv[lane + 32] : 0.f;
+          const int i2 = more ? bi[lane + 32] : 0;
+          __syncwarp();
+          if (more) {
+            bv[lane] = v2;
+            bi[lane] = i2;
+          }
+          cnt -= 32;
+          queue_absorb(q, v, id, lane, K);
+          __syncwarp();
+        }
+      }
+      __syncwarp();
+      if (lane == 0) {
+        *wcnt = cnt;
+        if (q.tv != -INFINITY) atomicMax(&s_floor, float_key(q.tv));
+      }
     };
 
     for (int st = 0; st < nstages; ++st) {
       const int sl = st % K1_NSTAGES;
       if (!mbar_wait_bounded(&full_bar[sl], (st / K1_NSTAGES) & 1, &g_err_k1, ERR_K1_FULL_WAIT))
         s_abort = 1;
-      if (s_abort) break;
-      const int soff = st * K1_STAGE_BYTES;
-      const int nbytes = min(K1_STAGE_BYTES, seg_bytes - soff);
+      if (st > 0 && s_abort) break;  // stage 0 first meets the other consumer warps
+      const int nbytes = min(K1_STAGE_BYTES, seg_bytes - st * K1_STAGE_BYTES);
       const uint8_t* sbuf = stage[sl];
+      // This thread's chunks of the stage into registers, and their maxima.
+      uint4 w[K1_CPT];
       float cm[K1_CPT];
       unsigned valid = 0;  // bit i: this thread has chunk i of the stage
 #pragma unroll
       for (int i = 0; i < K1_CPT; ++i) {
         const int c = tid + i * K1_CTHREADS;
-        cm[i] = -INFINITY;
+        w[i] = make_uint4(0u, 0u, 0u, 0u);
         if (c * 16 < nbytes) {
           valid |= 1u << i;
-          float x[NV];
-          unpack16<NV>(*reinterpret_cast<const uint4*>(sbuf + c * 16), x);
-          cm[i] = lse_chunk_g<NV>(x, m2, s2, gmax);
+          w[i] = *reinterpret_cast<const uint4*>(sbuf + c * 16);
         }
       }
+#pragma unroll
+      for (int i = 0; i < K1_CPT; ++i) cm[i] = ((valid >> i) & 1u) ? chunk_max<T>(w[i]) : -INFINITY;
+      // The stage is in registers: release the slot to the producer at once.
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty_bar[sl]);
+
+      float smax = cm[0];  // this thread's maximum of the stage
+#pragma unroll
+      for (int i = 1; i < K1_CPT; ++i) smax = fmaxf(smax, cm[i]);
+      float fl;
       if (st == 0) {
-#pragma unroll
-        for (int i = 0; i < K1_CPT; ++i) cm0[i] = cm[i];
-        valid0 = valid;
-      }
-      if constexpr (!DEFER0) {
-        if (st == 0) {
-          // immediate first floor: this warp's K-th largest thread maximum of stage 0
-          float tmax = cm[0];
-#pragma unroll
-          for (int i = 1; i < K1_CPT; ++i) tmax = fmaxf(tmax, cm[i]);
-          const float wf = __shfl_sync(FULL_MASK, warp_sort_desc(tmax, lane), K - 1);
-          if (lane == 0 && wf != -INFINITY) atomicMax(&s_floor, float_key(wf));
-          __syncwarp();
-        }
-        check_stage(st, cm, valid);
+        // First CTA floor: every thread offers its stage-0 maximum to its group, the
+        // consumer warps meet, and each takes the K-th largest of the 32 group maxima.
+        if (smax != -INFINITY) atomicMax(gmax, float_key(smax));
+        named_bar_sync(1, K1_CTHREADS);
+        if (s_abort) break;
+        fl = group_floor(s_gmax, lane, K);
+        if (warp == 0 && lane == 0) atomicMax(&s_floor, float_key(fl));
+        lse_stage<NV>(w, valid, smax, m2, s2, gmax);
       } else {
-        if (st == 1 || (st == 0 && nstages == 1)) {
-          // the group maxima now cover (most of) stage 0: the first CTA floor
-          const float f = group_floor(s_gmax, lane, K);
-          if (lane == 0) atomicMax(&s_floor, float_key(f));
-          __syncwarp();
-          check_stage(0, cm0, valid0);
-        }
-        if (st >= 1) check_stage(st, cm, valid);
+        lse_stage<NV>(w, valid, smax, m2, s2, gmax);
+        fl = key_float(*reinterpret_cast<volatile int*>(&s_floor));
       }
+      check_stage(st, cm, valid, smax, fl, [&](int i) { return w[i]; });
     }
     ssum = s2.x + s2.y;
-    // flush the warp buffer into the queue
-    __syncwarp();
-    const int cnt = *reinterpret_cast<volatile int*>(wcnt);
-    if (cnt > 0 && !s_abort) {
-      const bool has = lane < cnt;
-      queue_absorb(q, has ? bv[lane] : -INFINITY, has ? bi[lane] : INT_MAX, lane, K);
-    }
   }
 
-  // ---- CTA reduction: log-sum-exp partials and the 17 warp queues
+  // ---- CTA reduction.  Log-sum-exp: within each warp, then across the warps.  Top-K:
+  // every warp offers its K-th queue entry to the CTA floor; then only queue and buffer
+  // entries at or above that final floor can be among the segment's K best, and they are
+  // gathered into one list (in ring slot 0, free once every stage is consumed) that
+  // warp 0 folds.
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) {
     const float om = __shfl_xor_sync(FULL_MASK, m2, o);
     const float os = __shfl_xor_sync(FULL_MASK, ssum, o);
     lse_merge(m2, ssum, om, os);
   }
-  __syncwarp();
-  s_bv[warp][lane] = q.qv;
-  s_bi[warp][lane] = q.qid;
   if (lane == 0) {
     s_m2[warp] = m2;
     s_s[warp] = ssum;
+    if (q.tv != -INFINITY) atomicMax(&s_floor, float_key(q.tv));
   }
   __syncthreads();
   if (s_abort) {
@@ -561,25 +578,39 @@ __global__ void __launch_bounds__(K1_THREADS, K1_MIN_BLOCKS) logit_pass_kernel(c
                           ERR_K1_DRAIN);
     return;
   }
-  // tree merge of the queues: 17 -> 16 -> 8 -> 4 -> 2 -> 1
-  auto merge_into = [&](int dst, int src) {
-    float v = s_bv[dst][lane];
-    int id = s_bi[dst][lane];
-    bitonic_merge(v, id, s_bv[src][lane], s_bi[src][lane], lane);
-    __syncwarp();
-    s_bv[dst][lane] = v;
-    s_bi[dst][lane] = id;
-  };
-  if (warp == 0) merge_into(0, K1_CWARPS);
-  __syncthreads();
-  for (int half = K1_CWARPS / 2; half >= 1; half >>= 1) {
-    if (warp < half) merge_into(warp, warp + half);
-    __syncthreads();
+  float* uv = reinterpret_cast<float*>(stage[0]);
+  int* ui = reinterpret_cast<int*>(stage[0] + K1_UCAP * sizeof(float));
+  {
+    const float F = key_float(s_floor);
+    if (q.qid != INT_MAX && q.qv >= F) {
+      const int k = atomicAdd(&s_ucnt, 1);
+      uv[k] = q.qv;
+      ui[k] = q.qid;
+    }
+    if (warp < K1_CWARPS) {
+      const int cnt = min(s_wcnt[warp], K1_WCAP);
+      for (int j = lane; j < cnt; j += 32) {
+        const float bvj = s_bv[warp][j];
+        if (bvj >= F) {
+          const int k = atomicAdd(&s_ucnt, 1);
+          uv[k] = bvj;
+          ui[k] = s_bi[warp][j];
+        }
+      }
+    }
   }
+  __syncthreads();
   if (warp != 0) return;
 
-  float v = s_bv[0][lane];
-  int id = s_bi[0][lane];
+  WarpQueue fq;
+  fq.init();
+  const int nu = s_ucnt;
+  for (int b0 = 0; b0 < nu; b0 += 32) {
+    const bool has = b0 + lane < nu;
+    queue_absorb(fq, has ? uv[b0 + lane] : -INFINITY, has ? ui[b0 + lane] : INT_MAX, lane, K);
+  }
+  float v = fq.qv;
+  int id = fq.qid;
   float M = lane <= K1_CWARPS ? s_m2[lane] : M2_INIT;
   float S = lane <= K1_CWARPS ? s_s[lane] : 0.f;
 #pragma unroll
@@ -743,11 +774,6 @@ cudaError_t k1_launch(const void* logits, int esize, int64_t batch, int B, int64
   prm.partials = nullptr;
   prm.counters = nullptr;
   prm.row_stride = row_stride > 0 ? row_stride : V;
-  // First floor.  Deferred: stage 0 is checked one stage late against the K-th largest
-  // of the 32 group maxima, which by then cover it (strong, but holds a ring slot for a
-  // stage).  Immediate: checked at once against the warp's own K-th largest thread
-  // maximum (weaker; better for K <= 16 on long segments, where the slot matters more).
-  const bool defer0 = K > 16 || pl.seg_bytes < 6 * K1_STAGE_BYTES;
   prm.id_offset = id_offset;
   prm.records = static_cast<char*>(records);
   const int64_t rows = batch * (B - 1);
@@ -762,27 +788,16 @@ cudaError_t k1_launch(const void* logits, int esize, int64_t batch, int B, int64
   constexpr int dyn = K1_NSTAGES * K1_STAGE_BYTES;
   static bool attr_done = false;
   if (!attr_done) {
-    cudaFuncSetAttribute(logit_pass_kernel<__nv_bfloat16, true>,
+    cudaFuncSetAttribute(logit_pass_kernel<__nv_bfloat16>,
                          cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
-    cudaFuncSetAttribute(logit_pass_kernel<__nv_bfloat16, false>,
-                         cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
-    cudaFuncSetAttribute(logit_pass_kernel<float, true>,
-                         cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
-    cudaFuncSetAttribute(logit_pass_kernel<float, false>,
-                         cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
+    cudaFuncSetAttribute(logit_pass_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         dyn);
     attr_done = true;
   }
-  if (esize == 2) {
-    if (defer0)
-      logit_pass_kernel<__nv_bfloat16, true><<<grid, K1_THREADS, dyn, stream>>>(prm);
-    else
-      logit_pass_kernel<__nv_bfloat16, false><<<grid, K1_THREADS, dyn, stream>>>(prm);
-  } else {
-    if (defer0)
-      logit_pass_kernel<float, true><<<grid, K1_THREADS, dyn, stream>>>(prm);
-    else
-      logit_pass_kernel<float, false><<<grid, K1_THREADS, dyn, stream>>>(prm);
-  }
+  if (esize == 2)
+    logit_pass_kernel<__nv_bfloat16><<<grid, K1_THREADS, dyn, stream>>>(prm);
+  else
+    logit_pass_kernel<float><<<grid, K1_THREADS, dyn, stream>>>(prm);
   note_launch();
   return cudaGetLastError();
 }
