@@ -107,13 +107,13 @@ __device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src_gmem, u
       : "memory");
 }
 
-// Ordered key of a float: signed-int comparison of keys matches float comparison
-// (with -0.0 ordered just below +0.0, which only ever loosens a lower bound).
 // Barrier among the first nthreads (a multiple of 32) threads that use barrier id.
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Ordered key of a float: signed-int comparison of keys matches float comparison
+// (with -0.0 ordered just below +0.0, which only ever loosens a lower bound).
 __device__ __forceinline__ int float_key(float f) {
   int b = __float_as_int(f);
   return b >= 0 ? b : (b ^ 0x7fffffff);

@@ -226,6 +226,15 @@ __device__ __forceinline__ void unpack16(const uint4 w, float (&x)[NV]) {
   }
 }
 
+// Element j of a 16-byte chunk (8 bf16 or 4 f32).
+template <int NV>
+__device__ __forceinline__ float elem_of(const uint4 w, int j) {
+  const int k = NV == 8 ? j >> 1 : j;
+  const uint32_t wd = k == 0 ? w.x : k == 1 ? w.y : k == 2 ? w.z : w.w;
+  if constexpr (NV == 8) return __uint_as_float((j & 1) ? (wd & 0xffff0000u) : (wd << 16));
+  else return __uint_as_float(wd);
+}
+
 constexpr int K1_WCAP = 64;    // per-warp candidate buffer entries
 constexpr int K1_GROUPS = 32;  // thread groups whose running maxima give the CTA floor
 constexpr int K1_GSIZE = K1_CTHREADS / K1_GROUPS;
@@ -469,16 +478,17 @@ __global__ void __launch_bounds__(K1_THREADS, K1_MIN_BLOCKS) logit_pass_kernel(c
         // stage's chunks element by element; the buffer is dropped.
         const bool has = lane < prev;
         queue_absorb(q, has ? bv[lane] : -INFINITY, has ? bi[lane] : INT_MAX, lane, K);
+        // (a rolled loop: one copy of the fold keeps the kernel's code small)
+#pragma unroll 1
+        for (int e = 0; e < K1_CPT * NV; ++e) {
+          const int i = e / NV;
+          uint4 cw = chunk_at(0);
 #pragma unroll
-        for (int i = 0; i < K1_CPT; ++i) {
-          const int c = tid + i * K1_CTHREADS;
+          for (int k = 1; k < K1_CPT; ++k)
+            if (i == k) cw = chunk_at(k);
           const bool hv = (vmask >> i) & 1u;
-          float x[NV];
-          if (hv) unpack16<NV>(chunk_at(i), x);
-          const int id0 = seg_elem0 + (soff + c * 16) / ES;
-#pragma unroll
-          for (int j = 0; j < NV; ++j)
-            queue_absorb(q, hv ? x[j] : -INFINITY, hv ? id0 + j : INT_MAX, lane, K);
+          const int id = seg_elem0 + (soff + (tid + i * K1_CTHREADS) * 16) / ES + e % NV;
+          queue_absorb(q, hv ? elem_of<NV>(cw, e % NV) : -INFINITY, hv ? id : INT_MAX, lane, K);
         }
         cnt = 0;
       } else {
