@@ -132,40 +132,38 @@ __global__ void conf_hidden_kernel(const float* __restrict__ cand_logit,
                                    const float* __restrict__ lse, int64_t M, int K, int H,
                                    const float* __restrict__ w1, const float* __restrict__ b1,
                                    __nv_bfloat16* __restrict__ U) {
+  // One warp per slot (its K candidate rows share the slot's lse and top logit): lane k
+  // forms row k's five features, which are then broadcast row by row.
   const int lane = threadIdx.x & 31, nw = blockDim.x >> 5;
   const int nch = H / 8;
   float w[8][6];
   if (lane < nch) conf_load_w(w1, b1, lane * 8, w);
-  const int64_t step = int64_t(gridDim.x) * nw;
-  int64_t m = int64_t(blockIdx.x) * nw + (threadIdx.x >> 5);
-  // the three scalars of a row are loaded one row ahead
-  float nl = 0.f, nc = 0.f, nt = 0.f;
-  if (m < M) {
-    nl = __ldg(lse + m / K);
-    nc = __ldg(cand_logit + m);
-    nt = __ldg(cand_logit + (m / K) * K);
-  }
-  for (; m < M; m += step) {
-    const int k = static_cast<int>(m % K);
-    const float lp = nc - nl, lp_top = nt - nl;
-    const int64_t mn = m + step;
-    if (mn < M) {
-      nl = __ldg(lse + mn / K);
-      nc = __ldg(cand_logit + mn);
-      nt = __ldg(cand_logit + (mn / K) * K);
+  const int64_t nslots = M / K;
+  for (int64_t j = int64_t(blockIdx.x) * nw + (threadIdx.x >> 5); j < nslots;
+       j += int64_t(gridDim.x) * nw) {
+    const float* cl = cand_logit + j * K;
+    const float l2 = __ldg(lse + j);
+    const float top = __ldg(cl);
+    float g[5] = {0.f, 0.f, 0.f, 0.f, 0.f};
+    if (lane < K) {
+      const float lp = __ldg(cl + lane) - l2;
+      g[0] = lp;
+      g[1] = expf(lp);
+      g[2] = lp - (top - l2);
+      g[3] = K > 1 ? float(lane) / float(K - 1) : 0.f;
+      g[4] = lane == 0 ? 1.f : 0.f;
     }
-    float f[5];
-    f[0] = lp;
-    f[1] = expf(lp);
-    f[2] = lp - lp_top;
-    f[3] = K > 1 ? float(k) / float(K - 1) : 0.f;
-    f[4] = k == 0 ? 1.f : 0.f;
-    __nv_bfloat16* u = U + m * 2 * H;
-    if (lane < nch) conf_chunk(f, w, u + lane * 8, u + H + lane * 8);
-    for (int c = lane + 32; c < nch; c += 32) {  // hidden sizes above 256
-      float w2[8][6];
-      conf_load_w(w1, b1, c * 8, w2);
-      conf_chunk(f, w2, u + c * 8, u + H + c * 8);
+    __nv_bfloat16* u = U + j * K * 2 * H;
+    for (int k = 0; k < K; ++k, u += 2 * H) {
+      float f[5];
+#pragma unroll
+      for (int i = 0; i < 5; ++i) f[i] = __shfl_sync(FULL_MASK, g[i], k);
+      if (lane < nch) conf_chunk(f, w, u + lane * 8, u + H + lane * 8);
+      for (int c = lane + 32; c < nch; c += 32) {  // hidden sizes above 256
+        float w2[8][6];
+        conf_load_w(w1, b1, c * 8, w2);
+        conf_chunk(f, w2, u + c * 8, u + H + c * 8);
+      }
     }
   }
 }
@@ -435,70 +433,42 @@ cudaError_t launch_attention(const __nv_bfloat16* qkv, int64_t batch, int S, int
 __global__ void fuse_concat_kernel(const float* __restrict__ X,
                                    const __nv_bfloat16* __restrict__ target, int S, int64_t M,
                                    int H, __nv_bfloat16* __restrict__ out) {
+  // grid (chunks of one block's S x H/8 work items, blocks): no 64-bit division
   const int hv = H / 8;
-  const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (idx >= M * hv) return;
-  const int64_t m = idx / hv;
-  const int h0 = static_cast<int>(idx % hv) * 8;
-  float x[8], xt[8];
-  load8(X + m * H + h0, x);
-  if (target) {
-    const uint4 w = __ldg(reinterpret_cast<const uint4*>(target + (m / S) * H + h0));
-    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= S * hv) return;
+  const int64_t nblk = M / S;
+  const int r = t / hv;
+  const int h0 = (t % hv) * 8;
+  for (int64_t blk = blockIdx.y; blk < nblk; blk += gridDim.y) {
+    const int64_t m = blk * S + r;
+    float x[8], xt[8];
+    load8(X + m * H + h0, x);
+    if (target) {
+      const uint4 w = __ldg(reinterpret_cast<const uint4*>(target + blk * H + h0));
+      const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      xt[2 * j] = x[2 * j] * __uint_as_float(ww[j] << 16);
-      xt[2 * j + 1] = x[2 * j + 1] * __uint_as_float(ww[j] & 0xffff0000u);
+      for (int j = 0; j < 4; ++j) {
+        xt[2 * j] = x[2 * j] * __uint_as_float(ww[j] << 16);
+        xt[2 * j + 1] = x[2 * j + 1] * __uint_as_float(ww[j] & 0xffff0000u);
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) xt[j] = 0.f;
     }
-  } else {
-#pragma unroll
-    for (int j = 0; j < 8; ++j) xt[j] = 0.f;
+    __nv_bfloat16* o = out + m * 4 * H;
+    store_split8(x, o + h0, o + 2 * H + h0);
+    store_split8(xt, o + H + h0, o + 3 * H + h0);
   }
-  __nv_bfloat16* o = out + m * 4 * H;
-  store_split8(x, o + h0, o + 2 * H + h0);
-  store_split8(xt, o + H + h0, o + 3 * H + h0);
 }
 
-// Target-state term of the fusion layer, one per block: c[b, n] = Wt[n, :] . t_b + bf[n]
-// with Wt the middle H columns of fuse_w [H, 3H]; exact bf16 products summed in f32.
-__global__ void fuse_tbias_kernel(const __nv_bfloat16* __restrict__ target,
-                                  const __nv_bfloat16* __restrict__ fuse_w,
-                                  const float* __restrict__ fuse_b, int H, float* __restrict__ c) {
-  constexpr int R = 8;  // rows per warp pass, loads in flight together
-  const int64_t b = blockIdx.x;
-  const int lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-  const __nv_bfloat16* t = target ? target + b * H : nullptr;
-  for (int n0 = (threadIdx.x >> 5) * R; n0 < H; n0 += nw * R) {
-    float acc[R];
-#pragma unroll
-    for (int r = 0; r < R; ++r) acc[r] = 0.f;
-    if (t)
-      for (int h = lane * 8; h < H; h += 256) {
-        const uint4 tv = __ldg(reinterpret_cast<const uint4*>(t + h));
-        const uint32_t tw[4] = {tv.x, tv.y, tv.z, tv.w};
-        uint4 wv[R];
-#pragma unroll
-        for (int r = 0; r < R; ++r)
-          wv[r] = n0 + r < H ? __ldg(reinterpret_cast<const uint4*>(fuse_w + int64_t(n0 + r) * 3 * H + H + h))
-                             : make_uint4(0, 0, 0, 0);
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-          const uint32_t aw[4] = {wv[r].x, wv[r].y, wv[r].z, wv[r].w};
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            acc[r] = fmaf(__uint_as_float(aw[j] << 16), __uint_as_float(tw[j] << 16), acc[r]);
-            acc[r] = fmaf(__uint_as_float(aw[j] & 0xffff0000u), __uint_as_float(tw[j] & 0xffff0000u),
-                          acc[r]);
-          }
-        }
-      }
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-#pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) acc[r] += __shfl_xor_sync(FULL_MASK, acc[r], o);
-      if (lane == 0 && n0 + r < H) c[b * H + n0 + r] = acc[r] + fuse_b[n0 + r];
-    }
-  }
+// out[r, :] = bias for every row (the per-block target terms when there is no target state)
+__global__ void rows_bias_kernel(const float* __restrict__ bias, int64_t rows, int N,
+                                 float* __restrict__ out) {
+  const int64_t n = rows * N;
+  for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < n;
+       i += int64_t(gridDim.x) * blockDim.x)
+    out[i] = bias[i % N];
 }
 
 // ------------------------------------------------------------------ launchers
@@ -507,9 +477,10 @@ cudaError_t launch_conf_hidden(const float* cand_logit, const float* lse, int64_
                                const float* w1, const float* b1, __nv_bfloat16* U,
                                cudaStream_t stream) {
   if (H % 8) return cudaErrorInvalidValue;
-  const int64_t rows_per_cta = 8;
-  const unsigned grid =
-      static_cast<unsigned>(std::min<int64_t>((M + rows_per_cta - 1) / rows_per_cta, 152 * 8));
+  if (K < 1 || K > 32 || M % K) return cudaErrorInvalidValue;
+  const int64_t slots_per_cta = 8;  // one warp per slot
+  const unsigned grid = static_cast<unsigned>(
+      std::min<int64_t>((M / K + slots_per_cta - 1) / slots_per_cta, 152 * 8));
   conf_hidden_kernel<<<grid, 256, 0, stream>>>(cand_logit, lse, M, K, H, w1, b1, U);
   note_launch();
   return cudaGetLastError();
@@ -525,11 +496,11 @@ cudaError_t launch_rmsnorm_split(const float* X, const float* gain, int64_t M, i
   return cudaGetLastError();
 }
 
-cudaError_t launch_fuse_tbias(const __nv_bfloat16* target, const __nv_bfloat16* fuse_w,
-                              const float* fuse_b, int64_t batch, int H, float* c,
-                              cudaStream_t stream) {
-  if (H % 8 || reinterpret_cast<uintptr_t>(target) % 16) return cudaErrorInvalidValue;
-  fuse_tbias_kernel<<<static_cast<unsigned>(batch), 256, 0, stream>>>(target, fuse_w, fuse_b, H, c);
+cudaError_t launch_rows_bias(const float* bias, int64_t rows, int N, float* out,
+                             cudaStream_t stream) {
+  const int64_t n = rows * N;
+  rows_bias_kernel<<<static_cast<unsigned>(std::min<int64_t>((n + 255) / 256, 152 * 8)), 256, 0,
+                     stream>>>(bias, rows, N, out);
   note_launch();
   return cudaGetLastError();
 }
@@ -537,8 +508,10 @@ cudaError_t launch_fuse_tbias(const __nv_bfloat16* target, const __nv_bfloat16* 
 cudaError_t launch_fuse_concat(const float* X, const __nv_bfloat16* target, int S, int64_t M,
                                int H, __nv_bfloat16* out, cudaStream_t stream) {
   if (H % 8) return cudaErrorInvalidValue;
-  const int64_t n = M * (H / 8);
-  fuse_concat_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, stream>>>(X, target, S, M, H, out);
+  if (S <= 0 || M % S) return cudaErrorInvalidValue;
+  const dim3 grid(static_cast<unsigned>((int64_t(S) * (H / 8) + 255) / 256),
+                  static_cast<unsigned>(std::min<int64_t>(M / S, 65535)));
+  fuse_concat_kernel<<<grid, 256, 0, stream>>>(X, target, S, M, H, out);
   note_launch();
   return cudaGetLastError();
 }

@@ -247,7 +247,8 @@ __device__ __forceinline__ void tc_epilogue_staged(const GemmArgs& g, const CUte
                                                    float (&v)[32]) {
   const float* bias = g.bias + n;
   if (g.bias_group > 0)  // per-block bias row (rows past M reuse the last one)
-    bias += (std::min<int64_t>(row0 + lane, g.M - 1) / g.bias_group) * g.N;
+    bias += (std::min<int64_t>(row0 + lane, g.M - 1) / g.bias_group) *
+            (g.bias_stride > 0 ? g.bias_stride : int64_t(g.N));
 #pragma unroll
   for (int j = 0; j < 32 && BIAS; j += 4) {
     const float4 b4 = __ldg(reinterpret_cast<const float4*>(bias + j));

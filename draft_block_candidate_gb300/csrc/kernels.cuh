@@ -20,10 +20,10 @@ cudaError_t k1_read_device_error(uint32_t* code);
 void set_last_error(const char* msg);
 
 // a4 scores + a5 walk (walk.cu)
-cudaError_t launch_pair_scores(const float* heads, const __nv_bfloat16* target,
-                               const __nv_bfloat16* Wa, const float* ba, int64_t batch, int B,
-                               int K, int E, int H, float sigma, float* scores, float* out_tap,
-                               float* in_tap, float* anchor_tap, cudaStream_t stream);
+cudaError_t launch_pair_scores(const float* heads, const float* anchor_raw, int64_t anchor_stride,
+                               int64_t batch, int B, int K, int E, float sigma, float* scores,
+                               float* out_tap, float* in_tap, float* anchor_tap,
+                               cudaStream_t stream);
 cudaError_t launch_viterbi(const float* scores, const int32_t* cand_id,
                            const int32_t* anchor_ids, int64_t batch, int B, int K,
                            int32_t* tokens, int32_t* choice, float* path, double* total,
@@ -46,8 +46,9 @@ struct GemmArgs {
   const __nv_bfloat16* W;  // [N, Kw]
   int64_t M;
   int N, Kw, Ka;
-  const float* bias;       // [N], or [M / bias_group, N] when bias_group > 0
+  const float* bias;       // [N], or one row per bias_group rows when bias_group > 0
   int64_t bias_group;      // rows sharing one bias row (0: one bias for all rows)
+  int64_t bias_stride;     // elements between grouped bias rows (0: N)
   float* out;              // EPI_F32 / EPI_RESID / EPI_NODE: [M, N] f32
   __nv_bfloat16* out_split;  // EPI_SPLIT*: [M, 2N]
   // EPI_NODE extras: X = acc + bias + E[cand] + slot_table[s-1] + rank_table[k] + hidden
@@ -78,9 +79,8 @@ cudaError_t launch_attention_tc(const __nv_bfloat16* qkv, int64_t batch, int S, 
                                 int heads, int B_max, const float* dist_bias,
                                 const float* same_bias, __nv_bfloat16* out, cudaStream_t stream);
 cudaError_t at_read_device_error(uint32_t* code);
-cudaError_t launch_fuse_tbias(const __nv_bfloat16* target, const __nv_bfloat16* fuse_w,
-                              const float* fuse_b, int64_t batch, int H, float* c,
-                              cudaStream_t stream);
+cudaError_t launch_rows_bias(const float* bias, int64_t rows, int N, float* out,
+                             cudaStream_t stream);
 cudaError_t launch_fuse_concat(const float* X, const __nv_bfloat16* target, int S, int64_t M,
                                int H, __nv_bfloat16* out, cudaStream_t stream);
 }  // namespace lilicorr

@@ -91,9 +91,10 @@ struct lilicorr_weights {
   // bf16 (tensor-core operands and the gathered embedding)
   // fuse_w is [Wh | Wt | Wht] ([H, 3H]); fuse_w2 = [Wh | Wht] ([H, 2H]) for the
   // contraction over [h, h*t]; the Wt t term is a per-block bias
-  const __nv_bfloat16 *embed, *conf_w2, *fuse_w, *fuse_w2, *heads_w, *anchor_w;
+  const __nv_bfloat16 *embed, *conf_w2, *fuse_w, *fuse_w2, *heads_w, *anchor_w, *tgt_w;
   // f32 (exact widening of the bf16 inputs)
-  const float *slot_table, *rank_table, *conf_w1, *conf_b1, *conf_b2, *fuse_b, *heads_b, *anchor_b;
+  const float *slot_table, *rank_table, *conf_w1, *conf_b1, *conf_b2, *fuse_b, *heads_b, *anchor_b,
+      *tgt_b;
   struct Layer {
     const __nv_bfloat16 *in_w, *out_w, *w1, *w2;
     const float *norm1, *in_b, *out_b, *dist, *same, *norm2, *b1, *b2;
@@ -170,7 +171,7 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // Workspace layout of one rerank call.
 struct WsPlan {
-  size_t k1, cand_id, cand_logit, lse, act1, X, qkv, ffh, heads, scores, fuse_c, total;
+  size_t k1, cand_id, cand_logit, lse, act1, X, qkv, ffh, heads, scores, tgt, total;
 };
 
 WsPlan ws_plan(const lilicorr_dims& d, int64_t batch, int B, int K, int esize) {
@@ -194,7 +195,7 @@ WsPlan ws_plan(const lilicorr_dims& d, int64_t batch, int B, int K, int esize) {
   p.ffh = take(size_t(M) * 2 * F * 2);
   p.heads = take(size_t(M) * 2 * E * 4);
   p.scores = take(size_t(rows) * K * K * 4);
-  p.fuse_c = take(size_t(batch) * H * 4);
+  p.tgt = take(size_t(batch) * (H + E) * 4);
   p.total = off;
   return p;
 }
@@ -332,6 +333,27 @@ lilicorr_status lilicorr_weights_create(const lilicorr_dims* dims, const lilicor
     }
     off["heads.b"] = ob;
   }
+  // the two per-block terms of the target state are one contraction:
+  // [Wt; Wa] [H + E, H] (Wt = the middle H columns of fuse.w), b = [bf; ba]
+  {
+    const int64_t H = dims->hidden, E = dims->d_e;
+    const size_t o = align256(img.size());
+    img.resize(o + size_t((H + E) * H) * 2);
+    const uint8_t* fw = static_cast<const uint8_t*>(given["fuse.w"]->host_data);
+    for (int64_t n = 0; n < H; ++n)
+      std::memcpy(img.data() + o + size_t(n * H) * 2, fw + size_t(n * 3 * H + H) * 2, size_t(H) * 2);
+    std::memcpy(img.data() + o + size_t(H * H) * 2, given["head_anchor.w"]->host_data,
+                size_t(E * H) * 2);
+    off["tgt.w"] = o;
+    const size_t ob = align256(img.size());
+    img.resize(ob + size_t(H + E) * 4);
+    float* d = reinterpret_cast<float*>(img.data() + ob);
+    const uint16_t* fb = static_cast<const uint16_t*>(given["fuse.b"]->host_data);
+    const uint16_t* ab = static_cast<const uint16_t*>(given["head_anchor.b"]->host_data);
+    for (int64_t n = 0; n < H; ++n) d[n] = bf16_to_f32(fb[n]);
+    for (int64_t e = 0; e < E; ++e) d[H + e] = bf16_to_f32(ab[e]);
+    off["tgt.b"] = ob;
+  }
 
   int prev = 0;
   LC_CUDA(cudaGetDevice(&prev), "cudaGetDevice");
@@ -361,6 +383,7 @@ lilicorr_status lilicorr_weights_create(const lilicorr_dims* dims, const lilicor
   w->fuse_w2 = bf("fuse.w2");
   w->heads_w = bf("heads.w");
   w->anchor_w = bf("head_anchor.w");
+  w->tgt_w = bf("tgt.w");
   w->slot_table = f32("slot_table");
   w->rank_table = f32("rank_table");
   w->conf_w1 = f32("conf.w1");
@@ -369,6 +392,7 @@ lilicorr_status lilicorr_weights_create(const lilicorr_dims* dims, const lilicor
   w->fuse_b = f32("fuse.b");
   w->heads_b = f32("heads.b");
   w->anchor_b = f32("head_anchor.b");
+  w->tgt_b = f32("tgt.b");
   for (int l = 0; l < dims->layers; ++l) {
     const std::string p = "layers." + std::to_string(l) + ".";
     lilicorr_weights::Layer L;
@@ -612,16 +636,24 @@ lilicorr_status lilicorr_rerank(const lilicorr_weights* w, const void* logits,
     LC_CUDA(cudaMemcpyAsync(tp.hidden, X, size_t(M) * H * 4, cudaMemcpyDeviceToDevice, stream),
             "hidden tap");
   // a4: fusion and heads
-  float* fuse_c = reinterpret_cast<float*>(ws + pl.fuse_c);
-  LC_CUDA(launch_fuse_tbias(target, w->fuse_w, w->fuse_b, batch, H, fuse_c, stream),
-          "fusion target term");
+  // per-block target terms [Wt t + bf | Wa t + ba], one row per block
+  float* tgt = reinterpret_cast<float*>(ws + pl.tgt);
+  const int HE = static_cast<int>(H + E);
+  if (target) {
+    GemmArgs g{};
+    g.A = target; g.W = w->tgt_w; g.M = batch; g.N = HE; g.Kw = H; g.Ka = H; g.bias = w->tgt_b;
+    g.out = tgt;
+    LC_CUDA(launch_gemm(EPI_F32, g, stream), "target terms gemm");
+  } else {
+    LC_CUDA(launch_rows_bias(w->tgt_b, batch, HE, tgt, stream), "target terms");
+  }
   LC_CUDA(launch_fuse_concat(X, target, S, M, H, qkv, stream), "fusion input");
   MARK(T_FUSECAT);
   {
     // SiLU(Wh h + Wht (h*t) + [Wt t + bf]_block): A = [h, h*t] split, bias per block
     GemmArgs g{};
-    g.A = qkv; g.W = w->fuse_w2; g.M = M; g.N = H; g.Kw = 2 * H; g.Ka = 4 * H; g.bias = fuse_c;
-    g.bias_group = S; g.out_split = act1;
+    g.A = qkv; g.W = w->fuse_w2; g.M = M; g.N = H; g.Kw = 2 * H; g.Ka = 4 * H; g.bias = tgt;
+    g.bias_group = S; g.bias_stride = HE; g.out_split = act1;
     LC_CUDA(launch_gemm(EPI_SPLIT_SILU, g, stream), "fusion gemm");
     MARK(T_FUSE);
     g = GemmArgs{};
@@ -631,8 +663,8 @@ lilicorr_status lilicorr_rerank(const lilicorr_weights* w, const void* logits,
     MARK(T_HEADS);
   }
   // a4 scores (with the anchor head) + a5 walk
-  LC_CUDA(launch_pair_scores(heads, target, w->anchor_w, w->anchor_b, batch, B, K, E, H, d.sigma,
-                             scores, tp.out_vec, tp.in_vec, tp.anchor_vec, stream),
+  LC_CUDA(launch_pair_scores(heads, tgt + H, HE, batch, B, K, E, d.sigma, scores, tp.out_vec,
+                             tp.in_vec, tp.anchor_vec, stream),
           "pair scores");
   MARK(T_SCORES);
   LC_CUDA(launch_greedy_walk(scores, cand_id, anchor_ids, batch, B, K, tokens, tp.choice,

@@ -14,121 +14,156 @@
 
 namespace lilicorr {
 
-// One CTA per (block b, pair p).  heads [batch*S, 2E] holds the raw out | in head
-// outputs.  The p == 0 CTA of a block also evaluates the anchor head on the block's
-// target state (anchor_raw = Wa t + ba, f32 accumulation of exact bf16 products).
-// Vectors are normalised here (nrm(v) = v / max(||v||, 1e-12)) and dotted in f32.
-__global__ void __launch_bounds__(256) pair_scores_kernel(
-    const float* __restrict__ heads, const __nv_bfloat16* __restrict__ target,
-    const __nv_bfloat16* __restrict__ Wa, const float* __restrict__ ba, int B, int K, int E, int H,
-    float sigma, float* __restrict__ scores, float* __restrict__ out_tap,
+// One warp per (block b, pair p); a CTA holds up to four pairs of one block.  heads
+// [batch*S, 2E] holds the raw out | in head outputs; anchor_raw (row stride anchor_stride)
+// the block's raw anchor head output Wa t + ba.  The warp copies the raw out rows of slot
+// p (the anchor for p == 0) and the in rows of slot p+1 to shared memory with 16-byte
+// asynchronous copies, takes every row's inverse norm 1 / max(||v||, 1e-12) there, and
+// forms phi = sigma * (o . i) * inv(o) * inv(i), the cosine of the normalised vectors up
+// to f32 rounding.  Dot products are register-blocked: per 16 x 16 tile of outputs a lane
+// owns a 2 x 4 block over the whole E axis, so each shared operand is read once per block.
+constexpr int PS_MAX_WARPS = 4;
+
+__device__ __forceinline__ void cp_async16(void* dst_smem, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst_smem)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+__host__ __device__ inline size_t ps_warp_floats(int K, int E) {
+  const int K16 = (K + 15) & ~15;
+  return size_t(2) * K16 * (E + 4) + 2 * K16;
+}
+
+__global__ void __launch_bounds__(32 * PS_MAX_WARPS) pair_scores_kernel(
+    const float* __restrict__ heads, const float* __restrict__ anchor_raw, int64_t anchor_stride,
+    int B, int K, int E, float sigma, float* __restrict__ scores, float* __restrict__ out_tap,
     float* __restrict__ in_tap, float* __restrict__ anchor_tap) {
   extern __shared__ __align__(16) float ps_smem[];
-  const int E1 = E + 4;  // row pitch: 16-byte rows, rows of a warp on distinct banks
-  float* so = ps_smem;            // [K][E1] out vectors of slot p (or o_0 in row 0)
-  float* si = ps_smem + K * E1;   // [K][E1] in vectors of slot p+1
-  const int p = blockIdx.x, b = blockIdx.y;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int p = blockIdx.x * (blockDim.x >> 5) + warp;
+  const int b = blockIdx.y;
+  if (p >= B - 1) return;  // warp-uniform; no CTA-wide barrier follows
+  const int E1 = E + 4;  // row pitch: 16-byte rows on shifted banks
+  const int K16 = (K + 15) & ~15;
+  float* so = ps_smem + size_t(warp) * ps_warp_floats(K, E);  // [K16][E1] out rows / anchor
+  float* si = so + K16 * E1;                                   // [K16][E1] in rows of slot p+1
+  float* inv = si + K16 * E1;                                  // [2*K16] inverse norms
   const int S = (B - 1) * K;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
   const int64_t blk_row0 = int64_t(b) * S;
+  const int E4 = E >> 2;  // float4 columns (E % 4 == 0)
+  const int n_out = (p == 0) ? 1 : K;
 
-  if (p == 0) {
-    // raw anchor head output for this block, into row 0 of so
-    const __nv_bfloat16* t = target ? target + int64_t(b) * H : nullptr;
-    for (int e = warp; e < E; e += nw) {
-      float acc = 0.f;
-      if (t)
-        for (int h = lane * 8; h < H; h += 256) {
-          const uint4 wa = __ldg(reinterpret_cast<const uint4*>(Wa + int64_t(e) * H + h));
-          const uint4 tv = __ldg(reinterpret_cast<const uint4*>(t + h));
-          const uint32_t aw[4] = {wa.x, wa.y, wa.z, wa.w}, tw[4] = {tv.x, tv.y, tv.z, tv.w};
+  // rows 0..K16-1: out rows, K16..2*K16-1: in rows; rows past K (and past the anchor) zero
+  for (int r = 0; r < 2 * K16; ++r) {
+    const bool is_in = r >= K16;
+    const int k = is_in ? r - K16 : r;
+    float* dst = (is_in ? si : so) + k * E1;
+    const float* src = nullptr;
+    if (is_in) {
+      if (k < K) src = heads + (blk_row0 + int64_t(p) * K + k) * (2 * E) + E;
+    } else if (k < n_out) {
+      src = p == 0 ? anchor_raw + int64_t(b) * anchor_stride
+                   : heads + (blk_row0 + int64_t(p - 1) * K + k) * (2 * E);
+    }
+    for (int c = lane; c < E4; c += 32) {
+      if (src)
+        cp_async16(dst + 4 * c, src + 4 * c);
+      else
+        reinterpret_cast<float4*>(dst)[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+  cp_async_wait_all();
+  __syncwarp();
+
+  // inverse norms: lane per row
+  for (int r = lane; r < 2 * K16; r += 32) {
+    const float* v = r >= K16 ? si + (r - K16) * E1 : so + r * E1;
+    float ss = 0.f;
+    for (int c = 0; c < E4; ++c) {
+      const float4 x = reinterpret_cast<const float4*>(v)[c];
+      ss = fmaf(x.x, x.x, ss);
+      ss = fmaf(x.y, x.y, ss);
+      ss = fmaf(x.z, x.z, ss);
+      ss = fmaf(x.w, x.w, ss);
+    }
+    inv[r] = 1.0f / fmaxf(sqrtf(ss), 1e-12f);
+  }
+  __syncwarp();
+
+  // taps of the normalised vectors (checking only)
+  if (out_tap || in_tap || anchor_tap) {
+    for (int r = 0; r < n_out + K; ++r) {
+      const bool is_in = r >= n_out;
+      const int k = is_in ? r - n_out : r;
+      float* tap;
+      if (is_in)
+        tap = in_tap ? in_tap + (blk_row0 + int64_t(p) * K + k) * E : nullptr;
+      else if (p == 0)
+        tap = anchor_tap ? anchor_tap + int64_t(b) * E : nullptr;
+      else
+        tap = out_tap ? out_tap + (blk_row0 + int64_t(p - 1) * K + k) * E : nullptr;
+      if (!tap) continue;
+      const float* v = (is_in ? si : so) + k * E1;
+      const float sc = inv[is_in ? K16 + k : k];
+      for (int e = lane; e < E; e += 32) tap[e] = v[e] * sc;
+    }
+    if (p == 0 && out_tap) {  // slot B-1's out rows are used by no pair
+      for (int k = 0; k < K; ++k) {
+        const int64_t row = blk_row0 + int64_t(B - 2) * K + k;
+        const float* src = heads + row * (2 * E);
+        float ss = 0.f;
+        for (int e = lane; e < E; e += 32) ss = fmaf(src[e], src[e], ss);
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) ss += __shfl_xor_sync(FULL_MASK, ss, o);
+        const float sc = 1.0f / fmaxf(sqrtf(ss), 1e-12f);
+        for (int e = lane; e < E; e += 32) out_tap[row * E + e] = src[e] * sc;
+      }
+    }
+  }
+
+  // K x K dot products, 16 x 16 tiles; lane = (row pair kb, column quad cb) of the tile
+  float* dst_scores = scores + (int64_t(b) * (B - 1) + p) * K * K;
+  const int kb = lane >> 2, cb = lane & 3;
+  for (int t0 = 0; t0 < K; t0 += 16) {
+    for (int u0 = 0; u0 < K; u0 += 16) {
+      const int k0 = t0 + 2 * kb, kk0 = u0 + 4 * cb;
+      const float* a0 = so + k0 * E1;
+      const float* c0 = si + kk0 * E1;
+      float acc[2][4];
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+#pragma unroll 2
+      for (int c = 0; c < E4; ++c) {
+        float4 a[2], cv[4];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) a[i] = reinterpret_cast<const float4*>(a0 + i * E1)[c];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) cv[j] = reinterpret_cast<const float4*>(c0 + j * E1)[c];
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            acc = fmaf(__uint_as_float(aw[j] << 16), __uint_as_float(tw[j] << 16), acc);
-            acc = fmaf(__uint_as_float(aw[j] & 0xffff0000u), __uint_as_float(tw[j] & 0xffff0000u),
-                       acc);
+            acc[i][j] = fmaf(a[i].x, cv[j].x, acc[i][j]);
+            acc[i][j] = fmaf(a[i].y, cv[j].y, acc[i][j]);
+            acc[i][j] = fmaf(a[i].z, cv[j].z, acc[i][j]);
+            acc[i][j] = fmaf(a[i].w, cv[j].w, acc[i][j]);
           }
+      }
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int k = k0 + i, kk = kk0 + j;
+          if (k < K && kk < K)
+            dst_scores[k * K + kk] =
+                (p == 0 && k > 0) ? -INFINITY : sigma * acc[i][j] * inv[k] * inv[K16 + kk];
         }
-#pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) acc += __shfl_xor_sync(FULL_MASK, acc, o);
-      if (lane == 0) so[e] = acc + ba[e];
     }
-    __syncthreads();
-  }
-
-  // rows to normalise: out rows of slot p (p >= 1) or the anchor (p == 0); in rows of
-  // slot p+1; the p == 0 CTA also normalises slot B-1's out rows for the tap.
-  const int n_out = (p == 0) ? 1 : K;
-  for (int r = warp; r < n_out + K; r += nw) {
-    const float* src;
-    float* dst;
-    float* tap = nullptr;
-    if (r < n_out) {
-      if (p == 0) {
-        src = so;  // normalised in place
-        tap = anchor_tap ? anchor_tap + int64_t(b) * E : nullptr;
-      } else {
-        const int64_t row = blk_row0 + int64_t(p - 1) * K + r;
-        src = heads + row * (2 * E);
-        tap = out_tap ? out_tap + row * E : nullptr;
-      }
-      dst = so + r * E1;
-    } else {
-      const int k = r - n_out;
-      const int64_t row = blk_row0 + int64_t(p) * K + k;
-      src = heads + row * (2 * E) + E;
-      tap = in_tap ? in_tap + row * E : nullptr;
-      dst = si + k * E1;
-    }
-    float ss = 0.f;
-    for (int e = lane; e < E; e += 32) {
-      const float v = src[e];
-      ss = fmaf(v, v, ss);
-    }
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) ss += __shfl_xor_sync(FULL_MASK, ss, o);
-    const float inv = 1.0f / fmaxf(sqrtf(ss), 1e-12f);
-    for (int e = lane; e < E; e += 32) {
-      const float v = src[e] * inv;
-      dst[e] = v;
-      if (tap) tap[e] = v;
-    }
-  }
-  if (p == 0 && out_tap) {
-    for (int k = warp; k < K; k += nw) {
-      const int64_t row = blk_row0 + int64_t(B - 2) * K + k;
-      const float* src = heads + row * (2 * E);
-      float ss = 0.f;
-      for (int e = lane; e < E; e += 32) ss = fmaf(src[e], src[e], ss);
-#pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) ss += __shfl_xor_sync(FULL_MASK, ss, o);
-      const float inv = 1.0f / fmaxf(sqrtf(ss), 1e-12f);
-      for (int e = lane; e < E; e += 32) out_tap[row * E + e] = src[e] * inv;
-    }
-  }
-  __syncthreads();
-
-  float* dst = scores + (int64_t(b) * (B - 1) + p) * K * K;
-  for (int t = tid; t < K * K; t += blockDim.x) {
-    const int k = t / K, kk = t % K;
-    float v;
-    if (p == 0 && k > 0) {
-      v = -INFINITY;
-    } else {
-      const float* a = so + k * E1;
-      const float* c = si + kk * E1;
-      float acc = 0.f;
-      for (int e = 0; e < E; e += 4) {  // E % 4 == 0
-        const float4 a4 = *reinterpret_cast<const float4*>(a + e);
-        const float4 c4 = *reinterpret_cast<const float4*>(c + e);
-        acc = fmaf(a4.x, c4.x, acc);
-        acc = fmaf(a4.y, c4.y, acc);
-        acc = fmaf(a4.z, c4.z, acc);
-        acc = fmaf(a4.w, c4.w, acc);
-      }
-      v = sigma * acc;
-    }
-    dst[t] = v;
   }
 }
 
@@ -346,23 +381,26 @@ __global__ void __launch_bounds__(32) sample_walk_kernel(
   }
 }
 
-cudaError_t launch_pair_scores(const float* heads, const __nv_bfloat16* target,
-                               const __nv_bfloat16* Wa, const float* ba, int64_t batch, int B,
-                               int K, int E, int H, float sigma, float* scores, float* out_tap,
-                               float* in_tap, float* anchor_tap, cudaStream_t stream) {
-  if (H % 8 || (reinterpret_cast<uintptr_t>(Wa) % 16) || (reinterpret_cast<uintptr_t>(target) % 16))
+cudaError_t launch_pair_scores(const float* heads, const float* anchor_raw, int64_t anchor_stride,
+                               int64_t batch, int B, int K, int E, float sigma, float* scores,
+                               float* out_tap, float* in_tap, float* anchor_tap,
+                               cudaStream_t stream) {
+  if (E % 4 || E > 256 || K < 1 || K > 32 || B < 2 || anchor_stride % 4 ||
+      (reinterpret_cast<uintptr_t>(heads) % 16) || (reinterpret_cast<uintptr_t>(anchor_raw) % 16))
     return cudaErrorInvalidValue;
-  if (E % 4) return cudaErrorInvalidValue;
-  const size_t smem = size_t(2) * K * (E + 4) * sizeof(float);
+  const size_t per_warp = ps_warp_floats(K, E) * sizeof(float);
+  int pw = PS_MAX_WARPS;
+  while (pw > 1 && pw * per_warp > size_t(200) * 1024) --pw;
   static bool attr = false;
   if (!attr) {
     cudaFuncSetAttribute(pair_scores_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         2 * 32 * 260 * 4);
+                         static_cast<int>(size_t(200) * 1024));
     attr = true;
   }
-  const dim3 grid(B - 1, static_cast<unsigned>(batch));
-  pair_scores_kernel<<<grid, 256, smem, stream>>>(heads, target, Wa, ba, B, K, E, H, sigma, scores,
-                                                  out_tap, in_tap, anchor_tap);
+  const dim3 grid(static_cast<unsigned>((B - 1 + pw - 1) / pw), static_cast<unsigned>(batch));
+  pair_scores_kernel<<<grid, 32 * pw, pw * per_warp, stream>>>(heads, anchor_raw, anchor_stride, B,
+                                                                K, E, sigma, scores, out_tap,
+                                                                in_tap, anchor_tap);
   note_launch();
   return cudaGetLastError();
 }
