@@ -20,8 +20,8 @@ namespace lilicorr {
 // p (the anchor for p == 0) and the in rows of slot p+1 to shared memory with 16-byte
 // asynchronous copies, takes every row's inverse norm 1 / max(||v||, 1e-12) there, and
 // forms phi = sigma * (o . i) * inv(o) * inv(i), the cosine of the normalised vectors up
-// to f32 rounding.  Dot products are register-blocked: per 16 x 16 tile of outputs a lane
-// owns a 2 x 4 block over the whole E axis, so each shared operand is read once per block.
+// to f32 rounding.  The dot products run on the tensor cores (warp-level TF32 MMA with
+// split operands, f32-level accuracy), reading each shared operand once.
 constexpr int PS_MAX_WARPS = 4;
 
 __device__ __forceinline__ void cp_async16(void* dst_smem, const void* src) {
@@ -32,12 +32,29 @@ __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
+// x = hi + lo with hi, lo TF32 values (round to nearest, ties away from zero).
+__device__ __forceinline__ void tf32_split(float x, uint32_t& hi, uint32_t& lo) {
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(hi) : "f"(x));
+  const float r = x - __uint_as_float(hi);
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(lo) : "f"(r));
+}
+
+// d += a . b for one m16n8k8 TF32 tile (f32 accumulate).
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4],
+                                         const uint32_t (&b)[2]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
 __host__ __device__ inline size_t ps_warp_floats(int K, int E) {
   const int K16 = (K + 15) & ~15;
   return size_t(2) * K16 * (E + 4) + 2 * K16;
 }
 
-__global__ void __launch_bounds__(32 * PS_MAX_WARPS) pair_scores_kernel(
+__global__ void __launch_bounds__(32 * PS_MAX_WARPS, 3) pair_scores_kernel(
     const float* __restrict__ heads, const float* __restrict__ anchor_raw, int64_t anchor_stride,
     int B, int K, int E, float sigma, float* __restrict__ scores, float* __restrict__ out_tap,
     float* __restrict__ in_tap, float* __restrict__ anchor_tap) {
@@ -81,15 +98,16 @@ __global__ void __launch_bounds__(32 * PS_MAX_WARPS) pair_scores_kernel(
   // inverse norms: lane per row
   for (int r = lane; r < 2 * K16; r += 32) {
     const float* v = r >= K16 ? si + (r - K16) * E1 : so + r * E1;
-    float ss = 0.f;
+    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;  // independent chains
+#pragma unroll 8
     for (int c = 0; c < E4; ++c) {
       const float4 x = reinterpret_cast<const float4*>(v)[c];
-      ss = fmaf(x.x, x.x, ss);
-      ss = fmaf(x.y, x.y, ss);
-      ss = fmaf(x.z, x.z, ss);
-      ss = fmaf(x.w, x.w, ss);
+      s0 = fmaf(x.x, x.x, s0);
+      s1 = fmaf(x.y, x.y, s1);
+      s2 = fmaf(x.z, x.z, s2);
+      s3 = fmaf(x.w, x.w, s3);
     }
-    inv[r] = 1.0f / fmaxf(sqrtf(ss), 1e-12f);
+    inv[r] = 1.0f / fmaxf(sqrtf((s0 + s1) + (s2 + s3)), 1e-12f);
   }
   __syncwarp();
 
@@ -124,44 +142,51 @@ __global__ void __launch_bounds__(32 * PS_MAX_WARPS) pair_scores_kernel(
     }
   }
 
-  // K x K dot products, 16 x 16 tiles; lane = (row pair kb, column quad cb) of the tile
+  // K x K dot products on the tensor cores, 16 x 16 tiles: mma.sync m16n8k8 in TF32 with
+  // each operand split hi + lo (hi = tf32(x), lo = tf32(x - hi)) and the three products
+  // hi.hi + hi.lo + lo.hi accumulated in f32 (about 21 significant bits per product, the
+  // dropped lo.lo term below 2^-22 relative).  Fragments: g = lane / 4 picks the row
+  // (A) or column (B), t = lane % 4 the K index.
   float* dst_scores = scores + (int64_t(b) * (B - 1) + p) * K * K;
-  const int kb = lane >> 2, cb = lane & 3;
+  const int g = lane >> 2, t = lane & 3;
   for (int t0 = 0; t0 < K; t0 += 16) {
     for (int u0 = 0; u0 < K; u0 += 16) {
-      const int k0 = t0 + 2 * kb, kk0 = u0 + 4 * cb;
-      const float* a0 = so + k0 * E1;
-      const float* c0 = si + kk0 * E1;
+      const float* A0 = so + (t0 + g) * E1;
+      const float* A1 = so + (t0 + g + 8) * E1;
+      const float* B0 = si + (u0 + g) * E1;
+      const float* B1 = si + (u0 + 8 + g) * E1;
       float acc[2][4];
 #pragma unroll
-      for (int i = 0; i < 2; ++i)
+      for (int j = 0; j < 2; ++j)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-#pragma unroll 2
-      for (int c = 0; c < E4; ++c) {
-        float4 a[2], cv[4];
+        for (int i = 0; i < 4; ++i) acc[j][i] = 0.f;
+#pragma unroll 4
+      for (int e = t; e < E; e += 8) {
+        uint32_t ah[4], al[4], bh[2][2], bl[2][2];
+        tf32_split(A0[e], ah[0], al[0]);
+        tf32_split(A1[e], ah[1], al[1]);
+        tf32_split(A0[e + 4], ah[2], al[2]);
+        tf32_split(A1[e + 4], ah[3], al[3]);
+        tf32_split(B0[e], bh[0][0], bl[0][0]);
+        tf32_split(B0[e + 4], bh[0][1], bl[0][1]);
+        tf32_split(B1[e], bh[1][0], bl[1][0]);
+        tf32_split(B1[e + 4], bh[1][1], bl[1][1]);
 #pragma unroll
-        for (int i = 0; i < 2; ++i) a[i] = reinterpret_cast<const float4*>(a0 + i * E1)[c];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) cv[j] = reinterpret_cast<const float4*>(c0 + j * E1)[c];
-#pragma unroll
-        for (int i = 0; i < 2; ++i)
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            acc[i][j] = fmaf(a[i].x, cv[j].x, acc[i][j]);
-            acc[i][j] = fmaf(a[i].y, cv[j].y, acc[i][j]);
-            acc[i][j] = fmaf(a[i].z, cv[j].z, acc[i][j]);
-            acc[i][j] = fmaf(a[i].w, cv[j].w, acc[i][j]);
-          }
+        for (int j = 0; j < 2; ++j) {
+          mma_tf32(acc[j], al, bh[j]);
+          mma_tf32(acc[j], ah, bl[j]);
+          mma_tf32(acc[j], ah, bh[j]);
+        }
       }
+      // acc[j] = C[g][2t], C[g][2t+1], C[g+8][2t], C[g+8][2t+1] of column block j
 #pragma unroll
-      for (int i = 0; i < 2; ++i)
+      for (int j = 0; j < 2; ++j)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int k = k0 + i, kk = kk0 + j;
+        for (int i = 0; i < 4; ++i) {
+          const int k = t0 + g + (i >= 2 ? 8 : 0), kk = u0 + 8 * j + 2 * t + (i & 1);
           if (k < K && kk < K)
             dst_scores[k * K + kk] =
-                (p == 0 && k > 0) ? -INFINITY : sigma * acc[i][j] * inv[k] * inv[K16 + kk];
+                (p == 0 && k > 0) ? -INFINITY : sigma * acc[j][i] * inv[k] * inv[K16 + kk];
         }
     }
   }
@@ -182,25 +207,11 @@ __global__ void __launch_bounds__(32) greedy_walk_kernel(
   const int n = (B - 1) * K * K;
   const float* src = scores + b * n;
   if (staged) {
-    // independent 16-byte loads, eight in flight per lane (n = (B-1) K^2 is a multiple of
-    // 4 when K is even; an odd K takes the scalar loop)
-    if ((K & 1) == 0) {
-      const float4* s4 = reinterpret_cast<const float4*>(src);
-      float4* d4 = reinterpret_cast<float4*>(gw_smem);
-      const int n4 = n >> 2;
-      for (int i0 = 0; i0 < n4; i0 += 256) {
-        float4 t[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int i = i0 + j * 32 + lane;
-          t[j] = i < n4 ? __ldg(s4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int i = i0 + j * 32 + lane;
-          if (i < n4) d4[i] = t[j];
-        }
-      }
+    // every 16-byte copy of the block's scores in flight at once (n = (B-1) K^2 is a
+    // multiple of 4 when K is even; an odd K or an unaligned array takes the scalar loop)
+    if ((K & 1) == 0 && (reinterpret_cast<uintptr_t>(scores) & 15) == 0) {
+      for (int i = lane; i < (n >> 2); i += 32) cp_async16(gw_smem + 4 * i, src + 4 * i);
+      cp_async_wait_all();
     } else {
       for (int i = lane; i < n; i += 32) gw_smem[i] = __ldg(src + i);
     }
@@ -212,17 +223,12 @@ __global__ void __launch_bounds__(32) greedy_walk_kernel(
   for (int p = 0; p < B - 1; ++p) {
     const int64_t pr = b * (B - 1) + p;
     const float* row = sc + (p * K + prev) * K;
-    float v = lane < K ? row[lane] : -INFINITY;
-    int idx = lane < K ? lane : INT_MAX;
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) {
-      const float ov = __shfl_xor_sync(FULL_MASK, v, o);
-      const int oi = __shfl_xor_sync(FULL_MASK, idx, o);
-      if (ov > v || (ov == v && oi < idx)) {
-        v = ov;
-        idx = oi;
-      }
-    }
+    // argmax as one warp max over ordered keys (-0.0 folded into +0.0 so that equal
+    // values tie), then the lowest lane holding it
+    const int key = lane < K ? float_key(row[lane] + 0.0f) : INT_MIN;
+    const int kmax = __reduce_max_sync(FULL_MASK, key);
+    const int idx = __ffs(__ballot_sync(FULL_MASK, key == kmax)) - 1;
+    const float v = key_float(kmax);
     if (lane == 0) {
       if (choice) choice[pr] = idx;
       if (path) path[pr] = v;
