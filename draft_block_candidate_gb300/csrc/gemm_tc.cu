@@ -41,11 +41,12 @@ constexpr int TC_A_BYTES = TC_BM * TC_BK * 2;
 constexpr int TC_B_BYTES = TC_BN * TC_BK * 2;
 constexpr int TC_STG_BYTES = 4096;  // one 32 x 32 output chunk (f32, or bf16 hi + lo)
 // Shared memory of a configuration: operand ring of ST stages + NB epilogue staging
-// buffers per warp.  Two fit in 227 KB: 4 stages with 1 buffer (the default: more bytes
-// in flight for the operand stream) or 3 stages with 2 (for SiLU epilogues of short K,
-// where the epilogue, not the operand stream, sets the pace).
-__host__ __device__ constexpr int tc_smem(int st, int nb) {
-  return st * (TC_A_BYTES + TC_B_BYTES) + TC_EPI_WARPS * nb * TC_STG_BYTES + 1024;
+// buffers per warp.  A stage holds one 64-wide K block of A and of W, or, for a split
+// operand (pair), the A_hi and A_lo blocks that share one W block.  Configurations in
+// use: 4 plain stages or 3 paired stages, with 1 staging buffer per epilogue warp.
+__host__ __device__ constexpr int tc_smem(int st, int nb, bool pair) {
+  return st * ((pair ? 2 : 1) * TC_A_BYTES + TC_B_BYTES) + TC_EPI_WARPS * nb * TC_STG_BYTES +
+         1024;
 }
 constexpr uint32_t TC_TMEM_COLS = 2 * TC_BN;  // two accumulator buffers
 
@@ -309,22 +310,24 @@ __device__ __forceinline__ void tc_epilogue_staged(const GemmArgs& g, const CUte
 
 // ------------------------------------------------------------------ kernel
 
-template <int EPI, int TC_STAGES, int TC_STG_BUFS>
+template <int EPI, int TC_STAGES, int TC_STG_BUFS, bool PAIR>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const GemmArgs g) {
   extern __shared__ uint8_t tc_smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sA = smem;
-  uint8_t* sB = smem + TC_STAGES * TC_A_BYTES;
-  uint8_t* sStage = smem + TC_STAGES * (TC_A_BYTES + TC_B_BYTES);  // epilogue staging
+  constexpr int AST = PAIR ? 2 * TC_A_BYTES : TC_A_BYTES;  // A bytes of a stage
+  uint8_t* sA = smem;                                       // stage s at sA + s * AST
+  uint8_t* sB = smem + TC_STAGES * AST;
+  uint8_t* sStage = sB + TC_STAGES * TC_B_BYTES;  // epilogue staging
   __shared__ __align__(8) uint64_t full_bar[TC_STAGES], empty_bar[TC_STAGES];
   __shared__ __align__(8) uint64_t acc_full[2], acc_empty[2];
   __shared__ uint32_t s_tmem;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int KB = g.Ka / TC_BK;
+  // ring steps per tile: 64-wide K blocks of A, or of W when A_hi / A_lo share a stage
+  const int KB = (PAIR ? g.Kw : g.Ka) / TC_BK;
   const int NT = (g.N + TC_BN - 1) / TC_BN;
   const int MT = static_cast<int>((g.M + TC_BM - 1) / TC_BM);
   const int ntiles = NT * MT;
@@ -358,9 +361,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(&full_bar[s], TC_A_BYTES + TC_B_BYTES);
-        tma_load_2d(sA + s * TC_A_BYTES, &tmA, kb * TC_BK, m0, &full_bar[s]);
-        tma_load_2d(sB + s * TC_B_BYTES, &tmB, (kb * TC_BK) % g.Kw, n0, &full_bar[s]);
+        mbar_arrive_expect_tx(&full_bar[s], AST + TC_B_BYTES);
+        if constexpr (PAIR) {
+          tma_load_2d(sA + s * AST, &tmA, kb * TC_BK, m0, &full_bar[s]);
+          tma_load_2d(sA + s * AST + TC_A_BYTES, &tmA, g.Kw + kb * TC_BK, m0, &full_bar[s]);
+          tma_load_2d(sB + s * TC_B_BYTES, &tmB, kb * TC_BK, n0, &full_bar[s]);
+        } else {
+          tma_load_2d(sA + s * AST, &tmA, kb * TC_BK, m0, &full_bar[s]);
+          tma_load_2d(sB + s * TC_B_BYTES, &tmB, (kb * TC_BK) % g.Kw, n0, &full_bar[s]);
+        }
       }
     }
   } else if (warp == 1 && lane == 0) {
@@ -386,8 +395,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < TC_BK / 16; ++kk)
-          umma_bf16(acc, sw128_desc(sA + s * TC_A_BYTES + kk * 32),
+          umma_bf16(acc, sw128_desc(sA + s * AST + kk * 32),
                     sw128_desc(sB + s * TC_B_BYTES + kk * 32), idesc, (kb | kk) != 0);
+        if constexpr (PAIR) {  // A_lo against the same W block
+#pragma unroll
+          for (int kk = 0; kk < TC_BK / 16; ++kk)
+            umma_bf16(acc, sw128_desc(sA + s * AST + TC_A_BYTES + kk * 32),
+                      sw128_desc(sB + s * TC_B_BYTES + kk * 32), idesc, 1u);
+        }
         umma_commit(&empty_bar[s]);
       }
       umma_commit(&acc_full[buf]);
@@ -515,14 +530,22 @@ cudaError_t launch_gemm(int epi, const GemmArgs& g, cudaStream_t stream) {
         !make_tmap_out(&tc, g.out, uint64_t(g.M), uint64_t(g.N), true))
       return cudaErrorInvalidValue;
   }
+  // A split operand (Ka = 2 Kw) runs paired stages: A_hi and A_lo share one W block
+  const bool pair = g.Ka == 2 * g.Kw;
+  constexpr int sp = tc_smem(3, 1, true), sn = tc_smem(4, 1, false);
   static bool attr = false;
   if (!attr) {
-    cudaFuncSetAttribute(gemm_tc_kernel<EPI_F32, 4, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, tc_smem(4, 1));
-    cudaFuncSetAttribute(gemm_tc_kernel<EPI_RESID, 4, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, tc_smem(4, 1));
-    cudaFuncSetAttribute(gemm_tc_kernel<EPI_SPLIT, 4, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, tc_smem(4, 1));
-    cudaFuncSetAttribute(gemm_tc_kernel<EPI_SPLIT_SILU, 4, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, tc_smem(4, 1));
-    cudaFuncSetAttribute(gemm_tc_kernel<EPI_SPLIT_SILU, 3, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, tc_smem(3, 2));
-    cudaFuncSetAttribute(gemm_tc_kernel<EPI_NODE, 4, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, tc_smem(4, 1));
+#define LC_TC_ATTR(E)                                                                        \
+  cudaFuncSetAttribute(gemm_tc_kernel<E, 3, 1, true>,                                        \
+                       cudaFuncAttributeMaxDynamicSharedMemorySize, sp);                     \
+  cudaFuncSetAttribute(gemm_tc_kernel<E, 4, 1, false>,                                       \
+                       cudaFuncAttributeMaxDynamicSharedMemorySize, sn);
+    LC_TC_ATTR(EPI_F32)
+    LC_TC_ATTR(EPI_RESID)
+    LC_TC_ATTR(EPI_SPLIT)
+    LC_TC_ATTR(EPI_SPLIT_SILU)
+    LC_TC_ATTR(EPI_NODE)
+#undef LC_TC_ATTR
     attr = true;
   }
   static int sms = 0;
@@ -534,19 +557,19 @@ cudaError_t launch_gemm(int epi, const GemmArgs& g, cudaStream_t stream) {
   }
   const int64_t ntiles = int64_t((g.N + TC_BN - 1) / TC_BN) * ((g.M + TC_BM - 1) / TC_BM);
   const dim3 grid(static_cast<unsigned>(ntiles < sms ? ntiles : sms));
-  constexpr int s41 = tc_smem(4, 1), s32 = tc_smem(3, 2);
+#define LC_TC_LAUNCH(E)                                                                      \
+  if (pair)                                                                                  \
+    gemm_tc_kernel<E, 3, 1, true><<<grid, TC_THREADS, sp, stream>>>(ta, tb, tc, g);          \
+  else                                                                                       \
+    gemm_tc_kernel<E, 4, 1, false><<<grid, TC_THREADS, sn, stream>>>(ta, tb, tc, g);
   switch (epi) {
-    case EPI_F32: gemm_tc_kernel<EPI_F32, 4, 1><<<grid, TC_THREADS, s41, stream>>>(ta, tb, tc, g); break;
-    case EPI_RESID: gemm_tc_kernel<EPI_RESID, 4, 1><<<grid, TC_THREADS, s41, stream>>>(ta, tb, tc, g); break;
-    case EPI_SPLIT: gemm_tc_kernel<EPI_SPLIT, 4, 1><<<grid, TC_THREADS, s41, stream>>>(ta, tb, tc, g); break;
-    case EPI_SPLIT_SILU:
-      if (g.Ka <= 512)
-        gemm_tc_kernel<EPI_SPLIT_SILU, 3, 2><<<grid, TC_THREADS, s32, stream>>>(ta, tb, tc, g);
-      else
-        gemm_tc_kernel<EPI_SPLIT_SILU, 4, 1><<<grid, TC_THREADS, s41, stream>>>(ta, tb, tc, g);
-      break;
-    default: gemm_tc_kernel<EPI_NODE, 4, 1><<<grid, TC_THREADS, s41, stream>>>(ta, tb, tc, g); break;
+    case EPI_F32: LC_TC_LAUNCH(EPI_F32) break;
+    case EPI_RESID: LC_TC_LAUNCH(EPI_RESID) break;
+    case EPI_SPLIT: LC_TC_LAUNCH(EPI_SPLIT) break;
+    case EPI_SPLIT_SILU: LC_TC_LAUNCH(EPI_SPLIT_SILU) break;
+    default: LC_TC_LAUNCH(EPI_NODE) break;
   }
+#undef LC_TC_LAUNCH
   note_launch();
   return cudaGetLastError();
 }
