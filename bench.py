@@ -163,6 +163,35 @@ def run_reference(a):
     print(json.dumps(line), flush=True)
 
 
+def rank_workload(name, tier, batch, rank):
+    """This rank's blocks for a weak-scaling run: the model (weights) is the one every rank
+    shares; the blocks are drawn from a seed of their own, so that N ranks process N
+    different batches of the same workload."""
+    from synth import make_workload
+    from synth.inputs import CONFIGS
+    if rank == 0:
+        return make_workload(name, tier=tier, batch=batch)
+    shared = make_workload(name, tier=tier, batch=1).weights
+    return make_workload(name, tier=tier, batch=batch,
+                         seed=CONFIGS[name]["seed"] + 7919 * rank, weights=shared)
+
+
+def max_over_ranks(x, device):
+    """The largest x over all ranks (x itself on one rank)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(batch_per_rank, steps, world, seconds):
+    """Whole-job blocks/s: every rank's blocks over the slowest rank's time."""
+    return batch_per_rank * steps * world / seconds
+
+
 def run_gb300(a):
     import numpy as np
     import torch
@@ -180,7 +209,6 @@ def run_gb300(a):
     import __graft_entry__
     __graft_entry__.build()
     import draft_block_candidate_gb300 as lc
-    from synth import make_workload
 
     # CPU baseline first (a fresh, thread-pinned process), rank 0 at N = 1 only.
     cpu = None
@@ -190,7 +218,7 @@ def run_gb300(a):
                "sample": f"{a.cpu_blocks} blocks x 2 timed steps of the same workload "
                          f"(full rows, float64, 1 thread)"}
 
-    wl = make_workload(a.workload, tier=a.tier, batch=a.batch)
+    wl = rank_workload(a.workload, a.tier, a.batch, rank)
     batch, B, V, K = wl.batch, wl.B, wl.V, wl.K
     logits_host = torch.from_numpy(wl.logits.view(np.int16)).view(torch.bfloat16)
     logits = logits_host.to(dev)
@@ -263,11 +291,8 @@ def run_gb300(a):
         launch_mode = "CUDA graph of one lilicorr_rerank, replayed per step"
     launches = int(round(launches_per_step * a.steps))
     clk = clocks.stop()
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
-    value = batch * a.steps * world / (ms / 1e3)
+    ms = max_over_ranks(ms, dev)
+    value = job_throughput(batch, a.steps, world, ms / 1e3)
 
     # e2e through the host-memory entry point: H2D copies in, D2H tokens out, per step.
     e2e = None
@@ -288,14 +313,11 @@ def run_gb300(a):
                            tokens=tok_h, path_score=ps_h, workspace=wsh, stream=stream)
         el = time.perf_counter() - t0
         barrier()
-        if world > 1:
-            t = torch.tensor([el], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            el = float(t.item())
+        el = max_over_ranks(el, dev)
         # the entry point copies rows 1..B-1 of each block (row 0 is never read)
         h2d = (pin_logits.numel() // B * (B - 1) * 2 + pin_tgt.numel() * 2 + pin_anc.numel() * 4)
         d2h = tok_h.numel() * 4 + ps_h.numel() * 4
-        e2e = {"value": batch * a.e2e_steps * world / el, "unit": "blocks/s",
+        e2e = {"value": job_throughput(batch, a.e2e_steps, world, el), "unit": "blocks/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": a.e2e_steps,
                "api": "lilicorr_rerank_host (pinned host buffers; chunked copies overlapped "
                       "with compute)"}
