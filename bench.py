@@ -192,6 +192,39 @@ def job_throughput(batch_per_rank, steps, world, seconds):
     return batch_per_rank * steps * world / seconds
 
 
+LM_D = 4096  # drafter hidden width of the vocabulary projection (the 8B target's width)
+
+
+def time_lm_head(lc, rows, V, K, dev, stream, peak_tflops, calls=5, D=LM_D):
+    """The vocabulary projection fused with the top-K / log-partition pass
+    (lilicorr_lm_head_topk_lse) on `rows` drafter hidden states: random bf16 operands
+    made on the device, CUDA-event time per call on the launching stream."""
+    import torch
+    g = torch.Generator(device=dev)
+    g.manual_seed(1234)
+    h = torch.randn(rows, D, device=dev, generator=g).to(torch.bfloat16)
+    w = (torch.randn(V, D, device=dev, generator=g) * (1.5 / D ** 0.5)).to(torch.bfloat16)
+    out = lc.lm_head_topk_lse(h, w, K, stream=stream)
+    ws = torch.empty(lc.lm_head_workspace_bytes(rows, V, D, K), dtype=torch.uint8, device=dev)
+    for _ in range(3):
+        lc.lm_head_topk_lse(h, w, K, workspace=ws, out=out, stream=stream)
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(calls):
+        lc.lm_head_topk_lse(h, w, K, workspace=ws, out=out, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    us = e0.elapsed_time(e1) / calls * 1e3
+    tflops = 2.0 * rows * V * D / (us * 1e-6) / 1e12
+    del h, w, ws, out
+    return {"rows": rows, "V": V, "D": D, "K": K, "us_per_call": us, "bound": "tensor",
+            "achieved": tflops, "peak": peak_tflops, "unit": "TFLOP/s",
+            "frac": tflops / peak_tflops, "calls": calls,
+            "data": "synthetic: hidden N(0,1), vocabulary matrix N(0, 1.5^2/D), bf16, on device"}
+
+
 def run_gb300(a):
     import numpy as np
     import torch
@@ -366,6 +399,9 @@ def run_gb300(a):
     else:
         roof = {"bound": "latency", "kernel": dominant, "achieved": None, "peak": None,
                 "unit": None, "frac": None, "traffic": None}
+    lm = None
+    if not a.no_lm_head:
+        lm = time_lm_head(lc, batch * (B - 1), V, K, dev, stream, pk["bf16_tflops"])
     line = {
         "metric": METRIC, "value": value, "unit": "blocks/s", "n_gpus": world,
         "steps": a.steps, "warmup": a.warmup, "ms_per_step": step_ms,
@@ -384,6 +420,7 @@ def run_gb300(a):
         "e2e": e2e,
         "cpu_baseline": cpu,
         "clocks": clk,
+        "lm_head_topk_lse": lm,
     }
     print(json.dumps(line), flush=True)
     w.close()
@@ -436,6 +473,8 @@ def main():
     ap.add_argument("--ref-blocks", type=int, default=1)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-lm-head", action="store_true",
+                    help="skip the fused vocabulary projection + top-K / LSE measurement")
     ap.add_argument("--no-graph", action="store_true",
                     help="time eager launches instead of a replayed CUDA graph")
     ap.add_argument("--batch", type=int, default=None, help="override the workload's batch")

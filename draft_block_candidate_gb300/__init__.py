@@ -10,6 +10,8 @@ from .api import (  # noqa: F401
     greedy_walk,
     viterbi,
     launch_count,
+    lm_head_topk_lse,
+    lm_head_workspace_bytes,
     rerank,
     rerank_host,
     rerank_host_workspace,

@@ -44,6 +44,10 @@ SIGNATURES = {
                                           C.c_int64, C.c_int64, C.c_int32, _P, _P, C.c_size_t,
                                           _P]),
     "lilicorr_topk_lse_merge": (C.c_int, [_P, C.c_int32, C.c_int64, C.c_int32, _P, _P, _P, _P]),
+    "lilicorr_lm_head_workspace_bytes": (C.c_size_t, [C.c_int64, C.c_int64, C.c_int32,
+                                                      C.c_int32]),
+    "lilicorr_lm_head_topk_lse": (C.c_int, [_P, _P, C.c_int64, C.c_int64, C.c_int32, C.c_int32,
+                                            _P, _P, _P, _P, C.c_size_t, _P]),
     "lilicorr_status_string": (C.c_char_p, [C.c_int]),
     "lilicorr_last_error": (C.c_char_p, []),
     "lilicorr_launch_count": (C.c_uint64, []),

@@ -236,6 +236,37 @@ def topk_lse_merge(records: torch.Tensor, K: int, stream=None):
     return cid, cv, lse
 
 
+def lm_head_workspace_bytes(rows: int, V: int, D: int, K: int) -> int:
+    """lilicorr_lm_head_workspace_bytes (0 for unsupported sizes)."""
+    return int(L.lib().lilicorr_lm_head_workspace_bytes(rows, V, D, K))
+
+
+def lm_head_topk_lse(hidden: torch.Tensor, w_lm: torch.Tensor, K: int,
+                     workspace: Optional[torch.Tensor] = None, out=None, stream=None):
+    """lilicorr_lm_head_topk_lse: the projection hidden [rows, D] x w_lm [V, D]^T (bf16)
+    fused with the top-K / log-sum-exp pass.  Returns (cand_id [rows,K] int32,
+    cand_logit [rows,K] f32, lse [rows] f32); the logits themselves are never stored."""
+    if hidden.dtype != torch.bfloat16 or w_lm.dtype != torch.bfloat16:
+        raise ValueError("hidden and w_lm must be bfloat16")
+    rows, D = hidden.shape
+    V, D2 = w_lm.shape
+    if D2 != D:
+        raise ValueError("hidden and w_lm disagree on D")
+    dev = hidden.device
+    if out is None:
+        out = (torch.empty(rows, K, dtype=torch.int32, device=dev),
+               torch.empty(rows, K, dtype=torch.float32, device=dev),
+               torch.empty(rows, dtype=torch.float32, device=dev))
+    if workspace is None:
+        n = int(L.lib().lilicorr_lm_head_workspace_bytes(rows, V, D, K))
+        workspace = torch.empty(max(n, 1), dtype=torch.uint8, device=dev)
+    st = L.lib().lilicorr_lm_head_topk_lse(_ptr(hidden), _ptr(w_lm), rows, V, D, K,
+                                           _ptr(out[0]), _ptr(out[1]), _ptr(out[2]),
+                                           _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(st, "lilicorr_lm_head_topk_lse")
+    return out
+
+
 def greedy_walk(pair_scores: torch.Tensor, cand_id: torch.Tensor,
                 anchor_ids: Optional[torch.Tensor] = None, stream=None):
     """lilicorr_greedy_walk on given scores [batch,B-1,K,K]: (tokens, choice, path_score)."""

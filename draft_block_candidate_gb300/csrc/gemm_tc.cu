@@ -27,6 +27,9 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <float.h>
+#include <limits.h>
+
 #include <algorithm>
 
 #include "kernels.cuh"
@@ -572,6 +575,311 @@ cudaError_t launch_gemm(int epi, const GemmArgs& g, cudaStream_t stream) {
 #undef LC_TC_LAUNCH
   note_launch();
   return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ LM head + top-K / LSE
+//
+// The drafter's vocabulary projection fused with step a1 (the follow-on the serving
+// write-up lists after the rerank: the projection's logits go straight into the top-K /
+// log-partition pass instead of a round trip through HBM):
+//   logit[r, v] = hidden[r, :] . W[v, :]   (bf16 operands, f32 accumulation)
+// and for every row its K best (value desc, id asc) and the online log-sum-exp.  A CTA
+// owns one 128-row tile and one contiguous range of 256-column vocabulary tiles; the MMA
+// side is the plain (non-split) form of the kernel above, and the epilogue warps keep,
+// per (row, column half), a running base-2 log-sum-exp and a sorted top-K in registers.
+// At the end the two halves of a row are merged and one record per (row, range) is
+// written in the vocabulary-shard record format, which the shard merge reduces to the
+// outputs.
+constexpr float LM_LOG2E = 1.4426950408889634f;
+constexpr float LM_M2_INIT = -1e30f;
+
+struct LmArgs {
+  int64_t rows, V;
+  int D, K;
+  int nr;   // vocabulary ranges per row tile
+  int tpr;  // 256-column tiles per range
+  char* records;  // [nr][rows] records of 8 + 8 K bytes
+};
+
+__device__ __forceinline__ bool lm_better(float va, int ia, float vb, int ib) {
+  return va > vb || (va == vb && ia < ib);
+}
+
+template <int KM>
+__global__ void __launch_bounds__(TC_THREADS, 1)
+    lm_head_topk_kernel(const __grid_constant__ CUtensorMap tmA,
+                        const __grid_constant__ CUtensorMap tmB, const LmArgs a) {
+  constexpr int ST = 4;
+  extern __shared__ uint8_t tc_smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + ST * TC_A_BYTES;
+  __shared__ __align__(8) uint64_t full_bar[ST], empty_bar[ST];
+  __shared__ __align__(8) uint64_t acc_full[2], acc_empty[2];
+  __shared__ uint32_t s_tmem;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int KB = a.D / TC_BK;
+  const int NT = static_cast<int>((a.V + TC_BN - 1) / TC_BN);
+  const int mt = blockIdx.x / a.nr, rg = blockIdx.x % a.nr;
+  const int nt0 = rg * a.tpr, nt1 = min(NT, nt0 + a.tpr);
+  const int64_t m0 = int64_t(mt) * TC_BM;
+
+  if (tid == 0) {
+    for (int s = 0; s < ST; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], TC_EPI_WARPS);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 0) tmem_alloc(&s_tmem, TC_TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+
+  if (warp == 0 && lane == 0) {
+    // ---- producer: hidden rows of the tile and the vocabulary rows of each N tile
+    int it = 0;
+    bool ok = true;
+    for (int nt = nt0; nt < nt1 && ok; ++nt) {
+      for (int kb = 0; kb < KB; ++kb, ++it) {
+        const int s = it % ST, use = it / ST;
+        if (use > 0 && !mbar_wait_bounded(&empty_bar[s], (use - 1) & 1, &g_err_tc, ERR_TC_EMPTY)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&full_bar[s], TC_A_BYTES + TC_B_BYTES);
+        tma_load_2d(sA + s * TC_A_BYTES, &tmA, kb * TC_BK, static_cast<int>(m0), &full_bar[s]);
+        tma_load_2d(sB + s * TC_B_BYTES, &tmB, kb * TC_BK, nt * TC_BN, &full_bar[s]);
+      }
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---- MMA issuer
+    constexpr uint32_t idesc = idesc_bf16(TC_BM, TC_BN);
+    int it = 0, i = 0;
+    bool ok = true;
+    for (int nt = nt0; nt < nt1 && ok; ++nt, ++i) {
+      const int buf = i & 1;
+      const uint32_t acc = tmem + uint32_t(buf * TC_BN);
+      if (i >= 2 && !mbar_wait_bounded(&acc_empty[buf], ((i >> 1) - 1) & 1, &g_err_tc,
+                                        ERR_TC_ACC_EMPTY)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      for (int kb = 0; kb < KB; ++kb, ++it) {
+        const int s = it % ST, use = it / ST;
+        if (!mbar_wait_bounded(&full_bar[s], use & 1, &g_err_tc, ERR_TC_FULL)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < TC_BK / 16; ++kk)
+          umma_bf16(acc, sw128_desc(sA + s * TC_A_BYTES + kk * 32),
+                    sw128_desc(sB + s * TC_B_BYTES + kk * 32), idesc, (kb | kk) != 0);
+        umma_commit(&empty_bar[s]);
+      }
+      umma_commit(&acc_full[buf]);
+    }
+  } else if (warp >= 2) {
+    // ---- epilogue: quarter q = TMEM lanes 32q.. (rows), half = the tile's column half
+    const int q = warp & 3, half = (warp - 2) >> 2;
+    const int K = a.K;
+    float m2 = LM_M2_INIT, ssum = 0.f;
+    float tv[KM];
+    int ti[KM];
+#pragma unroll
+    for (int j = 0; j < KM; ++j) {
+      tv[j] = -INFINITY;
+      ti[j] = INT_MAX;
+    }
+    float kth = -INFINITY;  // tv[K - 1]
+    bool done = false;
+    int i = 0;
+    for (int nt = nt0; nt < nt1; ++nt, ++i) {
+      const int buf = i & 1;
+      if (!mbar_wait_bounded(&acc_full[buf], (i >> 1) & 1, &g_err_tc, ERR_TC_ACCUM)) {
+        done = true;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll 1
+      for (int cc = half * (TC_BN / 64); cc < (half + 1) * (TC_BN / 64); ++cc) {
+        float v[32];
+        tmem_ld32(tmem + (uint32_t(32 * q) << 16) + uint32_t(buf * TC_BN + cc * 32), v);
+        const int64_t n = int64_t(nt) * TC_BN + cc * 32;
+        const int64_t left = a.V - n;
+        const int nvalid = left < 32 ? static_cast<int>(left) : 32;
+        // online log-sum-exp over the chunk's valid columns
+        float cmax = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (j < nvalid) cmax = fmaxf(cmax, v[j]);
+        const float c2 = cmax * LM_LOG2E;
+        if (c2 > m2) {
+          ssum *= exp2f(m2 - c2);
+          m2 = c2;
+        }
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (j < nvalid) ssum += exp2f(fmaf(v[j], LM_LOG2E, -m2));
+        // top-K: ids only grow along this thread's columns, so a value equal to the K-th
+        // cannot enter; insertion keeps tv sorted (value desc, id asc)
+        if (cmax > kth) {
+#pragma unroll 1
+          for (int j = 0; j < nvalid; ++j) {
+            float x = v[0];
+#pragma unroll
+            for (int u = 1; u < 32; ++u)
+              if (j == u) x = v[u];
+            if (!(x > kth)) continue;
+            const int id = static_cast<int>(n) + j;
+            bool placed = false;
+#pragma unroll
+            for (int u = KM - 1; u >= 0; --u) {
+              if (u >= K || placed) continue;
+              if (u > 0 && lm_better(x, id, tv[u - 1], ti[u - 1])) {
+                tv[u] = tv[u - 1];
+                ti[u] = ti[u - 1];
+              } else {
+                tv[u] = x;
+                ti[u] = id;
+                placed = true;
+              }
+            }
+#pragma unroll
+            for (int u = 0; u < KM; ++u)
+              if (u == K - 1) kth = tv[u];
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[buf]);
+    }
+    // ---- merge the two column halves of each row through shared memory (the operand
+    // ring is idle once the last accumulator has been read), then write the record
+    tc_fence_before();
+    asm volatile("bar.sync %0, 256;" ::"r"(1) : "memory");  // every epilogue warp is done
+    float* scr = reinterpret_cast<float*>(sA);  // [128 rows][2 halves][2 + 2 KM]
+    constexpr int RS = 2 + 2 * KM;
+    const int r = 32 * q + lane;
+    float* mine = scr + (r * 2 + half) * RS;
+    mine[0] = m2;
+    mine[1] = ssum;
+#pragma unroll
+    for (int j = 0; j < KM; ++j) {
+      mine[2 + j] = tv[j];
+      reinterpret_cast<int*>(mine)[2 + KM + j] = ti[j];
+    }
+    asm volatile("bar.sync %0, 256;" ::"r"(1) : "memory");
+    const int64_t row = m0 + r;
+    if (half == 0 && row < a.rows && !done) {
+      const float* p0 = scr + (r * 2) * RS;
+      const float* p1 = p0 + RS;
+      float M = fmaxf(p0[0], p1[0]);
+      const float S = p0[1] * exp2f(p0[0] - M) + p1[1] * exp2f(p1[0] - M);
+      char* rec = a.records + (int64_t(rg) * a.rows + row) * (8 + 8 * int64_t(K));
+      reinterpret_cast<float*>(rec)[0] = M;
+      reinterpret_cast<float*>(rec)[1] = S;
+      float* rv = reinterpret_cast<float*>(rec + 8);
+      int* ri = reinterpret_cast<int*>(rec + 8 + 4 * K);
+      const int* i0 = reinterpret_cast<const int*>(p0) + 2 + KM;
+      const int* i1 = reinterpret_cast<const int*>(p1) + 2 + KM;
+      int x = 0, y = 0;
+      for (int o = 0; o < K; ++o) {
+        const bool take0 = y >= K || (x < K && lm_better(p0[2 + x], i0[x], p1[2 + y], i1[y]));
+        if (take0) {
+          rv[o] = p0[2 + x];
+          ri[o] = i0[x];
+          ++x;
+        } else {
+          rv[o] = p1[2 + y];
+          ri[o] = i1[y];
+          ++y;
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TC_TMEM_COLS);
+  }
+}
+
+bool lm_head_supported(int64_t rows, int64_t V, int D, int K) {
+  return rows >= 1 && V >= 1 && V < (int64_t(1) << 31) - 256 && D >= TC_BK && D % TC_BK == 0 &&
+         K >= 1 && K <= 32 && K <= V;
+}
+
+static void lm_head_plan(int64_t rows, int64_t V, int* nr, int* tpr) {
+  static int sms = 0;
+  if (!sms) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (sms <= 0) sms = 148;
+  }
+  const int64_t MT = (rows + TC_BM - 1) / TC_BM, NT = (V + TC_BN - 1) / TC_BN;
+  int64_t want = std::max<int64_t>(1, (sms + MT / 2) / MT);  // ranges so that MT x nr ~ SMs
+  want = std::min<int64_t>(want, NT);
+  *tpr = static_cast<int>((NT + want - 1) / want);
+  *nr = static_cast<int>((NT + *tpr - 1) / *tpr);
+}
+
+size_t lm_head_records_bytes(int64_t rows, int64_t V, int K) {
+  int nr = 1, tpr = 1;
+  lm_head_plan(rows, V, &nr, &tpr);
+  return size_t(nr) * size_t(rows) * (8 + 8 * size_t(K));
+}
+
+cudaError_t launch_lm_head_topk(const __nv_bfloat16* hidden, const __nv_bfloat16* w_lm,
+                                int64_t rows, int64_t V, int D, int K, void* records,
+                                int32_t* cand_id, float* cand_logit, float* lse,
+                                cudaStream_t stream) {
+  if (!lm_head_supported(rows, V, D, K) || reinterpret_cast<uintptr_t>(hidden) % 16 ||
+      reinterpret_cast<uintptr_t>(w_lm) % 16 || reinterpret_cast<uintptr_t>(records) % 4)
+    return cudaErrorInvalidValue;
+  CUtensorMap ta, tb;
+  if (!make_tmap(&ta, hidden, uint64_t(rows), uint64_t(D), TC_BM) ||
+      !make_tmap(&tb, w_lm, uint64_t(V), uint64_t(D), TC_BN))
+    return cudaErrorInvalidValue;
+  LmArgs la{};
+  la.rows = rows;
+  la.V = V;
+  la.D = D;
+  la.K = K;
+  la.records = static_cast<char*>(records);
+  lm_head_plan(rows, V, &la.nr, &la.tpr);
+  const int64_t MT = (rows + TC_BM - 1) / TC_BM;
+  const dim3 grid(static_cast<unsigned>(MT * la.nr));
+  constexpr int sm = 4 * (TC_A_BYTES + TC_B_BYTES) + 1024;
+  static bool attr = false;
+  if (!attr) {
+    cudaFuncSetAttribute(lm_head_topk_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
+    cudaFuncSetAttribute(lm_head_topk_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
+    cudaFuncSetAttribute(lm_head_topk_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
+    attr = true;
+  }
+  if (K <= 8)
+    lm_head_topk_kernel<8><<<grid, TC_THREADS, sm, stream>>>(ta, tb, la);
+  else if (K <= 16)
+    lm_head_topk_kernel<16><<<grid, TC_THREADS, sm, stream>>>(ta, tb, la);
+  else
+    lm_head_topk_kernel<32><<<grid, TC_THREADS, sm, stream>>>(ta, tb, la);
+  note_launch();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return k1_merge_launch(records, la.nr, rows, K, cand_id, cand_logit, lse, stream);
 }
 
 cudaError_t tc_read_device_error(uint32_t* code) {

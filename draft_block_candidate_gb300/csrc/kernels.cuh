@@ -64,6 +64,13 @@ struct GemmArgs {
 
 // tcgen05 tensor-core GEMM (gemm_tc.cu)
 cudaError_t launch_gemm(int epi, const GemmArgs& g, cudaStream_t stream);
+// LM-head projection fused with the top-K / log-sum-exp pass (gemm_tc.cu)
+bool lm_head_supported(int64_t rows, int64_t V, int D, int K);
+size_t lm_head_records_bytes(int64_t rows, int64_t V, int K);
+cudaError_t launch_lm_head_topk(const __nv_bfloat16* hidden, const __nv_bfloat16* w_lm,
+                                int64_t rows, int64_t V, int D, int K, void* records,
+                                int32_t* cand_id, float* cand_logit, float* lse,
+                                cudaStream_t stream);
 cudaError_t tc_read_device_error(uint32_t* code);
 cudaError_t launch_conf_hidden(const float* cand_logit, const float* lse, int64_t M, int K, int H,
                                const float* w1, const float* b1, __nv_bfloat16* U,

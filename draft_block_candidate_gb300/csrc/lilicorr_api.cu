@@ -502,6 +502,29 @@ lilicorr_status lilicorr_topk_lse_merge(const void* records, int32_t n_shards, i
   return LILICORR_OK;
 }
 
+size_t lilicorr_lm_head_workspace_bytes(int64_t rows, int64_t V, int32_t D, int32_t K) {
+  if (!lm_head_supported(rows, V, D, K)) return 0;
+  return align256(lm_head_records_bytes(rows, V, K));
+}
+
+lilicorr_status lilicorr_lm_head_topk_lse(const void* hidden, const void* w_lm, int64_t rows,
+                                          int64_t V, int32_t D, int32_t K, int32_t* cand_id,
+                                          float* cand_logit, float* lse, void* workspace,
+                                          size_t workspace_bytes, void* stream) {
+  if (!hidden || !w_lm || !cand_id || !cand_logit || !lse) return LILICORR_ERR_INVALID_ARG;
+  if (!lm_head_supported(rows, V, D, K)) return LILICORR_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(hidden) % 16 || reinterpret_cast<uintptr_t>(w_lm) % 16)
+    return LILICORR_ERR_INVALID_ARG;
+  const size_t need = lilicorr_lm_head_workspace_bytes(rows, V, D, K);
+  if (!workspace || workspace_bytes < need || reinterpret_cast<uintptr_t>(workspace) % 256)
+    return LILICORR_ERR_WORKSPACE;
+  LC_CUDA(launch_lm_head_topk(static_cast<const __nv_bfloat16*>(hidden),
+                              static_cast<const __nv_bfloat16*>(w_lm), rows, V, D, K, workspace,
+                              cand_id, cand_logit, lse, static_cast<cudaStream_t>(stream)),
+          "lm head + top-k / lse");
+  return LILICORR_OK;
+}
+
 lilicorr_status lilicorr_greedy_walk(const float* pair_scores, const int32_t* cand_id,
                                      const int32_t* anchor_ids, int64_t batch, int32_t B,
                                      int32_t K, int32_t* tokens, int32_t* choice,

@@ -213,6 +213,26 @@ lilicorr_status lilicorr_topk_lse_merge(const void* records, int32_t n_shards, i
                                         int32_t K, int32_t* cand_id, float* cand_logit,
                                         float* lse, void* stream);
 
+/* The drafter's vocabulary projection fused with step a1 (the serving write-up's list of
+ * follow-ons: the LM-head projection, 0.49 ms of a block in LiLiCorr Table 3, feeds the
+ * top-K / log-partition pass directly, so the [rows, V] logits never reach HBM):
+ *   logit[r,v] = sum_d hidden[r,d] * w_lm[v,d]     (bf16 operands, f32 accumulation)
+ *   cand_id / cand_logit [rows,K] = the K largest logits of row r by (value desc, id asc),
+ *   lse [rows] = log sum_v exp(logit[r,v]).
+ * hidden [rows, D] and w_lm [V, D] are bf16, row-major, 16-byte aligned; D % 64 == 0;
+ * 1 <= K <= min(32, V); V < 2^31 - 256.  The logits are f32 sums of exact bf16 products
+ * in the tensor cores' order, so two logits closer than their rounding may swap places
+ * against an exact reference.  Workspace: lilicorr_lm_head_workspace_bytes (0 for
+ * unsupported sizes), 256-byte aligned; it holds one vocabulary-shard record per row and
+ * vocabulary range, merged as lilicorr_topk_lse_merge does.
+ * Errors: LILICORR_ERR_INVALID_ARG (null pointers, sizes, alignment),
+ * LILICORR_ERR_WORKSPACE, LILICORR_ERR_CUDA. */
+size_t lilicorr_lm_head_workspace_bytes(int64_t rows, int64_t V, int32_t D, int32_t K);
+lilicorr_status lilicorr_lm_head_topk_lse(const void* hidden, const void* w_lm, int64_t rows,
+                                          int64_t V, int32_t D, int32_t K, int32_t* cand_id,
+                                          float* cand_logit, float* lse, void* workspace,
+                                          size_t workspace_bytes, void* stream);
+
 /* Step a5 alone (LiLiCorr Sec. 3.5, Eq. 8) on given scores pair_scores [batch,B-1,K,K]
  * (layout as in lilicorr_taps).  c_1 = argmax_k pair_scores[b,0,0,k]; c_s = argmax_k
  * pair_scores[b,s-1,c_{s-1},k]; ties go to the lowest k (serving PR: the Triton

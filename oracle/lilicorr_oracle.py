@@ -125,6 +125,22 @@ def logit_pass(block_logits: np.ndarray, K: int):
     return ids, vals, logsumexp_rows(rows)
 
 
+def lm_head_logits(hidden: np.ndarray, w_lm: np.ndarray) -> np.ndarray:
+    """logit[r, v] = sum_d hidden[r, d] * w_lm[v, d] in float64: the drafter's vocabulary
+    projection, the stage before the logit pass (LiLiCorr Table 3, "LM-head projection";
+    the serving PR's follow-ons fuse it with the top-k / log-partition pass)."""
+    return np.asarray(hidden, np.float64) @ np.asarray(w_lm, np.float64).T
+
+
+def lm_head_topk_lse(hidden: np.ndarray, w_lm: np.ndarray, K: int):
+    """The fused projection + a1 on rows of drafter hidden states [rows, D] with the
+    vocabulary matrix [V, D]: (cand_id [rows, K], cand_logit [rows, K], lse [rows]) of the
+    projected logits, ordered as in reading R-topk."""
+    rows = lm_head_logits(hidden, w_lm)
+    ids = topk_rows(rows, K)
+    return ids, np.take_along_axis(rows, ids, axis=1), logsumexp_rows(rows)
+
+
 # ---------------------------------------------------------------------------------
 # a2. node build (LiLiCorr Sec. 3.2 and App. A "Architecture")
 # ---------------------------------------------------------------------------------

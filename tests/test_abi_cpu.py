@@ -174,3 +174,18 @@ def test_shard_entry_points_check_arguments(lib):
     assert m(p, 0, 10, 8, p, p, p, None) == 1
     assert m(p, 2, 10, 33, p, p, p, None) == 1
     assert m(None, 2, 10, 8, p, p, p, None) == 1
+
+
+def test_lm_head_entry_points_check_arguments(lib):
+    p = C.c_void_p(256)
+    ws = lib.lilicorr_lm_head_workspace_bytes
+    assert ws(10, 1000, 100, 8) == 0    # D % 64 != 0
+    assert ws(10, 1000, 128, 33) == 0   # K > 32
+    assert ws(10, 4, 128, 8) == 0       # K > V
+    assert ws(0, 1000, 128, 8) == 0     # no rows
+    f = lib.lilicorr_lm_head_topk_lse
+    assert f(None, p, 10, 1000, 128, 8, p, p, p, p, 1 << 20, None) == 1
+    assert f(p, p, 10, 1000, 128, 8, None, p, p, p, 1 << 20, None) == 1
+    assert f(p, p, 10, 1000, 100, 8, p, p, p, p, 1 << 20, None) == 1       # D % 64
+    assert f(p, p, 10, 1000, 128, 0, p, p, p, p, 1 << 20, None) == 1       # K < 1
+    assert f(C.c_void_p(258), p, 10, 1000, 128, 8, p, p, p, p, 1 << 20, None) == 1  # align

@@ -93,6 +93,28 @@ def test_topk_all_equal_and_signed_zero():
     assert O.topk_rows(row[None], 10)[0].tolist()[-1] == 2
 
 
+def test_lm_head_logits_brute_force(rng):
+    """The projection against explicit per-element sums of Python floats."""
+    h = rng.standard_normal((3, 5))
+    w = rng.standard_normal((7, 5))
+    got = O.lm_head_logits(h, w)
+    for r in range(3):
+        for v in range(7):
+            assert math.isclose(got[r, v], math.fsum(h[r, d] * w[v, d] for d in range(5)),
+                                rel_tol=1e-14, abs_tol=1e-14)
+
+
+def test_lm_head_topk_lse_identity_matrix_is_the_logit_pass(rng):
+    """With the vocabulary matrix the identity (V = D), the logits are the hidden rows
+    themselves: the fused pass reduces to the plain top-K and log-partition."""
+    h = np.round(rng.standard_normal((4, 40)) * 4) / 4  # ties included
+    ids, vals, lse = O.lm_head_topk_lse(h, np.eye(40), 6)
+    ref = np.argsort(-h, axis=1, kind="stable")[:, :6]
+    assert np.array_equal(ids, ref)
+    assert np.array_equal(vals, np.take_along_axis(h, ref, axis=1))
+    assert np.allclose(lse, np.log(np.exp(h).sum(axis=1)), rtol=0, atol=1e-12)
+
+
 def test_logit_pass_ignores_anchor_row(rng):
     blk = rng.standard_normal((5, 300))
     a = O.logit_pass(blk, 3)
