@@ -428,6 +428,26 @@ def run_gb300(a):
         torch.distributed.destroy_process_group()
 
 
+def run_lm_head_only(a):
+    """lilicorr_lm_head_topk_lse alone on the workload's drafted rows (a small --batch or
+    --lm-v keeps an ncu capture short); CUDA-event timing on the launching stream."""
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import draft_block_candidate_gb300 as lc
+    from synth.inputs import CONFIGS
+    cfg = CONFIGS[a.workload]
+    batch = a.batch or cfg["batch"]
+    V = a.lm_v or cfg["V"]
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    pk, _ = peaks()
+    r = time_lm_head(lc, batch * (cfg["B"] - 1), V, cfg["K"], dev, torch.cuda.current_stream(dev),
+                     pk["bf16_tflops"], calls=a.steps)
+    print(json.dumps({"kernel": "lm_head_topk", **r}), flush=True)
+
+
 def run_logit_pass_only(a):
     """lilicorr_topk_lse alone on the workload's logits (a small --batch keeps an ncu
     capture short); CUDA-event timing on the launching stream."""
@@ -478,8 +498,10 @@ def main():
     ap.add_argument("--no-graph", action="store_true",
                     help="time eager launches instead of a replayed CUDA graph")
     ap.add_argument("--batch", type=int, default=None, help="override the workload's batch")
-    ap.add_argument("--only", default=None, choices=["logit_pass"],
+    ap.add_argument("--only", default=None, choices=["logit_pass", "lm_head"],
                     help="time one kernel alone (profiling driver); prints its own JSON")
+    ap.add_argument("--lm-v", type=int, default=None,
+                    help="vocabulary size of --only lm_head (default: the workload's V)")
     a = ap.parse_args()
     if a.workload != "highconc":
         a.tier = None
@@ -489,6 +511,8 @@ def main():
         run_reference(a)
     elif a.only == "logit_pass":
         run_logit_pass_only(a)
+    elif a.only == "lm_head":
+        run_lm_head_only(a)
     else:
         run_gb300(a)
 
