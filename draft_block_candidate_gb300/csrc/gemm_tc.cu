@@ -533,14 +533,21 @@ cudaError_t launch_gemm(int epi, const GemmArgs& g, cudaStream_t stream) {
         !make_tmap_out(&tc, g.out, uint64_t(g.M), uint64_t(g.N), true))
       return cudaErrorInvalidValue;
   }
-  // A split operand (Ka = 2 Kw) runs paired stages: A_hi and A_lo share one W block
+  // A split operand (Ka = 2 Kw) runs paired stages: A_hi and A_lo share one W block.
+  // Measured per epilogue at the high-concurrency sizes: the node sum (embedding-row
+  // gathers) and the SiLU epilogue of short K (FFN1) run faster with 2 paired stages in
+  // flight than with 3 (less operand traffic competing with their gathers and output
+  // stream); the others with 3.
   const bool pair = g.Ka == 2 * g.Kw;
-  constexpr int sp = tc_smem(3, 1, true), sn = tc_smem(4, 1, false);
+  const bool two = epi == EPI_NODE || (epi == EPI_SPLIT_SILU && g.Ka <= 512);
+  constexpr int sp = tc_smem(3, 1, true), sp2 = tc_smem(2, 1, true), sn = tc_smem(4, 1, false);
   static bool attr = false;
   if (!attr) {
 #define LC_TC_ATTR(E)                                                                        \
   cudaFuncSetAttribute(gemm_tc_kernel<E, 3, 1, true>,                                        \
                        cudaFuncAttributeMaxDynamicSharedMemorySize, sp);                     \
+  cudaFuncSetAttribute(gemm_tc_kernel<E, 2, 1, true>,                                        \
+                       cudaFuncAttributeMaxDynamicSharedMemorySize, sp2);                    \
   cudaFuncSetAttribute(gemm_tc_kernel<E, 4, 1, false>,                                       \
                        cudaFuncAttributeMaxDynamicSharedMemorySize, sn);
     LC_TC_ATTR(EPI_F32)
@@ -561,7 +568,9 @@ cudaError_t launch_gemm(int epi, const GemmArgs& g, cudaStream_t stream) {
   const int64_t ntiles = int64_t((g.N + TC_BN - 1) / TC_BN) * ((g.M + TC_BM - 1) / TC_BM);
   const dim3 grid(static_cast<unsigned>(ntiles < sms ? ntiles : sms));
 #define LC_TC_LAUNCH(E)                                                                      \
-  if (pair)                                                                                  \
+  if (pair && two)                                                                           \
+    gemm_tc_kernel<E, 2, 1, true><<<grid, TC_THREADS, sp2, stream>>>(ta, tb, tc, g);         \
+  else if (pair)                                                                             \
     gemm_tc_kernel<E, 3, 1, true><<<grid, TC_THREADS, sp, stream>>>(ta, tb, tc, g);          \
   else                                                                                       \
     gemm_tc_kernel<E, 4, 1, false><<<grid, TC_THREADS, sn, stream>>>(ta, tb, tc, g);
