@@ -197,6 +197,45 @@ __global__ void rmsnorm_split_kernel(const float* __restrict__ X, const float* _
   }
 }
 
+// Hidden width 256 (8 columns per lane): each warp takes RPW rows, issues all their
+// 16-byte loads before the first reduction, keeps the rows in registers, and loads the
+// gain once.
+template <int RPW>
+__global__ void __launch_bounds__(256) rmsnorm_split256_kernel(const float* __restrict__ X,
+                                                               const float* __restrict__ gain,
+                                                               int64_t M, float eps,
+                                                               __nv_bfloat16* __restrict__ out) {
+  constexpr int H = 256;
+  const int lane = threadIdx.x & 31;
+  const int64_t m0 = (int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5)) * RPW;
+  if (m0 >= M) return;
+  float v[RPW][8];
+#pragma unroll
+  for (int r = 0; r < RPW; ++r) {
+    if (m0 + r < M)
+      load8(X + (m0 + r) * H + lane * 8, v[r]);
+    else
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[r][j] = 0.f;
+  }
+  float g[8];
+  load8(gain + lane * 8, g);
+#pragma unroll
+  for (int r = 0; r < RPW; ++r) {
+    float ss = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) ss = fmaf(v[r][j], v[r][j], ss);
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) ss += __shfl_xor_sync(FULL_MASK, ss, o);
+    const float inv = 1.0f / sqrtf(ss / float(H) + eps);
+    if (m0 + r >= M) continue;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[r][j] = v[r][j] * inv * g[j];
+    __nv_bfloat16* o = out + (m0 + r) * 2 * H;
+    store_split8(v[r], o + lane * 8, o + H + lane * 8);
+  }
+}
+
 // ------------------------------------------------------------------ attention
 // Per (block, head): softmax_j(q_i.k_j / sqrt(dh) + dist[slot_j - slot_i + B_max - 2]
 // + [slot_i == slot_j] * same) v_j over all S lattice tokens (bidirectional, no mask).
@@ -490,8 +529,15 @@ cudaError_t launch_rmsnorm_split(const float* X, const float* gain, int64_t M, i
                                  __nv_bfloat16* out, cudaStream_t stream) {
   if (H % 8) return cudaErrorInvalidValue;
   const int wpb = 8;
-  rmsnorm_split_kernel<<<static_cast<unsigned>((M + wpb - 1) / wpb), wpb * 32, 0, stream>>>(
-      X, gain, M, H, eps, out);
+  if (H == 256) {
+    constexpr int RPW = 4;
+    const int64_t warps = (M + RPW - 1) / RPW;
+    rmsnorm_split256_kernel<RPW><<<static_cast<unsigned>((warps + wpb - 1) / wpb), wpb * 32, 0,
+                                   stream>>>(X, gain, M, eps, out);
+  } else {
+    rmsnorm_split_kernel<<<static_cast<unsigned>((M + wpb - 1) / wpb), wpb * 32, 0, stream>>>(
+        X, gain, M, H, eps, out);
+  }
   note_launch();
   return cudaGetLastError();
 }
