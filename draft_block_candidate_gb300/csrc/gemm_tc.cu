@@ -47,9 +47,8 @@ constexpr int TC_STG_BYTES = 4096;  // one 32 x 32 output chunk (f32, or bf16 hi
 // buffers per warp.  A stage holds one 64-wide K block of A and of W, or, for a split
 // operand (pair), the A_hi and A_lo blocks that share one W block.  Configurations in
 // use: 4 plain stages or 3 paired stages, with 1 staging buffer per epilogue warp.
-__host__ __device__ constexpr int tc_smem(int st, int nb, bool pair) {
-  return st * ((pair ? 2 : 1) * TC_A_BYTES + TC_B_BYTES) + TC_EPI_WARPS * nb * TC_STG_BYTES +
-         1024;
+__host__ __device__ constexpr int tc_smem(int st, int nb, bool pair, int ew = TC_EPI_WARPS) {
+  return st * ((pair ? 2 : 1) * TC_A_BYTES + TC_B_BYTES) + ew * nb * TC_STG_BYTES + 1024;
 }
 constexpr uint32_t TC_TMEM_COLS = 2 * TC_BN;  // two accumulator buffers
 
@@ -313,8 +312,10 @@ __device__ __forceinline__ void tc_epilogue_staged(const GemmArgs& g, const CUte
 
 // ------------------------------------------------------------------ kernel
 
-template <int EPI, int TC_STAGES, int TC_STG_BUFS, bool PAIR>
-__global__ void __launch_bounds__(TC_THREADS, 1)
+// EW epilogue warps: 8 (two per TMEM quarter, each half the columns) or 16 (four per
+// quarter, each a quarter of the columns: more warps to hide the epilogue's latencies).
+template <int EPI, int TC_STAGES, int TC_STG_BUFS, bool PAIR, int EW = TC_EPI_WARPS>
+__global__ void __launch_bounds__(32 * (2 + EW), 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const GemmArgs g) {
   extern __shared__ uint8_t tc_smem_raw[];
@@ -342,7 +343,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], TC_EPI_WARPS);
+      mbar_init(&acc_empty[b], EW);
     }
     fence_mbar_init();
   }
@@ -413,7 +414,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   } else if (warp >= 2) {
     // ---- epilogue: quarter q = warp % 4 owns TMEM lanes 32q..32q+31 (output rows);
     // the two warps of a quarter split the tile's columns in halves
-    const int q = warp & 3, half = (warp - 2) >> 2;
+    constexpr int CPP = (TC_BN / 32) / (EW / 4);  // 32-column chunks per epilogue warp
+    const int q = warp & 3, half = (warp - 2) >> 2;  // half: this warp's column part
     uint8_t* stg = sStage + (warp - 2) * TC_STG_BUFS * TC_STG_BYTES;
     int sb = 0;  // staging buffer of the next chunk
     int i = 0;
@@ -425,7 +427,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       tc_fence_after();
       const int64_t m = m0 + 32 * q + lane;
 #pragma unroll 1
-      for (int cc = half * (TC_BN / 64); cc < (half + 1) * (TC_BN / 64); ++cc) {
+      for (int cc = half * CPP; cc < (half + 1) * CPP; ++cc) {
         float v[32];
         tmem_ld32(tmem + (uint32_t(32 * q) << 16) + uint32_t(buf * TC_BN + cc * 32), v);
         const int n = n0 + cc * 32;
@@ -535,12 +537,15 @@ cudaError_t launch_gemm(int epi, const GemmArgs& g, cudaStream_t stream) {
   }
   // A split operand (Ka = 2 Kw) runs paired stages: A_hi and A_lo share one W block.
   // Measured per epilogue at the high-concurrency sizes: the node sum (embedding-row
-  // gathers) and the SiLU epilogue of short K (FFN1) run faster with 2 paired stages in
-  // flight than with 3 (less operand traffic competing with their gathers and output
-  // stream); the others with 3.
+  // gathers) runs faster with 2 paired stages in flight than with 3 (less operand traffic
+  // competing with its gathers); the others with 3.
   const bool pair = g.Ka == 2 * g.Kw;
-  const bool two = epi == EPI_NODE || (epi == EPI_SPLIT_SILU && g.Ka <= 512);
+  // The SiLU epilogue of short K (FFN1) is the longest epilogue per MMA: it runs 16
+  // epilogue warps (2 paired stages leave room for their staging buffers).
+  const bool wide = epi == EPI_SPLIT_SILU && g.Ka <= 512;
+  const bool two = epi == EPI_NODE;
   constexpr int sp = tc_smem(3, 1, true), sp2 = tc_smem(2, 1, true), sn = tc_smem(4, 1, false);
+  constexpr int sw = tc_smem(2, 1, true, 16);
   static bool attr = false;
   if (!attr) {
 #define LC_TC_ATTR(E)                                                                        \
@@ -548,6 +553,8 @@ cudaError_t launch_gemm(int epi, const GemmArgs& g, cudaStream_t stream) {
                        cudaFuncAttributeMaxDynamicSharedMemorySize, sp);                     \
   cudaFuncSetAttribute(gemm_tc_kernel<E, 2, 1, true>,                                        \
                        cudaFuncAttributeMaxDynamicSharedMemorySize, sp2);                    \
+  cudaFuncSetAttribute(gemm_tc_kernel<E, 2, 1, true, 16>,                                    \
+                       cudaFuncAttributeMaxDynamicSharedMemorySize, sw);                     \
   cudaFuncSetAttribute(gemm_tc_kernel<E, 4, 1, false>,                                       \
                        cudaFuncAttributeMaxDynamicSharedMemorySize, sn);
     LC_TC_ATTR(EPI_F32)
@@ -568,7 +575,9 @@ cudaError_t launch_gemm(int epi, const GemmArgs& g, cudaStream_t stream) {
   const int64_t ntiles = int64_t((g.N + TC_BN - 1) / TC_BN) * ((g.M + TC_BM - 1) / TC_BM);
   const dim3 grid(static_cast<unsigned>(ntiles < sms ? ntiles : sms));
 #define LC_TC_LAUNCH(E)                                                                      \
-  if (pair && two)                                                                           \
+  if (pair && wide)                                                                          \
+    gemm_tc_kernel<E, 2, 1, true, 16><<<grid, 32 * 18, sw, stream>>>(ta, tb, tc, g);         \
+  else if (pair && two)                                                                      \
     gemm_tc_kernel<E, 2, 1, true><<<grid, TC_THREADS, sp2, stream>>>(ta, tb, tc, g);         \
   else if (pair)                                                                             \
     gemm_tc_kernel<E, 3, 1, true><<<grid, TC_THREADS, sp, stream>>>(ta, tb, tc, g);          \
