@@ -530,7 +530,7 @@ lilicorr_status lilicorr_greedy_walk(const float* pair_scores, const int32_t* ca
                                      int32_t K, int32_t* tokens, int32_t* choice,
                                      float* path_score, void* stream) {
   if (!pair_scores || !cand_id || !tokens) return LILICORR_ERR_INVALID_ARG;
-  if (batch < 1 || B < 2 || K < 1 || K > 32) return LILICORR_ERR_INVALID_ARG;
+  if (batch < 1 || B < 2 || B > 64 || K < 1 || K > 32) return LILICORR_ERR_INVALID_ARG;
   LC_CUDA(launch_greedy_walk(pair_scores, cand_id, anchor_ids, batch, B, K, tokens, choice,
                              path_score, static_cast<cudaStream_t>(stream)),
           "greedy walk");

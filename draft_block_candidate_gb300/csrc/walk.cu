@@ -219,22 +219,37 @@ __global__ void __launch_bounds__(32) greedy_walk_kernel(
   }
   const float* sc = staged ? gw_smem : src;
   if (lane == 0) tokens[b * B] = anchor_ids ? anchor_ids[b] : -1;
+  // The walk keeps step p's choice and value in lane p % 32 (two rounds for B - 1 > 32);
+  // the outputs and the token lookups happen after the walk, in parallel, so no step
+  // waits for a global load.
   int prev = 0;
+  int c_lo = 0, c_hi = 0;
+  float v_lo = 0.f, v_hi = 0.f;
   for (int p = 0; p < B - 1; ++p) {
-    const int64_t pr = b * (B - 1) + p;
     const float* row = sc + (p * K + prev) * K;
     // argmax as one warp max over ordered keys (-0.0 folded into +0.0 so that equal
     // values tie), then the lowest lane holding it
     const int key = lane < K ? float_key(row[lane] + 0.0f) : INT_MIN;
     const int kmax = __reduce_max_sync(FULL_MASK, key);
     const int idx = __ffs(__ballot_sync(FULL_MASK, key == kmax)) - 1;
-    const float v = key_float(kmax);
-    if (lane == 0) {
-      if (choice) choice[pr] = idx;
-      if (path) path[pr] = v;
-      tokens[b * B + p + 1] = __ldg(cand_id + pr * K + idx);
+    if (lane == (p & 31)) {
+      if (p < 32) {
+        c_lo = idx;
+        v_lo = key_float(kmax);
+      } else {
+        c_hi = idx;
+        v_hi = key_float(kmax);
+      }
     }
     prev = idx;
+  }
+  for (int p = lane; p < B - 1; p += 32) {
+    const int c = p < 32 ? c_lo : c_hi;
+    const float v = p < 32 ? v_lo : v_hi;
+    const int64_t pr = b * (B - 1) + p;
+    if (choice) choice[pr] = c;
+    if (path) path[pr] = v;
+    tokens[b * B + p + 1] = __ldg(cand_id + pr * K + c);
   }
 }
 

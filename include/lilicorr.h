@@ -238,7 +238,8 @@ lilicorr_status lilicorr_lm_head_topk_lse(const void* hidden, const void* w_lm, 
  * pair_scores[b,s-1,c_{s-1},k]; ties go to the lowest k (serving PR: the Triton
  * argmax breaks ties toward the lower index).  cand_id [batch,B-1,K] maps choices to
  * tokens.  Outputs: tokens [batch,B] (tokens[:,0] = anchor_ids or -1), choice
- * [batch,B-1] (nullable), path_score [batch,B-1] (nullable).  1 <= K <= 32. */
+ * [batch,B-1] (nullable), path_score [batch,B-1] (nullable).  1 <= K <= 32,
+ * 2 <= B <= 64. */
 lilicorr_status lilicorr_greedy_walk(const float* pair_scores, const int32_t* cand_id,
                                      const int32_t* anchor_ids, int64_t batch, int32_t B,
                                      int32_t K, int32_t* tokens, int32_t* choice,

@@ -126,6 +126,7 @@ def test_greedy_walk_argument_checks(lib):
     assert lib.lilicorr_greedy_walk(p, p, None, 1, 16, 33, p, None, None, None) == 1
     assert lib.lilicorr_greedy_walk(None, p, None, 1, 16, 4, p, None, None, None) == 1
     assert lib.lilicorr_greedy_walk(p, p, None, 0, 16, 4, p, None, None, None) == 1
+    assert lib.lilicorr_greedy_walk(p, p, None, 1, 65, 4, p, None, None, None) == 1
 
 
 def test_rerank_refuses_null_weights(lib):
