@@ -168,6 +168,82 @@ __global__ void conf_hidden_kernel(const float* __restrict__ cand_logit,
   }
 }
 
+// Hidden width 256: the layer's weights (256 x 5 + 256 biases) sit in shared memory,
+// re-read per row (a lane's 48 values as 12 16-byte loads, interleaved across lanes so a
+// load is conflict-free) instead of held in 48 registers, so more warps fit on an SM;
+// one warp per (slot, 8 candidate rows).
+__device__ __forceinline__ float4 lds4_volatile(const float4* p) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(p))));
+  return v;
+}
+
+__global__ void __launch_bounds__(256) conf_hidden256_kernel(const float* __restrict__ cand_logit,
+                                                             const float* __restrict__ lse,
+                                                             int64_t M, int K,
+                                                             const float* __restrict__ w1,
+                                                             const float* __restrict__ b1,
+                                                             __nv_bfloat16* __restrict__ U) {
+  constexpr int H = 256, RPW = 8;
+  __shared__ float4 sw[12][32];  // lane l's 48 values (w[j][0..4], b[j] for j < 8) as 12 x 4
+  for (int idx = threadIdx.x; idx < 12 * 32 * 4; idx += blockDim.x) {
+    const int l = (idx >> 2) & 31, c = idx >> 7, e = idx & 3;
+    const int f = c * 4 + e, j = f / 6, i = f % 6;
+    const int h = 8 * l + j;
+    reinterpret_cast<float*>(&sw[c][l])[e] = i < 5 ? w1[h * 5 + i] : b1[h];
+  }
+  __syncthreads();
+  const int lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  const int64_t nslots = M / K;
+  const int gps = (K + RPW - 1) / RPW;  // row groups per slot
+  const int64_t units = nslots * gps;
+  for (int64_t un = int64_t(blockIdx.x) * nw + (threadIdx.x >> 5); un < units;
+       un += int64_t(gridDim.x) * nw) {
+    const int64_t j = un / gps;
+    const int k0 = static_cast<int>(un - j * gps) * RPW;
+    const int nk = min(RPW, K - k0);
+    const float* cl = cand_logit + j * K;
+    float g[5] = {0.f, 0.f, 0.f, 0.f, 0.f};
+    if (lane < nk) {
+      const float l2 = __ldg(lse + j);
+      const float top = __ldg(cl);
+      const int k = k0 + lane;
+      const float lp = __ldg(cl + k) - l2;
+      g[0] = lp;
+      g[1] = expf(lp);
+      g[2] = lp - (top - l2);
+      g[3] = K > 1 ? float(k) / float(K - 1) : 0.f;
+      g[4] = k == 0 ? 1.f : 0.f;
+    }
+    __nv_bfloat16* u = U + (j * K + k0) * 2 * H;
+    for (int t = 0; t < nk; ++t, u += 2 * H) {
+      float f[5];
+#pragma unroll
+      for (int i = 0; i < 5; ++i) f[i] = __shfl_sync(FULL_MASK, g[i], t);
+      float w[48];
+#pragma unroll
+      for (int c = 0; c < 12; ++c) {
+        const float4 v = lds4_volatile(&sw[c][lane]);
+        w[4 * c] = v.x;
+        w[4 * c + 1] = v.y;
+        w[4 * c + 2] = v.z;
+        w[4 * c + 3] = v.w;
+      }
+      float o[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        float acc = w[6 * q + 5];
+#pragma unroll
+        for (int i = 0; i < 5; ++i) acc = fmaf(w[6 * q + i], f[i], acc);
+        o[q] = silu(acc);
+      }
+      store_split8(o, u + lane * 8, u + H + lane * 8);
+    }
+  }
+}
+
 // ------------------------------------------------------------------ RMSNorm -> split
 // y = x / sqrt(mean(x^2) + eps) * g, one warp per row, 8 columns per lane per pass.
 __global__ void rmsnorm_split_kernel(const float* __restrict__ X, const float* __restrict__ gain,
@@ -520,7 +596,13 @@ cudaError_t launch_conf_hidden(const float* cand_logit, const float* lse, int64_
   const int64_t slots_per_cta = 8;  // one warp per slot
   const unsigned grid = static_cast<unsigned>(
       std::min<int64_t>((M / K + slots_per_cta - 1) / slots_per_cta, 152 * 8));
-  conf_hidden_kernel<<<grid, 256, 0, stream>>>(cand_logit, lse, M, K, H, w1, b1, U);
+  if (H == 256) {
+    const int64_t units = (M / K) * ((K + 7) / 8);  // (slot, 8 rows) per warp, 8 per CTA
+    const unsigned g2 = static_cast<unsigned>(std::min<int64_t>((units + 7) / 8, 152 * 16));
+    conf_hidden256_kernel<<<g2, 256, 0, stream>>>(cand_logit, lse, M, K, w1, b1, U);
+  } else {
+    conf_hidden_kernel<<<grid, 256, 0, stream>>>(cand_logit, lse, M, K, H, w1, b1, U);
+  }
   note_launch();
   return cudaGetLastError();
 }
