@@ -5,9 +5,10 @@
 //                     + [slot_i == slot_j] * same) v_j          (LiLiCorr App. A)
 // over all tokens of the block (bidirectional, no mask).
 //
-// Persistent: one CTA per SM walks the (128-query tile, head, block) items (the heads of
-// a block run on neighbouring CTAs at the same time, so its Q / K / V rows are read from
-// DRAM together), 18 warps:
+// Persistent: one CTA per SM walks the (128-query tile, block, head) items, head-major (a
+// CTA keeps one head's bias table for several items; the two query tiles of a (block,
+// head) run on neighbouring CTAs at the same time, so its K / V tiles are read from DRAM
+// once), 18 warps:
 //   warp 0     TMA: Q (128 x 64), K and V (256 x 64), each as bf16 hi and lo, 128-byte
 //              swizzle; the next item's Q and K load as soon as this item's S is formed,
 //              its V as soon as this item's second product is done; owns the TMEM
@@ -21,7 +22,9 @@
 //              takes the row max (the four parts combined through shared memory); pass 2
 //              recomputes the biased logit, forms p = 2^(x - max) and its sum and writes
 //              p as packed bf16 hi / lo over the logits it came from; the epilogue
-//              divides this warp's 16 columns of O by the sum and stores them split.
+//              divides this warp's 16 columns of O by the sum, splits them into a
+//              swizzled shared-memory tile, and one thread per quarter stores the
+//              quarter's 32 rows with a bulk tensor store (rows past the block clipped).
 // Every mbarrier wait is bounded; on a timeout the CTA records it and still frees TMEM.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -37,7 +40,8 @@ constexpr int AT_NSPLIT = AT_SOFT_WARPS / 4;      // softmax warps per 32-row qu
 constexpr int AT_OW = AT_DH / AT_NSPLIT;          // output columns per softmax warp
 constexpr int AT_THREADS = 32 * (2 + AT_SOFT_WARPS);
 constexpr int AT_TILE = 128 * 64 * 2;  // one [128 x 64] bf16 swizzled tile
-constexpr int AT_SMEM = 10 * AT_TILE + 1024;  // + the bias table, sized per launch
+constexpr int AT_SMEM = 12 * AT_TILE + 1024;  // + the bias table, sized per launch
+constexpr int AT_SMEM_MAX = 227 * 1024 - 8 * 1024;  // dynamic share (static use < 8 KB)
 constexpr int AT_BSTRIDE = AT_KMAX + 4;        // floats per bias-table row (bank offset)
 constexpr uint32_t AT_TMEM_COLS = 512, AT_O_COL = 256;
 constexpr float AT_LOG2E = 1.4426950408889634f;
@@ -59,6 +63,14 @@ __device__ __forceinline__ void at_tma(void* dst, const CUtensorMap* tm, int c0,
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes "
       "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(dst)),
       "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(smem_addr(bar))
+      : "memory");
+}
+__device__ __forceinline__ void at_store(const CUtensorMap* tm, const void* src, int c0, int c1,
+                                         int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(tm)),
+      "r"(smem_addr(src)), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
 }
 __device__ __forceinline__ void at_fence_before() {
@@ -172,14 +184,38 @@ __device__ __forceinline__ void at_st16f(uint32_t taddr, const float (&v)[16]) {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// (query tile, block, head) of a CTA's items, head-major, advanced by the grid stride
+// with carries instead of 64-bit divisions per item.
+struct ItemPos {
+  int qt, blk, h, dqt, dblk, dh, QT, batch;
+  __device__ ItemPos(int64_t t, int64_t G, int QT_, int64_t batch_)
+      : QT(QT_), batch(static_cast<int>(batch_)) {
+    qt = static_cast<int>(t % QT);
+    blk = static_cast<int>((t / QT) % batch_);
+    h = static_cast<int>(t / (QT * batch_));
+    dqt = static_cast<int>(G % QT);
+    dblk = static_cast<int>((G / QT) % batch_);
+    dh = static_cast<int>(G / (QT * batch_));
+  }
+  __device__ void next() {
+    qt += dqt;
+    int c = 0;
+    if (qt >= QT) { qt -= QT; c = 1; }
+    blk += dblk + c;
+    c = 0;
+    if (blk >= batch) { blk -= batch; c = 1; }
+    h += dh + c;
+  }
+};
+
 __device__ __forceinline__ void soft_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(32 * AT_SOFT_WARPS) : "memory");
 }
 
 __global__ void __launch_bounds__(AT_THREADS, 1)
-    attn_tc_kernel(const __grid_constant__ CUtensorMap tm, int S, int Kc, int H, int B_max,
-                   int heads, int64_t batch, const float* __restrict__ dist_bias,
-                   const float* __restrict__ same_bias, __nv_bfloat16* __restrict__ out) {
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tm, const __grid_constant__ CUtensorMap tmo,
+                   int S, int Kc, int H, int B_max, int heads, int64_t batch,
+                   const float* __restrict__ dist_bias, const float* __restrict__ same_bias) {
   extern __shared__ uint8_t at_smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(at_smem_raw) + 1023) & ~uintptr_t(1023));
@@ -189,14 +225,15 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   uint8_t* sKl = sm + 4 * AT_TILE;
   uint8_t* sVh = sm + 6 * AT_TILE;   // V hi / lo: 2 tiles each
   uint8_t* sVl = sm + 8 * AT_TILE;
+  uint8_t* sOh = sm + 10 * AT_TILE;  // output hi / lo tiles [128 rows][64] (128-byte swizzle)
+  uint8_t* sOl = sm + 11 * AT_TILE;
   // [query slot][key]: (dist + same-slot bias) * log2(e) of the current head, -inf for
   // keys beyond the block
-  float* s_btab = reinterpret_cast<float*>(sm + 10 * AT_TILE);
+  float* s_btab = reinterpret_cast<float*>(sm + 12 * AT_TILE);
   __shared__ __align__(8) uint64_t bar_qk, bar_qkfree, bar_v, bar_vfree, bar_s0, bar_s1,
       bar_p0, bar_p1, bar_pv0, bar_o, bar_ofree[2];
   __shared__ uint32_t s_tmem;
   __shared__ float s_pmax[2][AT_NSPLIT][128], s_psum[AT_NSPLIT][128];
-  __shared__ float s_dist[128];  // dist + same-slot bias of the current head
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int QT = (S + AT_QT - 1) / AT_QT;
@@ -236,10 +273,10 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   if (warp == 0 && lane == 0) {
     // ---- producer
     int i = 0;
-    for (int64_t t = blockIdx.x; t < nitems; t += gridDim.x, ++i) {
-      const int qt = static_cast<int>(t % QT);
-      const int h = static_cast<int>((t / QT) % heads);
-      const int tok0 = static_cast<int>((t / QT / heads) * S);
+    ItemPos it(blockIdx.x, gridDim.x, QT, batch);
+    for (int64_t t = blockIdx.x; t < nitems; t += gridDim.x, ++i, it.next()) {
+      const int qt = it.qt, h = it.h;
+      const int tok0 = it.blk * S;
       const int cq = h * AT_DH, ck = H + h * AT_DH, cv = 2 * H + h * AT_DH, lo = 3 * H;
       if (i > 0 && !mbar_wait_bounded(&bar_qkfree, (i - 1) & 1, &g_err_at, ERR_AT_QKFREE)) break;
       mbar_arrive_expect_tx(&bar_qk, 6 * AT_TILE);
@@ -258,9 +295,9 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     }
   } else if (warp == 1 && lane == 0) {
     // ---- MMA issuer.  Per item i: S0 = Q K[0:128]^T, S1 = Q K[128:256]^T (three-term
-    // products, N 128), PV0 into O[i&1] once P0 is ready, PV1 once P1 is ready.  The next
-    // item's S0 is issued as soon as PV0 has completed and its S1 as soon as PV1 has, so
-    // both overlap this item's softmax.
+    // products, N 128), PV0 into O[i&1] once P0 is ready, PV1 once P1 is ready, then the
+    // next item's S0 (over P0, once PV0 has completed) and S1 (once PV1 has), which run
+    // while the softmax warps finish this item's epilogue.
     constexpr uint32_t id_s = at_idesc(128, 128, false);
     constexpr uint32_t id_o = at_idesc(128, 64, true);
     auto qk_half = [&](int half) {
@@ -308,6 +345,12 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       at_fence_after();
       pv_half(0, tO);
       at_commit(&bar_pv0);
+      ok = mbar_wait_bounded(&bar_p1, i & 1, &g_err_at, ERR_AT_P);
+      if (!ok) break;
+      at_fence_after();
+      pv_half(1, tO);
+      at_commit(&bar_o);
+      at_commit(&bar_vfree);
       if (more) {
         // S0 of the next item overwrites P0: after PV0 has completed
         ok = mbar_wait_bounded(&bar_pv0, i & 1, &g_err_at, ERR_AT_O) &&
@@ -316,14 +359,6 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         at_fence_after();
         qk_half(0);
         at_commit(&bar_s0);
-      }
-      ok = mbar_wait_bounded(&bar_p1, i & 1, &g_err_at, ERR_AT_P);
-      if (!ok) break;
-      at_fence_after();
-      pv_half(1, tO);
-      at_commit(&bar_o);
-      at_commit(&bar_vfree);
-      if (more) {
         ok = mbar_wait_bounded(&bar_o, i & 1, &g_err_at, ERR_AT_O);
         if (!ok) break;
         at_fence_after();
@@ -342,23 +377,22 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     constexpr float RESCALE_AT = 16.f;      // log2 headroom before half 1 re-bases
     int i = 0;
     int cur_h = -1;
-    for (int64_t t = blockIdx.x; t < nitems; t += gridDim.x, ++i) {
-      const int qt = static_cast<int>(t % QT);
-      const int h = static_cast<int>((t / QT) % heads);
-      const int64_t tok0 = (t / QT / heads) * S;
+    const int bj = (tid - 64) & (AT_KMAX - 1);  // this thread's key in the bias-table fill
+    const int bks = bj / Kc;
+    ItemPos it(blockIdx.x, gridDim.x, QT, batch);
+    for (int64_t t = blockIdx.x; t < nitems; t += gridDim.x, ++i, it.next()) {
+      const int qt = it.qt, h = it.h, blk = it.blk;
       const int q = qt * AT_QT + r;
       const uint32_t tO = tO0 + uint32_t(64 * (i & 1));
       if (h != cur_h) {  // bias table of this head (all softmax warps take the same items)
         soft_sync();
-        // the head's distance row and same-slot bias, one global load per thread, then
-        // the [query slot][key] table from shared memory
-        for (int k = tid - 64; k < nd; k += 32 * AT_SOFT_WARPS)
-          s_dist[k] = dist_bias[h * nd + k] + (k == B_max - 2 ? same_bias[h] : 0.f);
-        soft_sync();
-        for (int idx = tid - 64; idx < nq * AT_KMAX; idx += 32 * AT_SOFT_WARPS) {
-          const int qs = idx / AT_KMAX, j = idx % AT_KMAX;
-          s_btab[qs * AT_BSTRIDE + j] =
-              j < S ? s_dist[j / Kc - qs + B_max - 2] * AT_LOG2E : -INFINITY;
+        // thread: key bj, query slots of its parity; distance entries from L1
+        const float* drow = dist_bias + h * nd;
+        const float same = same_bias[h];
+        for (int qs = (tid - 64) / AT_KMAX; qs < nq; qs += 32 * AT_SOFT_WARPS / AT_KMAX) {
+          const int k = bks - qs + B_max - 2;
+          s_btab[qs * AT_BSTRIDE + bj] =
+              bj < S ? (__ldg(drow + k) + (k == B_max - 2 ? same : 0.f)) * AT_LOG2E : -INFINITY;
         }
         soft_sync();
         cur_h = h;
@@ -431,6 +465,8 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         mbar_arrive(half ? &bar_p1 : &bar_p0);
       }
       s_psum[hf][r] = l0 + l1;
+      // the quarter's previous output store has finished reading its staging rows
+      if (hf == 0 && lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
       quarter_sync(qq);
       float lsum = 0.f;
 #pragma unroll
@@ -443,21 +479,32 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       at_ld16(tO + lane_off + AT_OW * hf, v);
       at_fence_before();
       mbar_arrive(&bar_ofree[i & 1]);
-      if (q < S && ok) {
-        __nv_bfloat16* dst = out + (tok0 + q) * 2 * H + h * AT_DH + AT_OW * hf;
+      {
         uint32_t hi[AT_OW / 2], lo[AT_OW / 2];
 #pragma unroll
         for (int e = 0; e < AT_OW; e += 2) at_split2(v[e] * inv, v[e + 1] * inv, hi[e / 2], lo[e / 2]);
+        // this warp's 16 columns = 16-byte chunks 2hf, 2hf + 1 of the row's 128 bytes,
+        // at chunk ^ (row & 7) under the 128-byte swizzle
 #pragma unroll
         for (int u = 0; u < AT_OW / 8; ++u) {
-          *reinterpret_cast<uint4*>(dst + 8 * u) =
+          const int off = r * 128 + 16 * ((AT_OW / 8 * hf + u) ^ (r & 7));
+          *reinterpret_cast<uint4*>(sOh + off) =
               make_uint4(hi[4 * u], hi[4 * u + 1], hi[4 * u + 2], hi[4 * u + 3]);
-          *reinterpret_cast<uint4*>(dst + H + 8 * u) =
+          *reinterpret_cast<uint4*>(sOl + off) =
               make_uint4(lo[4 * u], lo[4 * u + 1], lo[4 * u + 2], lo[4 * u + 3]);
         }
       }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      quarter_sync(qq);
+      if (hf == 0 && lane == 0 && ok && qt * AT_QT + 32 * qq < S) {
+        at_store(&tmo, sOh + 32 * qq * 128, h * AT_DH, qt * AT_QT + 32 * qq, blk);
+        at_store(&tmo, sOl + 32 * qq * 128, H + h * AT_DH, qt * AT_QT + 32 * qq, blk);
+        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+      }
     }
   }
+  if (warp >= 2 && ((warp - 2) >> 2) == 0 && lane == 0)
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
   at_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -483,8 +530,11 @@ static PFN_cuTensorMapEncodeTiled_v12000 at_encode_fn() {
   return fn;
 }
 
-bool attention_tc_supported(int S, int H, int heads, int B_max) {
-  return H / heads == AT_DH && S >= 1 && S <= AT_KMAX && H % 64 == 0 && B_max <= 64;
+static int at_smem_bytes(int S, int K) { return AT_SMEM + (S / K) * AT_BSTRIDE * 4; }
+
+bool attention_tc_supported(int S, int K, int H, int heads, int B_max) {
+  return H / heads == AT_DH && S >= 1 && S <= AT_KMAX && K >= 1 && H % 64 == 0 &&
+         B_max <= 64 && at_smem_bytes(S, K) <= AT_SMEM_MAX;
 }
 
 cudaError_t launch_attention_tc(const __nv_bfloat16* qkv, int64_t batch, int S, int K, int H,
@@ -492,7 +542,7 @@ cudaError_t launch_attention_tc(const __nv_bfloat16* qkv, int64_t batch, int S, 
                                 const float* same_bias, __nv_bfloat16* out,
                                 cudaStream_t stream) {
   auto fn = at_encode_fn();
-  if (!fn || !attention_tc_supported(S, H, heads, B_max)) return cudaErrorInvalidValue;
+  if (!fn || !attention_tc_supported(S, K, H, heads, B_max)) return cudaErrorInvalidValue;
   const int64_t M = batch * S;
   CUtensorMap tm;
   const cuuint64_t dims[2] = {cuuint64_t(6 * H), cuuint64_t(M)};
@@ -503,7 +553,17 @@ cudaError_t launch_attention_tc(const __nv_bfloat16* qkv, int64_t batch, int S, 
          box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
-  const int smem = AT_SMEM + (S / K) * AT_BSTRIDE * 4;
+  // output [batch][S][2H] (hi | lo): 3-D so that a store box never runs into the next block
+  CUtensorMap tmo;
+  const cuuint64_t odims[3] = {cuuint64_t(2 * H), cuuint64_t(S), cuuint64_t(batch)};
+  const cuuint64_t ostrides[2] = {cuuint64_t(2 * H) * 2, cuuint64_t(S) * 2 * H * 2};
+  const cuuint32_t obox[3] = {64, 32, 1};
+  const cuuint32_t oestr[3] = {1, 1, 1};
+  if (fn(&tmo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, out, odims, ostrides, obox, oestr,
+         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+         CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  const int smem = at_smem_bytes(S, K);
   static int attr = 0;
   if (attr < smem) {
     cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -518,8 +578,8 @@ cudaError_t launch_attention_tc(const __nv_bfloat16* qkv, int64_t batch, int S, 
   }
   const int64_t nitems = batch * heads * ((S + AT_QT - 1) / AT_QT);
   const dim3 grid(static_cast<unsigned>(nitems < sms ? nitems : sms));
-  attn_tc_kernel<<<grid, AT_THREADS, smem, stream>>>(tm, S, K, H, B_max, heads, batch,
-                                                        dist_bias, same_bias, out);
+  attn_tc_kernel<<<grid, AT_THREADS, smem, stream>>>(tm, tmo, S, K, H, B_max, heads, batch,
+                                                        dist_bias, same_bias);
   note_launch();
   return cudaGetLastError();
 }

@@ -632,7 +632,7 @@ lilicorr_status lilicorr_rerank(const lilicorr_weights* w, const void* logits,
     g.out_split = qkv;
     LC_CUDA(launch_gemm(EPI_SPLIT, g, stream), "qkv gemm");
     MARK(T_QKV);
-    if (attention_tc_supported(S, H, d.heads, d.B_max))
+    if (attention_tc_supported(S, K, H, d.heads, d.B_max))
       LC_CUDA(launch_attention_tc(qkv, batch, S, K, H, d.heads, d.B_max, L.dist, L.same, act1,
                                   stream),
               "attention");
