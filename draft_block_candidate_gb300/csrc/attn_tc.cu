@@ -12,10 +12,11 @@
 //   warp 0     TMA: Q (128 x 64), K and V (256 x 64), each as bf16 hi and lo, 128-byte
 //              swizzle; the next item's Q and K load as soon as this item's S is formed,
 //              its V as soon as this item's second product is done; owns the TMEM
-//              allocation (S / P: 256 columns, O: 64 columns)
+//              allocation (S / P: 256 columns, O: 2 x 128 columns)
 //   warp 1     MMA, per item: S0 / S1 = Q K^T over key halves 0-127 / 128-255
-//              O = Ph Vh + Ph Vl + Pl Vh with P read from TMEM and V as an MN-major
-//              shared-memory operand
+//              O' = Ph [Vh | Vl] + Pl [Vh | Vl] (N 128: the hi and lo tiles of V are the two
+//              64-column atoms of one MN-major operand) with P read from TMEM;
+//              O = O'[:, 0:64] + O'[:, 64:128]
 //   warps 2-17 four warps per query-row quarter, each taking a quarter of the keys:
 //              pass 1 scales, adds the slot bias (a per-query-slot row of the head's
 //              bias table, -inf beyond the block; one 16-byte load per four keys) and
@@ -43,7 +44,7 @@ constexpr int AT_TILE = 128 * 64 * 2;  // one [128 x 64] bf16 swizzled tile
 constexpr int AT_SMEM = 12 * AT_TILE + 1024;  // + the bias table, sized per launch
 constexpr int AT_SMEM_MAX = 227 * 1024 - 8 * 1024;  // dynamic share (static use < 8 KB)
 constexpr int AT_BSTRIDE = AT_KMAX + 4;        // floats per bias-table row (bank offset)
-constexpr uint32_t AT_TMEM_COLS = 512, AT_O_COL = 256;
+constexpr uint32_t AT_TMEM_COLS = 512, AT_O_COL = 256, AT_O_W = 128;
 constexpr float AT_LOG2E = 1.4426950408889634f;
 
 enum AtErr : uint32_t {
@@ -85,6 +86,11 @@ __device__ __forceinline__ uint64_t at_desc(const void* p) {
   const uint64_t a = smem_addr(p);
   return ((a >> 4) & 0x3FFFull) | (1ull << 16) | ((1024ull >> 4) << 32) | (1ull << 46) |
          (2ull << 61);
+}
+// The same for an MN-major operand two atoms wide along N: [V hi | V lo], the lo tile
+// 2 * AT_TILE bytes after the hi tile (leading-dimension byte offset).
+__device__ __forceinline__ uint64_t at_desc_vhl(const void* p) {
+  return at_desc(p) & ~(0x3FFFull << 16) | (uint64_t((2 * AT_TILE) >> 4) << 16);
 }
 __device__ __forceinline__ void at_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
                                        uint32_t acc) {
@@ -230,7 +236,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   // [query slot][key]: (dist + same-slot bias) * log2(e) of the current head, -inf for
   // keys beyond the block
   float* s_btab = reinterpret_cast<float*>(sm + 12 * AT_TILE);
-  __shared__ __align__(8) uint64_t bar_qk, bar_qkfree, bar_v, bar_vfree, bar_s0, bar_s1,
+  __shared__ __align__(8) uint64_t bar_qk, bar_qkfree, bar_v[2], bar_vfree[2], bar_s0, bar_s1,
       bar_p0, bar_p1, bar_pv0, bar_o, bar_ofree[2];
   __shared__ uint32_t s_tmem;
   __shared__ float s_pmax[2][AT_NSPLIT][128], s_psum[AT_NSPLIT][128];
@@ -243,8 +249,10 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   if (tid == 0) {
     mbar_init(&bar_qk, 1);
     mbar_init(&bar_qkfree, 1);
-    mbar_init(&bar_v, 1);
-    mbar_init(&bar_vfree, 1);
+    mbar_init(&bar_v[0], 1);
+    mbar_init(&bar_v[1], 1);
+    mbar_init(&bar_vfree[0], 1);
+    mbar_init(&bar_vfree[1], 1);
     mbar_init(&bar_s0, 1);
     mbar_init(&bar_s1, 1);
     mbar_init(&bar_p0, 32 * AT_SOFT_WARPS);
@@ -266,7 +274,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   __syncthreads();
   at_fence_after();
   const uint32_t tmem = s_tmem;
-  // S / P of key half 0 in columns 0-127, of half 1 in 128-255; O of even / odd items in
+  // S / P of key half 0 in columns 0-127, of half 1 in 128-255; O' of even / odd items in
   // 256-319 / 320-383
   const uint32_t tS = tmem, tO0 = tmem + AT_O_COL;
 
@@ -286,12 +294,18 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       at_tma(sKh + AT_TILE, &tm, ck, tok0 + 128, &bar_qk);
       at_tma(sKl, &tm, lo + ck, tok0, &bar_qk);
       at_tma(sKl + AT_TILE, &tm, lo + ck, tok0 + 128, &bar_qk);
-      if (i > 0 && !mbar_wait_bounded(&bar_vfree, (i - 1) & 1, &g_err_at, ERR_AT_VFREE)) break;
-      mbar_arrive_expect_tx(&bar_v, 4 * AT_TILE);
-      at_tma(sVh, &tm, cv, tok0, &bar_v);
-      at_tma(sVh + AT_TILE, &tm, cv, tok0 + 128, &bar_v);
-      at_tma(sVl, &tm, lo + cv, tok0, &bar_v);
-      at_tma(sVl + AT_TILE, &tm, lo + cv, tok0 + 128, &bar_v);
+      // V by key halves: half 0 is free once the previous item's first product is done
+      bool vok = true;
+      for (int vh = 0; vh < 2 && vok; ++vh) {
+        if (i > 0 && !mbar_wait_bounded(&bar_vfree[vh], (i - 1) & 1, &g_err_at, ERR_AT_VFREE)) {
+          vok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&bar_v[vh], 2 * AT_TILE);
+        at_tma(sVh + vh * AT_TILE, &tm, cv, tok0 + 128 * vh, &bar_v[vh]);
+        at_tma(sVl + vh * AT_TILE, &tm, lo + cv, tok0 + 128 * vh, &bar_v[vh]);
+      }
+      if (!vok) break;
     }
   } else if (warp == 1 && lane == 0) {
     // ---- MMA issuer.  Per item i: S0 = Q K[0:128]^T, S1 = Q K[128:256]^T (three-term
@@ -299,7 +313,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     // next item's S0 (over P0, once PV0 has completed) and S1 (once PV1 has), which run
     // while the softmax warps finish this item's epilogue.
     constexpr uint32_t id_s = at_idesc(128, 128, false);
-    constexpr uint32_t id_o = at_idesc(128, 64, true);
+    constexpr uint32_t id_o = at_idesc(128, 128, true);
     auto qk_half = [&](int half) {
       const uint32_t d = tS + uint32_t(128 * half);
       uint8_t* kh = sKh + half * AT_TILE;
@@ -318,10 +332,9 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       for (int jj = 0; jj < 8; ++jj) {
         const int j = 8 * half + jj;
         const uint32_t pc = uint32_t(32 * (j >> 1) + 8 * (j & 1));
-        const uint64_t vh = at_desc(sVh + 16 * j * 128), vl = at_desc(sVl + 16 * j * 128);
-        at_mma_ts(tO, tS + pc, vh, id_o, (half > 0 || jj > 0));
-        at_mma_ts(tO, tS + pc, vl, id_o, 1);
-        at_mma_ts(tO, tS + pc + 16, vh, id_o, 1);
+        const uint64_t vhl = at_desc_vhl(sVh + 16 * j * 128);
+        at_mma_ts(tO, tS + pc, vhl, id_o, (half > 0 || jj > 0));
+        at_mma_ts(tO, tS + pc + 16, vhl, id_o, 1);
       }
     };
     bool ok = mbar_wait_bounded(&bar_qk, 0, &g_err_at, ERR_AT_QK);
@@ -336,21 +349,23 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     int i = 0;
     for (int64_t t = blockIdx.x; t < nitems && ok; t += gridDim.x, ++i) {
       const bool more = t + gridDim.x < nitems;
-      const uint32_t tO = tO0 + uint32_t(64 * (i & 1));
+      const uint32_t tO = tO0 + AT_O_W * uint32_t(i & 1);
       ok = mbar_wait_bounded(&bar_p0, i & 1, &g_err_at, ERR_AT_P) &&
-           mbar_wait_bounded(&bar_v, i & 1, &g_err_at, ERR_AT_V) &&
+           mbar_wait_bounded(&bar_v[0], i & 1, &g_err_at, ERR_AT_V) &&
            (i < 2 || mbar_wait_bounded(&bar_ofree[i & 1], ((i >> 1) - 1) & 1, &g_err_at,
                                        ERR_AT_OFREE));
       if (!ok) break;
       at_fence_after();
       pv_half(0, tO);
       at_commit(&bar_pv0);
-      ok = mbar_wait_bounded(&bar_p1, i & 1, &g_err_at, ERR_AT_P);
+      at_commit(&bar_vfree[0]);
+      ok = mbar_wait_bounded(&bar_p1, i & 1, &g_err_at, ERR_AT_P) &&
+           mbar_wait_bounded(&bar_v[1], i & 1, &g_err_at, ERR_AT_V);
       if (!ok) break;
       at_fence_after();
       pv_half(1, tO);
       at_commit(&bar_o);
-      at_commit(&bar_vfree);
+      at_commit(&bar_vfree[1]);
       if (more) {
         // S0 of the next item overwrites P0: after PV0 has completed
         ok = mbar_wait_bounded(&bar_pv0, i & 1, &g_err_at, ERR_AT_O) &&
@@ -379,11 +394,47 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     int cur_h = -1;
     const int bj = (tid - 64) & (AT_KMAX - 1);  // this thread's key in the bias-table fill
     const int bks = bj / Kc;
+    // Epilogue of item pi: O / l for this warp's 16 of the 64 output columns, split,
+    // staged, stored by one thread per quarter.
+    int p_qt = 0, p_h = 0, p_blk = 0;
+    float p_inv = 0.f;
+    bool p_ok = false;
+    auto epilogue = [&](int pi) {
+      const uint32_t tOp = tO0 + AT_O_W * uint32_t(pi & 1);
+      const bool ok2 = mbar_wait_bounded(&bar_o, pi & 1, &g_err_at, ERR_AT_O) && p_ok;
+      at_fence_after();
+      float v[AT_OW], vl[AT_OW];
+      at_ld16(tOp + lane_off + AT_OW * hf, v);
+      at_ld16(tOp + lane_off + 64 + AT_OW * hf, vl);
+      at_fence_before();
+      mbar_arrive(&bar_ofree[pi & 1]);
+      uint32_t hi[AT_OW / 2], lo[AT_OW / 2];
+#pragma unroll
+      for (int e = 0; e < AT_OW; e += 2)
+        at_split2((v[e] + vl[e]) * p_inv, (v[e + 1] + vl[e + 1]) * p_inv, hi[e / 2], lo[e / 2]);
+      // this warp's 16 columns = 16-byte chunks 2hf, 2hf + 1 of the row's 128 bytes, at
+      // chunk ^ (row & 7) under the 128-byte swizzle
+#pragma unroll
+      for (int u = 0; u < AT_OW / 8; ++u) {
+        const int off = r * 128 + 16 * ((AT_OW / 8 * hf + u) ^ (r & 7));
+        *reinterpret_cast<uint4*>(sOh + off) =
+            make_uint4(hi[4 * u], hi[4 * u + 1], hi[4 * u + 2], hi[4 * u + 3]);
+        *reinterpret_cast<uint4*>(sOl + off) =
+            make_uint4(lo[4 * u], lo[4 * u + 1], lo[4 * u + 2], lo[4 * u + 3]);
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      quarter_sync(qq);
+      if (hf == 0 && lane == 0 && ok2 && p_qt * AT_QT + 32 * qq < S) {
+        at_store(&tmo, sOh + 32 * qq * 128, p_h * AT_DH, p_qt * AT_QT + 32 * qq, p_blk);
+        at_store(&tmo, sOl + 32 * qq * 128, H + p_h * AT_DH, p_qt * AT_QT + 32 * qq, p_blk);
+        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+      }
+    };
     ItemPos it(blockIdx.x, gridDim.x, QT, batch);
     for (int64_t t = blockIdx.x; t < nitems; t += gridDim.x, ++i, it.next()) {
       const int qt = it.qt, h = it.h, blk = it.blk;
       const int q = qt * AT_QT + r;
-      const uint32_t tO = tO0 + uint32_t(64 * (i & 1));
+      const uint32_t tO = tO0 + AT_O_W * uint32_t(i & 1);
       if (h != cur_h) {  // bias table of this head (all softmax warps take the same items)
         soft_sync();
         // thread: key bj, query slots of its parity; distance entries from L1
@@ -439,11 +490,14 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
             l0 *= sc;
             mbar_wait_bounded(&bar_pv0, i & 1, &g_err_at, ERR_AT_O);
             at_fence_after();
-            float o[AT_OW];
-            at_ld16(tO + lane_off + AT_OW * hf, o);
 #pragma unroll
-            for (int e = 0; e < AT_OW; ++e) o[e] *= sc;
-            at_st16f(tO + lane_off + AT_OW * hf, o);
+            for (int part = 0; part < 2; ++part) {
+              float o[AT_OW];
+              at_ld16(tO + lane_off + 64 * part + AT_OW * hf, o);
+#pragma unroll
+              for (int e = 0; e < AT_OW; ++e) o[e] *= sc;
+              at_st16f(tO + lane_off + 64 * part + AT_OW * hf, o);
+            }
           }
         }
         float2 l2 = make_float2(0.f, 0.f);
@@ -471,36 +525,12 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       float lsum = 0.f;
 #pragma unroll
       for (int k = 0; k < AT_NSPLIT; ++k) lsum += s_psum[k][r];
-      const float inv = 1.0f / lsum;
-      // epilogue: O / l for this warp's 16 of the 64 output columns, split, stored
-      ok = mbar_wait_bounded(&bar_o, i & 1, &g_err_at, ERR_AT_O) && ok;
-      at_fence_after();
-      float v[AT_OW];
-      at_ld16(tO + lane_off + AT_OW * hf, v);
-      at_fence_before();
-      mbar_arrive(&bar_ofree[i & 1]);
-      {
-        uint32_t hi[AT_OW / 2], lo[AT_OW / 2];
-#pragma unroll
-        for (int e = 0; e < AT_OW; e += 2) at_split2(v[e] * inv, v[e + 1] * inv, hi[e / 2], lo[e / 2]);
-        // this warp's 16 columns = 16-byte chunks 2hf, 2hf + 1 of the row's 128 bytes,
-        // at chunk ^ (row & 7) under the 128-byte swizzle
-#pragma unroll
-        for (int u = 0; u < AT_OW / 8; ++u) {
-          const int off = r * 128 + 16 * ((AT_OW / 8 * hf + u) ^ (r & 7));
-          *reinterpret_cast<uint4*>(sOh + off) =
-              make_uint4(hi[4 * u], hi[4 * u + 1], hi[4 * u + 2], hi[4 * u + 3]);
-          *reinterpret_cast<uint4*>(sOl + off) =
-              make_uint4(lo[4 * u], lo[4 * u + 1], lo[4 * u + 2], lo[4 * u + 3]);
-        }
-      }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      quarter_sync(qq);
-      if (hf == 0 && lane == 0 && ok && qt * AT_QT + 32 * qq < S) {
-        at_store(&tmo, sOh + 32 * qq * 128, h * AT_DH, qt * AT_QT + 32 * qq, blk);
-        at_store(&tmo, sOl + 32 * qq * 128, H + h * AT_DH, qt * AT_QT + 32 * qq, blk);
-        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-      }
+      p_inv = 1.0f / lsum;
+      p_qt = qt;
+      p_h = h;
+      p_blk = blk;
+      p_ok = ok;
+      epilogue(i);
     }
   }
   if (warp >= 2 && ((warp - 2) >> 2) == 0 && lane == 0)
