@@ -46,7 +46,8 @@ constexpr int TC_STG_BYTES = 4096;  // one 32 x 32 output chunk (f32, or bf16 hi
 // Shared memory of a configuration: operand ring of ST stages + NB epilogue staging
 // buffers per warp.  A stage holds one 64-wide K block of A and of W, or, for a split
 // operand (pair), the A_hi and A_lo blocks that share one W block.  Configurations in
-// use: 4 plain stages or 3 paired stages, with 1 staging buffer per epilogue warp.
+// use: 4 plain stages or 3 paired stages with 1 staging buffer per epilogue warp, 2 paired
+// stages with 2 (node sum) or with 16 epilogue warps (short-K SiLU).
 __host__ __device__ constexpr int tc_smem(int st, int nb, bool pair, int ew = TC_EPI_WARPS) {
   return st * ((pair ? 2 : 1) * TC_A_BYTES + TC_B_BYTES) + ew * nb * TC_STG_BYTES + 1024;
 }
@@ -181,7 +182,55 @@ __device__ __forceinline__ uint32_t pack2(__nv_bfloat16 a, __nv_bfloat16 b) {
 // Node epilogue terms of row m, columns n..n+31: v (the accumulator) += bias + E[cand]
 // + slot_table[s-1] + rank_table[k] (+ drafter hidden); the optional tap is written here,
 // X by the staged f32 store.
-__device__ __forceinline__ void tc_node_terms(const GemmArgs& g, int64_t m, int n, float (&v)[32]) {
+// Node sum of step a2 for one row: the row's gather sources, found once per tile.
+struct NodeRow {
+  const __nv_bfloat16* e;  // E[cand] row
+  const __nv_bfloat16* h;  // drafter hidden row of the slot, or null
+  const float* st;         // slot-table row
+  const float* rk;         // rank-table row
+};
+__device__ __forceinline__ NodeRow tc_node_row(const GemmArgs& g, int64_t m) {
+  const int S = (g.B - 1) * g.K;
+  const int64_t b = m / S;
+  const int t = static_cast<int>(m - b * S);
+  const int slot = t / g.K + 1, k = t - (slot - 1) * g.K;
+  int64_t id = g.cand_id[m];
+  id = id < 0 ? 0 : (id >= g.vocab ? g.vocab - 1 : id);
+  NodeRow r;
+  r.e = g.embed + id * g.N;
+  r.h = g.slot_hidden ? g.slot_hidden + (b * g.B + slot) * g.N : nullptr;
+  r.st = g.slot_table + int64_t(slot - 1) * g.N;
+  r.rk = g.rank_table + int64_t(k) * g.N;
+  return r;
+}
+// The row's bf16 gathers of columns n..n+31 (issued before the accumulator is read).
+__device__ __forceinline__ void tc_node_gather(const NodeRow& r, int n, uint4 (&ge)[4],
+                                               uint4 (&gh)[4]) {
+  const uint4* e4 = reinterpret_cast<const uint4*>(r.e + n);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) ge[j] = __ldg(e4 + j);
+  if (r.h) {
+    const uint4* h4 = reinterpret_cast<const uint4*>(r.h + n);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) gh[j] = __ldg(h4 + j);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) gh[j] = make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+__device__ __forceinline__ void tc_add_bf16x8(float* v, const uint4& e) {
+  const uint32_t ew[4] = {e.x, e.y, e.z, e.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    v[2 * q] += __uint_as_float(ew[q] << 16);
+    v[2 * q + 1] += __uint_as_float(ew[q] & 0xffff0000u);
+  }
+}
+// v[0..31] = accumulator columns n..n+31 of row m: + bias + E[cand] + slot + rank +
+// drafter hidden, in that order.
+__device__ __forceinline__ void tc_node_terms(const GemmArgs& g, const NodeRow& r, int64_t m,
+                                              int n, float (&v)[32], const uint4 (&ge)[4],
+                                              const uint4 (&gh)[4]) {
 #pragma unroll
   for (int j = 0; j < 32; j += 4) {
     const float4 b4 = __ldg(reinterpret_cast<const float4*>(g.bias + n + j));
@@ -190,53 +239,27 @@ __device__ __forceinline__ void tc_node_terms(const GemmArgs& g, int64_t m, int 
     v[j + 2] += b4.z;
     v[j + 3] += b4.w;
   }
-  {
-    const int S = (g.B - 1) * g.K;
-    const int64_t b = m / S;
-    const int t = static_cast<int>(m % S);
-    const int slot = t / g.K + 1, k = t % g.K;
-    int64_t id = g.cand_id[m];
-    id = id < 0 ? 0 : (id >= g.vocab ? g.vocab - 1 : id);
-    const uint4* e4 = reinterpret_cast<const uint4*>(g.embed + id * g.N + n);
-    const float4* st4 = reinterpret_cast<const float4*>(g.slot_table + int64_t(slot - 1) * g.N + n);
-    const float4* rk4 = reinterpret_cast<const float4*>(g.rank_table + int64_t(k) * g.N + n);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint4 e = __ldg(e4 + j);
-      const uint32_t ew[4] = {e.x, e.y, e.z, e.w};
+  for (int j = 0; j < 4; ++j) tc_add_bf16x8(v + 8 * j, ge[j]);
+  const float4* st4 = reinterpret_cast<const float4*>(r.st + n);
+  const float4* rk4 = reinterpret_cast<const float4*>(r.rk + n);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        v[8 * j + 2 * q] += __uint_as_float(ew[q] << 16);
-        v[8 * j + 2 * q + 1] += __uint_as_float(ew[q] & 0xffff0000u);
-      }
-    }
+  for (int j = 0; j < 8; ++j) {
+    const float4 a = __ldg(st4 + j), c = __ldg(rk4 + j);
+    v[4 * j] += a.x + c.x;
+    v[4 * j + 1] += a.y + c.y;
+    v[4 * j + 2] += a.z + c.z;
+    v[4 * j + 3] += a.w + c.w;
+  }
+  if (r.h) {
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const float4 a = __ldg(st4 + j), c = __ldg(rk4 + j);
-      v[4 * j] += a.x + c.x;
-      v[4 * j + 1] += a.y + c.y;
-      v[4 * j + 2] += a.z + c.z;
-      v[4 * j + 3] += a.w + c.w;
-    }
-    if (g.slot_hidden) {
-      const uint4* h4 = reinterpret_cast<const uint4*>(g.slot_hidden + (b * g.B + slot) * g.N + n);
+    for (int j = 0; j < 4; ++j) tc_add_bf16x8(v + 8 * j, gh[j]);
+  }
+  // X itself leaves through the staged f32 store; only the optional tap is written here
+  if (g.nodes_tap) {
+    float4* tp = reinterpret_cast<float4*>(g.nodes_tap + m * g.N + n);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint4 e = __ldg(h4 + j);
-        const uint32_t ew[4] = {e.x, e.y, e.z, e.w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          v[8 * j + 2 * q] += __uint_as_float(ew[q] << 16);
-          v[8 * j + 2 * q + 1] += __uint_as_float(ew[q] & 0xffff0000u);
-        }
-      }
-    }
-    // X itself leaves through the staged f32 store; only the optional tap is written here
-    if (g.nodes_tap) {
-      float4* tp = reinterpret_cast<float4*>(g.nodes_tap + m * g.N + n);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) tp[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-    }
+    for (int j = 0; j < 8; ++j) tp[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
   }
 }
 
@@ -423,25 +446,40 @@ __global__ void __launch_bounds__(32 * (2 + EW), 1)
       const int buf = i & 1;
       const int64_t m0 = int64_t(t / NT) * TC_BM;
       const int n0 = (t % NT) * TC_BN;
+      const int64_t m = m0 + 32 * q + lane;
+      // node sum: the row's gather sources before the accumulator is waited for
+      NodeRow nr{};
+      const bool mrow = m < g.M;
+      if constexpr (EPI == EPI_NODE) {
+        if (mrow) nr = tc_node_row(g, m);
+      }
       if (!mbar_wait_bounded(&acc_full[buf], (i >> 1) & 1, &g_err_tc, ERR_TC_ACCUM)) break;
       tc_fence_after();
-      const int64_t m = m0 + 32 * q + lane;
 #pragma unroll 1
       for (int cc = half * CPP; cc < (half + 1) * CPP; ++cc) {
         float v[32];
-        tmem_ld32(tmem + (uint32_t(32 * q) << 16) + uint32_t(buf * TC_BN + cc * 32), v);
         const int n = n0 + cc * 32;
         if constexpr (EPI == EPI_NODE) {
-          // gathers and sums per row (bias included), then the staged f32 store of X
-          if (m < g.M && n < g.N) tc_node_terms(g, m, n, v);
+          // DRAM gathers first, then the accumulator, the sums and the staged f32 store
+          uint4 ge[4], gh[4];
+          const bool live = mrow && n < g.N;
+          if (live) tc_node_gather(nr, n, ge, gh);
+          tmem_ld32(tmem + (uint32_t(32 * q) << 16) + uint32_t(buf * TC_BN + cc * 32), v);
+          if (live) tc_node_terms(g, nr, m, n, v, ge, gh);
           if (n < g.N) {
-            if (lane == 0) bulk_wait_read0();
+            if (lane == 0) {
+              if constexpr (TC_STG_BUFS == 2)
+                bulk_wait_read1();
+              else
+                bulk_wait_read0();
+            }
             __syncwarp();
             tc_epilogue_staged<EPI_F32, false>(g, &tmC, stg + sb * TC_STG_BYTES, lane,
                                                m0 + 32 * q, n, v);
             sb = (sb + 1) % TC_STG_BUFS;
           }
         } else if (n < g.N) {
+          tmem_ld32(tmem + (uint32_t(32 * q) << 16) + uint32_t(buf * TC_BN + cc * 32), v);
           // the buffer's previous bulk copy must have finished reading it
           if (lane == 0) {
             if constexpr (TC_STG_BUFS == 2)
@@ -538,20 +576,21 @@ cudaError_t launch_gemm(int epi, const GemmArgs& g, cudaStream_t stream) {
   // A split operand (Ka = 2 Kw) runs paired stages: A_hi and A_lo share one W block.
   // Measured per epilogue at the high-concurrency sizes: the node sum (embedding-row
   // gathers) runs faster with 2 paired stages in flight than with 3 (less operand traffic
-  // competing with its gathers); the others with 3.
+  // competing with its gathers), with two staging buffers per epilogue warp; the others
+  // with 3 stages.
   const bool pair = g.Ka == 2 * g.Kw;
   // The SiLU epilogue of short K (FFN1) is the longest epilogue per MMA: it runs 16
   // epilogue warps (2 paired stages leave room for their staging buffers).
   const bool wide = epi == EPI_SPLIT_SILU && g.Ka <= 512;
   const bool two = epi == EPI_NODE;
-  constexpr int sp = tc_smem(3, 1, true), sp2 = tc_smem(2, 1, true), sn = tc_smem(4, 1, false);
+  constexpr int sp = tc_smem(3, 1, true), sp2 = tc_smem(2, 2, true), sn = tc_smem(4, 1, false);
   constexpr int sw = tc_smem(2, 1, true, 16);
   static bool attr = false;
   if (!attr) {
 #define LC_TC_ATTR(E)                                                                        \
   cudaFuncSetAttribute(gemm_tc_kernel<E, 3, 1, true>,                                        \
                        cudaFuncAttributeMaxDynamicSharedMemorySize, sp);                     \
-  cudaFuncSetAttribute(gemm_tc_kernel<E, 2, 1, true>,                                        \
+  cudaFuncSetAttribute(gemm_tc_kernel<E, 2, 2, true>,                                        \
                        cudaFuncAttributeMaxDynamicSharedMemorySize, sp2);                    \
   cudaFuncSetAttribute(gemm_tc_kernel<E, 2, 1, true, 16>,                                    \
                        cudaFuncAttributeMaxDynamicSharedMemorySize, sw);                     \
@@ -578,7 +617,7 @@ cudaError_t launch_gemm(int epi, const GemmArgs& g, cudaStream_t stream) {
   if (pair && wide)                                                                          \
     gemm_tc_kernel<E, 2, 1, true, 16><<<grid, 32 * 18, sw, stream>>>(ta, tb, tc, g);         \
   else if (pair && two)                                                                      \
-    gemm_tc_kernel<E, 2, 1, true><<<grid, TC_THREADS, sp2, stream>>>(ta, tb, tc, g);         \
+    gemm_tc_kernel<E, 2, 2, true><<<grid, TC_THREADS, sp2, stream>>>(ta, tb, tc, g);         \
   else if (pair)                                                                             \
     gemm_tc_kernel<E, 3, 1, true><<<grid, TC_THREADS, sp, stream>>>(ta, tb, tc, g);          \
   else                                                                                       \
