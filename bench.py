@@ -375,12 +375,13 @@ def run_gb300(a):
                   "ffn1_gemm": 2 * M * F * 2 * H, "ffn2_gemm": 2 * M * H * 2 * F,
                   "node_gemm": 2 * M * H * 2 * H, "fuse_gemm": 2 * M * H * 4 * H,
                   "heads_gemm": 2 * M * 2 * E * 2 * H}
-    # attention: executed tensor work per launch (three-term split products, 128-query
-    # tiles, 256 key columns): S = Q K^T and O = P V
+    # attention: executed tensor work per launch (128-query tiles, 256 key columns):
+    # S = Q K^T as three split products, O' = P [V_hi | V_lo] as two products of width 2 dh
     import math
     nh = wl.dims["heads"]
     dh = H // nh
-    gemm_flops["attention"] = batch * nh * math.ceil(S / 128) * 2 * (3 * 2 * 128 * 256 * dh)
+    gemm_flops["attention"] = batch * nh * math.ceil(S / 128) * (
+        3 * 2 * 128 * 256 * dh + 2 * 2 * 128 * 256 * 2 * dh)
     k1 = per_kernel["logit_pass"]
     k1_gbs = logit_bytes / (k1["avg_launch_us"] * 1e-6) / 1e9
     logit_pass = {"achieved": k1_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
