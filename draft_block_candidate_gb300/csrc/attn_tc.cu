@@ -11,9 +11,10 @@
 // once), 18 warps:
 //   warp 0     TMA: Q (128 x 64), K and V (256 x 64), each as bf16 hi and lo, 128-byte
 //              swizzle; the next item's Q and K load as soon as this item's S is formed,
-//              its V as soon as this item's second product is done; owns the TMEM
-//              allocation (S / P: 256 columns, O: 2 x 128 columns)
-//   warp 1     MMA, per item: S0 / S1 = Q K^T over key halves 0-127 / 128-255
+//              each key half of its V as soon as this item's product over that half is
+//              done; owns the TMEM allocation (S / P: 256 columns, O': 2 x 128 columns)
+//   warp 1     MMA, per item: S0 / S1 = Q K^T over key halves 0-127 / 128-255 (three
+//              split products), then both P V halves, then the next item's S0 and S1
 //              O' = Ph [Vh | Vl] + Pl [Vh | Vl] (N 128: the hi and lo tiles of V are the two
 //              64-column atoms of one MN-major operand) with P read from TMEM;
 //              O = O'[:, 0:64] + O'[:, 64:128]
