@@ -92,6 +92,9 @@ SMALL = [  # name, overrides
     ("single", dict(V=4096, batch=2, with_slot_hidden=True)),
     ("single", dict(V=4096, batch=1, with_target=False, with_anchor=False)),
     ("highconc", dict(V=2048, batch=5, K=1)),
+    ("single", dict(V=2048, batch=2, B=26)),         # 25 query slots: the largest bias
+                                                     # table of the tcgen05 attention
+    ("single", dict(V=2048, batch=2, B=27)),         # 26: the mma.sync attention instead
 ]
 
 
