@@ -200,34 +200,6 @@ WsPlan ws_plan(const lilicorr_dims& d, int64_t batch, int B, int K, int esize) {
   return p;
 }
 
-// Helper stream for work of a call that depends on neither the logit pass nor the
-// encoder (the per-block target terms): forked from the caller's stream when the call
-// starts and joined back before its result is needed.  One per host thread and device, so
-// the fork / join events of calls from different threads never interleave.
-struct AuxStream {
-  cudaStream_t s = nullptr;
-  cudaEvent_t fork = nullptr, join = nullptr;
-};
-cudaError_t aux_stream(AuxStream** out) {
-  constexpr int kMaxDev = 64;
-  static thread_local AuxStream per_dev[kMaxDev];
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
-  AuxStream& a = per_dev[dev];
-  if (!a.s) {
-    AuxStream n;
-    e = cudaStreamCreateWithFlags(&n.s, cudaStreamNonBlocking);
-    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&n.fork, cudaEventDisableTiming);
-    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&n.join, cudaEventDisableTiming);
-    if (e != cudaSuccess) return e;
-    a = n;
-  }
-  *out = &a;
-  return cudaSuccess;
-}
-
 lilicorr_status check_call(const lilicorr_weights* w, lilicorr_dtype ldtype, int64_t batch,
                            int32_t B, int64_t V, int32_t K) {
   if (!w) return LILICORR_ERR_INVALID_ARG;
@@ -634,23 +606,6 @@ lilicorr_status lilicorr_rerank(const lilicorr_weights* w, const void* logits,
   CallTimer tm;
   LC_CUDA(tm.begin(stream), "timing event");
 #define MARK(slot) LC_CUDA(tm.mark(slot), "timing event")
-  // per-block target terms [Wt t + bf | Wa t + ba], one row per block, on the helper
-  // stream: they need only the inputs, and run beside the logit pass
-  float* tgt = reinterpret_cast<float*>(ws + pl.tgt);
-  const int HE = static_cast<int>(H + E);
-  AuxStream* aux = nullptr;
-  LC_CUDA(aux_stream(&aux), "helper stream");
-  LC_CUDA(cudaEventRecord(aux->fork, stream), "helper stream fork");
-  LC_CUDA(cudaStreamWaitEvent(aux->s, aux->fork, 0), "helper stream fork");
-  if (target) {
-    GemmArgs g{};
-    g.A = target; g.W = w->tgt_w; g.M = batch; g.N = HE; g.Kw = H; g.Ka = H; g.bias = w->tgt_b;
-    g.out = tgt;
-    LC_CUDA(launch_gemm(EPI_F32, g, aux->s), "target terms gemm");
-  } else {
-    LC_CUDA(launch_rows_bias(w->tgt_b, batch, HE, tgt, aux->s), "target terms");
-  }
-  LC_CUDA(cudaEventRecord(aux->join, aux->s), "helper stream join");
   // a1: logit pass
   LC_CUDA(k1_launch(logits, es, batch, B, V, K, cand_id, cand_logit, lse, ws + pl.k1, stream),
           "logit pass");
@@ -703,8 +658,18 @@ lilicorr_status lilicorr_rerank(const lilicorr_weights* w, const void* logits,
   if (tp.hidden)
     LC_CUDA(cudaMemcpyAsync(tp.hidden, X, size_t(M) * H * 4, cudaMemcpyDeviceToDevice, stream),
             "hidden tap");
-  // a4: fusion and heads (the target terms joined back first)
-  LC_CUDA(cudaStreamWaitEvent(stream, aux->join, 0), "helper stream join");
+  // a4: fusion and heads
+  // per-block target terms [Wt t + bf | Wa t + ba], one row per block
+  float* tgt = reinterpret_cast<float*>(ws + pl.tgt);
+  const int HE = static_cast<int>(H + E);
+  if (target) {
+    GemmArgs g{};
+    g.A = target; g.W = w->tgt_w; g.M = batch; g.N = HE; g.Kw = H; g.Ka = H; g.bias = w->tgt_b;
+    g.out = tgt;
+    LC_CUDA(launch_gemm(EPI_F32, g, stream), "target terms gemm");
+  } else {
+    LC_CUDA(launch_rows_bias(w->tgt_b, batch, HE, tgt, stream), "target terms");
+  }
   LC_CUDA(launch_fuse_concat(X, target, S, M, H, qkv, stream), "fusion input");
   MARK(T_FUSECAT);
   {

@@ -17,9 +17,7 @@
  *   - Device pointers are caller-owned CUDA device memory, contiguous, row-major.
  *   - `stream` is a cudaStream_t passed as void*; NULL means the legacy default stream.
  *     Device entry points only enqueue work on `stream`: they never allocate and never
- *     synchronise, so a call can be captured in a CUDA graph (lilicorr_rerank also runs
- *     a small part on a helper stream that it forks from and joins back into `stream`
- *     within the call; see there).
+ *     synchronise, so a call can be captured in a CUDA graph.
  *   - All arguments are checked on the host before any launch; a violation returns an
  *     error status and launches nothing.  A failed launch returns LILICORR_ERR_CUDA
  *     (lilicorr_last_error() has the CUDA message).  No device-side trap is used.
@@ -113,11 +111,7 @@ typedef struct {
   float* anchor_vec;    /* [batch,d_e]      unit anchor out vector o_0                   */
 } lilicorr_taps;
 
-/* The whole rerank on `stream`.  The per-block target terms, which need only the inputs,
- * run beside the logit pass on a helper stream of the calling host thread (one per thread
- * and device, created by the thread's first call: make that call before any stream
- * capture), forked from `stream` at the start of the call and joined back before the
- * fusion; a captured call records the fork and join as graph dependencies.
+/* The whole rerank on `stream`.
  *   logits       [batch,B,V] of ldtype (F32 or BF16); row 0 of each block (the anchor
  *                position) is not read.  Rows need only element alignment.
  *   B            2 <= B <= dims.B_max;  V == dims.V;  1 <= K <= min(dims.K_max, V)
