@@ -80,7 +80,8 @@ cudaError_t launch_rmsnorm_split(const float* X, const float* gain, int64_t M, i
 cudaError_t launch_attention(const __nv_bfloat16* qkv, int64_t batch, int S, int K, int H,
                              int heads, int B_max, const float* dist_bias,
                              const float* same_bias, __nv_bfloat16* out, cudaStream_t stream);
-// tcgen05 attention for head dim 64 and up to 256 tokens (attn_tc.cu)
+// tcgen05 attention for head dim 64, up to 256 tokens and a per-query-slot bias table
+// that fits beside its operand tiles (S / K <= 25 query slots) (attn_tc.cu)
 bool attention_tc_supported(int S, int K, int H, int heads, int B_max);
 cudaError_t launch_attention_tc(const __nv_bfloat16* qkv, int64_t batch, int S, int K, int H,
                                 int heads, int B_max, const float* dist_bias,
