@@ -159,9 +159,6 @@ __device__ __forceinline__ float at_ex2(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
-__device__ __forceinline__ uint32_t at_pack(__nv_bfloat16 a, __nv_bfloat16 b) {
-  return uint32_t(__bfloat16_as_ushort(a)) | (uint32_t(__bfloat16_as_ushort(b)) << 16);
-}
 
 // idesc kind::f16, f32 D, bf16 A/B; b_mn selects an MN-major B operand.
 __host__ __device__ constexpr uint32_t at_idesc(int M, int N, bool b_mn) {
