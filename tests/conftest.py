@@ -32,3 +32,29 @@ def oracle_inputs(wl):
 @pytest.fixture(scope="session")
 def rng():
     return np.random.default_rng(1234)
+
+
+def pytest_sessionfinish(session, exitstatus):
+    """Write the GPU parity record (tests/gpu_util.REPORT) when GPU parity tests ran:
+    per workload the blocks compared, the smallest oracle decision margin, the largest
+    score and lse differences and every token divergence.  Path: $LILICORR_PARITY_REPORT,
+    else tests/parity_report.json."""
+    gu = sys.modules.get("tests.gpu_util")
+    if gu is None or not getattr(gu, "REPORT", None):
+        return
+    import json
+    path = os.environ.get("LILICORR_PARITY_REPORT",
+                          os.path.join(ROOT, "tests", "parity_report.json"))
+    rep = {}
+    for label, r in sorted(gu.REPORT.items()):
+        r = dict(r)
+        if r.get("min_margin") == float("inf"):
+            r["min_margin"] = None
+        rep[label] = r
+    total = {"blocks": sum(r["blocks"] for r in rep.values()),
+             "decisions": sum(r.get("decisions", 0) for r in rep.values()),
+             "tie_ambiguous": sum(r.get("tie_ambiguous", 0) for r in rep.values()),
+             "pytest_exit_status": int(exitstatus)}
+    with open(path, "w") as f:
+        json.dump({"total": total, "workloads": rep}, f, indent=1, sort_keys=True)
+        f.write("\n")

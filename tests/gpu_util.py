@@ -36,9 +36,30 @@ def oracle_block(wl, b, mirror=False):
                           None if wl.anchor_ids is None else int(wl.anchor_ids[b]), mirror)
 
 
+# Parity record of the session, per workload label: blocks compared, greedy decisions, the
+# smallest oracle top-2 margin over them, the largest |dscore| and |dlse|, and every near
+# tie (a decision where the GPU took a candidate within twice the block's measured
+# |dscore| of the oracle's best).  tests/conftest.py writes it to JSON at session end.
+REPORT: dict = {}
+
+
+def report_for(label: str) -> dict:
+    return REPORT.setdefault(label, {"blocks": 0, "decisions": 0, "min_margin": float("inf"),
+                                     "max_dscore": 0.0, "max_dlse": 0.0, "tie_ambiguous": 0,
+                                     "divergences": []})
+
+
 def check_block(gpu, ref, b, report):
-    """Compare one block: ids exact, lse and scores within tolerance, tokens exact or
-    tie-ambiguous under the near-tie protocol.  Updates `report`."""
+    """Compare one block: ids and logits exact, lse and scores within tolerance, and the
+    committed tokens under the near-tie protocol (reading R20).
+
+    The walk is replayed on the oracle's float32 scores, following the GPU's choices:
+    at every slot the GPU must take the oracle's argmax (lowest rank on ties) of the row
+    its own previous choice selects.  The one exception is a near tie: the oracle's best
+    exceeds the GPU's choice by no more than twice this block's measured max |dscore|
+    (the two candidates are then separated by less than the scores' own measured error,
+    far inside the 1e-3 score contract).  Each near tie is recorded in the parity record
+    with its margin; anything else fails."""
     assert np.array_equal(gpu["cand_id"][b], ref["cand_id"]), f"block {b}: candidate ids differ"
     assert np.array_equal(gpu["cand_logit"][b], ref["cand_logit"].astype(np.float32))
     dl = np.abs(gpu["lse"][b].astype(np.float64) - ref["lse"]).max()
@@ -48,19 +69,44 @@ def check_block(gpu, ref, b, report):
     assert np.array_equal(np.isfinite(ps), fin)
     ds = np.abs(ps[fin] - rs[fin]).max()
     assert ds <= SCORE_ATOL, f"block {b}: |dscore| {ds}"
-    report["max_dlse"] = max(report.get("max_dlse", 0.0), dl)
-    report["max_dscore"] = max(report.get("max_dscore", 0.0), ds)
+    report["blocks"] = report.get("blocks", 0) + 1
+    report["max_dlse"] = max(report.get("max_dlse", 0.0), float(dl))
+    report["max_dscore"] = max(report.get("max_dscore", 0.0), float(ds))
+    margins = ref["margin"][np.isfinite(ref["margin"])]
+    report["decisions"] = report.get("decisions", 0) + int(margins.size)
+    if margins.size:
+        report["min_margin"] = min(report.get("min_margin", float("inf")), float(margins.min()))
     tg, tr = gpu["tokens"][b], ref["tokens"]
     assert tg[0] == tr[0]
-    diff = np.flatnonzero(tg[1:] != tr[1:])
-    report["blocks"] = report.get("blocks", 0) + 1
-    report["min_margin"] = min(report.get("min_margin", np.inf), float(ref["margin"].min()))
-    if diff.size:
-        s = int(diff[0])
-        margin = float(ref["margin"][s])
-        assert margin < 2 * ds, (f"block {b}: token differs at slot {s + 1} with oracle margin "
-                                 f"{margin:.3e} >= 2 x max|dscore| {ds:.3e}")
-        report["tie_ambiguous"] = report.get("tie_ambiguous", 0) + 1
-    else:
-        # path scores of an identical path agree within the score tolerance
-        assert np.abs(gpu["path_score"][b] - ref["path_score"]).max() <= SCORE_ATOL
+    cid = ref["cand_id"]
+    Bm1 = cid.shape[0]
+    z32 = rs.astype(np.float32).astype(np.float64)
+    prev = 0
+    near = 0
+    for s in range(Bm1):
+        hit = np.flatnonzero(cid[s] == tg[s + 1])
+        assert hit.size == 1, f"block {b}: slot {s + 1} committed a non-candidate token"
+        c_gpu = int(hit[0])
+        z = z32[s, prev]
+        c_ref = int(np.argmax(z))          # first maximum = lowest rank
+        if c_gpu != c_ref:
+            gap = float(z[c_ref] - z[c_gpu])
+            report.setdefault("divergences", []).append(
+                {"block": int(b), "slot": s + 1, "oracle_gap": gap, "block_max_dscore": float(ds)})
+            assert gap <= 2 * ds, (f"block {b}: slot {s + 1} took rank {c_gpu}, {gap:.3e} below "
+                                   f"the oracle's best (rank {c_ref}): more than twice the "
+                                   f"block's max |dscore| {ds:.3e}")
+            report["tie_ambiguous"] = report.get("tie_ambiguous", 0) + 1
+            near += 1
+        # the GPU's path score is the score of its own choice
+        assert abs(float(gpu["path_score"][b][s]) - z[c_gpu]) <= SCORE_ATOL
+        prev = c_gpu
+    report["near_tie_blocks"] = report.get("near_tie_blocks", 0) + int(near > 0)
+
+
+def assert_no_divergence(report, label):
+    """Small seeded cases: no near tie at all (the protocol's exceptions are for the
+    full-size runs, whose tens of thousands of decisions include margins below the
+    scores' measured error)."""
+    assert report.get("tie_ambiguous", 0) == 0, (
+        f"{label}: {report['tie_ambiguous']} near tie(s): {report['divergences']}")
