@@ -100,18 +100,48 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ CPU oracle timing
 
-def oracle_timing(workload, tier, blocks, steps, warmup, threads=1):
+def oracle_timing(workload, tier, blocks, steps=1, warmup=1, procs=0, batch=None):
+    """The oracle in a fresh process (oracle/time_oracle.py): one thread (procs = 0) timing
+    `steps` steps of `blocks` blocks, or `procs` one-thread processes with `blocks` blocks
+    each.  BLAS / OpenMP threads are pinned to one, so the cores reported are the ones
+    used."""
     env = dict(os.environ)
     for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
-        env[v] = str(threads)
+        env[v] = "1"
     cmd = [sys.executable, "-m", "oracle.time_oracle", "--workload", workload,
            "--blocks", str(blocks), "--steps", str(steps), "--warmup", str(warmup)]
+    if procs:
+        cmd += ["--procs", str(procs)]
+    else:
+        cmd += ["--batch", str(batch or blocks * (steps + warmup))]
     if tier:
         cmd += ["--tier", tier]
     r = subprocess.run(cmd, cwd=ROOT, env=env, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"oracle timing failed: {r.stderr[-2000:]}")
     return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_baseline(workload, tier, one_blocks=2, one_steps=2, all_blocks=2):
+    """The oracle on this host: one thread, and every core (one process per core)."""
+    n = host_cores()
+    one = oracle_timing(workload, tier, one_blocks, steps=one_steps, warmup=1)
+    allc = oracle_timing(workload, tier, all_blocks, steps=all_blocks, procs=n)
+    return {
+        "value": allc["blocks_per_s"], "unit": "blocks/s", "cores": n, "kind": "oracle",
+        "sample": (f"{allc['blocks']} blocks of {workload}{'/' + tier if tier else ''} "
+                   f"({all_blocks} per process after one warm-up block, {n} one-thread "
+                   f"processes, float64, full rows)"),
+        "one_thread": {"value": one["blocks_per_s"], "unit": "blocks/s", "cores": 1,
+                       "sample": f"{one_blocks} blocks x {one_steps} timed steps, 1 thread"},
+    }
 
 
 # ------------------------------------------------------------------ ncu traffic record
@@ -142,21 +172,26 @@ def recorded_traffic(kernel: str):
 # ------------------------------------------------------------------ arms
 
 def run_reference(a):
+    """The oracle as the reference arm, on every host core: one one-thread process per core,
+    each step one block per process (cycling over two distinct blocks per process)."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    res = oracle_timing(a.workload, a.tier, a.ref_blocks, a.steps, a.warmup)
+    n = host_cores()
+    res = oracle_timing(a.workload, a.tier, 2, steps=a.steps, procs=n)
     v = res["blocks_per_s"]
     wlname = a.workload + (f"/{a.tier}" if a.tier else "")
+    sample = (f"{n} blocks of {wlname} per step (one per host core, {n} one-thread "
+              f"processes), {a.steps} steps over {res['distinct_blocks']} distinct blocks "
+              f"after one warm-up block per process; float64, full rows")
     line = {
         "impl": "reference", "metric": METRIC, "value": v, "unit": "blocks/s",
         "n_gpus": a.gpus, "steps": a.steps, "warmup": a.warmup,
-        "ms_per_step": 1e3 * statistics.mean(res["step_s"]), "higher_is_better": True,
+        "ms_per_step": res["ms_per_step"], "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": wlname, "sample": f"{a.ref_blocks} block(s) per step"},
-        "cpu_baseline": {"value": v, "unit": "blocks/s", "cores": 1, "kind": "oracle",
-                         "sample": f"{a.ref_blocks} block(s) of {wlname} per step, "
-                                   f"{a.steps} steps, 1 thread (BLAS/OpenMP pinned)"},
+        "config": {"workload": wlname, "sample": sample},
+        "cpu_baseline": {"value": v, "unit": "blocks/s", "cores": n, "kind": "oracle",
+                         "sample": sample},
         "e2e": {"value": v, "unit": "blocks/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -225,6 +260,146 @@ def time_lm_head(lc, rows, V, K, dev, stream, peak_tflops, calls=5, D=LM_D):
             "data": "synthetic: hidden N(0,1), vocabulary matrix N(0, 1.5^2/D), bf16, on device"}
 
 
+# the per-workload sub-results the line carries beside the headline: every configuration
+# of the synthetic workloads at its stated size (the high-concurrency medium tier is the
+# headline itself)
+SUBCONFIGS = [
+    ("tiny", {}, "tiny"),
+    ("single", {}, "config 1 (single request)"),
+    *[("sweep", dict(batch=b), f"config 2 (sweep) batch {b}") for b in (1, 4, 16, 32, 64, 128)],
+    ("highconc", dict(tier="low"), "config 3 (high concurrency) low tier"),
+    ("highconc", dict(tier="high"), "config 3 (high concurrency) high tier"),
+    ("widepool", {}, "config 4 (wide pool)"),
+]
+HEADLINE_LABEL = "config 3 (high concurrency) medium tier"
+
+
+def gemm_work(wl, B, K):
+    """Executed tensor work per launch of each contraction (split-bf16 operands double the
+    contraction dimension) and of the attention."""
+    import math
+    H, F, E = wl.dims["hidden"], wl.dims["ffn"], wl.dims["d_e"]
+    S = (B - 1) * K
+    M = wl.batch * S
+    fl = {"qkv_gemm": 2 * M * 3 * H * 2 * H, "out_gemm": 2 * M * H * 2 * H,
+          "ffn1_gemm": 2 * M * F * 2 * H, "ffn2_gemm": 2 * M * H * 2 * F,
+          "node_gemm": 2 * M * H * 2 * H, "fuse_gemm": 2 * M * H * 4 * H,
+          "heads_gemm": 2 * M * 2 * E * 2 * H}
+    # attention (128-query tiles over all keys): S = Q K^T as three split products,
+    # O' = P [V_hi | V_lo] as two products of width 2 dh
+    nh = wl.dims["heads"]
+    dh = H // nh
+    keys = 128 * math.ceil(S / 128)
+    fl["attention"] = wl.batch * nh * math.ceil(S / 128) * (
+        3 * 2 * 128 * keys * dh + 2 * 2 * 128 * keys * 2 * dh)
+    return fl
+
+
+def measure_workload(lc, wl, steps, warmup, dev, stream, graph=True, world=1, barrier=None):
+    """Time lilicorr_rerank on workload `wl` (inputs resident on the device): an eager pass
+    with per-kernel events (breakdown, launch count), then the headline timing, one CUDA
+    graph of one call replayed per step (or the eager steps themselves)."""
+    import numpy as np
+    import torch
+    barrier = barrier or (lambda: None)
+    batch, B, V, K = wl.batch, wl.B, wl.V, wl.K
+    if wl.ldtype == "bf16":
+        logits = torch.from_numpy(wl.logits.view(np.int16)).view(torch.bfloat16).to(dev)
+    else:
+        logits = torch.from_numpy(wl.logits).to(dev)
+    tgt = torch.from_numpy(wl.target_state.view(np.int16)).view(torch.bfloat16).to(dev)
+    anc = torch.from_numpy(wl.anchor_ids).to(dev)
+    w = lc.Weights(wl.dims, wl.weights, device=dev.index or 0)
+    ws = w.workspace(batch, B, K)
+    out = {"tokens": torch.empty(batch, B, dtype=torch.int32, device=dev),
+           "path_score": torch.empty(batch, B - 1, dtype=torch.float32, device=dev)}
+
+    def step(st=stream):
+        lc.rerank(w, logits, K, target_state=tgt, anchor_ids=anc, workspace=ws, out=out,
+                  stream=st)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    lc.stage_timing(True)
+    lc.stage_times()  # clear
+    barrier()
+    torch.cuda.synchronize(dev)
+    n0 = lc.launch_count()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    launches_per_step = (lc.launch_count() - n0) / steps
+    ms_eager = e0.elapsed_time(e1)
+    lc.stage_timing(False)
+    st = lc.stage_times()
+    ms = ms_eager
+    mode = "eager (one lilicorr_rerank per step)"
+    if graph:
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            step(cap)
+        torch.cuda.synchronize(dev)
+        for _ in range(warmup):
+            g.replay()
+        torch.cuda.synchronize(dev)
+        barrier()
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for _ in range(steps):
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+        ms = e0.elapsed_time(e1)
+        mode = "CUDA graph of one lilicorr_rerank, replayed per step"
+        del g
+    calls = st.pop("calls")
+    per_kernel = {k: {"ms_per_step": v["ms"] / max(calls, 1),
+                      "avg_launch_us": 1e3 * v["ms"] / max(v["launches"], 1),
+                      "launches_per_step": v["launches"] / max(calls, 1)}
+                  for k, v in st.items() if v["launches"]}
+    res = {"ms": ms, "ms_eager": ms_eager, "mode": mode, "per_kernel": per_kernel,
+           "launches_per_step": launches_per_step,
+           "logit_bytes": batch * (B - 1) * V * (2 if wl.ldtype == "bf16" else 4),
+           "inputs": (logits, tgt, anc), "weights": w, "out": out}
+    return res
+
+
+def summarise(wl, m, pk, steps, world=1):
+    """The per-workload figures of one measurement."""
+    step_ms = m["ms"] / steps
+    k1 = m["per_kernel"]["logit_pass"]
+    gbs = m["logit_bytes"] / (k1["avg_launch_us"] * 1e-6) / 1e9
+    t_roof = m["logit_bytes"] / (pk["hbm_gbs"] * 1e9)
+    dominant = max(m["per_kernel"], key=lambda k: m["per_kernel"][k]["ms_per_step"])
+    fl = gemm_work(wl, wl.B, wl.K)
+    enc = {k: fl[k] / (v["avg_launch_us"] * 1e-6) / 1e12
+           for k, v in m["per_kernel"].items() if k in fl}
+    return {
+        "workload": describe(wl), "batch": wl.batch, "K": wl.K,
+        "blocks_per_s": job_throughput(wl.batch, steps, world, m["ms"] / 1e3),
+        "ms_per_step": step_ms, "eager_ms_per_step": m["ms_eager"] / steps,
+        "launch": m["mode"],
+        "logit_pass": {"avg_launch_us": k1["avg_launch_us"], "achieved_gbs": gbs,
+                       "frac_of_peak": gbs / pk["hbm_gbs"], "bytes_per_launch": m["logit_bytes"]},
+        "e2e_fraction_of_logits_roofline": t_roof / (step_ms / 1e3),
+        "logits_roofline_us": t_roof * 1e6,
+        "dominant_kernel": dominant,
+        "kernels_us_per_step": {k: round(1e3 * v["ms_per_step"], 2)
+                                for k, v in m["per_kernel"].items()},
+        "tensor_tflops_executed": {k: round(v, 1) for k, v in enc.items()},
+        "gpu_launches_per_step": m["launches_per_step"],
+    }
+
+
 def run_gb300(a):
     import numpy as np
     import torch
@@ -243,96 +418,37 @@ def run_gb300(a):
     __graft_entry__.build()
     import draft_block_candidate_gb300 as lc
 
-    # CPU baseline first (a fresh, thread-pinned process), rank 0 at N = 1 only.
+    # CPU baseline first (fresh, thread-pinned processes), rank 0 at N = 1 only.
     cpu = None
     if rank == 0 and world == 1 and not a.no_cpu_baseline:
-        res = oracle_timing(a.workload, a.tier, a.cpu_blocks, 2, 1)
-        cpu = {"value": res["blocks_per_s"], "unit": "blocks/s", "cores": 1, "kind": "oracle",
-               "sample": f"{a.cpu_blocks} blocks x 2 timed steps of the same workload "
-                         f"(full rows, float64, 1 thread)"}
-
-    wl = rank_workload(a.workload, a.tier, a.batch, rank)
-    batch, B, V, K = wl.batch, wl.B, wl.V, wl.K
-    logits_host = torch.from_numpy(wl.logits.view(np.int16)).view(torch.bfloat16)
-    logits = logits_host.to(dev)
-    tgt_host = torch.from_numpy(wl.target_state.view(np.int16)).view(torch.bfloat16)
-    tgt = tgt_host.to(dev)
-    anc_host = torch.from_numpy(wl.anchor_ids)
-    anc = anc_host.to(dev)
-    w = lc.Weights(wl.dims, wl.weights, device=local)
-    ws = w.workspace(batch, B, K)
-    out = {"tokens": torch.empty(batch, B, dtype=torch.int32, device=dev),
-           "path_score": torch.empty(batch, B - 1, dtype=torch.float32, device=dev)}
-    stream = torch.cuda.current_stream(dev)
-
-    def step():
-        lc.rerank(w, logits, K, target_state=tgt, anchor_ids=anc, workspace=ws, out=out,
-                  stream=stream)
-
-    for _ in range(a.warmup):
-        step()
-    torch.cuda.synchronize(dev)
+        cpu = oracle_baseline(a.workload, a.tier, one_blocks=a.cpu_blocks)
 
     def barrier():
         if world > 1:
             torch.distributed.barrier()
 
+    pk, pk_kind = peaks()
+    stream = torch.cuda.current_stream(dev)
+    wl = rank_workload(a.workload, a.tier, a.batch, rank)
+    batch, B, V, K = wl.batch, wl.B, wl.V, wl.K
     clocks = ClockSampler(local)
     time.sleep(0.3)
-    # (1) eager steps with per-kernel events: the breakdown and the launch count
-    lc.stage_timing(True)
-    lc.stage_times()  # clear
-    barrier()
-    torch.cuda.synchronize(dev)
-    n0 = lc.launch_count()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(a.steps):
-        step()
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    barrier()
-    launches_per_step = (lc.launch_count() - n0) / a.steps
-    ms_eager = e0.elapsed_time(e1)
-    lc.stage_timing(False)
-    st = lc.stage_times()
-    ms = ms_eager
-    launch_mode = "eager (one lilicorr_rerank per step)"
-    # (2) the headline: the same step captured once as a CUDA graph (the entry point
-    # allocates nothing and never synchronises) and replayed W + K times
-    if not a.no_graph:
-        cap = torch.cuda.Stream(dev)
-        cap.wait_stream(stream)
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=cap):
-            lc.rerank(w, logits, K, target_state=tgt, anchor_ids=anc, workspace=ws, out=out,
-                      stream=cap)
-        torch.cuda.synchronize(dev)
-        for _ in range(a.warmup):
-            graph.replay()
-        torch.cuda.synchronize(dev)
-        barrier()
-        torch.cuda.synchronize(dev)
-        e0.record(stream)
-        for _ in range(a.steps):
-            graph.replay()
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
-        barrier()
-        ms = e0.elapsed_time(e1)
-        launch_mode = "CUDA graph of one lilicorr_rerank, replayed per step"
-    launches = int(round(launches_per_step * a.steps))
+    m = measure_workload(lc, wl, a.steps, a.warmup, dev, stream, graph=not a.no_graph,
+                         world=world, barrier=barrier)
     clk = clocks.stop()
-    ms = max_over_ranks(ms, dev)
+    ms = max_over_ranks(m["ms"], dev)
     value = job_throughput(batch, a.steps, world, ms / 1e3)
+    launches = int(round(m["launches_per_step"] * a.steps))
+    logits, tgt, anc = m["inputs"]
+    w = m["weights"]
 
     # e2e through the host-memory entry point: H2D copies in, D2H tokens out, per step.
     e2e = None
     if not a.no_e2e:
+        logits_host = logits.cpu()
         pin_logits = logits_host.pin_memory()
-        pin_tgt = tgt_host.pin_memory()
-        pin_anc = anc_host.pin_memory()
+        pin_tgt = tgt.cpu().pin_memory()
+        pin_anc = anc.cpu().pin_memory()
         tok_h = torch.empty(batch, B, dtype=torch.int32).pin_memory()
         ps_h = torch.empty(batch, B - 1, dtype=torch.float32).pin_memory()
         wsh = lc.rerank_host_workspace(w, batch, B, K, lc.BF16)
@@ -354,45 +470,33 @@ def run_gb300(a):
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": a.e2e_steps,
                "api": "lilicorr_rerank_host (pinned host buffers; chunked copies overlapped "
                       "with compute)"}
-        del wsh
+        del wsh, pin_logits, logits_host
+    del logits, tgt, anc, m["inputs"]
+    w.close()
+    torch.cuda.empty_cache()
 
     if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
         return
 
-    pk, pk_kind = peaks()
-    calls = st.pop("calls")
-    per_kernel = {k: {"ms_per_step": v["ms"] / max(calls, 1),
-                      "avg_launch_us": 1e3 * v["ms"] / max(v["launches"], 1),
-                      "launches_per_step": v["launches"] / max(calls, 1)}
-                  for k, v in st.items() if v["launches"]}
+    head = summarise(wl, m, pk, a.steps, world)
+    per_kernel = m["per_kernel"]
     step_ms = ms / a.steps
-    dominant = max(per_kernel, key=lambda k: per_kernel[k]["ms_per_step"])
-    H, F, E, S = wl.dims["hidden"], wl.dims["ffn"], wl.dims["d_e"], (B - 1) * K
-    M = batch * S
-    logit_bytes = batch * (B - 1) * V * 2
-    # executed tensor work per launch (split-bf16: the contraction dimension is doubled)
-    gemm_flops = {"qkv_gemm": 2 * M * 3 * H * 2 * H, "out_gemm": 2 * M * H * 2 * H,
-                  "ffn1_gemm": 2 * M * F * 2 * H, "ffn2_gemm": 2 * M * H * 2 * F,
-                  "node_gemm": 2 * M * H * 2 * H, "fuse_gemm": 2 * M * H * 4 * H,
-                  "heads_gemm": 2 * M * 2 * E * 2 * H}
-    # attention: executed tensor work per launch (128-query tiles, 256 key columns):
-    # S = Q K^T as three split products, O' = P [V_hi | V_lo] as two products of width 2 dh
-    import math
-    nh = wl.dims["heads"]
-    dh = H // nh
-    gemm_flops["attention"] = batch * nh * math.ceil(S / 128) * (
-        3 * 2 * 128 * 256 * dh + 2 * 2 * 128 * 256 * 2 * dh)
+    dominant = head["dominant_kernel"]
     k1 = per_kernel["logit_pass"]
-    k1_gbs = logit_bytes / (k1["avg_launch_us"] * 1e-6) / 1e9
+    logit_bytes = m["logit_bytes"]
+    k1_gbs = head["logit_pass"]["achieved_gbs"]
     logit_pass = {"achieved": k1_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
                   "frac": k1_gbs / pk["hbm_gbs"], "bytes_per_launch": logit_bytes,
                   "avg_launch_us": k1["avg_launch_us"], "peak_kind": pk_kind}
+    fl = gemm_work(wl, B, K)
     if dominant == "logit_pass":
         roof = {"bound": "hbm", "kernel": "logit_pass", "achieved": k1_gbs, "peak": pk["hbm_gbs"],
                 "unit": "GB/s", "frac": k1_gbs / pk["hbm_gbs"],
                 "traffic": recorded_traffic("logit_pass"), "peak_kind": pk_kind}
-    elif dominant in gemm_flops:
-        tf = gemm_flops[dominant] / (per_kernel[dominant]["avg_launch_us"] * 1e-6) / 1e12
+    elif dominant in fl:
+        tf = fl[dominant] / (per_kernel[dominant]["avg_launch_us"] * 1e-6) / 1e12
         peak = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
         roof = {"bound": "tensor", "kernel": dominant, "achieved": tf, "peak": peak,
                 "unit": "TFLOP/s", "frac": tf / peak, "traffic": recorded_traffic(dominant),
@@ -400,6 +504,27 @@ def run_gb300(a):
     else:
         roof = {"bound": "latency", "kernel": dominant, "achieved": None, "peak": None,
                 "unit": None, "frac": None, "traffic": None}
+
+    # every other configuration at its stated size (same launch form as the headline)
+    configs = {}
+    if world == 1 and not a.no_configs:
+        for name, kw, label in SUBCONFIGS:
+            sw = rank_workload(name, kw.get("tier"), kw.get("batch"), 0)
+            sm = measure_workload(lc, sw, a.config_steps, 3, dev, stream, graph=not a.no_graph)
+            sm["weights"].close()
+            del sm["inputs"]
+            torch.cuda.empty_cache()
+            r = summarise(sw, sm, pk, a.config_steps)
+            if not a.no_cpu_baseline:
+                r["oracle"] = oracle_baseline(name, kw.get("tier"), one_blocks=1, one_steps=1,
+                                              all_blocks=1)
+            configs[label] = r
+            del sw
+        head_cfg = dict(head)
+        if cpu is not None:
+            head_cfg["oracle"] = cpu
+        configs[HEADLINE_LABEL] = head_cfg
+
     lm = None
     if not a.no_lm_head:
         lm = time_lm_head(lc, batch * (B - 1), V, K, dev, stream, pk["bf16_tflops"])
@@ -411,20 +536,20 @@ def run_gb300(a):
         "config": {"workload": describe(wl), "batch_per_gpu": batch, "B": B, "V": V, "K": K,
                    "l2": f"inputs larger than L2 ({logit_bytes / 1e6:.0f} MB of logits per step); no flush",
                    "parallelism": f"dp{world} (independent blocks per rank)",
-                   "launch": launch_mode},
+                   "launch": m["mode"]},
         "roofline": roof,
         "logit_pass": logit_pass,
-        "e2e_fraction_of_logits_roofline": (logit_bytes / (pk["hbm_gbs"] * 1e9)) / (step_ms / 1e3),
+        "e2e_fraction_of_logits_roofline": head["e2e_fraction_of_logits_roofline"],
         "gpu_launches": launches,
-        "eager_ms_per_step": ms_eager / a.steps,
+        "eager_ms_per_step": m["ms_eager"] / a.steps,
         "kernels": per_kernel,
         "e2e": e2e,
         "cpu_baseline": cpu,
         "clocks": clk,
         "lm_head_topk_lse": lm,
+        "configs": configs,
     }
     print(json.dumps(line), flush=True)
-    w.close()
     if world > 1:
         torch.distributed.destroy_process_group()
 
@@ -490,8 +615,12 @@ def main():
     ap.add_argument("--workload", default="highconc")
     ap.add_argument("--tier", default="medium")
     ap.add_argument("--e2e-steps", type=int, default=10)
-    ap.add_argument("--cpu-blocks", type=int, default=4)
-    ap.add_argument("--ref-blocks", type=int, default=1)
+    ap.add_argument("--cpu-blocks", type=int, default=2,
+                    help="blocks per timed step of the one-thread oracle leg")
+    ap.add_argument("--config-steps", type=int, default=20,
+                    help="timed steps of each per-configuration sub-result")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-configuration sub-results")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-lm-head", action="store_true",
