@@ -543,18 +543,368 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   }
 }
 
+// ------------------------------------------------------------------ long lattices
+//
+// Lattices of 257..512 tokens (the wide candidate pool: 15 slots x 32 candidates = 480
+// tokens).  The keys no longer fit the shared memory at once, so each (128-query tile,
+// block, head) item walks its keys in chunks of 128 with an online softmax:
+//   warp 0     TMA: the item's Q (hi, lo), then per chunk K (hi, lo) and V (hi, lo) into
+//              two-stage rings; owns the TMEM allocation (S / P: two 128-column buffers,
+//              O': two 128-column buffers, one per item parity)
+//   warp 1     MMA: S(g+1) = Q K(g+1)^T (three split products) while the softmax warps
+//              work on chunk g, then O' += P(g) [V hi | V lo] (two products, N 128, P read
+//              from TMEM); S into a buffer waits until the product that read its previous
+//              P has completed
+//   warps 2-17 per chunk: scale, add the slot bias, row maximum (four warps per query-row
+//              quarter, combined through shared memory), running maximum m: the first
+//              chunk sets it; a later chunk whose maximum exceeds m by more than 2^16
+//              re-bases the row (O' and the partial sums scaled down once the previous
+//              product has landed), otherwise its terms stay relative to m; p = 2^(x - m)
+//              written over S as packed bf16 hi / lo.  After the last chunk O / l is
+//              split into hi / lo and stored straight from registers (rows past the
+//              block skipped).
+// The bias table holds one row per query slot over all keys (-inf past the block).
+// Every wait is bounded and the first timeout makes every later wait of the CTA give up
+// at once, so that all warps still reach their named barriers and the final teardown.
+constexpr int AL_KC = 128;                     // keys per chunk
+constexpr int AL_KMAX = 512;
+constexpr int AL_BSTRIDE = AL_KMAX + 4;        // floats per bias-table row (bank offset)
+constexpr int AL_SMEM = 10 * AT_TILE + 1024;   // Q, K ring, V ring + the bias table
+
+__device__ __forceinline__ bool al_wait(uint64_t* bar, uint32_t parity, uint32_t site,
+                                        volatile int* fail) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((n & 63) == 0 && (*fail || clock64() - t0 > WAIT_LIMIT_CYCLES)) {
+      atomicOr(&g_err_at, site);
+      *fail = 1;
+      return false;
+    }
+  }
+}
+
+// MN-major [V hi | V lo] operand whose lo tile sits `lo_off` bytes after the hi tile.
+__device__ __forceinline__ uint64_t al_desc_v(const void* p, uint32_t lo_off) {
+  return (at_desc(p) & ~(0x3FFFull << 16)) | (uint64_t(lo_off >> 4) << 16);
+}
+
+__global__ void __launch_bounds__(AT_THREADS, 1)
+    attn_tc_long_kernel(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __restrict__ out,
+                        int S, int Kc, int H, int B_max, int heads, int64_t batch,
+                        const float* __restrict__ dist_bias, const float* __restrict__ same_bias) {
+  extern __shared__ uint8_t al_smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(al_smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQh = sm;                // Q hi / lo
+  uint8_t* sQl = sm + AT_TILE;
+  uint8_t* sK = sm + 2 * AT_TILE;   // stage s: K hi at sK + 2 s AT_TILE, K lo one tile later
+  uint8_t* sV = sm + 6 * AT_TILE;   // stage s: V hi at sV + 2 s AT_TILE, V lo one tile later
+  // [query slot][key]: (dist + same-slot bias) * log2(e) of the current head, -inf for
+  // keys beyond the block
+  float* s_btab = reinterpret_cast<float*>(sm + 10 * AT_TILE);
+  __shared__ __align__(8) uint64_t bar_q, bar_qfree, bar_k[2], bar_kfree[2], bar_v[2],
+      bar_vfree[2], bar_s[2], bar_p[2], bar_pv[2], bar_o[2], bar_ofree[2];
+  __shared__ uint32_t s_tmem;
+  __shared__ volatile int s_fail;
+  __shared__ float s_pmax[2][AT_NSPLIT][128], s_psum[AT_NSPLIT][128];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int QT = (S + AT_QT - 1) / AT_QT;
+  const int NC = (S + AL_KC - 1) / AL_KC;
+  const int64_t nitems = batch * heads * QT;
+  const int nd = 2 * B_max - 3;
+
+  if (tid == 0) {
+    mbar_init(&bar_q, 1);
+    mbar_init(&bar_qfree, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bar_k[b], 1);
+      mbar_init(&bar_kfree[b], 1);
+      mbar_init(&bar_v[b], 1);
+      mbar_init(&bar_vfree[b], 1);
+      mbar_init(&bar_s[b], 1);
+      mbar_init(&bar_p[b], 32 * AT_SOFT_WARPS);
+      mbar_init(&bar_pv[b], 1);
+      mbar_init(&bar_o[b], 1);
+      mbar_init(&bar_ofree[b], 32 * AT_SOFT_WARPS);
+    }
+    s_fail = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr(&s_tmem)),
+                 "r"(AT_TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  at_fence_before();
+  __syncthreads();
+  at_fence_after();
+  const uint32_t tmem = s_tmem;
+  // S / P of chunk g in columns 128 (g & 1) .. +127; O' of item i in 256 + 128 (i & 1)
+  const uint32_t tS = tmem, tO0 = tmem + AT_O_COL;
+  // this CTA's items and chunks
+  const int my_items =
+      blockIdx.x < nitems ? static_cast<int>((nitems - 1 - blockIdx.x) / gridDim.x) + 1 : 0;
+  const int total = my_items * NC;
+
+  if (warp == 0 && lane == 0) {
+    // ---- producer
+    int g = 0;
+    bool ok = true;
+    ItemPos it(blockIdx.x, gridDim.x, QT, batch);
+    for (int i = 0; i < my_items && ok; ++i, it.next()) {
+      const int tok0 = it.blk * S;
+      const int cq = it.h * AT_DH, ck = H + it.h * AT_DH, cv = 2 * H + it.h * AT_DH, lo = 3 * H;
+      if (i > 0 && !al_wait(&bar_qfree, (i - 1) & 1, ERR_AT_QKFREE, &s_fail)) break;
+      mbar_arrive_expect_tx(&bar_q, 2 * AT_TILE);
+      at_tma(sQh, &tm, cq, tok0 + it.qt * AT_QT, &bar_q);
+      at_tma(sQl, &tm, lo + cq, tok0 + it.qt * AT_QT, &bar_q);
+      for (int c = 0; c < NC; ++c, ++g) {
+        const int st = g & 1, use = g >> 1;
+        const int row = tok0 + c * AL_KC;
+        if (use > 0 && !al_wait(&bar_kfree[st], (use - 1) & 1, ERR_AT_QKFREE, &s_fail)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&bar_k[st], 2 * AT_TILE);
+        at_tma(sK + 2 * st * AT_TILE, &tm, ck, row, &bar_k[st]);
+        at_tma(sK + (2 * st + 1) * AT_TILE, &tm, lo + ck, row, &bar_k[st]);
+        if (use > 0 && !al_wait(&bar_vfree[st], (use - 1) & 1, ERR_AT_VFREE, &s_fail)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&bar_v[st], 2 * AT_TILE);
+        at_tma(sV + 2 * st * AT_TILE, &tm, cv, row, &bar_v[st]);
+        at_tma(sV + (2 * st + 1) * AT_TILE, &tm, lo + cv, row, &bar_v[st]);
+      }
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---- MMA issuer: S(0); then per chunk g: S(g + 1), O' += P(g) V(g)
+    constexpr uint32_t id_s = at_idesc(128, 128, false);
+    constexpr uint32_t id_o = at_idesc(128, 128, true);
+    auto qk = [&](int b) {  // S into buffer b from K stage b (both follow the chunk parity)
+      const uint32_t d = tS + uint32_t(128 * b);
+      const uint8_t* kh = sK + 2 * b * AT_TILE;
+      const uint8_t* kl = kh + AT_TILE;
+#pragma unroll
+      for (int ks = 0; ks < AT_DH / 16; ++ks) {
+        at_mma(d, at_desc(sQh + ks * 32), at_desc(kh + ks * 32), id_s, ks > 0);
+        at_mma(d, at_desc(sQh + ks * 32), at_desc(kl + ks * 32), id_s, 1);
+        at_mma(d, at_desc(sQl + ks * 32), at_desc(kh + ks * 32), id_s, 1);
+      }
+    };
+    auto pv = [&](int b, uint32_t tO, bool first) {
+      // P for keys 32c..32c+31 of the chunk: TMEM columns 32c (hi, 16 packed columns) and
+      // 32c + 16 (lo); a 16-key step j uses 8 of them
+      const uint8_t* vh = sV + 2 * b * AT_TILE;
+#pragma unroll 4
+      for (int j = 0; j < AL_KC / 16; ++j) {
+        const uint32_t pc = uint32_t(128 * b + 32 * (j >> 1) + 8 * (j & 1));
+        const uint64_t vhl = al_desc_v(vh + 16 * j * 128, AT_TILE);
+        at_mma_ts(tO, tS + pc, vhl, id_o, !(first && j == 0));
+        at_mma_ts(tO, tS + pc + 16, vhl, id_o, 1);
+      }
+    };
+    bool ok = total > 0 && al_wait(&bar_q, 0, ERR_AT_QK, &s_fail) &&
+              al_wait(&bar_k[0], 0, ERR_AT_QK, &s_fail);
+    if (ok) {
+      at_fence_after();
+      qk(0);
+      at_commit(&bar_s[0]);
+      at_commit(&bar_kfree[0]);
+    }
+    int i = 0, c = 0;  // item and chunk of g
+    for (int g = 0; g < total && ok; ++g) {
+      const int g1 = g + 1;
+      if (g1 < total) {
+        const int c1 = c + 1 == NC ? 0 : c + 1;
+        const int i1 = c1 == 0 ? i + 1 : i;
+        const int b1 = g1 & 1;
+        ok = (c1 != 0 || al_wait(&bar_q, i1 & 1, ERR_AT_QK, &s_fail)) &&
+             al_wait(&bar_k[b1], (g1 >> 1) & 1, ERR_AT_QK, &s_fail) &&
+             (g1 < 2 || al_wait(&bar_pv[b1], ((g1 - 2) >> 1) & 1, ERR_AT_O, &s_fail));
+        if (!ok) break;
+        at_fence_after();
+        qk(b1);
+        at_commit(&bar_s[b1]);
+        at_commit(&bar_kfree[b1]);
+        if (c1 == NC - 1) at_commit(&bar_qfree);
+      }
+      const int b = g & 1;
+      ok = al_wait(&bar_p[b], (g >> 1) & 1, ERR_AT_P, &s_fail) &&
+           al_wait(&bar_v[b], (g >> 1) & 1, ERR_AT_V, &s_fail) &&
+           (c != 0 || i < 2 ||
+            al_wait(&bar_ofree[i & 1], ((i >> 1) - 1) & 1, ERR_AT_OFREE, &s_fail));
+      if (!ok) break;
+      at_fence_after();
+      pv(b, tO0 + AT_O_W * uint32_t(i & 1), c == 0);
+      at_commit(&bar_pv[b]);
+      at_commit(&bar_vfree[b]);
+      if (c == NC - 1) at_commit(&bar_o[i & 1]);
+      if (++c == NC) {
+        c = 0;
+        ++i;
+      }
+    }
+  } else if (warp >= 2) {
+    // ---- softmax and epilogue
+    const int qq = warp & 3, hf = (warp - 2) >> 2;
+    const int r = 32 * qq + lane;  // TMEM lane = query row of the tile
+    const uint32_t lane_off = uint32_t(32 * qq) << 16;
+    const int nq = S / Kc;         // query slots
+    const int nk = NC * AL_KC;     // keys covered by the chunks
+    constexpr float C = 0.125f * AT_LOG2E;  // 1 / sqrt(64), in log2 units
+    constexpr float RESCALE_AT = 16.f;      // log2 headroom before a chunk re-bases a row
+    const int jb = 32 * hf;                 // this warp's 32 keys of every chunk
+    int cur_h = -1;
+    int g = 0;
+    ItemPos it(blockIdx.x, gridDim.x, QT, batch);
+    for (int i = 0; i < my_items; ++i, it.next()) {
+      const int qt = it.qt, h = it.h, blk = it.blk;
+      const int q = qt * AT_QT + r;
+      const uint32_t tO = tO0 + AT_O_W * uint32_t(i & 1);
+      if (h != cur_h) {  // bias table of this head (all softmax warps take the same items)
+        soft_sync();
+        const float* drow = dist_bias + h * nd;
+        const float same = same_bias[h];
+        for (int e = tid - 64; e < nq * nk; e += 32 * AT_SOFT_WARPS) {
+          const int qs = e / nk, key = e - qs * nk;
+          const int k = key / Kc - qs + B_max - 2;
+          s_btab[qs * AL_BSTRIDE + key] =
+              key < S ? (__ldg(drow + k) + (k == B_max - 2 ? same : 0.f)) * AT_LOG2E
+                      : -INFINITY;
+        }
+        soft_sync();
+        cur_h = h;
+      }
+      const float* brow = s_btab + (min(q, S - 1) / Kc) * AL_BSTRIDE;
+      bool ok = true;
+      float m = -INFINITY, l = 0.f;
+      for (int c = 0; c < NC; ++c, ++g) {
+        const int b = g & 1;
+        ok = al_wait(&bar_s[b], (g >> 1) & 1, ERR_AT_S, &s_fail) && ok;
+        at_fence_after();
+        float v[32];
+        at_ld32(tS + lane_off + uint32_t(128 * b + jb), v);
+        // x = v / 8 * log2(e) + bias (log2 units), two at a time
+        const float* bk = brow + c * AL_KC + jb;
+        float mx = -INFINITY;
+        const float2 c2 = make_float2(C, C);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const float4 b4 = *reinterpret_cast<const float4*>(bk + 4 * u);
+          const float2 xa = __ffma2_rn(make_float2(v[4 * u], v[4 * u + 1]), c2, make_float2(b4.x, b4.y));
+          const float2 xb = __ffma2_rn(make_float2(v[4 * u + 2], v[4 * u + 3]), c2, make_float2(b4.z, b4.w));
+          v[4 * u] = xa.x;
+          v[4 * u + 1] = xa.y;
+          v[4 * u + 2] = xb.x;
+          v[4 * u + 3] = xb.y;
+          mx = fmaxf(mx, fmaxf(fmaxf(xa.x, xa.y), fmaxf(xb.x, xb.y)));
+        }
+        s_pmax[c & 1][hf][r] = mx;
+        quarter_sync(qq);
+        float mh = s_pmax[c & 1][0][r];
+#pragma unroll
+        for (int k = 1; k < AT_NSPLIT; ++k) mh = fmaxf(mh, s_pmax[c & 1][k][r]);
+        if (c == 0) {
+          m = mh;
+        } else {
+          // a row whose new chunk holds a much larger logit re-bases on it: O' holds the
+          // earlier chunks' products (wait for the last of them) and is scaled down with
+          // the partial sum; other rows keep their base (terms up to 2^RESCALE_AT).  The
+          // TMEM access is warp-wide.
+          const bool rebase = mh > m + RESCALE_AT;
+          if (__any_sync(FULL_MASK, rebase)) {
+            const float sc = rebase ? at_ex2(m - mh) : 1.f;
+            l *= sc;
+            ok = al_wait(&bar_pv[(g - 1) & 1], ((g - 1) >> 1) & 1, ERR_AT_O, &s_fail) && ok;
+            at_fence_after();
+#pragma unroll
+            for (int part = 0; part < 2; ++part) {
+              float o[AT_OW];
+              at_ld16(tO + lane_off + 64 * part + AT_OW * hf, o);
+#pragma unroll
+              for (int e = 0; e < AT_OW; ++e) o[e] *= sc;
+              at_st16f(tO + lane_off + 64 * part + AT_OW * hf, o);
+            }
+          }
+          if (rebase) m = mh;
+        }
+        float2 l2 = make_float2(0.f, 0.f);
+        uint32_t ph[16], pl[16];
+        const float2 nm = make_float2(-m, -m);
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+          const float2 y = __fadd2_rn(make_float2(v[2 * u], v[2 * u + 1]), nm);
+          const float p0 = at_ex2(y.x), p1 = at_ex2(y.y);
+          l2 = __fadd2_rn(l2, make_float2(p0, p1));
+          at_split2(p0, p1, ph[u], pl[u]);
+        }
+        l += l2.x + l2.y;
+        at_st16(tS + lane_off + uint32_t(128 * b + jb), ph);
+        at_st16(tS + lane_off + uint32_t(128 * b + jb + 16), pl);
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        at_fence_before();
+        mbar_arrive(&bar_p[b]);
+      }
+      s_psum[hf][r] = l;
+      quarter_sync(qq);
+      float lsum = 0.f;
+#pragma unroll
+      for (int k = 0; k < AT_NSPLIT; ++k) lsum += s_psum[k][r];
+      const float inv = 1.0f / lsum;
+      // epilogue: O / l for this warp's 16 of the 64 output columns, split, stored from
+      // registers (hi at column h * 64, lo at H + h * 64 of the [tokens, 2H] output)
+      ok = al_wait(&bar_o[i & 1], (i >> 1) & 1, ERR_AT_O, &s_fail) && ok;
+      at_fence_after();
+      float v[AT_OW], vl[AT_OW];
+      at_ld16(tO + lane_off + AT_OW * hf, v);
+      at_ld16(tO + lane_off + 64 + AT_OW * hf, vl);
+      at_fence_before();
+      mbar_arrive(&bar_ofree[i & 1]);
+      if (ok && q < S) {
+        uint32_t hi[AT_OW / 2], lo[AT_OW / 2];
+#pragma unroll
+        for (int e = 0; e < AT_OW; e += 2)
+          at_split2((v[e] + vl[e]) * inv, (v[e + 1] + vl[e + 1]) * inv, hi[e / 2], lo[e / 2]);
+        __nv_bfloat16* orow = out + (int64_t(blk) * S + q) * (2 * H) + h * AT_DH + AT_OW * hf;
+        uint4* oh = reinterpret_cast<uint4*>(orow);
+        uint4* ol = reinterpret_cast<uint4*>(orow + H);
+#pragma unroll
+        for (int u = 0; u < AT_OW / 8; ++u) {
+          oh[u] = make_uint4(hi[4 * u], hi[4 * u + 1], hi[4 * u + 2], hi[4 * u + 3]);
+          ol[u] = make_uint4(lo[4 * u], lo[4 * u + 1], lo[4 * u + 2], lo[4 * u + 3]);
+        }
+      }
+    }
+  }
+  at_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    at_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(AT_TMEM_COLS)
+                 : "memory");
+  }
+}
+
 // ------------------------------------------------------------------ host
 
 static PFN_cuTensorMapEncodeTiled_v12000 at_encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
+  // looked up once per process (a thread-safe static initialisation)
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = []() {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
                                          &q) == cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
+      return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+  }();
   return fn;
 }
 
@@ -592,22 +942,50 @@ cudaError_t launch_attention_tc(const __nv_bfloat16* qkv, int64_t batch, int S, 
          CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
   const int smem = at_smem_bytes(S, K);
-  static int attr = 0;
-  if (attr < smem) {
-    cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    attr = smem;
-  }
-  static int sms = 0;
-  if (!sms) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (sms <= 0) sms = 148;
-  }
+  cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void*>(attn_tc_kernel), smem);
+  if (e != cudaSuccess) return e;
+  const int sms = device_sm_count();
   const int64_t nitems = batch * heads * ((S + AT_QT - 1) / AT_QT);
   const dim3 grid(static_cast<unsigned>(nitems < sms ? nitems : sms));
   attn_tc_kernel<<<grid, AT_THREADS, smem, stream>>>(tm, tmo, S, K, H, B_max, heads, batch,
                                                         dist_bias, same_bias);
+  note_launch();
+  return cudaGetLastError();
+}
+
+static int al_smem_bytes(int S, int K) { return AL_SMEM + (S / K) * AL_BSTRIDE * 4; }
+
+bool attention_tc_long_supported(int S, int K, int H, int heads, int B_max) {
+  return H / heads == AT_DH && S > AT_KMAX && S <= AL_KMAX && K >= 1 && H % 64 == 0 &&
+         B_max <= 64 && al_smem_bytes(S, K) <= AT_SMEM_MAX;
+}
+
+cudaError_t launch_attention_tc_long(const __nv_bfloat16* qkv, int64_t batch, int S, int K,
+                                     int H, int heads, int B_max, const float* dist_bias,
+                                     const float* same_bias, __nv_bfloat16* out,
+                                     cudaStream_t stream) {
+  auto fn = at_encode_fn();
+  if (!fn || !attention_tc_long_supported(S, K, H, heads, B_max) ||
+      reinterpret_cast<uintptr_t>(out) % 16)
+    return cudaErrorInvalidValue;
+  const int64_t M = batch * S;
+  CUtensorMap tm;
+  const cuuint64_t dims[2] = {cuuint64_t(6 * H), cuuint64_t(M)};
+  const cuuint64_t strides[1] = {cuuint64_t(6 * H) * 2};
+  const cuuint32_t box[2] = {64, 128};
+  const cuuint32_t estr[2] = {1, 1};
+  if (fn(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<__nv_bfloat16*>(qkv), dims, strides,
+         box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  const int smem = al_smem_bytes(S, K);
+  cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void*>(attn_tc_long_kernel), smem);
+  if (e != cudaSuccess) return e;
+  const int sms = device_sm_count();
+  const int64_t nitems = batch * heads * ((S + AT_QT - 1) / AT_QT);
+  const dim3 grid(static_cast<unsigned>(nitems < sms ? nitems : sms));
+  attn_tc_long_kernel<<<grid, AT_THREADS, smem, stream>>>(tm, out, S, K, H, B_max, heads, batch,
+                                                          dist_bias, same_bias);
   note_launch();
   return cudaGetLastError();
 }

@@ -10,7 +10,8 @@ size_t k1_workspace_bytes(int64_t batch, int B, int64_t V, int esize);
 cudaError_t k1_launch(const void* logits, int esize, int64_t batch, int B, int64_t V, int K,
                       int32_t* cand_id, float* cand_logit, float* lse, void* ws,
                       cudaStream_t stream, int64_t row_stride = 0, int id_offset = 0,
-                      void* records = nullptr);
+                      void* records = nullptr, long long wait_limit = WAIT_LIMIT_CYCLES,
+                      bool withhold_first = false);
 size_t k1_shard_record_bytes(int K);
 cudaError_t k1_merge_launch(const void* records, int n, int64_t rows, int K, int32_t* cand_id,
                             float* cand_logit, float* lse, cudaStream_t stream);
@@ -18,6 +19,13 @@ cudaError_t k1_read_device_error(uint32_t* code);
 
 // message returned by lilicorr_last_error() for this thread (lilicorr_api.cu)
 void set_last_error(const char* msg);
+
+// Per-device host state (lilicorr_api.cu), safe to call from several host threads:
+// the SM count of the current device (148 when no device can be queried), and the
+// dynamic shared-memory limit of a kernel raised to at least `bytes` on the current
+// device (cudaFuncSetAttribute once per kernel, size and device).
+int device_sm_count();
+cudaError_t allow_dynamic_smem(const void* kernel, int bytes);
 
 // a4 scores + a5 walk (walk.cu)
 cudaError_t launch_pair_scores(const float* heads, const float* anchor_raw, int64_t anchor_stride,
@@ -86,6 +94,13 @@ bool attention_tc_supported(int S, int K, int H, int heads, int B_max);
 cudaError_t launch_attention_tc(const __nv_bfloat16* qkv, int64_t batch, int S, int K, int H,
                                 int heads, int B_max, const float* dist_bias,
                                 const float* same_bias, __nv_bfloat16* out, cudaStream_t stream);
+// tcgen05 attention for head dim 64 and 257..512 tokens, keys in chunks of 128 with an
+// online softmax (attn_tc.cu)
+bool attention_tc_long_supported(int S, int K, int H, int heads, int B_max);
+cudaError_t launch_attention_tc_long(const __nv_bfloat16* qkv, int64_t batch, int S, int K,
+                                     int H, int heads, int B_max, const float* dist_bias,
+                                     const float* same_bias, __nv_bfloat16* out,
+                                     cudaStream_t stream);
 cudaError_t at_read_device_error(uint32_t* code);
 cudaError_t launch_rows_bias(const float* bias, int64_t rows, int N, float* out,
                              cudaStream_t stream);

@@ -17,6 +17,36 @@ void note_launch(int n) { g_launches.fetch_add(uint64_t(n), std::memory_order_re
 static thread_local std::string t_last_error;
 void set_last_error(const char* msg) { t_last_error = msg; }
 
+// ---- per-device host state (one mutex: these are looked up once per launch at most)
+static std::mutex g_dev_mu;
+static std::map<std::pair<const void*, int>, int> g_smem_allowed;  // (kernel, device) -> bytes
+static std::map<int, int> g_sm_count;                               // device -> SMs
+
+int device_sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  auto it = g_sm_count.find(dev);
+  if (it != g_sm_count.end()) return it->second;
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    return 148;
+  g_sm_count[dev] = n;
+  return n;
+}
+
+cudaError_t allow_dynamic_smem(const void* kernel, int bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  int& have = g_smem_allowed[{kernel, dev}];
+  if (have >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) have = bytes;
+  return e;
+}
+
 static lilicorr_status cuda_fail(cudaError_t e, const char* where) {
   t_last_error = std::string(where) + ": " + cudaGetErrorString(e);
   return LILICORR_ERR_CUDA;
@@ -635,6 +665,10 @@ lilicorr_status lilicorr_rerank(const lilicorr_weights* w, const void* logits,
     if (attention_tc_supported(S, K, H, d.heads, d.B_max))
       LC_CUDA(launch_attention_tc(qkv, batch, S, K, H, d.heads, d.B_max, L.dist, L.same, act1,
                                   stream),
+              "attention");
+    else if (attention_tc_long_supported(S, K, H, d.heads, d.B_max))
+      LC_CUDA(launch_attention_tc_long(qkv, batch, S, K, H, d.heads, d.B_max, L.dist, L.same,
+                                       act1, stream),
               "attention");
     else
       LC_CUDA(launch_attention(qkv, batch, S, K, H, d.heads, d.B_max, L.dist, L.same, act1, stream),

@@ -1,9 +1,9 @@
 """The whole path on the GPU against the oracle.
 
 Walk (a5) fed the oracle's own scores: choices bit-exact.  End to end: candidate ids
-bit-exact, lse within 1e-5, pair scores within 1e-3, committed tokens bit-exact unless
-the oracle's own top-2 margin at the first differing slot is below twice the measured
-score difference (reported as tie-ambiguous, never silently accepted)."""
+bit-exact, lse within 1e-5, pair scores within 1e-3, committed tokens bit-identical to the
+oracle on every block (a divergence at a float32 tie of the oracle's own scores is listed
+in the parity record and still fails these seeded cases)."""
 import json
 import os
 
@@ -13,7 +13,8 @@ import torch
 
 from oracle import lilicorr_oracle as O
 from synth import make_workload
-from tests.gpu_util import (SCORE_ATOL, check_block, dev_bf16, dev_logits, oracle_block)
+from tests.gpu_util import (SCORE_ATOL, assert_no_divergence, check_block, dev_bf16, dev_logits,
+                            oracle_block, report_for)
 
 pytestmark = pytest.mark.gpu
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
@@ -71,12 +72,18 @@ def _gpu_run(lc, wl, weights=None, taps=True, blocks=None):
     return res
 
 
-def _compare(lc, wl, blocks=None, report=None):
+def _label(name, kw):
+    return name + "".join(f" {k}={v}" for k, v in sorted(kw.items()))
+
+
+def _compare(lc, wl, blocks=None, label=None):
     gpu = _gpu_run(lc, wl)
-    report = {} if report is None else report
+    label = label or wl.name
+    report = report_for(label)
     for b in (range(wl.batch) if blocks is None else blocks):
         ref = oracle_block(wl, b)
         check_block(gpu, ref, b, report)
+    assert_no_divergence(report, label)
     return gpu, report
 
 
@@ -95,14 +102,19 @@ SMALL = [  # name, overrides
     ("single", dict(V=2048, batch=2, B=26)),         # 25 query slots: the largest bias
                                                      # table of the tcgen05 attention
     ("single", dict(V=2048, batch=2, B=27)),         # 26: the mma.sync attention instead
+    # lattices of 257..512 tokens: the chunked tcgen05 attention (keys in chunks of 128)
+    ("single", dict(V=2048, batch=3, K=20)),         # 300 tokens: 3 chunks, ragged last
+    ("single", dict(V=2048, batch=2, K=24, B=12)),   # 264 tokens, 11 slots
+    ("widepool", dict(V=2048, batch=2, B=12)),       # 352 tokens at hidden 512
+    ("single", dict(V=2048, batch=2, K=32, B=17)),   # 512 tokens: 4 full chunks
+    ("single", dict(V=2048, batch=1, K=32, B=18)),   # 544 tokens: the mma.sync attention
 ]
 
 
 @pytest.mark.parametrize("name,kw", SMALL)
 def test_rerank_small(lc, name, kw):
     wl = make_workload(name, **kw)
-    gpu, rep = _compare(lc, wl)
-    print(name, kw, rep)
+    gpu, rep = _compare(lc, wl, label="small: " + _label(name, kw))
     if kw.get("K") == 1:      # K = 1 reproduces the per-slot argmax block
         x = wl.logits_f32()
         for b in range(wl.batch):
@@ -156,8 +168,7 @@ def test_rerank_full_size_sampled_blocks(lc, name, kw, nblocks):
     wl = make_workload(name, **kw)
     rng = np.random.default_rng(1)
     blocks = sorted(rng.choice(wl.batch, nblocks, replace=False).tolist())
-    _, rep = _compare(lc, wl, blocks)
-    print(name, rep)
+    _compare(lc, wl, blocks, label="sampled: " + _label(name, kw))
 
 
 def test_rerank_captures_in_a_cuda_graph(lc):
@@ -201,7 +212,29 @@ def test_attention_rebase_when_far_keys_dominate(lc):
         f = bf16_bits_to_f32(bits).reshape(bits.shape)
         f[:, Bm - 2 + 8:] += 14.0
         wl.weights[f"layers.{l}.dist_bias"] = f32_to_bf16_bits(f).reshape(bits.shape)
-    gpu, rep = _compare(lc, wl)
+    gpu, rep = _compare(lc, wl, label="attention re-base case")
+    for b in range(wl.batch):
+        ref = oracle_block(wl, b)
+        g = gpu["hidden"][b].reshape(ref["hidden"].shape)
+        assert np.abs(g - ref["hidden"]).max() <= 1e-4
+
+
+def test_long_attention_rebase_when_far_chunks_dominate(lc):
+    """Wide pool (480 tokens, keys in four chunks of 128): slot-distance biases of +14 for
+    keys five or more slots ahead make the later key chunks dominate the first slots'
+    queries by more than 2^16, so the chunked attention re-bases those rows on a later
+    chunk and rescales the output accumulated so far.  Encoder output and tokens still
+    match the oracle."""
+    wl = make_workload("widepool", V=2048, batch=2)
+    Bm = wl.dims["B_max"]
+    from synth.inputs import bf16_bits_to_f32, f32_to_bf16_bits
+    for l in range(wl.dims["layers"]):
+        bits = wl.weights[f"layers.{l}.dist_bias"]
+        f = bf16_bits_to_f32(bits).reshape(bits.shape)
+        f[:, Bm - 2 + 5:] += 14.0
+        f[:, Bm - 2 + 10:] += 14.0
+        wl.weights[f"layers.{l}.dist_bias"] = f32_to_bf16_bits(f).reshape(bits.shape)
+    gpu, rep = _compare(lc, wl, label="long attention re-base case")
     for b in range(wl.batch):
         ref = oracle_block(wl, b)
         g = gpu["hidden"][b].reshape(ref["hidden"].shape)
