@@ -7,6 +7,7 @@ from .api import (  # noqa: F401
     LilicorrError,
     Weights,
     device_error,
+    diag_wait_timeout,
     greedy_walk,
     viterbi,
     launch_count,

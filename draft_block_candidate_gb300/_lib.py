@@ -52,6 +52,7 @@ SIGNATURES = {
     "lilicorr_last_error": (C.c_char_p, []),
     "lilicorr_launch_count": (C.c_uint64, []),
     "lilicorr_device_error": (C.c_int, [C.POINTER(C.c_uint32)]),
+    "lilicorr_diag_wait_timeout": (C.c_int, [_P, C.c_int64, C.c_uint32, _P, _P, _P, _P]),
     "lilicorr_stage_timing": (None, [C.c_int]),
     "lilicorr_stage_times": (C.c_int32, [C.POINTER(C.c_double), C.POINTER(C.c_int64),
                                          C.c_int32, C.POINTER(C.c_int64)]),

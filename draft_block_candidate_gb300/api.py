@@ -350,3 +350,17 @@ def stage_times() -> Dict[str, dict]:
            for i in range(k)}
     out["calls"] = int(calls.value)
     return out
+
+
+def diag_wait_timeout(logits_row: torch.Tensor, limit_cycles: int, stream=None) -> None:
+    """lilicorr_diag_wait_timeout on one bf16 row [V] (V <= 16384): a logit pass whose only
+    copy is withheld, so its bounded waits give up; read the result with device_error()."""
+    if logits_row.dtype != torch.bfloat16 or logits_row.dim() != 1:
+        raise ValueError("expected one bf16 row")
+    dev = logits_row.device
+    cid = torch.empty(1, dtype=torch.int32, device=dev)
+    cv = torch.empty(1, dtype=torch.float32, device=dev)
+    lse = torch.empty(1, dtype=torch.float32, device=dev)
+    st = L.lib().lilicorr_diag_wait_timeout(_ptr(logits_row), logits_row.numel(), limit_cycles,
+                                            _ptr(cid), _ptr(cv), _ptr(lse), _stream(stream))
+    _check(st, "lilicorr_diag_wait_timeout")

@@ -75,15 +75,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for phase `parity` of `bar` to complete, at most WAIT_LIMIT_CYCLES.  Returns false
-// (and records `site`) if the limit was hit.
+// Wait for phase `parity` of `bar` to complete, at most `limit` SM cycles (default
+// WAIT_LIMIT_CYCLES).  Returns false (and records `site`) if the limit was hit.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
-                                                  uint32_t* err_word, uint32_t site) {
+                                                  uint32_t* err_word, uint32_t site,
+                                                  long long limit = WAIT_LIMIT_CYCLES) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   for (uint32_t n = 1;; ++n) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((n & 63) == 0 && clock64() - t0 > WAIT_LIMIT_CYCLES) {
+    if ((n & 63) == 0 && clock64() - t0 > limit) {
       atomicOr(err_word, site);
       return false;
     }

@@ -523,13 +523,14 @@ cudaError_t launch_attention(const __nv_bfloat16* qkv, int64_t batch, int S, int
   const int dh = H / heads;
   const dim3 grid((S + AT_QROWS - 1) / AT_QROWS, heads, static_cast<unsigned>(batch));
   const int smem = (2 + 8) * AT_KT * dh * 2;
-  static bool attr = false;
-  if (!attr) {
-    cudaFuncSetAttribute(attention_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, 10 * 64 * 32 * 2);
-    cudaFuncSetAttribute(attention_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, 10 * 64 * 64 * 2);
-    cudaFuncSetAttribute(attention_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, 10 * 64 * 128 * 2);
-    attr = true;
+  cudaError_t e = cudaSuccess;
+  switch (dh) {
+    case 32: e = allow_dynamic_smem(reinterpret_cast<const void*>(attention_kernel<32>), smem); break;
+    case 64: e = allow_dynamic_smem(reinterpret_cast<const void*>(attention_kernel<64>), smem); break;
+    case 128: e = allow_dynamic_smem(reinterpret_cast<const void*>(attention_kernel<128>), smem); break;
+    default: return cudaErrorInvalidValue;
   }
+  if (e != cudaSuccess) return e;
   switch (dh) {
     case 32: attention_kernel<32><<<grid, AT_THREADS, smem, stream>>>(qkv, S, K, H, B_max, dist_bias, same_bias, out); break;
     case 64: attention_kernel<64><<<grid, AT_THREADS, smem, stream>>>(qkv, S, K, H, B_max, dist_bias, same_bias, out); break;

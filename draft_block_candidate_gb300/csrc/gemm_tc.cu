@@ -510,15 +510,16 @@ __global__ void __launch_bounds__(32 * (2 + EW), 1)
 // ------------------------------------------------------------------ host
 
 static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
+  // looked up once per process (a thread-safe static initialisation)
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = []() {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
                                          &q) == cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
+      return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+  }();
   return fn;
 }
 
@@ -585,43 +586,25 @@ cudaError_t launch_gemm(int epi, const GemmArgs& g, cudaStream_t stream) {
   const bool two = epi == EPI_NODE;
   constexpr int sp = tc_smem(3, 1, true), sp2 = tc_smem(2, 2, true), sn = tc_smem(4, 1, false);
   constexpr int sw = tc_smem(2, 1, true, 16);
-  static bool attr = false;
-  if (!attr) {
-#define LC_TC_ATTR(E)                                                                        \
-  cudaFuncSetAttribute(gemm_tc_kernel<E, 3, 1, true>,                                        \
-                       cudaFuncAttributeMaxDynamicSharedMemorySize, sp);                     \
-  cudaFuncSetAttribute(gemm_tc_kernel<E, 2, 2, true>,                                        \
-                       cudaFuncAttributeMaxDynamicSharedMemorySize, sp2);                    \
-  cudaFuncSetAttribute(gemm_tc_kernel<E, 2, 1, true, 16>,                                    \
-                       cudaFuncAttributeMaxDynamicSharedMemorySize, sw);                     \
-  cudaFuncSetAttribute(gemm_tc_kernel<E, 4, 1, false>,                                       \
-                       cudaFuncAttributeMaxDynamicSharedMemorySize, sn);
-    LC_TC_ATTR(EPI_F32)
-    LC_TC_ATTR(EPI_RESID)
-    LC_TC_ATTR(EPI_SPLIT)
-    LC_TC_ATTR(EPI_SPLIT_SILU)
-    LC_TC_ATTR(EPI_NODE)
-#undef LC_TC_ATTR
-    attr = true;
-  }
-  static int sms = 0;
-  if (!sms) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (sms <= 0) sms = 148;
-  }
+  const int sms = device_sm_count();
   const int64_t ntiles = int64_t((g.N + TC_BN - 1) / TC_BN) * ((g.M + TC_BM - 1) / TC_BM);
   const dim3 grid(static_cast<unsigned>(ntiles < sms ? ntiles : sms));
+  cudaError_t e = cudaSuccess;
+  // the chosen instance's shared-memory limit (once per device), then its launch
+#define LC_TC_RUN(E, KERNEL, THREADS, SMEM)                                                  \
+  {                                                                                          \
+    e = allow_dynamic_smem(reinterpret_cast<const void*>(KERNEL), SMEM);                     \
+    if (e == cudaSuccess) KERNEL<<<grid, THREADS, SMEM, stream>>>(ta, tb, tc, g);            \
+  }
 #define LC_TC_LAUNCH(E)                                                                      \
   if (pair && wide)                                                                          \
-    gemm_tc_kernel<E, 2, 1, true, 16><<<grid, 32 * 18, sw, stream>>>(ta, tb, tc, g);         \
+    LC_TC_RUN(E, (gemm_tc_kernel<E, 2, 1, true, 16>), 32 * 18, sw)                           \
   else if (pair && two)                                                                      \
-    gemm_tc_kernel<E, 2, 2, true><<<grid, TC_THREADS, sp2, stream>>>(ta, tb, tc, g);         \
+    LC_TC_RUN(E, (gemm_tc_kernel<E, 2, 2, true>), TC_THREADS, sp2)                           \
   else if (pair)                                                                             \
-    gemm_tc_kernel<E, 3, 1, true><<<grid, TC_THREADS, sp, stream>>>(ta, tb, tc, g);          \
+    LC_TC_RUN(E, (gemm_tc_kernel<E, 3, 1, true>), TC_THREADS, sp)                            \
   else                                                                                       \
-    gemm_tc_kernel<E, 4, 1, false><<<grid, TC_THREADS, sn, stream>>>(ta, tb, tc, g);
+    LC_TC_RUN(E, (gemm_tc_kernel<E, 4, 1, false>), TC_THREADS, sn)
   switch (epi) {
     case EPI_F32: LC_TC_LAUNCH(EPI_F32) break;
     case EPI_RESID: LC_TC_LAUNCH(EPI_RESID) break;
@@ -629,7 +612,9 @@ cudaError_t launch_gemm(int epi, const GemmArgs& g, cudaStream_t stream) {
     case EPI_SPLIT_SILU: LC_TC_LAUNCH(EPI_SPLIT_SILU) break;
     default: LC_TC_LAUNCH(EPI_NODE) break;
   }
+#undef LC_TC_RUN
 #undef LC_TC_LAUNCH
+  if (e != cudaSuccess) return e;
   note_launch();
   return cudaGetLastError();
 }
@@ -879,13 +864,7 @@ bool lm_head_supported(int64_t rows, int64_t V, int D, int K) {
 }
 
 static void lm_head_plan(int64_t rows, int64_t V, int* nr, int* tpr) {
-  static int sms = 0;
-  if (!sms) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (sms <= 0) sms = 148;
-  }
+  const int sms = device_sm_count();
   const int64_t MT = (rows + TC_BM - 1) / TC_BM, NT = (V + TC_BN - 1) / TC_BN;
   int64_t want = std::max<int64_t>(1, (sms + MT / 2) / MT);  // ranges so that MT x nr ~ SMs
   want = std::min<int64_t>(want, NT);
@@ -920,12 +899,13 @@ cudaError_t launch_lm_head_topk(const __nv_bfloat16* hidden, const __nv_bfloat16
   const int64_t MT = (rows + TC_BM - 1) / TC_BM;
   const dim3 grid(static_cast<unsigned>(MT * la.nr));
   constexpr int sm = 4 * (TC_A_BYTES + TC_B_BYTES) + 1024;
-  static bool attr = false;
-  if (!attr) {
-    cudaFuncSetAttribute(lm_head_topk_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
-    cudaFuncSetAttribute(lm_head_topk_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
-    cudaFuncSetAttribute(lm_head_topk_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
-    attr = true;
+  {
+    cudaError_t e = allow_dynamic_smem(
+        K <= 8    ? reinterpret_cast<const void*>(lm_head_topk_kernel<8>)
+        : K <= 16 ? reinterpret_cast<const void*>(lm_head_topk_kernel<16>)
+                  : reinterpret_cast<const void*>(lm_head_topk_kernel<32>),
+        sm);
+    if (e != cudaSuccess) return e;
   }
   if (K <= 8)
     lm_head_topk_kernel<8><<<grid, TC_THREADS, sm, stream>>>(ta, tb, la);

@@ -26,13 +26,12 @@
 //     + bitonic merge).
 //   * the CTA floor is the K-th largest of 32 thread-group running maxima (K distinct
 //     elements are at least that large).  After stage 0 the consumer warps meet once so
-//     that the first floor covers the whole stage; afterwards the producer warp keeps it
-//     fresh (once per stage and while it waits), and every fold raises it to the warp's
-//     own K-th entry.
+//     that the first floor covers the whole stage; afterwards the producer warp raises
+//     it after every refill, and every fold raises it to the warp's own K-th entry.
 // At the end every warp offers its K-th entry to the floor; only queue and buffer entries
 // at or above the final floor are gathered into one list, which one warp folds.
-// Rows are split into P segments when there are too few rows to fill 152 SMs; the last
-// CTA of a row (atomic counter, no waiting) merges the P partial results.
+// Rows are split into P segments only when fewer than about 90 rows are given (a single
+// request); the last CTA of a row (atomic counter, no waiting) merges the P partials.
 #include <float.h>
 #include <limits.h>
 
@@ -91,6 +90,8 @@ struct K1Params {
   int64_t row_stride;  // elements between consecutive rows (V for a whole-vocabulary pass)
   int id_offset;       // added to every candidate id (a vocabulary shard's first id)
   char* records;       // vocabulary-shard mode: packed per-row records instead of outputs
+  long long wait_limit;  // SM cycles after which a wait gives up (WAIT_LIMIT_CYCLES)
+  int withhold_first;    // self-check only: stage 0's copy is announced but never issued
 };
 
 // Packed per-row record of a vocabulary shard: {m2, s, v[K], id[K]}, K * 8 + 8 bytes.
@@ -372,7 +373,8 @@ __global__ void __launch_bounds__(K1_THREADS, K1_MIN_BLOCKS) logit_pass_kernel(c
       const int sl = st % K1_NSTAGES;
       const uint32_t bytes = static_cast<uint32_t>(min(K1_STAGE_BYTES, seg_bytes - off));
       mbar_arrive_expect_tx(&full_bar[sl], bytes);
-      bulk_g2s(stage[sl], p.logits + seg_lo + off, bytes, &full_bar[sl]);
+      if (!(p.withhold_first && st == 0))
+        bulk_g2s(stage[sl], p.logits + seg_lo + off, bytes, &full_bar[sl]);
       issued = st + 1;
     };
     if (lane == 0)
@@ -396,15 +398,12 @@ __global__ void __launch_bounds__(K1_THREADS, K1_MIN_BLOCKS) logit_pass_kernel(c
       queue_absorb(q, xv, has ? static_cast<int>(first / ES - row_elem0) + lane : INT_MAX, lane,
                    K);
     }
-    // Refill each slot as soon as every consumer warp has released it; while waiting,
-    // keep the CTA floor fresh from the group maxima.
+    // Refill each slot as soon as every consumer warp has released it (the wait only
+    // polls, so a released slot is refilled at once); after each refill the CTA floor is
+    // raised to the K-th largest of the group maxima.
     for (int st = K1_NSTAGES; st < nstages; ++st) {
       const int sl = st % K1_NSTAGES;
       const uint32_t par = ((st / K1_NSTAGES) - 1) & 1;
-      {
-        const float f = group_floor(s_gmax, lane, K);
-        if (lane == 0) atomicMax(&s_floor, float_key(f));
-      }
       const long long t0 = clock64();
       int ready = 0;
       for (;;) {
@@ -413,7 +412,7 @@ __global__ void __launch_bounds__(K1_THREADS, K1_MIN_BLOCKS) logit_pass_kernel(c
             ready = 1;
           } else if (s_abort) {
             ready = 2;
-          } else if (clock64() - t0 > WAIT_LIMIT_CYCLES) {
+          } else if (clock64() - t0 > p.wait_limit) {
             atomicOr(&g_err_k1, ERR_K1_EMPTY_WAIT);
             s_abort = 1;
             ready = 2;
@@ -421,12 +420,14 @@ __global__ void __launch_bounds__(K1_THREADS, K1_MIN_BLOCKS) logit_pass_kernel(c
         }
         ready = __shfl_sync(FULL_MASK, ready, 0);
         if (ready != 0) break;
-        const float f = group_floor(s_gmax, lane, K);
-        if (lane == 0) atomicMax(&s_floor, float_key(f));
         __nanosleep(K1_POLL_NS);
       }
       if (ready == 2) break;
       if (lane == 0) issue(st);
+      {
+        const float f = group_floor(s_gmax, lane, K);
+        if (lane == 0) atomicMax(&s_floor, float_key(f));
+      }
     }
   } else {
     // ================= consumer warps =================
@@ -517,7 +518,8 @@ __global__ void __launch_bounds__(K1_THREADS, K1_MIN_BLOCKS) logit_pass_kernel(c
 
     for (int st = 0; st < nstages; ++st) {
       const int sl = st % K1_NSTAGES;
-      if (!mbar_wait_bounded(&full_bar[sl], (st / K1_NSTAGES) & 1, &g_err_k1, ERR_K1_FULL_WAIT))
+      if (!mbar_wait_bounded(&full_bar[sl], (st / K1_NSTAGES) & 1, &g_err_k1, ERR_K1_FULL_WAIT,
+                             p.wait_limit))
         s_abort = 1;
       if (st > 0 && s_abort) break;  // stage 0 first meets the other consumer warps
       const int nbytes = min(K1_STAGE_BYTES, seg_bytes - st * K1_STAGE_BYTES);
@@ -585,7 +587,7 @@ __global__ void __launch_bounds__(K1_THREADS, K1_MIN_BLOCKS) logit_pass_kernel(c
     if (warp == K1_CWARPS && lane == 0)
       for (int st = max(0, issued - K1_NSTAGES); st < issued; ++st)
         mbar_wait_bounded(&full_bar[st % K1_NSTAGES], (st / K1_NSTAGES) & 1, &g_err_k1,
-                          ERR_K1_DRAIN);
+                          ERR_K1_DRAIN, p.wait_limit);
     return;
   }
   float* uv = reinterpret_cast<float*>(stage[0]);
@@ -719,42 +721,19 @@ struct K1Plan {
   size_t ws_bytes;
 };
 
-static int g_num_sms = 0;
-
-static int num_sms() {
-  if (g_num_sms == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
-    if (g_num_sms <= 0) g_num_sms = 148;
-  }
-  return g_num_sms;
-}
-
 K1Plan k1_plan(int64_t batch, int B, int64_t V, int esize) {
   K1Plan pl{1, 0, 0};
   const int64_t rows = batch * (B - 1);
   const int64_t row_bytes = V * esize;
   const int64_t stages = (row_bytes + K1_STAGE_BYTES - 1) / K1_STAGE_BYTES;
-  const int64_t conc = int64_t(num_sms()) * K1_MIN_BLOCKS;  // resident CTAs
-  // Smallest P (1..64, at least one stage per segment) whose work fills whole waves
-  // of resident CTAs to within 5%; otherwise the best-filled P.
-  int bestP = 1;
-  double best_eff = -1.0;
-  const int64_t pmax = std::max<int64_t>(1, std::min<int64_t>(64, stages));
-  for (int P = 1; P <= pmax; ++P) {
-    const double waves = double(rows * P) / double(conc);
-    const double eff = waves / std::ceil(waves);
-    if (eff >= 0.95) {
-      bestP = P;
-      break;
-    }
-    if (eff > best_eff + 1e-9) {
-      best_eff = eff;
-      bestP = P;
-    }
-  }
-  pl.P = bestP;
+  // A row is split into P segments only when there are too few rows to keep about 90
+  // CTAs streaming.  Measured on GB300 at V = 151,936 bf16 (P = 1 vs the best split):
+  // 15 rows 18.7 vs 15.7 us (P = 6); 60 rows 17.4 us, unsplit best; from 240 rows on,
+  // every split is slower than one CTA per row (960 rows: 74 us unsplit, 104 us at P = 2,
+  // 145 us at P = 4), because a CTA's start, first-stage latency and final gather cost
+  // about as much as streaming a third of a row.
+  const int64_t want = rows >= 90 ? 1 : 90 / rows;
+  pl.P = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>({want, 64, stages})));
   const int64_t seg = (row_bytes + pl.P - 1) / pl.P;
   pl.seg_bytes = std::max<int64_t>(16, (seg + 15) / 16 * 16);
   if (pl.P > 1)
@@ -768,7 +747,8 @@ size_t k1_workspace_bytes(int64_t batch, int B, int64_t V, int esize) {
 
 cudaError_t k1_launch(const void* logits, int esize, int64_t batch, int B, int64_t V, int K,
                       int32_t* cand_id, float* cand_logit, float* lse, void* ws,
-                      cudaStream_t stream, int64_t row_stride, int id_offset, void* records) {
+                      cudaStream_t stream, int64_t row_stride, int id_offset, void* records,
+                      long long wait_limit, bool withhold_first) {
   const K1Plan pl = k1_plan(batch, B, V, esize);
   K1Params prm;
   prm.logits = static_cast<const char*>(logits);
@@ -786,6 +766,8 @@ cudaError_t k1_launch(const void* logits, int esize, int64_t batch, int B, int64
   prm.row_stride = row_stride > 0 ? row_stride : V;
   prm.id_offset = id_offset;
   prm.records = static_cast<char*>(records);
+  prm.wait_limit = wait_limit;
+  prm.withhold_first = withhold_first ? 1 : 0;
   const int64_t rows = batch * (B - 1);
   if (pl.P > 1) {
     prm.partials = static_cast<K1Partial*>(ws);
@@ -796,13 +778,11 @@ cudaError_t k1_launch(const void* logits, int esize, int64_t batch, int B, int64
   }
   const dim3 grid(static_cast<unsigned>(rows * pl.P));
   constexpr int dyn = K1_NSTAGES * K1_STAGE_BYTES;
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaFuncSetAttribute(logit_pass_kernel<__nv_bfloat16>,
-                         cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
-    cudaFuncSetAttribute(logit_pass_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         dyn);
-    attr_done = true;
+  {
+    cudaError_t e = esize == 2 ? allow_dynamic_smem(
+                                     reinterpret_cast<const void*>(logit_pass_kernel<__nv_bfloat16>), dyn)
+                               : allow_dynamic_smem(reinterpret_cast<const void*>(logit_pass_kernel<float>), dyn);
+    if (e != cudaSuccess) return e;
   }
   if (esize == 2)
     logit_pass_kernel<__nv_bfloat16><<<grid, K1_THREADS, dyn, stream>>>(prm);
@@ -895,6 +875,29 @@ extern "C" lilicorr_status lilicorr_topk_lse_noalloc(const void* logits, lilicor
   // k1_launch zeroes the arrival counters inside the scratch before the kernel runs.
   e = k1_launch(logits, es, batch, B, V, K, cand_id, cand_logit, lse, scratch,
                 static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) {
+    set_last_error(cudaGetErrorString(e));
+    return LILICORR_ERR_CUDA;
+  }
+  return LILICORR_OK;
+}
+
+// Self-check of the bounded waits: one row that fits one stage, its only copy announced
+// to the stage's barrier but never issued.  The consumer warps' wait and the producer's
+// final drain both give up after `limit_cycles`, set their site bits and return; no
+// output is written.  Nothing else is in flight, so the kernel ends cleanly.
+extern "C" lilicorr_status lilicorr_diag_wait_timeout(const void* logits, int64_t V,
+                                                      uint32_t limit_cycles, int32_t* cand_id,
+                                                      float* cand_logit, float* lse,
+                                                      void* stream) {
+  using namespace lilicorr;
+  if (!logits || !cand_id || !cand_logit || !lse) return LILICORR_ERR_INVALID_ARG;
+  if (V < 1 || V * 2 > K1_STAGE_BYTES || reinterpret_cast<uintptr_t>(logits) % 16)
+    return LILICORR_ERR_INVALID_ARG;
+  if (limit_cycles < 1000u || limit_cycles > 100000000u) return LILICORR_ERR_INVALID_ARG;
+  const cudaError_t e = k1_launch(logits, 2, 1, 2, V, 1, cand_id, cand_logit, lse, nullptr,
+                                  static_cast<cudaStream_t>(stream), 0, 0, nullptr,
+                                  static_cast<long long>(limit_cycles), true);
   if (e != cudaSuccess) {
     set_last_error(cudaGetErrorString(e));
     return LILICORR_ERR_CUDA;

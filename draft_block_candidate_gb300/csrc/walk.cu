@@ -412,12 +412,9 @@ cudaError_t launch_pair_scores(const float* heads, const float* anchor_raw, int6
   const size_t per_warp = ps_warp_floats(K, E) * sizeof(float);
   int pw = PS_MAX_WARPS;
   while (pw > 1 && pw * per_warp > size_t(200) * 1024) --pw;
-  static bool attr = false;
-  if (!attr) {
-    cudaFuncSetAttribute(pair_scores_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         static_cast<int>(size_t(200) * 1024));
-    attr = true;
-  }
+  cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void*>(pair_scores_kernel),
+                                     static_cast<int>(pw * per_warp));
+  if (e != cudaSuccess) return e;
   const dim3 grid(static_cast<unsigned>((B - 1 + pw - 1) / pw), static_cast<unsigned>(batch));
   pair_scores_kernel<<<grid, 32 * pw, pw * per_warp, stream>>>(heads, anchor_raw, anchor_stride, B,
                                                                 K, E, sigma, scores, out_tap,
@@ -433,12 +430,9 @@ cudaError_t launch_greedy_walk(const float* scores, const int32_t* cand_id,
   constexpr size_t kMaxStage = 96 * 1024;
   const size_t need = size_t(B - 1) * K * K * sizeof(float);
   const bool staged = need <= kMaxStage;  // otherwise the walk reads the scores in place
-  static bool attr = false;
-  if (!attr) {
-    cudaFuncSetAttribute(greedy_walk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         static_cast<int>(kMaxStage));
-    attr = true;
-  }
+  cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void*>(greedy_walk_kernel),
+                                     static_cast<int>(kMaxStage));
+  if (e != cudaSuccess) return e;
   greedy_walk_kernel<<<static_cast<unsigned>(batch), 32, staged ? need : 0, stream>>>(
       scores, cand_id, anchor_ids, batch, B, K, tokens, choice, path, staged);
   note_launch();
@@ -453,12 +447,9 @@ cudaError_t launch_viterbi(const float* scores, const int32_t* cand_id,
   const size_t need = size_t(B - 1) * K * K * sizeof(float);
   const bool staged = need <= kMaxStage;  // otherwise the scores are read in place
   const size_t aux = ((size_t(B - 1) * K + 15) & ~size_t(15)) + size_t(B - 1) * sizeof(int);
-  static bool attr = false;
-  if (!attr) {
-    cudaFuncSetAttribute(viterbi_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         static_cast<int>(kMaxStage + 4096));
-    attr = true;
-  }
+  cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void*>(viterbi_kernel),
+                                     static_cast<int>(kMaxStage + 4096));
+  if (e != cudaSuccess) return e;
   viterbi_kernel<<<static_cast<unsigned>(batch), 32, (staged ? need : 0) + aux, stream>>>(
       scores, cand_id, anchor_ids, batch, B, K, tokens, choice, path, total, staged);
   note_launch();

@@ -174,7 +174,10 @@ lilicorr_status lilicorr_topk_lse(const void* logits, lilicorr_dtype ldtype, int
  *   - A shape that needs more scratch than 4 MiB returns LILICORR_ERR_WORKSPACE with a
  *     message in lilicorr_last_error(); use lilicorr_topk_lse for it.
  *   - The first call on each device looks up the scratch's device address (the library
- *     caches it per device); make that first call before any stream capture.
+ *     caches it per device); make that first call before any stream capture.  A
+ *     cudaDeviceReset (or any re-creation of the device's primary context) invalidates
+ *     the cached address and the library's per-device kernel settings: reload the library
+ *     after one.
  *   - All calls share the one scratch array, which keeps the previous call's contents
  *     (the parts that must start at zero are cleared by every call).  Calls whose work
  *     overlaps on the GPU (different streams, or host threads without ordering) race on
@@ -290,6 +293,20 @@ uint64_t lilicorr_launch_count(void);
  * device): 0 = no error; otherwise one bit per wait site that gave up (bits 0-7 the logit
  * pass, bits 8-15 the tensor-core GEMM, bits 16-23 the tensor-core attention). */
 lilicorr_status lilicorr_device_error(uint32_t* code);
+/* Self-check of the device-side timeouts (a diagnostic of this library; the pages have no
+ * counterpart).  Runs the logit pass on one row of V bf16 logits (device memory, 16-byte
+ * aligned, 1 <= V <= 16384 so that the row is a single stage) with that stage's bulk copy
+ * announced to its barrier but never issued.  The consumer warps' bounded wait gives up
+ * after limit_cycles SM cycles (1000 <= limit_cycles <= 1e8), then the producer's final
+ * wait for its copies does too; each records its site bit (bit 0: stage wait, bit 1:
+ * drain) in the device error word and the kernel returns without writing cand_id [1],
+ * cand_logit [1] or lse [1] (device memory, still required).  Nothing faults, traps or
+ * hangs: the context stays usable.  Read the bits with lilicorr_device_error.
+ * Errors: LILICORR_ERR_INVALID_ARG for null pointers or sizes out of range,
+ * LILICORR_ERR_CUDA for a failed launch. */
+lilicorr_status lilicorr_diag_wait_timeout(const void* logits, int64_t V, uint32_t limit_cycles,
+                                           int32_t* cand_id, float* cand_logit, float* lse,
+                                           void* stream);
 
 /* Per-kernel timing.  When enabled, lilicorr_rerank records a CUDA event on its stream
  * after each of its launches.  lilicorr_stage_times() synchronises on the recorded

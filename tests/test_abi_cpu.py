@@ -190,3 +190,20 @@ def test_lm_head_entry_points_check_arguments(lib):
     assert f(p, p, 10, 1000, 100, 8, p, p, p, p, 1 << 20, None) == 1       # D % 64
     assert f(p, p, 10, 1000, 128, 0, p, p, p, p, 1 << 20, None) == 1       # K < 1
     assert f(C.c_void_p(258), p, 10, 1000, 128, 8, p, p, p, p, 1 << 20, None) == 1  # align
+
+
+def test_logit_pass_scratch_stays_within_the_static_array(lib):
+    """lilicorr_topk_lse_noalloc keeps its split-row scratch in a 4 MiB array compiled into
+    the library and refuses shapes that need more.  Rows are split into segments only when
+    fewer than 90 rows are given (at most 90 segment partials in all), so no shape reaches
+    the limit: the largest need over a grid of shapes stays a few tens of KB."""
+    worst = 0
+    for batch in (1, 2, 3, 5, 6, 64):
+        for B in (2, 3, 9, 16, 31):
+            for V in (1, 1000, 16385, 151_936, 1 << 20, (1 << 30) - 7):
+                for ld in (0, 1):
+                    for K in (1, 8, 32):
+                        if K > V:
+                            continue
+                        worst = max(worst, lib.lilicorr_topk_lse_workspace_bytes(batch, B, V, K, ld))
+    assert 0 < worst <= 64 << 10
