@@ -549,12 +549,13 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
 // tokens).  The keys no longer fit the shared memory at once, so each (128-query tile,
 // block, head) item walks its keys in chunks of 128 with an online softmax:
 //   warp 0     TMA: the item's Q (hi, lo), then per chunk K (hi, lo) and V (hi, lo) into
-//              two-stage rings; owns the TMEM allocation (S / P: two 128-column buffers,
-//              O': two 128-column buffers, one per item parity)
+//              two-stage rings; owns the TMEM allocation (S / P: three 128-column buffers,
+//              O': one 128-column buffer, which the epilogue empties before the next item's
+//              first product)
 //   warp 1     MMA: S(g+1) = Q K(g+1)^T (three split products) while the softmax warps
 //              work on chunk g, then O' += P(g) [V hi | V lo] (two products, N 128, P read
 //              from TMEM); S into a buffer waits until the product that read its previous
-//              P has completed
+//              P (three chunks back) has completed
 //   warps 2-17 per chunk: scale, add the slot bias, row maximum (four warps per query-row
 //              quarter, combined through shared memory), running maximum m: the first
 //              chunk sets it; a later chunk whose maximum exceeds m by more than 2^16
@@ -567,6 +568,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
 // Every wait is bounded and the first timeout makes every later wait of the CTA give up
 // at once, so that all warps still reach their named barriers and the final teardown.
 constexpr int AL_KC = 128;                     // keys per chunk
+constexpr int AL_SBUF = 3;                     // S / P buffers in TMEM (+ one O' buffer)
 constexpr int AL_KMAX = 512;
 constexpr int AL_BSTRIDE = AL_KMAX + 4;        // floats per bias-table row (bank offset)
 constexpr int AL_SMEM = 10 * AT_TILE + 1024;   // Q, K ring, V ring + the bias table
@@ -605,7 +607,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   // keys beyond the block
   float* s_btab = reinterpret_cast<float*>(sm + 10 * AT_TILE);
   __shared__ __align__(8) uint64_t bar_q, bar_qfree, bar_k[2], bar_kfree[2], bar_v[2],
-      bar_vfree[2], bar_s[2], bar_p[2], bar_pv[2], bar_o[2], bar_ofree[2];
+      bar_vfree[2], bar_s[AL_SBUF], bar_p[AL_SBUF], bar_pv[AL_SBUF], bar_o, bar_ofree;
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_fail;
   __shared__ float s_pmax[2][AT_NSPLIT][128], s_psum[AT_NSPLIT][128];
@@ -624,12 +626,14 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       mbar_init(&bar_kfree[b], 1);
       mbar_init(&bar_v[b], 1);
       mbar_init(&bar_vfree[b], 1);
+    }
+    for (int b = 0; b < AL_SBUF; ++b) {
       mbar_init(&bar_s[b], 1);
       mbar_init(&bar_p[b], 32 * AT_SOFT_WARPS);
       mbar_init(&bar_pv[b], 1);
-      mbar_init(&bar_o[b], 1);
-      mbar_init(&bar_ofree[b], 32 * AT_SOFT_WARPS);
     }
+    mbar_init(&bar_o, 1);
+    mbar_init(&bar_ofree, 32 * AT_SOFT_WARPS);
     s_fail = 0;
     fence_mbar_init();
   }
@@ -644,18 +648,21 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   __syncthreads();
   at_fence_after();
   const uint32_t tmem = s_tmem;
-  // S / P of chunk g in columns 128 (g & 1) .. +127; O' of item i in 256 + 128 (i & 1)
-  const uint32_t tS = tmem, tO0 = tmem + AT_O_COL;
-  // this CTA's items and chunks
-  const int my_items =
-      blockIdx.x < nitems ? static_cast<int>((nitems - 1 - blockIdx.x) / gridDim.x) + 1 : 0;
+  // S / P of chunk g in columns 128 (g % 3) .. +127; O' in columns 384..511
+  const uint32_t tS = tmem, tO = tmem + AL_SBUF * AL_KC;
+  // this CTA's items: a contiguous range, so that the four query tiles of a (block, head)
+  // run back to back (their K / V chunks come from L2) and the head, with its bias table,
+  // changes at most once or twice per CTA
+  const int64_t per = (nitems + gridDim.x - 1) / gridDim.x;
+  const int64_t first = int64_t(blockIdx.x) * per;
+  const int my_items = first < nitems ? static_cast<int>(min(per, nitems - first)) : 0;
   const int total = my_items * NC;
 
   if (warp == 0 && lane == 0) {
     // ---- producer
     int g = 0;
     bool ok = true;
-    ItemPos it(blockIdx.x, gridDim.x, QT, batch);
+    ItemPos it(first, 1, QT, batch);
     for (int i = 0; i < my_items && ok; ++i, it.next()) {
       const int tok0 = it.blk * S;
       const int cq = it.h * AT_DH, ck = H + it.h * AT_DH, cv = 2 * H + it.h * AT_DH, lo = 3 * H;
@@ -686,9 +693,9 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     // ---- MMA issuer: S(0); then per chunk g: S(g + 1), O' += P(g) V(g)
     constexpr uint32_t id_s = at_idesc(128, 128, false);
     constexpr uint32_t id_o = at_idesc(128, 128, true);
-    auto qk = [&](int b) {  // S into buffer b from K stage b (both follow the chunk parity)
+    auto qk = [&](int b, int st) {  // S into buffer b from K stage st
       const uint32_t d = tS + uint32_t(128 * b);
-      const uint8_t* kh = sK + 2 * b * AT_TILE;
+      const uint8_t* kh = sK + 2 * st * AT_TILE;
       const uint8_t* kl = kh + AT_TILE;
 #pragma unroll
       for (int ks = 0; ks < AT_DH / 16; ++ks) {
@@ -697,10 +704,10 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         at_mma(d, at_desc(sQl + ks * 32), at_desc(kh + ks * 32), id_s, 1);
       }
     };
-    auto pv = [&](int b, uint32_t tO, bool first) {
+    auto pv = [&](int b, int st, bool first) {
       // P for keys 32c..32c+31 of the chunk: TMEM columns 32c (hi, 16 packed columns) and
       // 32c + 16 (lo); a 16-key step j uses 8 of them
-      const uint8_t* vh = sV + 2 * b * AT_TILE;
+      const uint8_t* vh = sV + 2 * st * AT_TILE;
 #pragma unroll 4
       for (int j = 0; j < AL_KC / 16; ++j) {
         const uint32_t pc = uint32_t(128 * b + 32 * (j >> 1) + 8 * (j & 1));
@@ -713,42 +720,45 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
               al_wait(&bar_k[0], 0, ERR_AT_QK, &s_fail);
     if (ok) {
       at_fence_after();
-      qk(0);
+      qk(0, 0);
       at_commit(&bar_s[0]);
       at_commit(&bar_kfree[0]);
     }
     int i = 0, c = 0;  // item and chunk of g
+    int b = 0, u = 0;  // S / P buffer of g and its use count (g = 3 u + b)
     for (int g = 0; g < total && ok; ++g) {
       const int g1 = g + 1;
+      const int b1 = b + 1 == AL_SBUF ? 0 : b + 1, u1 = b1 == 0 ? u + 1 : u;
       if (g1 < total) {
+        // S(g + 1) into the buffer that PV(g - 2) read last: once that product is done
         const int c1 = c + 1 == NC ? 0 : c + 1;
         const int i1 = c1 == 0 ? i + 1 : i;
-        const int b1 = g1 & 1;
         ok = (c1 != 0 || al_wait(&bar_q, i1 & 1, ERR_AT_QK, &s_fail)) &&
-             al_wait(&bar_k[b1], (g1 >> 1) & 1, ERR_AT_QK, &s_fail) &&
-             (g1 < 2 || al_wait(&bar_pv[b1], ((g1 - 2) >> 1) & 1, ERR_AT_O, &s_fail));
+             al_wait(&bar_k[g1 & 1], (g1 >> 1) & 1, ERR_AT_QK, &s_fail) &&
+             (u1 == 0 || al_wait(&bar_pv[b1], (u1 - 1) & 1, ERR_AT_O, &s_fail));
         if (!ok) break;
         at_fence_after();
-        qk(b1);
+        qk(b1, g1 & 1);
         at_commit(&bar_s[b1]);
-        at_commit(&bar_kfree[b1]);
+        at_commit(&bar_kfree[g1 & 1]);
         if (c1 == NC - 1) at_commit(&bar_qfree);
       }
-      const int b = g & 1;
-      ok = al_wait(&bar_p[b], (g >> 1) & 1, ERR_AT_P, &s_fail) &&
-           al_wait(&bar_v[b], (g >> 1) & 1, ERR_AT_V, &s_fail) &&
-           (c != 0 || i < 2 ||
-            al_wait(&bar_ofree[i & 1], ((i >> 1) - 1) & 1, ERR_AT_OFREE, &s_fail));
+      // O' of item i starts once the epilogue has read item i - 1's
+      ok = al_wait(&bar_p[b], u & 1, ERR_AT_P, &s_fail) &&
+           al_wait(&bar_v[g & 1], (g >> 1) & 1, ERR_AT_V, &s_fail) &&
+           (c != 0 || i < 1 || al_wait(&bar_ofree, (i - 1) & 1, ERR_AT_OFREE, &s_fail));
       if (!ok) break;
       at_fence_after();
-      pv(b, tO0 + AT_O_W * uint32_t(i & 1), c == 0);
+      pv(b, g & 1, c == 0);
       at_commit(&bar_pv[b]);
-      at_commit(&bar_vfree[b]);
-      if (c == NC - 1) at_commit(&bar_o[i & 1]);
+      at_commit(&bar_vfree[g & 1]);
+      if (c == NC - 1) at_commit(&bar_o);
       if (++c == NC) {
         c = 0;
         ++i;
       }
+      b = b1;
+      u = u1;
     }
   } else if (warp >= 2) {
     // ---- softmax and epilogue
@@ -761,22 +771,25 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     constexpr float RESCALE_AT = 16.f;      // log2 headroom before a chunk re-bases a row
     const int jb = 32 * hf;                 // this warp's 32 keys of every chunk
     int cur_h = -1;
-    int g = 0;
-    ItemPos it(blockIdx.x, gridDim.x, QT, batch);
+    int g = 0, sb = 0, su = 0;  // chunk, its S / P buffer and the buffer's use count
+    int psb = 0, psu = 0;       // the same of chunk g - 1
+    ItemPos it(first, 1, QT, batch);
     for (int i = 0; i < my_items; ++i, it.next()) {
       const int qt = it.qt, h = it.h, blk = it.blk;
       const int q = qt * AT_QT + r;
-      const uint32_t tO = tO0 + AT_O_W * uint32_t(i & 1);
       if (h != cur_h) {  // bias table of this head (all softmax warps take the same items)
         soft_sync();
+        // a thread per key column (no division per entry), all query slots down it
         const float* drow = dist_bias + h * nd;
         const float same = same_bias[h];
-        for (int e = tid - 64; e < nq * nk; e += 32 * AT_SOFT_WARPS) {
-          const int qs = e / nk, key = e - qs * nk;
-          const int k = key / Kc - qs + B_max - 2;
-          s_btab[qs * AL_BSTRIDE + key] =
-              key < S ? (__ldg(drow + k) + (k == B_max - 2 ? same : 0.f)) * AT_LOG2E
-                      : -INFINITY;
+        for (int key = tid - 64; key < nk; key += 32 * AT_SOFT_WARPS) {
+          const int ks = key / Kc;
+          for (int qs = 0; qs < nq; ++qs) {
+            const int k = ks - qs + B_max - 2;
+            s_btab[qs * AL_BSTRIDE + key] =
+                key < S ? (__ldg(drow + k) + (k == B_max - 2 ? same : 0.f)) * AT_LOG2E
+                        : -INFINITY;
+          }
         }
         soft_sync();
         cur_h = h;
@@ -785,11 +798,10 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       bool ok = true;
       float m = -INFINITY, l = 0.f;
       for (int c = 0; c < NC; ++c, ++g) {
-        const int b = g & 1;
-        ok = al_wait(&bar_s[b], (g >> 1) & 1, ERR_AT_S, &s_fail) && ok;
+        ok = al_wait(&bar_s[sb], su & 1, ERR_AT_S, &s_fail) && ok;
         at_fence_after();
         float v[32];
-        at_ld32(tS + lane_off + uint32_t(128 * b + jb), v);
+        at_ld32(tS + lane_off + uint32_t(128 * sb + jb), v);
         // x = v / 8 * log2(e) + bias (log2 units), two at a time
         const float* bk = brow + c * AL_KC + jb;
         float mx = -INFINITY;
@@ -821,7 +833,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
           if (__any_sync(FULL_MASK, rebase)) {
             const float sc = rebase ? at_ex2(m - mh) : 1.f;
             l *= sc;
-            ok = al_wait(&bar_pv[(g - 1) & 1], ((g - 1) >> 1) & 1, ERR_AT_O, &s_fail) && ok;
+            ok = al_wait(&bar_pv[psb], psu & 1, ERR_AT_O, &s_fail) && ok;
             at_fence_after();
 #pragma unroll
             for (int part = 0; part < 2; ++part) {
@@ -845,11 +857,17 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
           at_split2(p0, p1, ph[u], pl[u]);
         }
         l += l2.x + l2.y;
-        at_st16(tS + lane_off + uint32_t(128 * b + jb), ph);
-        at_st16(tS + lane_off + uint32_t(128 * b + jb + 16), pl);
+        at_st16(tS + lane_off + uint32_t(128 * sb + jb), ph);
+        at_st16(tS + lane_off + uint32_t(128 * sb + jb + 16), pl);
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         at_fence_before();
-        mbar_arrive(&bar_p[b]);
+        mbar_arrive(&bar_p[sb]);
+        psb = sb;
+        psu = su;
+        if (++sb == AL_SBUF) {
+          sb = 0;
+          ++su;
+        }
       }
       s_psum[hf][r] = l;
       quarter_sync(qq);
@@ -859,13 +877,13 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       const float inv = 1.0f / lsum;
       // epilogue: O / l for this warp's 16 of the 64 output columns, split, stored from
       // registers (hi at column h * 64, lo at H + h * 64 of the [tokens, 2H] output)
-      ok = al_wait(&bar_o[i & 1], (i >> 1) & 1, ERR_AT_O, &s_fail) && ok;
+      ok = al_wait(&bar_o, i & 1, ERR_AT_O, &s_fail) && ok;
       at_fence_after();
       float v[AT_OW], vl[AT_OW];
       at_ld16(tO + lane_off + AT_OW * hf, v);
       at_ld16(tO + lane_off + 64 + AT_OW * hf, vl);
       at_fence_before();
-      mbar_arrive(&bar_ofree[i & 1]);
+      mbar_arrive(&bar_ofree);
       if (ok && q < S) {
         uint32_t hi[AT_OW / 2], lo[AT_OW / 2];
 #pragma unroll

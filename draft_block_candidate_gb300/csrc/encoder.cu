@@ -102,73 +102,8 @@ __device__ __forceinline__ void load8(const float* p, float (&v)[8]) {
 // lp = l - lse, p = exp(lp), gap = lp - lp of the slot's top candidate, r = k/(K-1),
 // top = [k == 0] (App. A: log-probability and probability under the full vocabulary,
 // the gap to the slot's most likely token, the rank normalised to [0,1], top indicator).
-// One warp per row at a time, each lane 8 consecutive hidden units per chunk: 16-byte hi
-// and lo stores.  A lane's first chunk of W1 / b1 stays in registers for all its rows.
-__device__ __forceinline__ void conf_chunk(const float (&f)[5], const float (&w)[8][6],
-                                           __nv_bfloat16* hi, __nv_bfloat16* lo) {
-  float u[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    float acc = w[j][5];
-#pragma unroll
-    for (int i = 0; i < 5; ++i) acc = fmaf(w[j][i], f[i], acc);
-    u[j] = silu(acc);
-  }
-  store_split8(u, hi, lo);
-}
-
-__device__ __forceinline__ void conf_load_w(const float* __restrict__ w1,
-                                            const float* __restrict__ b1, int h0,
-                                            float (&w)[8][6]) {
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-#pragma unroll
-    for (int i = 0; i < 5; ++i) w[j][i] = __ldg(w1 + (h0 + j) * 5 + i);
-    w[j][5] = __ldg(b1 + h0 + j);
-  }
-}
-
-__global__ void conf_hidden_kernel(const float* __restrict__ cand_logit,
-                                   const float* __restrict__ lse, int64_t M, int K, int H,
-                                   const float* __restrict__ w1, const float* __restrict__ b1,
-                                   __nv_bfloat16* __restrict__ U) {
-  // One warp per slot (its K candidate rows share the slot's lse and top logit): lane k
-  // forms row k's five features, which are then broadcast row by row.
-  const int lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-  const int nch = H / 8;
-  float w[8][6];
-  if (lane < nch) conf_load_w(w1, b1, lane * 8, w);
-  const int64_t nslots = M / K;
-  for (int64_t j = int64_t(blockIdx.x) * nw + (threadIdx.x >> 5); j < nslots;
-       j += int64_t(gridDim.x) * nw) {
-    const float* cl = cand_logit + j * K;
-    const float l2 = __ldg(lse + j);
-    const float top = __ldg(cl);
-    float g[5] = {0.f, 0.f, 0.f, 0.f, 0.f};
-    if (lane < K) {
-      const float lp = __ldg(cl + lane) - l2;
-      g[0] = lp;
-      g[1] = expf(lp);
-      g[2] = lp - (top - l2);
-      g[3] = K > 1 ? float(lane) / float(K - 1) : 0.f;
-      g[4] = lane == 0 ? 1.f : 0.f;
-    }
-    __nv_bfloat16* u = U + j * K * 2 * H;
-    for (int k = 0; k < K; ++k, u += 2 * H) {
-      float f[5];
-#pragma unroll
-      for (int i = 0; i < 5; ++i) f[i] = __shfl_sync(FULL_MASK, g[i], k);
-      if (lane < nch) conf_chunk(f, w, u + lane * 8, u + H + lane * 8);
-      for (int c = lane + 32; c < nch; c += 32) {  // hidden sizes above 256
-        float w2[8][6];
-        conf_load_w(w1, b1, c * 8, w2);
-        conf_chunk(f, w2, u + c * 8, u + H + c * 8);
-      }
-    }
-  }
-}
-
-// Hidden width 256: the layer's weights (256 x 5 + 256 biases) sit in shared memory,
+// This pass serves hidden width 256; other widths form U inside the node GEMM.
+// The layer's weights (256 x 5 + 256 biases) sit in shared memory,
 // re-read per row (a lane's 48 values as 12 16-byte loads, interleaved across lanes so a
 // load is conflict-free) instead of held in 48 registers, so more warps fit on an SM;
 // one warp per (slot, 8 candidate rows).
@@ -541,43 +476,6 @@ cudaError_t launch_attention(const __nv_bfloat16* qkv, int64_t batch, int S, int
   return cudaGetLastError();
 }
 
-// ------------------------------------------------------------------ fusion input
-// out split [M, 6H] = [h, t, h*t]_hi | [h, t, h*t]_lo (App. A: "concatenating the
-// candidate state, the target state, and their elementwise product").
-// Fusion input without the target-state block: out split [M, 4H] = [h, h*t]_hi |
-// [h, h*t]_lo.  One thread per (row m, 8 consecutive columns), 16-byte stores.
-__global__ void fuse_concat_kernel(const float* __restrict__ X,
-                                   const __nv_bfloat16* __restrict__ target, int S, int64_t M,
-                                   int H, __nv_bfloat16* __restrict__ out) {
-  // grid (chunks of one block's S x H/8 work items, blocks): no 64-bit division
-  const int hv = H / 8;
-  const int t = blockIdx.x * blockDim.x + threadIdx.x;
-  if (t >= S * hv) return;
-  const int64_t nblk = M / S;
-  const int r = t / hv;
-  const int h0 = (t % hv) * 8;
-  for (int64_t blk = blockIdx.y; blk < nblk; blk += gridDim.y) {
-    const int64_t m = blk * S + r;
-    float x[8], xt[8];
-    load8(X + m * H + h0, x);
-    if (target) {
-      const uint4 w = __ldg(reinterpret_cast<const uint4*>(target + blk * H + h0));
-      const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        xt[2 * j] = x[2 * j] * __uint_as_float(ww[j] << 16);
-        xt[2 * j + 1] = x[2 * j + 1] * __uint_as_float(ww[j] & 0xffff0000u);
-      }
-    } else {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) xt[j] = 0.f;
-    }
-    __nv_bfloat16* o = out + m * 4 * H;
-    store_split8(x, o + h0, o + 2 * H + h0);
-    store_split8(xt, o + H + h0, o + 3 * H + h0);
-  }
-}
-
 // out[r, :] = bias for every row (the per-block target terms when there is no target state)
 __global__ void rows_bias_kernel(const float* __restrict__ bias, int64_t rows, int N,
                                  float* __restrict__ out) {
@@ -592,18 +490,13 @@ __global__ void rows_bias_kernel(const float* __restrict__ bias, int64_t rows, i
 cudaError_t launch_conf_hidden(const float* cand_logit, const float* lse, int64_t M, int K, int H,
                                const float* w1, const float* b1, __nv_bfloat16* U,
                                cudaStream_t stream) {
-  if (H % 8) return cudaErrorInvalidValue;
+  // the standalone layer is kept for hidden width 256 only (other widths make it inside
+  // the node GEMM)
+  if (H != 256) return cudaErrorInvalidValue;
   if (K < 1 || K > 32 || M % K) return cudaErrorInvalidValue;
-  const int64_t slots_per_cta = 8;  // one warp per slot
-  const unsigned grid = static_cast<unsigned>(
-      std::min<int64_t>((M / K + slots_per_cta - 1) / slots_per_cta, 152 * 8));
-  if (H == 256) {
-    const int64_t units = (M / K) * ((K + 7) / 8);  // (slot, 8 rows) per warp, 8 per CTA
-    const unsigned g2 = static_cast<unsigned>(std::min<int64_t>((units + 7) / 8, 152 * 16));
-    conf_hidden256_kernel<<<g2, 256, 0, stream>>>(cand_logit, lse, M, K, w1, b1, U);
-  } else {
-    conf_hidden_kernel<<<grid, 256, 0, stream>>>(cand_logit, lse, M, K, H, w1, b1, U);
-  }
+  const int64_t units = (M / K) * ((K + 7) / 8);  // (slot, 8 rows) per warp, 8 per CTA
+  const unsigned g2 = static_cast<unsigned>(std::min<int64_t>((units + 7) / 8, 152 * 16));
+  conf_hidden256_kernel<<<g2, 256, 0, stream>>>(cand_logit, lse, M, K, w1, b1, U);
   note_launch();
   return cudaGetLastError();
 }
@@ -634,16 +527,6 @@ cudaError_t launch_rows_bias(const float* bias, int64_t rows, int N, float* out,
   return cudaGetLastError();
 }
 
-cudaError_t launch_fuse_concat(const float* X, const __nv_bfloat16* target, int S, int64_t M,
-                               int H, __nv_bfloat16* out, cudaStream_t stream) {
-  if (H % 8) return cudaErrorInvalidValue;
-  if (S <= 0 || M % S) return cudaErrorInvalidValue;
-  const dim3 grid(static_cast<unsigned>((int64_t(S) * (H / 8) + 255) / 256),
-                  static_cast<unsigned>(std::min<int64_t>(M / S, 65535)));
-  fuse_concat_kernel<<<grid, 256, 0, stream>>>(X, target, S, M, H, out);
-  note_launch();
-  return cudaGetLastError();
-}
 
 
 }  // namespace lilicorr

@@ -333,14 +333,167 @@ __device__ __forceinline__ void tc_epilogue_staged(const GemmArgs& g, const CUte
   }
 }
 
+// ------------------------------------------------------------------ A made in the kernel
+//
+// Two contractions read an A operand that is cheap to form from data already on hand, so
+// forming it beside the MMAs saves its round trip through HBM (and the launch that wrote
+// it).  TC_A_WARPS warps (256 threads) fill the A_hi / A_lo halves of each ring stage in
+// the 128-byte-swizzled K-major layout the TMA would have written (16-byte unit u of
+// row r at r * 128 + ((u ^ (r & 7)) << 4)), each thread one unit of rows r, r + 32,
+// r + 64, r + 96; every thread arrives on the stage's full barrier after a proxy fence,
+// and waits for the stage's empty barrier before rewriting it.  Rows past M are zero.
+constexpr int TC_A_WARPS = 8;
+
+__device__ __forceinline__ void a_store_unit(uint8_t* ahi, uint8_t* alo, int r, int unit,
+                                             const float (&v)[8]) {
+  uint32_t hi[4], lo[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    __nv_bfloat16 ha, la, hb, lb;
+    split_bf16(v[2 * j], ha, la);
+    split_bf16(v[2 * j + 1], hb, lb);
+    hi[j] = pack2(ha, hb);
+    lo[j] = pack2(la, lb);
+  }
+  const int off = r * 128 + ((unit ^ (r & 7)) << 4);
+  *reinterpret_cast<uint4*>(ahi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+  *reinterpret_cast<uint4*>(alo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+}
+
+template <int ASRC, int STAGES>
+__device__ __forceinline__ void a_producer(const GemmArgs& g, uint8_t* sA, int AST,
+                                           uint64_t* full_bar, uint64_t* empty_bar, int KB,
+                                           int NT, int ntiles, int unit, int rsub,
+                                           const float* wt) {
+  int it = 0;
+  for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
+    const int64_t m0 = int64_t(t / NT) * TC_BM;
+    if constexpr (ASRC == ASRC_FUSION) {
+      // [h, h * t]: ring step kb = 2 cb + part holds column block cb of h (part 0) or of
+      // h * t (part 1), so a block of X is loaded once for both; the loads are issued
+      // before the wait for the stage, so their latency overlaps it
+      const int H = g.Kw / 2;
+      const float* xr[4];
+      const __nv_bfloat16* tr[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int64_t m = m0 + rsub + 32 * i;
+        const bool live = m < g.M;
+        xr[i] = live ? g.a_x + m * H + unit * 8 : nullptr;
+        tr[i] = live && g.a_t ? g.a_t + (m / g.a_group) * H + unit * 8 : nullptr;
+      }
+      float x[4][8];
+      uint4 tw[4];
+      for (int kb = 0; kb < KB; ++kb, ++it) {
+        const int cb = kb >> 1, part = kb & 1;
+        const int s = it % STAGES, use = it / STAGES;
+        if (part == 0) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+            if (xr[i]) {
+              a = __ldg(reinterpret_cast<const float4*>(xr[i] + cb * TC_BK));
+              b = __ldg(reinterpret_cast<const float4*>(xr[i] + cb * TC_BK + 4));
+            }
+            x[i][0] = a.x; x[i][1] = a.y; x[i][2] = a.z; x[i][3] = a.w;
+            x[i][4] = b.x; x[i][5] = b.y; x[i][6] = b.z; x[i][7] = b.w;
+            tw[i] = tr[i] ? __ldg(reinterpret_cast<const uint4*>(tr[i] + cb * TC_BK))
+                          : make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+        if (use > 0 &&
+            !mbar_wait_bounded(&empty_bar[s], (use - 1) & 1, &g_err_tc, ERR_TC_EMPTY))
+          return;
+        uint8_t* ahi = sA + s * AST;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          float v[8];
+          if (part == 0) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] = x[i][j];
+          } else {
+            const uint32_t ww[4] = {tw[i].x, tw[i].y, tw[i].z, tw[i].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              v[2 * j] = x[i][2 * j] * __uint_as_float(ww[j] << 16);
+              v[2 * j + 1] = x[i][2 * j + 1] * __uint_as_float(ww[j] & 0xffff0000u);
+            }
+          }
+          a_store_unit(ahi, ahi + TC_A_BYTES, rsub + 32 * i, unit, v);
+        }
+        fence_async_smem();
+        mbar_arrive(&full_bar[s]);
+      }
+    } else {
+      // U = SiLU(W1 f + b1): the five features of each of this thread's rows once per tile
+      // (log-prob, prob, gap to the slot's top candidate, normalised rank, top indicator),
+      // then per ring step the 8 hidden units of this thread's unit
+      float f[4][5];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int64_t m = m0 + rsub + 32 * i;
+#pragma unroll
+        for (int c = 0; c < 5; ++c) f[i][c] = 0.f;
+        if (m < g.M) {
+          const int64_t j = m / g.K;
+          const int k = static_cast<int>(m - j * g.K);
+          const float l2 = __ldg(g.a_lse + j);
+          const float lp = __ldg(g.a_cl + m) - l2;
+          f[i][0] = lp;
+          f[i][1] = expf(lp);
+          f[i][2] = lp - (__ldg(g.a_cl + j * g.K) - l2);
+          f[i][3] = g.K > 1 ? float(k) / float(g.K - 1) : 0.f;
+          f[i][4] = k == 0 ? 1.f : 0.f;
+        }
+      }
+      for (int kb = 0; kb < KB; ++kb, ++it) {
+        const int s = it % STAGES, use = it / STAGES;
+        // this unit's 8 hidden units: 48 consecutive floats of the weight table
+        float w[48];
+        const float4* w4 = reinterpret_cast<const float4*>(wt + (kb * TC_BK + unit * 8) * 6);
+#pragma unroll
+        for (int c = 0; c < 12; ++c) {
+          const float4 q = w4[c];
+          w[4 * c] = q.x;
+          w[4 * c + 1] = q.y;
+          w[4 * c + 2] = q.z;
+          w[4 * c + 3] = q.w;
+        }
+        if (use > 0 &&
+            !mbar_wait_bounded(&empty_bar[s], (use - 1) & 1, &g_err_tc, ERR_TC_EMPTY))
+          return;
+        uint8_t* ahi = sA + s * AST;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          float v[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            float acc = w[6 * q + 5];
+#pragma unroll
+            for (int c = 0; c < 5; ++c) acc = fmaf(w[6 * q + c], f[i][c], acc);
+            v[q] = silu(acc);
+          }
+          a_store_unit(ahi, ahi + TC_A_BYTES, rsub + 32 * i, unit, v);
+        }
+        fence_async_smem();
+        mbar_arrive(&full_bar[s]);
+      }
+    }
+  }
+}
+
 // ------------------------------------------------------------------ kernel
 
 // EW epilogue warps: 8 (two per TMEM quarter, each half the columns) or 16 (four per
 // quarter, each a quarter of the columns: more warps to hide the epilogue's latencies).
-template <int EPI, int TC_STAGES, int TC_STG_BUFS, bool PAIR, int EW = TC_EPI_WARPS>
-__global__ void __launch_bounds__(32 * (2 + EW), 1)
+// ASRC != ASRC_TMA: the A operand is made by TC_A_WARPS more warps (a_producer_stage)
+// straight into the stages' A halves; the TMA warp then loads only W.
+template <int EPI, int TC_STAGES, int TC_STG_BUFS, bool PAIR, int EW = TC_EPI_WARPS,
+          int ASRC = ASRC_TMA>
+__global__ void __launch_bounds__(32 * (2 + EW + (ASRC != ASRC_TMA ? TC_A_WARPS : 0)), 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const GemmArgs g) {
+  static_assert(ASRC == ASRC_TMA || PAIR, "a made A operand is always split");
   extern __shared__ uint8_t tc_smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~uintptr_t(1023));
@@ -361,7 +514,8 @@ __global__ void __launch_bounds__(32 * (2 + EW), 1)
 
   if (tid == 0) {
     for (int s = 0; s < TC_STAGES; ++s) {
-      mbar_init(&full_bar[s], 1);
+      // the TMA warp's expect-tx arrival, plus one arrival per A-producer thread
+      mbar_init(&full_bar[s], 1 + (ASRC != ASRC_TMA ? 32 * TC_A_WARPS : 0));
       mbar_init(&empty_bar[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -369,6 +523,14 @@ __global__ void __launch_bounds__(32 * (2 + EW), 1)
       mbar_init(&acc_empty[b], EW);
     }
     fence_mbar_init();
+  }
+  if constexpr (ASRC == ASRC_CONF) {
+    // the confidence layer's weights [Kw][5] and biases [Kw], as 6 floats per hidden unit
+    float* wt = reinterpret_cast<float*>(sStage + EW * TC_STG_BUFS * TC_STG_BYTES);
+    for (int i = tid; i < g.Kw * 6; i += blockDim.x) {
+      const int h = i / 6, c = i - 6 * h;
+      wt[i] = c < 5 ? g.a_w1[h * 5 + c] : g.a_b1[h];
+    }
   }
   if (warp == 0) tmem_alloc(&s_tmem, TC_TMEM_COLS);
   tc_fence_before();
@@ -387,6 +549,14 @@ __global__ void __launch_bounds__(32 * (2 + EW), 1)
         if (use > 0 && !mbar_wait_bounded(&empty_bar[s], (use - 1) & 1, &g_err_tc, ERR_TC_EMPTY)) {
           ok = false;
           break;
+        }
+        if constexpr (ASRC != ASRC_TMA) {
+          // W block of ring step kb: for the fusion input the steps alternate between the
+          // h and the h * t halves of one 64-column block
+          const int wk = ASRC == ASRC_FUSION ? (kb & 1) * (g.Kw / 2) + (kb >> 1) * TC_BK : kb * TC_BK;
+          mbar_arrive_expect_tx(&full_bar[s], TC_B_BYTES);
+          tma_load_2d(sB + s * TC_B_BYTES, &tmB, wk, n0, &full_bar[s]);
+          continue;
         }
         mbar_arrive_expect_tx(&full_bar[s], AST + TC_B_BYTES);
         if constexpr (PAIR) {
@@ -434,7 +604,7 @@ __global__ void __launch_bounds__(32 * (2 + EW), 1)
       }
       umma_commit(&acc_full[buf]);
     }
-  } else if (warp >= 2) {
+  } else if (warp >= 2 && warp < 2 + EW) {
     // ---- epilogue: quarter q = warp % 4 owns TMEM lanes 32q..32q+31 (output rows);
     // the two warps of a quarter split the tile's columns in halves
     constexpr int CPP = (TC_BN / 32) / (EW / 4);  // 32-column chunks per epilogue warp
@@ -498,6 +668,12 @@ __global__ void __launch_bounds__(32 * (2 + EW), 1)
     }
     if (lane == 0) bulk_wait_all();
     __syncwarp();
+  } else if (ASRC != ASRC_TMA && warp >= 2 + EW) {
+    // ---- A producers: each thread makes the same 16-byte unit of 4 rows of every stage
+    const int at = tid - 32 * (2 + EW);
+    const int unit = at & 7, rsub = at >> 3;  // rows rsub + 32 i
+    a_producer<ASRC, TC_STAGES>(g, sA, AST, full_bar, empty_bar, KB, NT, ntiles, unit, rsub,
+                     reinterpret_cast<const float*>(sStage + EW * TC_STG_BUFS * TC_STG_BYTES));
   }
   tc_fence_before();
   __syncthreads();
@@ -560,8 +736,53 @@ bool gemm_tc_supported(const GemmArgs& g) {
 }
 
 cudaError_t launch_gemm(int epi, const GemmArgs& g, cudaStream_t stream) {
-  if (!gemm_tc_supported(g)) return cudaErrorInvalidValue;
   CUtensorMap ta, tb, tc;
+  if (g.asrc != ASRC_TMA) {
+    // A made in the kernel: the fusion input under the SiLU-split epilogue, or the
+    // confidence layer under the node epilogue; both split (Ka = 2 Kw)
+    const bool fusion = g.asrc == ASRC_FUSION && epi == EPI_SPLIT_SILU && g.a_x &&
+                        g.a_group > 0 && g.Kw % (2 * TC_BK) == 0 &&
+                        reinterpret_cast<uintptr_t>(g.a_x) % 16 == 0 &&
+                        reinterpret_cast<uintptr_t>(g.a_t) % 16 == 0;
+    const bool conf = g.asrc == ASRC_CONF && epi == EPI_NODE && g.a_cl && g.a_lse && g.a_w1 &&
+                      g.a_b1 && g.K >= 1;
+    if (!(fusion || conf) || g.Ka != 2 * g.Kw || g.Kw % TC_BK || g.N % 32 || g.M <= 0 ||
+        reinterpret_cast<uintptr_t>(g.W) % 16)
+      return cudaErrorInvalidValue;
+    // (the A tensor map is not read; it is encoded over W only to fill the argument)
+    if (!make_tmap(&ta, g.W, uint64_t(g.N), uint64_t(g.Kw), TC_BM) ||
+        !make_tmap(&tb, g.W, uint64_t(g.N), uint64_t(g.Kw), TC_BN))
+      return cudaErrorInvalidValue;
+    if (fusion) {
+      if (!g.out_split || reinterpret_cast<uintptr_t>(g.out_split) % 16 ||
+          !make_tmap_out(&tc, g.out_split, uint64_t(g.M), uint64_t(2 * g.N), false))
+        return cudaErrorInvalidValue;
+    } else if (!g.out || reinterpret_cast<uintptr_t>(g.out) % 16 ||
+               !make_tmap_out(&tc, g.out, uint64_t(g.M), uint64_t(g.N), true)) {
+      return cudaErrorInvalidValue;
+    }
+    const int sms = device_sm_count();
+    const int64_t ntiles = int64_t((g.N + TC_BN - 1) / TC_BN) * ((g.M + TC_BM - 1) / TC_BM);
+    const dim3 grid(static_cast<unsigned>(ntiles < sms ? ntiles : sms));
+    constexpr int threads = 32 * (2 + TC_EPI_WARPS + TC_A_WARPS);
+    cudaError_t e;
+    if (fusion) {
+      constexpr int sm = tc_smem(3, 1, true);
+      auto k = gemm_tc_kernel<EPI_SPLIT_SILU, 3, 1, true, TC_EPI_WARPS, ASRC_FUSION>;
+      e = allow_dynamic_smem(reinterpret_cast<const void*>(k), sm);
+      if (e == cudaSuccess) k<<<grid, threads, sm, stream>>>(ta, tb, tc, g);
+    } else {
+      const int sm = tc_smem(2, 2, true) + g.Kw * 6 * 4;  // + the layer's weight table
+      if (sm > 227 * 1024) return cudaErrorInvalidValue;
+      auto k = gemm_tc_kernel<EPI_NODE, 2, 2, true, TC_EPI_WARPS, ASRC_CONF>;
+      e = allow_dynamic_smem(reinterpret_cast<const void*>(k), sm);
+      if (e == cudaSuccess) k<<<grid, threads, sm, stream>>>(ta, tb, tc, g);
+    }
+    if (e != cudaSuccess) return e;
+    note_launch();
+    return cudaGetLastError();
+  }
+  if (!gemm_tc_supported(g)) return cudaErrorInvalidValue;
   if (!make_tmap(&ta, g.A, uint64_t(g.M), uint64_t(g.Ka), TC_BM) ||
       !make_tmap(&tb, g.W, uint64_t(g.N), uint64_t(g.Kw), TC_BN))
     return cudaErrorInvalidValue;

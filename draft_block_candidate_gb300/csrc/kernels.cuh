@@ -68,7 +68,19 @@ struct GemmArgs {
   int K, B;
   int64_t vocab;                    // rows of embed (gather index is clamped to it)
   float* nodes_tap;                 // [M, N] or null
+  // A operand made in the kernel instead of read (A is then unused), split bf16 hi / lo
+  // written straight into the shared-memory stages:
+  //   ASRC_FUSION: A = [h, h * t] with h = a_x [M, Kw/2] f32 and t = a_t [M / a_group,
+  //                Kw/2] bf16 (null: zero), the column blocks of h and h * t interleaved
+  //   ASRC_CONF:   A = SiLU(a_w1 f + a_b1) [M, Kw], f the five confidence features of row
+  //                m from a_cl [M] (candidate logits), a_lse [M / K] and its rank m % K
+  int asrc;
+  const float* a_x;
+  const __nv_bfloat16* a_t;
+  int64_t a_group;
+  const float *a_cl, *a_lse, *a_w1, *a_b1;
 };
+enum ASrc : int { ASRC_TMA = 0, ASRC_FUSION = 1, ASRC_CONF = 2 };
 
 // tcgen05 tensor-core GEMM (gemm_tc.cu)
 cudaError_t launch_gemm(int epi, const GemmArgs& g, cudaStream_t stream);
@@ -80,6 +92,7 @@ cudaError_t launch_lm_head_topk(const __nv_bfloat16* hidden, const __nv_bfloat16
                                 int32_t* cand_id, float* cand_logit, float* lse,
                                 cudaStream_t stream);
 cudaError_t tc_read_device_error(uint32_t* code);
+// confidence layer as its own pass, hidden width 256 only (encoder.cu)
 cudaError_t launch_conf_hidden(const float* cand_logit, const float* lse, int64_t M, int K, int H,
                                const float* w1, const float* b1, __nv_bfloat16* U,
                                cudaStream_t stream);
@@ -104,6 +117,4 @@ cudaError_t launch_attention_tc_long(const __nv_bfloat16* qkv, int64_t batch, in
 cudaError_t at_read_device_error(uint32_t* code);
 cudaError_t launch_rows_bias(const float* bias, int64_t rows, int N, float* out,
                              cudaStream_t stream);
-cudaError_t launch_fuse_concat(const float* X, const __nv_bfloat16* target, int S, int64_t M,
-                               int H, __nv_bfloat16* out, cudaStream_t stream);
 }  // namespace lilicorr

@@ -59,12 +59,12 @@ static lilicorr_status cuda_fail(cudaError_t e, const char* where) {
 
 // ---- per-kernel timing: events recorded on the caller's stream after each launch
 enum Slot : int {
-  T_LOGIT = 0, T_CONF, T_NODE, T_NORM, T_QKV, T_ATTN, T_OUT, T_FFN1, T_FFN2, T_FUSECAT,
-  T_FUSE, T_HEADS, T_SCORES, T_WALK, NSLOT
+  T_LOGIT = 0, T_CONF, T_NODE, T_NORM, T_QKV, T_ATTN, T_OUT, T_FFN1, T_FFN2, T_TARGET, T_FUSE,
+  T_HEADS, T_SCORES, T_WALK, NSLOT
 };
 static const char* kSlotNames[NSLOT] = {
     "logit_pass", "conf_hidden", "node_gemm", "rmsnorm", "qkv_gemm", "attention", "out_gemm",
-    "ffn1_gemm", "ffn2_gemm", "fuse_concat", "fuse_gemm", "heads_gemm", "pair_scores",
+    "ffn1_gemm", "ffn2_gemm", "target_terms", "fuse_gemm", "heads_gemm", "pair_scores",
     "greedy_walk"};
 
 struct CallRecord {
@@ -640,13 +640,27 @@ lilicorr_status lilicorr_rerank(const lilicorr_weights* w, const void* logits,
   LC_CUDA(k1_launch(logits, es, batch, B, V, K, cand_id, cand_logit, lse, ws + pl.k1, stream),
           "logit pass");
   MARK(T_LOGIT);
-  // a2: node build
-  LC_CUDA(launch_conf_hidden(cand_logit, lse, M, K, H, w->conf_w1, w->conf_b1, act1, stream),
-          "confidence features");
-  MARK(T_CONF);
+  // a2: node build.  The confidence layer's hidden units are made inside the node GEMM
+  // from each candidate's five features, except at hidden width 256, where the
+  // standalone layer (weights in shared memory) and a TMA-fed node GEMM measured faster
+  // (81 against 91 us per step at batch 256; the node GEMM is bound by its gather
+  // epilogue, which the producer warps slow down; at width 512 the in-kernel form saves
+  // 17 us)
+  const bool conf_apart = H == 256;
+  if (conf_apart) {
+    LC_CUDA(launch_conf_hidden(cand_logit, lse, M, K, H, w->conf_w1, w->conf_b1, act1, stream),
+            "confidence features");
+    MARK(T_CONF);
+  }
   {
     GemmArgs g{};
-    g.A = act1; g.W = w->conf_w2; g.M = M; g.N = H; g.Kw = H; g.Ka = 2 * H; g.bias = w->conf_b2;
+    if (conf_apart) {
+      g.A = act1;
+    } else {
+      g.asrc = ASRC_CONF; g.a_cl = cand_logit; g.a_lse = lse; g.a_w1 = w->conf_w1;
+      g.a_b1 = w->conf_b1;
+    }
+    g.W = w->conf_w2; g.M = M; g.N = H; g.Kw = H; g.Ka = 2 * H; g.bias = w->conf_b2;
     g.out = X; g.embed = w->embed; g.cand_id = cand_id; g.slot_table = w->slot_table;
     g.rank_table = w->rank_table; g.slot_hidden = static_cast<const __nv_bfloat16*>(slot_hidden);
     g.K = K; g.B = B; g.vocab = d.V; g.nodes_tap = tp.nodes;
@@ -704,12 +718,13 @@ lilicorr_status lilicorr_rerank(const lilicorr_weights* w, const void* logits,
   } else {
     LC_CUDA(launch_rows_bias(w->tgt_b, batch, HE, tgt, stream), "target terms");
   }
-  LC_CUDA(launch_fuse_concat(X, target, S, M, H, qkv, stream), "fusion input");
-  MARK(T_FUSECAT);
+  MARK(T_TARGET);
   {
-    // SiLU(Wh h + Wht (h*t) + [Wt t + bf]_block): A = [h, h*t] split, bias per block
+    // SiLU(Wh h + Wht (h*t) + [Wt t + bf]_block): A = [h, h*t] split, made inside the GEMM
+    // from the residual stream and the block's target state; bias per block
     GemmArgs g{};
-    g.A = qkv; g.W = w->fuse_w2; g.M = M; g.N = H; g.Kw = 2 * H; g.Ka = 4 * H; g.bias = tgt;
+    g.asrc = ASRC_FUSION; g.a_x = X; g.a_t = target; g.a_group = S;
+    g.W = w->fuse_w2; g.M = M; g.N = H; g.Kw = 2 * H; g.Ka = 4 * H; g.bias = tgt;
     g.bias_group = S; g.bias_stride = HE; g.out_split = act1;
     LC_CUDA(launch_gemm(EPI_SPLIT_SILU, g, stream), "fusion gemm");
     MARK(T_FUSE);

@@ -52,6 +52,10 @@ CASES = [  # (ldtype, batch, B, V, K)
     ("bf16", 1, 16, 151_936, 8),       # full vocabulary, few rows -> split rows
     ("bf16", 1, 4, 151_936, 32),
     ("f32", 40, 16, 3000, 16),         # many short rows
+    # many unsplit rows of varying alignment (each its own CTA)
+    ("bf16", 64, 16, 16397, 16),       # 960 unaligned rows of 3 stages
+    ("f32", 30, 16, 9001, 32),         # 450 unaligned f32 rows, K = 32
+    ("bf16", 200, 16, 700, 8),         # 3,000 one-stage rows: ~10 rows per CTA
 ]
 
 
