@@ -180,6 +180,12 @@ __device__ __forceinline__ void at_split2(float a, float b, uint32_t& hi, uint32
 __device__ __forceinline__ void quarter_sync(int q) {
   asm volatile("bar.sync %0, 128;" ::"r"(2 + q) : "memory");
 }
+__device__ __forceinline__ void at_st8(uint32_t taddr, const uint32_t (&v)[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+      : "memory");
+}
 __device__ __forceinline__ void at_st16f(uint32_t taddr, const float (&v)[16]) {
   uint32_t u[16];
 #pragma unroll
@@ -548,8 +554,9 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
 // Lattices of 257..512 tokens (the wide candidate pool: 15 slots x 32 candidates = 480
 // tokens).  The keys no longer fit the shared memory at once, so each (128-query tile,
 // block, head) item walks its keys in chunks of 128 with an online softmax:
-//   warp 0     TMA: the item's Q (hi, lo), then per chunk K (hi, lo) and V (hi, lo) into
-//              two-stage rings; owns the TMEM allocation (S / P: three 128-column buffers,
+//   warp 0     TMA: the item's Q (hi, lo) and per chunk K (hi, lo) into a two-stage ring;
+//              warp 18 the V chunks (hi, lo) into their own; warp 0 owns the TMEM
+//              allocation (S / P: three 128-column buffers,
 //              O': one 128-column buffer, which the epilogue empties before the next item's
 //              first product)
 //   warp 1     MMA: S(g+1) = Q K(g+1)^T (three split products) while the softmax warps
@@ -569,9 +576,11 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
 // at once, so that all warps still reach their named barriers and the final teardown.
 constexpr int AL_KC = 128;                     // keys per chunk
 constexpr int AL_SBUF = 3;                     // S / P buffers in TMEM (+ one O' buffer)
+constexpr int AL_VWARP = 2 + AT_SOFT_WARPS;    // the V producer, after the softmax warps
+constexpr int AL_THREADS = AT_THREADS + 32;
 constexpr int AL_KMAX = 512;
 constexpr int AL_BSTRIDE = AL_KMAX + 4;        // floats per bias-table row (bank offset)
-constexpr int AL_SMEM = 10 * AT_TILE + 1024;   // Q, K ring, V ring + the bias table
+constexpr int AL_SMEM = 11 * AT_TILE + 1024;   // Q, K ring, V ring, output staging + bias table
 
 __device__ __forceinline__ bool al_wait(uint64_t* bar, uint32_t parity, uint32_t site,
                                         volatile int* fail) {
@@ -592,8 +601,8 @@ __device__ __forceinline__ uint64_t al_desc_v(const void* p, uint32_t lo_off) {
   return (at_desc(p) & ~(0x3FFFull << 16)) | (uint64_t(lo_off >> 4) << 16);
 }
 
-__global__ void __launch_bounds__(AT_THREADS, 1)
-    attn_tc_long_kernel(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __restrict__ out,
+__global__ void __launch_bounds__(AL_THREADS, 1)
+    attn_tc_long_kernel(const __grid_constant__ CUtensorMap tm, const __grid_constant__ CUtensorMap tmo,
                         int S, int Kc, int H, int B_max, int heads, int64_t batch,
                         const float* __restrict__ dist_bias, const float* __restrict__ same_bias) {
   extern __shared__ uint8_t al_smem_raw[];
@@ -603,9 +612,10 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   uint8_t* sQl = sm + AT_TILE;
   uint8_t* sK = sm + 2 * AT_TILE;   // stage s: K hi at sK + 2 s AT_TILE, K lo one tile later
   uint8_t* sV = sm + 6 * AT_TILE;   // stage s: V hi at sV + 2 s AT_TILE, V lo one tile later
+  uint8_t* sO = sm + 10 * AT_TILE;  // output staging [128 rows][64] (hi, then lo)
   // [query slot][key]: (dist + same-slot bias) * log2(e) of the current head, -inf for
   // keys beyond the block
-  float* s_btab = reinterpret_cast<float*>(sm + 10 * AT_TILE);
+  float* s_btab = reinterpret_cast<float*>(sm + 11 * AT_TILE);
   __shared__ __align__(8) uint64_t bar_q, bar_qfree, bar_k[2], bar_kfree[2], bar_v[2],
       bar_vfree[2], bar_s[AL_SBUF], bar_p[AL_SBUF], bar_pv[AL_SBUF], bar_o, bar_ofree;
   __shared__ uint32_t s_tmem;
@@ -658,41 +668,44 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   const int my_items = first < nitems ? static_cast<int>(min(per, nitems - first)) : 0;
   const int total = my_items * NC;
 
-  if (warp == 0 && lane == 0) {
-    // ---- producer
+  if ((warp == 0 || warp == AL_VWARP) && lane == 0) {
+    // ---- producers: warp 0 loads Q and the K chunks, the last warp the V chunks, so
+    // that a K load never waits behind a V slot (freed only by a later product)
+    const bool kside = warp == 0;
     int g = 0;
     bool ok = true;
     ItemPos it(first, 1, QT, batch);
     for (int i = 0; i < my_items && ok; ++i, it.next()) {
       const int tok0 = it.blk * S;
       const int cq = it.h * AT_DH, ck = H + it.h * AT_DH, cv = 2 * H + it.h * AT_DH, lo = 3 * H;
-      if (i > 0 && !al_wait(&bar_qfree, (i - 1) & 1, ERR_AT_QKFREE, &s_fail)) break;
-      mbar_arrive_expect_tx(&bar_q, 2 * AT_TILE);
-      at_tma(sQh, &tm, cq, tok0 + it.qt * AT_QT, &bar_q);
-      at_tma(sQl, &tm, lo + cq, tok0 + it.qt * AT_QT, &bar_q);
+      if (kside) {
+        if (i > 0 && !al_wait(&bar_qfree, (i - 1) & 1, ERR_AT_QKFREE, &s_fail)) break;
+        mbar_arrive_expect_tx(&bar_q, 2 * AT_TILE);
+        at_tma(sQh, &tm, cq, tok0 + it.qt * AT_QT, &bar_q);
+        at_tma(sQl, &tm, lo + cq, tok0 + it.qt * AT_QT, &bar_q);
+      }
       for (int c = 0; c < NC; ++c, ++g) {
         const int st = g & 1, use = g >> 1;
         const int row = tok0 + c * AL_KC;
-        if (use > 0 && !al_wait(&bar_kfree[st], (use - 1) & 1, ERR_AT_QKFREE, &s_fail)) {
+        uint64_t* freed = kside ? &bar_kfree[st] : &bar_vfree[st];
+        if (use > 0 &&
+            !al_wait(freed, (use - 1) & 1, kside ? ERR_AT_QKFREE : ERR_AT_VFREE, &s_fail)) {
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(&bar_k[st], 2 * AT_TILE);
-        at_tma(sK + 2 * st * AT_TILE, &tm, ck, row, &bar_k[st]);
-        at_tma(sK + (2 * st + 1) * AT_TILE, &tm, lo + ck, row, &bar_k[st]);
-        if (use > 0 && !al_wait(&bar_vfree[st], (use - 1) & 1, ERR_AT_VFREE, &s_fail)) {
-          ok = false;
-          break;
-        }
-        mbar_arrive_expect_tx(&bar_v[st], 2 * AT_TILE);
-        at_tma(sV + 2 * st * AT_TILE, &tm, cv, row, &bar_v[st]);
-        at_tma(sV + (2 * st + 1) * AT_TILE, &tm, lo + cv, row, &bar_v[st]);
+        uint64_t* full = kside ? &bar_k[st] : &bar_v[st];
+        uint8_t* dst = (kside ? sK : sV) + 2 * st * AT_TILE;
+        const int col = kside ? ck : cv;
+        mbar_arrive_expect_tx(full, 2 * AT_TILE);
+        at_tma(dst, &tm, col, row, full);
+        at_tma(dst + AT_TILE, &tm, lo + col, row, full);
       }
     }
   } else if (warp == 1 && lane == 0) {
     // ---- MMA issuer: S(0); then per chunk g: S(g + 1), O' += P(g) V(g)
     constexpr uint32_t id_s = at_idesc(128, 128, false);
     constexpr uint32_t id_o = at_idesc(128, 128, true);
+    constexpr uint32_t id_o64 = at_idesc(128, 64, true);
     auto qk = [&](int b, int st) {  // S into buffer b from K stage st
       const uint32_t d = tS + uint32_t(128 * b);
       const uint8_t* kh = sK + 2 * st * AT_TILE;
@@ -712,8 +725,10 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       for (int j = 0; j < AL_KC / 16; ++j) {
         const uint32_t pc = uint32_t(128 * b + 32 * (j >> 1) + 8 * (j & 1));
         const uint64_t vhl = al_desc_v(vh + 16 * j * 128, AT_TILE);
+        // O'[:, 0:64] += P hi V hi + P lo V hi; O'[:, 64:128] += P hi V lo (P lo V lo,
+        // 2^-16 of the others, is left out)
         at_mma_ts(tO, tS + pc, vhl, id_o, !(first && j == 0));
-        at_mma_ts(tO, tS + pc + 16, vhl, id_o, 1);
+        at_mma_ts(tO, tS + pc + 16, vhl, id_o64, 1);
       }
     };
     bool ok = total > 0 && al_wait(&bar_q, 0, ERR_AT_QK, &s_fail) &&
@@ -760,7 +775,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       b = b1;
       u = u1;
     }
-  } else if (warp >= 2) {
+  } else if (warp >= 2 && warp < 2 + AT_SOFT_WARPS) {
     // ---- softmax and epilogue
     const int qq = warp & 3, hf = (warp - 2) >> 2;
     const int r = 32 * qq + lane;  // TMEM lane = query row of the tile
@@ -846,19 +861,25 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
           }
           if (rebase) m = mh;
         }
+        // p = 2^(x - m) as packed bf16 hi / lo over the logits, 16 keys at a time (hi
+        // words of keys 2u, 2u + 1 at column jb + u, lo words 16 columns further)
         float2 l2 = make_float2(0.f, 0.f);
-        uint32_t ph[16], pl[16];
         const float2 nm = make_float2(-m, -m);
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
-          const float2 y = __fadd2_rn(make_float2(v[2 * u], v[2 * u + 1]), nm);
-          const float p0 = at_ex2(y.x), p1 = at_ex2(y.y);
-          l2 = __fadd2_rn(l2, make_float2(p0, p1));
-          at_split2(p0, p1, ph[u], pl[u]);
+        for (int h2 = 0; h2 < 2; ++h2) {
+          uint32_t ph[8], pl[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int e = 16 * h2 + 2 * u;
+            const float2 y = __fadd2_rn(make_float2(v[e], v[e + 1]), nm);
+            const float p0 = at_ex2(y.x), p1 = at_ex2(y.y);
+            l2 = __fadd2_rn(l2, make_float2(p0, p1));
+            at_split2(p0, p1, ph[u], pl[u]);
+          }
+          at_st8(tS + lane_off + uint32_t(128 * sb + jb + 8 * h2), ph);
+          at_st8(tS + lane_off + uint32_t(128 * sb + jb + 16 + 8 * h2), pl);
         }
         l += l2.x + l2.y;
-        at_st16(tS + lane_off + uint32_t(128 * sb + jb), ph);
-        at_st16(tS + lane_off + uint32_t(128 * sb + jb + 16), pl);
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         at_fence_before();
         mbar_arrive(&bar_p[sb]);
@@ -870,6 +891,8 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         }
       }
       s_psum[hf][r] = l;
+      // the quarter's previous output store has finished reading its staging rows
+      if (hf == 0 && lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
       quarter_sync(qq);
       float lsum = 0.f;
 #pragma unroll
@@ -884,22 +907,39 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       at_ld16(tO + lane_off + 64 + AT_OW * hf, vl);
       at_fence_before();
       mbar_arrive(&bar_ofree);
-      if (ok && q < S) {
-        uint32_t hi[AT_OW / 2], lo[AT_OW / 2];
+      uint32_t hi[AT_OW / 2], lo[AT_OW / 2];
 #pragma unroll
-        for (int e = 0; e < AT_OW; e += 2)
-          at_split2((v[e] + vl[e]) * inv, (v[e + 1] + vl[e + 1]) * inv, hi[e / 2], lo[e / 2]);
-        __nv_bfloat16* orow = out + (int64_t(blk) * S + q) * (2 * H) + h * AT_DH + AT_OW * hf;
-        uint4* oh = reinterpret_cast<uint4*>(orow);
-        uint4* ol = reinterpret_cast<uint4*>(orow + H);
+      for (int e = 0; e < AT_OW; e += 2)
+        at_split2((v[e] + vl[e]) * inv, (v[e + 1] + vl[e + 1]) * inv, hi[e / 2], lo[e / 2]);
+      // stored through the staging tile by bulk tensor stores of the quarter's 32 rows
+      // (rows past the block are clipped): first the hi words, then, once that store has
+      // read the staging, the lo words.  This warp's 16 columns = 16-byte chunks 2 hf,
+      // 2 hf + 1 of the row's 128 bytes, at chunk ^ (row & 7) under the 128-byte swizzle.
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const uint32_t* wv = half ? lo : hi;
 #pragma unroll
         for (int u = 0; u < AT_OW / 8; ++u) {
-          oh[u] = make_uint4(hi[4 * u], hi[4 * u + 1], hi[4 * u + 2], hi[4 * u + 3]);
-          ol[u] = make_uint4(lo[4 * u], lo[4 * u + 1], lo[4 * u + 2], lo[4 * u + 3]);
+          const int off = r * 128 + 16 * ((AT_OW / 8 * hf + u) ^ (r & 7));
+          *reinterpret_cast<uint4*>(sO + off) =
+              make_uint4(wv[4 * u], wv[4 * u + 1], wv[4 * u + 2], wv[4 * u + 3]);
         }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        quarter_sync(qq);
+        if (hf == 0 && lane == 0) {
+          if (ok && qt * AT_QT + 32 * qq < S) {
+            at_store(&tmo, sO + 32 * qq * 128, (half ? H : 0) + h * AT_DH, qt * AT_QT + 32 * qq,
+                     blk);
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+          }
+          if (!half) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+        }
+        if (!half) quarter_sync(qq);
       }
     }
   }
+  if (warp >= 2 && warp < 2 + AT_SOFT_WARPS && ((warp - 2) >> 2) == 0 && lane == 0)
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
   at_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -996,13 +1036,23 @@ cudaError_t launch_attention_tc_long(const __nv_bfloat16* qkv, int64_t batch, in
          box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
+  // output [batch][S][2H] (hi | lo): 3-D so that a store box never runs into the next block
+  CUtensorMap tmo;
+  const cuuint64_t odims[3] = {cuuint64_t(2 * H), cuuint64_t(S), cuuint64_t(batch)};
+  const cuuint64_t ostrides[2] = {cuuint64_t(2 * H) * 2, cuuint64_t(S) * 2 * H * 2};
+  const cuuint32_t obox[3] = {64, 32, 1};
+  const cuuint32_t oestr[3] = {1, 1, 1};
+  if (fn(&tmo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, out, odims, ostrides, obox, oestr,
+         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+         CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
   const int smem = al_smem_bytes(S, K);
   cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void*>(attn_tc_long_kernel), smem);
   if (e != cudaSuccess) return e;
   const int sms = device_sm_count();
   const int64_t nitems = batch * heads * ((S + AT_QT - 1) / AT_QT);
   const dim3 grid(static_cast<unsigned>(nitems < sms ? nitems : sms));
-  attn_tc_long_kernel<<<grid, AT_THREADS, smem, stream>>>(tm, out, S, K, H, B_max, heads, batch,
+  attn_tc_long_kernel<<<grid, AL_THREADS, smem, stream>>>(tm, tmo, S, K, H, B_max, heads, batch,
                                                           dist_bias, same_bias);
   note_launch();
   return cudaGetLastError();
