@@ -278,6 +278,8 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   __syncthreads();
   at_fence_after();
   const uint32_t tmem = s_tmem;
+  pdl_wait();
+  pdl_trigger();
   // S / P of key half 0 in columns 0-127, of half 1 in 128-255; O' of even / odd items in
   // 256-319 / 320-383
   const uint32_t tS = tmem, tO0 = tmem + AT_O_COL;
@@ -658,6 +660,8 @@ __global__ void __launch_bounds__(AL_THREADS, 1)
   __syncthreads();
   at_fence_after();
   const uint32_t tmem = s_tmem;
+  pdl_wait();
+  pdl_trigger();
   // S / P of chunk g in columns 128 (g % 3) .. +127; O' in columns 384..511
   const uint32_t tS = tmem, tO = tmem + AL_SBUF * AL_KC;
   // this CTA's items: a contiguous range, so that the four query tiles of a (block, head)
@@ -705,7 +709,6 @@ __global__ void __launch_bounds__(AL_THREADS, 1)
     // ---- MMA issuer: S(0); then per chunk g: S(g + 1), O' += P(g) V(g)
     constexpr uint32_t id_s = at_idesc(128, 128, false);
     constexpr uint32_t id_o = at_idesc(128, 128, true);
-    constexpr uint32_t id_o64 = at_idesc(128, 64, true);
     auto qk = [&](int b, int st) {  // S into buffer b from K stage st
       const uint32_t d = tS + uint32_t(128 * b);
       const uint8_t* kh = sK + 2 * st * AT_TILE;
@@ -725,10 +728,8 @@ __global__ void __launch_bounds__(AL_THREADS, 1)
       for (int j = 0; j < AL_KC / 16; ++j) {
         const uint32_t pc = uint32_t(128 * b + 32 * (j >> 1) + 8 * (j & 1));
         const uint64_t vhl = al_desc_v(vh + 16 * j * 128, AT_TILE);
-        // O'[:, 0:64] += P hi V hi + P lo V hi; O'[:, 64:128] += P hi V lo (P lo V lo,
-        // 2^-16 of the others, is left out)
         at_mma_ts(tO, tS + pc, vhl, id_o, !(first && j == 0));
-        at_mma_ts(tO, tS + pc + 16, vhl, id_o64, 1);
+        at_mma_ts(tO, tS + pc + 16, vhl, id_o, 1);
       }
     };
     bool ok = total > 0 && al_wait(&bar_q, 0, ERR_AT_QK, &s_fail) &&
@@ -1005,8 +1006,9 @@ cudaError_t launch_attention_tc(const __nv_bfloat16* qkv, int64_t batch, int S, 
   const int sms = device_sm_count();
   const int64_t nitems = batch * heads * ((S + AT_QT - 1) / AT_QT);
   const dim3 grid(static_cast<unsigned>(nitems < sms ? nitems : sms));
-  attn_tc_kernel<<<grid, AT_THREADS, smem, stream>>>(tm, tmo, S, K, H, B_max, heads, batch,
-                                                        dist_bias, same_bias);
+  e = launch_k(attn_tc_kernel, grid, dim3(AT_THREADS), smem, stream, tm, tmo, S, K, H, B_max,
+               heads, batch, dist_bias, same_bias);
+  if (e != cudaSuccess) return e;
   note_launch();
   return cudaGetLastError();
 }
@@ -1052,8 +1054,9 @@ cudaError_t launch_attention_tc_long(const __nv_bfloat16* qkv, int64_t batch, in
   const int sms = device_sm_count();
   const int64_t nitems = batch * heads * ((S + AT_QT - 1) / AT_QT);
   const dim3 grid(static_cast<unsigned>(nitems < sms ? nitems : sms));
-  attn_tc_long_kernel<<<grid, AL_THREADS, smem, stream>>>(tm, tmo, S, K, H, B_max, heads, batch,
-                                                          dist_bias, same_bias);
+  e = launch_k(attn_tc_long_kernel, grid, dim3(AL_THREADS), smem, stream, tm, tmo, S, K, H, B_max,
+               heads, batch, dist_bias, same_bias);
+  if (e != cudaSuccess) return e;
   note_launch();
   return cudaGetLastError();
 }

@@ -122,6 +122,17 @@ __device__ __forceinline__ void split_bf16(float v, __nv_bfloat16& hi, __nv_bflo
   lo = __float2bfloat16_rn(v - __bfloat162float(hi));
 }
 
+// Programmatic dependent launch.  pdl_wait: every memory access of the kernel comes after
+// it; it returns once the kernel before this one on the stream has completed and its
+// writes are visible (at once when this launch was not programmatic).  pdl_trigger: the
+// next kernel on the stream may start launching (its CTAs then wait in their own
+// pdl_wait); issued right after the wait, so that the next kernel's launch and set-up
+// overlap this one.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // x * sigmoid(x); fast exponential and division (relative error ~1e-6, below the
 // ~16-bit precision the split operands carry).
 __device__ __forceinline__ float silu(float x) { return __fdividef(x, 1.0f + __expf(-x)); }

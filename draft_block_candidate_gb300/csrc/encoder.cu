@@ -130,6 +130,8 @@ __global__ void __launch_bounds__(256) conf_hidden256_kernel(const float* __rest
     reinterpret_cast<float*>(&sw[c][l])[e] = i < 5 ? w1[h * 5 + i] : b1[h];
   }
   __syncthreads();
+  pdl_wait();  // (the layer's weights above are never written by a kernel)
+  pdl_trigger();
   const int lane = threadIdx.x & 31, nw = blockDim.x >> 5;
   const int64_t nslots = M / K;
   const int gps = (K + RPW - 1) / RPW;  // row groups per slot
@@ -183,6 +185,8 @@ __global__ void __launch_bounds__(256) conf_hidden256_kernel(const float* __rest
 // y = x / sqrt(mean(x^2) + eps) * g, one warp per row, 8 columns per lane per pass.
 __global__ void rmsnorm_split_kernel(const float* __restrict__ X, const float* __restrict__ gain,
                                      int64_t M, int H, float eps, __nv_bfloat16* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int64_t m = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (m >= M) return;
@@ -217,6 +221,8 @@ __global__ void __launch_bounds__(256) rmsnorm_split256_kernel(const float* __re
                                                                int64_t M, float eps,
                                                                __nv_bfloat16* __restrict__ out) {
   constexpr int H = 256;
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int64_t m0 = (int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5)) * RPW;
   if (m0 >= M) return;
@@ -275,6 +281,8 @@ __global__ void __launch_bounds__(AT_THREADS) attention_kernel(
   const int nd = 2 * B_max - 3;
   for (int i = tid; i < nd; i += AT_THREADS) s_dist[i] = dist_bias[h * nd + i];
   const float same = same_bias[h];
+  pdl_wait();  // (the bias tables above are weights)
+  pdl_trigger();
   const float scale = 1.0f / sqrtf(float(DH));
 
   // Q tile
@@ -467,11 +475,12 @@ cudaError_t launch_attention(const __nv_bfloat16* qkv, int64_t batch, int S, int
   }
   if (e != cudaSuccess) return e;
   switch (dh) {
-    case 32: attention_kernel<32><<<grid, AT_THREADS, smem, stream>>>(qkv, S, K, H, B_max, dist_bias, same_bias, out); break;
-    case 64: attention_kernel<64><<<grid, AT_THREADS, smem, stream>>>(qkv, S, K, H, B_max, dist_bias, same_bias, out); break;
-    case 128: attention_kernel<128><<<grid, AT_THREADS, smem, stream>>>(qkv, S, K, H, B_max, dist_bias, same_bias, out); break;
+    case 32: e = launch_k(attention_kernel<32>, grid, dim3(AT_THREADS), smem, stream, qkv, S, K, H, B_max, dist_bias, same_bias, out); break;
+    case 64: e = launch_k(attention_kernel<64>, grid, dim3(AT_THREADS), smem, stream, qkv, S, K, H, B_max, dist_bias, same_bias, out); break;
+    case 128: e = launch_k(attention_kernel<128>, grid, dim3(AT_THREADS), smem, stream, qkv, S, K, H, B_max, dist_bias, same_bias, out); break;
     default: return cudaErrorInvalidValue;
   }
+  if (e != cudaSuccess) return e;
   note_launch();
   return cudaGetLastError();
 }
@@ -479,6 +488,8 @@ cudaError_t launch_attention(const __nv_bfloat16* qkv, int64_t batch, int S, int
 // out[r, :] = bias for every row (the per-block target terms when there is no target state)
 __global__ void rows_bias_kernel(const float* __restrict__ bias, int64_t rows, int N,
                                  float* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t n = rows * N;
   for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < n;
        i += int64_t(gridDim.x) * blockDim.x)
@@ -496,7 +507,9 @@ cudaError_t launch_conf_hidden(const float* cand_logit, const float* lse, int64_
   if (K < 1 || K > 32 || M % K) return cudaErrorInvalidValue;
   const int64_t units = (M / K) * ((K + 7) / 8);  // (slot, 8 rows) per warp, 8 per CTA
   const unsigned g2 = static_cast<unsigned>(std::min<int64_t>((units + 7) / 8, 152 * 16));
-  conf_hidden256_kernel<<<g2, 256, 0, stream>>>(cand_logit, lse, M, K, w1, b1, U);
+  const cudaError_t e = launch_k(conf_hidden256_kernel, dim3(g2), dim3(256), 0, stream, cand_logit,
+                                 lse, M, K, w1, b1, U);
+  if (e != cudaSuccess) return e;
   note_launch();
   return cudaGetLastError();
 }
@@ -505,15 +518,17 @@ cudaError_t launch_rmsnorm_split(const float* X, const float* gain, int64_t M, i
                                  __nv_bfloat16* out, cudaStream_t stream) {
   if (H % 8) return cudaErrorInvalidValue;
   const int wpb = 8;
+  cudaError_t e;
   if (H == 256) {
     constexpr int RPW = 4;
     const int64_t warps = (M + RPW - 1) / RPW;
-    rmsnorm_split256_kernel<RPW><<<static_cast<unsigned>((warps + wpb - 1) / wpb), wpb * 32, 0,
-                                   stream>>>(X, gain, M, eps, out);
+    e = launch_k(rmsnorm_split256_kernel<RPW>, dim3(static_cast<unsigned>((warps + wpb - 1) / wpb)),
+                 dim3(wpb * 32), 0, stream, X, gain, M, eps, out);
   } else {
-    rmsnorm_split_kernel<<<static_cast<unsigned>((M + wpb - 1) / wpb), wpb * 32, 0, stream>>>(
-        X, gain, M, H, eps, out);
+    e = launch_k(rmsnorm_split_kernel, dim3(static_cast<unsigned>((M + wpb - 1) / wpb)),
+                 dim3(wpb * 32), 0, stream, X, gain, M, H, eps, out);
   }
+  if (e != cudaSuccess) return e;
   note_launch();
   return cudaGetLastError();
 }
@@ -521,8 +536,10 @@ cudaError_t launch_rmsnorm_split(const float* X, const float* gain, int64_t M, i
 cudaError_t launch_rows_bias(const float* bias, int64_t rows, int N, float* out,
                              cudaStream_t stream) {
   const int64_t n = rows * N;
-  rows_bias_kernel<<<static_cast<unsigned>(std::min<int64_t>((n + 255) / 256, 152 * 8)), 256, 0,
-                     stream>>>(bias, rows, N, out);
+  const cudaError_t e =
+      launch_k(rows_bias_kernel, dim3(static_cast<unsigned>(std::min<int64_t>((n + 255) / 256, 152 * 8))),
+               dim3(256), 0, stream, bias, rows, N, out);
+  if (e != cudaSuccess) return e;
   note_launch();
   return cudaGetLastError();
 }

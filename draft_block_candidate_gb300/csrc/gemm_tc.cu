@@ -537,6 +537,8 @@ __global__ void __launch_bounds__(32 * (2 + EW + (ASRC != ASRC_TMA ? TC_A_WARPS 
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem;
+  pdl_wait();
+  pdl_trigger();
 
   if (warp == 0 && lane == 0) {
     // ---- producer: the smem ring runs on across this CTA's tiles
@@ -770,13 +772,13 @@ cudaError_t launch_gemm(int epi, const GemmArgs& g, cudaStream_t stream) {
       constexpr int sm = tc_smem(3, 1, true);
       auto k = gemm_tc_kernel<EPI_SPLIT_SILU, 3, 1, true, TC_EPI_WARPS, ASRC_FUSION>;
       e = allow_dynamic_smem(reinterpret_cast<const void*>(k), sm);
-      if (e == cudaSuccess) k<<<grid, threads, sm, stream>>>(ta, tb, tc, g);
+      if (e == cudaSuccess) e = launch_k(k, grid, dim3(threads), sm, stream, ta, tb, tc, g);
     } else {
       const int sm = tc_smem(2, 2, true) + g.Kw * 6 * 4;  // + the layer's weight table
       if (sm > 227 * 1024) return cudaErrorInvalidValue;
       auto k = gemm_tc_kernel<EPI_NODE, 2, 2, true, TC_EPI_WARPS, ASRC_CONF>;
       e = allow_dynamic_smem(reinterpret_cast<const void*>(k), sm);
-      if (e == cudaSuccess) k<<<grid, threads, sm, stream>>>(ta, tb, tc, g);
+      if (e == cudaSuccess) e = launch_k(k, grid, dim3(threads), sm, stream, ta, tb, tc, g);
     }
     if (e != cudaSuccess) return e;
     note_launch();
@@ -815,7 +817,7 @@ cudaError_t launch_gemm(int epi, const GemmArgs& g, cudaStream_t stream) {
 #define LC_TC_RUN(E, KERNEL, THREADS, SMEM)                                                  \
   {                                                                                          \
     e = allow_dynamic_smem(reinterpret_cast<const void*>(KERNEL), SMEM);                     \
-    if (e == cudaSuccess) KERNEL<<<grid, THREADS, SMEM, stream>>>(ta, tb, tc, g);            \
+    if (e == cudaSuccess) e = launch_k(KERNEL, grid, dim3(THREADS), SMEM, stream, ta, tb, tc, g); \
   }
 #define LC_TC_LAUNCH(E)                                                                      \
   if (pair && wide)                                                                          \

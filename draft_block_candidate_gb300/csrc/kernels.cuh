@@ -1,6 +1,8 @@
 // Host-side launchers of the rerank kernels (one declaration shared by all units).
 #pragma once
 
+#include <utility>
+
 #include "common.cuh"
 
 namespace lilicorr {
@@ -117,4 +119,31 @@ cudaError_t launch_attention_tc_long(const __nv_bfloat16* qkv, int64_t batch, in
 cudaError_t at_read_device_error(uint32_t* code);
 cudaError_t launch_rows_bias(const float* bias, int64_t rows, int N, float* out,
                              cudaStream_t stream);
+
+// Programmatic dependent launch of the path's kernels (lilicorr_api.cu): while a
+// PdlScope with `on` is alive in this host thread, launch_k lets each launch begin before
+// the previous kernel on the stream has finished; the kernels order their memory
+// accesses after it with pdl_wait.  Off by default (the standalone entry points).
+bool pdl_enabled();
+struct PdlScope {
+  bool prev;
+  explicit PdlScope(bool on);
+  ~PdlScope();
+  void set(bool on);
+};
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                     cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 }  // namespace lilicorr

@@ -360,6 +360,8 @@ __global__ void __launch_bounds__(K1_THREADS, K1_MIN_BLOCKS) logit_pass_kernel(c
   if (tid < K1_GROUPS) s_gmax[tid] = float_key(-INFINITY);
   if (tid < K1_CWARPS) s_wcnt[tid] = 0;
   __syncthreads();
+  pdl_wait();
+  pdl_trigger();
 
   float m2 = M2_INIT, ssum = 0.f;
   WarpQueue q;  // this warp's running top-32 (one entry per lane, sorted)
@@ -784,10 +786,12 @@ cudaError_t k1_launch(const void* logits, int esize, int64_t batch, int B, int64
                                : allow_dynamic_smem(reinterpret_cast<const void*>(logit_pass_kernel<float>), dyn);
     if (e != cudaSuccess) return e;
   }
-  if (esize == 2)
-    logit_pass_kernel<__nv_bfloat16><<<grid, K1_THREADS, dyn, stream>>>(prm);
-  else
-    logit_pass_kernel<float><<<grid, K1_THREADS, dyn, stream>>>(prm);
+  const cudaError_t e = esize == 2
+                            ? launch_k(logit_pass_kernel<__nv_bfloat16>, grid, dim3(K1_THREADS), dyn,
+                                       stream, prm)
+                            : launch_k(logit_pass_kernel<float>, grid, dim3(K1_THREADS), dyn, stream,
+                                       prm);
+  if (e != cudaSuccess) return e;
   note_launch();
   return cudaGetLastError();
 }

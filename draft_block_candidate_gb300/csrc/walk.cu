@@ -59,6 +59,8 @@ __global__ void __launch_bounds__(32 * PS_MAX_WARPS, 3) pair_scores_kernel(
     int B, int K, int E, float sigma, float* __restrict__ scores, float* __restrict__ out_tap,
     float* __restrict__ in_tap, float* __restrict__ anchor_tap) {
   extern __shared__ __align__(16) float ps_smem[];
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int p = blockIdx.x * (blockDim.x >> 5) + warp;
   const int b = blockIdx.y;
@@ -201,6 +203,8 @@ __global__ void __launch_bounds__(32) greedy_walk_kernel(
     int32_t* __restrict__ tokens, int32_t* __restrict__ choice, float* __restrict__ path,
     bool staged) {
   extern __shared__ __align__(16) float gw_smem[];
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int64_t b = blockIdx.x;
   if (b >= batch) return;
@@ -416,9 +420,9 @@ cudaError_t launch_pair_scores(const float* heads, const float* anchor_raw, int6
                                      static_cast<int>(pw * per_warp));
   if (e != cudaSuccess) return e;
   const dim3 grid(static_cast<unsigned>((B - 1 + pw - 1) / pw), static_cast<unsigned>(batch));
-  pair_scores_kernel<<<grid, 32 * pw, pw * per_warp, stream>>>(heads, anchor_raw, anchor_stride, B,
-                                                                K, E, sigma, scores, out_tap,
-                                                                in_tap, anchor_tap);
+  e = launch_k(pair_scores_kernel, grid, dim3(32 * pw), pw * per_warp, stream, heads, anchor_raw,
+               anchor_stride, B, K, E, sigma, scores, out_tap, in_tap, anchor_tap);
+  if (e != cudaSuccess) return e;
   note_launch();
   return cudaGetLastError();
 }
@@ -433,8 +437,9 @@ cudaError_t launch_greedy_walk(const float* scores, const int32_t* cand_id,
   cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void*>(greedy_walk_kernel),
                                      static_cast<int>(kMaxStage));
   if (e != cudaSuccess) return e;
-  greedy_walk_kernel<<<static_cast<unsigned>(batch), 32, staged ? need : 0, stream>>>(
-      scores, cand_id, anchor_ids, batch, B, K, tokens, choice, path, staged);
+  e = launch_k(greedy_walk_kernel, dim3(static_cast<unsigned>(batch)), dim3(32), staged ? need : 0,
+               stream, scores, cand_id, anchor_ids, batch, B, K, tokens, choice, path, staged);
+  if (e != cudaSuccess) return e;
   note_launch();
   return cudaGetLastError();
 }
