@@ -166,16 +166,6 @@ __host__ __device__ constexpr uint32_t at_idesc(int M, int N, bool b_mn) {
          (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
 }
 
-// (a, b) -> packed bf16 hi words and lo words: hi = bf16(x), lo = bf16(x - hi).
-__device__ __forceinline__ void at_split2(float a, float b, uint32_t& hi, uint32_t& lo) {
-  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-  const uint32_t hw = *reinterpret_cast<const uint32_t*>(&h);
-  const __nv_bfloat162 l2 = __floats2bfloat162_rn(a - __uint_as_float(hw << 16),
-                                                  b - __uint_as_float(hw & 0xffff0000u));
-  hi = hw;
-  lo = *reinterpret_cast<const uint32_t*>(&l2);
-}
-
 // The four softmax warps of one 32-row quarter (named barriers 2-5).
 __device__ __forceinline__ void quarter_sync(int q) {
   asm volatile("bar.sync %0, 128;" ::"r"(2 + q) : "memory");
@@ -417,7 +407,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       uint32_t hi[AT_OW / 2], lo[AT_OW / 2];
 #pragma unroll
       for (int e = 0; e < AT_OW; e += 2)
-        at_split2((v[e] + vl[e]) * p_inv, (v[e + 1] + vl[e + 1]) * p_inv, hi[e / 2], lo[e / 2]);
+        split2_bf16((v[e] + vl[e]) * p_inv, (v[e + 1] + vl[e + 1]) * p_inv, hi[e / 2], lo[e / 2]);
       // this warp's 16 columns = 16-byte chunks 2hf, 2hf + 1 of the row's 128 bytes, at
       // chunk ^ (row & 7) under the 128-byte swizzle
 #pragma unroll
@@ -514,7 +504,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
           const float2 y = __fadd2_rn(make_float2(v[2 * u], v[2 * u + 1]), nm);
           const float p0 = at_ex2(y.x), p1 = at_ex2(y.y);
           l2 = __fadd2_rn(l2, make_float2(p0, p1));
-          at_split2(p0, p1, ph[u], pl[u]);
+          split2_bf16(p0, p1, ph[u], pl[u]);
         }
         const float l = l2.x + l2.y;
         at_st16(tS + lane_off + jb, ph);
@@ -875,7 +865,7 @@ __global__ void __launch_bounds__(AL_THREADS, 1)
             const float2 y = __fadd2_rn(make_float2(v[e], v[e + 1]), nm);
             const float p0 = at_ex2(y.x), p1 = at_ex2(y.y);
             l2 = __fadd2_rn(l2, make_float2(p0, p1));
-            at_split2(p0, p1, ph[u], pl[u]);
+            split2_bf16(p0, p1, ph[u], pl[u]);
           }
           at_st8(tS + lane_off + uint32_t(128 * sb + jb + 8 * h2), ph);
           at_st8(tS + lane_off + uint32_t(128 * sb + jb + 16 + 8 * h2), pl);
@@ -911,7 +901,7 @@ __global__ void __launch_bounds__(AL_THREADS, 1)
       uint32_t hi[AT_OW / 2], lo[AT_OW / 2];
 #pragma unroll
       for (int e = 0; e < AT_OW; e += 2)
-        at_split2((v[e] + vl[e]) * inv, (v[e + 1] + vl[e + 1]) * inv, hi[e / 2], lo[e / 2]);
+        split2_bf16((v[e] + vl[e]) * inv, (v[e + 1] + vl[e + 1]) * inv, hi[e / 2], lo[e / 2]);
       // stored through the staging tile by bulk tensor stores of the quarter's 32 rows
       // (rows past the block are clipped): first the hi words, then, once that store has
       // read the staging, the lo words.  This warp's 16 columns = 16-byte chunks 2 hf,

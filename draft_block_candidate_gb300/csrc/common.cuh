@@ -121,6 +121,17 @@ __device__ __forceinline__ void split_bf16(float v, __nv_bfloat16& hi, __nv_bflo
   hi = __float2bfloat16_rn(v);
   lo = __float2bfloat16_rn(v - __bfloat162float(hi));
 }
+// The same for a pair, as packed words (a in the low half): one paired conversion per
+// word instead of two single ones (the conversions, not the arithmetic, set the pace of the
+// split epilogues).  Bit-identical to split_bf16 on each element.
+__device__ __forceinline__ void split2_bf16(float a, float b, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  const uint32_t hw = *reinterpret_cast<const uint32_t*>(&h);
+  const __nv_bfloat162 l2 = __floats2bfloat162_rn(a - __uint_as_float(hw << 16),
+                                                  b - __uint_as_float(hw & 0xffff0000u));
+  hi = hw;
+  lo = *reinterpret_cast<const uint32_t*>(&l2);
+}
 
 // Programmatic dependent launch.  pdl_wait: every memory access of the kernel comes after
 // it; it returns once the kernel before this one on the stream has completed and its

@@ -79,13 +79,7 @@ __device__ __forceinline__ void store_split8(const float (&v)[8], __nv_bfloat16*
                                              __nv_bfloat16* lo_dst) {
   uint32_t hi[4], lo[4];
 #pragma unroll
-  for (int j = 0; j < 8; j += 2) {
-    __nv_bfloat16 ha, la, hb, lb;
-    split_bf16(v[j], ha, la);
-    split_bf16(v[j + 1], hb, lb);
-    hi[j / 2] = uint32_t(__bfloat16_as_ushort(ha)) | (uint32_t(__bfloat16_as_ushort(hb)) << 16);
-    lo[j / 2] = uint32_t(__bfloat16_as_ushort(la)) | (uint32_t(__bfloat16_as_ushort(lb)) << 16);
-  }
+  for (int j = 0; j < 8; j += 2) split2_bf16(v[j], v[j + 1], hi[j / 2], lo[j / 2]);
   *reinterpret_cast<uint4*>(hi_dst) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
   *reinterpret_cast<uint4*>(lo_dst) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
 }
@@ -451,11 +445,10 @@ __global__ void __launch_bounds__(AT_THREADS) attention_kernel(
 #pragma unroll
     for (int dt = 0; dt < DH / 8; ++dt) {
       const int d = dt * 8 + (lane & 3) * 2;
-      __nv_bfloat16 h0, l0, h1, l1;
-      split_bf16(o[dt][rr * 2] * inv, h0, l0);
-      split_bf16(o[dt][rr * 2 + 1] * inv, h1, l1);
-      *reinterpret_cast<__nv_bfloat162*>(dst + d) = __halves2bfloat162(h0, h1);
-      *reinterpret_cast<__nv_bfloat162*>(dst + H + d) = __halves2bfloat162(l0, l1);
+      uint32_t hw, lw;
+      split2_bf16(o[dt][rr * 2] * inv, o[dt][rr * 2 + 1] * inv, hw, lw);
+      *reinterpret_cast<uint32_t*>(dst + d) = hw;
+      *reinterpret_cast<uint32_t*>(dst + H + d) = lw;
     }
   }
 }
