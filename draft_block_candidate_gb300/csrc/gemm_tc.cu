@@ -259,25 +259,36 @@ __device__ __forceinline__ void tc_node_terms(const GemmArgs& g, const NodeRow& 
   }
 }
 
-// Staged form of the bias / SiLU / split / residual epilogues: v[0..31] = accumulator
-// columns n..n+31 of this lane's row; the warp's 32 x 32 chunk goes to shared memory in
-// the layout of the output tensor map's swizzle (16-byte unit u of row r at u ^ f(r)),
-// then one lane stores it (or adds it into the residual) with a bulk tensor copy.
-template <int EPI, bool BIAS = true>
-__device__ __forceinline__ void tc_epilogue_staged(const GemmArgs& g, const CUtensorMap* tmC,
-                                                   uint8_t* stg, int lane, int64_t row0, int n,
-                                                   float (&v)[32]) {
+// The bias of this lane's row, columns n..n+31 (one bias for all rows, or the row's block
+// row when bias_group > 0; rows past M reuse the last one): loaded before the accumulator
+// and the staging buffer are waited for, so its latency overlaps those waits.
+__device__ __forceinline__ void tc_bias_fetch(const GemmArgs& g, int64_t row0, int lane, int n,
+                                              float4 (&bq)[8]) {
   const float* bias = g.bias + n;
-  if (g.bias_group > 0)  // per-block bias row (rows past M reuse the last one)
+  if (g.bias_group > 0)
     bias += (std::min<int64_t>(row0 + lane, g.M - 1) / g.bias_group) *
             (g.bias_stride > 0 ? g.bias_stride : int64_t(g.N));
 #pragma unroll
-  for (int j = 0; j < 32 && BIAS; j += 4) {
-    const float4 b4 = __ldg(reinterpret_cast<const float4*>(bias + j));
-    v[j] += b4.x;
-    v[j + 1] += b4.y;
-    v[j + 2] += b4.z;
-    v[j + 3] += b4.w;
+  for (int j = 0; j < 8; ++j) bq[j] = __ldg(reinterpret_cast<const float4*>(bias) + j);
+}
+
+// Staged form of the bias / SiLU / split / residual epilogues: v[0..31] = accumulator
+// columns n..n+31 of this lane's row (bq its bias, or null); the warp's 32 x 32 chunk goes
+// to shared memory in the layout of the output tensor map's swizzle (16-byte unit u of row
+// r at u ^ f(r)), then one lane stores it (or adds it into the residual) with bulk tensor
+// copies.
+template <int EPI>
+__device__ __forceinline__ void tc_epilogue_staged(const GemmArgs& g, const CUtensorMap* tmC,
+                                                   uint8_t* stg, int lane, int64_t row0, int n,
+                                                   float (&v)[32], const float4* bq) {
+  if (bq) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      v[4 * j] += bq[j].x;
+      v[4 * j + 1] += bq[j].y;
+      v[4 * j + 2] += bq[j].z;
+      v[4 * j + 3] += bq[j].w;
+    }
   }
   if constexpr (EPI == EPI_SPLIT || EPI == EPI_SPLIT_SILU) {
     uint32_t hi[16], lo[16];
@@ -632,11 +643,16 @@ __global__ void __launch_bounds__(32 * (2 + EW + (ASRC != ASRC_TMA ? TC_A_WARPS 
                 bulk_wait_read0();
             }
             __syncwarp();
-            tc_epilogue_staged<EPI_F32, false>(g, &tmC, stg + sb * TC_STG_BYTES, lane,
-                                               m0 + 32 * q, n, v);
+            tc_epilogue_staged<EPI_F32>(g, &tmC, stg + sb * TC_STG_BYTES, lane, m0 + 32 * q,
+                                        n, v, nullptr);
             sb = (sb + 1) % TC_STG_BUFS;
           }
         } else if (n < g.N) {
+          // the bias is loaded ahead of the waits where registers allow (8 epilogue warps,
+          // no producer warps: 112+ registers a thread)
+          constexpr bool EARLY = EW == 8 && ASRC == ASRC_TMA;
+          float4 bq[8];
+          if constexpr (EARLY) tc_bias_fetch(g, m0 + 32 * q, lane, n, bq);
           tmem_ld32(tmem + (uint32_t(32 * q) << 16) + uint32_t(buf * TC_BN + cc * 32), v);
           // the buffer's previous bulk copy must have finished reading it
           if (lane == 0) {
@@ -646,7 +662,8 @@ __global__ void __launch_bounds__(32 * (2 + EW + (ASRC != ASRC_TMA ? TC_A_WARPS 
               bulk_wait_read0();
           }
           __syncwarp();
-          tc_epilogue_staged<EPI>(g, &tmC, stg + sb * TC_STG_BYTES, lane, m0 + 32 * q, n, v);
+          if constexpr (!EARLY) tc_bias_fetch(g, m0 + 32 * q, lane, n, bq);
+          tc_epilogue_staged<EPI>(g, &tmC, stg + sb * TC_STG_BYTES, lane, m0 + 32 * q, n, v, bq);
           sb = (sb + 1) % TC_STG_BUFS;
         }
       }
@@ -817,10 +834,12 @@ __global__ void __launch_bounds__(NM_THREADS, 1)
         const int n = n0 + cc * 32;
         if (n >= g.N) continue;
         float v[32];
+        float4 bq[8];
         tmem_ld32(tmem + (uint32_t(32 * q) << 16) + uint32_t(buf * TC_BN + cc * 32), v);
         if (lane == 0) bulk_wait_read0();  // the previous chunk's store has read the buffer
         __syncwarp();
-        tc_epilogue_staged<EPI>(g, &tmC, stg, lane, m0 + 32 * q, n, v);
+        tc_bias_fetch(g, m0 + 32 * q, lane, n, bq);
+        tc_epilogue_staged<EPI>(g, &tmC, stg, lane, m0 + 32 * q, n, v, bq);
       }
       tc_fence_before();
       __syncwarp();
