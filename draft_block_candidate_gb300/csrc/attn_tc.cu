@@ -273,23 +273,34 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   // S / P of key half 0 in columns 0-127, of half 1 in 128-255; O' of even / odd items in
   // 256-319 / 320-383
   const uint32_t tS = tmem, tO0 = tmem + AT_O_COL;
+  // this CTA's items: a contiguous range (query tile fastest), so that the query tiles of a
+  // (block, head) follow each other and the later ones reuse the K / V tiles already in
+  // shared memory (only Q is loaded), and the head (with its bias table) rarely changes
+  const int64_t per = (nitems + gridDim.x - 1) / gridDim.x;
+  const int64_t first = int64_t(blockIdx.x) * per;
+  const int my_items = first < nitems ? static_cast<int>(min(per, nitems - first)) : 0;
 
   if (warp == 0 && lane == 0) {
     // ---- producer
-    int i = 0;
-    ItemPos it(blockIdx.x, gridDim.x, QT, batch);
-    for (int64_t t = blockIdx.x; t < nitems; t += gridDim.x, ++i, it.next()) {
+    ItemPos it(first, 1, QT, batch);
+    int pblk = -1, ph = -1;  // (block, head) whose K / V tiles are in shared memory
+    for (int i = 0; i < my_items; ++i, it.next()) {
       const int qt = it.qt, h = it.h;
       const int tok0 = it.blk * S;
       const int cq = h * AT_DH, ck = H + h * AT_DH, cv = 2 * H + h * AT_DH, lo = 3 * H;
+      const bool same_kv = it.blk == pblk && h == ph;
+      pblk = it.blk;
+      ph = h;
       if (i > 0 && !mbar_wait_bounded(&bar_qkfree, (i - 1) & 1, &g_err_at, ERR_AT_QKFREE)) break;
-      mbar_arrive_expect_tx(&bar_qk, 6 * AT_TILE);
+      mbar_arrive_expect_tx(&bar_qk, (same_kv ? 2 : 6) * AT_TILE);
       at_tma(sQh, &tm, cq, tok0 + qt * AT_QT, &bar_qk);
       at_tma(sQl, &tm, lo + cq, tok0 + qt * AT_QT, &bar_qk);
-      at_tma(sKh, &tm, ck, tok0, &bar_qk);
-      at_tma(sKh + AT_TILE, &tm, ck, tok0 + 128, &bar_qk);
-      at_tma(sKl, &tm, lo + ck, tok0, &bar_qk);
-      at_tma(sKl + AT_TILE, &tm, lo + ck, tok0 + 128, &bar_qk);
+      if (!same_kv) {
+        at_tma(sKh, &tm, ck, tok0, &bar_qk);
+        at_tma(sKh + AT_TILE, &tm, ck, tok0 + 128, &bar_qk);
+        at_tma(sKl, &tm, lo + ck, tok0, &bar_qk);
+        at_tma(sKl + AT_TILE, &tm, lo + ck, tok0 + 128, &bar_qk);
+      }
       // V by key halves: half 0 is free once the previous item's first product is done
       bool vok = true;
       for (int vh = 0; vh < 2 && vok; ++vh) {
@@ -297,9 +308,13 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
           vok = false;
           break;
         }
-        mbar_arrive_expect_tx(&bar_v[vh], 2 * AT_TILE);
-        at_tma(sVh + vh * AT_TILE, &tm, cv, tok0 + 128 * vh, &bar_v[vh]);
-        at_tma(sVl + vh * AT_TILE, &tm, lo + cv, tok0 + 128 * vh, &bar_v[vh]);
+        if (same_kv) {
+          mbar_arrive(&bar_v[vh]);  // the tiles in place serve this item too
+        } else {
+          mbar_arrive_expect_tx(&bar_v[vh], 2 * AT_TILE);
+          at_tma(sVh + vh * AT_TILE, &tm, cv, tok0 + 128 * vh, &bar_v[vh]);
+          at_tma(sVl + vh * AT_TILE, &tm, lo + cv, tok0 + 128 * vh, &bar_v[vh]);
+        }
       }
       if (!vok) break;
     }
@@ -333,8 +348,8 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         at_mma_ts(tO, tS + pc + 16, vhl, id_o, 1);
       }
     };
-    bool ok = mbar_wait_bounded(&bar_qk, 0, &g_err_at, ERR_AT_QK);
-    if (ok && blockIdx.x < nitems) {
+    bool ok = my_items > 0 && mbar_wait_bounded(&bar_qk, 0, &g_err_at, ERR_AT_QK);
+    if (ok) {
       at_fence_after();
       qk_half(0);
       at_commit(&bar_s0);
@@ -342,9 +357,8 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       at_commit(&bar_s1);
       at_commit(&bar_qkfree);
     }
-    int i = 0;
-    for (int64_t t = blockIdx.x; t < nitems && ok; t += gridDim.x, ++i) {
-      const bool more = t + gridDim.x < nitems;
+    for (int i = 0; i < my_items && ok; ++i) {
+      const bool more = i + 1 < my_items;
       const uint32_t tO = tO0 + AT_O_W * uint32_t(i & 1);
       ok = mbar_wait_bounded(&bar_p0, i & 1, &g_err_at, ERR_AT_P) &&
            mbar_wait_bounded(&bar_v[0], i & 1, &g_err_at, ERR_AT_V) &&
@@ -426,8 +440,8 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         asm volatile("cp.async.bulk.commit_group;" ::: "memory");
       }
     };
-    ItemPos it(blockIdx.x, gridDim.x, QT, batch);
-    for (int64_t t = blockIdx.x; t < nitems; t += gridDim.x, ++i, it.next()) {
+    ItemPos it(first, 1, QT, batch);
+    for (; i < my_items; ++i, it.next()) {
       const int qt = it.qt, h = it.h, blk = it.blk;
       const int q = qt * AT_QT + r;
       const uint32_t tO = tO0 + AT_O_W * uint32_t(i & 1);
@@ -995,7 +1009,9 @@ cudaError_t launch_attention_tc(const __nv_bfloat16* qkv, int64_t batch, int S, 
   if (e != cudaSuccess) return e;
   const int sms = device_sm_count();
   const int64_t nitems = batch * heads * ((S + AT_QT - 1) / AT_QT);
-  const dim3 grid(static_cast<unsigned>(nitems < sms ? nitems : sms));
+  // contiguous item ranges of ceil(nitems / SMs): as many CTAs as that takes, none empty
+  const int64_t per = (nitems + sms - 1) / sms;
+  const dim3 grid(static_cast<unsigned>((nitems + per - 1) / per));
   e = launch_k(attn_tc_kernel, grid, dim3(AT_THREADS), smem, stream, tm, tmo, S, K, H, B_max,
                heads, batch, dist_bias, same_bias);
   if (e != cudaSuccess) return e;
