@@ -67,6 +67,22 @@ __device__ __forceinline__ void at_tma(void* dst, const CUtensorMap* tm, int c0,
       "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(smem_addr(bar))
       : "memory");
 }
+__device__ __forceinline__ void at_tma3(void* dst, const CUtensorMap* tm, int c0, int c1, int c2,
+                                        uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_addr(bar))
+      : "memory");
+}
+__device__ __forceinline__ void at_store4(const CUtensorMap* tm, const void* src, int c0, int c1,
+                                          int c2, int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(tm)),
+      "r"(smem_addr(src)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
 __device__ __forceinline__ void at_store(const CUtensorMap* tm, const void* src, int c0, int c1,
                                          int c2) {
   asm volatile(
@@ -215,7 +231,8 @@ __device__ __forceinline__ void soft_sync() {
 __global__ void __launch_bounds__(AT_THREADS, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm, const __grid_constant__ CUtensorMap tmo,
                    int S, int Kc, int H, int B_max, int heads, int64_t batch,
-                   const float* __restrict__ dist_bias, const float* __restrict__ same_bias) {
+                   const float* __restrict__ dist_bias, const float* __restrict__ same_bias,
+                   int dh) {
   extern __shared__ uint8_t at_smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(at_smem_raw) + 1023) & ~uintptr_t(1023));
@@ -287,19 +304,27 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     for (int i = 0; i < my_items; ++i, it.next()) {
       const int qt = it.qt, h = it.h;
       const int tok0 = it.blk * S;
-      const int cq = h * AT_DH, ck = H + h * AT_DH, cv = 2 * H + h * AT_DH, lo = 3 * H;
+      const int cq = h * dh, ck = H + h * dh, cv = 2 * H + h * dh, lo = 3 * H;
+      // a [128 x 64] tile at column col: plain 2-D box, or for head dim 32 the 3-D view
+      // whose 64-wide box over 32-wide heads has its upper half zero-filled
+      auto ld = [&](void* dst, int col, int row, uint64_t* bar) {
+        if (dh == AT_DH)
+          at_tma(dst, &tm, col, row, bar);
+        else
+          at_tma3(dst, &tm, 0, col >> 5, row, bar);
+      };
       const bool same_kv = it.blk == pblk && h == ph;
       pblk = it.blk;
       ph = h;
       if (i > 0 && !mbar_wait_bounded(&bar_qkfree, (i - 1) & 1, &g_err_at, ERR_AT_QKFREE)) break;
       mbar_arrive_expect_tx(&bar_qk, (same_kv ? 2 : 6) * AT_TILE);
-      at_tma(sQh, &tm, cq, tok0 + qt * AT_QT, &bar_qk);
-      at_tma(sQl, &tm, lo + cq, tok0 + qt * AT_QT, &bar_qk);
+      ld(sQh, cq, tok0 + qt * AT_QT, &bar_qk);
+      ld(sQl, lo + cq, tok0 + qt * AT_QT, &bar_qk);
       if (!same_kv) {
-        at_tma(sKh, &tm, ck, tok0, &bar_qk);
-        at_tma(sKh + AT_TILE, &tm, ck, tok0 + 128, &bar_qk);
-        at_tma(sKl, &tm, lo + ck, tok0, &bar_qk);
-        at_tma(sKl + AT_TILE, &tm, lo + ck, tok0 + 128, &bar_qk);
+        ld(sKh, ck, tok0, &bar_qk);
+        ld(sKh + AT_TILE, ck, tok0 + 128, &bar_qk);
+        ld(sKl, lo + ck, tok0, &bar_qk);
+        ld(sKl + AT_TILE, lo + ck, tok0 + 128, &bar_qk);
       }
       // V by key halves: half 0 is free once the previous item's first product is done
       bool vok = true;
@@ -312,8 +337,8 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
           mbar_arrive(&bar_v[vh]);  // the tiles in place serve this item too
         } else {
           mbar_arrive_expect_tx(&bar_v[vh], 2 * AT_TILE);
-          at_tma(sVh + vh * AT_TILE, &tm, cv, tok0 + 128 * vh, &bar_v[vh]);
-          at_tma(sVl + vh * AT_TILE, &tm, lo + cv, tok0 + 128 * vh, &bar_v[vh]);
+          ld(sVh + vh * AT_TILE, cv, tok0 + 128 * vh, &bar_v[vh]);
+          ld(sVl + vh * AT_TILE, lo + cv, tok0 + 128 * vh, &bar_v[vh]);
         }
       }
       if (!vok) break;
@@ -398,7 +423,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     const int r = 32 * qq + lane;  // TMEM lane = query row of the tile
     const uint32_t lane_off = uint32_t(32 * qq) << 16;
     const int nq = S / Kc;         // query slots
-    constexpr float C = 0.125f * AT_LOG2E;  // 1 / sqrt(64), in log2 units
+    const float C = (dh == AT_DH ? 0.125f : 0.17677669529663687f) * AT_LOG2E;  // 1/sqrt(dh), log2 units
     constexpr float RESCALE_AT = 16.f;      // log2 headroom before half 1 re-bases
     int i = 0;
     int cur_h = -1;
@@ -435,8 +460,14 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       quarter_sync(qq);
       if (hf == 0 && lane == 0 && ok2 && p_qt * AT_QT + 32 * qq < S) {
-        at_store(&tmo, sOh + 32 * qq * 128, p_h * AT_DH, p_qt * AT_QT + 32 * qq, p_blk);
-        at_store(&tmo, sOl + 32 * qq * 128, H + p_h * AT_DH, p_qt * AT_QT + 32 * qq, p_blk);
+        if (dh == AT_DH) {
+          at_store(&tmo, sOh + 32 * qq * 128, p_h * AT_DH, p_qt * AT_QT + 32 * qq, p_blk);
+          at_store(&tmo, sOl + 32 * qq * 128, H + p_h * AT_DH, p_qt * AT_QT + 32 * qq, p_blk);
+        } else {
+          // 4-D view over 32-wide heads: the box's upper 32 columns (zeros) are clipped
+          at_store4(&tmo, sOh + 32 * qq * 128, 0, p_h, p_qt * AT_QT + 32 * qq, p_blk);
+          at_store4(&tmo, sOl + 32 * qq * 128, 0, heads + p_h, p_qt * AT_QT + 32 * qq, p_blk);
+        }
         asm volatile("cp.async.bulk.commit_group;" ::: "memory");
       }
     };
@@ -973,9 +1004,12 @@ static PFN_cuTensorMapEncodeTiled_v12000 at_encode_fn() {
 
 static int at_smem_bytes(int S, int K) { return AT_SMEM + (S / K) * AT_BSTRIDE * 4; }
 
+// Head dim 64, or 32 through zero-filled 64-wide tiles (the products then run at the
+// head-dim-64 cost; the workloads' head-dim-32 lattice is the 12-token tiny one).
 bool attention_tc_supported(int S, int K, int H, int heads, int B_max) {
-  return H / heads == AT_DH && S >= 1 && S <= AT_KMAX && K >= 1 && H % 64 == 0 &&
-         B_max <= 64 && at_smem_bytes(S, K) <= AT_SMEM_MAX;
+  const int dh = heads > 0 ? H / heads : 0;
+  return (dh == AT_DH || dh == 32) && dh * heads == H && S >= 1 && S <= AT_KMAX && K >= 1 &&
+         H % 64 == 0 && B_max <= 64 && at_smem_bytes(S, K) <= AT_SMEM_MAX;
 }
 
 cudaError_t launch_attention_tc(const __nv_bfloat16* qkv, int64_t batch, int S, int K, int H,
@@ -985,25 +1019,47 @@ cudaError_t launch_attention_tc(const __nv_bfloat16* qkv, int64_t batch, int S, 
   auto fn = at_encode_fn();
   if (!fn || !attention_tc_supported(S, K, H, heads, B_max)) return cudaErrorInvalidValue;
   const int64_t M = batch * S;
-  CUtensorMap tm;
-  const cuuint64_t dims[2] = {cuuint64_t(6 * H), cuuint64_t(M)};
-  const cuuint64_t strides[1] = {cuuint64_t(6 * H) * 2};
-  const cuuint32_t box[2] = {64, 128};
-  const cuuint32_t estr[2] = {1, 1};
-  if (fn(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<__nv_bfloat16*>(qkv), dims, strides,
-         box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-    return cudaErrorInvalidValue;
-  // output [batch][S][2H] (hi | lo): 3-D so that a store box never runs into the next block
-  CUtensorMap tmo;
-  const cuuint64_t odims[3] = {cuuint64_t(2 * H), cuuint64_t(S), cuuint64_t(batch)};
-  const cuuint64_t ostrides[2] = {cuuint64_t(2 * H) * 2, cuuint64_t(S) * 2 * H * 2};
-  const cuuint32_t obox[3] = {64, 32, 1};
-  const cuuint32_t oestr[3] = {1, 1, 1};
-  if (fn(&tmo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, out, odims, ostrides, obox, oestr,
-         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-         CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-    return cudaErrorInvalidValue;
+  const int dh = H / heads;
+  CUtensorMap tm, tmo;
+  if (dh == AT_DH) {
+    const cuuint64_t dims[2] = {cuuint64_t(6 * H), cuuint64_t(M)};
+    const cuuint64_t strides[1] = {cuuint64_t(6 * H) * 2};
+    const cuuint32_t box[2] = {64, 128};
+    const cuuint32_t estr[2] = {1, 1};
+    if (fn(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<__nv_bfloat16*>(qkv), dims,
+           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+    // output [batch][S][2H] (hi | lo): 3-D so that a store box never runs into the next block
+    const cuuint64_t odims[3] = {cuuint64_t(2 * H), cuuint64_t(S), cuuint64_t(batch)};
+    const cuuint64_t ostrides[2] = {cuuint64_t(2 * H) * 2, cuuint64_t(S) * 2 * H * 2};
+    const cuuint32_t obox[3] = {64, 32, 1};
+    const cuuint32_t oestr[3] = {1, 1, 1};
+    if (fn(&tmo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, out, odims, ostrides, obox, oestr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+           CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  } else {
+    // head dim 32: qkv as [M][6H / 32][32], read in [128][1][64] boxes (the 32 columns
+    // past each head's end zero-filled), and the output as [batch][S][2H / 32][32],
+    // written in [1][32][1][64] boxes (the zero half clipped)
+    const cuuint64_t dims[3] = {32, cuuint64_t(6 * H / 32), cuuint64_t(M)};
+    const cuuint64_t strides[2] = {64, cuuint64_t(6 * H) * 2};
+    const cuuint32_t box[3] = {64, 1, 128};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    if (fn(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<__nv_bfloat16*>(qkv), dims,
+           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+    const cuuint64_t odims[4] = {32, cuuint64_t(2 * H / 32), cuuint64_t(S), cuuint64_t(batch)};
+    const cuuint64_t ostrides[3] = {64, cuuint64_t(2 * H) * 2, cuuint64_t(S) * 2 * H * 2};
+    const cuuint32_t obox[4] = {64, 1, 32, 1};
+    const cuuint32_t oestr[4] = {1, 1, 1, 1};
+    if (fn(&tmo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, out, odims, ostrides, obox, oestr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+           CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
   const int smem = at_smem_bytes(S, K);
   cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void*>(attn_tc_kernel), smem);
   if (e != cudaSuccess) return e;
@@ -1013,7 +1069,7 @@ cudaError_t launch_attention_tc(const __nv_bfloat16* qkv, int64_t batch, int S, 
   const int64_t per = (nitems + sms - 1) / sms;
   const dim3 grid(static_cast<unsigned>((nitems + per - 1) / per));
   e = launch_k(attn_tc_kernel, grid, dim3(AT_THREADS), smem, stream, tm, tmo, S, K, H, B_max,
-               heads, batch, dist_bias, same_bias);
+               heads, batch, dist_bias, same_bias, dh);
   if (e != cudaSuccess) return e;
   note_launch();
   return cudaGetLastError();

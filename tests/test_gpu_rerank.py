@@ -108,6 +108,10 @@ SMALL = [  # name, overrides
     ("widepool", dict(V=2048, batch=2, B=12)),       # 352 tokens at hidden 512
     ("single", dict(V=2048, batch=2, K=32, B=17)),   # 512 tokens: 4 full chunks
     ("single", dict(V=2048, batch=1, K=32, B=18)),   # 544 tokens: the mma.sync attention
+    # head dim 32 on the tcgen05 attention (zero-filled 64-wide tiles): two query tiles
+    # with the K / V tiles reused, and a 3-slot lattice
+    ("single", dict(V=2048, batch=3, heads=8, K=16)),  # hidden 256, 8 heads, 240 tokens
+    ("tiny", dict(batch=2, seed=5)),
 ]
 
 
