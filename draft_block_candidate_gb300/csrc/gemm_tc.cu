@@ -688,253 +688,6 @@ __global__ void __launch_bounds__(32 * (2 + EW + (ASRC != ASRC_TMA ? TC_A_WARPS 
   }
 }
 
-// ------------------------------------------------------------------ RMSNorm-fed contractions
-//
-// QKV and FFN1 read RMSNorm(X) * gain (LiLiCorr App. A: pre-norm layers) as a split
-// operand.  Made once per 128-row tile and kept resident in shared memory for every column
-// tile of that row tile, it replaces the standalone normalisation pass (its read of X and
-// its write and re-read of the normalised operand).  Hidden width 256: the resident
-// operand is 128 rows x 256 columns x (hi + lo) = 128 KB, as 8 swizzled K-major blocks
-// (A_hi of K block kb at kb, A_lo at 4 + kb).
-//
-// Each CTA takes a contiguous range of the (row tile, column tile) grid, column tiles
-// fastest: its tiles of one row tile run back to back, and tile counts per CTA differ by at
-// most one.  18 warps:
-//   warp 0      TMA for W (a 2-stage ring of 256 x 64 blocks) and TMEM owner
-//   warp 1      MMA issuer as in gemm_tc_kernel, A from the resident blocks; after the
-//               last tile of a row tile it commits each block's release barrier
-//   warps 2-9   epilogue as in gemm_tc_kernel (bias, optional SiLU, split, bulk stores)
-//   warps 10-17 the operand: per row tile, 16 rows per warp.  First the inverse RMS of the
-//               rows (X read from HBM, lane l holding columns 8l..8l+7 and the sum of squares
-//               taken in the same order as the standalone pass, so the operand is bit-
-//               identical to it), overlapping the previous row tile's MMAs; then per
-//               64-column block kb, once those MMAs have released the block, X re-read
-//               (from L2) times inv times gain, split and stored, and the block's full
-//               barrier raised.
-constexpr int NM_H = 256, NM_KB = NM_H / TC_BK, NM_WST = 2, NM_EW = 8, NM_PW = 8;
-constexpr int NM_THREADS = 32 * (2 + NM_EW + NM_PW);
-constexpr int NM_A_BYTES = 2 * NM_KB * TC_A_BYTES;  // resident A_hi and A_lo blocks
-constexpr int NM_SMEM = NM_A_BYTES + NM_WST * TC_B_BYTES + NM_EW * TC_STG_BYTES + 1024;
-
-template <int EPI>
-__global__ void __launch_bounds__(NM_THREADS, 1)
-    gemm_norm_kernel(const __grid_constant__ CUtensorMap tmB,
-                     const __grid_constant__ CUtensorMap tmC, const GemmArgs g) {
-  extern __shared__ uint8_t tc_smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sA = smem;                   // block b at sA + b * TC_A_BYTES
-  uint8_t* sB = smem + NM_A_BYTES;      // W stage s at sB + s * TC_B_BYTES
-  uint8_t* sStage = sB + NM_WST * TC_B_BYTES;
-  __shared__ __align__(8) uint64_t w_full[NM_WST], w_empty[NM_WST];
-  __shared__ __align__(8) uint64_t a_full[NM_KB], a_empty[NM_KB];
-  __shared__ __align__(8) uint64_t acc_full[2], acc_empty[2];
-  __shared__ uint32_t s_tmem;
-
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int NT = (g.N + TC_BN - 1) / TC_BN;
-  const int MT = static_cast<int>((g.M + TC_BM - 1) / TC_BM);
-  const int ntiles = NT * MT;
-  const int per = ntiles / gridDim.x, rem = ntiles % gridDim.x;
-  const int bx = blockIdx.x;
-  const int t0 = bx * per + (bx < rem ? bx : rem);
-  const int t1 = t0 + per + (bx < rem ? 1 : 0);
-
-  if (tid == 0) {
-    for (int s = 0; s < NM_WST; ++s) {
-      mbar_init(&w_full[s], 1);
-      mbar_init(&w_empty[s], 1);
-    }
-    for (int b = 0; b < NM_KB; ++b) {
-      mbar_init(&a_full[b], 32 * NM_PW);
-      mbar_init(&a_empty[b], 1);
-    }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], NM_EW);
-    }
-    fence_mbar_init();
-  }
-  if (warp == 0) tmem_alloc(&s_tmem, TC_TMEM_COLS);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = s_tmem;
-  pdl_wait();
-  pdl_trigger();
-
-  if (warp == 0 && lane == 0) {
-    // ---- W producer: the ring runs on across tiles and row tiles
-    int it = 0;
-    bool ok = true;
-    for (int t = t0; t < t1 && ok; ++t) {
-      const int n0 = (t % NT) * TC_BN;
-      for (int kb = 0; kb < NM_KB; ++kb, ++it) {
-        const int s = it % NM_WST, use = it / NM_WST;
-        if (use > 0 && !mbar_wait_bounded(&w_empty[s], (use - 1) & 1, &g_err_tc, ERR_TC_EMPTY)) {
-          ok = false;
-          break;
-        }
-        mbar_arrive_expect_tx(&w_full[s], TC_B_BYTES);
-        tma_load_2d(sB + s * TC_B_BYTES, &tmB, kb * TC_BK, n0, &w_full[s]);
-      }
-    }
-  } else if (warp == 1 && lane == 0) {
-    // ---- MMA issuer
-    constexpr uint32_t idesc = idesc_bf16(TC_BM, TC_BN);
-    int it = 0, i = 0, u = -1;
-    bool ok = true;
-    for (int t = t0; t < t1 && ok; ++t, ++i) {
-      const int j = t % NT;
-      const bool first = t == t0 || j == 0, last = t + 1 == t1 || j == NT - 1;
-      if (first) ++u;
-      const int buf = i & 1;
-      const uint32_t acc = tmem + uint32_t(buf * TC_BN);
-      if (i >= 2 && !mbar_wait_bounded(&acc_empty[buf], ((i >> 1) - 1) & 1, &g_err_tc,
-                                        ERR_TC_ACC_EMPTY))
-        break;
-      tc_fence_after();
-      for (int kb = 0; kb < NM_KB; ++kb, ++it) {
-        const int s = it % NM_WST, use = it / NM_WST;
-        if (!mbar_wait_bounded(&w_full[s], use & 1, &g_err_tc, ERR_TC_FULL) ||
-            (first && !mbar_wait_bounded(&a_full[kb], u & 1, &g_err_tc, ERR_TC_FULL))) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint8_t* ahi = sA + kb * TC_A_BYTES;
-        const uint8_t* alo = sA + (NM_KB + kb) * TC_A_BYTES;
-        const uint8_t* wb = sB + s * TC_B_BYTES;
-#pragma unroll
-        for (int kk = 0; kk < TC_BK / 16; ++kk)
-          umma_bf16(acc, sw128_desc(ahi + kk * 32), sw128_desc(wb + kk * 32), idesc,
-                    (kb | kk) != 0);
-#pragma unroll
-        for (int kk = 0; kk < TC_BK / 16; ++kk)
-          umma_bf16(acc, sw128_desc(alo + kk * 32), sw128_desc(wb + kk * 32), idesc, 1u);
-        umma_commit(&w_empty[s]);
-        if (last) umma_commit(&a_empty[kb]);  // the row tile's last reads of block kb
-      }
-      if (ok) umma_commit(&acc_full[buf]);
-    }
-  } else if (warp >= 2 && warp < 2 + NM_EW) {
-    // ---- epilogue: quarter q = warp % 4 owns TMEM lanes 32q..32q+31, half the columns
-    constexpr int CPP = (TC_BN / 32) / (NM_EW / 4);
-    const int q = warp & 3, half = (warp - 2) >> 2;
-    uint8_t* stg = sStage + (warp - 2) * TC_STG_BYTES;
-    int i = 0;
-    for (int t = t0; t < t1; ++t, ++i) {
-      const int buf = i & 1;
-      const int64_t m0 = int64_t(t / NT) * TC_BM;
-      const int n0 = (t % NT) * TC_BN;
-      if (!mbar_wait_bounded(&acc_full[buf], (i >> 1) & 1, &g_err_tc, ERR_TC_ACCUM)) break;
-      tc_fence_after();
-#pragma unroll 1
-      for (int cc = half * CPP; cc < (half + 1) * CPP; ++cc) {
-        const int n = n0 + cc * 32;
-        if (n >= g.N) continue;
-        float v[32];
-        float4 bq[8];
-        tmem_ld32(tmem + (uint32_t(32 * q) << 16) + uint32_t(buf * TC_BN + cc * 32), v);
-        if (lane == 0) bulk_wait_read0();  // the previous chunk's store has read the buffer
-        __syncwarp();
-        tc_bias_fetch(g, m0 + 32 * q, lane, n, bq);
-        tc_epilogue_staged<EPI>(g, &tmC, stg, lane, m0 + 32 * q, n, v, bq);
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[buf]);
-    }
-    if (lane == 0) bulk_wait_all();
-    __syncwarp();
-  } else if (warp >= 2 + NM_EW) {
-    // ---- operand producers: warp pw owns rows 16 pw .. 16 pw + 15 of each row tile
-    const int pw = warp - (2 + NM_EW);
-    const int rbase = 16 * pw;
-    const int unit = lane & 7, rq = lane >> 3;  // phase 2: rows rbase + rq + 4 i, unit
-    const float* X = g.a_x;
-    int u = -1;
-    bool ok = true;
-    for (int t = t0; t < t1 && ok; ++t) {
-      if (!(t == t0 || t % NT == 0)) continue;
-      ++u;
-      const int64_t m0 = int64_t(t / NT) * TC_BM;
-      // phase 1: inverse RMS of the warp's 16 rows, 4 rows per batch of loads
-      float myinv[4];
-#pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        float v[4][8];
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          const int64_t m = m0 + rbase + 4 * h + r;
-          if (m < g.M) {
-            const float4 a = *reinterpret_cast<const float4*>(X + m * NM_H + lane * 8);
-            const float4 b = *reinterpret_cast<const float4*>(X + m * NM_H + lane * 8 + 4);
-            v[r][0] = a.x; v[r][1] = a.y; v[r][2] = a.z; v[r][3] = a.w;
-            v[r][4] = b.x; v[r][5] = b.y; v[r][6] = b.z; v[r][7] = b.w;
-          } else {
-#pragma unroll
-            for (int c = 0; c < 8; ++c) v[r][c] = 0.f;
-          }
-        }
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          float ss = 0.f;
-#pragma unroll
-          for (int c = 0; c < 8; ++c) ss = fmaf(v[r][c], v[r][c], ss);
-#pragma unroll
-          for (int o = 16; o >= 1; o >>= 1) ss += __shfl_xor_sync(FULL_MASK, ss, o);
-          const float inv = 1.0f / sqrtf(ss / float(NM_H) + g.a_eps);
-          if (rq == r) myinv[h] = inv;  // row 4 h + r
-        }
-      }
-      // phase 2: per K block, the normalised split operand into the resident blocks
-#pragma unroll 1
-      for (int kb = 0; kb < NM_KB; ++kb) {
-        const int c0 = kb * TC_BK + unit * 8;
-        float x[4][8];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int64_t m = m0 + rbase + rq + 4 * i;
-          if (m < g.M) {
-            const float4 a = *reinterpret_cast<const float4*>(X + m * NM_H + c0);
-            const float4 b = *reinterpret_cast<const float4*>(X + m * NM_H + c0 + 4);
-            x[i][0] = a.x; x[i][1] = a.y; x[i][2] = a.z; x[i][3] = a.w;
-            x[i][4] = b.x; x[i][5] = b.y; x[i][6] = b.z; x[i][7] = b.w;
-          } else {
-#pragma unroll
-            for (int c = 0; c < 8; ++c) x[i][c] = 0.f;
-          }
-        }
-        const float4 ga = __ldg(reinterpret_cast<const float4*>(g.a_gain + c0));
-        const float4 gb = __ldg(reinterpret_cast<const float4*>(g.a_gain + c0 + 4));
-        const float gn[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
-        if (u > 0 &&
-            !mbar_wait_bounded(&a_empty[kb], (u - 1) & 1, &g_err_tc, ERR_TC_EMPTY)) {
-          ok = false;
-          break;
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          float v[8];
-#pragma unroll
-          for (int c = 0; c < 8; ++c) v[c] = x[i][c] * myinv[i] * gn[c];
-          a_store_unit(sA + kb * TC_A_BYTES, sA + (NM_KB + kb) * TC_A_BYTES, rbase + rq + 4 * i,
-                       unit, v);
-        }
-        fence_async_smem();
-        mbar_arrive(&a_full[kb]);
-      }
-    }
-  }
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 0) {
-    tc_fence_after();
-    tmem_dealloc(tmem, TC_TMEM_COLS);
-  }
-}
-
 // ------------------------------------------------------------------ host
 
 static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -987,33 +740,7 @@ bool gemm_tc_supported(const GemmArgs& g) {
          (reinterpret_cast<uintptr_t>(g.A) % 16) == 0 && (reinterpret_cast<uintptr_t>(g.W) % 16) == 0;
 }
 
-// RMSNorm-fed contraction (gemm_norm_kernel): Kw = 256, split A, bias [N], split output
-// with or without SiLU.
-static cudaError_t launch_gemm_norm(int epi, const GemmArgs& g, cudaStream_t stream) {
-  if ((epi != EPI_SPLIT && epi != EPI_SPLIT_SILU) || g.Kw != NM_H || g.Ka != 2 * NM_H ||
-      g.N % 32 || g.M <= 0 || !g.a_x || !g.a_gain || !g.bias || g.bias_group != 0 ||
-      !g.out_split || reinterpret_cast<uintptr_t>(g.a_x) % 16 ||
-      reinterpret_cast<uintptr_t>(g.a_gain) % 16 || reinterpret_cast<uintptr_t>(g.W) % 16 ||
-      reinterpret_cast<uintptr_t>(g.out_split) % 16)
-    return cudaErrorInvalidValue;
-  CUtensorMap tb, tc;
-  if (!make_tmap(&tb, g.W, uint64_t(g.N), uint64_t(g.Kw), TC_BN) ||
-      !make_tmap_out(&tc, g.out_split, uint64_t(g.M), uint64_t(2 * g.N), false))
-    return cudaErrorInvalidValue;
-  const int64_t ntiles = int64_t((g.N + TC_BN - 1) / TC_BN) * ((g.M + TC_BM - 1) / TC_BM);
-  if (ntiles > INT_MAX) return cudaErrorInvalidValue;
-  const int sms = device_sm_count();
-  const dim3 grid(static_cast<unsigned>(ntiles < sms ? ntiles : sms));
-  auto k = epi == EPI_SPLIT ? gemm_norm_kernel<EPI_SPLIT> : gemm_norm_kernel<EPI_SPLIT_SILU>;
-  cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void*>(k), NM_SMEM);
-  if (e == cudaSuccess) e = launch_k(k, grid, dim3(NM_THREADS), NM_SMEM, stream, tb, tc, g);
-  if (e != cudaSuccess) return e;
-  note_launch();
-  return cudaGetLastError();
-}
-
 cudaError_t launch_gemm(int epi, const GemmArgs& g, cudaStream_t stream) {
-  if (g.asrc == ASRC_NORM) return launch_gemm_norm(epi, g, stream);
   CUtensorMap ta, tb, tc;
   if (g.asrc != ASRC_TMA) {
     // A made in the kernel: the fusion input under the SiLU-split epilogue, or the

@@ -76,17 +76,13 @@ struct GemmArgs {
   //                Kw/2] bf16 (null: zero), the column blocks of h and h * t interleaved
   //   ASRC_CONF:   A = SiLU(a_w1 f + a_b1) [M, Kw], f the five confidence features of row
   //                m from a_cl [M] (candidate logits), a_lse [M / K] and its rank m % K
-  //   ASRC_NORM:   A = RMSNorm(a_x) * a_gain [M, Kw] (Kw = 256), eps a_eps, made once per
-  //                128-row tile and kept resident for all of that row tile's column tiles
   int asrc;
   const float* a_x;
   const __nv_bfloat16* a_t;
   int64_t a_group;
   const float *a_cl, *a_lse, *a_w1, *a_b1;
-  const float* a_gain;
-  float a_eps;
 };
-enum ASrc : int { ASRC_TMA = 0, ASRC_FUSION = 1, ASRC_CONF = 2, ASRC_NORM = 3 };
+enum ASrc : int { ASRC_TMA = 0, ASRC_FUSION = 1, ASRC_CONF = 2 };
 
 // tcgen05 tensor-core GEMM (gemm_tc.cu)
 cudaError_t launch_gemm(int epi, const GemmArgs& g, cudaStream_t stream);

@@ -12,9 +12,6 @@
 #ifndef LILICORR_PDL
 #define LILICORR_PDL 1
 #endif
-#ifndef LILICORR_NORM_GEMM
-#define LILICORR_NORM_GEMM 0
-#endif
 
 namespace lilicorr {
 
@@ -690,20 +687,12 @@ lilicorr_status lilicorr_rerank(const lilicorr_weights* w, const void* logits,
     LC_CUDA(launch_gemm(EPI_NODE, g, stream), "node gemm");
     MARK(T_NODE);
   }
-  // a3: encoder.  At hidden width 256 the pre-norms are made inside the QKV and FFN1
-  // GEMMs, once per 128-row tile (the operand stays resident for all column tiles);
-  // other widths run the standalone normalisation pass first.
-  const bool norm_in_gemm = LILICORR_NORM_GEMM != 0 && H == 256;
+  // a3: encoder
   for (const auto& L : w->layers) {
+    LC_CUDA(launch_rmsnorm_split(X, L.norm1, M, H, d.rms_eps, act1, stream), "rmsnorm");
+    MARK(T_NORM);
     GemmArgs g{};
-    if (norm_in_gemm) {
-      g.asrc = ASRC_NORM; g.a_x = X; g.a_gain = L.norm1; g.a_eps = d.rms_eps;
-    } else {
-      LC_CUDA(launch_rmsnorm_split(X, L.norm1, M, H, d.rms_eps, act1, stream), "rmsnorm");
-      MARK(T_NORM);
-      g.A = act1;
-    }
-    g.W = L.in_w; g.M = M; g.N = 3 * H; g.Kw = H; g.Ka = 2 * H; g.bias = L.in_b;
+    g.A = act1; g.W = L.in_w; g.M = M; g.N = 3 * H; g.Kw = H; g.Ka = 2 * H; g.bias = L.in_b;
     g.out_split = qkv;
     LC_CUDA(launch_gemm(EPI_SPLIT, g, stream), "qkv gemm");
     MARK(T_QKV);
@@ -723,15 +712,10 @@ lilicorr_status lilicorr_rerank(const lilicorr_weights* w, const void* logits,
     g.A = act1; g.W = L.out_w; g.M = M; g.N = H; g.Kw = H; g.Ka = 2 * H; g.bias = L.out_b; g.out = X;
     LC_CUDA(launch_gemm(EPI_RESID, g, stream), "out-proj gemm");
     MARK(T_OUT);
+    LC_CUDA(launch_rmsnorm_split(X, L.norm2, M, H, d.rms_eps, act1, stream), "rmsnorm");
+    MARK(T_NORM);
     g = GemmArgs{};
-    if (norm_in_gemm) {
-      g.asrc = ASRC_NORM; g.a_x = X; g.a_gain = L.norm2; g.a_eps = d.rms_eps;
-    } else {
-      LC_CUDA(launch_rmsnorm_split(X, L.norm2, M, H, d.rms_eps, act1, stream), "rmsnorm");
-      MARK(T_NORM);
-      g.A = act1;
-    }
-    g.W = L.w1; g.M = M; g.N = F; g.Kw = H; g.Ka = 2 * H; g.bias = L.b1; g.out_split = ffh;
+    g.A = act1; g.W = L.w1; g.M = M; g.N = F; g.Kw = H; g.Ka = 2 * H; g.bias = L.b1; g.out_split = ffh;
     LC_CUDA(launch_gemm(EPI_SPLIT_SILU, g, stream), "ffn1 gemm");
     MARK(T_FFN1);
     g = GemmArgs{};
