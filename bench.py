@@ -288,11 +288,30 @@ def gemm_work(wl, B, K):
     # attention (128-query tiles over all keys): S = Q K^T as three split products,
     # O' = P [V_hi | V_lo] as two products of width 2 dh
     nh = wl.dims["heads"]
-    dh = H // nh
+    dh = max(H // nh, 64)  # head dim 32 runs on zero-filled 64-wide tiles
     keys = 128 * math.ceil(S / 128)
     fl["attention"] = wl.batch * nh * math.ceil(S / 128) * (
         3 * 2 * 128 * keys * dh + 2 * 2 * 128 * keys * 2 * dh)
     return fl
+
+
+def algorithmic_bytes(wl):
+    """Bytes one call must move at least: the logits read once (rows 1..B-1 of every
+    block), the gathered embedding rows, every weight once, the target state and the
+    outputs (tokens, path scores)."""
+    import numpy as np
+    es = 2 if wl.ldtype == "bf16" else 4
+    logits = wl.batch * (wl.B - 1) * wl.V * es
+    H = wl.dims["hidden"]
+    M = wl.batch * (wl.B - 1) * wl.K
+    emb = M * H * wl.weights["embed"].dtype.itemsize
+    weights = sum(int(np.asarray(v).nbytes) for v in wl.weights.values()
+                  if v is not wl.weights["embed"])
+    tgt = 0 if wl.target_state is None else int(wl.target_state.nbytes)
+    outs = wl.batch * wl.B * 4 + wl.batch * (wl.B - 1) * 4
+    return {"logits": logits, "embedding_rows": emb, "weights": weights,
+            "target_state": tgt, "outputs": outs,
+            "total": logits + emb + weights + tgt + outs}
 
 
 def measure_workload(lc, wl, steps, warmup, dev, stream, graph=True, world=1, barrier=None):
@@ -396,6 +415,7 @@ def summarise(wl, m, pk, steps, world=1):
         "kernels_us_per_step": {k: round(1e3 * v["ms_per_step"], 2)
                                 for k, v in m["per_kernel"].items()},
         "tensor_tflops_executed": {k: round(v, 1) for k, v in enc.items()},
+        "algorithmic_bytes": algorithmic_bytes(wl),
         "gpu_launches_per_step": m["launches_per_step"],
     }
 
