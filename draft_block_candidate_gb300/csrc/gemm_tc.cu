@@ -336,6 +336,24 @@ __device__ __forceinline__ void tc_epilogue_staged(const GemmArgs& g, const CUte
   }
 }
 
+// ------------------------------------------------------------------ work items
+//
+// Item i of a launch: tile t, columns [c0, c0 + bn) of it.  The first ntiles - tail_tiles
+// items are whole tiles; the rest are the last tail_tiles tiles cut into tail_split column
+// pieces, so that the last round of the persistent grid is spread over more SMs.
+struct TcItem {
+  int t, c0, bn;
+};
+__device__ __forceinline__ int tc_items(const GemmArgs& g, int ntiles) {
+  return g.tail_split > 1 ? ntiles + g.tail_tiles * (g.tail_split - 1) : ntiles;
+}
+__device__ __forceinline__ TcItem tc_item(const GemmArgs& g, int ntiles, int i) {
+  const int nfull = g.tail_split > 1 ? ntiles - g.tail_tiles : ntiles;
+  if (i < nfull) return {i, 0, TC_BN};
+  const int j = i - nfull, bn = TC_BN / g.tail_split;
+  return {nfull + j / g.tail_split, (j % g.tail_split) * bn, bn};
+}
+
 // ------------------------------------------------------------------ A made in the kernel
 //
 // Two contractions read an A operand that is cheap to form from data already on hand, so
@@ -363,7 +381,9 @@ __device__ __forceinline__ void a_producer(const GemmArgs& g, uint8_t* sA, int A
                                            int NT, int ntiles, int unit, int rsub,
                                            const float* wt) {
   int it = 0;
-  for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
+  const int nitems = tc_items(g, ntiles);
+  for (int w = blockIdx.x; w < nitems; w += gridDim.x) {
+    const int t = tc_item(g, ntiles, w).t;  // the operand rows depend only on the tile
     const int64_t m0 = int64_t(t / NT) * TC_BM;
     if constexpr (ASRC == ASRC_FUSION) {
       // [h, h * t]: ring step kb = 2 cb + part holds column block cb of h (part 0) or of
@@ -541,8 +561,12 @@ __global__ void __launch_bounds__(32 * (2 + EW + (ASRC != ASRC_TMA ? TC_A_WARPS 
     // ---- producer: the smem ring runs on across this CTA's tiles
     int it = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-      const int m0 = (t / NT) * TC_BM, n0 = (t % NT) * TC_BN;
+    const int nitems = tc_items(g, ntiles);
+    for (int w = blockIdx.x; w < nitems && ok; w += gridDim.x) {
+      const TcItem item = tc_item(g, ntiles, w);
+      const int t = item.t;
+      // W rows from the piece's first column (a 256-row box; rows past the piece unused)
+      const int m0 = (t / NT) * TC_BM, n0 = (t % NT) * TC_BN + item.c0;
       for (int kb = 0; kb < KB; ++kb, ++it) {
         const int s = it % TC_STAGES, use = it / TC_STAGES;
         if (use > 0 && !mbar_wait_bounded(&empty_bar[s], (use - 1) & 1, &g_err_tc, ERR_TC_EMPTY)) {
@@ -570,10 +594,11 @@ __global__ void __launch_bounds__(32 * (2 + EW + (ASRC != ASRC_TMA ? TC_A_WARPS 
     }
   } else if (warp == 1 && lane == 0) {
     // ---- MMA issuer
-    constexpr uint32_t idesc = idesc_bf16(TC_BM, TC_BN);
     int it = 0, i = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++i) {
+    const int nitems = tc_items(g, ntiles);
+    for (int w = blockIdx.x; w < nitems && ok; w += gridDim.x, ++i) {
+      const uint32_t idesc = idesc_bf16(TC_BM, tc_item(g, ntiles, w).bn);
       const int buf = i & 1;
       const uint32_t acc = tmem + uint32_t(buf * TC_BN);
       if (i >= 2 && !mbar_wait_bounded(&acc_empty[buf], ((i >> 1) - 1) & 1, &g_err_tc,
@@ -611,10 +636,13 @@ __global__ void __launch_bounds__(32 * (2 + EW + (ASRC != ASRC_TMA ? TC_A_WARPS 
     uint8_t* stg = sStage + (warp - 2) * TC_STG_BUFS * TC_STG_BYTES;
     int sb = 0;  // staging buffer of the next chunk
     int i = 0;
-    for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
+    const int nitems = tc_items(g, ntiles);
+    for (int w = blockIdx.x; w < nitems; w += gridDim.x, ++i) {
+      const TcItem item = tc_item(g, ntiles, w);
+      const int t = item.t;
       const int buf = i & 1;
       const int64_t m0 = int64_t(t / NT) * TC_BM;
-      const int n0 = (t % NT) * TC_BN;
+      const int n0 = (t % NT) * TC_BN + item.c0;  // the accumulator's column 0
       const int64_t m = m0 + 32 * q + lane;
       // node sum: the row's gather sources before the accumulator is waited for
       NodeRow nr{};
@@ -626,6 +654,7 @@ __global__ void __launch_bounds__(32 * (2 + EW + (ASRC != ASRC_TMA ? TC_A_WARPS 
       tc_fence_after();
 #pragma unroll 1
       for (int cc = half * CPP; cc < (half + 1) * CPP; ++cc) {
+        if (cc * 32 >= item.bn) break;  // a piece: only its own columns
         float v[32];
         const int n = n0 + cc * 32;
         if constexpr (EPI == EPI_NODE) {
@@ -740,7 +769,25 @@ bool gemm_tc_supported(const GemmArgs& g) {
          (reinterpret_cast<uintptr_t>(g.A) % 16) == 0 && (reinterpret_cast<uintptr_t>(g.W) % 16) == 0;
 }
 
-cudaError_t launch_gemm(int epi, const GemmArgs& g, cudaStream_t stream) {
+// The tail plan of a launch over ntiles tiles on `sms` SMs: the tiles of the last,
+// part-filled round of the persistent grid (all of them when there are fewer tiles than
+// SMs) run as 2, 4 or 8 column pieces, as many as keep the pieces within one round.
+// Returns the number of work items (the grid is min(items, sms)).
+static int64_t tc_tail_plan(GemmArgs& g, int64_t ntiles, int sms) {
+  g.tail_tiles = 0;
+  g.tail_split = 1;
+  const int64_t r = ntiles % sms;
+  if (r == 0) return ntiles;
+  int sp = 1;
+  while (sp < 8 && r * sp * 2 <= sms) sp *= 2;
+  if (sp == 1) return ntiles;
+  g.tail_tiles = static_cast<int>(r);
+  g.tail_split = sp;
+  return ntiles + r * (sp - 1);
+}
+
+cudaError_t launch_gemm(int epi, const GemmArgs& g_in, cudaStream_t stream) {
+  GemmArgs g = g_in;
   CUtensorMap ta, tb, tc;
   if (g.asrc != ASRC_TMA) {
     // A made in the kernel: the fusion input under the SiLU-split epilogue, or the
@@ -768,7 +815,8 @@ cudaError_t launch_gemm(int epi, const GemmArgs& g, cudaStream_t stream) {
     }
     const int sms = device_sm_count();
     const int64_t ntiles = int64_t((g.N + TC_BN - 1) / TC_BN) * ((g.M + TC_BM - 1) / TC_BM);
-    const dim3 grid(static_cast<unsigned>(ntiles < sms ? ntiles : sms));
+    const int64_t nitems = tc_tail_plan(g, ntiles, sms);
+    const dim3 grid(static_cast<unsigned>(nitems < sms ? nitems : sms));
     constexpr int threads = 32 * (2 + TC_EPI_WARPS + TC_A_WARPS);
     cudaError_t e;
     if (fusion) {
@@ -814,7 +862,8 @@ cudaError_t launch_gemm(int epi, const GemmArgs& g, cudaStream_t stream) {
   constexpr int sw = tc_smem(2, 1, true, 16);
   const int sms = device_sm_count();
   const int64_t ntiles = int64_t((g.N + TC_BN - 1) / TC_BN) * ((g.M + TC_BM - 1) / TC_BM);
-  const dim3 grid(static_cast<unsigned>(ntiles < sms ? ntiles : sms));
+  const int64_t nitems = tc_tail_plan(g, ntiles, sms);
+  const dim3 grid(static_cast<unsigned>(nitems < sms ? nitems : sms));
   cudaError_t e = cudaSuccess;
   // the chosen instance's shared-memory limit (once per device), then its launch
 #define LC_TC_RUN(E, KERNEL, THREADS, SMEM)                                                  \

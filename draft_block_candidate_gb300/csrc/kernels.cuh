@@ -81,6 +81,10 @@ struct GemmArgs {
   const __nv_bfloat16* a_t;
   int64_t a_group;
   const float *a_cl, *a_lse, *a_w1, *a_b1;
+  // The last tail_tiles output tiles run as tail_split column pieces each (128 x 256 /
+  // tail_split), so that the last round of the persistent grid keeps more SMs busy; every
+  // piece owns its outputs (no reduction).  Set by launch_gemm.
+  int tail_tiles, tail_split;
 };
 enum ASrc : int { ASRC_TMA = 0, ASRC_FUSION = 1, ASRC_CONF = 2 };
 
