@@ -509,7 +509,8 @@ template <int EPI, int TC_STAGES, int TC_STG_BUFS, bool PAIR, int EW = TC_EPI_WA
           int ASRC = ASRC_TMA>
 __global__ void __launch_bounds__(32 * (2 + EW + (ASRC != ASRC_TMA ? TC_A_WARPS : 0)), 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmC, const GemmArgs g) {
+                   const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmBp,
+                   const GemmArgs g) {
   static_assert(ASRC == ASRC_TMA || PAIR, "a made A operand is always split");
   extern __shared__ uint8_t tc_smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -565,8 +566,10 @@ __global__ void __launch_bounds__(32 * (2 + EW + (ASRC != ASRC_TMA ? TC_A_WARPS 
     for (int w = blockIdx.x; w < nitems && ok; w += gridDim.x) {
       const TcItem item = tc_item(g, ntiles, w);
       const int t = item.t;
-      // W rows from the piece's first column (a 256-row box; rows past the piece unused)
+      // W rows of the tile, or of the piece (tmBp: boxes of the piece's width)
       const int m0 = (t / NT) * TC_BM, n0 = (t % NT) * TC_BN + item.c0;
+      const CUtensorMap* wmap = item.bn == TC_BN ? &tmB : &tmBp;
+      const uint32_t wbytes = uint32_t(item.bn) * TC_BK * 2;
       for (int kb = 0; kb < KB; ++kb, ++it) {
         const int s = it % TC_STAGES, use = it / TC_STAGES;
         if (use > 0 && !mbar_wait_bounded(&empty_bar[s], (use - 1) & 1, &g_err_tc, ERR_TC_EMPTY)) {
@@ -577,18 +580,18 @@ __global__ void __launch_bounds__(32 * (2 + EW + (ASRC != ASRC_TMA ? TC_A_WARPS 
           // W block of ring step kb: for the fusion input the steps alternate between the
           // h and the h * t halves of one 64-column block
           const int wk = ASRC == ASRC_FUSION ? (kb & 1) * (g.Kw / 2) + (kb >> 1) * TC_BK : kb * TC_BK;
-          mbar_arrive_expect_tx(&full_bar[s], TC_B_BYTES);
-          tma_load_2d(sB + s * TC_B_BYTES, &tmB, wk, n0, &full_bar[s]);
+          mbar_arrive_expect_tx(&full_bar[s], wbytes);
+          tma_load_2d(sB + s * TC_B_BYTES, wmap, wk, n0, &full_bar[s]);
           continue;
         }
-        mbar_arrive_expect_tx(&full_bar[s], AST + TC_B_BYTES);
+        mbar_arrive_expect_tx(&full_bar[s], AST + wbytes);
         if constexpr (PAIR) {
           tma_load_2d(sA + s * AST, &tmA, kb * TC_BK, m0, &full_bar[s]);
           tma_load_2d(sA + s * AST + TC_A_BYTES, &tmA, g.Kw + kb * TC_BK, m0, &full_bar[s]);
-          tma_load_2d(sB + s * TC_B_BYTES, &tmB, kb * TC_BK, n0, &full_bar[s]);
+          tma_load_2d(sB + s * TC_B_BYTES, wmap, kb * TC_BK, n0, &full_bar[s]);
         } else {
           tma_load_2d(sA + s * AST, &tmA, kb * TC_BK, m0, &full_bar[s]);
-          tma_load_2d(sB + s * TC_B_BYTES, &tmB, (kb * TC_BK) % g.Kw, n0, &full_bar[s]);
+          tma_load_2d(sB + s * TC_B_BYTES, wmap, (kb * TC_BK) % g.Kw, n0, &full_bar[s]);
         }
       }
     }
@@ -817,19 +820,23 @@ cudaError_t launch_gemm(int epi, const GemmArgs& g_in, cudaStream_t stream) {
     const int64_t ntiles = int64_t((g.N + TC_BN - 1) / TC_BN) * ((g.M + TC_BM - 1) / TC_BM);
     const int64_t nitems = tc_tail_plan(g, ntiles, sms);
     const dim3 grid(static_cast<unsigned>(nitems < sms ? nitems : sms));
+    CUtensorMap tbp = tb;  // W in boxes of a tail piece's width
+    if (g.tail_split > 1 &&
+        !make_tmap(&tbp, g.W, uint64_t(g.N), uint64_t(g.Kw), uint32_t(TC_BN / g.tail_split)))
+      return cudaErrorInvalidValue;
     constexpr int threads = 32 * (2 + TC_EPI_WARPS + TC_A_WARPS);
     cudaError_t e;
     if (fusion) {
       constexpr int sm = tc_smem(3, 1, true);
       auto k = gemm_tc_kernel<EPI_SPLIT_SILU, 3, 1, true, TC_EPI_WARPS, ASRC_FUSION>;
       e = allow_dynamic_smem(reinterpret_cast<const void*>(k), sm);
-      if (e == cudaSuccess) e = launch_k(k, grid, dim3(threads), sm, stream, ta, tb, tc, g);
+      if (e == cudaSuccess) e = launch_k(k, grid, dim3(threads), sm, stream, ta, tb, tc, tbp, g);
     } else {
       const int sm = tc_smem(2, 2, true) + g.Kw * 6 * 4;  // + the layer's weight table
       if (sm > 227 * 1024) return cudaErrorInvalidValue;
       auto k = gemm_tc_kernel<EPI_NODE, 2, 2, true, TC_EPI_WARPS, ASRC_CONF>;
       e = allow_dynamic_smem(reinterpret_cast<const void*>(k), sm);
-      if (e == cudaSuccess) e = launch_k(k, grid, dim3(threads), sm, stream, ta, tb, tc, g);
+      if (e == cudaSuccess) e = launch_k(k, grid, dim3(threads), sm, stream, ta, tb, tc, tbp, g);
     }
     if (e != cudaSuccess) return e;
     note_launch();
@@ -864,12 +871,16 @@ cudaError_t launch_gemm(int epi, const GemmArgs& g_in, cudaStream_t stream) {
   const int64_t ntiles = int64_t((g.N + TC_BN - 1) / TC_BN) * ((g.M + TC_BM - 1) / TC_BM);
   const int64_t nitems = tc_tail_plan(g, ntiles, sms);
   const dim3 grid(static_cast<unsigned>(nitems < sms ? nitems : sms));
+  CUtensorMap tbp = tb;  // W in boxes of a tail piece's width
+  if (g.tail_split > 1 &&
+      !make_tmap(&tbp, g.W, uint64_t(g.N), uint64_t(g.Kw), uint32_t(TC_BN / g.tail_split)))
+    return cudaErrorInvalidValue;
   cudaError_t e = cudaSuccess;
   // the chosen instance's shared-memory limit (once per device), then its launch
 #define LC_TC_RUN(E, KERNEL, THREADS, SMEM)                                                  \
   {                                                                                          \
     e = allow_dynamic_smem(reinterpret_cast<const void*>(KERNEL), SMEM);                     \
-    if (e == cudaSuccess) e = launch_k(KERNEL, grid, dim3(THREADS), SMEM, stream, ta, tb, tc, g); \
+    if (e == cudaSuccess) e = launch_k(KERNEL, grid, dim3(THREADS), SMEM, stream, ta, tb, tc, tbp, g); \
   }
 #define LC_TC_LAUNCH(E)                                                                      \
   if (pair && wide)                                                                          \
