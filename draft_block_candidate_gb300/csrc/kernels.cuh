@@ -9,6 +9,8 @@ namespace lilicorr {
 
 // a1 logit pass (logit_pass.cu)
 size_t k1_workspace_bytes(int64_t batch, int B, int64_t V, int esize);
+// The logit pass splits rows into segments only in calls of fewer than this many rows.
+constexpr int K1_SPLIT_BELOW_ROWS = 90;
 cudaError_t k1_launch(const void* logits, int esize, int64_t batch, int B, int64_t V, int K,
                       int32_t* cand_id, float* cand_logit, float* lse, void* ws,
                       cudaStream_t stream, int64_t row_stride = 0, int id_offset = 0,

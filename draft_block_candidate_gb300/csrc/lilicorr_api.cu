@@ -822,8 +822,17 @@ lilicorr_status lilicorr_rerank_host(const lilicorr_weights* w, const void* logi
   // The logits arrive in chunks of blocks on a copy stream, rows 1..B-1 only (row 0, the
   // anchor position, is never read); each chunk's rerank starts on `stream` as soon as
   // its rows have landed, so the compute of one chunk hides under the copy of the next.
-  const int64_t nchunk = std::min<int64_t>(batch, 8);
-  const int64_t per = (batch + nchunk - 1) / nchunk;
+  // Chunks of at least K1_SPLIT_BELOW_ROWS rows (or one chunk): the logit pass splits rows
+  // into segments only in calls of fewer rows, so every chunk then processes its rows
+  // exactly as one call over the whole batch does, and the results are the same bits.
+  const int64_t rows_all = batch * (B - 1);
+  int64_t nchunk = std::min<int64_t>(std::min<int64_t>(batch, 8),
+                                     std::max<int64_t>(1, rows_all / K1_SPLIT_BELOW_ROWS));
+  int64_t per = (batch + nchunk - 1) / nchunk;
+  while (nchunk > 1 && (batch - (nchunk - 1) * per) * (B - 1) < K1_SPLIT_BELOW_ROWS) {
+    --nchunk;
+    per = (batch + nchunk - 1) / nchunk;
+  }
   cudaStream_t copy = nullptr;
   std::vector<cudaEvent_t> ev(size_t(nchunk) + 1, nullptr);
   auto cleanup = [&]() {

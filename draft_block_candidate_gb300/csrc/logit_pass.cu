@@ -734,7 +734,7 @@ K1Plan k1_plan(int64_t batch, int B, int64_t V, int esize) {
   // every split is slower than one CTA per row (960 rows: 74 us unsplit, 104 us at P = 2,
   // 145 us at P = 4), because a CTA's start, first-stage latency and final gather cost
   // about as much as streaming a third of a row.
-  const int64_t want = rows >= 90 ? 1 : 90 / rows;
+  const int64_t want = rows >= K1_SPLIT_BELOW_ROWS ? 1 : K1_SPLIT_BELOW_ROWS / rows;
   pl.P = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>({want, 64, stages})));
   const int64_t seg = (row_bytes + pl.P - 1) / pl.P;
   pl.seg_bytes = std::max<int64_t>(16, (seg + 15) / 16 * 16);

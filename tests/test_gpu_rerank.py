@@ -247,7 +247,10 @@ def test_long_attention_rebase_when_far_chunks_dominate(lc):
 
 @pytest.mark.parametrize("name,kw", [("highconc", dict(V=4096, batch=11)),
                                      ("single", dict(V=3001, batch=3, B=9, with_slot_hidden=True)),
-                                     ("tiny", dict(batch=1))])
+                                     ("tiny", dict(batch=1)),
+                                     # full vocabulary, 8 blocks = 120 rows: chunks of
+                                     # fewer rows would split the rows' logit pass
+                                     ("sweep", dict(batch=8))])
 def test_rerank_host_matches_device_entry(lc, name, kw):
     """The host-memory entry point (chunked copies of rows 1..B-1 overlapped with the
     per-chunk reranks) returns exactly what the device entry point returns."""
