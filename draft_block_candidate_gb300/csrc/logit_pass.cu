@@ -68,6 +68,29 @@ constexpr int KQ = 32;                                      // queue slots per w
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float M2_INIT = -1e30f;                           // "no element yet", finite
 
+// Natural-log lse of a base-2 pair (M, S), sum = S 2^M: (M + log2 S) / LOG2E, in float
+// with one rounding's worth of care.  S = f 2^e with f in [0.5, 1), so log2 S = e + log2 f
+// (the float log2 f within one ulp of a value below 1 in magnitude).  M + e is formed
+// exactly as a head s and tail t (two-sum), the tail takes log2 f, and the pair is scaled
+// by the reciprocal of the same float LOG2E that scaled the logits, held as a head and
+// tail float: the head product exactly by an FMA, the rest added before the one final
+// rounding.  Rounding-named intrinsics keep the compiler from contracting the steps.
+__device__ __forceinline__ float lse_of(float M, float S) {
+  constexpr double INV_L = 1.0 / static_cast<double>(LOG2E);
+  constexpr float IH = static_cast<float>(INV_L);
+  constexpr float IL = static_cast<float>(INV_L - static_cast<double>(IH));
+  int e;
+  const float f = frexpf(S, &e);
+  const float E = static_cast<float>(e);
+  const float s = __fadd_rn(M, E);
+  const float bb = __fsub_rn(s, M);
+  const float t = __fadd_rn(__fsub_rn(M, __fsub_rn(s, bb)), __fsub_rn(E, bb));
+  const float lo = __fadd_rn(t, log2f(f));
+  const float ph = __fmul_rn(s, IH);
+  const float pe = __fmaf_rn(s, IH, -ph);
+  return __fadd_rn(ph, __fadd_rn(pe, __fmaf_rn(s, IL, __fmul_rn(lo, IH))));
+}
+
 struct K1Partial {
   float m2, s;
   float v[KQ];
@@ -242,6 +265,7 @@ constexpr int K1_GSIZE = K1_CTHREADS / K1_GROUPS;
 // Final candidate list: at most every queue entry (17 warps) and every buffer entry.
 constexpr int K1_UCAP = (K1_CWARPS + 1) * KQ + K1_CWARPS * K1_WCAP;
 static_assert(K1_UCAP * 8 <= K1_STAGE_BYTES, "final candidate list must fit in one ring slot");
+static_assert(K1_WCAP >= KQ, "a warp buffer holds the sorted result at the end");
 
 __device__ __forceinline__ float max3f(float a, float b, float c) {
   float r;
@@ -437,24 +461,20 @@ __global__ void __launch_bounds__(K1_THREADS, K1_MIN_BLOCKS) logit_pass_kernel(c
     int* bi = s_bi[warp];
     int* gmax = &s_gmax[tid / K1_GSIZE];
     int* wcnt = &s_wcnt[warp];
+    int wprev = 0;  // *wcnt as this warp last left it (only this warp appends)
     float2 s2 = make_float2(0.f, 0.f);  // partial sums of this thread's exponentials
 
     // Candidates of stage st (chunk maxima cmx, validity bits vmask, chunk words from
-    // chunk_at(i)): compare with the threshold, the better of the warp's K-th entry and
-    // the CTA floor fl; append the elements of hit chunks that can still enter to the
-    // warp buffer; fold it into the queue 32 entries at a time.
+    // chunk_at(i)): compare with the threshold tv, the better of the warp's K-th entry and
+    // the CTA floor fl; append the elements of hit chunks at or above tv to the warp
+    // buffer (a superset of those that beat the threshold in (value, id) order: the
+    // queue's folds order ties by id); fold the buffer into the queue 32 entries at a time.
     auto check_stage = [&](int st, const float (&cmx)[K1_CPT], unsigned vmask, float smax,
                            float fl, auto&& chunk_at) {
       const int soff = st * K1_STAGE_BYTES;
-      float tv = q.tv;
-      int ti = q.tid;
-      if (fl > tv) {
-        tv = fl;
-        ti = INT_MAX;
-      }
+      const float tv = fmaxf(q.tv, fl);
       if (!__any_sync(FULL_MASK, smax >= tv)) return;
-      const int prev = *reinterpret_cast<volatile int*>(wcnt);
-      __syncwarp();
+      const int prev = wprev;
 #pragma unroll
       for (int i = 0; i < K1_CPT; ++i) {
         if (((vmask >> i) & 1u) && cmx[i] >= tv) {
@@ -464,7 +484,7 @@ __global__ void __launch_bounds__(K1_THREADS, K1_MIN_BLOCKS) logit_pass_kernel(c
           const int id0 = seg_elem0 + (soff + c * 16) / ES;
 #pragma unroll
           for (int j = 0; j < NV; ++j)
-            if (better(x[j], id0 + j, tv, ti)) {
+            if (x[j] >= tv) {
               const int idx = atomicAdd(wcnt, 1);
               if (idx < K1_WCAP) {
                 bv[idx] = x[j];
@@ -475,7 +495,10 @@ __global__ void __launch_bounds__(K1_THREADS, K1_MIN_BLOCKS) logit_pass_kernel(c
       }
       __syncwarp();
       int cnt = *reinterpret_cast<volatile int*>(wcnt);
-      if (cnt < 32) return;
+      if (cnt < 32) {
+        wprev = cnt;
+        return;
+      }
       if (cnt > K1_WCAP) {
         // Too many ties for the buffer: fold the earlier stages' entries, then this
         // stage's chunks element by element; the buffer is dropped.
@@ -512,6 +535,7 @@ __global__ void __launch_bounds__(K1_THREADS, K1_MIN_BLOCKS) logit_pass_kernel(c
         }
       }
       __syncwarp();
+      wprev = cnt;
       if (lane == 0) {
         *wcnt = cnt;
         if (q.tv != -INFINITY) atomicMax(&s_floor, float_key(q.tv));
@@ -616,15 +640,51 @@ __global__ void __launch_bounds__(K1_THREADS, K1_MIN_BLOCKS) logit_pass_kernel(c
   __syncthreads();
   if (warp != 0) return;
 
-  WarpQueue fq;
-  fq.init();
   const int nu = s_ucnt;
-  for (int b0 = 0; b0 < nu; b0 += 32) {
-    const bool has = b0 + lane < nu;
-    queue_absorb(fq, has ? uv[b0 + lane] : -INFINITY, has ? ui[b0 + lane] : INT_MAX, lane, K);
+  float v = -INFINITY;
+  int id = INT_MAX;
+  if (nu <= 64) {
+    // The list's entries are distinct (value, id) pairs, so under (value desc, id asc)
+    // each has its own rank, the number of entries better than it: each lane ranks its
+    // one or two entries and places those ranked below KQ in warp 0's buffer (no longer
+    // read), which then holds the sorted result.
+    float* rv = s_bv[0];
+    int* ri = s_bi[0];
+    const bool h0 = lane < nu, h1 = lane + 32 < nu;
+    const float c0 = h0 ? uv[lane] : 0.f, c1 = h1 ? uv[lane + 32] : 0.f;
+    const int i0 = h0 ? ui[lane] : 0, i1 = h1 ? ui[lane + 32] : 0;
+    int r0 = 0, r1 = 0;
+#pragma unroll 4
+    for (int j = 0; j < nu; ++j) {
+      const float vj = uv[j];
+      const int ij = ui[j];
+      r0 += better(vj, ij, c0, i0) ? 1 : 0;
+      r1 += better(vj, ij, c1, i1) ? 1 : 0;
+    }
+    rv[lane] = -INFINITY;
+    ri[lane] = INT_MAX;
+    __syncwarp();
+    if (h0 && r0 < KQ) {
+      rv[r0] = c0;
+      ri[r0] = i0;
+    }
+    if (h1 && r1 < KQ) {
+      rv[r1] = c1;
+      ri[r1] = i1;
+    }
+    __syncwarp();
+    v = rv[lane];
+    id = ri[lane];
+  } else {
+    WarpQueue fq;
+    fq.init();
+    for (int b0 = 0; b0 < nu; b0 += 32) {
+      const bool has = b0 + lane < nu;
+      queue_absorb(fq, has ? uv[b0 + lane] : -INFINITY, has ? ui[b0 + lane] : INT_MAX, lane, K);
+    }
+    v = fq.qv;
+    id = fq.qid;
   }
-  float v = fq.qv;
-  int id = fq.qid;
   float M = lane <= K1_CWARPS ? s_m2[lane] : M2_INIT;
   float S = lane <= K1_CWARPS ? s_s[lane] : 0.f;
 #pragma unroll
@@ -677,10 +737,7 @@ __global__ void __launch_bounds__(K1_THREADS, K1_MIN_BLOCKS) logit_pass_kernel(c
     p.cand_id[r * K + lane] = id + p.id_offset;
     p.cand_logit[r * K + lane] = v;
   }
-  if (lane == 0) {
-    const double l2 = static_cast<double>(M) + log2(static_cast<double>(S));
-    p.lse[r] = static_cast<float>(l2 / static_cast<double>(LOG2E));
-  }
+  if (lane == 0) p.lse[r] = lse_of(M, S);
 }
 
 // Merge of n vocabulary-shard records per row (one warp per row): the shards' sorted
@@ -709,10 +766,7 @@ __global__ void __launch_bounds__(128) k1_merge_kernel(const char* __restrict__ 
     cand_id[r * K + lane] = id;
     cand_logit[r * K + lane] = v;
   }
-  if (lane == 0) {
-    const double l2 = static_cast<double>(M) + log2(static_cast<double>(S));
-    lse[r] = static_cast<float>(l2 / static_cast<double>(LOG2E));
-  }
+  if (lane == 0) lse[r] = lse_of(M, S);
 }
 
 // ------------------------------------------------------------------------------ host
