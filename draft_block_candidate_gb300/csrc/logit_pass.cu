@@ -21,15 +21,17 @@
 //   * top-K: each consumer warp keeps its own running top-32 (value, id) pairs, sorted
 //     across its lanes.  After a stage one vote compares every thread's stage maximum
 //     with the warp's threshold, the better of its own K-th entry and a CTA-wide floor.
-//     Only on a hit are the hit chunks unpacked and the elements that can still enter
-//     appended to the warp's buffer, which is folded in 32 at a time (warp bitonic sort
-//     + bitonic merge).
-//   * the CTA floor is the K-th largest of 32 thread-group running maxima (K distinct
-//     elements are at least that large).  After stage 0 the consumer warps meet once so
-//     that the first floor covers the whole stage; afterwards the producer warp raises
-//     it after every refill, and every fold raises it to the warp's own K-th entry.
+//     Only on a hit are the hit chunks unpacked and their elements at or above the
+//     threshold appended to the warp's buffer, which is folded in 32 at a time (warp
+//     bitonic sort + bitonic merge).
+//   * the CTA floor is the K-th largest of 32 thread-group running maxima (of 64 above
+//     K = 16; K distinct elements are at least that large).  After stage 0 the consumer
+//     warps meet once so that the first floor covers the whole stage; afterwards the
+//     producer warp raises it after every refill, and every fold raises it to the warp's
+//     own K-th entry.
 // At the end every warp offers its K-th entry to the floor; only queue and buffer entries
-// at or above the final floor are gathered into one list, which one warp folds.
+// at or above the final floor are gathered into one list, placed by rank (or folded by
+// one warp when long).
 // Rows are split into P segments only when fewer than about 90 rows are given (a single
 // request); the last CTA of a row (atomic counter, no waiting) merges the P partials.
 #include <float.h>
@@ -115,6 +117,8 @@ struct K1Params {
   char* records;       // vocabulary-shard mode: packed per-row records instead of outputs
   long long wait_limit;  // SM cycles after which a wait gives up (WAIT_LIMIT_CYCLES)
   int withhold_first;    // self-check only: stage 0's copy is announced but never issued
+  int64_t prefetch_ahead;  // > 0: at its last refill a CTA prefetches into L2 the first
+                           // stage of unit blockIdx + prefetch_ahead (co-resident CTAs)
 };
 
 // Packed per-row record of a vocabulary shard: {m2, s, v[K], id[K]}, K * 8 + 8 bytes.
@@ -260,8 +264,11 @@ __device__ __forceinline__ float elem_of(const uint4 w, int j) {
 }
 
 constexpr int K1_WCAP = 64;    // per-warp candidate buffer entries
-constexpr int K1_GROUPS = 32;  // thread groups whose running maxima give the CTA floor
-constexpr int K1_GSIZE = K1_CTHREADS / K1_GROUPS;
+// Thread groups whose running maxima give the CTA floor: 32 (16 threads each) up to
+// K = 16; 64 (8 threads each) above, where the K-th largest of 32 would be loose.
+template <bool WIDE>
+__host__ __device__ constexpr int k1_groups() { return WIDE ? 64 : 32; }
+constexpr int K1_WIDE_ABOVE_K = 16;
 // Final candidate list: at most every queue entry (17 warps) and every buffer entry.
 constexpr int K1_UCAP = (K1_CWARPS + 1) * KQ + K1_CWARPS * K1_WCAP;
 static_assert(K1_UCAP * 8 <= K1_STAGE_BYTES, "final candidate list must fit in one ring slot");
@@ -321,23 +328,60 @@ __device__ __forceinline__ void lse_stage(const uint4 (&w)[K1_CPT], unsigned val
   }
 }
 
-// Warp-uniform: the K-th largest of the 32 group maxima.  Each group's maximum is an
-// element of a distinct set of threads, so K elements of the segment are at least this
-// large: a valid inclusive floor for the K-th largest value.
-__device__ __forceinline__ float group_floor(const int* gmax, int lane, int K) {
-  float g = key_float(*reinterpret_cast<const volatile int*>(&gmax[lane]));
-  if (K == 1) {
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) g = fmaxf(g, __shfl_xor_sync(FULL_MASK, g, o));
-    return g;
-  }
-  return __shfl_sync(FULL_MASK, warp_sort_desc(g, lane), K - 1);
+// The 16-byte aligned byte range [lo, hi) of p.logits that unit u (row u / P, segment
+// u % P) streams.
+__device__ __forceinline__ void k1_unit_range(const K1Params& p, int64_t u, int es, int64_t& lo,
+                                              int64_t& hi) {
+  const int64_t r = u / p.P;
+  const int64_t seg = u % p.P;
+  const int64_t row_start = ((r / (p.B - 1)) * p.B + r % (p.B - 1) + 1) * p.row_stride * es;
+  const int64_t row_end = row_start + p.V * es;
+  const uintptr_t base = reinterpret_cast<uintptr_t>(p.logits);
+  int64_t bs = static_cast<int64_t>(((base + row_start + 15) & ~uintptr_t(15)) - base);
+  int64_t be = static_cast<int64_t>(((base + row_end) & ~uintptr_t(15)) - base);
+  if (bs >= be) bs = be = row_end;
+  lo = i64min(be, bs + seg * p.seg_bytes);
+  hi = i64min(be, lo + p.seg_bytes);
 }
 
-template <typename T>
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// Warp-uniform: the K-th largest of the group maxima.  Each group's maximum is an element
+// of a distinct set of threads, so K elements of the segment are at least this large: a
+// valid inclusive floor for the K-th largest value.  32 groups: one per lane, one sort.
+// 64 groups: lane l holds groups l and l + 32; the first half sorted descending and the
+// second ascending give, lane by lane, the larger of the two as a bitonic sequence of the
+// 32 largest, which one merge sorts.
+template <bool WIDE>
+__device__ __forceinline__ float group_floor(const int* gmax, int lane, int K) {
+  float g = key_float(*reinterpret_cast<const volatile int*>(&gmax[lane]));
+  if constexpr (!WIDE) {
+    if (K == 1) {
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) g = fmaxf(g, __shfl_xor_sync(FULL_MASK, g, o));
+      return g;
+    }
+    return __shfl_sync(FULL_MASK, warp_sort_desc(g, lane), K - 1);
+  } else {
+    const float h = key_float(*reinterpret_cast<const volatile int*>(&gmax[lane + 32]));
+    g = warp_sort_desc(g, lane);
+    float c = fmaxf(g, __shfl_sync(FULL_MASK, warp_sort_desc(h, lane), 31 - lane));
+#pragma unroll
+    for (int j = 16; j >= 1; j >>= 1) {
+      const float o = __shfl_xor_sync(FULL_MASK, c, j);
+      c = (lane & j) == 0 ? fmaxf(c, o) : fminf(c, o);
+    }
+    return __shfl_sync(FULL_MASK, c, K - 1);
+  }
+}
+
+template <typename T, bool WIDE>
 __global__ void __launch_bounds__(K1_THREADS, K1_MIN_BLOCKS) logit_pass_kernel(const K1Params p) {
   constexpr int ES = sizeof(T);
   constexpr int NV = 16 / ES;
+  constexpr int K1_GROUPS = k1_groups<WIDE>();
   extern __shared__ __align__(128) uint8_t k1_dyn_smem[];
   uint8_t(*stage)[K1_STAGE_BYTES] = reinterpret_cast<uint8_t(*)[K1_STAGE_BYTES]>(k1_dyn_smem);
   __shared__ __align__(8) uint64_t full_bar[K1_NSTAGES], empty_bar[K1_NSTAGES];
@@ -449,9 +493,18 @@ __global__ void __launch_bounds__(K1_THREADS, K1_MIN_BLOCKS) logit_pass_kernel(c
         __nanosleep(K1_POLL_NS);
       }
       if (ready == 2) break;
-      if (lane == 0) issue(st);
+      if (lane == 0) {
+        issue(st);
+        // the first stage of the unit a CTA will likely start on this slot when this one
+        // ends, into L2 (a hint: its first copy then waits on L2, not on DRAM)
+        if (st == nstages - 1 && p.prefetch_ahead > 0 && u + p.prefetch_ahead < gridDim.x) {
+          int64_t lo, hi;
+          k1_unit_range(p, u + p.prefetch_ahead, ES, lo, hi);
+          if (hi > lo) prefetch_l2(p.logits + lo, static_cast<uint32_t>(i64min(K1_STAGE_BYTES, hi - lo)));
+        }
+      }
       {
-        const float f = group_floor(s_gmax, lane, K);
+        const float f = group_floor<WIDE>(s_gmax, lane, K);
         if (lane == 0) atomicMax(&s_floor, float_key(f));
       }
     }
@@ -459,7 +512,7 @@ __global__ void __launch_bounds__(K1_THREADS, K1_MIN_BLOCKS) logit_pass_kernel(c
     // ================= consumer warps =================
     float* bv = s_bv[warp];
     int* bi = s_bi[warp];
-    int* gmax = &s_gmax[tid / K1_GSIZE];
+    int* gmax = &s_gmax[tid / (K1_CTHREADS / K1_GROUPS)];
     int* wcnt = &s_wcnt[warp];
     int wprev = 0;  // *wcnt as this warp last left it (only this warp appends)
     float2 s2 = make_float2(0.f, 0.f);  // partial sums of this thread's exponentials
@@ -575,11 +628,11 @@ __global__ void __launch_bounds__(K1_THREADS, K1_MIN_BLOCKS) logit_pass_kernel(c
       float fl;
       if (st == 0) {
         // First CTA floor: every thread offers its stage-0 maximum to its group, the
-        // consumer warps meet, and each takes the K-th largest of the 32 group maxima.
+        // consumer warps meet, and each takes the K-th largest of the group maxima.
         if (smax != -INFINITY) atomicMax(gmax, float_key(smax));
         named_bar_sync(1, K1_CTHREADS);
         if (s_abort) break;
-        fl = group_floor(s_gmax, lane, K);
+        fl = group_floor<WIDE>(s_gmax, lane, K);
         if (warp == 0 && lane == 0) atomicMax(&s_floor, float_key(fl));
         lse_stage<NV>(w, valid, smax, m2, s2, gmax);
       } else {
@@ -824,6 +877,10 @@ cudaError_t k1_launch(const void* logits, int esize, int64_t batch, int B, int64
   prm.records = static_cast<char*>(records);
   prm.wait_limit = wait_limit;
   prm.withhold_first = withhold_first ? 1 : 0;
+  {
+    const int64_t resident = int64_t(K1_MIN_BLOCKS) * device_sm_count();
+    prm.prefetch_ahead = batch * (B - 1) * pl.P > resident ? resident : 0;
+  }
   const int64_t rows = batch * (B - 1);
   if (pl.P > 1) {
     prm.partials = static_cast<K1Partial*>(ws);
@@ -834,17 +891,15 @@ cudaError_t k1_launch(const void* logits, int esize, int64_t batch, int B, int64
   }
   const dim3 grid(static_cast<unsigned>(rows * pl.P));
   constexpr int dyn = K1_NSTAGES * K1_STAGE_BYTES;
+  const bool wide = K > K1_WIDE_ABOVE_K;
+  void (*kern)(const K1Params) =
+      esize == 2 ? (wide ? logit_pass_kernel<__nv_bfloat16, true> : logit_pass_kernel<__nv_bfloat16, false>)
+                 : (wide ? logit_pass_kernel<float, true> : logit_pass_kernel<float, false>);
   {
-    cudaError_t e = esize == 2 ? allow_dynamic_smem(
-                                     reinterpret_cast<const void*>(logit_pass_kernel<__nv_bfloat16>), dyn)
-                               : allow_dynamic_smem(reinterpret_cast<const void*>(logit_pass_kernel<float>), dyn);
+    cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void*>(kern), dyn);
     if (e != cudaSuccess) return e;
   }
-  const cudaError_t e = esize == 2
-                            ? launch_k(logit_pass_kernel<__nv_bfloat16>, grid, dim3(K1_THREADS), dyn,
-                                       stream, prm)
-                            : launch_k(logit_pass_kernel<float>, grid, dim3(K1_THREADS), dyn, stream,
-                                       prm);
+  const cudaError_t e = launch_k(kern, grid, dim3(K1_THREADS), dyn, stream, prm);
   if (e != cudaSuccess) return e;
   note_launch();
   return cudaGetLastError();
