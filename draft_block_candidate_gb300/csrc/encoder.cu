@@ -97,18 +97,10 @@ __device__ __forceinline__ void load8(const float* p, float (&v)[8]) {
 // top = [k == 0] (App. A: log-probability and probability under the full vocabulary,
 // the gap to the slot's most likely token, the rank normalised to [0,1], top indicator).
 // This pass serves hidden width 256; other widths form U inside the node GEMM.
-// The layer's weights (256 x 5 + 256 biases) sit in shared memory,
-// re-read per row (a lane's 48 values as 12 16-byte loads, interleaved across lanes so a
-// load is conflict-free) instead of held in 48 registers, so more warps fit on an SM;
-// one warp per (slot, 8 candidate rows).
-__device__ __forceinline__ float4 lds4_volatile(const float4* p) {
-  float4 v;
-  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(p))));
-  return v;
-}
-
+// The layer's weights (256 x 5 + 256 biases) are staged in shared memory (a lane's 48
+// values as 12 16-byte units, interleaved across lanes so a load is conflict-free) and
+// taken into 48 registers once per warp; one warp per (slot, 8 candidate rows), three
+// CTAs per SM looping over them (80 registers a thread).
 __global__ void __launch_bounds__(256) conf_hidden256_kernel(const float* __restrict__ cand_logit,
                                                              const float* __restrict__ lse,
                                                              int64_t M, int K,
@@ -130,6 +122,15 @@ __global__ void __launch_bounds__(256) conf_hidden256_kernel(const float* __rest
   const int64_t nslots = M / K;
   const int gps = (K + RPW - 1) / RPW;  // row groups per slot
   const int64_t units = nslots * gps;
+  float w[48];  // this lane's 8 hidden units: w1 row (5) and bias for each
+#pragma unroll
+  for (int c = 0; c < 12; ++c) {
+    const float4 v = sw[c][lane];
+    w[4 * c] = v.x;
+    w[4 * c + 1] = v.y;
+    w[4 * c + 2] = v.z;
+    w[4 * c + 3] = v.w;
+  }
   for (int64_t un = int64_t(blockIdx.x) * nw + (threadIdx.x >> 5); un < units;
        un += int64_t(gridDim.x) * nw) {
     const int64_t j = un / gps;
@@ -153,15 +154,6 @@ __global__ void __launch_bounds__(256) conf_hidden256_kernel(const float* __rest
       float f[5];
 #pragma unroll
       for (int i = 0; i < 5; ++i) f[i] = __shfl_sync(FULL_MASK, g[i], t);
-      float w[48];
-#pragma unroll
-      for (int c = 0; c < 12; ++c) {
-        const float4 v = lds4_volatile(&sw[c][lane]);
-        w[4 * c] = v.x;
-        w[4 * c + 1] = v.y;
-        w[4 * c + 2] = v.z;
-        w[4 * c + 3] = v.w;
-      }
       float o[8];
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
@@ -499,7 +491,10 @@ cudaError_t launch_conf_hidden(const float* cand_logit, const float* lse, int64_
   if (H != 256) return cudaErrorInvalidValue;
   if (K < 1 || K > 32 || M % K) return cudaErrorInvalidValue;
   const int64_t units = (M / K) * ((K + 7) / 8);  // (slot, 8 rows) per warp, 8 per CTA
-  const unsigned g2 = static_cast<unsigned>(std::min<int64_t>((units + 7) / 8, 152 * 16));
+  // three resident CTAs per SM (measured: 23 -> 21 us at the high-concurrency size,
+  // against one CTA per 64 units with the weights re-read from shared memory per row)
+  const unsigned g2 =
+      static_cast<unsigned>(std::min<int64_t>((units + 7) / 8, int64_t(3) * device_sm_count()));
   const cudaError_t e = launch_k(conf_hidden256_kernel, dim3(g2), dim3(256), 0, stream, cand_logit,
                                  lse, M, K, w1, b1, U);
   if (e != cudaSuccess) return e;

@@ -46,6 +46,8 @@ CASES = [  # (ldtype, batch, B, V, K)
     ("f32", 1, 16, 1024, 4),
     ("bf16", 2, 16, 1001, 8),          # rows not 16-byte aligned: head and tail elements
     ("bf16", 3, 16, 2 * 8192 + 13, 16),  # several stages + ragged tail
+    ("bf16", 3, 16, 2 * 8192 + 13, 17),  # the smallest K whose floor takes 64 thread groups
+    ("f32", 4, 16, 40_000, 24),          # 64 groups, f32 rows of several stages
     ("f32", 2, 5, 4097, 32),
     ("bf16", 1, 3, 5, 5),              # K = V, body-free rows
     ("f32", 1, 2, 1, 1),               # V = 1
